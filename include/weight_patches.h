@@ -1,0 +1,198 @@
+/*
+ * weight_patches.h -- C ABI of the GB300 (sm_103a) dynamic-LoRA linear library.
+ *
+ * Computes the dynamic, unmerged LoRA linear
+ *
+ *     Y = X W^T + bias + sum_p s_p (X A_p^T) B_p^T,
+ *     s_p = alpha_p / rank_p * strength_p * request_scale,
+ *
+ * and its siblings (stacked column groups, closed-form backward, dense patches) on
+ * one GPU.  Sources of the operations, cited by page title and section:
+ *   - sglang PR "[diffusion] Add the dynamic LoRA delta inside the second GEMM",
+ *     Motivation and Modifications: the combined scale multiplies the rank-wide
+ *     intermediate X A^T as a runtime value, the second low-rank GEMM accumulates
+ *     straight onto the base output so the [tokens, out] delta is never stored, the
+ *     bias lives in the base GEMM's epilogue, stacked q/k/v (gate/up) adapters take
+ *     one update per column group, an FP32 adapter keeps FP32 GEMMs and adds once;
+ *   - InvokeAI sidecar-patch article, sections 三-四: several patches on one layer are
+ *     summed, each weighted by its own strength;
+ *   - Unsloth fast_lora walkthrough, sections 2-4: 4-bit base weights dequantised
+ *     into the matmul, and the closed-form backward dX, dA, dB;
+ *   - FastVideo API docs, fastvideo.models.loader.lora_patch, DenseLoRAPatch:
+ *     .diff / .diff_b additive deltas summed in float32 and .set_weight replacement.
+ *
+ * Conventions for every entry point:
+ *   - All tensors are row-major.  X [T, in], W [out, in], A [r, in], B [out, r],
+ *     bias [1, out], Y [T, out].  "ld" is the row pitch in elements.
+ *   - Every data pointer is a DEVICE pointer on the current CUDA device; the caller
+ *     owns all memory.  The library allocates no device memory, never synchronises
+ *     and launches only on the caller's stream (`stream` is a cudaStream_t; NULL is
+ *     the legacy default stream).  Inputs are never written.
+ *   - Return value: WP_OK (0) or a negative WP_ERR_* code.  Argument checks run on
+ *     the host before anything is launched; a rejected call launches nothing.
+ *   - A kernel whose bounded wait expires records WP_ERR_TIMEOUT in a device status
+ *     word instead of hanging; read it with lora_device_status() after the stream has
+ *     been synchronised.
+ */
+#ifndef WEIGHT_PATCHES_H
+#define WEIGHT_PATCHES_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* storage types */
+enum {
+  WP_BF16 = 0, /* bfloat16 */
+  WP_FP32 = 1, /* IEEE binary32 */
+  WP_NF4 = 2   /* 4-bit NormalFloat: packed codes + one fp32 absmax per 64 elements */
+};
+
+/* status codes */
+enum {
+  WP_OK = 0,
+  WP_ERR_INVALID = -1,     /* null pointer, non-finite alpha/strength/scale, rank <= 0, bad kind */
+  WP_ERR_SHAPE = -2,       /* dimensions disagree (e.g. payload numel != parameter numel) */
+  WP_ERR_DTYPE = -3,       /* unsupported storage type or combination */
+  WP_ERR_ALIGN = -4,       /* a pointer or row pitch breaks the 16-byte alignment rule */
+  WP_ERR_WORKSPACE = -5,   /* workspace missing or smaller than lora_workspace_size() */
+  WP_ERR_CUDA = -6,        /* a CUDA runtime/driver call or a launch failed */
+  WP_ERR_TIMEOUT = -7,     /* a bounded device wait expired (device status word) */
+  WP_ERR_UNSUPPORTED = -8  /* a size beyond the documented limits */
+};
+
+/* dense-patch kinds */
+enum { WP_PATCH_ADD = 0, WP_PATCH_SET = 1 };
+
+/* An input matrix.  For WP_NF4, `data` holds rows*cols/2 bytes (row-major; byte k of
+ * the stream holds element 2k in its high nibble and element 2k+1 in its low
+ * nibble), `absmax` holds rows*cols/64 fp32 scales (one per 64 consecutive
+ * elements), cols % 64 == 0, and `ld` must equal `cols`. */
+typedef struct wp_mat {
+  const void* data;
+  int32_t dtype;
+  int64_t rows, cols, ld;
+  const float* absmax;
+} wp_mat;
+
+/* An output matrix (WP_BF16 or WP_FP32). */
+typedef struct wp_out {
+  void* data;
+  int32_t dtype;
+  int64_t rows, cols, ld;
+} wp_out;
+
+/* One low-rank patch.  A [r, in], B [out, r] (for grouped calls, out = the group's
+ * width); both WP_BF16, or both WP_FP32 for an FP32 adapter.  The combined scale
+ * s = alpha / r * strength * request_scale is formed on the host in double and
+ * rounded once to fp32; an adapter whose s is exactly +-0 contributes nothing. */
+typedef struct wp_adapter {
+  wp_mat A;
+  wp_mat B;
+  double alpha;
+  double strength;
+} wp_adapter;
+
+/* Operation ids for lora_workspace_size(). */
+enum { WP_OP_FWD = 0, WP_OP_FWD_GROUPED = 1, WP_OP_BWD = 2 };
+
+/*
+ * lora_linear_fwd -- Y = X W^T + bias + sum_p s_p (X A_p^T) B_p^T.
+ * (sglang PR "Add the dynamic LoRA delta inside the second GEMM", Modifications;
+ *  InvokeAI sidecar-patch article, section 四, for the sum over patches.)
+ *
+ *   X        [T, in], WP_BF16 (tensor-core path) or WP_FP32 (exact FP32 path).
+ *   W        [out, in], WP_BF16 or WP_NF4 with a bf16 X, WP_FP32 with an fp32 X;
+ *            NULL computes the low-rank delta only.
+ *   bias     [1, out] WP_BF16 or WP_FP32, or NULL; added in the epilogue.
+ *   adapters n_adapters patches (0..8); bf16 adapters on a bf16 X run on the tensor
+ *            cores, FP32 adapters run in FP32 on the CUDA cores and are added to the
+ *            same FP32 accumulator before the single output rounding.
+ *   Y        [T, out] WP_BF16 or WP_FP32, ld >= out; must not overlap the inputs.
+ *   workspace device scratch of at least lora_workspace_size(WP_OP_FWD, ...) bytes
+ *            (may be NULL when that size is 0).
+ * Alignment (tensor-core path): every base pointer 16-byte aligned, every ld a
+ * multiple of 8 elements (bf16) / 4 (fp32), in % 8 == 0, out % 8 == 0.
+ * Limits: the bf16 adapters of one call fit 256 tensor-memory columns, counting
+ * each adapter as ceil(r / 64) * 64 columns; r <= 256 per adapter; FP32 adapters
+ * total r <= 64.
+ */
+int lora_linear_fwd(const wp_mat* X, const wp_mat* W, const wp_mat* bias,
+                    const wp_adapter* adapters, int32_t n_adapters, double request_scale,
+                    const wp_out* Y, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * lora_linear_fwd_grouped -- stacked column groups (q/k/v, gate/up):
+ *   Y[:, g*out_g:(g+1)*out_g] = X W_g^T + bias_g + s_g (X A_g^T) B_g^T,
+ * with W_stacked = [W_0; ...; W_{G-1}] of shape [G*out_g, in] and one adapter per
+ * group (adapters[g], B_g of shape [out_g, r_g]).
+ * (sglang PR, Modifications: one update per group on column views of the output;
+ *  Unsloth walkthrough, section 4, LoRA_QKV.)
+ * Same dtypes, alignment and ownership as lora_linear_fwd; 1 <= n_groups <= 8,
+ * out_g % 8 == 0.
+ */
+int lora_linear_fwd_grouped(const wp_mat* X, const wp_mat* W_stacked, const wp_mat* bias,
+                            int32_t n_groups, const wp_adapter* adapters, double request_scale,
+                            const wp_out* Y, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * lora_linear_bwd -- closed-form gradients of Y = X W_g^T + s_g (X A_g^T) B_g^T over
+ * n_groups column groups (n_groups = 1 for a plain layer), with G_g = dY_g B_g:
+ *     dX   = sum_g dY_g W_g + s_g G_g A_g          [T, in]
+ *     dA_g = s_g G_g^T X                          [r_g, in]
+ *     dB_g = s_g dY_g^T (X A_g^T)                 [out_g, r_g]
+ * (Unsloth fast_lora walkthrough, sections 2 and 4: dX, dA, dB by hand, no
+ *  autograd graph, only X kept from the forward.)
+ *   X [T, in] WP_BF16; W [G*out_g, in] WP_BF16 or WP_NF4; dY [T, G*out_g] WP_BF16.
+ *   dX: WP_BF16 or WP_FP32 output, or NULL to skip; dA[g], dB[g]: WP_FP32 outputs.
+ *   dA/dB are overwritten (not accumulated).
+ */
+int lora_linear_bwd(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int32_t n_groups,
+                    const wp_adapter* adapters, double request_scale, const wp_out* dX,
+                    const wp_out* dA, const wp_out* dB, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/*
+ * lora_dense_patch -- the dense half of an adapter, applied in place to `param`.
+ * (FastVideo API docs, fastvideo.models.loader.lora_patch, DenseLoRAPatch.apply_to
+ *  and replacement_for.)
+ *   kind WP_PATCH_ADD (.diff / .diff_b): param = cast(fp32(param) + fp32(payload) * k)
+ *   kind WP_PATCH_SET (.set_weight):     param = cast(fp32(payload) * k)
+ * where k = (float)strength, the product and the sum are separate float32 roundings
+ * (no fused multiply-add) and cast is round-to-nearest-even into param_dtype.
+ *   param: param_numel elements of param_dtype (WP_BF16 or WP_FP32), device.
+ *   payload: payload_numel elements of payload_dtype (WP_BF16 or WP_FP32), device.
+ * Errors: WP_ERR_SHAPE if payload_numel != param_numel; WP_ERR_INVALID for a
+ * non-finite strength or unknown kind.  param and payload must not overlap.
+ */
+int lora_dense_patch(void* param, int32_t param_dtype, int64_t param_numel,
+                     const void* payload, int32_t payload_dtype, int64_t payload_numel,
+                     int32_t kind, double strength, void* stream);
+
+/* Bytes of device workspace the given call needs (0 if none).  `op` is WP_OP_*;
+ * the other arguments are those of the call (adapters: n_adapters, or n_groups). */
+size_t lora_workspace_size(int32_t op, const wp_mat* X, const wp_mat* W,
+                           const wp_adapter* adapters, int32_t n_adapters);
+
+/* Human-readable text for a status code (static storage). */
+const char* lora_status_string(int status);
+
+/* Reads (and, if `reset` != 0, clears) the device status word of the current device:
+ * WP_OK or WP_ERR_TIMEOUT.  Synchronous: call after the stream has finished. */
+int lora_device_status(int32_t reset);
+
+/* The library's 16 NormalFloat levels in ascending order (host memory, fp32). */
+void lora_nf4_codebook(float out[16]);
+
+/* The last CUDA error text the library saw on this host thread ("" if none). */
+const char* lora_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WEIGHT_PATCHES_H */

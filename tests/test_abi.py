@@ -1,0 +1,125 @@
+"""The C-ABI library loads, exports every function include/*.h declares, and rejects
+bad arguments on the host (no GPU needed: a rejected call launches nothing)."""
+import ctypes
+import glob
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import weight_patches_gb300 as wpg
+from oracle import nf4
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", src, flags=re.M):
+            name = m.group(1)
+            if name not in ("if", "for", "while", "sizeof", "return"):
+                names.add(name)
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return wpg.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert "lora_linear_fwd" in names and "lora_dense_patch" in names and len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_nf4_codebook_matches_oracle_bitwise():
+    got = np.array(wpg.lora_nf4_codebook(), dtype=np.float32)
+    want = nf4.codebook_f32()
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+FAKE = 0x10000  # a non-null, 16-byte aligned "device" address never dereferenced
+
+
+def _m(rows, cols, dtype=wpg.WP_BF16, ld=None, data=FAKE):
+    return wpg.WpMat(data, dtype, rows, cols, cols if ld is None else ld, None)
+
+
+def _o(rows, cols, dtype=wpg.WP_BF16, ld=None):
+    return wpg.WpOut(FAKE, dtype, rows, cols, cols if ld is None else ld)
+
+
+def _ad(r, n_in, n_out, alpha=8.0, strength=1.0, dtype=wpg.WP_BF16):
+    return wpg.WpAdapter(_m(r, n_in, dtype), _m(n_out, r, dtype), alpha, strength)
+
+
+def _fwd(lib, X, W, bias, ads, Y, rs=1.0):
+    arr = (wpg.WpAdapter * max(1, len(ads)))(*ads)
+    return lib.lora_linear_fwd(ctypes.byref(X), ctypes.byref(W) if W else None,
+                               ctypes.byref(bias) if bias else None, arr, len(ads), rs,
+                               ctypes.byref(Y), None, 0, None)
+
+
+def test_fwd_rejections(lib):
+    X, W, Y = _m(64, 128), _m(256, 128), _o(64, 256)
+    assert _fwd(lib, X, W, None, [_ad(8, 128, 256)], _o(64, 255)) == -2          # Y cols
+    assert _fwd(lib, X, _m(256, 127), None, [], Y) == -2                          # W cols
+    assert _fwd(lib, X, W, None, [_ad(8, 128, 300)], Y) == -2                     # B rows
+    assert _fwd(lib, X, W, None, [_ad(8, 120, 256)], Y) == -2                     # A cols
+    assert _fwd(lib, X, W, None, [_ad(8, 128, 256, alpha=math.nan)], Y) == -1     # non-finite alpha
+    assert _fwd(lib, X, W, None, [_ad(8, 128, 256, strength=math.inf)], Y) == -1
+    assert _fwd(lib, X, W, None, [_ad(8, 128, 256)], Y, rs=math.nan) == -1       # request scale
+    assert _fwd(lib, X, W, _m(1, 255), [], Y) == -2                               # bias numel
+    bad = wpg.WpAdapter(_m(8, 128), _m(256, 8, wpg.WP_FP32), 8.0, 1.0)
+    assert _fwd(lib, X, W, None, [bad], Y) == -3                                  # mixed A/B dtypes
+    assert _fwd(lib, _m(64, 128, data=None), W, None, [], Y) == -1               # null X
+    # fp32 adapter needs workspace (s * X A^T in fp32); none given
+    assert _fwd(lib, X, W, None, [_ad(8, 128, 256, dtype=wpg.WP_FP32)], Y) == -5
+    # tensor-core path alignment: row pitch not a multiple of 8 elements
+    assert _fwd(lib, _m(64, 128, ld=130), W, None, [], Y) == -4
+    assert _fwd(lib, X, W, None, [], _o(64, 256, ld=260)) == -4
+    # too many bf16 adapters' rank chunks for the tensor-memory rank region
+    many = [_ad(128, 128, 256) for _ in range(3)]
+    assert _fwd(lib, X, W, None, many, Y) == -8
+
+
+def test_grouped_rejections(lib):
+    X, W = _m(64, 128), _m(3 * 256, 128)
+    Y = _o(64, 3 * 256)
+    arr = (wpg.WpAdapter * 2)(_ad(8, 128, 256), _ad(8, 128, 256))
+    assert lib.lora_linear_fwd_grouped(ctypes.byref(X), ctypes.byref(W), None, 3, arr, 1.0,
+                                       ctypes.byref(Y), None, 0, None) != 0   # adapters per group
+    arr = (wpg.WpAdapter * 3)(_ad(8, 128, 256), _ad(8, 128, 256), _ad(8, 128, 200))
+    assert lib.lora_linear_fwd_grouped(ctypes.byref(X), ctypes.byref(W), None, 3, arr, 1.0,
+                                       ctypes.byref(Y), None, 0, None) == -2
+
+
+def test_dense_patch_rejections(lib):
+    assert lib.lora_dense_patch(FAKE, wpg.WP_BF16, 10, FAKE, wpg.WP_BF16, 11, 0, 1.0, None) == -2
+    assert lib.lora_dense_patch(FAKE, wpg.WP_BF16, 10, FAKE, wpg.WP_BF16, 10, 0, math.nan, None) == -1
+    assert lib.lora_dense_patch(FAKE, wpg.WP_BF16, 10, FAKE, wpg.WP_BF16, 10, 7, 1.0, None) == -1
+    assert lib.lora_dense_patch(FAKE, wpg.WP_NF4, 10, FAKE, wpg.WP_BF16, 10, 0, 1.0, None) == -3
+    assert lib.lora_dense_patch(None, wpg.WP_BF16, 10, FAKE, wpg.WP_BF16, 10, 0, 1.0, None) == -1
+
+
+def test_workspace_sizes(lib):
+    X, W = _m(1000, 128), _m(256, 128)
+    arr = (wpg.WpAdapter * 2)(_ad(8, 128, 256), _ad(16, 128, 256, dtype=wpg.WP_FP32))
+    # tensor-core path: only the fp32 adapter's s * X A^T is staged, 1000 x 16 fp32
+    assert lib.lora_workspace_size(0, ctypes.byref(X), ctypes.byref(W), arr, 2) == 64000
+    assert lib.lora_workspace_size(0, ctypes.byref(X), ctypes.byref(W), arr, 1) == 0
+    Xf = _m(1000, 128, wpg.WP_FP32)
+    # fp32 path: every adapter's s * X A^T, 1000 x 24 fp32, rounded up to 256 bytes
+    assert lib.lora_workspace_size(0, ctypes.byref(Xf), ctypes.byref(W), arr, 2) == 96000
+
+
+def test_status_strings(lib):
+    for code in wpg.STATUS:
+        assert wpg.lora_status_string(code)

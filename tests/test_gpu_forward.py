@@ -1,0 +1,171 @@
+"""GPU parity of the fused forward against the CPU FP64 oracle, through the C ABI.
+
+Tolerances (from the method's accuracy gate): bf16 outputs within relative RMS 4e-3 and
+no worse than the unfused bf16 chain that materialises the delta; FP32 cases within
+1e-5."""
+import numpy as np
+import pytest
+import torch
+
+import weight_patches_gb300 as wpg
+import workloads
+from oracle import lora as olora
+from oracle.numerics import relative_rms
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+BF16_TOL = 4e-3
+FP32_TOL = 1e-5
+
+
+def _gate(err, chain):
+    assert err <= BF16_TOL, err
+    assert err <= chain, (err, chain)
+
+
+def test_c0_tiny_fp32():
+    lin = workloads.config0()
+    Y = gu.run_fwd(lin, out_dtype=torch.float32)
+    err = relative_rms(gu.to_f64(Y), olora.reference_output(lin))
+    assert err <= FP32_TOL, err
+
+
+def test_c1_grouped_small():
+    lin = workloads.config1("small")
+    Y = gu.run_fwd(lin)
+    _gate(*gu.errors(lin, Y))
+    assert wpg.lora_device_status() == 0
+
+
+def test_c2_ffn_small_with_bias():
+    up, down, _ = workloads.config2("small")
+    for lin in (up, down):
+        Y = gu.run_fwd(lin)
+        _gate(*gu.errors(lin, Y))
+
+
+def test_c4_multipatch_small():
+    lin, _ = workloads.config4("small")
+    Y = gu.run_fwd(lin)
+    _gate(*gu.errors(lin, Y))
+
+
+def test_c4_fp32_adapter_fp32_output():
+    lin, _ = workloads.config4("small")
+    lin.patches = lin.patches[:1]            # the fp32 adapter alone, on the bf16 layer
+    Y = gu.run_fwd(lin, out_dtype=torch.float32)
+    err = relative_rms(gu.to_f64(Y), olora.reference_output(lin))
+    assert err <= FP32_TOL, err
+    # delta only (no base weight): the fp32 adapter's contribution by itself
+    Yd = gu.run_fwd(lin, out_dtype=torch.float32, with_base=False)
+    X, _, _, patches = olora.decode_linear(lin)
+    want = olora.linear_fwd(X, None, None, patches, lin.request_scale, out_features=lin.out_features)
+    err = relative_rms(gu.to_f64(Yd), want)
+    assert err <= FP32_TOL, err
+
+
+def test_fp32_output_bf16_adapters():
+    lin = workloads.config1("small")
+    Y = gu.run_fwd(lin, out_dtype=torch.float32)
+    err, _ = gu.errors(lin, Y)
+    # one bf16 rounding of s * X A^T remains; the base is exact to fp32 accumulation
+    assert err <= 2e-3, err
+
+
+def test_zero_scale_equals_no_adapter_bitwise():
+    lin = workloads.config1("small")
+    X, W = gu.dev(lin.X), gu.dev(lin.W)
+    ads = gu.adapters(lin)
+    y0 = wpg.lora_linear_fwd_grouped(X, W, None, ads, 0.0)
+    zero = [wpg.Adapter(a.A, a.B, a.alpha, 0.0) for a in ads]
+    y1 = wpg.lora_linear_fwd_grouped(X, W, None, zero, 1.0)
+    # base only, through the plain entry with no adapters
+    y2 = wpg.lora_linear_fwd(X, W, None, [])
+    torch.cuda.synchronize()
+    assert torch.equal(y0.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_delta_linear_in_scale():
+    lin = workloads.config1("small")
+    X, W = gu.dev(lin.X), gu.dev(lin.W)
+    ads = gu.adapters(lin)
+    base = wpg.lora_linear_fwd(X, W, None, [], out_dtype=torch.float32)
+    y1 = wpg.lora_linear_fwd_grouped(X, W, None, ads, 0.25, out_dtype=torch.float32)
+    y2 = wpg.lora_linear_fwd_grouped(X, W, None, ads, 0.5, out_dtype=torch.float32)
+    d1, d2 = (y1 - base).double(), (y2 - base).double()
+    # s * H is rounded to bf16 once, so doubling s doubles the delta exactly up to fp32 sums
+    assert float(((d2 - 2 * d1).norm() / d2.norm()).item()) < 1e-5
+
+
+def test_multi_patch_is_sum_of_single_patches():
+    lin, _ = workloads.config4("small")
+    lin.patches = lin.patches[1:]           # the two bf16 patches
+    X, W = gu.dev(lin.X), gu.dev(lin.W)
+    ads = gu.adapters(lin)
+    base = wpg.lora_linear_fwd(X, W, None, [], out_dtype=torch.float32).double()
+    both = wpg.lora_linear_fwd(X, W, None, ads, out_dtype=torch.float32).double() - base
+    one = sum(wpg.lora_linear_fwd(X, W, None, [a], out_dtype=torch.float32).double() - base for a in ads)
+    assert float(((both - one).norm() / both.norm()).item()) < 1e-5
+
+
+@pytest.mark.parametrize("T,K,N,r", [(1, 64, 256, 8), (127, 200, 520, 16), (129, 64, 8, 8),
+                                     (300, 72, 264, 24), (640, 1024, 768, 96), (256, 128, 256, 256)])
+def test_edge_shapes(T, K, N, r):
+    rng = np.random.default_rng(T * 7 + K)
+    X = workloads.draw(rng, T, K, 1.0)
+    W = workloads.draw(rng, N, K, (1.0 / K) ** 0.5)
+    A = workloads.draw(rng, r, K, (1.0 / K) ** 0.5)
+    B = workloads.draw(rng, N, r, 0.02)
+    bias = workloads.draw(rng, 1, N, 0.01)
+    lin = workloads.Linear("edge", X, W, bias, [workloads.Patch(A, B, float(2 * r), 0.9)], request_scale=0.7)
+    Y = gu.run_fwd(lin)
+    _gate(*gu.errors(lin, Y))
+
+
+def test_rank_without_aligned_pitch_is_rejected():
+    X = torch.zeros(16, 64, dtype=torch.bfloat16, device=gu.DEV)
+    W = torch.zeros(64, 64, dtype=torch.bfloat16, device=gu.DEV)
+    A = torch.zeros(3, 64, dtype=torch.bfloat16, device=gu.DEV)
+    B = torch.zeros(64, 3, dtype=torch.bfloat16, device=gu.DEV)   # row pitch 3: not TMA-able
+    with pytest.raises(wpg.WeightPatchesError) as e:
+        wpg.lora_linear_fwd(X, W, None, [wpg.Adapter(A, B, 3.0)])
+    assert e.value.status == -4
+    # the same adapter with a padded pitch works
+    Bp = torch.zeros(64, 8, dtype=torch.bfloat16, device=gu.DEV)[:, :3]
+    Ap = torch.zeros(3, 64, dtype=torch.bfloat16, device=gu.DEV)
+    wpg.lora_linear_fwd(X, W, None, [wpg.Adapter(Ap, Bp, 3.0)])
+    torch.cuda.synchronize()
+
+
+def test_no_worse_than_torch_unfused_chain():
+    lin = workloads.config1("small")
+    Y = gu.run_fwd(lin)
+    want = olora.reference_output(lin)
+    err = relative_rms(gu.to_f64(Y), want)
+    chain = relative_rms(gu.to_f64(gu.torch_unfused_chain(lin)), want)
+    assert err <= chain, (err, chain)
+
+
+# ----------------------------------------------------------------- full sizes (spot checks)
+def test_c1_full_sampled_rows():
+    lin = workloads.config1("full")
+    Y = gu.run_fwd(lin)
+    rows = workloads.sample_rows(lin.T, 192)
+    _gate(*gu.errors(lin, Y, rows))
+
+
+def test_c2_full_sampled_rows():
+    up, down, _ = workloads.config2("full")
+    for lin in (up, down):
+        Y = gu.run_fwd(lin)
+        rows = workloads.sample_rows(lin.T, 96)
+        _gate(*gu.errors(lin, Y, rows))
+
+
+def test_c4_full_sampled_rows():
+    lin, _ = workloads.config4("full")
+    Y = gu.run_fwd(lin)
+    rows = workloads.sample_rows(lin.T, 96)
+    _gate(*gu.errors(lin, Y, rows))

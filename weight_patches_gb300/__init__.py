@@ -1,0 +1,261 @@
+"""weight_patches_gb300 -- the dynamic, unmerged LoRA linear on GB300 (sm_103a).
+
+A thin ctypes binding over ``libweight_patches_gb300.so`` (C ABI in
+``include/weight_patches.h``).  The functions here only marshal arguments: torch
+tensors supply device memory and the current CUDA stream; every step of the
+computation runs in the library's CUDA kernels.  There is no fallback: if the shared
+library has not been built, importing it raises.
+
+Entry points (same names as the C ABI):
+    lora_linear_fwd          Y = X W^T + bias + sum_p s_p (X A_p^T) B_p^T
+    lora_linear_fwd_grouped  stacked column groups, one adapter per group
+    lora_linear_bwd          closed-form dX, dA, dB
+    lora_dense_patch         .diff / .diff_b (add) and .set_weight (replace), in place
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libweight_patches_gb300.so")
+
+WP_BF16, WP_FP32, WP_NF4 = 0, 1, 2
+WP_PATCH_ADD, WP_PATCH_SET = 0, 1
+WP_OP_FWD, WP_OP_FWD_GROUPED, WP_OP_BWD = 0, 1, 2
+STATUS = {0: "WP_OK", -1: "WP_ERR_INVALID", -2: "WP_ERR_SHAPE", -3: "WP_ERR_DTYPE",
+          -4: "WP_ERR_ALIGN", -5: "WP_ERR_WORKSPACE", -6: "WP_ERR_CUDA", -7: "WP_ERR_TIMEOUT",
+          -8: "WP_ERR_UNSUPPORTED"}
+
+
+class WpMat(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("rows", ctypes.c_int64),
+                ("cols", ctypes.c_int64), ("ld", ctypes.c_int64), ("absmax", ctypes.c_void_p)]
+
+
+class WpOut(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("rows", ctypes.c_int64),
+                ("cols", ctypes.c_int64), ("ld", ctypes.c_int64)]
+
+
+class WpAdapter(ctypes.Structure):
+    _fields_ = [("A", WpMat), ("B", WpMat), ("alpha", ctypes.c_double),
+                ("strength", ctypes.c_double)]
+
+
+class WeightPatchesError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        lib = _load()
+        msg = lib.lora_status_string(status).decode()
+        cuda = lib.lora_last_cuda_error().decode()
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({msg}){' / ' + cuda if cuda else ''}")
+
+
+_LIB = None
+
+
+def _load():
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()'"
+            " or python weight_patches_gb300/build.py)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, D, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double, ctypes.c_size_t
+    pm, po, pa = ctypes.POINTER(WpMat), ctypes.POINTER(WpOut), ctypes.POINTER(WpAdapter)
+    lib.lora_linear_fwd.argtypes = [pm, pm, pm, pa, I32, D, po, P, SZ, P]
+    lib.lora_linear_fwd_grouped.argtypes = [pm, pm, pm, I32, pa, D, po, P, SZ, P]
+    lib.lora_linear_bwd.argtypes = [pm, pm, pm, I32, pa, D, po, po, po, P, SZ, P]
+    lib.lora_dense_patch.argtypes = [P, I32, I64, P, I32, I64, I32, D, P]
+    lib.lora_workspace_size.argtypes = [I32, pm, pm, pa, I32]
+    lib.lora_workspace_size.restype = SZ
+    lib.lora_status_string.argtypes = [ctypes.c_int]
+    lib.lora_status_string.restype = ctypes.c_char_p
+    lib.lora_device_status.argtypes = [I32]
+    lib.lora_nf4_codebook.argtypes = [ctypes.POINTER(ctypes.c_float)]
+    lib.lora_nf4_codebook.restype = None
+    lib.lora_last_cuda_error.restype = ctypes.c_char_p
+    for name in ("lora_linear_fwd", "lora_linear_fwd_grouped", "lora_linear_bwd", "lora_dense_patch",
+                 "lora_device_status"):
+        getattr(lib, name).restype = ctypes.c_int
+    _LIB = lib
+    return lib
+
+
+def lib():
+    """The loaded shared library (ctypes.CDLL)."""
+    return _load()
+
+
+# ------------------------------------------------------------------------- marshalling
+@dataclass
+class NF4Weight:
+    """A 4-bit NormalFloat weight [rows, cols]: ``packed`` uint8 [rows, cols // 2] (element
+    2k in the high nibble of byte k), ``absmax`` fp32 [rows * cols // 64]."""
+
+    packed: torch.Tensor
+    absmax: torch.Tensor
+    rows: int
+    cols: int
+
+
+@dataclass
+class Adapter:
+    """One low-rank patch: A [r, in], B [out, r] (bf16, or fp32 for an FP32 adapter)."""
+
+    A: torch.Tensor
+    B: torch.Tensor
+    alpha: float
+    strength: float = 1.0
+
+
+_DT = {torch.bfloat16: WP_BF16, torch.float32: WP_FP32}
+
+
+def _mat(t) -> Optional[WpMat]:
+    if t is None:
+        return None
+    if isinstance(t, NF4Weight):
+        if not (t.packed.is_contiguous() and t.absmax.is_contiguous()):
+            raise ValueError("NF4Weight tensors must be contiguous")
+        return WpMat(t.packed.data_ptr(), WP_NF4, t.rows, t.cols, t.cols, t.absmax.data_ptr())
+    if t.dim() == 1:
+        return WpMat(t.data_ptr(), _DT[t.dtype], 1, t.shape[0], t.shape[0], None)
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D row-major tensor (stride(1) == 1)")
+    return WpMat(t.data_ptr(), _DT[t.dtype], t.shape[0], t.shape[1], t.stride(0), None)
+
+
+def _out(t: torch.Tensor) -> WpOut:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D row-major output tensor")
+    return WpOut(t.data_ptr(), _DT[t.dtype], t.shape[0], t.shape[1], t.stride(0))
+
+
+def _adapters(adapters: Sequence[Adapter]):
+    arr = (WpAdapter * max(1, len(adapters)))()
+    for i, a in enumerate(adapters):
+        arr[i] = WpAdapter(_mat(a.A), _mat(a.B), float(a.alpha), float(a.strength))
+    return arr
+
+
+def _ref(m):
+    return ctypes.byref(m) if m is not None else None
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise WeightPatchesError(status, where)
+
+
+def _workspace(op, xm, wm, arr, n, device, workspace):
+    need = _load().lora_workspace_size(op, ctypes.byref(xm), _ref(wm), arr, n)
+    if need == 0:
+        return None, 0
+    if workspace is not None and workspace.numel() * workspace.element_size() >= need:
+        return workspace, need
+    return torch.empty(need, dtype=torch.uint8, device=device), need
+
+
+def lora_workspace_size(op: int, X, W, adapters: Sequence[Adapter]) -> int:
+    xm, wm, arr = _mat(X), _mat(W), _adapters(adapters)
+    return _load().lora_workspace_size(op, ctypes.byref(xm), _ref(wm), arr, len(adapters))
+
+
+def _out_features(X, W, adapters):
+    if W is not None:
+        return W.rows if isinstance(W, NF4Weight) else W.shape[0]
+    return adapters[0].B.shape[0]
+
+
+def lora_linear_fwd(X: torch.Tensor, W, bias: Optional[torch.Tensor], adapters: Sequence[Adapter],
+                    request_scale: float = 1.0, out: Optional[torch.Tensor] = None,
+                    out_dtype: torch.dtype = torch.bfloat16,
+                    workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Y = X W^T + bias + sum_p s_p (X A_p^T) B_p^T with s_p = alpha/r * strength * request_scale."""
+    if out is None:
+        out = torch.empty(X.shape[0], _out_features(X, W, adapters), dtype=out_dtype, device=X.device)
+    xm, wm, bm, arr, ym = _mat(X), _mat(W), _mat(bias), _adapters(adapters), _out(out)
+    ws, nbytes = _workspace(WP_OP_FWD, xm, wm, arr, len(adapters), X.device, workspace)
+    st = _load().lora_linear_fwd(ctypes.byref(xm), _ref(wm), _ref(bm), arr, len(adapters),
+                                 float(request_scale), ctypes.byref(ym),
+                                 ws.data_ptr() if ws is not None else None, nbytes, _stream(X.device))
+    _check(st, "lora_linear_fwd")
+    return out
+
+
+def lora_linear_fwd_grouped(X: torch.Tensor, W_stacked, bias: Optional[torch.Tensor],
+                            adapters: Sequence[Adapter], request_scale: float = 1.0,
+                            out: Optional[torch.Tensor] = None, out_dtype: torch.dtype = torch.bfloat16,
+                            workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Stacked column groups: group g of the output gets X W_g^T + bias_g + s_g (X A_g^T) B_g^T."""
+    n = W_stacked.rows if isinstance(W_stacked, NF4Weight) else W_stacked.shape[0]
+    if out is None:
+        out = torch.empty(X.shape[0], n, dtype=out_dtype, device=X.device)
+    xm, wm, bm, arr, ym = _mat(X), _mat(W_stacked), _mat(bias), _adapters(adapters), _out(out)
+    ws, nbytes = _workspace(WP_OP_FWD_GROUPED, xm, wm, arr, len(adapters), X.device, workspace)
+    st = _load().lora_linear_fwd_grouped(ctypes.byref(xm), ctypes.byref(wm), _ref(bm), len(adapters),
+                                         arr, float(request_scale), ctypes.byref(ym),
+                                         ws.data_ptr() if ws is not None else None, nbytes,
+                                         _stream(X.device))
+    _check(st, "lora_linear_fwd_grouped")
+    return out
+
+
+def lora_linear_bwd(X: torch.Tensor, W, dY: torch.Tensor, adapters: Sequence[Adapter],
+                    request_scale: float = 1.0, need_dX: bool = True,
+                    dX_dtype: torch.dtype = torch.bfloat16, workspace: Optional[torch.Tensor] = None):
+    """Closed-form (dX, [dA_g], [dB_g]) of Y = X W_g^T + s_g (X A_g^T) B_g^T over len(adapters) groups."""
+    G = len(adapters)
+    dX = torch.empty_like(X, dtype=dX_dtype) if need_dX else None
+    dA = [torch.empty(a.A.shape, dtype=torch.float32, device=X.device) for a in adapters]
+    dB = [torch.empty(a.B.shape, dtype=torch.float32, device=X.device) for a in adapters]
+    xm, wm, dym, arr = _mat(X), _mat(W), _mat(dY), _adapters(adapters)
+    dxo = _out(dX) if dX is not None else None
+    dao = (WpOut * G)(*[_out(t) for t in dA])
+    dbo = (WpOut * G)(*[_out(t) for t in dB])
+    ws, nbytes = _workspace(WP_OP_BWD, xm, wm, arr, G, X.device, workspace)
+    st = _load().lora_linear_bwd(ctypes.byref(xm), ctypes.byref(wm), ctypes.byref(dym), G, arr,
+                                 float(request_scale), _ref(dxo), dao, dbo,
+                                 ws.data_ptr() if ws is not None else None, nbytes, _stream(X.device))
+    _check(st, "lora_linear_bwd")
+    return dX, dA, dB
+
+
+def lora_dense_patch(param: torch.Tensor, payload: torch.Tensor, kind: int, strength: float = 1.0) -> torch.Tensor:
+    """Apply a dense payload to ``param`` in place (.diff/.diff_b: kind=WP_PATCH_ADD,
+    .set_weight: kind=WP_PATCH_SET) and return it."""
+    if not (param.is_contiguous() and payload.is_contiguous()):
+        raise ValueError("dense patch tensors must be contiguous")
+    st = _load().lora_dense_patch(param.data_ptr(), _DT[param.dtype], param.numel(), payload.data_ptr(),
+                                  _DT[payload.dtype], payload.numel(), int(kind), float(strength),
+                                  _stream(param.device))
+    _check(st, "lora_dense_patch")
+    return param
+
+
+def lora_device_status(reset: bool = True) -> int:
+    """The device status word (0, or -7 after a bounded wait expired).  Synchronises."""
+    torch.cuda.synchronize()
+    return _load().lora_device_status(1 if reset else 0)
+
+
+def lora_nf4_codebook() -> list:
+    buf = (ctypes.c_float * 16)()
+    _load().lora_nf4_codebook(buf)
+    return list(buf)
+
+
+def lora_status_string(status: int) -> str:
+    return _load().lora_status_string(status).decode()

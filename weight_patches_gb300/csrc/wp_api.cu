@@ -1,0 +1,380 @@
+// wp_api.cu -- the C ABI: argument checks, combined scales, tensor maps, dispatch.
+//
+// Every entry point validates on the host and launches nothing when it rejects a
+// call.  The library never allocates device memory and never synchronises; all work
+// is enqueued on the caller's stream.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "wp_internal.h"
+
+namespace wp {
+
+namespace {
+thread_local std::string g_last_error;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [outer, inner] matrix with row pitch ld
+// (elements), 128-byte swizzled boxes of {box_inner, box_outer}; out-of-range
+// elements read as zero.
+int make_map_bf16(CUtensorMap* m, const void* ptr, long long inner, long long outer, long long ld,
+                  int box_inner, int box_outer) {
+  auto fn = encode_fn();
+  if (!fn) {
+    g_last_error = "cuTensorMapEncodeTiled unavailable";
+    return WP_ERR_CUDA;
+  }
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[96];
+    snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    g_last_error = buf;
+    return WP_ERR_CUDA;
+  }
+  return WP_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_input(const wp_mat* m, bool allow_nf4) {
+  if (!m || !m->data) return false;
+  if (m->rows < 0 || m->cols <= 0) return false;
+  if (m->dtype == WP_NF4) {
+    if (!allow_nf4 || !m->absmax) return false;
+    return true;
+  }
+  if (m->dtype != WP_BF16 && m->dtype != WP_FP32) return false;
+  return m->ld >= m->cols;
+}
+
+bool valid_output(const wp_out* y) {
+  if (!y || !y->data) return false;
+  if (y->dtype != WP_BF16 && y->dtype != WP_FP32) return false;
+  return y->rows >= 0 && y->cols > 0 && y->ld >= y->cols;
+}
+
+size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+struct FwdPlan {
+  bool tc = false;        // tensor-core path
+  int rank32_total = 0;   // fp32 adapters' total rank (tensor-core path)
+  int rank_all = 0;       // all adapters' total rank (fp32 path)
+};
+
+// Decide the path from the dtypes alone (the same answer lora_workspace_size gives).
+int plan_fwd(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int n, FwdPlan* plan) {
+  plan->tc = X->dtype == WP_BF16 && (!W || W->dtype == WP_BF16 || W->dtype == WP_NF4);
+  for (int i = 0; i < n; ++i) {
+    const int r = static_cast<int>(ad[i].A.rows);
+    plan->rank_all += r;
+    if (ad[i].A.dtype == WP_FP32) plan->rank32_total += r;
+  }
+  return WP_OK;
+}
+
+size_t fwd_workspace(const wp_mat* X, const FwdPlan& plan) {
+  const size_t T = static_cast<size_t>(X->rows);
+  if (plan.tc) return plan.rank32_total ? round256(T * plan.rank32_total * 4) : 0;
+  return plan.rank_all ? round256(T * plan.rank_all * 4) : 0;
+}
+
+int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool grouped,
+             const wp_adapter* adapters, int n_adapters, double request_scale, const wp_out* Y,
+             void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (!valid_input(X, false)) return WP_ERR_INVALID;
+  if (W && !valid_input(W, true)) return WP_ERR_INVALID;
+  if (!valid_output(Y)) return WP_ERR_INVALID;
+  if (!std::isfinite(request_scale)) return WP_ERR_INVALID;
+  if (n_adapters < 0 || n_adapters > kMaxAd + kMaxAd32) return WP_ERR_UNSUPPORTED;
+  if (n_adapters > 0 && !adapters) return WP_ERR_INVALID;
+  if (grouped && (G < 1 || G > kMaxGroups || n_adapters != G)) return WP_ERR_INVALID;
+  if (!grouped) G = 1;
+
+  const long long T = X->rows, K = X->cols;
+  const long long N = W ? W->rows : Y->cols;
+  if (W && W->cols != K) return WP_ERR_SHAPE;
+  if (Y->rows != T || Y->cols != N) return WP_ERR_SHAPE;
+  if (N % G) return WP_ERR_SHAPE;
+  const long long out_g = N / G;
+  if (W && W->dtype == WP_NF4 && (K % 64 != 0 || W->ld != K)) return WP_ERR_SHAPE;
+  if (bias) {
+    if (!bias->data || (bias->dtype != WP_BF16 && bias->dtype != WP_FP32)) return WP_ERR_INVALID;
+    if (bias->rows * bias->cols != N) return WP_ERR_SHAPE;
+  }
+  if (T > 0x7FFFFFFFLL || K > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL) return WP_ERR_UNSUPPORTED;
+
+  // adapters: shapes, dtypes and combined scales
+  float s_of[kMaxAd + kMaxAd32];
+  for (int i = 0; i < n_adapters; ++i) {
+    const wp_adapter& a = adapters[i];
+    if (!valid_input(&a.A, false) || !valid_input(&a.B, false)) return WP_ERR_INVALID;
+    if (a.A.dtype != a.B.dtype) return WP_ERR_DTYPE;
+    const long long r = a.A.rows;
+    if (r <= 0) return WP_ERR_INVALID;
+    if (a.A.cols != K || a.B.cols != r || a.B.rows != (grouped ? out_g : N)) return WP_ERR_SHAPE;
+    if (!std::isfinite(a.alpha) || !std::isfinite(a.strength)) return WP_ERR_INVALID;
+    const double s = a.alpha / static_cast<double>(r) * a.strength * request_scale;
+    if (!std::isfinite(s) || !std::isfinite(static_cast<float>(s))) return WP_ERR_INVALID;
+    s_of[i] = static_cast<float>(s);
+  }
+
+  FwdPlan plan;
+  plan_fwd(X, W, adapters, n_adapters, &plan);
+  const size_t need = fwd_workspace(X, plan);
+  if (need > 0 && (!workspace || ws_bytes < need)) return WP_ERR_WORKSPACE;
+  if (need > 0 && !aligned16(workspace)) return WP_ERR_ALIGN;
+  if (T == 0) return WP_OK;
+
+  if (!plan.tc) {
+    // ------------------------------------------------------------- exact FP32 path
+    if (W && W->dtype == WP_NF4) return WP_ERR_DTYPE;
+    F32Params fp{};
+    fp.T = static_cast<int>(T); fp.K = static_cast<int>(K); fp.N = static_cast<int>(N);
+    fp.X = X->data; fp.x_dtype = X->dtype; fp.ldx = X->ld;
+    fp.W = W ? W->data : nullptr; fp.w_dtype = W ? W->dtype : WP_FP32; fp.ldw = W ? W->ld : 0;
+    fp.bias = bias ? bias->data : nullptr; fp.bias_dtype = bias ? bias->dtype : WP_FP32;
+    fp.Y = Y->data; fp.y_dtype = Y->dtype; fp.ldy = Y->ld;
+    H32Params hp{};
+    hp.T = fp.T; hp.K = fp.K; hp.X = X->data; hp.x_dtype = X->dtype; hp.ldx = X->ld;
+    int off = 0;
+    for (int i = 0; i < n_adapters; ++i) {
+      if (s_of[i] == 0.0f) continue;
+      const wp_adapter& a = adapters[i];
+      const int k = fp.n_ad++;
+      fp.ad[k].A = a.A.data; fp.ad[k].a_dtype = a.A.dtype; fp.ad[k].lda = a.A.ld;
+      fp.ad[k].B = a.B.data; fp.ad[k].b_dtype = a.B.dtype; fp.ad[k].ldb = a.B.ld;
+      fp.ad[k].rank = static_cast<int>(a.A.rows); fp.ad[k].s = s_of[i];
+      const int g = grouped ? i : 0;
+      fp.col_begin[k] = static_cast<int>(g * out_g);
+      fp.col_end[k] = static_cast<int>((g + 1) * out_g);
+      hp.A[k] = a.A.data; hp.a_dtype[k] = a.A.dtype; hp.lda[k] = a.A.ld;
+      hp.rank[k] = fp.ad[k].rank; hp.h_off[k] = off; hp.s[k] = s_of[i];
+      off += fp.ad[k].rank;
+    }
+    hp.n_ad = fp.n_ad; hp.H = static_cast<float*>(workspace); hp.h_cols = off;
+    int rc = WP_OK;
+    if (hp.n_ad > 0) rc = launch_h32(hp, stream);
+    if (rc != WP_OK) return rc;
+    return launch_f32_linear(fp, static_cast<const float*>(workspace), off, stream);
+  }
+
+  // --------------------------------------------------------------- tensor-core path
+  if (W && W->dtype == WP_NF4) return WP_ERR_UNSUPPORTED;   // 4-bit mainloop not built yet
+  if (!aligned16(X->data) || X->ld % 8) return WP_ERR_ALIGN;
+  if (W && (!aligned16(W->data) || W->ld % 8)) return WP_ERR_ALIGN;
+  if (!aligned16(Y->data) || Y->ld % (Y->dtype == WP_BF16 ? 8 : 4)) return WP_ERR_ALIGN;
+  if (out_g % 8) return WP_ERR_ALIGN;
+
+  TcParams p{};
+  TcMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  p.T = static_cast<int>(T); p.K = static_cast<int>(K); p.N = static_cast<int>(N);
+  p.out_g = static_cast<int>(out_g); p.G = G;
+  p.nt_g = static_cast<int>((out_g + kBN - 1) / kBN);
+  p.m_tiles = static_cast<int>((T + kBM - 1) / kBM);
+  const long long total = static_cast<long long>(p.m_tiles) * G * p.nt_g;
+  if (total > 0x7FFFFFFFLL) return WP_ERR_UNSUPPORTED;
+  p.total_tiles = static_cast<int>(total);
+  p.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
+  p.has_base = W ? 1 : 0;
+  p.bias = bias ? bias->data : nullptr; p.bias_f32 = bias && bias->dtype == WP_FP32;
+  p.Y = Y->data; p.ldy = Y->ld; p.y_f32 = Y->dtype == WP_FP32;
+  p.timeout_ns = 2000000000ull;
+
+  // Plan the adapters (host only; every rejection happens before any CUDA call).
+  H32Params hp{};
+  hp.T = p.T; hp.K = p.K; hp.X = X->data; hp.x_dtype = WP_BF16; hp.ldx = X->ld;
+  int src_of[kMaxAd];
+  int h_off = 0;
+  for (int g = 0; g < G; ++g) {
+    p.ad_begin[g] = p.n_ad;
+    int chunk = 0;
+    for (int i = 0; i < n_adapters; ++i) {
+      const int ag = grouped ? i : 0;
+      if (ag != g || s_of[i] == 0.0f) continue;
+      const wp_adapter& a = adapters[i];
+      const int r = static_cast<int>(a.A.rows);
+      if (a.A.dtype == WP_FP32) {
+        if (p.n_ad32 >= kMaxAd32) return WP_ERR_UNSUPPORTED;
+        TcAdapter32& d = p.ad32[p.n_ad32++];
+        d.group = g; d.rank = r; d.h_off = h_off; d.ldb = static_cast<int>(a.B.ld);
+        d.B = static_cast<const float*>(a.B.data);
+        const int k = hp.n_ad++;
+        hp.A[k] = a.A.data; hp.a_dtype[k] = WP_FP32; hp.lda[k] = a.A.ld; hp.rank[k] = r;
+        hp.h_off[k] = h_off; hp.s[k] = s_of[i];
+        h_off += r;
+        continue;
+      }
+      if (p.n_ad >= kMaxAd) return WP_ERR_UNSUPPORTED;
+      if (r > 256) return WP_ERR_UNSUPPORTED;
+      if (!aligned16(a.A.data) || a.A.ld % 8 || !aligned16(a.B.data) || a.B.ld % 8)
+        return WP_ERR_ALIGN;
+      TcAdapter& d = p.ad[p.n_ad];
+      d.group = g; d.rank = r; d.rpad16 = (r + 15) / 16 * 16; d.chunk_off = chunk;
+      d.nchunks = (r + 63) / 64; d.s = s_of[i];
+      chunk += d.nchunks;
+      if (chunk * 64 > kHCols) return WP_ERR_UNSUPPORTED;
+      src_of[p.n_ad] = i;
+      ++p.n_ad;
+    }
+    if (chunk > p.hchunks) p.hchunks = chunk;
+  }
+  p.ad_begin[G] = p.n_ad;
+  p.h32 = static_cast<const float*>(workspace);
+  p.h32_cols = h_off;
+  hp.H = static_cast<float*>(workspace); hp.h_cols = h_off;
+
+  // Tensor maps (driver calls from here on).
+  int rc = make_map_bf16(&maps.x, X->data, K, T, X->ld, kBK, kBM);
+  if (rc != WP_OK) return rc;
+  if (W) {
+    rc = make_map_bf16(&maps.w, W->data, K, N, W->ld, kBK, kBN);
+    if (rc != WP_OK) return rc;
+  }
+  for (int k = 0; k < p.n_ad; ++k) {
+    const wp_adapter& a = adapters[src_of[k]];
+    rc = make_map_bf16(&maps.a[k], a.A.data, K, p.ad[k].rank, a.A.ld, kBK, p.ad[k].rpad16);
+    if (rc != WP_OK) return rc;
+    rc = make_map_bf16(&maps.b[k], a.B.data, p.ad[k].rank, out_g, a.B.ld, 64, kBN);
+    if (rc != WP_OK) return rc;
+  }
+
+  const size_t fixed = 1024 + static_cast<size_t>(p.hchunks) * kHChunkBytes + 256;
+  int stages = static_cast<int>((kSmemLimit - fixed) / kStageBytes);
+  if (stages > 4) stages = 4;
+  if (stages < 2) return WP_ERR_UNSUPPORTED;
+  p.stages = stages;
+  const size_t smem = fixed + static_cast<size_t>(stages) * kStageBytes;
+
+  if (hp.n_ad > 0) {
+    rc = launch_h32(hp, stream);
+    if (rc != WP_OK) return rc;
+  }
+  int grid = device_sm_count();
+  if (grid > p.total_tiles) grid = p.total_tiles;
+  return launch_tc_fwd(maps, p, grid, smem, stream);
+}
+
+}  // namespace
+
+void set_last_cuda_error(cudaError_t e) { g_last_error = cudaGetErrorString(e); }
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
+}  // namespace wp
+
+using namespace wp;
+
+extern "C" {
+
+int lora_linear_fwd(const wp_mat* X, const wp_mat* W, const wp_mat* bias,
+                    const wp_adapter* adapters, int32_t n_adapters, double request_scale,
+                    const wp_out* Y, void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_impl(X, W, bias, 1, false, adapters, n_adapters, request_scale, Y, workspace,
+                  workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int lora_linear_fwd_grouped(const wp_mat* X, const wp_mat* W_stacked, const wp_mat* bias,
+                            int32_t n_groups, const wp_adapter* adapters, double request_scale,
+                            const wp_out* Y, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (!W_stacked) return WP_ERR_INVALID;
+  return fwd_impl(X, W_stacked, bias, n_groups, true, adapters, n_groups, request_scale, Y,
+                  workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int lora_linear_bwd(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int32_t n_groups,
+                    const wp_adapter* adapters, double request_scale, const wp_out* dX,
+                    const wp_out* dA, const wp_out* dB, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  (void)X; (void)W; (void)dY; (void)n_groups; (void)adapters; (void)request_scale; (void)dX;
+  (void)dA; (void)dB; (void)workspace; (void)workspace_bytes; (void)stream;
+  return WP_ERR_UNSUPPORTED;
+}
+
+int lora_dense_patch(void* param, int32_t param_dtype, int64_t param_numel, const void* payload,
+                     int32_t payload_dtype, int64_t payload_numel, int32_t kind, double strength,
+                     void* stream) {
+  if (!param || !payload) return WP_ERR_INVALID;
+  if (kind != WP_PATCH_ADD && kind != WP_PATCH_SET) return WP_ERR_INVALID;
+  if (!std::isfinite(strength)) return WP_ERR_INVALID;
+  if ((param_dtype != WP_BF16 && param_dtype != WP_FP32) ||
+      (payload_dtype != WP_BF16 && payload_dtype != WP_FP32))
+    return WP_ERR_DTYPE;
+  if (param_numel < 0 || payload_numel != param_numel) return WP_ERR_SHAPE;
+  return launch_dense_patch(param, param_dtype, payload, payload_dtype, param_numel, kind,
+                            static_cast<float>(strength), static_cast<cudaStream_t>(stream));
+}
+
+size_t lora_workspace_size(int32_t op, const wp_mat* X, const wp_mat* W,
+                           const wp_adapter* adapters, int32_t n_adapters) {
+  if (!X || n_adapters < 0 || (n_adapters > 0 && !adapters)) return 0;
+  if (op == WP_OP_FWD || op == WP_OP_FWD_GROUPED) {
+    FwdPlan plan;
+    plan_fwd(X, W, adapters, n_adapters, &plan);
+    return fwd_workspace(X, plan);
+  }
+  return 0;
+}
+
+const char* lora_status_string(int status) {
+  switch (status) {
+    case WP_OK: return "ok";
+    case WP_ERR_INVALID: return "invalid argument";
+    case WP_ERR_SHAPE: return "shape mismatch";
+    case WP_ERR_DTYPE: return "unsupported dtype";
+    case WP_ERR_ALIGN: return "misaligned pointer or row pitch";
+    case WP_ERR_WORKSPACE: return "workspace missing or too small";
+    case WP_ERR_CUDA: return "CUDA error";
+    case WP_ERR_TIMEOUT: return "device wait timed out";
+    case WP_ERR_UNSUPPORTED: return "unsupported size or feature";
+    default: return "unknown status";
+  }
+}
+
+int lora_device_status(int32_t reset) {
+  const int tc = tc_fwd_status(reset);
+  return tc;
+}
+
+void lora_nf4_codebook(float out[16]) { nf4_codebook_host(out); }
+
+const char* lora_last_cuda_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,126 @@
+// wp_internal.h -- launch descriptors shared by the C-ABI front (wp_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/weight_patches.h"
+
+namespace wp {
+
+// ------------------------------------------------------------------ tensor-core path
+constexpr int kBM = 128;            // output rows per tile (TMEM lanes)
+constexpr int kBN = 256;            // output columns per tile (TMEM columns)
+constexpr int kBK = 64;             // K per pipeline stage (one 128-byte swizzle atom)
+constexpr int kMaxAd = 8;           // bf16 adapters per call (all groups)
+constexpr int kMaxAd32 = 4;         // fp32 adapters per call
+constexpr int kMaxGroups = 8;
+constexpr int kHCols = 256;         // TMEM columns reserved for X A^T (rank region)
+constexpr int kATileBytes = kBM * kBK * 2;      // 16 KiB
+constexpr int kBTileBytes = kBN * kBK * 2;      // 32 KiB
+constexpr int kStageBytes = kATileBytes + kBTileBytes;
+constexpr int kHChunkBytes = kBM * 64 * 2;      // one 64-rank chunk of s*X A^T in bf16
+constexpr int kTcThreads = 320;     // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kSmemLimit = 227 * 1024;
+
+struct TcAdapter {
+  int group;       // column group this adapter belongs to
+  int rank;        // r
+  int rpad16;      // r rounded up to 16 (MMA N for X A^T and K extent of the 2nd GEMM)
+  int chunk_off;   // first 64-column chunk of the group's rank region
+  int nchunks;     // ceil(r / 64)
+  float s;         // combined scale, fp32
+};
+
+struct TcAdapter32 {
+  int group;
+  int rank;
+  int h_off;             // column offset in the s * X A^T fp32 workspace matrix
+  int ldb;               // row pitch of B (elements)
+  const float* B;        // [out_g, r] fp32
+};
+
+struct TcParams {
+  int T, K, N;                 // tokens, in_features, total out_features
+  int out_g, G, nt_g;          // group width, groups, N-tiles per group
+  int m_tiles, total_tiles, k_blocks;
+  int has_base;
+  int n_ad;                    // bf16 adapters
+  int ad_begin[kMaxGroups + 1];
+  int hchunks;                 // max rank chunks in any group (shared-memory H buffers)
+  int stages;
+  TcAdapter ad[kMaxAd];
+  int n_ad32;                  // fp32 adapters (epilogue FFMA)
+  TcAdapter32 ad32[kMaxAd32];
+  const float* h32;            // [T, h32_cols] fp32: s * X A^T of the fp32 adapters
+  int h32_cols;
+  const void* bias;            // [N] or null
+  int bias_f32;
+  void* Y;
+  long long ldy;
+  int y_f32;
+  unsigned long long timeout_ns;
+};
+
+struct TcMaps {
+  CUtensorMap x;
+  CUtensorMap w;
+  CUtensorMap a[kMaxAd];
+  CUtensorMap b[kMaxAd];
+};
+
+int launch_tc_fwd(const TcMaps& maps, const TcParams& p, int grid, size_t smem_bytes,
+                  cudaStream_t stream);
+int tc_fwd_status(int reset);
+
+// ------------------------------------------------------------------ fp32 CUDA-core path
+struct F32Adapter {
+  const void* A; int a_dtype; long long lda;   // [r, in]
+  const void* B; int b_dtype; long long ldb;   // [out, r]
+  int rank;
+  float s;
+};
+
+struct F32Params {
+  int T, K, N;
+  const void* X; int x_dtype; long long ldx;
+  const void* W; int w_dtype; long long ldw;   // may be null
+  const void* bias; int bias_dtype;            // may be null
+  void* Y; int y_dtype; long long ldy;
+  int n_ad;
+  F32Adapter ad[kMaxAd + kMaxAd32];
+  int col_begin[kMaxAd + kMaxAd32];            // output column window of each adapter
+  int col_end[kMaxAd + kMaxAd32];
+};
+
+// H: [T, h_cols] fp32 = s * X A^T of the adapters, in adapter order (rank_proj_kernel).
+int launch_f32_linear(const F32Params& p, const float* H, int h_cols, cudaStream_t stream);
+
+// s * X A^T of a list of adapters, written to an fp32 [T, h_cols] workspace matrix.
+struct H32Params {
+  int T, K;
+  const void* X; int x_dtype; long long ldx;
+  int n_ad;
+  const void* A[kMaxAd + kMaxAd32]; long long lda[kMaxAd + kMaxAd32];
+  int a_dtype[kMaxAd + kMaxAd32];
+  int rank[kMaxAd + kMaxAd32], h_off[kMaxAd + kMaxAd32];
+  float s[kMaxAd + kMaxAd32];
+  float* H; int h_cols;
+};
+int launch_h32(const H32Params& p, cudaStream_t stream);
+
+// ------------------------------------------------------------------ dense patch
+int launch_dense_patch(void* param, int param_dtype, const void* payload, int payload_dtype,
+                       long long n, int kind, float k, cudaStream_t stream);
+
+// ------------------------------------------------------------------ NF4 table (host)
+void nf4_codebook_host(float out[16]);
+
+// ------------------------------------------------------------------ misc
+void set_last_cuda_error(cudaError_t e);
+int device_sm_count();
+
+}  // namespace wp
