@@ -197,7 +197,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   p.T = static_cast<int>(T); p.K = static_cast<int>(K); p.N = static_cast<int>(N);
   p.out_g = static_cast<int>(out_g); p.G = G;
   p.nt_g = static_cast<int>((out_g + kBN - 1) / kBN);
-  p.m_tiles = static_cast<int>((T + kBM - 1) / kBM);
+  p.m_tiles = static_cast<int>((T + kPairM - 1) / kPairM);
   const long long total = static_cast<long long>(p.m_tiles) * G * p.nt_g;
   if (total > 0x7FFFFFFFLL) return WP_ERR_UNSUPPORTED;
   p.total_tiles = static_cast<int>(total);
@@ -215,6 +215,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   for (int g = 0; g < G; ++g) {
     p.ad_begin[g] = p.n_ad;
     int chunk = 0;
+    int roff = 0;
     for (int i = 0; i < n_adapters; ++i) {
       const int ag = grouped ? i : 0;
       if (ag != g || s_of[i] == 0.0f) continue;
@@ -238,12 +239,15 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
       TcAdapter& d = p.ad[p.n_ad];
       d.group = g; d.rank = r; d.rpad16 = (r + 15) / 16 * 16; d.chunk_off = chunk;
       d.nchunks = (r + 63) / 64; d.s = s_of[i];
+      d.roff = roff;
       chunk += d.nchunks;
+      roff += d.rpad16 / 2;
       if (chunk * 64 > kHCols) return WP_ERR_UNSUPPORTED;
       src_of[p.n_ad] = i;
       ++p.n_ad;
     }
     if (chunk > p.hchunks) p.hchunks = chunk;
+    if (roff > p.rslot_rows) p.rslot_rows = roff;
   }
   p.ad_begin[G] = p.n_ad;
   p.h32 = static_cast<const float*>(workspace);
@@ -251,34 +255,38 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   hp.H = static_cast<float*>(workspace); hp.h_cols = h_off;
 
   // Tensor maps (driver calls from here on).
+  // Each CTA of a pair loads 128 rows of X, 128 rows of the weight tile, half of an
+  // adapter's A rows and 128 rows of its B tile.
   int rc = make_map_bf16(&maps.x, X->data, K, T, X->ld, kBK, kBM);
   if (rc != WP_OK) return rc;
   if (W) {
-    rc = make_map_bf16(&maps.w, W->data, K, N, W->ld, kBK, kBN);
+    rc = make_map_bf16(&maps.w, W->data, K, N, W->ld, kBK, 128);
     if (rc != WP_OK) return rc;
   }
   for (int k = 0; k < p.n_ad; ++k) {
     const wp_adapter& a = adapters[src_of[k]];
-    rc = make_map_bf16(&maps.a[k], a.A.data, K, p.ad[k].rank, a.A.ld, kBK, p.ad[k].rpad16);
+    rc = make_map_bf16(&maps.a[k], a.A.data, K, p.ad[k].rank, a.A.ld, kBK, p.ad[k].rpad16 / 2);
     if (rc != WP_OK) return rc;
-    rc = make_map_bf16(&maps.b[k], a.B.data, p.ad[k].rank, out_g, a.B.ld, 64, kBN);
+    rc = make_map_bf16(&maps.b[k], a.B.data, p.ad[k].rank, out_g, a.B.ld, 64, 128);
     if (rc != WP_OK) return rc;
   }
 
+  p.stage_bytes = kATileBytes + kBHalfBytes + p.rslot_rows * 128;
   const size_t fixed = 1024 + static_cast<size_t>(p.hchunks) * kHChunkBytes + 256;
-  int stages = static_cast<int>((kSmemLimit - fixed) / kStageBytes);
-  if (stages > 4) stages = 4;
+  int stages = static_cast<int>((kSmemLimit - fixed) / p.stage_bytes);
+  if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return WP_ERR_UNSUPPORTED;
   p.stages = stages;
-  const size_t smem = fixed + static_cast<size_t>(stages) * kStageBytes;
+  const size_t smem = fixed + static_cast<size_t>(stages) * p.stage_bytes;
 
   if (hp.n_ad > 0) {
     rc = launch_h32(hp, stream);
     if (rc != WP_OK) return rc;
   }
-  int grid = device_sm_count();
-  if (grid > p.total_tiles) grid = p.total_tiles;
-  return launch_tc_fwd(maps, p, grid, smem, stream);
+  int pairs = tc_max_pairs(smem);
+  if (pairs <= 0) return WP_ERR_CUDA;
+  if (pairs > p.total_tiles) pairs = p.total_tiles;
+  return launch_tc_fwd(maps, p, 2 * pairs, smem, stream);
 }
 
 }  // namespace

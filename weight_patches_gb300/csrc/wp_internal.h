@@ -12,26 +12,30 @@
 namespace wp {
 
 // ------------------------------------------------------------------ tensor-core path
-constexpr int kBM = 128;            // output rows per tile (TMEM lanes)
-constexpr int kBN = 256;            // output columns per tile (TMEM columns)
+// A CTA pair (cluster of 2) computes a 256 x 256 output tile: each CTA owns 128 token
+// rows (its TMEM lanes) and holds half of the weight tile's 256 rows as MMA operand.
+constexpr int kBM = 128;            // token rows per CTA (TMEM lanes)
+constexpr int kPairM = 256;         // token rows per CTA pair
+constexpr int kBN = 256;            // output columns per tile (TMEM columns per buffer)
 constexpr int kBK = 64;             // K per pipeline stage (one 128-byte swizzle atom)
 constexpr int kMaxAd = 8;           // bf16 adapters per call (all groups)
 constexpr int kMaxAd32 = 4;         // fp32 adapters per call
 constexpr int kMaxGroups = 8;
-constexpr int kHCols = 256;         // TMEM columns reserved for X A^T (rank region)
-constexpr int kATileBytes = kBM * kBK * 2;      // 16 KiB
-constexpr int kBTileBytes = kBN * kBK * 2;      // 32 KiB
-constexpr int kStageBytes = kATileBytes + kBTileBytes;
+constexpr int kHCols = 256;         // TMEM columns available for X A^T (one buffer)
+constexpr int kATileBytes = kBM * kBK * 2;      // 16 KiB: this CTA's X rows
+constexpr int kBHalfBytes = 128 * kBK * 2;      // 16 KiB: this CTA's half of a B tile
 constexpr int kHChunkBytes = kBM * 64 * 2;      // one 64-rank chunk of s*X A^T in bf16
-constexpr int kTcThreads = 320;     // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kTcThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 227 * 1024;
 
 struct TcAdapter {
   int group;       // column group this adapter belongs to
   int rank;        // r
   int rpad16;      // r rounded up to 16 (MMA N for X A^T and K extent of the 2nd GEMM)
-  int chunk_off;   // first 64-column chunk of the group's rank region
+  int chunk_off;   // first 64-rank chunk of the group's rank region (TMEM col / 64, H~ buffer)
   int nchunks;     // ceil(r / 64)
+  int roff;        // row offset of this CTA's rpad16/2 rows of A in a stage's rank slot
   float s;         // combined scale, fp32
 };
 
@@ -46,12 +50,14 @@ struct TcAdapter32 {
 struct TcParams {
   int T, K, N;                 // tokens, in_features, total out_features
   int out_g, G, nt_g;          // group width, groups, N-tiles per group
-  int m_tiles, total_tiles, k_blocks;
+  int m_tiles, total_tiles, k_blocks;   // m_tiles counts 256-row pair blocks
   int has_base;
   int n_ad;                    // bf16 adapters
   int ad_begin[kMaxGroups + 1];
-  int hchunks;                 // max rank chunks in any group (shared-memory H buffers)
+  int hchunks;                 // max rank chunks in any group (shared-memory H~ buffers)
+  int rslot_rows;              // rows of the per-stage rank slot (A rows, per CTA)
   int stages;
+  int stage_bytes;             // 32 KiB + rslot_rows * 128
   TcAdapter ad[kMaxAd];
   int n_ad32;                  // fp32 adapters (epilogue FFMA)
   TcAdapter32 ad32[kMaxAd32];
@@ -72,6 +78,8 @@ struct TcMaps {
   CUtensorMap b[kMaxAd];
 };
 
+// Number of CTA pairs that can be resident at once for this shared-memory size.
+int tc_max_pairs(size_t smem_bytes);
 int launch_tc_fwd(const TcMaps& maps, const TcParams& p, int grid, size_t smem_bytes,
                   cudaStream_t stream);
 int tc_fwd_status(int reset);

@@ -9,27 +9,27 @@
 // (gate/up) adapters take one update per column group, and an FP32 adapter keeps its
 // FP32 GEMMs and is added once.  Here all of it happens inside one persistent kernel:
 //
-//   * tiles are 128 (tokens) x 256 (output columns); each CTA owns a contiguous range
-//     of tiles ordered (row block, group, column tile), so consecutive tiles share
-//     their X row block and their group's adapters;
-//   * when a CTA enters a new (row block, group) "unit" it first runs a rank pass: a
-//     K-loop over the X row block against A_p (N = r_p) that leaves H_p = X A_p^T in
-//     tensor memory; the epilogue warps scale it by the runtime s_p, round it once to
-//     bf16 and park it in shared memory in the MMA operand layout;
-//   * every tile then runs its base K-loop (X W^T into a 128x256 fp32 accumulator in
-//     tensor memory) followed by the second contraction H~ B_tile^T into the same
-//     accumulator, so the low-rank update costs K = r extra MMA steps per tile and the
-//     rank pass costs r / (tiles per unit * 256) of the base work;
-//   * the epilogue (8 warps) drains the accumulator to registers, frees tensor memory
-//     for the next tile, adds the bias and the FP32 adapters' terms
-//     (sum_j (s X A32^T)[t, j] * B32[o, j] with FFMA, before the single rounding),
-//     and writes bf16 or fp32.
+//   * a CTA pair (cluster of 2) computes 256 x 256 output tiles with tcgen05.mma
+//     cta_group::2: each CTA stages its own 128 X rows and half of the weight tile, so
+//     every SM receives 32 KiB of operands per 64-deep K step;
+//   * each pair owns a contiguous range of tiles ordered (row block, group, column
+//     tile); consecutive tiles share their X rows and their group's adapters, a "unit";
+//   * in the first tile of a unit the K loop also runs X A_p^T (N = r_p) on the same X
+//     stage, into the idle tensor-memory accumulator buffer; the epilogue warps scale
+//     it by the runtime s_p, round it once to bf16 and park it in shared memory in the
+//     MMA operand layout (H~);
+//   * every tile then adds H~ B_tile^T (K = r) into its own accumulator, so the
+//     [T, out] delta never leaves tensor memory;
+//   * two accumulator buffers (2 x 256 TMEM columns) let the epilogue of tile n overlap
+//     the MMAs of tile n+1; the epilogue adds the bias and the FP32 adapters' terms
+//     (sum_j (s X A32^T)[t, j] B32[o, j], FFMA, before the single rounding) and writes
+//     bf16 or fp32 rows.
 //
-// Warp roles: warp 0 issues TMA loads, warp 1 issues tcgen05.mma (one thread each),
-// warps 2..9 are the epilogue.  Operands are K-major bf16 in the 128-byte swizzle
-// layout, one 64-element K slice per pipeline stage.  Every mbarrier wait is bounded
-// (wall clock); on expiry the CTA records WP_ERR_TIMEOUT, waits for its own copies in
-// flight, frees tensor memory and returns.
+// Warp roles per CTA: warp 0 issues TMA loads (both CTAs), warp 1 allocates tensor
+// memory (both CTAs) and issues the pair MMAs (leader CTA only), warps 2..5 are the
+// epilogue (one token row per thread).  Operands are K-major bf16 in the 128-byte
+// swizzle layout.  Every mbarrier wait is bounded (wall clock); on expiry the CTA records
+// WP_ERR_TIMEOUT, waits for its own copies in flight, frees tensor memory and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -57,8 +57,9 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, int L) {
 
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
-
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(uint32_t(h) << 16); }
+
+constexpr uint16_t kBothCtas = 0x3;
 
 }  // namespace
 
@@ -70,28 +71,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* sbase = smem_raw + (base_addr - raw_addr);
 
   const int S = p.stages;
-  uint8_t* hbuf = sbase + S * kStageBytes;
+  const int SB = p.stage_bytes;
+  uint8_t* hbuf = sbase + S * SB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(hbuf + p.hchunks * kHChunkBytes);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + S;
-  uint64_t* acc_full = bars + 2 * S;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* h_full = acc_full + 2;
-  uint64_t* h_ready = acc_full + 3;
-  uint64_t* drain = acc_full + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 5);
+  uint64_t* full = bars;                  // [S]  leader: TMA bytes of both CTAs landed
+  uint64_t* empty = bars + S;             // [S]  both: the pair MMAs consumed the stage
+  uint64_t* acc_full = bars + 2 * S;      // [2]  both: accumulator buffer ready
+  uint64_t* acc_empty = acc_full + 2;     // [2]  leader: both epilogues drained it
+  uint64_t* h_full = acc_full + 4;        //      both: X A^T of the unit is in TMEM
+  uint64_t* h_ready = acc_full + 5;       //      leader: both CTAs wrote their H~ rows
+  uint64_t* drain = acc_full + 6;         //      leader: every MMA issued has finished
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 7);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t cta = cluster_ctarank();
+  const bool leader = cta == 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 8);
+    mbar_init(&acc_full[0], 1);
+    mbar_init(&acc_full[1], 1);
+    mbar_init(&acc_empty[0], 8);          // 4 epilogue warps x 2 CTAs
+    mbar_init(&acc_empty[1], 8);
     mbar_init(h_full, 1);
     mbar_init(h_ready, 8);
     mbar_init(drain, 1);
@@ -103,319 +109,368 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (p.has_base) tma_prefetch_desc(&maps.w);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();                          // peer barriers initialised before remote use
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_acc = tmem;             // columns [0, 256)
-  const uint32_t tmem_h = tmem + kBN;         // columns [256, 512)
 
   const long long total = p.total_tiles;
-  const int t_begin = static_cast<int>(blockIdx.x * total / gridDim.x);
-  const int t_end = static_cast<int>((blockIdx.x + 1) * total / gridDim.x);
+  const long long npairs = gridDim.x >> 1;
+  const long long pair = blockIdx.x >> 1;
+  const int t_begin = static_cast<int>(pair * total / npairs);
+  const int t_end = static_cast<int>((pair + 1) * total / npairs);
   const uint64_t tmo = p.timeout_ns;
   int* status = &g_tc_status;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int issued[16];
-      for (int s = 0; s < S; ++s) issued[s] = 0;
+      int issued[kMaxStages];
+      for (int s = 0; s < kMaxStages; ++s) issued[s] = 0;
       bool ok = true;
       for (int L = t_begin; L < t_end && ok; ++L) {
         const Tile t = decode_tile(p, L);
         const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
         const bool lora = a1 > a0;
-        const bool new_unit = (L == t_begin) || (t.j == 0);
-        const int m0 = t.m * kBM;
-        if (lora && new_unit) {
-          uint32_t bytes = kATileBytes;
-          for (int a = a0; a < a1; ++a) bytes += p.ad[a].rpad16 * 128;
+        const bool first = lora && ((L == t_begin) || (t.j == 0));
+        const int x_row = t.m * kPairM + static_cast<int>(cta) * kBM;
+        if (p.has_base || first) {
+          uint32_t tx = (p.has_base ? 4u : 2u) * kATileBytes;     // both CTAs
+          if (first)
+            for (int a = a0; a < a1; ++a) tx += p.ad[a].rpad16 * 128;
+          const int w_row = t.g * p.out_g + t.j * kBN + static_cast<int>(cta) * 128;
           for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!(ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, tmo, status))) break;
-            uint8_t* st = sbase + stage * kStageBytes;
-            mbar_arrive_expect_tx(&full[stage], bytes);
-            tma_load_2d(st, &maps.x, kb * kBK, m0, &full[stage]);
-            for (int a = a0; a < a1; ++a)
-              tma_load_2d(st + kATileBytes + p.ad[a].chunk_off * 64 * 128, &maps.a[a], kb * kBK, 0,
-                          &full[stage]);
-            ++issued[stage];
-            if (++stage == S) { stage = 0; phase ^= 1; }
-          }
-        }
-        if (ok && p.has_base) {
-          const int n_row0 = t.g * p.out_g + t.j * kBN;
-          for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!(ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, tmo, status))) break;
-            uint8_t* st = sbase + stage * kStageBytes;
-            mbar_arrive_expect_tx(&full[stage], kStageBytes);
-            tma_load_2d(st, &maps.x, kb * kBK, m0, &full[stage]);
-            tma_load_2d(st + kATileBytes, &maps.w, kb * kBK, n_row0, &full[stage]);
+            if (!(ok = mbar_wait_cluster(&empty[stage], phase ^ 1, abort_flag, tmo, status))) break;
+            uint8_t* st = sbase + stage * SB;
+            const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+            if (leader) mbar_arrive_expect_tx(&full[stage], tx);
+            tma_load_2d_pair(st, &maps.x, kb * kBK, x_row, fb);
+            if (p.has_base) tma_load_2d_pair(st + kATileBytes, &maps.w, kb * kBK, w_row, fb);
+            if (first)
+              for (int a = a0; a < a1; ++a)
+                tma_load_2d_pair(st + 2 * kATileBytes + p.ad[a].roff * 128, &maps.a[a], kb * kBK,
+                                 static_cast<int>(cta) * (p.ad[a].rpad16 >> 1), fb);
             ++issued[stage];
             if (++stage == S) { stage = 0; phase ^= 1; }
           }
         }
         if (ok && lora) {
+          const int b_row = t.j * kBN + static_cast<int>(cta) * 128;
           for (int a = a0; a < a1 && ok; ++a) {
             for (int c = 0; c < p.ad[a].nchunks; ++c) {
-              if (!(ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, tmo, status))) break;
-              uint8_t* st = sbase + stage * kStageBytes;
-              mbar_arrive_expect_tx(&full[stage], kBTileBytes);
-              tma_load_2d(st + kATileBytes, &maps.b[a], c * 64, t.j * kBN, &full[stage]);
+              if (!(ok = mbar_wait_cluster(&empty[stage], phase ^ 1, abort_flag, tmo, status))) break;
+              uint8_t* st = sbase + stage * SB;
+              const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+              if (leader) mbar_arrive_expect_tx(&full[stage], 2u * kBHalfBytes);
+              tma_load_2d_pair(st + kATileBytes, &maps.b[a], c * 64, b_row, fb);
               ++issued[stage];
               if (++stage == S) { stage = 0; phase ^= 1; }
             }
           }
         }
       }
-      if (!ok) {
-        // Wait (bounded) for the copies this thread put in flight before the CTA exits.
+      if (!ok && leader) {
+        // Wait (bounded) for the copies put in flight before the CTA exits.
         for (int s = 0; s < S; ++s) {
           if (issued[s] == 0) continue;
           const uint32_t par = static_cast<uint32_t>((issued[s] - 1) & 1);
           const uint32_t a = smem_u32(&full[s]);
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(a, par) && globaltimer_ns() - t0 < 100000000ull) {
+          while (!mbar_try_wait_cluster(a, par) && globaltimer_ns() - t0 < 100000000ull) {
           }
         }
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t acc_phase = 0;
+      uint32_t nuse[2] = {0, 0};
+      int count = 0;
       uint32_t unit_phase = 0;
-      const uint32_t idesc_acc = idesc_bf16_f32(kBM, kBN);
+      const uint32_t idesc_acc = idesc_bf16_f32(kPairM, kBN);
       const uint32_t hbuf_addr = smem_u32(hbuf);
       bool ok = true;
       for (int L = t_begin; L < t_end && ok; ++L) {
         const Tile t = decode_tile(p, L);
         const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
         const bool lora = a1 > a0;
-        const bool new_unit = (L == t_begin) || (t.j == 0);
-        if (lora && new_unit) {
+        const bool first = lora && ((L == t_begin) || (t.j == 0));
+        if (!(p.has_base || lora)) continue;
+        const int b = count & 1;
+        if (!(ok = mbar_wait_cluster(&acc_empty[b], (nuse[b] & 1) ^ 1, abort_flag, tmo, status)))
+          break;
+        if (first &&
+            !(ok = mbar_wait_cluster(&acc_empty[b ^ 1], (nuse[b ^ 1] & 1) ^ 1, abort_flag, tmo, status)))
+          break;
+        tc_fence_after();
+        const uint32_t acc_t = tmem + b * kBN;
+        const uint32_t h_t = tmem + (b ^ 1) * kBN;
+        if (p.has_base || first) {
           for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
+            if (!(ok = mbar_wait_cluster(&full[stage], phase, abort_flag, tmo, status))) break;
             tc_fence_after();
-            const uint32_t st = smem_u32(sbase + stage * kStageBytes);
+            const uint32_t st = smem_u32(sbase + stage * SB);
             for (int kk = 0; kk < kBK / 16; ++kk) {
               const uint64_t adesc = sw128_kmajor_desc(st + kk * 32);
-              for (int a = a0; a < a1; ++a) {
-                const uint64_t bdesc =
-                    sw128_kmajor_desc(st + kATileBytes + p.ad[a].chunk_off * 64 * 128 + kk * 32);
-                mma_bf16(tmem_h + p.ad[a].chunk_off * 64, adesc, bdesc,
-                         idesc_bf16_f32(kBM, p.ad[a].rpad16), (kb | kk) != 0);
-              }
+              const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+              if (p.has_base)
+                mma_bf16_pair(acc_t, adesc, sw128_kmajor_desc(st + kATileBytes + kk * 32), idesc_acc,
+                              acc);
+              if (first)
+                for (int a = a0; a < a1; ++a)
+                  mma_bf16_pair(h_t + p.ad[a].chunk_off * 64, adesc,
+                                sw128_kmajor_desc(st + 2 * kATileBytes + p.ad[a].roff * 128 + kk * 32),
+                                idesc_bf16_f32(kPairM, p.ad[a].rpad16), acc);
             }
-            mma_commit(&empty[stage]);
-            if (++stage == S) { stage = 0; phase ^= 1; }
-          }
-          if (!ok) break;
-          mma_commit(h_full);
-        }
-        if (!(p.has_base || lora)) continue;
-        if (!(ok = mbar_wait(acc_empty, acc_phase ^ 1, abort_flag, tmo, status))) break;
-        tc_fence_after();
-        bool accum = false;
-        if (p.has_base) {
-          for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
-            tc_fence_after();
-            const uint32_t st = smem_u32(sbase + stage * kStageBytes);
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              mma_bf16(tmem_acc, sw128_kmajor_desc(st + kk * 32),
-                       sw128_kmajor_desc(st + kATileBytes + kk * 32), idesc_acc,
-                       (accum || kk > 0) ? 1u : 0u);
-            }
-            accum = true;
-            mma_commit(&empty[stage]);
+            mma_commit_pair_mc(&empty[stage], kBothCtas);
             if (++stage == S) { stage = 0; phase ^= 1; }
           }
           if (!ok) break;
         }
+        bool accum = p.has_base != 0;
         if (lora) {
-          if (new_unit) {
-            if (!(ok = mbar_wait(h_ready, unit_phase, abort_flag, tmo, status))) break;
+          if (first) {
+            mma_commit_pair_mc(h_full, kBothCtas);
+            if (!(ok = mbar_wait_cluster(h_ready, unit_phase, abort_flag, tmo, status))) break;
             tc_fence_after();
             unit_phase ^= 1;
           }
           for (int a = a0; a < a1 && ok; ++a) {
             for (int c = 0; c < p.ad[a].nchunks; ++c) {
-              if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
+              if (!(ok = mbar_wait_cluster(&full[stage], phase, abort_flag, tmo, status))) break;
               tc_fence_after();
-              const uint32_t st = smem_u32(sbase + stage * kStageBytes);
+              const uint32_t st = smem_u32(sbase + stage * SB);
               const int kext = min(64, p.ad[a].rpad16 - 64 * c);
               const uint32_t hchunk = hbuf_addr + (p.ad[a].chunk_off + c) * kHChunkBytes;
-              for (int kk = 0; kk < kext / 16; ++kk) {
-                mma_bf16(tmem_acc, sw128_kmajor_desc(hchunk + kk * 32),
-                         sw128_kmajor_desc(st + kATileBytes + kk * 32), idesc_acc,
-                         (accum || kk > 0) ? 1u : 0u);
-              }
+              for (int kk = 0; kk < kext / 16; ++kk)
+                mma_bf16_pair(acc_t, sw128_kmajor_desc(hchunk + kk * 32),
+                              sw128_kmajor_desc(st + kATileBytes + kk * 32), idesc_acc,
+                              (accum || kk > 0) ? 1u : 0u);
               accum = true;
-              mma_commit(&empty[stage]);
+              mma_commit_pair_mc(&empty[stage], kBothCtas);
               if (++stage == S) { stage = 0; phase ^= 1; }
             }
           }
           if (!ok) break;
         }
-        mma_commit(acc_full);
-        acc_phase ^= 1;
+        mma_commit_pair_mc(&acc_full[b], kBothCtas);
+        ++nuse[b];
+        ++count;
       }
-      // Make sure every MMA this thread issued has finished before TMEM is freed.
-      mma_commit(drain);
+      // Every MMA this thread issued must finish before tensor memory is freed.
+      mma_commit_pair_mc(drain, 0x1);
       const uint32_t a = smem_u32(drain);
       const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(a, 0) && globaltimer_ns() - t0 < 100000000ull) {
+      while (!mbar_try_wait_cluster(a, 0) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue (8 warps)
-    const int e = warp - 2;
+    // ------------------------------------------------------------ epilogue (4 warps)
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int half = e >> 2;                // which 128 of the 256 tile columns
-    const int row_in_tile = q * 32 + lane;
+    const int row_in_cta = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t hbuf_addr = smem_u32(hbuf);
-    uint32_t acc_phase = 0;
+    const uint32_t acc_empty_l[2] = {mapa_shared(smem_u32(&acc_empty[0]), 0),
+                                     mapa_shared(smem_u32(&acc_empty[1]), 0)};
+    const uint32_t h_ready_l = mapa_shared(smem_u32(h_ready), 0);
+    uint32_t nuse[2] = {0, 0};
+    int count = 0;
     uint32_t unit_phase = 0;
     for (int L = t_begin; L < t_end; ++L) {
       const Tile t = decode_tile(p, L);
       const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
       const bool lora = a1 > a0;
-      const bool new_unit = (L == t_begin) || (t.j == 0);
-      if (lora && new_unit) {
+      const bool first = lora && ((L == t_begin) || (t.j == 0));
+      const bool any_mma = p.has_base || lora;
+      const int b = count & 1;
+      if (first) {
         // every lane waits; the warp proceeds only if all lanes saw the phase, so the
         // .sync.aligned TMEM loads below are always executed by the whole warp
-        if (!__all_sync(0xffffffffu, mbar_wait(h_full, unit_phase, abort_flag, tmo, status))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait_cluster(h_full, unit_phase, abort_flag, tmo, status)))
+          break;
         tc_fence_after();
         unit_phase ^= 1;
+        const uint32_t h_t = tmem + (b ^ 1) * kBN;
         for (int a = a0; a < a1; ++a) {
           const float s = p.ad[a].s;
           const int units = p.ad[a].rpad16 >> 3;
-          for (int u = half; u < units; u += 2) {
+          for (int u = 0; u < units; ++u) {
             uint32_t r[8];
-            tmem_ld8(tmem_h + lane_base + p.ad[a].chunk_off * 64 + u * 8, r);
+            tmem_ld8(h_t + lane_base + p.ad[a].chunk_off * 64 + u * 8, r);
             const uint32_t w0 = pack_bf16x2(u2f(r[0]) * s, u2f(r[1]) * s);
             const uint32_t w1 = pack_bf16x2(u2f(r[2]) * s, u2f(r[3]) * s);
             const uint32_t w2 = pack_bf16x2(u2f(r[4]) * s, u2f(r[5]) * s);
             const uint32_t w3 = pack_bf16x2(u2f(r[6]) * s, u2f(r[7]) * s);
             const int chunk = p.ad[a].chunk_off + (u >> 3);
-            const int unit16 = (u & 7) ^ (row_in_tile & 7);
-            st_shared_v4(hbuf_addr + chunk * kHChunkBytes + row_in_tile * 128 + unit16 * 16, w0,
-                         w1, w2, w3);
+            const int unit16 = (u & 7) ^ (row_in_cta & 7);
+            st_shared_v4(hbuf_addr + chunk * kHChunkBytes + row_in_cta * 128 + unit16 * 16, w0, w1,
+                         w2, w3);
           }
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(h_ready);
+        if (lane == 0) mbar_arrive_cluster(h_ready_l);
       }
-
-      float acc[128];
-      const bool any_mma = p.has_base || lora;
       if (any_mma) {
-        if (!__all_sync(0xffffffffu, mbar_wait(acc_full, acc_phase, abort_flag, tmo, status))) break;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_cluster(&acc_full[b], nuse[b] & 1, abort_flag, tmo, status)))
+          break;
         tc_fence_after();
-        acc_phase ^= 1;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
+      }
+
+      const int row = t.m * kPairM + static_cast<int>(cta) * kBM + row_in_cta;
+      const bool row_ok = row < p.T;
+      const uint32_t acc_t = tmem + b * kBN;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        const int cig = t.j * kBN + c * 32;                 // first column, within the group
+        const int ncols = min(32, p.out_g - cig);           // uniform across the warp
+        if (ncols <= 0) break;
+        const int gcol = t.g * p.out_g + cig;
+        float v[32];
+        if (any_mma) {
           uint32_t r[32];
-          tmem_ld32(tmem_acc + lane_base + half * 128 + c * 32, r);
+          tmem_ld32(acc_t + lane_base + c * 32, r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[c * 32 + i] = u2f(r[i]);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(acc_empty);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 128; ++i) acc[i] = 0.f;
-      }
-
-      const int row = t.m * kBM + row_in_tile;
-      const int col_in_group0 = t.j * kBN + half * 128;     // first column of this thread
-      const int gcol0 = t.g * p.out_g + col_in_group0;      // same, in Y
-      const int ncols = min(128, p.out_g - col_in_group0);  // valid columns (may be <= 0)
-      if (ncols <= 0) continue;
-
-      if (p.bias) {
-        if (p.bias_f32) {
-          const float* b = static_cast<const float*>(p.bias) + gcol0;
-#pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (i < ncols) acc[i] += b[i];
+          for (int i = 0; i < 32; ++i) v[i] = u2f(r[i]);
         } else {
-          const uint16_t* b = static_cast<const uint16_t*>(p.bias) + gcol0;
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (i < ncols) acc[i] += bf16_to_f32(b[i]);
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
-      }
-
-      if (p.n_ad32 > 0 && row < p.T) {
-        for (int a = 0; a < p.n_ad32; ++a) {
-          if (p.ad32[a].group != t.g) continue;
-          const float* hrow = p.h32 + static_cast<long long>(row) * p.h32_cols + p.ad32[a].h_off;
-          const int r = p.ad32[a].rank;
-          const float* Bm = p.ad32[a].B;
-          const long long ldb = p.ad32[a].ldb;
-          for (int jj = 0; jj < r; ++jj) {
-            const float h = hrow[jj];
+        if (p.bias) {
+          if (p.bias_f32) {
+            const float* bp = static_cast<const float*>(p.bias) + gcol;
 #pragma unroll
-            for (int i = 0; i < 128; ++i)
-              if (i < ncols) acc[i] = fmaf(h, Bm[static_cast<long long>(col_in_group0 + i) * ldb + jj], acc[i]);
+            for (int i = 0; i < 32; ++i)
+              if (i < ncols) v[i] += bp[i];
+          } else {
+            const uint16_t* bp = static_cast<const uint16_t*>(p.bias) + gcol;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < ncols) v[i] += bf16_to_f32(bp[i]);
+          }
+        }
+        if (p.n_ad32 > 0 && row_ok) {
+          for (int a = 0; a < p.n_ad32; ++a) {
+            if (p.ad32[a].group != t.g) continue;
+            const float* hrow = p.h32 + static_cast<long long>(row) * p.h32_cols + p.ad32[a].h_off;
+            const float* Bm = p.ad32[a].B + static_cast<long long>(cig) * p.ad32[a].ldb;
+            const long long ldb = p.ad32[a].ldb;
+            for (int jj = 0; jj < p.ad32[a].rank; ++jj) {
+              const float h = hrow[jj];
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < ncols) v[i] = fmaf(h, Bm[i * ldb + jj], v[i]);
+            }
+          }
+        }
+        if (row_ok) {
+          if (p.y_f32) {
+            float* y = static_cast<float*>(p.Y) + static_cast<long long>(row) * p.ldy + gcol;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (i * 4 < ncols)
+                st_global_v4(y + i * 4, f2u(v[4 * i]), f2u(v[4 * i + 1]), f2u(v[4 * i + 2]),
+                             f2u(v[4 * i + 3]));
+          } else {
+            uint16_t* y = static_cast<uint16_t*>(p.Y) + static_cast<long long>(row) * p.ldy + gcol;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (i * 8 < ncols)
+                st_global_v4(y + i * 8, pack_bf16x2(v[8 * i], v[8 * i + 1]),
+                             pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                             pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                             pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
           }
         }
       }
-
-      if (row < p.T) {
-        if (p.y_f32) {
-          float* yrow = static_cast<float*>(p.Y) + static_cast<long long>(row) * p.ldy + gcol0;
-#pragma unroll
-          for (int v = 0; v < 32; ++v)
-            if (v * 4 < ncols)
-              st_global_v4(yrow + v * 4, f2u(acc[4 * v]), f2u(acc[4 * v + 1]), f2u(acc[4 * v + 2]),
-                           f2u(acc[4 * v + 3]));
-        } else {
-          uint16_t* yrow = static_cast<uint16_t*>(p.Y) + static_cast<long long>(row) * p.ldy + gcol0;
-#pragma unroll
-          for (int v = 0; v < 16; ++v)
-            if (v * 8 < ncols)
-              st_global_v4(yrow + v * 8, pack_bf16x2(acc[8 * v], acc[8 * v + 1]),
-                           pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]),
-                           pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]),
-                           pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]));
-        }
+      if (any_mma) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_l[b]);
+        ++nuse[b];
+        ++count;
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();                          // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc_pair(tmem, 512);
   }
+}
+
+namespace {
+
+cudaLaunchConfig_t pair_config(int grid, size_t smem_bytes, cudaStream_t stream,
+                               cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+}  // namespace
+
+int tc_max_pairs(size_t smem_bytes) {
+  static size_t cached_smem = 0;
+  static int cached = 0;
+  static int cached_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (cached_smem == smem_bytes && cached_dev == dev && cached > 0) return cached;
+  cudaError_t e = cudaFuncSetAttribute(tc_fused_fwd_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    return 0;
+  }
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config(2 * 256, smem_bytes, nullptr, attr);
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, tc_fused_fwd_kernel, &cfg);
+  if (e != cudaSuccess || n <= 0) {
+    if (e != cudaSuccess) set_last_cuda_error(e);
+    n = device_sm_count() / 2;
+  }
+  cached_smem = smem_bytes;
+  cached = n;
+  cached_dev = dev;
+  return n;
 }
 
 int launch_tc_fwd(const TcMaps& maps, const TcParams& p, int grid, size_t smem_bytes,
                   cudaStream_t stream) {
-  cudaError_t ea = cudaFuncSetAttribute(tc_fused_fwd_kernel,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-  if (ea != cudaSuccess) {
-    set_last_cuda_error(ea);
+  cudaError_t e = cudaFuncSetAttribute(tc_fused_fwd_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
     return WP_ERR_CUDA;
   }
-  tc_fused_fwd_kernel<<<grid, kTcThreads, smem_bytes, stream>>>(maps, p);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config(grid, smem_bytes, stream, attr);
+  e = cudaLaunchKernelEx(&cfg, tc_fused_fwd_kernel, maps, p);
   if (e != cudaSuccess) {
     set_last_cuda_error(e);
     return WP_ERR_CUDA;
