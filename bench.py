@@ -51,6 +51,24 @@ def measured_peaks():
     return 1900.0, 6800.0, "fallback"
 
 
+def captured_traffic():
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary, or None
+    when the kernel source changed since that capture."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "tc_fused_fwd_c1_wan_qkv.md")
+    src = os.path.join(ROOT, "weight_patches_gb300", "csrc", "wp_tc_fwd.cu")
+    try:
+        text = open(prof).read()
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    vals = dict(line.strip().split(": ", 1) for line in text.splitlines()
+                if line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_sha256_16")))
+    if vals.get("kernel_source_sha256_16") != h:
+        return None
+    return int(vals["traffic_bytes_per_launch"])
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -209,7 +227,7 @@ def run_fused(args):
                    "l2": "inputs larger than L2 (X 101 MB + W 14 MB + Y 302 MB per step > 129 MB)",
                    "parallelism": f"replicas x{ws} (token-local, no collective)"},
         "roofline": {"bound": "tensor", "achieved": round(per_launch_tflops, 2), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(per_launch_tflops / peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(per_launch_tflops / peak, 4), "traffic": captured_traffic(),
                      "peak_source": f"{peak_kind} bf16 burst"},
         "overhead": {"vs_cublas_base_gemm": round(ms_step / base_ms - 1.0, 4),
                      "vs_own_base_kernel": round(ms_step / own_base_ms - 1.0, 4),

@@ -37,19 +37,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 2-D bf16 tensor map over a row-major [outer, inner] matrix with row pitch ld
 // (elements), 128-byte swizzled boxes of {box_inner, box_outer}; out-of-range
 // elements read as zero.
-int make_map_bf16(CUtensorMap* m, const void* ptr, long long inner, long long outer, long long ld,
-                  int box_inner, int box_outer) {
+int make_map(CUtensorMap* m, int dtype, const void* ptr, long long inner, long long outer,
+             long long ld, int box_inner, int box_outer) {
   auto fn = encode_fn();
   if (!fn) {
     g_last_error = "cuTensorMapEncodeTiled unavailable";
     return WP_ERR_CUDA;
   }
+  const int esz = dtype == WP_FP32 ? 4 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esz};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(m, dtype == WP_FP32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char buf[96];
@@ -58,6 +60,11 @@ int make_map_bf16(CUtensorMap* m, const void* ptr, long long inner, long long ou
     return WP_ERR_CUDA;
   }
   return WP_OK;
+}
+
+int make_map_bf16(CUtensorMap* m, const void* ptr, long long inner, long long outer, long long ld,
+                  int box_inner, int box_outer) {
+  return make_map(m, WP_BF16, ptr, inner, outer, ld, box_inner, box_outer);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -80,6 +87,14 @@ bool valid_output(const wp_out* y) {
 }
 
 size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+// Tiles per scheduling chunk.  Pairs take chunks round-robin; one chunk per pair
+// (contiguous ranges) balances best and starts the fewest X A^T units, while smaller
+// chunks keep the pairs on nearby rows of X.  Contiguous ranges are the default.
+int chunk_tiles_for(int total, int pairs, int nt_g) {
+  (void)nt_g;
+  return (total + pairs - 1) / pairs;
+}
 
 struct FwdPlan {
   bool tc = false;        // tensor-core path
@@ -263,6 +278,8 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     rc = make_map_bf16(&maps.w, W->data, K, N, W->ld, kBK, 128);
     if (rc != WP_OK) return rc;
   }
+  rc = make_map(&maps.y, Y->dtype, Y->data, N, T, Y->ld, Y->dtype == WP_FP32 ? 32 : 64, kBM);
+  if (rc != WP_OK) return rc;
   for (int k = 0; k < p.n_ad; ++k) {
     const wp_adapter& a = adapters[src_of[k]];
     rc = make_map_bf16(&maps.a[k], a.A.data, K, p.ad[k].rank, a.A.ld, kBK, p.ad[k].rpad16 / 2);
@@ -272,7 +289,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   }
 
   p.stage_bytes = kATileBytes + kBHalfBytes + p.rslot_rows * 128;
-  const size_t fixed = 1024 + static_cast<size_t>(p.hchunks) * kHChunkBytes + 256;
+  const size_t fixed = 1024 + static_cast<size_t>(p.hchunks) * kHChunkBytes + 2 * kStgBytes + 256;
   int stages = static_cast<int>((kSmemLimit - fixed) / p.stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return WP_ERR_UNSUPPORTED;
@@ -286,6 +303,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   int pairs = tc_max_pairs(smem);
   if (pairs <= 0) return WP_ERR_CUDA;
   if (pairs > p.total_tiles) pairs = p.total_tiles;
+  p.chunk_tiles = chunk_tiles_for(p.total_tiles, pairs, p.nt_g);
   return launch_tc_fwd(maps, p, 2 * pairs, smem, stream);
 }
 

@@ -7,7 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/weight_patches.h"
+#include "weight_patches.h"
 
 namespace wp {
 
@@ -25,6 +25,7 @@ constexpr int kHCols = 256;         // TMEM columns available for X A^T (one buf
 constexpr int kATileBytes = kBM * kBK * 2;      // 16 KiB: this CTA's X rows
 constexpr int kBHalfBytes = 128 * kBK * 2;      // 16 KiB: this CTA's half of a B tile
 constexpr int kHChunkBytes = kBM * 64 * 2;      // one 64-rank chunk of s*X A^T in bf16
+constexpr int kStgBytes = kBM * 128;            // output staging: 128 rows x 128 bytes
 constexpr int kTcThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 227 * 1024;
@@ -51,6 +52,7 @@ struct TcParams {
   int T, K, N;                 // tokens, in_features, total out_features
   int out_g, G, nt_g;          // group width, groups, N-tiles per group
   int m_tiles, total_tiles, k_blocks;   // m_tiles counts 256-row pair blocks
+  int chunk_tiles;             // pairs take chunks p, p + P, ... of this many tiles
   int has_base;
   int n_ad;                    // bf16 adapters
   int ad_begin[kMaxGroups + 1];
@@ -74,6 +76,7 @@ struct TcParams {
 struct TcMaps {
   CUtensorMap x;
   CUtensorMap w;
+  CUtensorMap y;                 // output, 128-byte swizzled boxes of 128 rows
   CUtensorMap a[kMaxAd];
   CUtensorMap b[kMaxAd];
 };

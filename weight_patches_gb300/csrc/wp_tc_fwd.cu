@@ -73,7 +73,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int S = p.stages;
   const int SB = p.stage_bytes;
   uint8_t* hbuf = sbase + S * SB;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(hbuf + p.hchunks * kHChunkBytes);
+  uint8_t* stg = hbuf + p.hchunks * kHChunkBytes;      // 2 output staging buffers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + 2 * kStgBytes);
   uint64_t* full = bars;                  // [S]  leader: TMA bytes of both CTAs landed
   uint64_t* empty = bars + S;             // [S]  both: the pair MMAs consumed the stage
   uint64_t* acc_full = bars + 2 * S;      // [2]  both: accumulator buffer ready
@@ -118,27 +119,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const long long total = p.total_tiles;
-  const long long npairs = gridDim.x >> 1;
-  const long long pair = blockIdx.x >> 1;
-  const int t_begin = static_cast<int>(pair * total / npairs);
-  const int t_end = static_cast<int>((pair + 1) * total / npairs);
+  // Pair `pair` takes chunks pair, pair + npairs, ... of `chunk_tiles` consecutive tiles
+  // in (row block, group, column tile) order: at any moment the pairs work on nearby
+  // row blocks (X stays in L2) while each chunk reuses its X A^T across its tiles.
+  const int npairs = static_cast<int>(gridDim.x >> 1);
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int CH = p.chunk_tiles;
+  const int nchunks = (p.total_tiles + CH - 1) / CH;
   const uint64_t tmo = p.timeout_ns;
   int* status = &g_tc_status;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
+      const uint64_t keep = l2_evict_last();   // weights and adapters: re-read by every row block
       int stage = 0;
       uint32_t phase = 0;
       int issued[kMaxStages];
       for (int s = 0; s < kMaxStages; ++s) issued[s] = 0;
       bool ok = true;
-      for (int L = t_begin; L < t_end && ok; ++L) {
+      for (int L = 0, chunk = pair, c_end = 0; ok; ++L) {
+        if (L >= c_end) {
+          if (chunk >= nchunks) break;
+          L = chunk * CH;
+          c_end = min(L + CH, p.total_tiles);
+          chunk += npairs;
+        }
         const Tile t = decode_tile(p, L);
         const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
         const bool lora = a1 > a0;
-        const bool first = lora && ((L == t_begin) || (t.j == 0));
+        const bool first = lora && ((L % CH == 0) || (t.j == 0));
         const int x_row = t.m * kPairM + static_cast<int>(cta) * kBM;
         if (p.has_base || first) {
           uint32_t tx = (p.has_base ? 4u : 2u) * kATileBytes;     // both CTAs
@@ -151,11 +161,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
             if (leader) mbar_arrive_expect_tx(&full[stage], tx);
             tma_load_2d_pair(st, &maps.x, kb * kBK, x_row, fb);
-            if (p.has_base) tma_load_2d_pair(st + kATileBytes, &maps.w, kb * kBK, w_row, fb);
+            if (p.has_base)
+              tma_load_2d_pair_hint(st + kATileBytes, &maps.w, kb * kBK, w_row, fb, keep);
             if (first)
               for (int a = a0; a < a1; ++a)
-                tma_load_2d_pair(st + 2 * kATileBytes + p.ad[a].roff * 128, &maps.a[a], kb * kBK,
-                                 static_cast<int>(cta) * (p.ad[a].rpad16 >> 1), fb);
+                tma_load_2d_pair_hint(st + 2 * kATileBytes + p.ad[a].roff * 128, &maps.a[a],
+                                      kb * kBK, static_cast<int>(cta) * (p.ad[a].rpad16 >> 1), fb,
+                                      keep);
             ++issued[stage];
             if (++stage == S) { stage = 0; phase ^= 1; }
           }
@@ -168,7 +180,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               uint8_t* st = sbase + stage * SB;
               const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
               if (leader) mbar_arrive_expect_tx(&full[stage], 2u * kBHalfBytes);
-              tma_load_2d_pair(st + kATileBytes, &maps.b[a], c * 64, b_row, fb);
+              tma_load_2d_pair_hint(st + kATileBytes, &maps.b[a], c * 64, b_row, fb, keep);
               ++issued[stage];
               if (++stage == S) { stage = 0; phase ^= 1; }
             }
@@ -197,12 +209,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t unit_phase = 0;
       const uint32_t idesc_acc = idesc_bf16_f32(kPairM, kBN);
       const uint32_t hbuf_addr = smem_u32(hbuf);
+      const uint32_t stage_base = smem_u32(sbase);
       bool ok = true;
-      for (int L = t_begin; L < t_end && ok; ++L) {
+      for (int L = 0, chunk = pair, c_end = 0; ok; ++L) {
+        if (L >= c_end) {
+          if (chunk >= nchunks) break;
+          L = chunk * CH;
+          c_end = min(L + CH, p.total_tiles);
+          chunk += npairs;
+        }
         const Tile t = decode_tile(p, L);
         const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
         const bool lora = a1 > a0;
-        const bool first = lora && ((L == t_begin) || (t.j == 0));
+        const bool first = lora && ((L % CH == 0) || (t.j == 0));
         if (!(p.has_base || lora)) continue;
         const int b = count & 1;
         if (!(ok = mbar_wait_cluster(&acc_empty[b], (nuse[b] & 1) ^ 1, abort_flag, tmo, status)))
@@ -213,22 +232,56 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const uint32_t acc_t = tmem + b * kBN;
         const uint32_t h_t = tmem + (b ^ 1) * kBN;
-        if (p.has_base || first) {
+        if (p.has_base && !first) {
+          // the hot loop: four 256x256x16 pair MMAs per stage; a K step of 16 elements is
+          // +32 bytes, i.e. +2 in the descriptors' 16-byte address field
           for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!(ok = mbar_wait_cluster(&full[stage], phase, abort_flag, tmo, status))) break;
+            if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
             tc_fence_after();
-            const uint32_t st = smem_u32(sbase + stage * SB);
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              const uint64_t adesc = sw128_kmajor_desc(st + kk * 32);
-              const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-              if (p.has_base)
-                mma_bf16_pair(acc_t, adesc, sw128_kmajor_desc(st + kATileBytes + kk * 32), idesc_acc,
-                              acc);
-              if (first)
-                for (int a = a0; a < a1; ++a)
-                  mma_bf16_pair(h_t + p.ad[a].chunk_off * 64, adesc,
-                                sw128_kmajor_desc(st + 2 * kATileBytes + p.ad[a].roff * 128 + kk * 32),
-                                idesc_bf16_f32(kPairM, p.ad[a].rpad16), acc);
+            const uint32_t st = stage_base + stage * SB;
+            const uint64_t ad = sw128_kmajor_desc(st);
+            const uint64_t bd = sw128_kmajor_desc(st + kATileBytes);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_bf16_pair(acc_t, ad + 2 * kk, bd + 2 * kk, idesc_acc, (kb | kk) != 0 ? 1u : 0u);
+            mma_commit_pair_mc(&empty[stage], kBothCtas);
+            if (++stage == S) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
+        } else if (p.has_base || first) {
+          // first tile of a unit: the same K loop also runs X A_p^T into the other buffer
+          const int na = a1 - a0;
+          uint32_t hcol[kMaxAd], roffd[kMaxAd], hid[kMaxAd];
+#pragma unroll
+          for (int i = 0; i < kMaxAd; ++i) {
+            const int a = min(a0 + i, kMaxAd - 1);
+            hcol[i] = h_t + p.ad[a].chunk_off * 64;
+            roffd[i] = static_cast<uint32_t>(p.ad[a].roff * 128) >> 4;
+            hid[i] = idesc_bf16_f32(kPairM, p.ad[a].rpad16);
+          }
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
+            tc_fence_after();
+            const uint32_t st = stage_base + stage * SB;
+            const uint64_t ad = sw128_kmajor_desc(st);
+            const uint64_t bd = sw128_kmajor_desc(st + kATileBytes);
+            const uint64_t rd = sw128_kmajor_desc(st + 2 * kATileBytes);
+            // MMAs grouped by destination: alternating accumulators within a K step
+            // stalls the tensor pipe, so the base tile's four K steps go first, then
+            // each adapter's four
+            if (p.has_base) {
+#pragma unroll
+              for (int kk = 0; kk < kBK / 16; ++kk)
+                mma_bf16_pair(acc_t, ad + 2 * kk, bd + 2 * kk, idesc_acc, (kb | kk) != 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int i = 0; i < kMaxAd; ++i) {
+              if (i < na) {
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                  mma_bf16_pair(hcol[i], ad + 2 * kk, rd + roffd[i] + 2 * kk, hid[i],
+                                (kb | kk) != 0 ? 1u : 0u);
+              }
             }
             mma_commit_pair_mc(&empty[stage], kBothCtas);
             if (++stage == S) { stage = 0; phase ^= 1; }
@@ -245,15 +298,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           for (int a = a0; a < a1 && ok; ++a) {
             for (int c = 0; c < p.ad[a].nchunks; ++c) {
-              if (!(ok = mbar_wait_cluster(&full[stage], phase, abort_flag, tmo, status))) break;
+              if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
               tc_fence_after();
-              const uint32_t st = smem_u32(sbase + stage * SB);
+              const uint32_t st = stage_base + stage * SB;
               const int kext = min(64, p.ad[a].rpad16 - 64 * c);
-              const uint32_t hchunk = hbuf_addr + (p.ad[a].chunk_off + c) * kHChunkBytes;
+              const uint64_t hd = sw128_kmajor_desc(hbuf_addr + (p.ad[a].chunk_off + c) * kHChunkBytes);
+              const uint64_t bd = sw128_kmajor_desc(st + kATileBytes);
               for (int kk = 0; kk < kext / 16; ++kk)
-                mma_bf16_pair(acc_t, sw128_kmajor_desc(hchunk + kk * 32),
-                              sw128_kmajor_desc(st + kATileBytes + kk * 32), idesc_acc,
-                              (accum || kk > 0) ? 1u : 0u);
+                mma_bf16_pair(acc_t, hd + 2 * kk, bd + 2 * kk, idesc_acc, (accum || kk > 0) ? 1u : 0u);
               accum = true;
               mma_commit_pair_mc(&empty[stage], kBothCtas);
               if (++stage == S) { stage = 0; phase ^= 1; }
@@ -274,45 +326,74 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (4 warps)
+    // Output chunks of 128 bytes per row (64 bf16 or 32 fp32 columns) are staged in two
+    // 128-byte-swizzled shared buffers and written by TMA bulk stores (evict-first in L2);
+    // a partial chunk at the end of a column group is written with plain stores.  Every
+    // wait outcome is OR-reduced over the four warps so that they always leave together
+    // and never strand each other at a named barrier.
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
     const int row_in_cta = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t hbuf_addr = smem_u32(hbuf);
+    const uint32_t stg_addr = hbuf_addr + p.hchunks * kHChunkBytes;
+    const bool elected = threadIdx.x == 64;
     const uint32_t acc_empty_l[2] = {mapa_shared(smem_u32(&acc_empty[0]), 0),
                                      mapa_shared(smem_u32(&acc_empty[1]), 0)};
     const uint32_t h_ready_l = mapa_shared(smem_u32(h_ready), 0);
+    const uint64_t stream_out = l2_evict_first();   // Y is written once: keep X and W in L2
+    const int cw = p.y_f32 ? 32 : 64;               // columns per 128-byte row chunk
     uint32_t nuse[2] = {0, 0};
     int count = 0;
     uint32_t unit_phase = 0;
-    for (int L = t_begin; L < t_end; ++L) {
+    uint32_t sidx = 0;                              // staging chunks issued so far
+    for (int L = 0, chunk = pair, c_end = 0;; ++L) {
+      if (L >= c_end) {
+        if (chunk >= nchunks) break;
+        L = chunk * CH;
+        c_end = min(L + CH, p.total_tiles);
+        chunk += npairs;
+      }
       const Tile t = decode_tile(p, L);
       const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
       const bool lora = a1 > a0;
-      const bool first = lora && ((L == t_begin) || (t.j == 0));
+      const bool first = lora && ((L % CH == 0) || (t.j == 0));
       const bool any_mma = p.has_base || lora;
       const int b = count & 1;
       if (first) {
-        // every lane waits; the warp proceeds only if all lanes saw the phase, so the
-        // .sync.aligned TMEM loads below are always executed by the whole warp
-        if (!__all_sync(0xffffffffu, mbar_wait_cluster(h_full, unit_phase, abort_flag, tmo, status)))
-          break;
+        const bool ok = mbar_wait_cluster(h_full, unit_phase, abort_flag, tmo, status);
+        if (named_bar_any(!ok, 2, 128)) break;
         tc_fence_after();
         unit_phase ^= 1;
         const uint32_t h_t = tmem + (b ^ 1) * kBN;
         for (int a = a0; a < a1; ++a) {
           const float s = p.ad[a].s;
-          const int units = p.ad[a].rpad16 >> 3;
-          for (int u = 0; u < units; ++u) {
-            uint32_t r[8];
-            tmem_ld8(h_t + lane_base + p.ad[a].chunk_off * 64 + u * 8, r);
-            const uint32_t w0 = pack_bf16x2(u2f(r[0]) * s, u2f(r[1]) * s);
-            const uint32_t w1 = pack_bf16x2(u2f(r[2]) * s, u2f(r[3]) * s);
-            const uint32_t w2 = pack_bf16x2(u2f(r[4]) * s, u2f(r[5]) * s);
-            const uint32_t w3 = pack_bf16x2(u2f(r[6]) * s, u2f(r[7]) * s);
-            const int chunk = p.ad[a].chunk_off + (u >> 3);
-            const int unit16 = (u & 7) ^ (row_in_cta & 7);
-            st_shared_v4(hbuf_addr + chunk * kHChunkBytes + row_in_cta * 128 + unit16 * 16, w0, w1,
-                         w2, w3);
+          const int units = p.ad[a].rpad16 >> 3;       // 8 ranks (16 bytes of H~) per unit
+          for (int u0 = 0; u0 < units; u0 += 4) {
+            // 32 ranks per TMEM load where the rank allows it, 8 otherwise
+            uint32_t r[32];
+            const int n = min(4, units - u0);
+            if (n == 4) {
+              tmem_ld32(h_t + lane_base + p.ad[a].chunk_off * 64 + u0 * 8, r);
+            } else {
+              for (int k = 0; k < n; ++k) {
+                uint32_t r8[8];
+                tmem_ld8(h_t + lane_base + p.ad[a].chunk_off * 64 + (u0 + k) * 8, r8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) r[k * 8 + i] = r8[i];
+              }
+            }
+            for (int k = 0; k < n; ++k) {
+              const int u = u0 + k;
+              const uint32_t* q8 = r + k * 8;
+              const uint32_t w0 = pack_bf16x2(u2f(q8[0]) * s, u2f(q8[1]) * s);
+              const uint32_t w1 = pack_bf16x2(u2f(q8[2]) * s, u2f(q8[3]) * s);
+              const uint32_t w2 = pack_bf16x2(u2f(q8[4]) * s, u2f(q8[5]) * s);
+              const uint32_t w3 = pack_bf16x2(u2f(q8[6]) * s, u2f(q8[7]) * s);
+              const int chunk16 = p.ad[a].chunk_off + (u >> 3);
+              const int unit16 = (u & 7) ^ (row_in_cta & 7);
+              st_shared_v4(hbuf_addr + chunk16 * kHChunkBytes + row_in_cta * 128 + unit16 * 16, w0,
+                           w1, w2, w3);
+            }
           }
         }
         fence_proxy_async_smem();
@@ -321,41 +402,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) mbar_arrive_cluster(h_ready_l);
       }
       if (any_mma) {
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait_cluster(&acc_full[b], nuse[b] & 1, abort_flag, tmo, status)))
-          break;
+        const bool ok = mbar_wait_cluster(&acc_full[b], nuse[b] & 1, abort_flag, tmo, status);
+        if (named_bar_any(!ok, 2, 128)) break;
         tc_fence_after();
       }
 
-      const int row = t.m * kPairM + static_cast<int>(cta) * kBM + row_in_cta;
+      const int row0 = t.m * kPairM + static_cast<int>(cta) * kBM;
+      const int row = row0 + row_in_cta;
       const bool row_ok = row < p.T;
       const uint32_t acc_t = tmem + b * kBN;
+      // valid chunks of this tile (the last tile of a group may be partial)
+      const int nchunk = min(kBN / cw, (p.out_g - t.j * kBN + cw - 1) / cw);
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        const int cig = t.j * kBN + c * 32;                 // first column, within the group
-        const int ncols = min(32, p.out_g - cig);           // uniform across the warp
-        if (ncols <= 0) break;
+      for (int c = 0; c < nchunk; ++c) {
+        const int cig = t.j * kBN + c * cw;                 // first column, within the group
+        const int ncols = min(cw, p.out_g - cig);           // uniform across the warps
         const int gcol = t.g * p.out_g + cig;
-        float v[32];
+        float v[64];
         if (any_mma) {
           uint32_t r[32];
-          tmem_ld32(acc_t + lane_base + c * 32, r);
+          tmem_ld32(acc_t + lane_base + c * cw, r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = u2f(r[i]);
+          if (cw == 64) {
+            tmem_ld32(acc_t + lane_base + c * cw + 32, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[32 + i] = u2f(r[i]);
+          }
+          if (c == nchunk - 1) {
+            // the accumulator is fully in registers: hand it back to the MMA before the
+            // last chunk's stores
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty_l[b]);
+          }
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          for (int i = 0; i < 64; ++i) v[i] = 0.f;
         }
         if (p.bias) {
           if (p.bias_f32) {
             const float* bp = static_cast<const float*>(p.bias) + gcol;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
+            for (int i = 0; i < 64; ++i)
               if (i < ncols) v[i] += bp[i];
           } else {
             const uint16_t* bp = static_cast<const uint16_t*>(p.bias) + gcol;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
+            for (int i = 0; i < 64; ++i)
               if (i < ncols) v[i] += bf16_to_f32(bp[i]);
           }
         }
@@ -368,39 +462,63 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int jj = 0; jj < p.ad32[a].rank; ++jj) {
               const float h = hrow[jj];
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
+              for (int i = 0; i < 64; ++i)
                 if (i < ncols) v[i] = fmaf(h, Bm[i * ldb + jj], v[i]);
             }
           }
         }
-        if (row_ok) {
+        if (ncols == cw) {
+          // full chunk: stage (128-byte swizzle) and bulk-store the 128 x cw box
+          if (sidx >= 2 && elected) bulk_wait_read_le1();
+          named_bar_sync(1, 128);
+          const uint32_t buf = stg_addr + (sidx & 1) * kStgBytes;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            uint32_t w0, w1, w2, w3;
+            if (cw == 64) {
+              w0 = pack_bf16x2(v[8 * u], v[8 * u + 1]);
+              w1 = pack_bf16x2(v[8 * u + 2], v[8 * u + 3]);
+              w2 = pack_bf16x2(v[8 * u + 4], v[8 * u + 5]);
+              w3 = pack_bf16x2(v[8 * u + 6], v[8 * u + 7]);
+            } else {
+              w0 = f2u(v[4 * u]); w1 = f2u(v[4 * u + 1]); w2 = f2u(v[4 * u + 2]); w3 = f2u(v[4 * u + 3]);
+            }
+            st_shared_v4(buf + row_in_cta * 128 + ((u ^ (row_in_cta & 7)) * 16), w0, w1, w2, w3);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (elected) {
+            tma_store_2d_hint(&maps.y, gcol, row0, stg + (sidx & 1) * kStgBytes, stream_out);
+            bulk_commit();
+          }
+          ++sidx;
+        } else if (row_ok) {
+          // partial chunk at the end of a group: plain stores, masked
           if (p.y_f32) {
             float* y = static_cast<float*>(p.Y) + static_cast<long long>(row) * p.ldy + gcol;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               if (i * 4 < ncols)
-                st_global_v4(y + i * 4, f2u(v[4 * i]), f2u(v[4 * i + 1]), f2u(v[4 * i + 2]),
-                             f2u(v[4 * i + 3]));
+                st_global_v4_hint(y + i * 4, f2u(v[4 * i]), f2u(v[4 * i + 1]), f2u(v[4 * i + 2]),
+                                  f2u(v[4 * i + 3]), stream_out);
           } else {
             uint16_t* y = static_cast<uint16_t*>(p.Y) + static_cast<long long>(row) * p.ldy + gcol;
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 8; ++i)
               if (i * 8 < ncols)
-                st_global_v4(y + i * 8, pack_bf16x2(v[8 * i], v[8 * i + 1]),
-                             pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                             pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
-                             pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+                st_global_v4_hint(y + i * 8, pack_bf16x2(v[8 * i], v[8 * i + 1]),
+                                  pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                  pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                                  pack_bf16x2(v[8 * i + 6], v[8 * i + 7]), stream_out);
           }
         }
       }
       if (any_mma) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(acc_empty_l[b]);
         ++nuse[b];
         ++count;
       }
     }
+    if (elected) bulk_wait_all();
   }
 
   tc_fence_before();
