@@ -173,6 +173,32 @@ int lora_dense_patch(void* param, int32_t param_dtype, int64_t param_numel,
                      const void* payload, int32_t payload_dtype, int64_t payload_numel,
                      int32_t kind, double strength, void* stream);
 
+/*
+ * lora_linear_fwd_noalloc -- lora_linear_fwd for callers that cannot provide or allocate
+ * device scratch memory.  The pages have no counterpart: this is a deployment variant.
+ *
+ * Who needs it: code embedded in a host that owns all device memory through its own
+ * allocator and gives plug-ins no allocation rights, fixed-budget inference servers, and
+ * latency-critical paths where cudaMalloc/cudaFree (which may synchronise the device)
+ * are not acceptable.  Such a caller still passes its inputs and output; the scratch that
+ * FP32 adapters need (s * X A^T in fp32, T x sum of their ranks floats, and T x sum of all
+ * ranks on the all-FP32 path) comes from a fixed 4 MiB array inside the library, held on
+ * every device that uses it until the process exits.  The call allocates nothing.
+ *
+ * Same arguments, dtypes, alignment rules and errors as lora_linear_fwd, minus the
+ * workspace.  A call that would need more than 4 MiB of scratch is rejected with
+ * WP_ERR_WORKSPACE before anything is launched (lora_last_cuda_error() says how much was
+ * needed).  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ * capture.  Every call on a device shares the one array and leaves its contents behind
+ * (every scratch element is written before it is read, so nothing needs clearing): calls
+ * whose kernels overlap on the GPU, e.g. on two streams at once, race on it and must be
+ * serialised by the caller.
+ */
+int lora_linear_fwd_noalloc(const wp_mat* X, const wp_mat* W, const wp_mat* bias,
+                            const wp_adapter* adapters, int32_t n_adapters, double request_scale,
+                            const wp_out* Y, void* stream);
+
 /* Bytes of device workspace the given call needs (0 if none).  `op` is WP_OP_*;
  * the other arguments are those of the call (adapters: n_adapters, or n_groups). */
 size_t lora_workspace_size(int32_t op, const wp_mat* X, const wp_mat* W,

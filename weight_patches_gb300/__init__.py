@@ -72,6 +72,7 @@ def _load():
     pm, po, pa = ctypes.POINTER(WpMat), ctypes.POINTER(WpOut), ctypes.POINTER(WpAdapter)
     lib.lora_linear_fwd.argtypes = [pm, pm, pm, pa, I32, D, po, P, SZ, P]
     lib.lora_linear_fwd_grouped.argtypes = [pm, pm, pm, I32, pa, D, po, P, SZ, P]
+    lib.lora_linear_fwd_noalloc.argtypes = [pm, pm, pm, pa, I32, D, po, P]
     lib.lora_linear_bwd.argtypes = [pm, pm, pm, I32, pa, D, po, po, po, P, SZ, P]
     lib.lora_dense_patch.argtypes = [P, I32, I64, P, I32, I64, I32, D, P]
     lib.lora_workspace_size.argtypes = [I32, pm, pm, pa, I32]
@@ -83,7 +84,7 @@ def _load():
     lib.lora_nf4_codebook.restype = None
     lib.lora_last_cuda_error.restype = ctypes.c_char_p
     for name in ("lora_linear_fwd", "lora_linear_fwd_grouped", "lora_linear_bwd", "lora_dense_patch",
-                 "lora_device_status"):
+                 "lora_device_status", "lora_linear_fwd_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     _LIB = lib
     return lib

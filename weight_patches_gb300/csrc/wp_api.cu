@@ -404,3 +404,77 @@ void lora_nf4_codebook(float out[16]) { nf4_codebook_host(out); }
 const char* lora_last_cuda_error(void) { return g_last_error.c_str(); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Forward without any device allocation by anyone.
+//
+// Some callers cannot hand the library a workspace and cannot allocate one either: hosts
+// that own every byte of device memory through their own allocator and give plug-ins no
+// allocation rights, fixed-budget inference servers, and latency-critical paths where
+// cudaMalloc/cudaFree (which may synchronise the device) are not acceptable.  For them the
+// scratch that the FP32-adapter projection needs (s * X A^T in fp32, T x sum(r) floats)
+// lives in a fixed array in this library's own device memory instead of a workspace.
+//
+// The array holds kNoAllocScratchBytes per device, for as long as the library is loaded.
+// Host code must not pass the array's name to a kernel (on the host it is only a stand-in
+// symbol); the device address is looked up once per device with cudaGetSymbolAddress, on
+// the first call made with that device current, and passed to the kernels.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;   // 4 MiB: T * sum(r) <= 1 Mi floats
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {nullptr};
+
+// Device address of the scratch array for the current device (set-up on first use).
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    return WP_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= 64) return WP_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr) {
+      set_last_cuda_error(e);
+      return WP_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return WP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lora_linear_fwd_noalloc(const wp_mat* X, const wp_mat* W, const wp_mat* bias,
+                            const wp_adapter* adapters, int32_t n_adapters, double request_scale,
+                            const wp_out* Y, void* stream) {
+  if (!X || n_adapters < 0 || (n_adapters > 0 && !adapters)) return WP_ERR_INVALID;
+  const size_t need = lora_workspace_size(WP_OP_FWD, X, W, adapters, n_adapters);
+  if (need > kNoAllocScratchBytes) {
+    char buf[160];
+    snprintf(buf, sizeof(buf),
+             "lora_linear_fwd_noalloc: needs %zu bytes of scratch, the static array holds %zu",
+             need, kNoAllocScratchBytes);
+    g_last_error = buf;
+    return WP_ERR_WORKSPACE;
+  }
+  void* scratch = nullptr;
+  if (need > 0) {
+    const int rc = noalloc_scratch(&scratch);
+    if (rc != WP_OK) return rc;
+  }
+  return fwd_impl(X, W, bias, 1, false, adapters, n_adapters, request_scale, Y, scratch,
+                  need > 0 ? kNoAllocScratchBytes : 0, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
