@@ -62,6 +62,31 @@ int make_map(CUtensorMap* m, int dtype, const void* ptr, long long inner, long l
   return WP_OK;
 }
 
+// 2-D byte tensor map (4-bit codes, two per byte) without swizzle: boxes of
+// {box_inner bytes, box_outer rows}, rows box_inner bytes apart in shared memory.
+int make_map_u8(CUtensorMap* m, const void* ptr, long long inner_bytes, long long outer,
+                long long ld_bytes, int box_inner, int box_outer) {
+  auto fn = encode_fn();
+  if (!fn) {
+    g_last_error = "cuTensorMapEncodeTiled unavailable";
+    return WP_ERR_CUDA;
+  }
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner_bytes), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_bytes)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[96];
+    snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled (u8) failed (%d)", static_cast<int>(r));
+    g_last_error = buf;
+    return WP_ERR_CUDA;
+  }
+  return WP_OK;
+}
+
 int make_map_bf16(CUtensorMap* m, const void* ptr, long long inner, long long outer, long long ld,
                   int box_inner, int box_outer) {
   return make_map(m, WP_BF16, ptr, inner, outer, ld, box_inner, box_outer);
@@ -200,7 +225,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   }
 
   // --------------------------------------------------------------- tensor-core path
-  if (W && W->dtype == WP_NF4) return WP_ERR_UNSUPPORTED;   // 4-bit mainloop not built yet
+  const bool nf4 = W && W->dtype == WP_NF4;
   if (!aligned16(X->data) || X->ld % 8) return WP_ERR_ALIGN;
   if (W && (!aligned16(W->data) || W->ld % 8)) return WP_ERR_ALIGN;
   if (!aligned16(Y->data) || Y->ld % (Y->dtype == WP_BF16 ? 8 : 4)) return WP_ERR_ALIGN;
@@ -274,7 +299,13 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   // adapter's A rows and 128 rows of its B tile.
   int rc = make_map_bf16(&maps.x, X->data, K, T, X->ld, kBK, kBM);
   if (rc != WP_OK) return rc;
-  if (W) {
+  if (nf4) {
+    // codes: [N rows, K/2 bytes]; each CTA loads 128 rows x 32 bytes (64 elements) per K step
+    rc = make_map_u8(&maps.wq, W->data, K / 2, N, K / 2, kBK / 2, 128);
+    if (rc != WP_OK) return rc;
+    p.absmax = W->absmax;
+    nf4_codebook_host(p.nf4_code);
+  } else if (W) {
     rc = make_map_bf16(&maps.w, W->data, K, N, W->ld, kBK, 128);
     if (rc != WP_OK) return rc;
   }
@@ -288,8 +319,11 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     if (rc != WP_OK) return rc;
   }
 
-  p.stage_bytes = kATileBytes + kBHalfBytes + p.rslot_rows * 128;
-  const size_t fixed = 1024 + static_cast<size_t>(p.hchunks) * kHChunkBytes + 2 * kStgBytes + 256;
+  // stage: X rows | bf16 W half (or 4-bit codes, padded to 4 KiB) | rank slot
+  p.rslot_off = kATileBytes + (nf4 ? kRawBytes : kBHalfBytes);
+  p.stage_bytes = p.rslot_off + p.rslot_rows * 128;
+  const size_t fixed = 1024 + (nf4 ? static_cast<size_t>(kWRing) * kBHalfBytes : 0) +
+                       static_cast<size_t>(p.hchunks) * kHChunkBytes + 2 * kStgBytes + 512;
   int stages = static_cast<int>((kSmemLimit - fixed) / p.stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return WP_ERR_UNSUPPORTED;
@@ -300,11 +334,11 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     rc = launch_h32(hp, stream);
     if (rc != WP_OK) return rc;
   }
-  int pairs = tc_max_pairs(smem);
+  int pairs = tc_max_pairs(smem, nf4);
   if (pairs <= 0) return WP_ERR_CUDA;
   if (pairs > p.total_tiles) pairs = p.total_tiles;
   p.chunk_tiles = chunk_tiles_for(p.total_tiles, pairs, p.nt_g);
-  return launch_tc_fwd(maps, p, 2 * pairs, smem, stream);
+  return launch_tc_fwd(maps, p, 2 * pairs, smem, stream, nf4);
 }
 
 }  // namespace

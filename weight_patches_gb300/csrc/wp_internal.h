@@ -27,6 +27,9 @@ constexpr int kBHalfBytes = 128 * kBK * 2;      // 16 KiB: this CTA's half of a 
 constexpr int kHChunkBytes = kBM * 64 * 2;      // one 64-rank chunk of s*X A^T in bf16
 constexpr int kStgBytes = kBM * 128;            // output staging: 128 rows x 128 bytes
 constexpr int kTcThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kTcThreadsNF4 = 448;  // + warps 6..13: 4-bit dequantisation
+constexpr int kRawBytes = 128 * 32;             // 4-bit codes of 128 rows x 64 K per stage
+constexpr int kWRing = 3;                       // dequantised weight tiles in flight
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 227 * 1024;
 
@@ -59,7 +62,10 @@ struct TcParams {
   int hchunks;                 // max rank chunks in any group (shared-memory H~ buffers)
   int rslot_rows;              // rows of the per-stage rank slot (A rows, per CTA)
   int stages;
-  int stage_bytes;             // 32 KiB + rslot_rows * 128
+  int stage_bytes;             // bf16 W: 32 KiB + rank slot; 4-bit W: 16 KiB + 4 KiB codes + rank slot
+  int rslot_off;               // byte offset of the rank slot inside a stage
+  const float* absmax;         // 4-bit W: [N * K / 64] fp32 block scales
+  float nf4_code[16];          // 4-bit W: the NormalFloat levels
   TcAdapter ad[kMaxAd];
   int n_ad32;                  // fp32 adapters (epilogue FFMA)
   TcAdapter32 ad32[kMaxAd32];
@@ -77,14 +83,15 @@ struct TcMaps {
   CUtensorMap x;
   CUtensorMap w;
   CUtensorMap y;                 // output, 128-byte swizzled boxes of 128 rows
+  CUtensorMap wq;                // 4-bit W codes: [N rows, K/2 bytes], boxes of 128 x 32 bytes
   CUtensorMap a[kMaxAd];
   CUtensorMap b[kMaxAd];
 };
 
 // Number of CTA pairs that can be resident at once for this shared-memory size.
-int tc_max_pairs(size_t smem_bytes);
+int tc_max_pairs(size_t smem_bytes, bool nf4);
 int launch_tc_fwd(const TcMaps& maps, const TcParams& p, int grid, size_t smem_bytes,
-                  cudaStream_t stream);
+                  cudaStream_t stream, bool nf4);
 int tc_fwd_status(int reset);
 
 // ------------------------------------------------------------------ fp32 CUDA-core path

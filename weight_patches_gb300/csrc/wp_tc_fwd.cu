@@ -7,7 +7,9 @@
 // second low-rank GEMM accumulates straight onto the base output so the [T, out]
 // delta never exists, the bias belongs to the base GEMM's epilogue, stacked q/k/v
 // (gate/up) adapters take one update per column group, and an FP32 adapter keeps its
-// FP32 GEMMs and is added once.  Here all of it happens inside one persistent kernel:
+// FP32 GEMMs and is added once.  Unsloth fast_lora walkthrough, section 3 (matmul_lora):
+// a 4-bit base weight is dequantised into the matmul.  Here all of it happens inside one
+// persistent kernel:
 //
 //   * a CTA pair (cluster of 2) computes 256 x 256 output tiles with tcgen05.mma
 //     cta_group::2: each CTA stages its own 128 X rows and half of the weight tile, so
@@ -23,13 +25,18 @@
 //   * two accumulator buffers (2 x 256 TMEM columns) let the epilogue of tile n overlap
 //     the MMAs of tile n+1; the epilogue adds the bias and the FP32 adapters' terms
 //     (sum_j (s X A32^T)[t, j] B32[o, j], FFMA, before the single rounding) and writes
-//     bf16 or fp32 rows.
+//     bf16 or fp32 rows through TMA bulk stores;
+//   * with a 4-bit NormalFloat base weight, TMA brings the packed codes (32 bytes per row
+//     per K step) and eight dequantisation warps per CTA turn them into the bf16 weight
+//     tile in shared memory -- bf16(fl32(level[q]) * absmax) through a per-row, per-block
+//     16-entry table and register byte permutes -- so no bf16 copy of W ever exists.
 //
 // Warp roles per CTA: warp 0 issues TMA loads (both CTAs), warp 1 allocates tensor
 // memory (both CTAs) and issues the pair MMAs (leader CTA only), warps 2..5 are the
-// epilogue (one token row per thread).  Operands are K-major bf16 in the 128-byte
-// swizzle layout.  Every mbarrier wait is bounded (wall clock); on expiry the CTA records
-// WP_ERR_TIMEOUT, waits for its own copies in flight, frees tensor memory and returns.
+// epilogue (one token row per thread), warps 6..13 dequantise (4-bit weights only).
+// Operands are K-major bf16 in the 128-byte swizzle layout.  Every mbarrier wait is
+// bounded (wall clock); on expiry the CTA records WP_ERR_TIMEOUT, waits for its own copies
+// in flight, frees tensor memory and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -59,21 +66,44 @@ __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(uint32_t(h) << 16); }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Four 4-bit codes (nibble i of `sel4` is the code of element i) -> four bf16 values
+// from a 16-entry table split into byte planes: lo[j] / hi[j] hold the low / high bytes
+// of entries 4j..4j+3.  Returns two words: elements (0,1) and (2,3).
+__device__ __forceinline__ void lookup4(uint32_t sel4, const uint32_t (&lo)[4], const uint32_t (&hi)[4],
+                                        uint32_t& out01, uint32_t& out23) {
+  const uint32_t sel3 = sel4 & 0x7777u;                  // byte index within a half-table
+  const uint32_t x = (sel4 >> 3) & 0x1111u;              // 1 where the code is >= 8
+  const uint32_t m = ((x & 0x1u) | ((x & 0x10u) << 4) | ((x & 0x100u) << 8) | ((x & 0x1000u) << 12)) * 0xFFu;
+  const uint32_t l = (prmt(lo[0], lo[1], sel3) & ~m) | (prmt(lo[2], lo[3], sel3) & m);
+  const uint32_t h = (prmt(hi[0], hi[1], sel3) & ~m) | (prmt(hi[2], hi[3], sel3) & m);
+  out01 = prmt(l, h, 0x5140u);
+  out23 = prmt(l, h, 0x7362u);
+}
+
 constexpr uint16_t kBothCtas = 0x3;
 
 }  // namespace
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <bool kNF4>
+__global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     tc_fused_fwd_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base_addr - raw_addr);
 
+  // Stage s: [X rows 16 KiB | bf16 W half 16 KiB, or 4-bit codes 4 KiB | rank slot]
   const int S = p.stages;
   const int SB = p.stage_bytes;
-  uint8_t* hbuf = sbase + S * SB;
-  uint8_t* stg = hbuf + p.hchunks * kHChunkBytes;      // 2 output staging buffers
+  uint8_t* wring = sbase + S * SB;                      // 4-bit W: dequantised tiles
+  uint8_t* hbuf = wring + (kNF4 ? kWRing * kBHalfBytes : 0);
+  uint8_t* stg = hbuf + p.hchunks * kHChunkBytes;       // 2 output staging buffers
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg + 2 * kStgBytes);
   uint64_t* full = bars;                  // [S]  leader: TMA bytes of both CTAs landed
   uint64_t* empty = bars + S;             // [S]  both: the pair MMAs consumed the stage
@@ -82,7 +112,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* h_full = acc_full + 4;        //      both: X A^T of the unit is in TMEM
   uint64_t* h_ready = acc_full + 5;       //      leader: both CTAs wrote their H~ rows
   uint64_t* drain = acc_full + 6;         //      leader: every MMA issued has finished
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 7);
+  uint64_t* raw_full = acc_full + 7;      // [S]  4-bit W, local: this CTA's codes landed
+  uint64_t* wfull = raw_full + S;         // [kWRing] leader: both CTAs' tiles dequantised
+  uint64_t* wempty = wfull + kWRing;      // [kWRing] both: the MMAs consumed the tile
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + kWRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -94,6 +127,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&raw_full[s], 1);
     }
     mbar_init(&acc_full[0], 1);
     mbar_init(&acc_full[1], 1);
@@ -102,12 +136,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(h_full, 1);
     mbar_init(h_ready, 8);
     mbar_init(drain, 1);
+    for (int w = 0; w < kWRing; ++w) {
+      mbar_init(&wfull[w], 16);           // 8 dequantisation warps x 2 CTAs
+      mbar_init(&wempty[w], 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&maps.x);
-    if (p.has_base) tma_prefetch_desc(&maps.w);
+    if (p.has_base) tma_prefetch_desc(kNF4 ? &maps.wq : &maps.w);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, 512);
@@ -120,8 +158,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   // Pair `pair` takes chunks pair, pair + npairs, ... of `chunk_tiles` consecutive tiles
-  // in (row block, group, column tile) order: at any moment the pairs work on nearby
-  // row blocks (X stays in L2) while each chunk reuses its X A^T across its tiles.
+  // in (row block, group, column tile) order; each chunk reuses its X A^T across its tiles.
   const int npairs = static_cast<int>(gridDim.x >> 1);
   const int pair = static_cast<int>(blockIdx.x >> 1);
   const int CH = p.chunk_tiles;
@@ -151,7 +188,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool first = lora && ((L % CH == 0) || (t.j == 0));
         const int x_row = t.m * kPairM + static_cast<int>(cta) * kBM;
         if (p.has_base || first) {
-          uint32_t tx = (p.has_base ? 4u : 2u) * kATileBytes;     // both CTAs
+          uint32_t tx = (p.has_base && !kNF4 ? 4u : 2u) * kATileBytes;     // both CTAs
           if (first)
             for (int a = a0; a < a1; ++a) tx += p.ad[a].rpad16 * 128;
           const int w_row = t.g * p.out_g + t.j * kBN + static_cast<int>(cta) * 128;
@@ -161,13 +198,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
             if (leader) mbar_arrive_expect_tx(&full[stage], tx);
             tma_load_2d_pair(st, &maps.x, kb * kBK, x_row, fb);
-            if (p.has_base)
-              tma_load_2d_pair_hint(st + kATileBytes, &maps.w, kb * kBK, w_row, fb, keep);
+            if (p.has_base) {
+              if (kNF4) {
+                // this CTA's codes complete on its own barrier; the dequantisation warps
+                // turn them into the bf16 tile the MMA reads
+                mbar_arrive_expect_tx(&raw_full[stage], kRawBytes);
+                tma_load_2d(st + kATileBytes, &maps.wq, kb * (kBK / 2), w_row, &raw_full[stage]);
+              } else {
+                tma_load_2d_pair_hint(st + kATileBytes, &maps.w, kb * kBK, w_row, fb, keep);
+              }
+            } else if (kNF4) {
+              mbar_arrive(&raw_full[stage]);
+            }
             if (first)
               for (int a = a0; a < a1; ++a)
-                tma_load_2d_pair_hint(st + 2 * kATileBytes + p.ad[a].roff * 128, &maps.a[a],
-                                      kb * kBK, static_cast<int>(cta) * (p.ad[a].rpad16 >> 1), fb,
-                                      keep);
+                tma_load_2d_pair_hint(st + p.rslot_off + p.ad[a].roff * 128, &maps.a[a], kb * kBK,
+                                      static_cast<int>(cta) * (p.ad[a].rpad16 >> 1), fb, keep);
             ++issued[stage];
             if (++stage == S) { stage = 0; phase ^= 1; }
           }
@@ -180,7 +226,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               uint8_t* st = sbase + stage * SB;
               const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
               if (leader) mbar_arrive_expect_tx(&full[stage], 2u * kBHalfBytes);
-              tma_load_2d_pair_hint(st + kATileBytes, &maps.b[a], c * 64, b_row, fb, keep);
+              // with a 4-bit W the stage has no bf16 weight slot: B rides in the X slot
+              tma_load_2d_pair_hint(st + (kNF4 ? 0 : kATileBytes), &maps.b[a], c * 64, b_row, fb, keep);
+              if (kNF4) mbar_arrive(&raw_full[stage]);      // keep the code barrier in phase
               ++issued[stage];
               if (++stage == S) { stage = 0; phase ^= 1; }
             }
@@ -204,12 +252,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
+      int wb = 0;
+      uint32_t wphase = 0;
       uint32_t nuse[2] = {0, 0};
       int count = 0;
       uint32_t unit_phase = 0;
       const uint32_t idesc_acc = idesc_bf16_f32(kPairM, kBN);
       const uint32_t hbuf_addr = smem_u32(hbuf);
       const uint32_t stage_base = smem_u32(sbase);
+      const uint32_t wring_base = smem_u32(wring);
       bool ok = true;
       for (int L = 0, chunk = pair, c_end = 0; ok; ++L) {
         if (L >= c_end) {
@@ -232,25 +283,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const uint32_t acc_t = tmem + b * kBN;
         const uint32_t h_t = tmem + (b ^ 1) * kBN;
-        if (p.has_base && !first) {
-          // the hot loop: four 256x256x16 pair MMAs per stage; a K step of 16 elements is
-          // +32 bytes, i.e. +2 in the descriptors' 16-byte address field
-          for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
-            tc_fence_after();
-            const uint32_t st = stage_base + stage * SB;
-            const uint64_t ad = sw128_kmajor_desc(st);
-            const uint64_t bd = sw128_kmajor_desc(st + kATileBytes);
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-              mma_bf16_pair(acc_t, ad + 2 * kk, bd + 2 * kk, idesc_acc, (kb | kk) != 0 ? 1u : 0u);
-            mma_commit_pair_mc(&empty[stage], kBothCtas);
-            if (++stage == S) { stage = 0; phase ^= 1; }
-          }
-          if (!ok) break;
-        } else if (p.has_base || first) {
+        if (p.has_base || first) {
           // first tile of a unit: the same K loop also runs X A_p^T into the other buffer
-          const int na = a1 - a0;
+          const int na = first ? a1 - a0 : 0;
           uint32_t hcol[kMaxAd], roffd[kMaxAd], hid[kMaxAd];
 #pragma unroll
           for (int i = 0; i < kMaxAd; ++i) {
@@ -261,30 +296,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           for (int kb = 0; kb < p.k_blocks; ++kb) {
             if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
+            if (kNF4 && p.has_base &&
+                !(ok = mbar_wait_cluster(&wfull[wb], wphase, abort_flag, tmo, status)))
+              break;
             tc_fence_after();
             const uint32_t st = stage_base + stage * SB;
             const uint64_t ad = sw128_kmajor_desc(st);
-            const uint64_t bd = sw128_kmajor_desc(st + kATileBytes);
-            const uint64_t rd = sw128_kmajor_desc(st + 2 * kATileBytes);
-            // MMAs grouped by destination: alternating accumulators within a K step
-            // stalls the tensor pipe, so the base tile's four K steps go first, then
-            // each adapter's four
+            const uint64_t bd = sw128_kmajor_desc(kNF4 ? wring_base + wb * kBHalfBytes : st + kATileBytes);
+            // MMAs grouped by destination: alternating accumulators within a K step stalls
+            // the tensor pipe, so the base tile's four K steps go first, then each adapter's
             if (p.has_base) {
 #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk)
                 mma_bf16_pair(acc_t, ad + 2 * kk, bd + 2 * kk, idesc_acc, (kb | kk) != 0 ? 1u : 0u);
             }
+            if (na > 0) {
+              const uint64_t rd = sw128_kmajor_desc(st + p.rslot_off);
 #pragma unroll
-            for (int i = 0; i < kMaxAd; ++i) {
-              if (i < na) {
+              for (int i = 0; i < kMaxAd; ++i) {
+                if (i < na) {
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)
-                  mma_bf16_pair(hcol[i], ad + 2 * kk, rd + roffd[i] + 2 * kk, hid[i],
-                                (kb | kk) != 0 ? 1u : 0u);
+                  for (int kk = 0; kk < kBK / 16; ++kk)
+                    mma_bf16_pair(hcol[i], ad + 2 * kk, rd + roffd[i] + 2 * kk, hid[i],
+                                  (kb | kk) != 0 ? 1u : 0u);
+                }
               }
             }
             mma_commit_pair_mc(&empty[stage], kBothCtas);
             if (++stage == S) { stage = 0; phase ^= 1; }
+            if (kNF4 && p.has_base) {
+              mma_commit_pair_mc(&wempty[wb], kBothCtas);
+              if (++wb == kWRing) { wb = 0; wphase ^= 1; }
+            }
           }
           if (!ok) break;
         }
@@ -303,7 +346,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const uint32_t st = stage_base + stage * SB;
               const int kext = min(64, p.ad[a].rpad16 - 64 * c);
               const uint64_t hd = sw128_kmajor_desc(hbuf_addr + (p.ad[a].chunk_off + c) * kHChunkBytes);
-              const uint64_t bd = sw128_kmajor_desc(st + kATileBytes);
+              const uint64_t bd = sw128_kmajor_desc(st + (kNF4 ? 0 : kATileBytes));
               for (int kk = 0; kk < kext / 16; ++kk)
                 mma_bf16_pair(acc_t, hd + 2 * kk, bd + 2 * kk, idesc_acc, (accum || kk > 0) ? 1u : 0u);
               accum = true;
@@ -324,7 +367,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       while (!mbar_try_wait_cluster(a, 0) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue (4 warps)
     // Output chunks of 128 bytes per row (64 bf16 or 32 fp32 columns) are staged in two
     // 128-byte-swizzled shared buffers and written by TMA bulk stores (evict-first in L2);
@@ -418,73 +461,98 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int cig = t.j * kBN + c * cw;                 // first column, within the group
         const int ncols = min(cw, p.out_g - cig);           // uniform across the warps
         const int gcol = t.g * p.out_g + cig;
-        float v[64];
-        if (any_mma) {
-          uint32_t r[32];
-          tmem_ld32(acc_t + lane_base + c * cw, r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = u2f(r[i]);
-          if (cw == 64) {
-            tmem_ld32(acc_t + lane_base + c * cw + 32, r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[32 + i] = u2f(r[i]);
-          }
-          if (c == nchunk - 1) {
-            // the accumulator is fully in registers: hand it back to the MMA before the
-            // last chunk's stores
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acc_empty_l[b]);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 64; ++i) v[i] = 0.f;
-        }
-        if (p.bias) {
-          if (p.bias_f32) {
-            const float* bp = static_cast<const float*>(p.bias) + gcol;
-#pragma unroll
-            for (int i = 0; i < 64; ++i)
-              if (i < ncols) v[i] += bp[i];
-          } else {
-            const uint16_t* bp = static_cast<const uint16_t*>(p.bias) + gcol;
-#pragma unroll
-            for (int i = 0; i < 64; ++i)
-              if (i < ncols) v[i] += bf16_to_f32(bp[i]);
-          }
-        }
-        if (p.n_ad32 > 0 && row_ok) {
-          for (int a = 0; a < p.n_ad32; ++a) {
-            if (p.ad32[a].group != t.g) continue;
-            const float* hrow = p.h32 + static_cast<long long>(row) * p.h32_cols + p.ad32[a].h_off;
-            const float* Bm = p.ad32[a].B + static_cast<long long>(cig) * p.ad32[a].ldb;
-            const long long ldb = p.ad32[a].ldb;
-            for (int jj = 0; jj < p.ad32[a].rank; ++jj) {
-              const float h = hrow[jj];
-#pragma unroll
-              for (int i = 0; i < 64; ++i)
-                if (i < ncols) v[i] = fmaf(h, Bm[i * ldb + jj], v[i]);
-            }
-          }
-        }
-        if (ncols == cw) {
-          // full chunk: stage (128-byte swizzle) and bulk-store the 128 x cw box
+        const bool full_chunk = ncols == cw;
+        const uint32_t buf = stg_addr + (sidx & 1) * kStgBytes;
+        if (full_chunk) {
+          // the staging buffer is free once the bulk store two chunks back has read it
           if (sidx >= 2 && elected) bulk_wait_read_le1();
           named_bar_sync(1, 128);
-          const uint32_t buf = stg_addr + (sidx & 1) * kStgBytes;
+        }
+        // 32 columns at a time: TMEM -> registers -> bias / FP32 adapters -> staging
+#pragma unroll 1
+        for (int sub = 0; sub < cw / 32; ++sub) {
+          const int c0 = sub * 32;                          // first column of the sub-chunk
+          float v[32];
+          if (any_mma) {
+            uint32_t r[32];
+            tmem_ld32(acc_t + lane_base + c * cw + c0, r);
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            uint32_t w0, w1, w2, w3;
-            if (cw == 64) {
-              w0 = pack_bf16x2(v[8 * u], v[8 * u + 1]);
-              w1 = pack_bf16x2(v[8 * u + 2], v[8 * u + 3]);
-              w2 = pack_bf16x2(v[8 * u + 4], v[8 * u + 5]);
-              w3 = pack_bf16x2(v[8 * u + 6], v[8 * u + 7]);
-            } else {
-              w0 = f2u(v[4 * u]); w1 = f2u(v[4 * u + 1]); w2 = f2u(v[4 * u + 2]); w3 = f2u(v[4 * u + 3]);
+            for (int i = 0; i < 32; ++i) v[i] = u2f(r[i]);
+            if (c == nchunk - 1 && sub == cw / 32 - 1) {
+              // the accumulator is fully in registers: hand it back to the MMA
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster(acc_empty_l[b]);
             }
-            st_shared_v4(buf + row_in_cta * 128 + ((u ^ (row_in_cta & 7)) * 16), w0, w1, w2, w3);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
           }
+          const int nc = min(32, ncols - c0);               // valid columns of the sub-chunk
+          if (p.bias && nc > 0) {
+            if (p.bias_f32) {
+              const float* bp = static_cast<const float*>(p.bias) + gcol + c0;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < nc) v[i] += bp[i];
+            } else {
+              const uint16_t* bp = static_cast<const uint16_t*>(p.bias) + gcol + c0;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < nc) v[i] += bf16_to_f32(bp[i]);
+            }
+          }
+          if (p.n_ad32 > 0 && row_ok && nc > 0) {
+            for (int a = 0; a < p.n_ad32; ++a) {
+              if (p.ad32[a].group != t.g) continue;
+              const float* hrow = p.h32 + static_cast<long long>(row) * p.h32_cols + p.ad32[a].h_off;
+              const float* Bm = p.ad32[a].B + static_cast<long long>(cig + c0) * p.ad32[a].ldb;
+              const long long ldb = p.ad32[a].ldb;
+              for (int jj = 0; jj < p.ad32[a].rank; ++jj) {
+                const float h = hrow[jj];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (i < nc) v[i] = fmaf(h, Bm[i * ldb + jj], v[i]);
+              }
+            }
+          }
+          if (full_chunk) {
+            // four (bf16) or eight (fp32) 16-byte units of this row, 128-byte swizzled
+            const uint32_t rowb = buf + row_in_cta * 128;
+            if (cw == 64) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                st_shared_v4(rowb + (((sub * 4 + u) ^ (row_in_cta & 7)) * 16),
+                             pack_bf16x2(v[8 * u], v[8 * u + 1]), pack_bf16x2(v[8 * u + 2], v[8 * u + 3]),
+                             pack_bf16x2(v[8 * u + 4], v[8 * u + 5]), pack_bf16x2(v[8 * u + 6], v[8 * u + 7]));
+            } else {
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                st_shared_v4(rowb + ((u ^ (row_in_cta & 7)) * 16), f2u(v[4 * u]), f2u(v[4 * u + 1]),
+                             f2u(v[4 * u + 2]), f2u(v[4 * u + 3]));
+            }
+          } else if (row_ok && nc > 0) {
+            // partial chunk at the end of a group: plain stores, masked
+            if (p.y_f32) {
+              float* y = static_cast<float*>(p.Y) + static_cast<long long>(row) * p.ldy + gcol + c0;
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (i * 4 < nc)
+                  st_global_v4_hint(y + i * 4, f2u(v[4 * i]), f2u(v[4 * i + 1]), f2u(v[4 * i + 2]),
+                                    f2u(v[4 * i + 3]), stream_out);
+            } else {
+              uint16_t* y = static_cast<uint16_t*>(p.Y) + static_cast<long long>(row) * p.ldy + gcol + c0;
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                if (i * 8 < nc)
+                  st_global_v4_hint(y + i * 8, pack_bf16x2(v[8 * i], v[8 * i + 1]),
+                                    pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                    pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                                    pack_bf16x2(v[8 * i + 6], v[8 * i + 7]), stream_out);
+            }
+          }
+        }
+        if (full_chunk) {
           fence_proxy_async_smem();
           named_bar_sync(1, 128);
           if (elected) {
@@ -492,25 +560,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bulk_commit();
           }
           ++sidx;
-        } else if (row_ok) {
-          // partial chunk at the end of a group: plain stores, masked
-          if (p.y_f32) {
-            float* y = static_cast<float*>(p.Y) + static_cast<long long>(row) * p.ldy + gcol;
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (i * 4 < ncols)
-                st_global_v4_hint(y + i * 4, f2u(v[4 * i]), f2u(v[4 * i + 1]), f2u(v[4 * i + 2]),
-                                  f2u(v[4 * i + 3]), stream_out);
-          } else {
-            uint16_t* y = static_cast<uint16_t*>(p.Y) + static_cast<long long>(row) * p.ldy + gcol;
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (i * 8 < ncols)
-                st_global_v4_hint(y + i * 8, pack_bf16x2(v[8 * i], v[8 * i + 1]),
-                                  pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                                  pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
-                                  pack_bf16x2(v[8 * i + 6], v[8 * i + 7]), stream_out);
-          }
         }
       }
       if (any_mma) {
@@ -519,6 +568,89 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     if (elected) bulk_wait_all();
+  } else if (kNF4) {
+    // ------------------------------------------------------------ 4-bit dequantisation
+    // Thread d of 256 owns row d/2 of this CTA's 128 weight rows and half (32 elements) of
+    // each 64-element K step.  For every (row, K step) -- one 64-element absmax block --
+    // it builds the 16 bf16 values bf16(fl32(level[i]) * absmax) in registers, split into
+    // low-byte and high-byte planes, and looks its codes up four at a time with byte
+    // permutes; the result is written in the 128-byte swizzle K-major layout.
+    const int d = threadIdx.x - 192;
+    const int r = d >> 1;
+    const int hh = d & 1;
+    const uint32_t wfull_l[kWRing] = {mapa_shared(smem_u32(&wfull[0]), 0),
+                                      mapa_shared(smem_u32(&wfull[1]), 0),
+                                      mapa_shared(smem_u32(&wfull[2]), 0)};
+    float lv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) lv[i] = p.nf4_code[i];
+    const int kb64 = p.K / 64;
+    int stage = 0;
+    uint32_t phase = 0;
+    int wb = 0;
+    uint32_t wphase = 0;
+    bool ok = true;
+    for (int L = 0, chunk = pair, c_end = 0; ok; ++L) {
+      if (L >= c_end) {
+        if (chunk >= nchunks) break;
+        L = chunk * CH;
+        c_end = min(L + CH, p.total_tiles);
+        chunk += npairs;
+      }
+      const Tile t = decode_tile(p, L);
+      const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
+      const bool lora = a1 > a0;
+      const int wrow = t.g * p.out_g + t.j * kBN + static_cast<int>(cta) * 128 + r;
+      const bool wrow_ok = wrow < p.N;
+      const float* am_row = p.absmax + static_cast<long long>(wrow_ok ? wrow : 0) * kb64;
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const float am = wrow_ok ? __ldg(am_row + kb) : 0.f;
+        ok = mbar_wait(&raw_full[stage], phase, abort_flag, tmo, status);
+        ok = ok && mbar_wait_cluster(&wempty[wb], wphase ^ 1, abort_flag, tmo, status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        // table: entries 2k, 2k+1 packed in e[k]; byte planes lo/hi of entries 4j..4j+3
+        uint32_t e[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) e[k] = pack_bf16x2(lv[2 * k] * am, lv[2 * k + 1] * am);
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          lo[j] = prmt(e[2 * j], e[2 * j + 1], 0x6420u);
+          hi[j] = prmt(e[2 * j], e[2 * j + 1], 0x7531u);
+        }
+        const uint8_t* codes = sbase + stage * SB + kATileBytes + r * 32 + hh * 16;
+        const uint4 cw4 = *reinterpret_cast<const uint4*>(codes);
+        const uint32_t cwords[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
+        const uint32_t dst = smem_u32(wring) + wb * kBHalfBytes + r * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          // 4 bytes = 8 codes, element 2k in the high nibble of byte k: swap nibbles so
+          // that nibble i holds element i
+          const uint32_t c = cwords[u];
+          const uint32_t s = ((c >> 4) & 0x0F0F0F0Fu) | ((c & 0x0F0F0F0Fu) << 4);
+          uint32_t o0, o1, o2, o3;
+          lookup4(s & 0xFFFFu, lo, hi, o0, o1);
+          lookup4(s >> 16, lo, hi, o2, o3);
+          const int unit = hh * 4 + u;                    // 16-byte unit = 8 elements
+          st_shared_v4(dst + ((unit ^ (r & 7)) * 16), o0, o1, o2, o3);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(wfull_l[wb]);
+        if (++stage == S) { stage = 0; phase ^= 1; }
+        if (++wb == kWRing) { wb = 0; wphase ^= 1; }
+      }
+      if (!ok) break;
+      if (lora) {
+        // the second-contraction stages carry no codes; the producer still arrives on
+        // their code barrier, and waiting here keeps every stage's phase count exact
+        for (int a = a0; a < a1 && ok; ++a)
+          for (int c = 0; c < p.ad[a].nchunks && ok; ++c) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&raw_full[stage], phase, abort_flag, tmo, status));
+            if (++stage == S) { stage = 0; phase ^= 1; }
+          }
+      }
+    }
   }
 
   tc_fence_before();
@@ -533,11 +665,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 namespace {
 
+template <bool kNF4>
 cudaLaunchConfig_t pair_config(int grid, size_t smem_bytes, cudaStream_t stream,
                                cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(kNF4 ? kTcThreadsNF4 : kTcThreads);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -549,51 +682,65 @@ cudaLaunchConfig_t pair_config(int grid, size_t smem_bytes, cudaStream_t stream,
   return cfg;
 }
 
-}  // namespace
-
-int tc_max_pairs(size_t smem_bytes) {
-  static size_t cached_smem = 0;
-  static int cached = 0;
-  static int cached_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (cached_smem == smem_bytes && cached_dev == dev && cached > 0) return cached;
-  cudaError_t e = cudaFuncSetAttribute(tc_fused_fwd_kernel,
+template <bool kNF4>
+int max_pairs_impl(size_t smem_bytes) {
+  cudaError_t e = cudaFuncSetAttribute(tc_fused_fwd_kernel<kNF4>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   if (e != cudaSuccess) {
     set_last_cuda_error(e);
     return 0;
   }
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pair_config(2 * 256, smem_bytes, nullptr, attr);
+  cudaLaunchConfig_t cfg = pair_config<kNF4>(2 * 256, smem_bytes, nullptr, attr);
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, tc_fused_fwd_kernel, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, tc_fused_fwd_kernel<kNF4>, &cfg);
   if (e != cudaSuccess || n <= 0) {
     if (e != cudaSuccess) set_last_cuda_error(e);
     n = device_sm_count() / 2;
   }
-  cached_smem = smem_bytes;
-  cached = n;
-  cached_dev = dev;
   return n;
 }
 
-int launch_tc_fwd(const TcMaps& maps, const TcParams& p, int grid, size_t smem_bytes,
-                  cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(tc_fused_fwd_kernel,
+template <bool kNF4>
+int launch_impl(const TcMaps& maps, const TcParams& p, int grid, size_t smem_bytes,
+                cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(tc_fused_fwd_kernel<kNF4>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   if (e != cudaSuccess) {
     set_last_cuda_error(e);
     return WP_ERR_CUDA;
   }
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pair_config(grid, smem_bytes, stream, attr);
-  e = cudaLaunchKernelEx(&cfg, tc_fused_fwd_kernel, maps, p);
+  cudaLaunchConfig_t cfg = pair_config<kNF4>(grid, smem_bytes, stream, attr);
+  e = cudaLaunchKernelEx(&cfg, tc_fused_fwd_kernel<kNF4>, maps, p);
   if (e != cudaSuccess) {
     set_last_cuda_error(e);
     return WP_ERR_CUDA;
   }
   return WP_OK;
+}
+
+}  // namespace
+
+int tc_max_pairs(size_t smem_bytes, bool nf4) {
+  static size_t cached_smem[2] = {0, 0};
+  static int cached[2] = {0, 0};
+  static int cached_dev[2] = {-1, -1};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int k = nf4 ? 1 : 0;
+  if (cached_smem[k] == smem_bytes && cached_dev[k] == dev && cached[k] > 0) return cached[k];
+  const int n = nf4 ? max_pairs_impl<true>(smem_bytes) : max_pairs_impl<false>(smem_bytes);
+  cached_smem[k] = smem_bytes;
+  cached[k] = n;
+  cached_dev[k] = dev;
+  return n;
+}
+
+int launch_tc_fwd(const TcMaps& maps, const TcParams& p, int grid, size_t smem_bytes,
+                  cudaStream_t stream, bool nf4) {
+  return nf4 ? launch_impl<true>(maps, p, grid, smem_bytes, stream)
+             : launch_impl<false>(maps, p, grid, smem_bytes, stream);
 }
 
 int tc_fwd_status(int reset) {
