@@ -38,7 +38,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // (elements), 128-byte swizzled boxes of {box_inner, box_outer}; out-of-range
 // elements read as zero.
 int make_map(CUtensorMap* m, int dtype, const void* ptr, long long inner, long long outer,
-             long long ld, int box_inner, int box_outer) {
+             long long ld, int box_inner, int box_outer, bool swizzle128 = true) {
   auto fn = encode_fn();
   if (!fn) {
     g_last_error = "cuTensorMapEncodeTiled unavailable";
@@ -51,7 +51,8 @@ int make_map(CUtensorMap* m, int dtype, const void* ptr, long long inner, long l
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, dtype == WP_FP32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                   2, const_cast<void*>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char buf[96];
@@ -304,6 +305,12 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     rc = make_map_u8(&maps.wq, W->data, K / 2, N, K / 2, kBK / 2, 128);
     if (rc != WP_OK) return rc;
     p.absmax = W->absmax;
+    // block scales [N, K/64] by TMA when a row of them is a multiple of 16 bytes
+    p.am_tma = (K % 256 == 0 && aligned16(W->absmax)) ? 1 : 0;
+    if (p.am_tma) {
+      rc = make_map(&maps.am, WP_FP32, W->absmax, K / 64, N, K / 64, 4, 128, /*swizzle128=*/false);
+      if (rc != WP_OK) return rc;
+    }
     nf4_codebook_host(p.nf4_code);
   } else if (W) {
     rc = make_map_bf16(&maps.w, W->data, K, N, W->ld, kBK, 128);
@@ -320,7 +327,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   }
 
   // stage: X rows | bf16 W half (or 4-bit codes, padded to 4 KiB) | rank slot
-  p.rslot_off = kATileBytes + (nf4 ? kRawBytes : kBHalfBytes);
+  p.rslot_off = kATileBytes + (nf4 ? kRawBytes + kAmBytes : kBHalfBytes);
   p.stage_bytes = p.rslot_off + p.rslot_rows * 128;
   const size_t fixed = 1024 + (nf4 ? static_cast<size_t>(kWRing) * kBHalfBytes : 0) +
                        static_cast<size_t>(p.hchunks) * kHChunkBytes + 2 * kStgBytes + 512;

@@ -29,6 +29,7 @@ constexpr int kStgBytes = kBM * 128;            // output staging: 128 rows x 12
 constexpr int kTcThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kTcThreadsNF4 = 448;  // + warps 6..13: 4-bit dequantisation
 constexpr int kRawBytes = 128 * 32;             // 4-bit codes of 128 rows x 64 K per stage
+constexpr int kAmBytes = 128 * 4 * 4;           // block scales of 128 rows x 4 K steps
 constexpr int kWRing = 3;                       // dequantised weight tiles in flight
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 227 * 1024;
@@ -65,6 +66,7 @@ struct TcParams {
   int stage_bytes;             // bf16 W: 32 KiB + rank slot; 4-bit W: 16 KiB + 4 KiB codes + rank slot
   int rslot_off;               // byte offset of the rank slot inside a stage
   const float* absmax;         // 4-bit W: [N * K / 64] fp32 block scales
+  int am_tma;                  // 4-bit W: block scales arrive by TMA with the codes
   float nf4_code[16];          // 4-bit W: the NormalFloat levels
   TcAdapter ad[kMaxAd];
   int n_ad32;                  // fp32 adapters (epilogue FFMA)
@@ -84,6 +86,7 @@ struct TcMaps {
   CUtensorMap w;
   CUtensorMap y;                 // output, 128-byte swizzled boxes of 128 rows
   CUtensorMap wq;                // 4-bit W codes: [N rows, K/2 bytes], boxes of 128 x 32 bytes
+  CUtensorMap am;                // 4-bit W block scales: [N rows, K/64] fp32, boxes of 128 x 4
   CUtensorMap a[kMaxAd];
   CUtensorMap b[kMaxAd];
 };

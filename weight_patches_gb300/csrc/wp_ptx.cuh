@@ -126,6 +126,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Arrive on another CTA's mbarrier with the default (release, CTA-scope) semantics.  For
+// shared-memory tiles that a tensor-core MMA of the pair reads after the waiter observes
+// the phase, the writer's fence.proxy.async before this arrive is the ordering that
+// matters; a cluster-scope release additionally drains every outstanding memory
+// operation of the thread and costs close to a microsecond per arrive.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
   asm volatile(
       "barrier.cluster.arrive.release.aligned;\n\t"

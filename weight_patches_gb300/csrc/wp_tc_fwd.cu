@@ -72,18 +72,21 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// Four 4-bit codes (nibble i of `sel4` is the code of element i) -> four bf16 values
-// from a 16-entry table split into byte planes: lo[j] / hi[j] hold the low / high bytes
-// of entries 4j..4j+3.  Returns two words: elements (0,1) and (2,3).
-__device__ __forceinline__ void lookup4(uint32_t sel4, const uint32_t (&lo)[4], const uint32_t (&hi)[4],
+// Four 4-bit codes -> four bf16 values from a 16-entry table split into byte planes:
+// lo[j] / hi[j] hold the low / high bytes of entries 4j..4j+3.  `codes` is 16 bits of the
+// packed stream as stored (byte k: element 2k in the high nibble), so its nibbles, low
+// to high, are the codes of elements 1, 0, 3, 2.  Each plane is looked up in both
+// half-tables (3-bit byte selects); a fourth permute keeps, per byte, the half the code's
+// bit 3 points at; the last two permutes interleave the planes back into element order.
+// Returns the words holding elements (0, 1) and (2, 3).
+__device__ __forceinline__ void lookup4(uint32_t codes, const uint32_t (&lo)[4], const uint32_t (&hi)[4],
                                         uint32_t& out01, uint32_t& out23) {
-  const uint32_t sel3 = sel4 & 0x7777u;                  // byte index within a half-table
-  const uint32_t x = (sel4 >> 3) & 0x1111u;              // 1 where the code is >= 8
-  const uint32_t m = ((x & 0x1u) | ((x & 0x10u) << 4) | ((x & 0x100u) << 8) | ((x & 0x1000u) << 12)) * 0xFFu;
-  const uint32_t l = (prmt(lo[0], lo[1], sel3) & ~m) | (prmt(lo[2], lo[3], sel3) & m);
-  const uint32_t h = (prmt(hi[0], hi[1], sel3) & ~m) | (prmt(hi[2], hi[3], sel3) & m);
-  out01 = prmt(l, h, 0x5140u);
-  out23 = prmt(l, h, 0x7362u);
+  const uint32_t sel3 = codes & 0x7777u;
+  const uint32_t pick = 0x3210u | ((codes >> 1) & 0x4444u);     // byte i from the upper half-table if code >= 8
+  const uint32_t l = prmt(prmt(lo[0], lo[1], sel3), prmt(lo[2], lo[3], sel3), pick);
+  const uint32_t h = prmt(prmt(hi[0], hi[1], sel3), prmt(hi[2], hi[3], sel3), pick);
+  out01 = prmt(l, h, 0x4051u);
+  out23 = prmt(l, h, 0x6273u);
 }
 
 constexpr uint16_t kBothCtas = 0x3;
@@ -202,8 +205,11 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               if (kNF4) {
                 // this CTA's codes complete on its own barrier; the dequantisation warps
                 // turn them into the bf16 tile the MMA reads
-                mbar_arrive_expect_tx(&raw_full[stage], kRawBytes);
+                mbar_arrive_expect_tx(&raw_full[stage], kRawBytes + (p.am_tma ? kAmBytes : 0));
                 tma_load_2d(st + kATileBytes, &maps.wq, kb * (kBK / 2), w_row, &raw_full[stage]);
+                // the block scales of this K step and the next three (16-byte boxes)
+                if (p.am_tma)
+                  tma_load_2d(st + kATileBytes + kRawBytes, &maps.am, kb & ~3, w_row, &raw_full[stage]);
               } else {
                 tma_load_2d_pair_hint(st + kATileBytes, &maps.w, kb * kBK, w_row, fb, keep);
               }
@@ -604,10 +610,15 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       const bool wrow_ok = wrow < p.N;
       const float* am_row = p.absmax + static_cast<long long>(wrow_ok ? wrow : 0) * kb64;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
-        const float am = wrow_ok ? __ldg(am_row + kb) : 0.f;
         ok = mbar_wait(&raw_full[stage], phase, abort_flag, tmo, status);
         ok = ok && mbar_wait_cluster(&wempty[wb], wphase ^ 1, abort_flag, tmo, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        // block scale: from the stage (TMA, no global load left in flight when this warp
+        // releases the tile to the peer CTA) or, for K % 256 != 0, straight from memory
+        const float am = p.am_tma
+                             ? reinterpret_cast<const float*>(sbase + stage * SB + kATileBytes +
+                                                              kRawBytes)[r * 4 + (kb & 3)]
+                             : (wrow_ok ? __ldg(am_row + kb) : 0.f);
         // table: entries 2k, 2k+1 packed in e[k]; byte planes lo/hi of entries 4j..4j+3
         uint32_t e[8];
 #pragma unroll
@@ -624,19 +635,17 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         const uint32_t dst = smem_u32(wring) + wb * kBHalfBytes + r * 128;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          // 4 bytes = 8 codes, element 2k in the high nibble of byte k: swap nibbles so
-          // that nibble i holds element i
+          // 4 bytes = 8 codes of consecutive elements
           const uint32_t c = cwords[u];
-          const uint32_t s = ((c >> 4) & 0x0F0F0F0Fu) | ((c & 0x0F0F0F0Fu) << 4);
           uint32_t o0, o1, o2, o3;
-          lookup4(s & 0xFFFFu, lo, hi, o0, o1);
-          lookup4(s >> 16, lo, hi, o2, o3);
+          lookup4(c & 0xFFFFu, lo, hi, o0, o1);
+          lookup4(c >> 16, lo, hi, o2, o3);
           const int unit = hh * 4 + u;                    // 16-byte unit = 8 elements
           st_shared_v4(dst + ((unit ^ (r & 7)) * 16), o0, o1, o2, o3);
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(wfull_l[wb]);
+        if (lane == 0) mbar_arrive_remote(wfull_l[wb]);
         if (++stage == S) { stage = 0; phase ^= 1; }
         if (++wb == kWRing) { wb = 0; wphase ^= 1; }
       }
