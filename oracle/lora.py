@@ -113,20 +113,38 @@ def linear_bwd(X: np.ndarray, W: np.ndarray, dY: np.ndarray,
         dA_g = s_g G_g^T X
         dB_g = s_g dY_g^T (X A_g^T)
     """
+    dX = grad_X(X, W, dY, group_patches, request_scale)
+    dA, dB = grad_AB(X, dY, group_patches, request_scale)
+    return Grads(dX, dA, dB)
+
+
+def grad_X(X: np.ndarray, W: np.ndarray, dY: np.ndarray, group_patches: Sequence[DecodedPatch],
+           request_scale: float) -> np.ndarray:
+    """dX = sum_g dY_g W_g + s_g (dY_g B_g) A_g (rows of dX depend only on the same rows of
+    dY, so it may be evaluated on any subset of token rows)."""
     G = len(group_patches)
-    out = W.shape[0]
-    og = out // G
-    dX = np.zeros_like(X)
+    og = W.shape[0] // G
+    dX = np.zeros((dY.shape[0], W.shape[1]))
+    for g, p in enumerate(group_patches):
+        s = combined_scale(p.alpha, p.rank, p.strength, request_scale)
+        dYg = dY[:, g * og:(g + 1) * og]
+        dX = dX + dYg @ W[g * og:(g + 1) * og] + s * ((dYg @ p.B) @ p.A)
+    return dX
+
+
+def grad_AB(X: np.ndarray, dY: np.ndarray, group_patches: Sequence[DecodedPatch],
+            request_scale: float):
+    """dA_g = s_g (dY_g B_g)^T X and dB_g = s_g dY_g^T (X A_g^T).  Both are sums over token
+    rows, so the results of disjoint row sets add up to the result of their union."""
+    G = len(group_patches)
+    og = dY.shape[1] // G
     dA, dB = [], []
     for g, p in enumerate(group_patches):
         s = combined_scale(p.alpha, p.rank, p.strength, request_scale)
         dYg = dY[:, g * og:(g + 1) * og]
-        Wg = W[g * og:(g + 1) * og]
-        Gg = dYg @ p.B
-        dX = dX + dYg @ Wg + s * (Gg @ p.A)
-        dA.append(s * (Gg.T @ X))
+        dA.append(s * ((dYg @ p.B).T @ X))
         dB.append(s * (dYg.T @ (X @ p.A.T)))
-    return Grads(dX, dA, dB)
+    return dA, dB
 
 
 def unfused_bf16_chain(X: np.ndarray, W: Optional[np.ndarray], bias: Optional[np.ndarray],

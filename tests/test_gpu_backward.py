@@ -1,0 +1,95 @@
+"""GPU parity of the closed-form backward (dX, dA, dB) against the FP64 oracle.
+
+dX goes through the bf16 tensor-core kernel (relative RMS <= 4e-3); dA and dB are fp32
+reductions over tokens of exact bf16 inputs and fp32 intermediates, held to 1e-4."""
+import numpy as np
+import pytest
+import torch
+
+import weight_patches_gb300 as wpg
+import workloads
+from oracle import lora as olora
+from oracle.numerics import relative_rms, to_f64
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+DX_TOL = 4e-3
+DAB_TOL = 1e-4
+
+
+def _run(lin, need_dX=True, dX_dtype=torch.bfloat16):
+    X, W, dY = gu.dev(lin.X), gu.dev(lin.W), gu.dev(lin.dY)
+    ads = gu.adapters(lin)
+    dX, dA, dB = wpg.lora_linear_bwd(X, W, dY, ads, lin.request_scale, need_dX=need_dX, dX_dtype=dX_dtype)
+    torch.cuda.synchronize()
+    assert wpg.lora_device_status() == 0
+    return dX, dA, dB
+
+
+def _check_full(lin, dX, dA, dB, dx_tol=DX_TOL):
+    X, W, _, patches = olora.decode_linear(lin)
+    g = olora.linear_bwd(X, W, to_f64(lin.dY), patches, lin.request_scale)
+    if dX is not None:
+        err = relative_rms(gu.to_f64(dX), g.dX)
+        assert err <= dx_tol, err
+    for i in range(len(patches)):
+        ea = relative_rms(dA[i].double().cpu().numpy(), g.dA[i])
+        eb = relative_rms(dB[i].double().cpu().numpy(), g.dB[i])
+        assert ea <= DAB_TOL and eb <= DAB_TOL, (i, ea, eb)
+
+
+def _with_dY(lin, seed):
+    rng = np.random.default_rng(seed)
+    lin.dY = workloads.draw(rng, lin.T, lin.W.rows, 1.0)
+    return lin
+
+
+def test_bwd_bf16_single_group():
+    lin = _with_dY(workloads.config2("small")[0], 21)    # 192 -> 520, rank 64, s = 0.35
+    lin.bias = None
+    dX, dA, dB = _run(lin)
+    _check_full(lin, dX, dA, dB)
+
+
+def test_bwd_bf16_grouped_and_fp32_dX():
+    lin = _with_dY(workloads.config1("small"), 22)        # 3 groups of 320, rank 32
+    dX, dA, dB = _run(lin, dX_dtype=torch.float32)
+    _check_full(lin, dX, dA, dB, dx_tol=2e-3)
+
+
+def test_bwd_without_dX():
+    lin = _with_dY(workloads.config1("small"), 23)
+    dX, dA, dB = _run(lin, need_dX=False)
+    assert dX is None
+    _check_full(lin, None, dA, dB)
+
+
+def test_bwd_nf4_small():
+    gate_up, down = workloads.config3("small")
+    for lin in (gate_up, down):
+        dX, dA, dB = _run(lin)
+        _check_full(lin, dX, dA, dB)
+
+
+def test_bwd_nf4_full_sampled():
+    gate_up, _ = workloads.config3("full")
+    lin = gate_up
+    dX, dA, dB = _run(lin)
+    X, W, _, patches = olora.decode_linear(lin)
+    rows = workloads.sample_rows(lin.T, 48)
+    from oracle.numerics import bf16_bits_to_f64
+    dY_rows = bf16_bits_to_f64(lin.dY.data[rows])
+    want_dX = olora.grad_X(X[rows], W, dY_rows, patches, lin.request_scale)
+    assert relative_rms(gu.to_f64(dX)[rows], want_dX) <= DX_TOL
+    # dA, dB: sums over all tokens, accumulated over row chunks
+    sumA = [0.0] * len(patches)
+    sumB = [0.0] * len(patches)
+    for r0 in range(0, lin.T, 1024):
+        sl = slice(r0, min(lin.T, r0 + 1024))
+        a, b = olora.grad_AB(X[sl], bf16_bits_to_f64(lin.dY.data[sl]), patches, lin.request_scale)
+        sumA = [x + y for x, y in zip(sumA, a)]
+        sumB = [x + y for x, y in zip(sumB, b)]
+    for i in range(len(patches)):
+        assert relative_rms(dA[i].double().cpu().numpy(), sumA[i]) <= DAB_TOL
+        assert relative_rms(dB[i].double().cpu().numpy(), sumB[i]) <= DAB_TOL

@@ -3,6 +3,7 @@
 // Every entry point validates on the host and launches nothing when it rejects a
 // call.  The library never allocates device memory and never synchronises; all work
 // is enqueued on the caller's stream.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -147,7 +148,8 @@ size_t fwd_workspace(const wp_mat* X, const FwdPlan& plan) {
 
 int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool grouped,
              const wp_adapter* adapters, int n_adapters, double request_scale, const wp_out* Y,
-             void* workspace, size_t ws_bytes, cudaStream_t stream) {
+             void* workspace, size_t ws_bytes, cudaStream_t stream, float* h_out = nullptr,
+             int h_out_ld = 0) {
   if (!valid_input(X, false)) return WP_ERR_INVALID;
   if (W && !valid_input(W, true)) return WP_ERR_INVALID;
   if (!valid_output(Y)) return WP_ERR_INVALID;
@@ -253,6 +255,13 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   hp.T = p.T; hp.K = p.K; hp.X = X->data; hp.x_dtype = WP_BF16; hp.ldx = X->ld;
   int src_of[kMaxAd];
   int h_off = 0;
+  int hout_of[kMaxAd + kMaxAd32];          // column of adapter i in h_out: ranks of 0..i-1
+  for (int i = 0, acc = 0; i < n_adapters; ++i) {
+    hout_of[i] = acc;
+    acc += static_cast<int>(adapters[i].A.rows);
+  }
+  p.h_out = h_out;
+  p.h_out_ld = h_out_ld;
   for (int g = 0; g < G; ++g) {
     p.ad_begin[g] = p.n_ad;
     int chunk = 0;
@@ -281,6 +290,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
       d.group = g; d.rank = r; d.rpad16 = (r + 15) / 16 * 16; d.chunk_off = chunk;
       d.nchunks = (r + 63) / 64; d.s = s_of[i];
       d.roff = roff;
+      d.hout_off = hout_of[i];
       chunk += d.nchunks;
       roff += d.rpad16 / 2;
       if (chunk * 64 > kHCols) return WP_ERR_UNSUPPORTED;
@@ -348,6 +358,200 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   return launch_tc_fwd(maps, p, 2 * pairs, smem, stream, nf4);
 }
 
+// ------------------------------------------------------------------ backward
+// Workspace of lora_linear_bwd, in order (each region 256-byte aligned):
+//   W^T [in, Ntot] bf16 | per group: B_g^T padded to [r_g, Ntot] bf16 | per group: A_g^T
+//   [in, r8_g] bf16 | s G [T, R] fp32 | H [T, R] fp32 | reduction partials
+struct BwdLayout {
+  size_t wt, bhat[kMaxGroups], at[kMaxGroups], gs, h, part, total;
+  int r8[kMaxGroups];
+  int roff[kMaxGroups];
+  int R;
+};
+
+bool bwd_layout(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int G, BwdLayout* L) {
+  if (!X || !W || !ad || G < 1 || G > kMaxGroups) return false;
+  const size_t T = static_cast<size_t>(X->rows), K = static_cast<size_t>(X->cols);
+  const size_t Ntot = static_cast<size_t>(W->rows);
+  if (Ntot % G) return false;
+  const size_t og = Ntot / G;
+  size_t off = 0;
+  L->wt = off;
+  off += round256(K * Ntot * 2);
+  int R = 0;
+  size_t max_part = 0;
+  for (int g = 0; g < G; ++g) {
+    const int r = static_cast<int>(ad[g].A.rows);
+    if (r <= 0) return false;
+    L->r8[g] = (r + 7) / 8 * 8;
+    L->roff[g] = R;
+    R += r;
+    L->bhat[g] = off;
+    off += round256(static_cast<size_t>(r) * Ntot * 2);
+  }
+  for (int g = 0; g < G; ++g) {
+    L->at[g] = off;
+    off += round256(K * L->r8[g] * 2);
+  }
+  L->R = R;
+  L->gs = off;
+  off += round256(T * R * 4);
+  L->h = off;
+  off += round256(T * R * 4);
+  for (int g = 0; g < G; ++g) {
+    const size_t r = static_cast<size_t>(ad[g].A.rows);
+    const int Tn = static_cast<int>(T);
+    const size_t pa = static_cast<size_t>(skinny_chunks(Tn, static_cast<int>(K))) * K * r;
+    const size_t pb = static_cast<size_t>(skinny_chunks(Tn, static_cast<int>(og))) * og * r;
+    max_part = std::max(max_part, std::max(pa, pb));
+  }
+  L->part = off;
+  off += round256(max_part * 4);
+  L->total = off;
+  return true;
+}
+
+int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp_adapter* ad,
+             double request_scale, const wp_out* dX, const wp_out* dA, const wp_out* dB,
+             void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (!valid_input(X, false) || !valid_input(W, true) || !valid_input(dY, false)) return WP_ERR_INVALID;
+  if (!ad || !dA || !dB || G < 1 || G > kMaxGroups) return WP_ERR_INVALID;
+  if (!std::isfinite(request_scale)) return WP_ERR_INVALID;
+  if (X->dtype != WP_BF16 || dY->dtype != WP_BF16) return WP_ERR_DTYPE;
+  if (W->dtype != WP_BF16 && W->dtype != WP_NF4) return WP_ERR_DTYPE;
+  const long long T = X->rows, K = X->cols, Ntot = W->rows;
+  if (W->cols != K || dY->rows != T || dY->cols != Ntot || Ntot % G) return WP_ERR_SHAPE;
+  if (W->dtype == WP_NF4 && (K % 64 || W->ld != K)) return WP_ERR_SHAPE;
+  const long long og = Ntot / G;
+  if (K % 8 || og % 8 || Ntot % 8) return WP_ERR_ALIGN;
+  if (!aligned16(X->data) || X->ld % 8 || !aligned16(dY->data) || dY->ld % 8) return WP_ERR_ALIGN;
+  if (T > 0x7FFFFFFFLL || K > 0x7FFFFFFFLL || Ntot > 0x7FFFFFFFLL) return WP_ERR_UNSUPPORTED;
+  if (dX) {
+    if (!valid_output(dX)) return WP_ERR_INVALID;
+    if (dX->rows != T || dX->cols != K) return WP_ERR_SHAPE;
+  }
+  float s_of[kMaxGroups];
+  int chunks = 0;
+  for (int g = 0; g < G; ++g) {
+    const wp_adapter& a = ad[g];
+    if (!valid_input(&a.A, false) || !valid_input(&a.B, false)) return WP_ERR_INVALID;
+    if (a.A.dtype != WP_BF16 || a.B.dtype != WP_BF16) return WP_ERR_DTYPE;
+    const long long r = a.A.rows;
+    if (r <= 0) return WP_ERR_INVALID;
+    if (r > 64) return WP_ERR_UNSUPPORTED;
+    if (a.A.cols != K || a.B.rows != og || a.B.cols != r) return WP_ERR_SHAPE;
+    if (!std::isfinite(a.alpha) || !std::isfinite(a.strength)) return WP_ERR_INVALID;
+    const double s = a.alpha / static_cast<double>(r) * a.strength * request_scale;
+    if (!std::isfinite(s) || !std::isfinite(static_cast<float>(s))) return WP_ERR_INVALID;
+    s_of[g] = static_cast<float>(s);
+    chunks += static_cast<int>((r + 63) / 64);
+    const wp_out& da = dA[g];
+    const wp_out& db = dB[g];
+    if (!valid_output(&da) || !valid_output(&db)) return WP_ERR_INVALID;
+    if (da.dtype != WP_FP32 || db.dtype != WP_FP32) return WP_ERR_DTYPE;
+    if (da.rows != r || da.cols != K || db.rows != og || db.cols != r) return WP_ERR_SHAPE;
+  }
+  if (chunks * 64 > kHCols) return WP_ERR_UNSUPPORTED;
+  BwdLayout L;
+  if (!bwd_layout(X, W, ad, G, &L)) return WP_ERR_INVALID;
+  if (!workspace || ws_bytes < L.total) return WP_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return WP_ERR_ALIGN;
+  if (T == 0) return WP_OK;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint16_t* Wt = reinterpret_cast<uint16_t*>(ws + L.wt);
+  float* Gs = reinterpret_cast<float*>(ws + L.gs);
+  float* H = reinterpret_cast<float*>(ws + L.h);
+  float* part = reinterpret_cast<float*>(ws + L.part);
+  int rc;
+
+  // 1. W^T [K, Ntot] bf16: the K-major B operand of dX = dY W
+  if (W->dtype == WP_NF4) {
+    NF4Table tab;
+    nf4_codebook_host(tab.level);
+    rc = launch_nf4_dequant_t(W->data, W->absmax, static_cast<int>(Ntot), static_cast<int>(K), tab,
+                              Wt, Ntot, stream);
+  } else {
+    rc = launch_transpose_bf16(W->data, W->ld, static_cast<int>(Ntot), static_cast<int>(K), Wt, Ntot,
+                               stream);
+  }
+  if (rc != WP_OK) return rc;
+
+  // 2. per group: B_g^T placed at the group's columns of a zero [r_g, Ntot] matrix (so
+  //    dY B_hat_g^T = dY_g B_g), and A_g^T [K, r8_g]
+  wp_adapter fwd_ad[kMaxGroups];
+  for (int g = 0; g < G; ++g) {
+    const wp_adapter& a = ad[g];
+    const int r = static_cast<int>(a.A.rows);
+    uint16_t* bh = reinterpret_cast<uint16_t*>(ws + L.bhat[g]);
+    uint16_t* at = reinterpret_cast<uint16_t*>(ws + L.at[g]);
+    cudaError_t e = cudaMemsetAsync(bh, 0, static_cast<size_t>(r) * Ntot * 2, stream);
+    if (e != cudaSuccess) { set_last_cuda_error(e); return WP_ERR_CUDA; }
+    rc = launch_transpose_bf16(a.B.data, a.B.ld, static_cast<int>(og), r, bh + g * og, Ntot, stream);
+    if (rc != WP_OK) return rc;
+    rc = launch_transpose_bf16(a.A.data, a.A.ld, r, static_cast<int>(K), at, L.r8[g], stream);
+    if (rc != WP_OK) return rc;
+    fwd_ad[g].A = wp_mat{bh, WP_BF16, r, Ntot, Ntot, nullptr};
+    fwd_ad[g].B = wp_mat{at, WP_BF16, K, r, L.r8[g], nullptr};
+    fwd_ad[g].alpha = a.alpha;
+    fwd_ad[g].strength = a.strength;
+  }
+
+  // 3. H = X A_g^T (fp32, for dB)
+  H32Params hp{};
+  hp.T = static_cast<int>(T); hp.K = static_cast<int>(K);
+  hp.X = X->data; hp.x_dtype = WP_BF16; hp.ldx = X->ld;
+  hp.n_ad = G; hp.H = H; hp.h_cols = L.R;
+  for (int g = 0; g < G; ++g) {
+    hp.A[g] = ad[g].A.data; hp.a_dtype[g] = WP_BF16; hp.lda[g] = ad[g].A.ld;
+    hp.rank[g] = static_cast<int>(ad[g].A.rows); hp.h_off[g] = L.roff[g]; hp.s[g] = 1.0f;
+  }
+  rc = launch_h32(hp, stream);
+  if (rc != WP_OK) return rc;
+
+  // 4. dX = dY W + sum_g s_g (dY B_g) A_g on the fused tensor-core kernel, which also
+  //    leaves s_g dY B_g (fp32) in Gs; without dX, Gs comes from the fp32 projection
+  const wp_mat Wt_m{Wt, WP_BF16, K, Ntot, Ntot, nullptr};
+  if (dX) {
+    rc = fwd_impl(dY, &Wt_m, nullptr, 1, false, fwd_ad, G, request_scale, dX, nullptr, 0, stream,
+                  Gs, L.R);
+    if (rc != WP_OK) return rc;
+  } else {
+    H32Params gp{};
+    gp.T = static_cast<int>(T); gp.K = static_cast<int>(Ntot);
+    gp.X = dY->data; gp.x_dtype = WP_BF16; gp.ldx = dY->ld;
+    gp.n_ad = G; gp.H = Gs; gp.h_cols = L.R;
+    for (int g = 0; g < G; ++g) {
+      gp.A[g] = fwd_ad[g].A.data; gp.a_dtype[g] = WP_BF16; gp.lda[g] = Ntot;
+      gp.rank[g] = static_cast<int>(ad[g].A.rows); gp.h_off[g] = L.roff[g]; gp.s[g] = s_of[g];
+    }
+    rc = launch_h32(gp, stream);
+    if (rc != WP_OK) return rc;
+  }
+
+  // 5. dA_g = (s_g G_g)^T X  and  dB_g = s_g dY_g^T H_g  (exact zeros when s_g == 0)
+  for (int g = 0; g < G; ++g) {
+    const int r = static_cast<int>(ad[g].A.rows);
+    if (s_of[g] == 0.0f) {
+      for (const wp_out* o : {&dA[g], &dB[g]}) {
+        cudaError_t e = cudaMemset2DAsync(o->data, o->ld * 4, 0, o->cols * 4, o->rows, stream);
+        if (e != cudaSuccess) { set_last_cuda_error(e); return WP_ERR_CUDA; }
+      }
+      continue;
+    }
+    rc = launch_skinny(X->data, WP_BF16, X->ld, static_cast<int>(T), static_cast<int>(K),
+                       Gs + L.roff[g], L.R, r, 1.0f, part, static_cast<float*>(dA[g].data), dA[g].ld,
+                       /*transposed=*/true, stream);
+    if (rc != WP_OK) return rc;
+    const uint16_t* dyg = static_cast<const uint16_t*>(dY->data) + g * og;
+    rc = launch_skinny(dyg, WP_BF16, dY->ld, static_cast<int>(T), static_cast<int>(og),
+                       H + L.roff[g], L.R, r, s_of[g], part, static_cast<float*>(dB[g].data), dB[g].ld,
+                       /*transposed=*/false, stream);
+    if (rc != WP_OK) return rc;
+  }
+  return WP_OK;
+}
+
 }  // namespace
 
 void set_last_cuda_error(cudaError_t e) { g_last_error = cudaGetErrorString(e); }
@@ -390,9 +594,8 @@ int lora_linear_bwd(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int32_t 
                     const wp_adapter* adapters, double request_scale, const wp_out* dX,
                     const wp_out* dA, const wp_out* dB, void* workspace,
                     size_t workspace_bytes, void* stream) {
-  (void)X; (void)W; (void)dY; (void)n_groups; (void)adapters; (void)request_scale; (void)dX;
-  (void)dA; (void)dB; (void)workspace; (void)workspace_bytes; (void)stream;
-  return WP_ERR_UNSUPPORTED;
+  return bwd_impl(X, W, dY, n_groups, adapters, request_scale, dX, dA, dB, workspace,
+                  workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 int lora_dense_patch(void* param, int32_t param_dtype, int64_t param_numel, const void* payload,
@@ -416,6 +619,10 @@ size_t lora_workspace_size(int32_t op, const wp_mat* X, const wp_mat* W,
     FwdPlan plan;
     plan_fwd(X, W, adapters, n_adapters, &plan);
     return fwd_workspace(X, plan);
+  }
+  if (op == WP_OP_BWD) {
+    BwdLayout L;
+    return bwd_layout(X, W, adapters, n_adapters, &L) ? L.total : 0;
   }
   return 0;
 }

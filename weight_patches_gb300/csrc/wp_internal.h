@@ -41,6 +41,7 @@ struct TcAdapter {
   int chunk_off;   // first 64-rank chunk of the group's rank region (TMEM col / 64, H~ buffer)
   int nchunks;     // ceil(r / 64)
   int roff;        // row offset of this CTA's rpad16/2 rows of A in a stage's rank slot
+  int hout_off;    // column of this adapter's s * X A^T in TcParams::h_out (if stored)
   float s;         // combined scale, fp32
 };
 
@@ -71,6 +72,8 @@ struct TcParams {
   TcAdapter ad[kMaxAd];
   int n_ad32;                  // fp32 adapters (epilogue FFMA)
   TcAdapter32 ad32[kMaxAd32];
+  float* h_out;                // optional [T, h_out_ld] fp32: s * X A^T of the bf16 adapters
+  int h_out_ld;
   const float* h32;            // [T, h32_cols] fp32: s * X A^T of the fp32 adapters
   int h32_cols;
   const void* bias;            // [N] or null
@@ -132,6 +135,21 @@ struct H32Params {
   float* H; int h_cols;
 };
 int launch_h32(const H32Params& p, cudaStream_t stream);
+
+// ------------------------------------------------------------------ backward helpers
+struct NF4Table {
+  float level[16];
+};
+int launch_transpose_bf16(const void* src, long long ld_s, int R, int C, void* dst, long long ld_d,
+                          cudaStream_t stream);
+int launch_nf4_dequant_t(const void* codes, const float* absmax, int N, int K, const NF4Table& tab,
+                         void* dst, long long ld_d, cudaStream_t stream);
+int skinny_chunks(int T, int M);
+// out = scale * P^T Q (M x R), or its transpose; P [T, M] bf16/fp32, Q [T, R] fp32, R <= 64;
+// `part` holds skinny_chunks(T, M) * M * R floats.
+int launch_skinny(const void* P, int p_dtype, long long ldp, int T, int M, const float* Q,
+                  long long ldq, int R, float scale, float* part, float* out, long long ldo,
+                  bool transposed, cudaStream_t stream);
 
 // ------------------------------------------------------------------ dense patch
 int launch_dense_patch(void* param, int param_dtype, const void* payload, int payload_dtype,

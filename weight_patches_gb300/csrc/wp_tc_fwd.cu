@@ -431,6 +431,16 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
                 for (int i = 0; i < 8; ++i) r[k * 8 + i] = r8[i];
               }
             }
+            if (p.h_out) {
+              // keep s * X A^T in fp32 as well (the backward needs it for dA)
+              const int row = t.m * kPairM + static_cast<int>(cta) * kBM + row_in_cta;
+              if (row < p.T) {
+                float* ho = p.h_out + static_cast<long long>(row) * p.h_out_ld + p.ad[a].hout_off;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (i < n * 8 && u0 * 8 + i < p.ad[a].rank) ho[u0 * 8 + i] = u2f(r[i]) * s;
+              }
+            }
             for (int k = 0; k < n; ++k) {
               const int u = u0 + k;
               const uint32_t* q8 = r + k * 8;
