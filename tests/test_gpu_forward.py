@@ -124,6 +124,21 @@ def test_edge_shapes(T, K, N, r):
     _gate(*gu.errors(lin, Y))
 
 
+@pytest.mark.parametrize("ranks", [(128, 64, 48), (136, 32, 8), (8, 8, 8, 8, 8), (120,), (40, 24)])
+def test_rank_mixes(ranks):
+    """Rank mixes that place whole adapters on either CTA of the pair (lopsided or even
+    halves) and ones that must split every adapter between the two halves."""
+    rng = np.random.default_rng(sum(ranks))
+    T, K, N = 520, 192, 384
+    X = workloads.draw(rng, T, K, 1.0)
+    W = workloads.draw(rng, N, K, (1.0 / K) ** 0.5)
+    patches = [workloads.Patch(workloads.draw(rng, r, K, (1.0 / K) ** 0.5), workloads.draw(rng, N, r, 0.02),
+                               float(r), 0.5 + 0.1 * i) for i, r in enumerate(ranks)]
+    lin = workloads.Linear("mix", X, W, None, patches, request_scale=1.1)
+    Y = gu.run_fwd(lin)
+    _gate(*gu.errors(lin, Y))
+
+
 def test_rank_without_aligned_pitch_is_rejected():
     X = torch.zeros(16, 64, dtype=torch.bfloat16, device=gu.DEV)
     W = torch.zeros(64, 64, dtype=torch.bfloat16, device=gu.DEV)

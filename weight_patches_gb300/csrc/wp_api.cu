@@ -262,6 +262,11 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   }
   p.h_out = h_out;
   p.h_out_ld = h_out_ld;
+  // bf16 W: one rank pass per 256-row block serves every group's adapters, packed in one
+  // rank space (16-aligned); 4-bit W: a pass per (row block, group) folded into the first
+  // tile's K loop, each group's adapters at 64-rank chunks of their own.
+  p.hpass = nf4 ? 0 : 1;
+  int hglob = 0;
   for (int g = 0; g < G; ++g) {
     p.ad_begin[g] = p.n_ad;
     int chunk = 0;
@@ -287,22 +292,72 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
       if (!aligned16(a.A.data) || a.A.ld % 8 || !aligned16(a.B.data) || a.B.ld % 8)
         return WP_ERR_ALIGN;
       TcAdapter& d = p.ad[p.n_ad];
-      d.group = g; d.rank = r; d.rpad16 = (r + 15) / 16 * 16; d.chunk_off = chunk;
+      d.group = g; d.rank = r; d.rpad16 = (r + 15) / 16 * 16;
       d.nchunks = (r + 63) / 64; d.s = s_of[i];
-      d.roff = roff;
       d.hout_off = hout_of[i];
-      chunk += d.nchunks;
-      roff += d.rpad16 / 2;
-      if (chunk * 64 > kHCols) return WP_ERR_UNSUPPORTED;
+      if (p.hpass) {
+        d.toff = hglob;                 // H~ columns: packed in adapter order
+        d.roff = 0;
+        hglob += d.rpad16;
+        if (hglob > kHCols) return WP_ERR_UNSUPPORTED;
+      } else {
+        d.hoff = d.toff = 64 * chunk;
+        d.hoff2 = d.hoff + d.rpad16 / 2;
+        d.roff = roff;
+        chunk += d.nchunks;
+        roff += d.rpad16 / 2;
+        if (chunk * 64 > kHCols) return WP_ERR_UNSUPPORTED;
+      }
       src_of[p.n_ad] = i;
       ++p.n_ad;
     }
     if (chunk > p.hchunks) p.hchunks = chunk;
     if (roff > p.rslot_rows) p.rslot_rows = roff;
   }
+  if (p.hpass && p.n_ad > 0) {
+    // split the adapters between the two CTAs of a pair (largest first, onto the lighter
+    // CTA); each CTA's adapters sit contiguously in its half of the rank-pass columns
+    int order[kMaxAd];
+    for (int k = 0; k < p.n_ad; ++k) order[k] = k;
+    std::sort(order, order + p.n_ad, [&](int x, int y) { return p.ad[x].rpad16 > p.ad[y].rpad16; });
+    int load[2] = {0, 0};
+    for (int k = 0; k < p.n_ad; ++k) {
+      TcAdapter& d = p.ad[order[k]];
+      d.cta = load[1] < load[0] ? 1 : 0;
+      d.hoff = load[d.cta];              // relative to the CTA's half, fixed up below
+      load[d.cta] += d.rpad16;
+    }
+    int half = std::max(load[0], load[1]);
+    if (2 * half <= kHCols) {
+      for (int k = 0; k < p.n_ad; ++k) {
+        p.ad[k].hoff += p.ad[k].cta * half;
+        p.ad[k].hoff2 = p.ad[k].hoff + p.ad[k].rpad16 / 2;
+      }
+    } else {
+      // too lopsided to give whole adapters to one CTA: split every adapter, each CTA
+      // loading half of its rows at the same place in its half of the columns
+      half = 0;
+      for (int k = 0; k < p.n_ad; ++k) half += p.ad[k].rpad16 / 2;
+      int off = 0;
+      for (int k = 0; k < p.n_ad; ++k) {
+        p.ad[k].cta = 2;
+        p.ad[k].hoff = off;
+        p.ad[k].hoff2 = half + off;
+        off += p.ad[k].rpad16 / 2;
+      }
+    }
+    p.htot = 2 * half;
+    p.hchunks = (hglob + 63) / 64;
+    p.rslot_rows = 0;
+  }
   p.ad_begin[G] = p.n_ad;
   p.h32 = static_cast<const float*>(workspace);
   p.h32_cols = h_off;
+  for (int i = 0; i < p.n_ad32; ++i) {
+    TcAdapter32& d = p.ad32[i];
+    d.vec4 = (d.rank % 4 == 0 && d.ldb % 4 == 0 && d.h_off % 4 == 0 && h_off % 4 == 0 &&
+              aligned16(d.B) && aligned16(workspace)) ? 1 : 0;
+  }
   hp.H = static_cast<float*>(workspace); hp.h_cols = h_off;
 
   // Tensor maps (driver calls from here on).
@@ -330,7 +385,9 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   if (rc != WP_OK) return rc;
   for (int k = 0; k < p.n_ad; ++k) {
     const wp_adapter& a = adapters[src_of[k]];
-    rc = make_map_bf16(&maps.a[k], a.A.data, K, p.ad[k].rank, a.A.ld, kBK, p.ad[k].rpad16 / 2);
+    // rank pass: the whole adapter from one CTA; folded pass: each CTA's half of its rows
+    rc = make_map_bf16(&maps.a[k], a.A.data, K, p.ad[k].rank, a.A.ld, kBK,
+                       p.hpass && p.ad[k].cta != 2 ? p.ad[k].rpad16 : p.ad[k].rpad16 / 2);
     if (rc != WP_OK) return rc;
     rc = make_map_bf16(&maps.b[k], a.B.data, p.ad[k].rank, out_g, a.B.ld, 64, 128);
     if (rc != WP_OK) return rc;
@@ -354,7 +411,8 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   int pairs = tc_max_pairs(smem, nf4);
   if (pairs <= 0) return WP_ERR_CUDA;
   if (pairs > p.total_tiles) pairs = p.total_tiles;
-  p.chunk_tiles = chunk_tiles_for(p.total_tiles, pairs, p.nt_g);
+  p.pair_group = 1;
+  p.chunk_tiles = chunk_tiles_for(p.total_tiles, pairs / p.pair_group, p.nt_g);
   return launch_tc_fwd(maps, p, 2 * pairs, smem, stream, nf4);
 }
 

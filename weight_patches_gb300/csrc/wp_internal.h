@@ -38,7 +38,11 @@ struct TcAdapter {
   int group;       // column group this adapter belongs to
   int rank;        // r
   int rpad16;      // r rounded up to 16 (MMA N for X A^T and K extent of the 2nd GEMM)
-  int chunk_off;   // first 64-rank chunk of the group's rank region (TMEM col / 64, H~ buffer)
+  int hoff;        // TMEM column of ranks [0, rpad16/2) of this adapter's X A^T
+  int hoff2;       // TMEM column of ranks [rpad16/2, rpad16) (hoff + rpad16/2 unless split)
+  int toff;        // first column of this adapter's H~ in shared memory (multiple of 16)
+  int cta;         // rank pass: the CTA of the pair that loads all A rows (0, 1), or 2 when
+                   // each CTA loads half of them (the adapter is split between the halves)
   int nchunks;     // ceil(r / 64)
   int roff;        // row offset of this CTA's rpad16/2 rows of A in a stage's rank slot
   int hout_off;    // column of this adapter's s * X A^T in TcParams::h_out (if stored)
@@ -50,6 +54,7 @@ struct TcAdapter32 {
   int rank;
   int h_off;             // column offset in the s * X A^T fp32 workspace matrix
   int ldb;               // row pitch of B (elements)
+  int vec4;              // rank, pitch, offset and base all allow 16-byte loads
   const float* B;        // [out_g, r] fp32
 };
 
@@ -57,11 +62,14 @@ struct TcParams {
   int T, K, N;                 // tokens, in_features, total out_features
   int out_g, G, nt_g;          // group width, groups, N-tiles per group
   int m_tiles, total_tiles, k_blocks;   // m_tiles counts 256-row pair blocks
-  int chunk_tiles;             // pairs take chunks p, p + P, ... of this many tiles
+  int chunk_tiles;             // tiles per scheduling chunk
+  int pair_group;              // pairs per group: a group's pairs interleave a chunk's tiles
   int has_base;
   int n_ad;                    // bf16 adapters
   int ad_begin[kMaxGroups + 1];
-  int hchunks;                 // max rank chunks in any group (shared-memory H~ buffers)
+  int hchunks;                 // 64-rank chunks of the H~ buffer
+  int hpass;                   // bf16 W: one rank pass per 256-row block over every adapter
+  int htot;                    // rank-pass MMA width: twice the larger CTA half (<= 256)
   int rslot_rows;              // rows of the per-stage rank slot (A rows, per CTA)
   int stages;
   int stage_bytes;             // bf16 W: 32 KiB + rank slot; 4-bit W: 16 KiB + 4 KiB codes + rank slot

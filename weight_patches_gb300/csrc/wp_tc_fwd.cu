@@ -91,6 +91,46 @@ __device__ __forceinline__ void lookup4(uint32_t codes, const uint32_t (&lo)[4],
 
 constexpr uint16_t kBothCtas = 0x3;
 
+// Tile order.  Pairs form groups of `pair_group`; chunks of `chunk_tiles` consecutive tiles
+// in (row block, group, column tile) order go to the groups round-robin, and the pairs of a
+// group take every pair_group-th tile of the chunk, so they work on the same X rows at the
+// same time.  Every role of every CTA walks the same sequence.
+struct Sched {
+  int c;        // next chunk of this pair's group
+  int L;        // current tile (-1 before the first)
+  int c_end;    // end of the current chunk
+  int prev_mg;  // (row block, group) of the previous tile, -1 before the first
+};
+
+__device__ __forceinline__ bool sched_next(Sched& s, const TcParams& p, int q, int ngroups,
+                                           int nchunks) {
+  const int PG = p.pair_group, CH = p.chunk_tiles;
+  int L = s.L < 0 ? -1 : s.L + PG;
+  while (L < 0 || L >= s.c_end) {
+    if (s.c >= nchunks) return false;
+    L = s.c * CH + q;
+    s.c_end = min(s.c * CH + CH, p.total_tiles);
+    s.c += ngroups;
+  }
+  s.L = L;
+  return true;
+}
+
+// True when tile t starts a new unit for this pair: a new 256-row block in rank-pass mode
+// (one X A^T pass serves every group), a new (row block, group) otherwise.
+__device__ __forceinline__ bool sched_new_unit(Sched& s, const TcParams& p, const Tile& t) {
+  const int key = p.hpass ? t.m : t.m * p.G + t.g;
+  const bool fresh = key != s.prev_mg;
+  s.prev_mg = key;
+  return fresh;
+}
+
+// Shared-memory descriptor of rank k of the H~ buffer (64-rank chunks of 128 rows, 128-byte
+// swizzle); k is a multiple of 16, so a 16-rank K step never leaves its chunk.
+__device__ __forceinline__ uint64_t htilde_desc(uint32_t hbuf_addr, int k) {
+  return sw128_kmajor_desc(hbuf_addr + (k >> 6) * kHChunkBytes + (k & 63) * 2);
+}
+
 }  // namespace
 
 template <bool kNF4>
@@ -164,8 +204,10 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
   // in (row block, group, column tile) order; each chunk reuses its X A^T across its tiles.
   const int npairs = static_cast<int>(gridDim.x >> 1);
   const int pair = static_cast<int>(blockIdx.x >> 1);
-  const int CH = p.chunk_tiles;
-  const int nchunks = (p.total_tiles + CH - 1) / CH;
+  const int ngroups = npairs / p.pair_group;
+  const int group = pair / p.pair_group;
+  const int q_in_group = pair % p.pair_group;
+  const int nchunks = (p.total_tiles + p.chunk_tiles - 1) / p.chunk_tiles;
   const uint64_t tmo = p.timeout_ns;
   int* status = &g_tc_status;
 
@@ -178,19 +220,47 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       int issued[kMaxStages];
       for (int s = 0; s < kMaxStages; ++s) issued[s] = 0;
       bool ok = true;
-      for (int L = 0, chunk = pair, c_end = 0; ok; ++L) {
-        if (L >= c_end) {
-          if (chunk >= nchunks) break;
-          L = chunk * CH;
-          c_end = min(L + CH, p.total_tiles);
-          chunk += npairs;
-        }
+      Sched sc{group, -1, 0, -1};
+      while (ok && sched_next(sc, p, q_in_group, ngroups, nchunks)) {
+        const int L = sc.L;
         const Tile t = decode_tile(p, L);
         const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
         const bool lora = a1 > a0;
-        const bool first = lora && ((L % CH == 0) || (t.j == 0));
+        const bool new_unit = sched_new_unit(sc, p, t);
+        const bool hpass_now = !kNF4 && p.hpass && new_unit && p.n_ad > 0;
+        const bool first = kNF4 && new_unit && lora;     // rank pass folded into the K loop
         const int x_row = t.m * kPairM + static_cast<int>(cta) * kBM;
-        if (p.has_base || first) {
+        if (hpass_now) {
+          // rank pass of the row block: X rows and every adapter's A rows.  Each adapter is
+          // loaded whole by one CTA of the pair into that CTA's half of the rank space
+          // (rows [cta * htot/2, ...)); rows of a half that no adapter fills are not loaded:
+          // they only feed rank columns nothing reads.
+          uint32_t tx = 2u * kATileBytes;
+          for (int a = 0; a < p.n_ad; ++a) tx += p.ad[a].rpad16 * 128;
+          const int half = p.htot >> 1;
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!(ok = mbar_wait_cluster(&empty[stage], phase ^ 1, abort_flag, tmo, status))) break;
+            uint8_t* st = sbase + stage * SB;
+            const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+            if (leader) mbar_arrive_expect_tx(&full[stage], tx);
+            tma_load_2d_pair(st, &maps.x, kb * kBK, x_row, fb);
+            for (int a = 0; a < p.n_ad; ++a) {
+              const TcAdapter& d = p.ad[a];
+              if (d.cta == 2) {            // split: this CTA's half of the rows
+                const int col = cta ? d.hoff2 : d.hoff;
+                tma_load_2d_pair_hint(st + kATileBytes + (col - static_cast<int>(cta) * half) * 128,
+                                      &maps.a[a], kb * kBK, static_cast<int>(cta) * (d.rpad16 >> 1),
+                                      fb, keep);
+              } else if (d.cta == static_cast<int>(cta)) {
+                tma_load_2d_pair_hint(st + kATileBytes + (d.hoff - static_cast<int>(cta) * half) * 128,
+                                      &maps.a[a], kb * kBK, 0, fb, keep);
+              }
+            }
+            ++issued[stage];
+            if (++stage == S) { stage = 0; phase ^= 1; }
+          }
+        }
+        if (ok && (p.has_base || first)) {
           uint32_t tx = (p.has_base && !kNF4 ? 4u : 2u) * kATileBytes;     // both CTAs
           if (first)
             for (int a = a0; a < a1; ++a) tx += p.ad[a].rpad16 * 128;
@@ -263,24 +333,60 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       uint32_t nuse[2] = {0, 0};
       int count = 0;
       uint32_t unit_phase = 0;
+      bool h_pending = false;                  // a rank pass whose H~ the MMAs have not waited for
+      int h_buf = 0;                           // accumulator buffer holding that pass's X A^T
       const uint32_t idesc_acc = idesc_bf16_f32(kPairM, kBN);
       const uint32_t hbuf_addr = smem_u32(hbuf);
       const uint32_t stage_base = smem_u32(sbase);
       const uint32_t wring_base = smem_u32(wring);
       bool ok = true;
-      for (int L = 0, chunk = pair, c_end = 0; ok; ++L) {
-        if (L >= c_end) {
-          if (chunk >= nchunks) break;
-          L = chunk * CH;
-          c_end = min(L + CH, p.total_tiles);
-          chunk += npairs;
-        }
+      Sched sc{group, -1, 0, -1};
+      while (ok && sched_next(sc, p, q_in_group, ngroups, nchunks)) {
+        const int L = sc.L;
         const Tile t = decode_tile(p, L);
         const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
         const bool lora = a1 > a0;
-        const bool first = lora && ((L % CH == 0) || (t.j == 0));
-        if (!(p.has_base || lora)) continue;
+        const bool new_unit = sched_new_unit(sc, p, t);
+        const bool hpass_now = !kNF4 && p.hpass && new_unit && p.n_ad > 0;
+        const bool first = kNF4 && new_unit && lora;     // rank pass folded into the K loop
         const int b = count & 1;
+        if (hpass_now) {
+          // the previous unit's H~ must be out of tensor memory before this pass reuses it
+          if (h_pending) {
+            if (!(ok = mbar_wait_cluster(h_ready, unit_phase, abort_flag, tmo, status))) break;
+            unit_phase ^= 1;
+            h_pending = false;
+          }
+          if (!(ok = mbar_wait_cluster(&acc_empty[b ^ 1], (nuse[b ^ 1] & 1) ^ 1, abort_flag, tmo, status)))
+            break;
+          tc_fence_after();
+          // one MMA per K step covers every adapter: N = htot ranks into the idle buffer
+          const uint32_t h_t = tmem + (b ^ 1) * kBN;
+          const uint32_t idesc_h = idesc_bf16_f32(kPairM, p.htot);
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
+            tc_fence_after();
+            const uint32_t st = stage_base + stage * SB;
+            const uint64_t ad = sw128_kmajor_desc(st);
+            const uint64_t rd = sw128_kmajor_desc(st + kATileBytes);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_bf16_pair(h_t, ad + 2 * kk, rd + 2 * kk, idesc_h, (kb | kk) != 0 ? 1u : 0u);
+            mma_commit_pair_mc(&empty[stage], kBothCtas);
+            if (++stage == S) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
+          mma_commit_pair_mc(h_full, kBothCtas);
+          h_pending = true;
+          h_buf = b ^ 1;
+        }
+        if (!(p.has_base || lora)) continue;
+        if (h_pending && b == h_buf) {
+          // this tile's accumulator still holds the unit's X A^T: wait for the epilogue
+          if (!(ok = mbar_wait_cluster(h_ready, unit_phase, abort_flag, tmo, status))) break;
+          unit_phase ^= 1;
+          h_pending = false;
+        }
         if (!(ok = mbar_wait_cluster(&acc_empty[b], (nuse[b] & 1) ^ 1, abort_flag, tmo, status)))
           break;
         if (first &&
@@ -290,13 +396,13 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         const uint32_t acc_t = tmem + b * kBN;
         const uint32_t h_t = tmem + (b ^ 1) * kBN;
         if (p.has_base || first) {
-          // first tile of a unit: the same K loop also runs X A_p^T into the other buffer
+          // first tile of a unit (4-bit W): the same K loop also runs X A_p^T into the other buffer
           const int na = first ? a1 - a0 : 0;
           uint32_t hcol[kMaxAd], roffd[kMaxAd], hid[kMaxAd];
 #pragma unroll
           for (int i = 0; i < kMaxAd; ++i) {
             const int a = min(a0 + i, kMaxAd - 1);
-            hcol[i] = h_t + p.ad[a].chunk_off * 64;
+            hcol[i] = h_t + p.ad[a].hoff;
             roffd[i] = static_cast<uint32_t>(p.ad[a].roff * 128) >> 4;
             hid[i] = idesc_bf16_f32(kPairM, p.ad[a].rpad16);
           }
@@ -344,6 +450,11 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
             if (!(ok = mbar_wait_cluster(h_ready, unit_phase, abort_flag, tmo, status))) break;
             tc_fence_after();
             unit_phase ^= 1;
+          } else if (h_pending) {
+            if (!(ok = mbar_wait_cluster(h_ready, unit_phase, abort_flag, tmo, status))) break;
+            tc_fence_after();
+            unit_phase ^= 1;
+            h_pending = false;
           }
           for (int a = a0; a < a1 && ok; ++a) {
             for (int c = 0; c < p.ad[a].nchunks; ++c) {
@@ -351,10 +462,10 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               tc_fence_after();
               const uint32_t st = stage_base + stage * SB;
               const int kext = min(64, p.ad[a].rpad16 - 64 * c);
-              const uint64_t hd = sw128_kmajor_desc(hbuf_addr + (p.ad[a].chunk_off + c) * kHChunkBytes);
               const uint64_t bd = sw128_kmajor_desc(st + (kNF4 ? 0 : kATileBytes));
               for (int kk = 0; kk < kext / 16; ++kk)
-                mma_bf16_pair(acc_t, hd + 2 * kk, bd + 2 * kk, idesc_acc, (accum || kk > 0) ? 1u : 0u);
+                mma_bf16_pair(acc_t, htilde_desc(hbuf_addr, p.ad[a].toff + 64 * c + 16 * kk),
+                              bd + 2 * kk, idesc_acc, (accum || kk > 0) ? 1u : 0u);
               accum = true;
               mma_commit_pair_mc(&empty[stage], kBothCtas);
               if (++stage == S) { stage = 0; phase ^= 1; }
@@ -395,38 +506,40 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     int count = 0;
     uint32_t unit_phase = 0;
     uint32_t sidx = 0;                              // staging chunks issued so far
-    for (int L = 0, chunk = pair, c_end = 0;; ++L) {
-      if (L >= c_end) {
-        if (chunk >= nchunks) break;
-        L = chunk * CH;
-        c_end = min(L + CH, p.total_tiles);
-        chunk += npairs;
-      }
+    Sched sc{group, -1, 0, -1};
+    while (sched_next(sc, p, q_in_group, ngroups, nchunks)) {
+      const int L = sc.L;
       const Tile t = decode_tile(p, L);
       const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
       const bool lora = a1 > a0;
-      const bool first = lora && ((L % CH == 0) || (t.j == 0));
+      const bool new_unit = sched_new_unit(sc, p, t);
+      const bool hpass_now = !kNF4 && p.hpass && new_unit && p.n_ad > 0;
+      const bool first = kNF4 && new_unit && lora;
       const bool any_mma = p.has_base || lora;
       const int b = count & 1;
-      if (first) {
+      if (hpass_now || first) {
         const bool ok = mbar_wait_cluster(h_full, unit_phase, abort_flag, tmo, status);
         if (named_bar_any(!ok, 2, 128)) break;
         tc_fence_after();
         unit_phase ^= 1;
         const uint32_t h_t = tmem + (b ^ 1) * kBN;
-        for (int a = a0; a < a1; ++a) {
+        // the rank pass covers every adapter; the folded one only this group's
+        for (int a = hpass_now ? 0 : a0; a < (hpass_now ? p.n_ad : a1); ++a) {
           const float s = p.ad[a].s;
           const int units = p.ad[a].rpad16 >> 3;       // 8 ranks (16 bytes of H~) per unit
           for (int u0 = 0; u0 < units; u0 += 4) {
             // 32 ranks per TMEM load where the rank allows it, 8 otherwise
             uint32_t r[32];
             const int n = min(4, units - u0);
-            if (n == 4) {
-              tmem_ld32(h_t + lane_base + p.ad[a].chunk_off * 64 + u0 * 8, r);
+            // TMEM column of unit u: the two halves of an adapter's ranks may lie apart
+            const int hu = units >> 1;
+            auto col = [&](int u) { return u < hu ? p.ad[a].hoff + u * 8 : p.ad[a].hoff2 + (u - hu) * 8; };
+            if (n == 4 && col(u0 + 3) == col(u0) + 24) {
+              tmem_ld32(h_t + lane_base + col(u0), r);
             } else {
               for (int k = 0; k < n; ++k) {
                 uint32_t r8[8];
-                tmem_ld8(h_t + lane_base + p.ad[a].chunk_off * 64 + (u0 + k) * 8, r8);
+                tmem_ld8(h_t + lane_base + col(u0 + k), r8);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) r[k * 8 + i] = r8[i];
               }
@@ -448,9 +561,9 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               const uint32_t w1 = pack_bf16x2(u2f(q8[2]) * s, u2f(q8[3]) * s);
               const uint32_t w2 = pack_bf16x2(u2f(q8[4]) * s, u2f(q8[5]) * s);
               const uint32_t w3 = pack_bf16x2(u2f(q8[6]) * s, u2f(q8[7]) * s);
-              const int chunk16 = p.ad[a].chunk_off + (u >> 3);
-              const int unit16 = (u & 7) ^ (row_in_cta & 7);
-              st_shared_v4(hbuf_addr + chunk16 * kHChunkBytes + row_in_cta * 128 + unit16 * 16, w0,
+              const int kr = p.ad[a].toff + u * 8;            // H~ column of the unit's first rank
+              const int unit16 = ((kr & 63) >> 3) ^ (row_in_cta & 7);
+              st_shared_v4(hbuf_addr + (kr >> 6) * kHChunkBytes + row_in_cta * 128 + unit16 * 16, w0,
                            w1, w2, w3);
             }
           }
@@ -524,11 +637,29 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               const float* hrow = p.h32 + static_cast<long long>(row) * p.h32_cols + p.ad32[a].h_off;
               const float* Bm = p.ad32[a].B + static_cast<long long>(cig + c0) * p.ad32[a].ldb;
               const long long ldb = p.ad32[a].ldb;
-              for (int jj = 0; jj < p.ad32[a].rank; ++jj) {
-                const float h = hrow[jj];
+              if (p.ad32[a].vec4) {
+                // four ranks per 16-byte load of h and of each B row (B rows are read by
+                // every thread of the warp: broadcast, L1-resident)
+                for (int jj = 0; jj < p.ad32[a].rank; jj += 4) {
+                  const float4 h4 = *reinterpret_cast<const float4*>(hrow + jj);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (i < nc) v[i] = fmaf(h, Bm[i * ldb + jj], v[i]);
+                  for (int i = 0; i < 32; ++i) {
+                    if (i < nc) {
+                      const float4 b4 = __ldg(reinterpret_cast<const float4*>(Bm + i * ldb + jj));
+                      v[i] = fmaf(h4.x, b4.x, v[i]);
+                      v[i] = fmaf(h4.y, b4.y, v[i]);
+                      v[i] = fmaf(h4.z, b4.z, v[i]);
+                      v[i] = fmaf(h4.w, b4.w, v[i]);
+                    }
+                  }
+                }
+              } else {
+                for (int jj = 0; jj < p.ad32[a].rank; ++jj) {
+                  const float h = hrow[jj];
+#pragma unroll
+                  for (int i = 0; i < 32; ++i)
+                    if (i < nc) v[i] = fmaf(h, Bm[i * ldb + jj], v[i]);
+                }
               }
             }
           }
@@ -606,13 +737,9 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     int wb = 0;
     uint32_t wphase = 0;
     bool ok = true;
-    for (int L = 0, chunk = pair, c_end = 0; ok; ++L) {
-      if (L >= c_end) {
-        if (chunk >= nchunks) break;
-        L = chunk * CH;
-        c_end = min(L + CH, p.total_tiles);
-        chunk += npairs;
-      }
+    Sched sc{group, -1, 0, -1};
+    while (ok && sched_next(sc, p, q_in_group, ngroups, nchunks)) {
+      const int L = sc.L;
       const Tile t = decode_tile(p, L);
       const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
       const bool lora = a1 > a0;
