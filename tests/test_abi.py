@@ -112,8 +112,9 @@ def test_dense_patch_rejections(lib):
 def test_workspace_sizes(lib):
     X, W = _m(1000, 128), _m(256, 128)
     arr = (wpg.WpAdapter * 2)(_ad(8, 128, 256), _ad(16, 128, 256, dtype=wpg.WP_FP32))
-    # tensor-core path: only the fp32 adapter's s * X A^T is staged, 1000 x 16 fp32
-    assert lib.lora_workspace_size(0, ctypes.byref(X), ctypes.byref(W), arr, 2) == 64000
+    # tensor-core path: the fp32 adapter's s * X A^T (1000 x 16 fp32, for the CUDA-core
+    # route) plus its bf16 pieces (A: 3 x 16 x 128, B: 256 x 6 x 16)
+    assert lib.lora_workspace_size(0, ctypes.byref(X), ctypes.byref(W), arr, 2) == 64000 + 12288 + 49152
     assert lib.lora_workspace_size(0, ctypes.byref(X), ctypes.byref(W), arr, 1) == 0
     Xf = _m(1000, 128, wpg.WP_FP32)
     # fp32 path: every adapter's s * X A^T, 1000 x 24 fp32, rounded up to 256 bytes

@@ -65,6 +65,22 @@ def test_c4_fp32_adapter_fp32_output():
     assert err <= FP32_TOL, err
 
 
+@pytest.mark.parametrize("T,K,N,r,xkind", [(77, 70, 40, 5, workloads.FP32), (131, 200, 96, 24, workloads.FP32),
+                                           (300, 200, 264, 20, workloads.BF16), (70, 64, 48, 40, workloads.BF16)])
+def test_fp32_adapter_odd_shapes(T, K, N, r, xkind):
+    """FP32 adapters with ragged K (partial chunks, unaligned rows) and rank widths that
+    span one or two column blocks of the rank projection; all-fp32 and bf16 layers."""
+    rng = np.random.default_rng(T + K + r)
+    X = workloads.draw(rng, T, K, 1.0, xkind)
+    W = workloads.draw(rng, N, K, (1.0 / K) ** 0.5, xkind)
+    A = workloads.draw(rng, r, K, (1.0 / K) ** 0.5, workloads.FP32)
+    B = workloads.draw(rng, N, r, 0.02, workloads.FP32)
+    lin = workloads.Linear("odd32", X, W, None, [workloads.Patch(A, B, float(r), 0.8)], request_scale=1.3)
+    Y = gu.run_fwd(lin, out_dtype=torch.float32)
+    err = relative_rms(gu.to_f64(Y), olora.reference_output(lin))
+    assert err <= FP32_TOL, err
+
+
 def test_fp32_output_bf16_adapters():
     lin = workloads.config1("small")
     Y = gu.run_fwd(lin, out_dtype=torch.float32)

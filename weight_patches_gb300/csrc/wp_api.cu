@@ -127,7 +127,18 @@ struct FwdPlan {
   bool tc = false;        // tensor-core path
   int rank32_total = 0;   // fp32 adapters' total rank (tensor-core path)
   int rank_all = 0;       // all adapters' total rank (fp32 path)
+  size_t split_bytes = 0; // bf16 pieces of the fp32 adapters (tensor-core path)
 };
+
+// FP32 adapters on the tensor-core path travel as three bf16 pieces per factor: rank
+// padded to rp (16), A pieces [3 rp, round8(K)], B pieces [out, 6 rp].
+int split_rp(long long r) { return static_cast<int>((r + 15) / 16 * 16); }
+size_t split_a_bytes(long long r, long long K) {
+  return round256(static_cast<size_t>(3 * split_rp(r)) * static_cast<size_t>((K + 7) / 8 * 8) * 2);
+}
+size_t split_b_bytes(long long r, long long out) {
+  return round256(static_cast<size_t>(out) * 6 * split_rp(r) * 2);
+}
 
 // Decide the path from the dtypes alone (the same answer lora_workspace_size gives).
 int plan_fwd(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int n, FwdPlan* plan) {
@@ -135,14 +146,17 @@ int plan_fwd(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int n, FwdP
   for (int i = 0; i < n; ++i) {
     const int r = static_cast<int>(ad[i].A.rows);
     plan->rank_all += r;
-    if (ad[i].A.dtype == WP_FP32) plan->rank32_total += r;
+    if (ad[i].A.dtype == WP_FP32) {
+      plan->rank32_total += r;
+      plan->split_bytes += split_a_bytes(r, ad[i].A.cols) + split_b_bytes(r, ad[i].B.rows);
+    }
   }
   return WP_OK;
 }
 
 size_t fwd_workspace(const wp_mat* X, const FwdPlan& plan) {
   const size_t T = static_cast<size_t>(X->rows);
-  if (plan.tc) return plan.rank32_total ? round256(T * plan.rank32_total * 4) : 0;
+  if (plan.tc) return plan.rank32_total ? round256(T * plan.rank32_total * 4) + plan.split_bytes : 0;
   return plan.rank_all ? round256(T * plan.rank_all * 4) : 0;
 }
 
@@ -253,7 +267,6 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   // Plan the adapters (host only; every rejection happens before any CUDA call).
   H32Params hp{};
   hp.T = p.T; hp.K = p.K; hp.X = X->data; hp.x_dtype = WP_BF16; hp.ldx = X->ld;
-  int src_of[kMaxAd];
   int h_off = 0;
   int hout_of[kMaxAd + kMaxAd32];          // column of adapter i in h_out: ranks of 0..i-1
   for (int i = 0, acc = 0; i < n_adapters; ++i) {
@@ -266,6 +279,27 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   // rank space (16-aligned); 4-bit W: a pass per (row block, group) folded into the first
   // tile's K loop, each group's adapters at 64-rank chunks of their own.
   p.hpass = nf4 ? 0 : 1;
+  // FP32 adapters ride on the tensor cores as bf16 pieces when their H~ (6 rp columns each)
+  // fits beside the bf16 adapters' and the bf16 W path is taken; else the FP32 CUDA-core
+  // projection plus an epilogue product carry them
+  bool split3 = false;
+  {
+    int n16 = 0, n32 = 0, width = 0;
+    for (int i = 0; i < n_adapters; ++i) {
+      if (s_of[i] == 0.0f) continue;
+      const int r = static_cast<int>(adapters[i].A.rows);
+      if (adapters[i].A.dtype == WP_FP32) { ++n32; width += 6 * split_rp(r); }
+      else { ++n16; width += (r + 15) / 16 * 16; }
+    }
+    split3 = p.hpass && n32 > 0 && n16 + n32 <= kMaxAd && width <= kHCols && !h_out;
+  }
+  const size_t h32_bytes = round256(static_cast<size_t>(T) * plan.rank32_total * 4);
+  size_t split_off = h32_bytes;
+  struct SplitJob { const wp_adapter* a; int rp, out; uint16_t* As; uint16_t* Bs; int lda_s; };
+  SplitJob jobs[kMaxAd];
+  int n_jobs = 0;
+  const void* amap_ptr[kMaxAd]; long long amap_rows[kMaxAd], amap_ld[kMaxAd];
+  const void* bmap_ptr[kMaxAd]; long long bmap_cols[kMaxAd], bmap_ld[kMaxAd];
   int hglob = 0;
   for (int g = 0; g < G; ++g) {
     p.ad_begin[g] = p.n_ad;
@@ -276,6 +310,26 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
       if (ag != g || s_of[i] == 0.0f) continue;
       const wp_adapter& a = adapters[i];
       const int r = static_cast<int>(a.A.rows);
+      if (a.A.dtype == WP_FP32 && split3) {
+        TcAdapter& d = p.ad[p.n_ad];
+        const int rp = split_rp(r);
+        SplitJob& j = jobs[n_jobs++];
+        j.a = &a; j.rp = rp; j.out = static_cast<int>(a.B.rows);
+        j.lda_s = static_cast<int>((K + 7) / 8 * 8);
+        j.As = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + split_off);
+        split_off += split_a_bytes(r, K);
+        j.Bs = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + split_off);
+        split_off += split_b_bytes(r, a.B.rows);
+        d.group = g; d.rank = 6 * rp; d.rpad16 = 6 * rp; d.pw = 3 * rp; d.split3 = 1;
+        d.nchunks = (6 * rp + 63) / 64; d.s = s_of[i];
+        d.hout_off = hout_of[i];
+        d.toff = hglob; d.roff = 0;
+        hglob += d.rpad16;
+        amap_ptr[p.n_ad] = j.As; amap_rows[p.n_ad] = 3 * rp; amap_ld[p.n_ad] = j.lda_s;
+        bmap_ptr[p.n_ad] = j.Bs; bmap_cols[p.n_ad] = 6 * rp; bmap_ld[p.n_ad] = 6 * rp;
+        ++p.n_ad;
+        continue;
+      }
       if (a.A.dtype == WP_FP32) {
         if (p.n_ad32 >= kMaxAd32) return WP_ERR_UNSUPPORTED;
         TcAdapter32& d = p.ad32[p.n_ad32++];
@@ -292,8 +346,10 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
       if (!aligned16(a.A.data) || a.A.ld % 8 || !aligned16(a.B.data) || a.B.ld % 8)
         return WP_ERR_ALIGN;
       TcAdapter& d = p.ad[p.n_ad];
-      d.group = g; d.rank = r; d.rpad16 = (r + 15) / 16 * 16;
+      d.group = g; d.rank = r; d.rpad16 = (r + 15) / 16 * 16; d.pw = d.rpad16; d.split3 = 0;
       d.nchunks = (r + 63) / 64; d.s = s_of[i];
+      amap_ptr[p.n_ad] = a.A.data; amap_rows[p.n_ad] = r; amap_ld[p.n_ad] = a.A.ld;
+      bmap_ptr[p.n_ad] = a.B.data; bmap_cols[p.n_ad] = r; bmap_ld[p.n_ad] = a.B.ld;
       d.hout_off = hout_of[i];
       if (p.hpass) {
         d.toff = hglob;                 // H~ columns: packed in adapter order
@@ -308,7 +364,6 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
         roff += d.rpad16 / 2;
         if (chunk * 64 > kHCols) return WP_ERR_UNSUPPORTED;
       }
-      src_of[p.n_ad] = i;
       ++p.n_ad;
     }
     if (chunk > p.hchunks) p.hchunks = chunk;
@@ -319,31 +374,31 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     // CTA); each CTA's adapters sit contiguously in its half of the rank-pass columns
     int order[kMaxAd];
     for (int k = 0; k < p.n_ad; ++k) order[k] = k;
-    std::sort(order, order + p.n_ad, [&](int x, int y) { return p.ad[x].rpad16 > p.ad[y].rpad16; });
+    std::sort(order, order + p.n_ad, [&](int x, int y) { return p.ad[x].pw > p.ad[y].pw; });
     int load[2] = {0, 0};
     for (int k = 0; k < p.n_ad; ++k) {
       TcAdapter& d = p.ad[order[k]];
       d.cta = load[1] < load[0] ? 1 : 0;
       d.hoff = load[d.cta];              // relative to the CTA's half, fixed up below
-      load[d.cta] += d.rpad16;
+      load[d.cta] += d.pw;
     }
     int half = std::max(load[0], load[1]);
     if (2 * half <= kHCols) {
       for (int k = 0; k < p.n_ad; ++k) {
         p.ad[k].hoff += p.ad[k].cta * half;
-        p.ad[k].hoff2 = p.ad[k].hoff + p.ad[k].rpad16 / 2;
+        p.ad[k].hoff2 = p.ad[k].hoff + p.ad[k].pw / 2;
       }
     } else {
       // too lopsided to give whole adapters to one CTA: split every adapter, each CTA
       // loading half of its rows at the same place in its half of the columns
       half = 0;
-      for (int k = 0; k < p.n_ad; ++k) half += p.ad[k].rpad16 / 2;
+      for (int k = 0; k < p.n_ad; ++k) half += p.ad[k].pw / 2;
       int off = 0;
       for (int k = 0; k < p.n_ad; ++k) {
         p.ad[k].cta = 2;
         p.ad[k].hoff = off;
         p.ad[k].hoff2 = half + off;
-        off += p.ad[k].rpad16 / 2;
+        off += p.ad[k].pw / 2;
       }
     }
     p.htot = 2 * half;
@@ -384,12 +439,11 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   rc = make_map(&maps.y, Y->dtype, Y->data, N, T, Y->ld, Y->dtype == WP_FP32 ? 32 : 64, kBM);
   if (rc != WP_OK) return rc;
   for (int k = 0; k < p.n_ad; ++k) {
-    const wp_adapter& a = adapters[src_of[k]];
     // rank pass: the whole adapter from one CTA; folded pass: each CTA's half of its rows
-    rc = make_map_bf16(&maps.a[k], a.A.data, K, p.ad[k].rank, a.A.ld, kBK,
-                       p.hpass && p.ad[k].cta != 2 ? p.ad[k].rpad16 : p.ad[k].rpad16 / 2);
+    rc = make_map_bf16(&maps.a[k], amap_ptr[k], K, amap_rows[k], amap_ld[k], kBK,
+                       p.hpass && p.ad[k].cta != 2 ? p.ad[k].pw : p.ad[k].pw / 2);
     if (rc != WP_OK) return rc;
-    rc = make_map_bf16(&maps.b[k], a.B.data, p.ad[k].rank, out_g, a.B.ld, 64, 128);
+    rc = make_map_bf16(&maps.b[k], bmap_ptr[k], bmap_cols[k], out_g, bmap_ld[k], 64, 128);
     if (rc != WP_OK) return rc;
   }
 
@@ -406,6 +460,13 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
 
   if (hp.n_ad > 0) {
     rc = launch_h32(hp, stream);
+    if (rc != WP_OK) return rc;
+  }
+  for (int k = 0; k < n_jobs; ++k) {
+    const SplitJob& j = jobs[k];
+    rc = launch_split3(static_cast<const float*>(j.a->A.data), j.a->A.ld, static_cast<int>(j.a->A.rows),
+                       static_cast<int>(K), j.rp, j.As, j.lda_s, static_cast<const float*>(j.a->B.data),
+                       j.a->B.ld, j.out, j.Bs, stream);
     if (rc != WP_OK) return rc;
   }
   int pairs = tc_max_pairs(smem, nf4);

@@ -37,9 +37,12 @@ constexpr int kSmemLimit = 227 * 1024;
 struct TcAdapter {
   int group;       // column group this adapter belongs to
   int rank;        // r
-  int rpad16;      // r rounded up to 16 (MMA N for X A^T and K extent of the 2nd GEMM)
-  int hoff;        // TMEM column of ranks [0, rpad16/2) of this adapter's X A^T
-  int hoff2;       // TMEM column of ranks [rpad16/2, rpad16) (hoff + rpad16/2 unless split)
+  int rpad16;      // r rounded up to 16 (MMA N for X A^T and K extent of the 2nd GEMM); for
+                   // an FP32 adapter carried as bf16 pieces, 6 * rp (the width of its H~)
+  int pw;          // rank-pass columns: rpad16, or 3 * rp for an FP32 adapter (X a_i^T, i=1..3)
+  int split3;      // FP32 adapter as three bf16 pieces (rp = pw / 3 ranks per piece)
+  int hoff;        // TMEM column of rank-pass columns [0, pw/2) of this adapter
+  int hoff2;       // TMEM column of columns [pw/2, pw) (hoff + pw/2 unless split)
   int toff;        // first column of this adapter's H~ in shared memory (multiple of 16)
   int cta;         // rank pass: the CTA of the pair that loads all A rows (0, 1), or 2 when
                    // each CTA loads half of them (the adapter is split between the halves)
@@ -135,14 +138,22 @@ int launch_f32_linear(const F32Params& p, const float* H, int h_cols, cudaStream
 struct H32Params {
   int T, K;
   const void* X; int x_dtype; long long ldx;
+  int x_vec;                       // X rows 16-byte aligned (vector loads allowed)
   int n_ad;
   const void* A[kMaxAd + kMaxAd32]; long long lda[kMaxAd + kMaxAd32];
   int a_dtype[kMaxAd + kMaxAd32];
+  int a_vec[kMaxAd + kMaxAd32];    // 4-element runs of A aligned for one vector load
   int rank[kMaxAd + kMaxAd32], h_off[kMaxAd + kMaxAd32];
   float s[kMaxAd + kMaxAd32];
   float* H; int h_cols;
 };
 int launch_h32(const H32Params& p, cudaStream_t stream);
+
+// An FP32 adapter (A [r, K], B [out, r], fp32) as bf16 pieces x = x1 + x2 + x3 (each the
+// bf16 rounding of what the previous ones leave): As [3 rp, lda_s] = [a1; a2; a3] and
+// Bs [out, 6 rp] = [b1 b2 b1 b3 b2 b1], rows / columns past r zero.
+int launch_split3(const float* A, long long lda, int r, int K, int rp, uint16_t* As, int lda_s,
+                  const float* B, long long ldb, int out, uint16_t* Bs, cudaStream_t stream);
 
 // ------------------------------------------------------------------ backward helpers
 struct NF4Table {

@@ -13,6 +13,9 @@
 // kernel's epilogue when an FP32 adapter rides on a bf16 layer.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cstdint>
+
 #include "wp_internal.h"
 
 namespace wp {
@@ -39,53 +42,202 @@ constexpr int kKc = 32;
 
 }  // namespace
 
-// One block: 32 token rows x 64 rank columns of H (all adapters concatenated).
-__global__ void __launch_bounds__(256) rank_proj_kernel(const H32Params p) {
-  __shared__ float xs[32][kKc + 1];
-  __shared__ float as[64][kKc + 1];
-  const int t0 = blockIdx.x * 32;
-  const int c0 = blockIdx.y * 64;
-  const int tid = threadIdx.x;
-  const int c_lo = c0 + (tid & 63);   // this thread's rank column
-  const int r_lo = tid >> 6;          // rows r_lo, r_lo + 4, ..., (8 rows)
-  int ad = -1;
-  for (int a = 0; a < p.n_ad; ++a)
-    if (c_lo >= p.h_off[a] && c_lo < p.h_off[a] + p.rank[a]) ad = a;
-  float acc[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (int k0 = 0; k0 < p.K; k0 += kKc) {
-    for (int idx = tid; idx < 32 * kKc; idx += 256) {
-      const int r = idx / kKc, k = idx % kKc;
-      const int t = t0 + r, kk = k0 + k;
-      xs[r][k] = (t < p.T && kk < p.K) ? load_as_f32(p.X, p.x_dtype, (long long)t * p.ldx + kk) : 0.f;
-    }
-    for (int idx = tid; idx < 64 * kKc; idx += 256) {
-      const int c = c0 + idx / kKc, k = idx % kKc;
-      const int kk = k0 + k;
-      float v = 0.f;
-      if (kk < p.K) {
-        for (int a = 0; a < p.n_ad; ++a)
-          if (c >= p.h_off[a] && c < p.h_off[a] + p.rank[a])
-            v = load_as_f32(p.A[a], p.a_dtype[a], (long long)(c - p.h_off[a]) * p.lda[a] + kk);
-      }
-      as[c - c0][k] = v;
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int k = 0; k < kKc; ++k) {
-      const float av = as[c_lo - c0][k];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(xs[r_lo + 4 * i][k], av, acc[i]);
-    }
-    __syncthreads();
+// s * X A^T for skinny A (a few to a few hundred rank columns).  One block: 32 token
+// rows x CW rank columns (adapters concatenated), 4 warps.  A lane owns two rows
+// (r and r + 4 of its warp's 8) and one 8-wide k segment of each 64-wide K chunk; the
+// chunk of A sits in shared memory as [segment][k][column], each segment's block padded
+// by 16 bytes so that the 8 segments a warp reads at once fall in distinct banks (lanes
+// of one segment read the same address: a broadcast).  At the end the 8 segment partial
+// sums of a row are combined by a fixed butterfly (reduce-scatter over shuffles), so the
+// result does not depend on timing.
+template <int CW, bool kXf32>
+__global__ void __launch_bounds__(128) rank_proj_kernel(const H32Params p) {
+  constexpr int kKC = 64;
+  constexpr int kSeg = 8 * CW + 4;            // floats per segment block, padded
+  constexpr int kSlots = CW / 8;              // A quads (4 consecutive k) per thread per chunk
+  __shared__ __align__(16) float As[8 * kSeg];
+  __shared__ float col_s[CW];
+  __shared__ int col_ok[CW];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c0 = blockIdx.x * CW;
+  const int s8 = lane & 7;
+
+  if (tid < CW) {
+    const int col = c0 + tid;
+    int ok = 0;
+    float sc = 0.f;
+    for (int a = 0; a < p.n_ad; ++a)
+      if (col < p.h_cols && col >= p.h_off[a] && col < p.h_off[a] + p.rank[a]) { ok = 1; sc = p.s[a]; }
+    col_s[tid] = sc;
+    col_ok[tid] = ok;
   }
-  if (ad < 0 || c_lo >= p.h_cols) return;
-  const float s = p.s[ad];
+
+  // this thread's A quads: column c0 + (e >> 4), k offset 4 * (e & 15) within a chunk
+  const char* asrc[kSlots];
+  long long ald[kSlots];
+  int adt[kSlots];
+  bool avec[kSlots];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int t = t0 + r_lo + 4 * i;
-    if (t < p.T) p.H[(long long)t * p.h_cols + c_lo] = s * acc[i];
+  for (int i = 0; i < kSlots; ++i) {
+    const int e = tid + 128 * i;
+    const int col = c0 + (e >> 4);
+    asrc[i] = nullptr; ald[i] = 0; adt[i] = WP_BF16; avec[i] = false;
+    for (int a = 0; a < p.n_ad; ++a) {
+      if (col < p.h_cols && col >= p.h_off[a] && col < p.h_off[a] + p.rank[a]) {
+        const int es = p.a_dtype[a] == WP_FP32 ? 4 : 2;
+        asrc[i] = static_cast<const char*>(p.A[a]) + static_cast<long long>(col - p.h_off[a]) * p.lda[a] * es;
+        ald[i] = p.lda[a];
+        adt[i] = p.a_dtype[a];
+        avec[i] = p.a_vec[a] != 0;
+      }
+    }
+  }
+
+  float areg[kSlots][4];
+  auto load_a = [&](int k0) {
+#pragma unroll
+    for (int i = 0; i < kSlots; ++i) {
+      const int k = k0 + 4 * ((tid + 128 * i) & 15);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) areg[i][j] = 0.f;
+      if (!asrc[i]) continue;
+      if (adt[i] == WP_FP32) {
+        const float* a = reinterpret_cast<const float*>(asrc[i]);
+        if (avec[i] && k + 3 < p.K) {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(a + k));
+          areg[i][0] = v.x; areg[i][1] = v.y; areg[i][2] = v.z; areg[i][3] = v.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) if (k + j < p.K) areg[i][j] = a[k + j];
+        }
+      } else {
+        const uint16_t* a = reinterpret_cast<const uint16_t*>(asrc[i]);
+        if (avec[i] && k + 3 < p.K) {
+          const uint2 v = __ldg(reinterpret_cast<const uint2*>(a + k));
+          areg[i][0] = __uint_as_float(v.x << 16); areg[i][1] = __uint_as_float(v.x & 0xffff0000u);
+          areg[i][2] = __uint_as_float(v.y << 16); areg[i][3] = __uint_as_float(v.y & 0xffff0000u);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (k + j < p.K) areg[i][j] = __uint_as_float(static_cast<uint32_t>(a[k + j]) << 16);
+        }
+      }
+    }
+  };
+  auto store_a = [&]() {
+#pragma unroll
+    for (int i = 0; i < kSlots; ++i) {
+      const int e = tid + 128 * i;
+      const int c = e >> 4, k4 = e & 15;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) As[(k4 >> 1) * kSeg + ((k4 & 1) * 4 + j) * CW + c] = areg[i][j];
+    }
+  };
+
+  float xr[2][8];
+  auto load_x = [&](int rb, int k0) {
+    const int k = k0 + 8 * s8;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = rb * 32 + warp * 8 + (lane >> 3) + 4 * h;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) xr[h][j] = 0.f;
+      if (t >= p.T) continue;
+      if (kXf32) {
+        const float* x = static_cast<const float*>(p.X) + static_cast<long long>(t) * p.ldx;
+        if (p.x_vec && k + 7 < p.K) {
+          const float4 u = __ldg(reinterpret_cast<const float4*>(x + k));
+          const float4 v = __ldg(reinterpret_cast<const float4*>(x + k + 4));
+          xr[h][0] = u.x; xr[h][1] = u.y; xr[h][2] = u.z; xr[h][3] = u.w;
+          xr[h][4] = v.x; xr[h][5] = v.y; xr[h][6] = v.z; xr[h][7] = v.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) if (k + j < p.K) xr[h][j] = x[k + j];
+        }
+      } else {
+        const uint16_t* x = static_cast<const uint16_t*>(p.X) + static_cast<long long>(t) * p.ldx;
+        if (p.x_vec && k + 7 < p.K) {
+          const uint4 u = __ldg(reinterpret_cast<const uint4*>(x + k));
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            xr[h][2 * j] = __uint_as_float(w[j] << 16);
+            xr[h][2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (k + j < p.K) xr[h][j] = __uint_as_float(static_cast<uint32_t>(x[k + j]) << 16);
+        }
+      }
+    }
+  };
+
+  const int row_blocks = (p.T + 31) / 32;
+  for (int rb = blockIdx.y; rb < row_blocks; rb += gridDim.y) {
+    float acc[2][CW];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int c = 0; c < CW; ++c) acc[h][c] = 0.f;
+    load_a(0);
+    load_x(rb, 0);
+    for (int k0 = 0; k0 < p.K; k0 += kKC) {
+      __syncthreads();                      // the previous chunk is no longer read
+      store_a();
+      __syncthreads();
+      float xc[2][8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) xc[h][j] = xr[h][j];
+      if (k0 + kKC < p.K) {                 // next chunk in flight during the FMAs
+        load_a(k0 + kKC);
+        load_x(rb, k0 + kKC);
+      }
+      const float* as = As + s8 * kSeg;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+        for (int c4 = 0; c4 < CW / 4; ++c4) {
+          const float4 a = *reinterpret_cast<const float4*>(as + kk * CW + 4 * c4);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            acc[h][4 * c4 + 0] = fmaf(xc[h][kk], a.x, acc[h][4 * c4 + 0]);
+            acc[h][4 * c4 + 1] = fmaf(xc[h][kk], a.y, acc[h][4 * c4 + 1]);
+            acc[h][4 * c4 + 2] = fmaf(xc[h][kk], a.z, acc[h][4 * c4 + 2]);
+            acc[h][4 * c4 + 3] = fmaf(xc[h][kk], a.w, acc[h][4 * c4 + 3]);
+          }
+        }
+      }
+    }
+    // combine the 8 segments: after the butterfly each lane of a row's 8 holds CW/8 sums
+#pragma unroll
+    for (int step = 0; step < 3; ++step) {
+      const int m = 4 >> step;
+      const int half = (CW / 2) >> step;
+      const bool hi = (lane & m) != 0;
+#pragma unroll
+      for (int i = 0; i < half; ++i) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float keep = hi ? acc[h][i + half] : acc[h][i];
+          const float send = hi ? acc[h][i] : acc[h][i + half];
+          acc[h][i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+      }
+    }
+    const int cofs = ((lane >> 2) & 1) * (CW / 2) + ((lane >> 1) & 1) * (CW / 4) + (lane & 1) * (CW / 8);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = rb * 32 + warp * 8 + (lane >> 3) + 4 * h;
+      if (t >= p.T) continue;
+#pragma unroll
+      for (int i = 0; i < CW / 8; ++i) {
+        const int c = cofs + i;
+        if (col_ok[c]) p.H[static_cast<long long>(t) * p.h_cols + c0 + c] = col_s[c] * acc[h][i];
+      }
+    }
   }
 }
 
@@ -154,10 +306,82 @@ __global__ void __launch_bounds__(256) f32_linear_kernel(const F32Params p, cons
   }
 }
 
-int launch_h32(const H32Params& p, cudaStream_t stream) {
-  if (p.T <= 0 || p.n_ad <= 0) return WP_OK;
-  dim3 grid((p.T + 31) / 32, (p.h_cols + 63) / 64);
-  rank_proj_kernel<<<grid, 256, 0, stream>>>(p);
+int launch_h32(const H32Params& p0, cudaStream_t stream) {
+  if (p0.T <= 0 || p0.n_ad <= 0) return WP_OK;
+  // vector loads where every row start is aligned: 8 elements of X, 4 of A
+  H32Params p = p0;
+  const auto aligned = [](const void* ptr, long long ld, int bytes, int align) {
+    return reinterpret_cast<uintptr_t>(ptr) % align == 0 && (ld * bytes) % align == 0;
+  };
+  const int xb = p.x_dtype == WP_FP32 ? 4 : 2;
+  p.x_vec = aligned(p.X, p.ldx, xb, 16);
+  for (int a = 0; a < p.n_ad; ++a) {
+    const int ab = p.a_dtype[a] == WP_FP32 ? 4 : 2;
+    p.a_vec[a] = aligned(p.A[a], p.lda[a], ab, 4 * ab);
+  }
+  const int cw = p.h_cols <= 16 ? 16 : 32;
+  dim3 grid((p.h_cols + cw - 1) / cw, std::min((p.T + 31) / 32, 65535));
+  if (p.x_dtype == WP_FP32) {
+    if (cw == 16) rank_proj_kernel<16, true><<<grid, 128, 0, stream>>>(p);
+    else rank_proj_kernel<32, true><<<grid, 128, 0, stream>>>(p);
+  } else {
+    if (cw == 16) rank_proj_kernel<16, false><<<grid, 128, 0, stream>>>(p);
+    else rank_proj_kernel<32, false><<<grid, 128, 0, stream>>>(p);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    return WP_ERR_CUDA;
+  }
+  return WP_OK;
+}
+
+namespace {
+
+__device__ __forceinline__ void split3_bf16(float x, uint16_t* h) {
+  uint16_t a;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(a) : "f"(x));
+  const float r1 = x - __uint_as_float(static_cast<uint32_t>(a) << 16);     // exact
+  uint16_t b;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(b) : "f"(r1));
+  const float r2 = r1 - __uint_as_float(static_cast<uint32_t>(b) << 16);    // exact
+  uint16_t c;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(c) : "f"(r2));
+  h[0] = a; h[1] = b; h[2] = c;
+}
+
+}  // namespace
+
+// Grid-stride over the As elements, then over the Bs elements.
+__global__ void split3_kernel(const float* A, long long lda, int r, int K, int rp, uint16_t* As,
+                              int lda_s, const float* B, long long ldb, int out, uint16_t* Bs) {
+  const long long na = static_cast<long long>(rp) * lda_s;
+  const long long nb = static_cast<long long>(out) * rp;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < na + nb;
+       e += stride) {
+    uint16_t h[3] = {0, 0, 0};
+    if (e < na) {
+      const int j = static_cast<int>(e / lda_s), k = static_cast<int>(e % lda_s);
+      if (j < r && k < K) split3_bf16(A[j * lda + k], h);
+#pragma unroll
+      for (int i = 0; i < 3; ++i) As[(static_cast<long long>(i) * rp + j) * lda_s + k] = h[i];
+    } else {
+      const long long f = e - na;
+      const int o = static_cast<int>(f / rp), j = static_cast<int>(f % rp);
+      if (j < r) split3_bf16(B[o * ldb + j], h);
+      uint16_t* row = Bs + static_cast<long long>(o) * 6 * rp;
+      row[j] = h[0]; row[rp + j] = h[1]; row[2 * rp + j] = h[0];
+      row[3 * rp + j] = h[2]; row[4 * rp + j] = h[1]; row[5 * rp + j] = h[0];
+    }
+  }
+}
+
+int launch_split3(const float* A, long long lda, int r, int K, int rp, uint16_t* As, int lda_s,
+                  const float* B, long long ldb, int out, uint16_t* Bs, cudaStream_t stream) {
+  const long long n = static_cast<long long>(rp) * lda_s + static_cast<long long>(out) * rp;
+  const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, 4LL * device_sm_count()));
+  split3_kernel<<<blocks, 256, 0, stream>>>(A, lda, r, K, rp, As, lda_s, B, ldb, out, Bs);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_last_cuda_error(e);

@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
           // (rows [cta * htot/2, ...)); rows of a half that no adapter fills are not loaded:
           // they only feed rank columns nothing reads.
           uint32_t tx = 2u * kATileBytes;
-          for (int a = 0; a < p.n_ad; ++a) tx += p.ad[a].rpad16 * 128;
+          for (int a = 0; a < p.n_ad; ++a) tx += p.ad[a].pw * 128;
           const int half = p.htot >> 1;
           for (int kb = 0; kb < p.k_blocks; ++kb) {
             if (!(ok = mbar_wait_cluster(&empty[stage], phase ^ 1, abort_flag, tmo, status))) break;
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               if (d.cta == 2) {            // split: this CTA's half of the rows
                 const int col = cta ? d.hoff2 : d.hoff;
                 tma_load_2d_pair_hint(st + kATileBytes + (col - static_cast<int>(cta) * half) * 128,
-                                      &maps.a[a], kb * kBK, static_cast<int>(cta) * (d.rpad16 >> 1),
+                                      &maps.a[a], kb * kBK, static_cast<int>(cta) * (d.pw >> 1),
                                       fb, keep);
               } else if (d.cta == static_cast<int>(cta)) {
                 tma_load_2d_pair_hint(st + kATileBytes + (d.hoff - static_cast<int>(cta) * half) * 128,
@@ -526,14 +526,45 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         // the rank pass covers every adapter; the folded one only this group's
         for (int a = hpass_now ? 0 : a0; a < (hpass_now ? p.n_ad : a1); ++a) {
           const float s = p.ad[a].s;
-          const int units = p.ad[a].rpad16 >> 3;       // 8 ranks (16 bytes of H~) per unit
+          const int units = p.ad[a].pw >> 3;           // 8 rank-pass columns per unit
+          // TMEM column of unit u: the two halves of an adapter's columns may lie apart
+          const int hu = units >> 1;
+          auto col = [&](int u) { return u < hu ? p.ad[a].hoff + u * 8 : p.ad[a].hoff2 + (u - hu) * 8; };
+          if (p.ad[a].split3) {
+            // FP32 adapter: s X A^T = s (X a1^T + X a2^T + X a3^T) in fp32, split again into
+            // bf16 pieces h1 + h2 + h3 and laid out as [h1 h1 h2 h1 h2 h3] against the
+            // [b1 b2 b1 b3 b2 b1] of B: every product above 2^-24 of the leading one is kept
+            const int pu = units / 3;                  // units per piece
+            for (int u = 0; u < pu; ++u) {
+              uint32_t q0[8], q1[8], q2[8];
+              tmem_ld8(h_t + lane_base + col(u), q0);
+              tmem_ld8(h_t + lane_base + col(u + pu), q1);
+              tmem_ld8(h_t + lane_base + col(u + 2 * pu), q2);
+              uint32_t w1[4], w2[4], w3[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float x0 = s * ((u2f(q0[2 * i]) + u2f(q1[2 * i])) + u2f(q2[2 * i]));
+                const float x1 = s * ((u2f(q0[2 * i + 1]) + u2f(q1[2 * i + 1])) + u2f(q2[2 * i + 1]));
+                w1[i] = pack_bf16x2(x0, x1);
+                const float y0 = x0 - __uint_as_float(w1[i] << 16);
+                const float y1 = x1 - __uint_as_float(w1[i] & 0xffff0000u);
+                w2[i] = pack_bf16x2(y0, y1);
+                w3[i] = pack_bf16x2(y0 - __uint_as_float(w2[i] << 16), y1 - __uint_as_float(w2[i] & 0xffff0000u));
+              }
+              auto put = [&](int k, const uint32_t* w) {
+                const int kr = p.ad[a].toff + (k * pu + u) * 8;
+                const int unit16 = ((kr & 63) >> 3) ^ (row_in_cta & 7);
+                st_shared_v4(hbuf_addr + (kr >> 6) * kHChunkBytes + row_in_cta * 128 + unit16 * 16,
+                             w[0], w[1], w[2], w[3]);
+              };
+              put(0, w1); put(1, w1); put(2, w2); put(3, w1); put(4, w2); put(5, w3);
+            }
+            continue;
+          }
           for (int u0 = 0; u0 < units; u0 += 4) {
             // 32 ranks per TMEM load where the rank allows it, 8 otherwise
             uint32_t r[32];
             const int n = min(4, units - u0);
-            // TMEM column of unit u: the two halves of an adapter's ranks may lie apart
-            const int hu = units >> 1;
-            auto col = [&](int u) { return u < hu ? p.ad[a].hoff + u * 8 : p.ad[a].hoff2 + (u - hu) * 8; };
             if (n == 4 && col(u0 + 3) == col(u0) + 24) {
               tmem_ld32(h_t + lane_base + col(u0), r);
             } else {
