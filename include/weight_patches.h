@@ -181,9 +181,11 @@ int lora_dense_patch(void* param, int32_t param_dtype, int64_t param_numel,
  * allocator and gives plug-ins no allocation rights, fixed-budget inference servers, and
  * latency-critical paths where cudaMalloc/cudaFree (which may synchronise the device)
  * are not acceptable.  Such a caller still passes its inputs and output; the scratch that
- * FP32 adapters need (s * X A^T in fp32, T x sum of their ranks floats, and T x sum of all
- * ranks on the all-FP32 path) comes from a fixed 4 MiB array inside the library, held on
- * every device that uses it until the process exits.  The call allocates nothing.
+ * lora_workspace_size(WP_OP_FWD, ...) reports (on the tensor-core path about T x sum of the
+ * ranks rounded up to 16 x 2 bytes for the bf16 s * X A^T rows, plus the FP32 adapters'
+ * share; on the all-FP32 path T x sum of the ranks floats) comes from a fixed 4 MiB array
+ * inside the library, held on every device that uses it until the process exits.  The
+ * call allocates nothing.
  *
  * Same arguments, dtypes, alignment rules and errors as lora_linear_fwd, minus the
  * workspace.  A call that would need more than 4 MiB of scratch is rejected with
@@ -191,9 +193,9 @@ int lora_dense_patch(void* param, int32_t param_dtype, int64_t param_numel,
  * needed).  The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any stream
  * capture.  Every call on a device shares the one array and leaves its contents behind
- * (every scratch element is written before it is read, so nothing needs clearing): calls
- * whose kernels overlap on the GPU, e.g. on two streams at once, race on it and must be
- * serialised by the caller.
+ * (the call clears the few flags it needs on its stream; every other scratch element is
+ * written before it is read): calls whose kernels overlap on the GPU, e.g. on two streams
+ * at once, race on it and must be serialised by the caller.
  */
 int lora_linear_fwd_noalloc(const wp_mat* X, const wp_mat* W, const wp_mat* bias,
                             const wp_adapter* adapters, int32_t n_adapters, double request_scale,

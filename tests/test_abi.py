@@ -60,11 +60,11 @@ def _ad(r, n_in, n_out, alpha=8.0, strength=1.0, dtype=wpg.WP_BF16):
     return wpg.WpAdapter(_m(r, n_in, dtype), _m(n_out, r, dtype), alpha, strength)
 
 
-def _fwd(lib, X, W, bias, ads, Y, rs=1.0):
+def _fwd(lib, X, W, bias, ads, Y, rs=1.0, ws=None, ws_bytes=0):
     arr = (wpg.WpAdapter * max(1, len(ads)))(*ads)
     return lib.lora_linear_fwd(ctypes.byref(X), ctypes.byref(W) if W else None,
                                ctypes.byref(bias) if bias else None, arr, len(ads), rs,
-                               ctypes.byref(Y), None, 0, None)
+                               ctypes.byref(Y), ws, ws_bytes, None)
 
 
 def test_fwd_rejections(lib):
@@ -85,9 +85,11 @@ def test_fwd_rejections(lib):
     # tensor-core path alignment: row pitch not a multiple of 8 elements
     assert _fwd(lib, _m(64, 128, ld=130), W, None, [], Y) == -4
     assert _fwd(lib, X, W, None, [], _o(64, 256, ld=260)) == -4
-    # too many bf16 adapters' rank chunks for the tensor-memory rank region
+    # bf16 adapters need workspace too (their H~ rows); none given
+    assert _fwd(lib, X, W, None, [_ad(8, 128, 256)], Y) == -5
+    # too many bf16 adapters' rank columns for one tensor-memory accumulator buffer
     many = [_ad(128, 128, 256) for _ in range(3)]
-    assert _fwd(lib, X, W, None, many, Y) == -8
+    assert _fwd(lib, X, W, None, many, Y, ws=FAKE, ws_bytes=1 << 30) == -8
 
 
 def test_grouped_rejections(lib):
@@ -113,9 +115,12 @@ def test_workspace_sizes(lib):
     X, W = _m(1000, 128), _m(256, 128)
     arr = (wpg.WpAdapter * 2)(_ad(8, 128, 256), _ad(16, 128, 256, dtype=wpg.WP_FP32))
     # tensor-core path: the fp32 adapter's s * X A^T (1000 x 16 fp32, for the CUDA-core
-    # route) plus its bf16 pieces (A: 3 x 16 x 128, B: 256 x 6 x 16)
-    assert lib.lora_workspace_size(0, ctypes.byref(X), ctypes.byref(W), arr, 2) == 64000 + 12288 + 49152
-    assert lib.lora_workspace_size(0, ctypes.byref(X), ctypes.byref(W), arr, 1) == 0
+    # route), its bf16 pieces (A: 3 x 16 x 128, B: 256 x 6 x 16), the H~ rows of both
+    # adapters (1000 x (16 + 96) bf16) and one flag per 256-row block (4, padded to 256 B)
+    assert (lib.lora_workspace_size(0, ctypes.byref(X), ctypes.byref(W), arr, 2)
+            == 64000 + 12288 + 49152 + 224000 + 256)
+    assert lib.lora_workspace_size(0, ctypes.byref(X), ctypes.byref(W), arr, 1) == 32000 + 256
+    assert lib.lora_workspace_size(0, ctypes.byref(X), ctypes.byref(W), arr, 0) == 0
     Xf = _m(1000, 128, wpg.WP_FP32)
     # fp32 path: every adapter's s * X A^T, 1000 x 24 fp32, rounded up to 256 bytes
     assert lib.lora_workspace_size(0, ctypes.byref(Xf), ctypes.byref(W), arr, 2) == 96000

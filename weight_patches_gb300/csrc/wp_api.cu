@@ -115,19 +115,12 @@ bool valid_output(const wp_out* y) {
 
 size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
-// Tiles per scheduling chunk.  Pairs take chunks round-robin; one chunk per pair
-// (contiguous ranges) balances best and starts the fewest X A^T units, while smaller
-// chunks keep the pairs on nearby rows of X.  Contiguous ranges are the default.
-int chunk_tiles_for(int total, int pairs, int nt_g) {
-  (void)nt_g;
-  return (total + pairs - 1) / pairs;
-}
-
 struct FwdPlan {
   bool tc = false;        // tensor-core path
   int rank32_total = 0;   // fp32 adapters' total rank (tensor-core path)
   int rank_all = 0;       // all adapters' total rank (fp32 path)
   size_t split_bytes = 0; // bf16 pieces of the fp32 adapters (tensor-core path)
+  int htilde_cols = 0;    // H~ columns, at most (tensor-core path)
 };
 
 // FP32 adapters on the tensor-core path travel as three bf16 pieces per factor: rank
@@ -149,6 +142,9 @@ int plan_fwd(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int n, FwdP
     if (ad[i].A.dtype == WP_FP32) {
       plan->rank32_total += r;
       plan->split_bytes += split_a_bytes(r, ad[i].A.cols) + split_b_bytes(r, ad[i].B.rows);
+      plan->htilde_cols += 6 * split_rp(r);
+    } else {
+      plan->htilde_cols += static_cast<int>((r + 15) / 16 * 16);
     }
   }
   return WP_OK;
@@ -156,7 +152,12 @@ int plan_fwd(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int n, FwdP
 
 size_t fwd_workspace(const wp_mat* X, const FwdPlan& plan) {
   const size_t T = static_cast<size_t>(X->rows);
-  if (plan.tc) return plan.rank32_total ? round256(T * plan.rank32_total * 4) + plan.split_bytes : 0;
+  if (plan.tc) {
+    if (plan.htilde_cols == 0) return 0;
+    const size_t m_tiles = (T + kPairM - 1) / kPairM;
+    return round256(T * plan.rank32_total * 4) + plan.split_bytes +
+           round256(T * plan.htilde_cols * 2) + round256(m_tiles * 4);
+  }
   return plan.rank_all ? round256(T * plan.rank_all * 4) : 0;
 }
 
@@ -275,36 +276,33 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   }
   p.h_out = h_out;
   p.h_out_ld = h_out_ld;
-  // bf16 W: one rank pass per 256-row block serves every group's adapters, packed in one
-  // rank space (16-aligned); 4-bit W: a pass per (row block, group) folded into the first
-  // tile's K loop, each group's adapters at 64-rank chunks of their own.
-  p.hpass = nf4 ? 0 : 1;
-  // FP32 adapters ride on the tensor cores as bf16 pieces when their H~ (6 rp columns each)
-  // fits beside the bf16 adapters' and the bf16 W path is taken; else the FP32 CUDA-core
-  // projection plus an epilogue product carry them
+  // FP32 adapters ride on the tensor cores as bf16 pieces when every adapter's rank
+  // columns (3 rp for such an adapter) fit one accumulator buffer; else the FP32
+  // CUDA-core projection plus an epilogue product carry them
   bool split3 = false;
   {
     int n16 = 0, n32 = 0, width = 0;
     for (int i = 0; i < n_adapters; ++i) {
       if (s_of[i] == 0.0f) continue;
       const int r = static_cast<int>(adapters[i].A.rows);
-      if (adapters[i].A.dtype == WP_FP32) { ++n32; width += 6 * split_rp(r); }
+      if (adapters[i].A.dtype == WP_FP32) { ++n32; width += 3 * split_rp(r); }
       else { ++n16; width += (r + 15) / 16 * 16; }
     }
-    split3 = p.hpass && n32 > 0 && n16 + n32 <= kMaxAd && width <= kHCols && !h_out;
+    split3 = n32 > 0 && n16 + n32 <= kMaxAd && width <= kHCols && !h_out;
   }
+  // workspace: [fp32 s X A^T | bf16 pieces | H~ | row-block flags]
   const size_t h32_bytes = round256(static_cast<size_t>(T) * plan.rank32_total * 4);
   size_t split_off = h32_bytes;
+  const size_t hq_off = h32_bytes + plan.split_bytes;
+  const size_t flags_off = hq_off + round256(static_cast<size_t>(T) * plan.htilde_cols * 2);
   struct SplitJob { const wp_adapter* a; int rp, out; uint16_t* As; uint16_t* Bs; int lda_s; };
   SplitJob jobs[kMaxAd];
   int n_jobs = 0;
   const void* amap_ptr[kMaxAd]; long long amap_rows[kMaxAd], amap_ld[kMaxAd];
   const void* bmap_ptr[kMaxAd]; long long bmap_cols[kMaxAd], bmap_ld[kMaxAd];
-  int hglob = 0;
+  int hcols = 0;                           // H~ columns: every adapter packed, 16-aligned
   for (int g = 0; g < G; ++g) {
     p.ad_begin[g] = p.n_ad;
-    int chunk = 0;
-    int roff = 0;
     for (int i = 0; i < n_adapters; ++i) {
       const int ag = grouped ? i : 0;
       if (ag != g || s_of[i] == 0.0f) continue;
@@ -323,8 +321,8 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
         d.group = g; d.rank = 6 * rp; d.rpad16 = 6 * rp; d.pw = 3 * rp; d.split3 = 1;
         d.nchunks = (6 * rp + 63) / 64; d.s = s_of[i];
         d.hout_off = hout_of[i];
-        d.toff = hglob; d.roff = 0;
-        hglob += d.rpad16;
+        d.toff = hcols;
+        hcols += d.rpad16;
         amap_ptr[p.n_ad] = j.As; amap_rows[p.n_ad] = 3 * rp; amap_ld[p.n_ad] = j.lda_s;
         bmap_ptr[p.n_ad] = j.Bs; bmap_cols[p.n_ad] = 6 * rp; bmap_ld[p.n_ad] = 6 * rp;
         ++p.n_ad;
@@ -342,57 +340,46 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
         continue;
       }
       if (p.n_ad >= kMaxAd) return WP_ERR_UNSUPPORTED;
-      if (r > 256) return WP_ERR_UNSUPPORTED;
+      if (r > kHCols) return WP_ERR_UNSUPPORTED;
       if (!aligned16(a.A.data) || a.A.ld % 8 || !aligned16(a.B.data) || a.B.ld % 8)
         return WP_ERR_ALIGN;
       TcAdapter& d = p.ad[p.n_ad];
       d.group = g; d.rank = r; d.rpad16 = (r + 15) / 16 * 16; d.pw = d.rpad16; d.split3 = 0;
       d.nchunks = (r + 63) / 64; d.s = s_of[i];
+      d.hout_off = hout_of[i];
+      d.toff = hcols;
+      hcols += d.rpad16;
       amap_ptr[p.n_ad] = a.A.data; amap_rows[p.n_ad] = r; amap_ld[p.n_ad] = a.A.ld;
       bmap_ptr[p.n_ad] = a.B.data; bmap_cols[p.n_ad] = r; bmap_ld[p.n_ad] = a.B.ld;
-      d.hout_off = hout_of[i];
-      if (p.hpass) {
-        d.toff = hglob;                 // H~ columns: packed in adapter order
-        d.roff = 0;
-        hglob += d.rpad16;
-        if (hglob > kHCols) return WP_ERR_UNSUPPORTED;
-      } else {
-        d.hoff = d.toff = 64 * chunk;
-        d.hoff2 = d.hoff + d.rpad16 / 2;
-        d.roff = roff;
-        chunk += d.nchunks;
-        roff += d.rpad16 / 2;
-        if (chunk * 64 > kHCols) return WP_ERR_UNSUPPORTED;
-      }
       ++p.n_ad;
     }
-    if (chunk > p.hchunks) p.hchunks = chunk;
-    if (roff > p.rslot_rows) p.rslot_rows = roff;
   }
-  if (p.hpass && p.n_ad > 0) {
-    // split the adapters between the two CTAs of a pair (largest first, onto the lighter
-    // CTA); each CTA's adapters sit contiguously in its half of the rank-pass columns
+  p.ad_begin[G] = p.n_ad;
+  if (p.n_ad > 0) {
+    // Rank columns of the pair's MMA (N = htot): each CTA supplies the A rows of its half.
+    // Whole adapters per CTA (largest first, onto the lighter CTA) when that is no wider
+    // than splitting every adapter across both halves; else split them all.
     int order[kMaxAd];
     for (int k = 0; k < p.n_ad; ++k) order[k] = k;
     std::sort(order, order + p.n_ad, [&](int x, int y) { return p.ad[x].pw > p.ad[y].pw; });
     int load[2] = {0, 0};
+    int sum_pw = 0;
     for (int k = 0; k < p.n_ad; ++k) {
       TcAdapter& d = p.ad[order[k]];
       d.cta = load[1] < load[0] ? 1 : 0;
       d.hoff = load[d.cta];              // relative to the CTA's half, fixed up below
       load[d.cta] += d.pw;
+      sum_pw += d.pw;
     }
     int half = std::max(load[0], load[1]);
-    if (2 * half <= kHCols) {
+    if (2 * half <= sum_pw) {
       for (int k = 0; k < p.n_ad; ++k) {
         p.ad[k].hoff += p.ad[k].cta * half;
         p.ad[k].hoff2 = p.ad[k].hoff + p.ad[k].pw / 2;
       }
     } else {
-      // too lopsided to give whole adapters to one CTA: split every adapter, each CTA
-      // loading half of its rows at the same place in its half of the columns
-      half = 0;
-      for (int k = 0; k < p.n_ad; ++k) half += p.ad[k].pw / 2;
+      // each CTA loads half of every adapter's rows at the same place in its half
+      half = sum_pw / 2;
       int off = 0;
       for (int k = 0; k < p.n_ad; ++k) {
         p.ad[k].cta = 2;
@@ -401,11 +388,12 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
         off += p.ad[k].pw / 2;
       }
     }
+    if (2 * half > kHCols) return WP_ERR_UNSUPPORTED;
     p.htot = 2 * half;
-    p.hchunks = (hglob + 63) / 64;
-    p.rslot_rows = 0;
+    p.hq = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + hq_off);
+    p.hq_ld = hcols;
+    p.flags = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + flags_off);
   }
-  p.ad_begin[G] = p.n_ad;
   p.h32 = static_cast<const float*>(workspace);
   p.h32_cols = h_off;
   for (int i = 0; i < p.n_ad32; ++i) {
@@ -415,9 +403,18 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   }
   hp.H = static_cast<float*>(workspace); hp.h_cols = h_off;
 
+  // stage: X rows | bf16 W half (or 4-bit codes + block scales)
+  p.stage_bytes = kATileBytes + (nf4 ? kRawBytes + kAmBytes : kBHalfBytes);
+  const size_t fixed = 1024 + (nf4 ? static_cast<size_t>(kWRing) * kBHalfBytes : 0) + 2 * kStgBytes + 512;
+  int stages = static_cast<int>((kSmemLimit - fixed) / p.stage_bytes);
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 2) return WP_ERR_UNSUPPORTED;
+  p.stages = stages;
+  const size_t smem = fixed + static_cast<size_t>(stages) * p.stage_bytes;
+
   // Tensor maps (driver calls from here on).
-  // Each CTA of a pair loads 128 rows of X, 128 rows of the weight tile, half of an
-  // adapter's A rows and 128 rows of its B tile.
+  // Each CTA of a pair loads 128 rows of X, 128 rows of the weight tile, its share of the
+  // adapters' A rows, 128 rows of H~ and 128 rows of a B tile.
   int rc = make_map_bf16(&maps.x, X->data, K, T, X->ld, kBK, kBM);
   if (rc != WP_OK) return rc;
   if (nf4) {
@@ -438,25 +435,18 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   }
   rc = make_map(&maps.y, Y->dtype, Y->data, N, T, Y->ld, Y->dtype == WP_FP32 ? 32 : 64, kBM);
   if (rc != WP_OK) return rc;
+  if (p.n_ad > 0) {
+    rc = make_map_bf16(&maps.hq, p.hq, p.hq_ld, T, p.hq_ld, 64, kBM);
+    if (rc != WP_OK) return rc;
+  }
   for (int k = 0; k < p.n_ad; ++k) {
-    // rank pass: the whole adapter from one CTA; folded pass: each CTA's half of its rows
+    // rank item: the whole adapter from one CTA, or half of its rows from each
     rc = make_map_bf16(&maps.a[k], amap_ptr[k], K, amap_rows[k], amap_ld[k], kBK,
-                       p.hpass && p.ad[k].cta != 2 ? p.ad[k].pw : p.ad[k].pw / 2);
+                       p.ad[k].cta != 2 ? p.ad[k].pw : p.ad[k].pw / 2);
     if (rc != WP_OK) return rc;
     rc = make_map_bf16(&maps.b[k], bmap_ptr[k], bmap_cols[k], out_g, bmap_ld[k], 64, 128);
     if (rc != WP_OK) return rc;
   }
-
-  // stage: X rows | bf16 W half (or 4-bit codes, padded to 4 KiB) | rank slot
-  p.rslot_off = kATileBytes + (nf4 ? kRawBytes + kAmBytes : kBHalfBytes);
-  p.stage_bytes = p.rslot_off + p.rslot_rows * 128;
-  const size_t fixed = 1024 + (nf4 ? static_cast<size_t>(kWRing) * kBHalfBytes : 0) +
-                       static_cast<size_t>(p.hchunks) * kHChunkBytes + 2 * kStgBytes + 512;
-  int stages = static_cast<int>((kSmemLimit - fixed) / p.stage_bytes);
-  if (stages > kMaxStages) stages = kMaxStages;
-  if (stages < 2) return WP_ERR_UNSUPPORTED;
-  p.stages = stages;
-  const size_t smem = fixed + static_cast<size_t>(stages) * p.stage_bytes;
 
   if (hp.n_ad > 0) {
     rc = launch_h32(hp, stream);
@@ -469,11 +459,20 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
                        j.a->B.ld, j.out, j.Bs, stream);
     if (rc != WP_OK) return rc;
   }
+  if (p.n_ad > 0) {
+    cudaError_t e = cudaMemsetAsync(p.flags, 0, static_cast<size_t>(p.m_tiles) * 4, stream);
+    if (e != cudaSuccess) {
+      set_last_cuda_error(e);
+      return WP_ERR_CUDA;
+    }
+  }
   int pairs = tc_max_pairs(smem, nf4);
   if (pairs <= 0) return WP_ERR_CUDA;
   if (pairs > p.total_tiles) pairs = p.total_tiles;
-  p.pair_group = 1;
-  p.chunk_tiles = chunk_tiles_for(p.total_tiles, pairs / p.pair_group, p.nt_g);
+  // rank items two rounds of tiles ahead, or one when the X rows of two rounds would not
+  // stay in L2 until their tiles come
+  const double x_two_rounds = 2.0 * pairs / (G * p.nt_g) * kPairM * static_cast<double>(K) * 2;
+  p.rlead = x_two_rounds <= 48.0 * (1 << 20) ? 2 : 1;
   return launch_tc_fwd(maps, p, 2 * pairs, smem, stream, nf4);
 }
 
@@ -482,7 +481,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
 //   W^T [in, Ntot] bf16 | per group: B_g^T padded to [r_g, Ntot] bf16 | per group: A_g^T
 //   [in, r8_g] bf16 | s G [T, R] fp32 | H [T, R] fp32 | reduction partials
 struct BwdLayout {
-  size_t wt, bhat[kMaxGroups], at[kMaxGroups], gs, h, part, total;
+  size_t wt, bhat[kMaxGroups], at[kMaxGroups], gs, h, part, fwd, fwd_bytes, total;
   int r8[kMaxGroups];
   int roff[kMaxGroups];
   int R;
@@ -526,6 +525,12 @@ bool bwd_layout(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int G, B
   }
   L->part = off;
   off += round256(max_part * 4);
+  // workspace of the forward call that computes dX (H~ of dY B_g and its row-block flags)
+  int hcols = 0;
+  for (int g = 0; g < G; ++g) hcols += static_cast<int>((ad[g].A.rows + 15) / 16 * 16);
+  L->fwd = off;
+  L->fwd_bytes = round256(T * hcols * 2) + round256((T + kPairM - 1) / kPairM * 4);
+  off += L->fwd_bytes;
   L->total = off;
   return true;
 }
@@ -632,8 +637,8 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
   //    leaves s_g dY B_g (fp32) in Gs; without dX, Gs comes from the fp32 projection
   const wp_mat Wt_m{Wt, WP_BF16, K, Ntot, Ntot, nullptr};
   if (dX) {
-    rc = fwd_impl(dY, &Wt_m, nullptr, 1, false, fwd_ad, G, request_scale, dX, nullptr, 0, stream,
-                  Gs, L.R);
+    rc = fwd_impl(dY, &Wt_m, nullptr, 1, false, fwd_ad, G, request_scale, dX, ws + L.fwd,
+                  L.fwd_bytes, stream, Gs, L.R);
     if (rc != WP_OK) return rc;
   } else {
     H32Params gp{};
@@ -779,8 +784,9 @@ const char* lora_last_cuda_error(void) { return g_last_error.c_str(); }
 // that own every byte of device memory through their own allocator and give plug-ins no
 // allocation rights, fixed-budget inference servers, and latency-critical paths where
 // cudaMalloc/cudaFree (which may synchronise the device) are not acceptable.  For them the
-// scratch that the FP32-adapter projection needs (s * X A^T in fp32, T x sum(r) floats)
-// lives in a fixed array in this library's own device memory instead of a workspace.
+// forward's scratch (the bf16 s * X A^T rows of the adapters with a flag per 256-row
+// block, and for FP32 adapters their bf16 pieces or fp32 projection) lives in a fixed
+// array in this library's own device memory instead of a workspace.
 //
 // The array holds kNoAllocScratchBytes per device, for as long as the library is loaded.
 // Host code must not pass the array's name to a kernel (on the host it is only a stand-in
@@ -788,7 +794,7 @@ const char* lora_last_cuda_error(void) { return g_last_error.c_str(); }
 // the first call made with that device current, and passed to the kernels.
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;   // 4 MiB: T * sum(r) <= 1 Mi floats
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;   // 4 MiB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -24,7 +24,6 @@ constexpr int kMaxGroups = 8;
 constexpr int kHCols = 256;         // TMEM columns available for X A^T (one buffer)
 constexpr int kATileBytes = kBM * kBK * 2;      // 16 KiB: this CTA's X rows
 constexpr int kBHalfBytes = 128 * kBK * 2;      // 16 KiB: this CTA's half of a B tile
-constexpr int kHChunkBytes = kBM * 64 * 2;      // one 64-rank chunk of s*X A^T in bf16
 constexpr int kStgBytes = kBM * 128;            // output staging: 128 rows x 128 bytes
 constexpr int kTcThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kTcThreadsNF4 = 448;  // + warps 6..13: 4-bit dequantisation
@@ -43,11 +42,10 @@ struct TcAdapter {
   int split3;      // FP32 adapter as three bf16 pieces (rp = pw / 3 ranks per piece)
   int hoff;        // TMEM column of rank-pass columns [0, pw/2) of this adapter
   int hoff2;       // TMEM column of columns [pw/2, pw) (hoff + pw/2 unless split)
-  int toff;        // first column of this adapter's H~ in shared memory (multiple of 16)
+  int toff;        // first column of this adapter's H~ (multiple of 16)
   int cta;         // rank pass: the CTA of the pair that loads all A rows (0, 1), or 2 when
                    // each CTA loads half of them (the adapter is split between the halves)
   int nchunks;     // ceil(r / 64)
-  int roff;        // row offset of this CTA's rpad16/2 rows of A in a stage's rank slot
   int hout_off;    // column of this adapter's s * X A^T in TcParams::h_out (if stored)
   float s;         // combined scale, fp32
 };
@@ -65,22 +63,20 @@ struct TcParams {
   int T, K, N;                 // tokens, in_features, total out_features
   int out_g, G, nt_g;          // group width, groups, N-tiles per group
   int m_tiles, total_tiles, k_blocks;   // m_tiles counts 256-row pair blocks
-  int chunk_tiles;             // tiles per scheduling chunk
-  int pair_group;              // pairs per group: a group's pairs interleave a chunk's tiles
+  int rlead;                   // rank items run this many rounds of tiles ahead of their tiles
   int has_base;
-  int n_ad;                    // bf16 adapters
+  int n_ad;                    // adapters on the tensor cores (bf16, or FP32 as pieces)
   int ad_begin[kMaxGroups + 1];
-  int hchunks;                 // 64-rank chunks of the H~ buffer
-  int hpass;                   // bf16 W: one rank pass per 256-row block over every adapter
-  int htot;                    // rank-pass MMA width: twice the larger CTA half (<= 256)
-  int rslot_rows;              // rows of the per-stage rank slot (A rows, per CTA)
+  int htot;                    // rank-item MMA width: twice the larger CTA half (<= 256)
   int stages;
-  int stage_bytes;             // bf16 W: 32 KiB + rank slot; 4-bit W: 16 KiB + 4 KiB codes + rank slot
-  int rslot_off;               // byte offset of the rank slot inside a stage
+  int stage_bytes;             // bf16 W: 32 KiB; 4-bit W: 16 KiB + 4 KiB codes + 2 KiB scales
   const float* absmax;         // 4-bit W: [N * K / 64] fp32 block scales
   int am_tma;                  // 4-bit W: block scales arrive by TMA with the codes
   float nf4_code[16];          // 4-bit W: the NormalFloat levels
   TcAdapter ad[kMaxAd];
+  uint16_t* hq;                // [T, hq_ld] bf16: H~ = s X A^T of every adapter (toff columns)
+  int hq_ld;
+  uint32_t* flags;             // [m_tiles]: 2 once both CTAs wrote the block's H~ rows
   int n_ad32;                  // fp32 adapters (epilogue FFMA)
   TcAdapter32 ad32[kMaxAd32];
   float* h_out;                // optional [T, h_out_ld] fp32: s * X A^T of the bf16 adapters
@@ -101,6 +97,7 @@ struct TcMaps {
   CUtensorMap y;                 // output, 128-byte swizzled boxes of 128 rows
   CUtensorMap wq;                // 4-bit W codes: [N rows, K/2 bytes], boxes of 128 x 32 bytes
   CUtensorMap am;                // 4-bit W block scales: [N rows, K/64] fp32, boxes of 128 x 4
+  CUtensorMap hq;                // H~ [T rows, hq_ld], boxes of 128 rows x 64 ranks
   CUtensorMap a[kMaxAd];
   CUtensorMap b[kMaxAd];
 };

@@ -14,18 +14,21 @@
 //   * a CTA pair (cluster of 2) computes 256 x 256 output tiles with tcgen05.mma
 //     cta_group::2: each CTA stages its own 128 X rows and half of the weight tile, so
 //     every SM receives 32 KiB of operands per 64-deep K step;
-//   * each pair owns a contiguous range of tiles ordered (row block, group, column
-//     tile); consecutive tiles share their X rows and their group's adapters, a "unit";
-//   * in the first tile of a unit the K loop also runs X A_p^T (N = r_p) on the same X
-//     stage, into the idle tensor-memory accumulator buffer; the epilogue warps scale
-//     it by the runtime s_p, round it once to bf16 and park it in shared memory in the
-//     MMA operand layout (H~);
-//   * every tile then adds H~ B_tile^T (K = r) into its own accumulator, so the
-//     [T, out] delta never leaves tensor memory;
-//   * two accumulator buffers (2 x 256 TMEM columns) let the epilogue of tile n overlap
-//     the MMAs of tile n+1; the epilogue adds the bias and the FP32 adapters' terms
-//     (sum_j (s X A32^T)[t, j] B32[o, j], FFMA, before the single rounding) and writes
-//     bf16 or fp32 rows through TMA bulk stores;
+//   * output tiles are dealt round-robin to the pairs, so the pairs busy at any moment
+//     share a few 256-row blocks of X and sweep W together (both stay in L2); per row
+//     block m, a rank item computes X_m A^T for every adapter at once (one MMA of
+//     N = total rank per K step), one or two rounds of tiles before the tiles of m;
+//   * the rank item's epilogue scales X A^T by the runtime s_p, rounds it once to bf16
+//     (H~) and writes it to a small [T, total rank] buffer, then releases a flag for row
+//     block m; every tile of m waits for that flag before its second contraction
+//     H~ B_tile^T (K = r), which TMA feeds like extra K steps and which accumulates onto
+//     the base tile in tensor memory, so the [T, out] delta never leaves the SM;
+//   * an FP32 adapter rides on the same path as bf16 pieces (A = a1 + a2 + a3, the same
+//     for B and for s X A^T), keeping every product above 2^-24 of the leading one;
+//   * two accumulator buffers (2 x 256 TMEM columns) let the epilogue of item n overlap
+//     the MMAs of item n+1; the tile epilogue adds the bias (and, for FP32 adapters too
+//     wide for the pieces, sum_j (s X A32^T)[t, j] B32[o, j] by FFMA) before the single
+//     rounding and writes bf16 or fp32 rows through TMA bulk stores;
 //   * with a 4-bit NormalFloat base weight, TMA brings the packed codes (32 bytes per row
 //     per K step) and eight dequantisation warps per CTA turn them into the bf16 weight
 //     tile in shared memory -- bf16(fl32(level[q]) * absmax) through a per-row, per-block
@@ -34,9 +37,9 @@
 // Warp roles per CTA: warp 0 issues TMA loads (both CTAs), warp 1 allocates tensor
 // memory (both CTAs) and issues the pair MMAs (leader CTA only), warps 2..5 are the
 // epilogue (one token row per thread), warps 6..13 dequantise (4-bit weights only).
-// Operands are K-major bf16 in the 128-byte swizzle layout.  Every mbarrier wait is
-// bounded (wall clock); on expiry the CTA records WP_ERR_TIMEOUT, waits for its own copies
-// in flight, frees tensor memory and returns.
+// Operands are K-major bf16 in the 128-byte swizzle layout.  Every wait (mbarrier or
+// flag) is bounded (wall clock); on expiry the CTA records WP_ERR_TIMEOUT, waits for its
+// own copies in flight, frees tensor memory and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -53,6 +56,7 @@ struct Tile {
   int m, g, j;
 };
 
+// Tile L in (row block, column group, column tile) order.
 __device__ __forceinline__ Tile decode_tile(const TcParams& p, int L) {
   Tile t;
   const int mg = L / p.nt_g;
@@ -60,6 +64,44 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, int L) {
   t.m = mg / p.G;
   t.g = mg - t.m * p.G;
   return t;
+}
+
+// Work items of one pair.  Output tiles are dealt round-robin: round k of pair q is tile
+// q + k * npairs.  The rank item of row block m belongs to pair m mod npairs and runs at
+// the start of that pair's round r(m) - rlead, where r(m) = floor(m * tpb / npairs) is
+// the first round that can hold a tile of m (or as soon as the pair has no tiles left).
+// A tile of round k waits only for rank items of rounds < k, and every pair walks its
+// items in order, so the schedule cannot deadlock while all pairs are resident.
+struct Item {
+  bool rank;   // rank item (X_m A^T of every adapter) rather than an output tile
+  int m;       // row block
+  Tile t;      // the tile (output items)
+};
+
+struct ItemIter {
+  int k;        // next tile round of this pair
+  int m_next;   // next row block whose rank item this pair owns
+};
+
+__device__ __forceinline__ bool next_item(ItemIter& s, const TcParams& p, int pair, int npairs,
+                                          Item& it) {
+  const int tile_pos = pair + s.k * npairs;
+  if (p.n_ad > 0 && s.m_next < p.m_tiles) {
+    const int due = static_cast<int>((static_cast<long long>(s.m_next) * p.G * p.nt_g) / npairs) - p.rlead;
+    if (due <= s.k || tile_pos >= p.total_tiles) {
+      it.rank = true;
+      it.m = s.m_next;
+      it.t = Tile{0, 0, 0};
+      s.m_next += npairs;
+      return true;
+    }
+  }
+  if (tile_pos >= p.total_tiles) return false;
+  it.rank = false;
+  it.t = decode_tile(p, tile_pos);
+  it.m = it.t.m;
+  ++s.k;
+  return true;
 }
 
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
@@ -91,49 +133,11 @@ __device__ __forceinline__ void lookup4(uint32_t codes, const uint32_t (&lo)[4],
 
 constexpr uint16_t kBothCtas = 0x3;
 
-// Tile order.  Pairs form groups of `pair_group`; chunks of `chunk_tiles` consecutive tiles
-// in (row block, group, column tile) order go to the groups round-robin, and the pairs of a
-// group take every pair_group-th tile of the chunk, so they work on the same X rows at the
-// same time.  Every role of every CTA walks the same sequence.
-struct Sched {
-  int c;        // next chunk of this pair's group
-  int L;        // current tile (-1 before the first)
-  int c_end;    // end of the current chunk
-  int prev_mg;  // (row block, group) of the previous tile, -1 before the first
-};
-
-__device__ __forceinline__ bool sched_next(Sched& s, const TcParams& p, int q, int ngroups,
-                                           int nchunks) {
-  const int PG = p.pair_group, CH = p.chunk_tiles;
-  int L = s.L < 0 ? -1 : s.L + PG;
-  while (L < 0 || L >= s.c_end) {
-    if (s.c >= nchunks) return false;
-    L = s.c * CH + q;
-    s.c_end = min(s.c * CH + CH, p.total_tiles);
-    s.c += ngroups;
-  }
-  s.L = L;
-  return true;
-}
-
-// True when tile t starts a new unit for this pair: a new 256-row block in rank-pass mode
-// (one X A^T pass serves every group), a new (row block, group) otherwise.
-__device__ __forceinline__ bool sched_new_unit(Sched& s, const TcParams& p, const Tile& t) {
-  const int key = p.hpass ? t.m : t.m * p.G + t.g;
-  const bool fresh = key != s.prev_mg;
-  s.prev_mg = key;
-  return fresh;
-}
-
-// Shared-memory descriptor of rank k of the H~ buffer (64-rank chunks of 128 rows, 128-byte
-// swizzle); k is a multiple of 16, so a 16-rank K step never leaves its chunk.
-__device__ __forceinline__ uint64_t htilde_desc(uint32_t hbuf_addr, int k) {
-  return sw128_kmajor_desc(hbuf_addr + (k >> 6) * kHChunkBytes + (k & 63) * 2);
-}
-
 }  // namespace
 
-template <bool kNF4>
+// kF32: the epilogue also adds FP32 adapters by FFMA (those too wide to ride as bf16
+// pieces); a separate instantiation so that the common kernels do not carry its registers.
+template <bool kNF4, bool kF32>
 __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     tc_fused_fwd_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -141,21 +145,20 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
   const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base_addr - raw_addr);
 
-  // Stage s: [X rows 16 KiB | bf16 W half 16 KiB, or 4-bit codes 4 KiB | rank slot]
+  // Stage s: [X rows (or H~ rows) 16 KiB | bf16 W half (or B) 16 KiB], or with a 4-bit W
+  // [X 16 KiB | codes 4 KiB | block scales 2 KiB]; a step with two bf16 operands other
+  // than W (rank K step, second contraction) then takes two stages, one per operand.
   const int S = p.stages;
   const int SB = p.stage_bytes;
   uint8_t* wring = sbase + S * SB;                      // 4-bit W: dequantised tiles
-  uint8_t* hbuf = wring + (kNF4 ? kWRing * kBHalfBytes : 0);
-  uint8_t* stg = hbuf + p.hchunks * kHChunkBytes;       // 2 output staging buffers
+  uint8_t* stg = wring + (kNF4 ? kWRing * kBHalfBytes : 0);   // 2 output staging buffers
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg + 2 * kStgBytes);
   uint64_t* full = bars;                  // [S]  leader: TMA bytes of both CTAs landed
   uint64_t* empty = bars + S;             // [S]  both: the pair MMAs consumed the stage
   uint64_t* acc_full = bars + 2 * S;      // [2]  both: accumulator buffer ready
   uint64_t* acc_empty = acc_full + 2;     // [2]  leader: both epilogues drained it
-  uint64_t* h_full = acc_full + 4;        //      both: X A^T of the unit is in TMEM
-  uint64_t* h_ready = acc_full + 5;       //      leader: both CTAs wrote their H~ rows
-  uint64_t* drain = acc_full + 6;         //      leader: every MMA issued has finished
-  uint64_t* raw_full = acc_full + 7;      // [S]  4-bit W, local: this CTA's codes landed
+  uint64_t* drain = acc_full + 4;         //      leader: every MMA issued has finished
+  uint64_t* raw_full = acc_full + 5;      // [S]  4-bit W, local: this CTA's codes landed
   uint64_t* wfull = raw_full + S;         // [kWRing] leader: both CTAs' tiles dequantised
   uint64_t* wempty = wfull + kWRing;      // [kWRing] both: the MMAs consumed the tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + kWRing);
@@ -176,8 +179,6 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     mbar_init(&acc_full[1], 1);
     mbar_init(&acc_empty[0], 8);          // 4 epilogue warps x 2 CTAs
     mbar_init(&acc_empty[1], 8);
-    mbar_init(h_full, 1);
-    mbar_init(h_ready, 8);
     mbar_init(drain, 1);
     for (int w = 0; w < kWRing; ++w) {
       mbar_init(&wfull[w], 16);           // 8 dequantisation warps x 2 CTAs
@@ -189,6 +190,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&maps.x);
     if (p.has_base) tma_prefetch_desc(kNF4 ? &maps.wq : &maps.w);
+    if (p.n_ad > 0) tma_prefetch_desc(&maps.hq);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, 512);
@@ -200,113 +202,118 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Pair `pair` takes chunks pair, pair + npairs, ... of `chunk_tiles` consecutive tiles
-  // in (row block, group, column tile) order; each chunk reuses its X A^T across its tiles.
+  // Pair `pair` takes items pair, pair + npairs, pair + 2 npairs, ...
   const int npairs = static_cast<int>(gridDim.x >> 1);
   const int pair = static_cast<int>(blockIdx.x >> 1);
-  const int ngroups = npairs / p.pair_group;
-  const int group = pair / p.pair_group;
-  const int q_in_group = pair % p.pair_group;
-  const int nchunks = (p.total_tiles + p.chunk_tiles - 1) / p.chunk_tiles;
   const uint64_t tmo = p.timeout_ns;
   int* status = &g_tc_status;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
-      const uint64_t keep = l2_evict_last();   // weights and adapters: re-read by every row block
+      const uint64_t keep = l2_evict_last();   // W, A, B and H~ are re-read by many tiles
       int stage = 0;
       uint32_t phase = 0;
       int issued[kMaxStages];
       for (int s = 0; s < kMaxStages; ++s) issued[s] = 0;
       bool ok = true;
-      Sched sc{group, -1, 0, -1};
-      while (ok && sched_next(sc, p, q_in_group, ngroups, nchunks)) {
-        const int L = sc.L;
-        const Tile t = decode_tile(p, L);
-        const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
-        const bool lora = a1 > a0;
-        const bool new_unit = sched_new_unit(sc, p, t);
-        const bool hpass_now = !kNF4 && p.hpass && new_unit && p.n_ad > 0;
-        const bool first = kNF4 && new_unit && lora;     // rank pass folded into the K loop
-        const int x_row = t.m * kPairM + static_cast<int>(cta) * kBM;
-        if (hpass_now) {
-          // rank pass of the row block: X rows and every adapter's A rows.  Each adapter is
-          // loaded whole by one CTA of the pair into that CTA's half of the rank space
-          // (rows [cta * htot/2, ...)); rows of a half that no adapter fills are not loaded:
-          // they only feed rank columns nothing reads.
-          uint32_t tx = 2u * kATileBytes;
-          for (int a = 0; a < p.n_ad; ++a) tx += p.ad[a].pw * 128;
-          const int half = p.htot >> 1;
+      // Claim the next stage once the MMAs have released it; the leader's full barrier
+      // expects `tx` bytes from both CTAs.
+      auto claim = [&](uint32_t tx, uint8_t*& st, uint32_t& fb) -> bool {
+        if (!mbar_wait_cluster(&empty[stage], phase ^ 1, abort_flag, tmo, status)) return false;
+        st = sbase + stage * SB;
+        fb = mapa_shared(smem_u32(&full[stage]), 0);
+        if (leader) mbar_arrive_expect_tx(&full[stage], tx);
+        return true;
+      };
+      auto advance = [&]() {
+        ++issued[stage];
+        if (++stage == S) { stage = 0; phase ^= 1; }
+      };
+      uint32_t rank_tx = 0;                     // A rows of every adapter, both CTAs
+      for (int a = 0; a < p.n_ad; ++a) rank_tx += p.ad[a].pw * 128;
+      const int half = p.htot >> 1;
+      ItemIter iter{0, pair};
+      Item it;
+      while (ok && next_item(iter, p, pair, npairs, it)) {
+        const int x_row = it.m * kPairM + static_cast<int>(cta) * kBM;
+        if (it.rank) {
+          // X rows of the block and every adapter's A rows.  An adapter is loaded whole by
+          // one CTA of the pair into its half of the rank columns, or split between them;
+          // rows of a half that no adapter fills are not loaded (their columns are unread).
           for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!(ok = mbar_wait_cluster(&empty[stage], phase ^ 1, abort_flag, tmo, status))) break;
-            uint8_t* st = sbase + stage * SB;
-            const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-            if (leader) mbar_arrive_expect_tx(&full[stage], tx);
+            uint8_t* st;
+            uint32_t fb;
+            if (!(ok = claim(kNF4 ? 2u * kATileBytes : 2u * kATileBytes + rank_tx, st, fb))) break;
             tma_load_2d_pair(st, &maps.x, kb * kBK, x_row, fb);
+            uint8_t* ra = st + kATileBytes;
+            if (kNF4) {
+              mbar_arrive(&raw_full[stage]);      // no codes in this stage
+              advance();
+              if (!(ok = claim(rank_tx, st, fb))) break;
+              ra = st;
+            }
             for (int a = 0; a < p.n_ad; ++a) {
               const TcAdapter& d = p.ad[a];
-              if (d.cta == 2) {            // split: this CTA's half of the rows
+              if (d.cta == 2) {
                 const int col = cta ? d.hoff2 : d.hoff;
-                tma_load_2d_pair_hint(st + kATileBytes + (col - static_cast<int>(cta) * half) * 128,
-                                      &maps.a[a], kb * kBK, static_cast<int>(cta) * (d.pw >> 1),
-                                      fb, keep);
+                tma_load_2d_pair_hint(ra + (col - static_cast<int>(cta) * half) * 128, &maps.a[a],
+                                      kb * kBK, static_cast<int>(cta) * (d.pw >> 1), fb, keep);
               } else if (d.cta == static_cast<int>(cta)) {
-                tma_load_2d_pair_hint(st + kATileBytes + (d.hoff - static_cast<int>(cta) * half) * 128,
-                                      &maps.a[a], kb * kBK, 0, fb, keep);
+                tma_load_2d_pair_hint(ra + (d.hoff - static_cast<int>(cta) * half) * 128, &maps.a[a],
+                                      kb * kBK, 0, fb, keep);
               }
             }
-            ++issued[stage];
-            if (++stage == S) { stage = 0; phase ^= 1; }
+            if (kNF4) mbar_arrive(&raw_full[stage]);
+            advance();
           }
+          continue;
         }
-        if (ok && (p.has_base || first)) {
-          uint32_t tx = (p.has_base && !kNF4 ? 4u : 2u) * kATileBytes;     // both CTAs
-          if (first)
-            for (int a = a0; a < a1; ++a) tx += p.ad[a].rpad16 * 128;
+        const Tile& t = it.t;
+        const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
+        if (p.has_base) {
           const int w_row = t.g * p.out_g + t.j * kBN + static_cast<int>(cta) * 128;
           for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!(ok = mbar_wait_cluster(&empty[stage], phase ^ 1, abort_flag, tmo, status))) break;
-            uint8_t* st = sbase + stage * SB;
-            const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-            if (leader) mbar_arrive_expect_tx(&full[stage], tx);
+            uint8_t* st;
+            uint32_t fb;
+            if (!(ok = claim((kNF4 ? 2u : 4u) * kATileBytes, st, fb))) break;
             tma_load_2d_pair(st, &maps.x, kb * kBK, x_row, fb);
-            if (p.has_base) {
-              if (kNF4) {
-                // this CTA's codes complete on its own barrier; the dequantisation warps
-                // turn them into the bf16 tile the MMA reads
-                mbar_arrive_expect_tx(&raw_full[stage], kRawBytes + (p.am_tma ? kAmBytes : 0));
-                tma_load_2d(st + kATileBytes, &maps.wq, kb * (kBK / 2), w_row, &raw_full[stage]);
-                // the block scales of this K step and the next three (16-byte boxes)
-                if (p.am_tma)
-                  tma_load_2d(st + kATileBytes + kRawBytes, &maps.am, kb & ~3, w_row, &raw_full[stage]);
-              } else {
-                tma_load_2d_pair_hint(st + kATileBytes, &maps.w, kb * kBK, w_row, fb, keep);
-              }
-            } else if (kNF4) {
-              mbar_arrive(&raw_full[stage]);
+            if (kNF4) {
+              // this CTA's codes complete on its own barrier; the dequantisation warps
+              // turn them into the bf16 tile the MMA reads
+              mbar_arrive_expect_tx(&raw_full[stage], kRawBytes + (p.am_tma ? kAmBytes : 0));
+              tma_load_2d(st + kATileBytes, &maps.wq, kb * (kBK / 2), w_row, &raw_full[stage]);
+              // the block scales of this K step and the next three (16-byte boxes)
+              if (p.am_tma)
+                tma_load_2d(st + kATileBytes + kRawBytes, &maps.am, kb & ~3, w_row, &raw_full[stage]);
+            } else {
+              tma_load_2d_pair_hint(st + kATileBytes, &maps.w, kb * kBK, w_row, fb, keep);
             }
-            if (first)
-              for (int a = a0; a < a1; ++a)
-                tma_load_2d_pair_hint(st + p.rslot_off + p.ad[a].roff * 128, &maps.a[a], kb * kBK,
-                                      static_cast<int>(cta) * (p.ad[a].rpad16 >> 1), fb, keep);
-            ++issued[stage];
-            if (++stage == S) { stage = 0; phase ^= 1; }
+            advance();
           }
+          if (!ok) break;
         }
-        if (ok && lora) {
+        if (a1 > a0) {
+          // second contraction: H~ of this row block (written by its rank item) and B
+          if (!(ok = flag_wait(p.flags + t.m, 2u, abort_flag, tmo, status))) break;
+          fence_proxy_async_global();
           const int b_row = t.j * kBN + static_cast<int>(cta) * 128;
           for (int a = a0; a < a1 && ok; ++a) {
             for (int c = 0; c < p.ad[a].nchunks; ++c) {
-              if (!(ok = mbar_wait_cluster(&empty[stage], phase ^ 1, abort_flag, tmo, status))) break;
-              uint8_t* st = sbase + stage * SB;
-              const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-              if (leader) mbar_arrive_expect_tx(&full[stage], 2u * kBHalfBytes);
-              // with a 4-bit W the stage has no bf16 weight slot: B rides in the X slot
-              tma_load_2d_pair_hint(st + (kNF4 ? 0 : kATileBytes), &maps.b[a], c * 64, b_row, fb, keep);
-              if (kNF4) mbar_arrive(&raw_full[stage]);      // keep the code barrier in phase
-              ++issued[stage];
-              if (++stage == S) { stage = 0; phase ^= 1; }
+              uint8_t* st;
+              uint32_t fb;
+              if (!(ok = claim((kNF4 ? 2u : 4u) * kATileBytes, st, fb))) break;
+              tma_load_2d_pair_hint(st, &maps.hq, p.ad[a].toff + 64 * c, x_row, fb, keep);
+              uint8_t* bs = st + kATileBytes;
+              if (kNF4) {
+                mbar_arrive(&raw_full[stage]);
+                advance();
+                if (!(ok = claim(2u * kBHalfBytes, st, fb))) break;
+                bs = st;
+              }
+              tma_load_2d_pair_hint(bs, &maps.b[a], c * 64, b_row, fb, keep);
+              if (kNF4) mbar_arrive(&raw_full[stage]);
+              advance();
             }
           }
         }
@@ -332,147 +339,92 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       uint32_t wphase = 0;
       uint32_t nuse[2] = {0, 0};
       int count = 0;
-      uint32_t unit_phase = 0;
-      bool h_pending = false;                  // a rank pass whose H~ the MMAs have not waited for
-      int h_buf = 0;                           // accumulator buffer holding that pass's X A^T
       const uint32_t idesc_acc = idesc_bf16_f32(kPairM, kBN);
-      const uint32_t hbuf_addr = smem_u32(hbuf);
+      const uint32_t idesc_h = idesc_bf16_f32(kPairM, p.htot > 0 ? p.htot : 16);
       const uint32_t stage_base = smem_u32(sbase);
       const uint32_t wring_base = smem_u32(wring);
       bool ok = true;
-      Sched sc{group, -1, 0, -1};
-      while (ok && sched_next(sc, p, q_in_group, ngroups, nchunks)) {
-        const int L = sc.L;
-        const Tile t = decode_tile(p, L);
-        const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
-        const bool lora = a1 > a0;
-        const bool new_unit = sched_new_unit(sc, p, t);
-        const bool hpass_now = !kNF4 && p.hpass && new_unit && p.n_ad > 0;
-        const bool first = kNF4 && new_unit && lora;     // rank pass folded into the K loop
+      // Operands of a step with two bf16 operands: A in this stage's first slot, B in
+      // its second slot (bf16 W) or in the next stage's first slot (4-bit W).
+      int s0 = 0, s1 = 0;
+      auto take = [&](uint32_t& a_st, uint32_t& b_st) -> bool {
+        if (!mbar_wait(&full[stage], phase, abort_flag, tmo, status)) return false;
+        s0 = stage;
+        if (++stage == S) { stage = 0; phase ^= 1; }
+        if (kNF4) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, tmo, status)) return false;
+          s1 = stage;
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
+        tc_fence_after();
+        a_st = stage_base + s0 * SB;
+        b_st = kNF4 ? stage_base + s1 * SB : a_st + kATileBytes;
+        return true;
+      };
+      auto give_back = [&]() {
+        mma_commit_pair_mc(&empty[s0], kBothCtas);
+        if (kNF4) mma_commit_pair_mc(&empty[s1], kBothCtas);
+      };
+      ItemIter iter{0, pair};
+      Item it;
+      while (next_item(iter, p, pair, npairs, it)) {
+        const int a0 = it.rank ? 0 : p.ad_begin[it.t.g];
+        const int a1 = it.rank ? 0 : p.ad_begin[it.t.g + 1];
+        if (!it.rank && !(p.has_base || a1 > a0)) continue;   // bias-only tile: no MMA
         const int b = count & 1;
-        if (hpass_now) {
-          // the previous unit's H~ must be out of tensor memory before this pass reuses it
-          if (h_pending) {
-            if (!(ok = mbar_wait_cluster(h_ready, unit_phase, abort_flag, tmo, status))) break;
-            unit_phase ^= 1;
-            h_pending = false;
-          }
-          if (!(ok = mbar_wait_cluster(&acc_empty[b ^ 1], (nuse[b ^ 1] & 1) ^ 1, abort_flag, tmo, status)))
-            break;
-          tc_fence_after();
-          // one MMA per K step covers every adapter: N = htot ranks into the idle buffer
-          const uint32_t h_t = tmem + (b ^ 1) * kBN;
-          const uint32_t idesc_h = idesc_bf16_f32(kPairM, p.htot);
-          for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
-            tc_fence_after();
-            const uint32_t st = stage_base + stage * SB;
-            const uint64_t ad = sw128_kmajor_desc(st);
-            const uint64_t rd = sw128_kmajor_desc(st + kATileBytes);
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-              mma_bf16_pair(h_t, ad + 2 * kk, rd + 2 * kk, idesc_h, (kb | kk) != 0 ? 1u : 0u);
-            mma_commit_pair_mc(&empty[stage], kBothCtas);
-            if (++stage == S) { stage = 0; phase ^= 1; }
-          }
-          if (!ok) break;
-          mma_commit_pair_mc(h_full, kBothCtas);
-          h_pending = true;
-          h_buf = b ^ 1;
-        }
-        if (!(p.has_base || lora)) continue;
-        if (h_pending && b == h_buf) {
-          // this tile's accumulator still holds the unit's X A^T: wait for the epilogue
-          if (!(ok = mbar_wait_cluster(h_ready, unit_phase, abort_flag, tmo, status))) break;
-          unit_phase ^= 1;
-          h_pending = false;
-        }
         if (!(ok = mbar_wait_cluster(&acc_empty[b], (nuse[b] & 1) ^ 1, abort_flag, tmo, status)))
-          break;
-        if (first &&
-            !(ok = mbar_wait_cluster(&acc_empty[b ^ 1], (nuse[b ^ 1] & 1) ^ 1, abort_flag, tmo, status)))
           break;
         tc_fence_after();
         const uint32_t acc_t = tmem + b * kBN;
-        const uint32_t h_t = tmem + (b ^ 1) * kBN;
-        if (p.has_base || first) {
-          // first tile of a unit (4-bit W): the same K loop also runs X A_p^T into the other buffer
-          const int na = first ? a1 - a0 : 0;
-          uint32_t hcol[kMaxAd], roffd[kMaxAd], hid[kMaxAd];
-#pragma unroll
-          for (int i = 0; i < kMaxAd; ++i) {
-            const int a = min(a0 + i, kMaxAd - 1);
-            hcol[i] = h_t + p.ad[a].hoff;
-            roffd[i] = static_cast<uint32_t>(p.ad[a].roff * 128) >> 4;
-            hid[i] = idesc_bf16_f32(kPairM, p.ad[a].rpad16);
-          }
+        if (it.rank) {
+          // one MMA per K step covers every adapter: N = htot rank columns
           for (int kb = 0; kb < p.k_blocks; ++kb) {
-            if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
-            if (kNF4 && p.has_base &&
-                !(ok = mbar_wait_cluster(&wfull[wb], wphase, abort_flag, tmo, status)))
-              break;
-            tc_fence_after();
-            const uint32_t st = stage_base + stage * SB;
-            const uint64_t ad = sw128_kmajor_desc(st);
-            const uint64_t bd = sw128_kmajor_desc(kNF4 ? wring_base + wb * kBHalfBytes : st + kATileBytes);
-            // MMAs grouped by destination: alternating accumulators within a K step stalls
-            // the tensor pipe, so the base tile's four K steps go first, then each adapter's
-            if (p.has_base) {
+            uint32_t a_st, b_st;
+            if (!(ok = take(a_st, b_st))) break;
+            const uint64_t ad = sw128_kmajor_desc(a_st);
+            const uint64_t rd = sw128_kmajor_desc(b_st);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_bf16_pair(acc_t, ad + 2 * kk, rd + 2 * kk, idesc_h, (kb | kk) != 0 ? 1u : 0u);
+            give_back();
+          }
+        } else {
+          if (p.has_base) {
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+              if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
+              if (kNF4 && !(ok = mbar_wait_cluster(&wfull[wb], wphase, abort_flag, tmo, status)))
+                break;
+              tc_fence_after();
+              const uint32_t st = stage_base + stage * SB;
+              const uint64_t ad = sw128_kmajor_desc(st);
+              const uint64_t bd = sw128_kmajor_desc(kNF4 ? wring_base + wb * kBHalfBytes : st + kATileBytes);
 #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk)
                 mma_bf16_pair(acc_t, ad + 2 * kk, bd + 2 * kk, idesc_acc, (kb | kk) != 0 ? 1u : 0u);
-            }
-            if (na > 0) {
-              const uint64_t rd = sw128_kmajor_desc(st + p.rslot_off);
-#pragma unroll
-              for (int i = 0; i < kMaxAd; ++i) {
-                if (i < na) {
-#pragma unroll
-                  for (int kk = 0; kk < kBK / 16; ++kk)
-                    mma_bf16_pair(hcol[i], ad + 2 * kk, rd + roffd[i] + 2 * kk, hid[i],
-                                  (kb | kk) != 0 ? 1u : 0u);
-                }
-              }
-            }
-            mma_commit_pair_mc(&empty[stage], kBothCtas);
-            if (++stage == S) { stage = 0; phase ^= 1; }
-            if (kNF4 && p.has_base) {
-              mma_commit_pair_mc(&wempty[wb], kBothCtas);
-              if (++wb == kWRing) { wb = 0; wphase ^= 1; }
-            }
-          }
-          if (!ok) break;
-        }
-        bool accum = p.has_base != 0;
-        if (lora) {
-          if (first) {
-            mma_commit_pair_mc(h_full, kBothCtas);
-            if (!(ok = mbar_wait_cluster(h_ready, unit_phase, abort_flag, tmo, status))) break;
-            tc_fence_after();
-            unit_phase ^= 1;
-          } else if (h_pending) {
-            if (!(ok = mbar_wait_cluster(h_ready, unit_phase, abort_flag, tmo, status))) break;
-            tc_fence_after();
-            unit_phase ^= 1;
-            h_pending = false;
-          }
-          for (int a = a0; a < a1 && ok; ++a) {
-            for (int c = 0; c < p.ad[a].nchunks; ++c) {
-              if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
-              tc_fence_after();
-              const uint32_t st = stage_base + stage * SB;
-              const int kext = min(64, p.ad[a].rpad16 - 64 * c);
-              const uint64_t bd = sw128_kmajor_desc(st + (kNF4 ? 0 : kATileBytes));
-              for (int kk = 0; kk < kext / 16; ++kk)
-                mma_bf16_pair(acc_t, htilde_desc(hbuf_addr, p.ad[a].toff + 64 * c + 16 * kk),
-                              bd + 2 * kk, idesc_acc, (accum || kk > 0) ? 1u : 0u);
-              accum = true;
               mma_commit_pair_mc(&empty[stage], kBothCtas);
               if (++stage == S) { stage = 0; phase ^= 1; }
+              if (kNF4) {
+                mma_commit_pair_mc(&wempty[wb], kBothCtas);
+                if (++wb == kWRing) { wb = 0; wphase ^= 1; }
+              }
             }
           }
-          if (!ok) break;
+          bool accum = p.has_base != 0;
+          for (int a = a0; a < a1 && ok; ++a) {
+            for (int c = 0; c < p.ad[a].nchunks; ++c) {
+              uint32_t h_st, b_st;
+              if (!(ok = take(h_st, b_st))) break;
+              const int kext = min(64, p.ad[a].rpad16 - 64 * c);
+              const uint64_t hd = sw128_kmajor_desc(h_st);
+              const uint64_t bd = sw128_kmajor_desc(b_st);
+              for (int kk = 0; kk < kext / 16; ++kk)
+                mma_bf16_pair(acc_t, hd + 2 * kk, bd + 2 * kk, idesc_acc, (accum || kk > 0) ? 1u : 0u);
+              accum = true;
+              give_back();
+            }
+          }
         }
+        if (!ok) break;
         mma_commit_pair_mc(&acc_full[b], kBothCtas);
         ++nuse[b];
         ++count;
@@ -494,39 +446,32 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
     const int row_in_cta = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    const uint32_t hbuf_addr = smem_u32(hbuf);
-    const uint32_t stg_addr = hbuf_addr + p.hchunks * kHChunkBytes;
+    const uint32_t stg_addr = smem_u32(stg);
     const bool elected = threadIdx.x == 64;
     const uint32_t acc_empty_l[2] = {mapa_shared(smem_u32(&acc_empty[0]), 0),
                                      mapa_shared(smem_u32(&acc_empty[1]), 0)};
-    const uint32_t h_ready_l = mapa_shared(smem_u32(h_ready), 0);
     const uint64_t stream_out = l2_evict_first();   // Y is written once: keep X and W in L2
     const int cw = p.y_f32 ? 32 : 64;               // columns per 128-byte row chunk
     uint32_t nuse[2] = {0, 0};
     int count = 0;
-    uint32_t unit_phase = 0;
     uint32_t sidx = 0;                              // staging chunks issued so far
-    Sched sc{group, -1, 0, -1};
-    while (sched_next(sc, p, q_in_group, ngroups, nchunks)) {
-      const int L = sc.L;
-      const Tile t = decode_tile(p, L);
-      const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
-      const bool lora = a1 > a0;
-      const bool new_unit = sched_new_unit(sc, p, t);
-      const bool hpass_now = !kNF4 && p.hpass && new_unit && p.n_ad > 0;
-      const bool first = kNF4 && new_unit && lora;
-      const bool any_mma = p.has_base || lora;
+    ItemIter iter{0, pair};
+    Item it;
+    while (next_item(iter, p, pair, npairs, it)) {
       const int b = count & 1;
-      if (hpass_now || first) {
-        const bool ok = mbar_wait_cluster(h_full, unit_phase, abort_flag, tmo, status);
-        if (named_bar_any(!ok, 2, 128)) break;
+      if (it.rank) {
+        // s X A^T of every adapter -> bf16 H~ rows of this block in global memory (and
+        // the fp32 values in h_out when asked), then the block's flag
+        const bool okw = mbar_wait_cluster(&acc_full[b], nuse[b] & 1, abort_flag, tmo, status);
+        if (named_bar_any(!okw, 2, 128)) break;
         tc_fence_after();
-        unit_phase ^= 1;
-        const uint32_t h_t = tmem + (b ^ 1) * kBN;
-        // the rank pass covers every adapter; the folded one only this group's
-        for (int a = hpass_now ? 0 : a0; a < (hpass_now ? p.n_ad : a1); ++a) {
+        const uint32_t h_t = tmem + b * kBN;
+        const int row = it.m * kPairM + static_cast<int>(cta) * kBM + row_in_cta;
+        const bool row_ok = row < p.T;
+        uint16_t* hrow = p.hq + static_cast<long long>(row_ok ? row : 0) * p.hq_ld;
+        for (int a = 0; a < p.n_ad; ++a) {
           const float s = p.ad[a].s;
-          const int units = p.ad[a].pw >> 3;           // 8 rank-pass columns per unit
+          const int units = p.ad[a].pw >> 3;           // 8 rank columns per unit
           // TMEM column of unit u: the two halves of an adapter's columns may lie apart
           const int hu = units >> 1;
           auto col = [&](int u) { return u < hu ? p.ad[a].hoff + u * 8 : p.ad[a].hoff2 + (u - hu) * 8; };
@@ -551,18 +496,17 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
                 w2[i] = pack_bf16x2(y0, y1);
                 w3[i] = pack_bf16x2(y0 - __uint_as_float(w2[i] << 16), y1 - __uint_as_float(w2[i] & 0xffff0000u));
               }
-              auto put = [&](int k, const uint32_t* w) {
-                const int kr = p.ad[a].toff + (k * pu + u) * 8;
-                const int unit16 = ((kr & 63) >> 3) ^ (row_in_cta & 7);
-                st_shared_v4(hbuf_addr + (kr >> 6) * kHChunkBytes + row_in_cta * 128 + unit16 * 16,
-                             w[0], w[1], w[2], w[3]);
-              };
-              put(0, w1); put(1, w1); put(2, w2); put(3, w1); put(4, w2); put(5, w3);
+              if (row_ok) {
+                auto put = [&](int k, const uint32_t* w) {
+                  st_global_v4(hrow + p.ad[a].toff + (k * pu + u) * 8, w[0], w[1], w[2], w[3]);
+                };
+                put(0, w1); put(1, w1); put(2, w2); put(3, w1); put(4, w2); put(5, w3);
+              }
             }
             continue;
           }
           for (int u0 = 0; u0 < units; u0 += 4) {
-            // 32 ranks per TMEM load where the rank allows it, 8 otherwise
+            // 32 ranks per TMEM load where the columns allow it, 8 otherwise
             uint32_t r[32];
             const int n = min(4, units - u0);
             if (n == 4 && col(u0 + 3) == col(u0) + 24) {
@@ -575,35 +519,38 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
                 for (int i = 0; i < 8; ++i) r[k * 8 + i] = r8[i];
               }
             }
+            if (!row_ok) continue;
             if (p.h_out) {
               // keep s * X A^T in fp32 as well (the backward needs it for dA)
-              const int row = t.m * kPairM + static_cast<int>(cta) * kBM + row_in_cta;
-              if (row < p.T) {
-                float* ho = p.h_out + static_cast<long long>(row) * p.h_out_ld + p.ad[a].hout_off;
+              float* ho = p.h_out + static_cast<long long>(row) * p.h_out_ld + p.ad[a].hout_off;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (i < n * 8 && u0 * 8 + i < p.ad[a].rank) ho[u0 * 8 + i] = u2f(r[i]) * s;
-              }
+              for (int i = 0; i < 32; ++i)
+                if (i < n * 8 && u0 * 8 + i < p.ad[a].rank) ho[u0 * 8 + i] = u2f(r[i]) * s;
             }
             for (int k = 0; k < n; ++k) {
-              const int u = u0 + k;
               const uint32_t* q8 = r + k * 8;
-              const uint32_t w0 = pack_bf16x2(u2f(q8[0]) * s, u2f(q8[1]) * s);
-              const uint32_t w1 = pack_bf16x2(u2f(q8[2]) * s, u2f(q8[3]) * s);
-              const uint32_t w2 = pack_bf16x2(u2f(q8[4]) * s, u2f(q8[5]) * s);
-              const uint32_t w3 = pack_bf16x2(u2f(q8[6]) * s, u2f(q8[7]) * s);
-              const int kr = p.ad[a].toff + u * 8;            // H~ column of the unit's first rank
-              const int unit16 = ((kr & 63) >> 3) ^ (row_in_cta & 7);
-              st_shared_v4(hbuf_addr + (kr >> 6) * kHChunkBytes + row_in_cta * 128 + unit16 * 16, w0,
-                           w1, w2, w3);
+              st_global_v4(hrow + p.ad[a].toff + (u0 + k) * 8, pack_bf16x2(u2f(q8[0]) * s, u2f(q8[1]) * s),
+                           pack_bf16x2(u2f(q8[2]) * s, u2f(q8[3]) * s), pack_bf16x2(u2f(q8[4]) * s, u2f(q8[5]) * s),
+                           pack_bf16x2(u2f(q8[6]) * s, u2f(q8[7]) * s));
             }
           }
         }
-        fence_proxy_async_smem();
+        // the accumulator is fully in registers: hand it back to the MMA
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(h_ready_l);
+        if (lane == 0) mbar_arrive_cluster(acc_empty_l[b]);
+        // H~ rows visible to the TMA loads of other pairs, then count this CTA in
+        fence_proxy_async_global();
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (elected) red_release_gpu_add(p.flags + it.m, 1u);
+        ++nuse[b];
+        ++count;
+        continue;
       }
+      const Tile& t = it.t;
+      const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
+      const bool any_mma = p.has_base || a1 > a0;
       if (any_mma) {
         const bool ok = mbar_wait_cluster(&acc_full[b], nuse[b] & 1, abort_flag, tmo, status);
         if (named_bar_any(!ok, 2, 128)) break;
@@ -662,35 +609,45 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
                 if (i < nc) v[i] += bf16_to_f32(bp[i]);
             }
           }
-          if (p.n_ad32 > 0 && row_ok && nc > 0) {
+          if (kF32 && p.n_ad32 > 0 && row_ok && nc > 0) {
             for (int a = 0; a < p.n_ad32; ++a) {
               if (p.ad32[a].group != t.g) continue;
               const float* hrow = p.h32 + static_cast<long long>(row) * p.h32_cols + p.ad32[a].h_off;
               const float* Bm = p.ad32[a].B + static_cast<long long>(cig + c0) * p.ad32[a].ldb;
               const long long ldb = p.ad32[a].ldb;
-              if (p.ad32[a].vec4) {
-                // four ranks per 16-byte load of h and of each B row (B rows are read by
-                // every thread of the warp: broadcast, L1-resident)
-                for (int jj = 0; jj < p.ad32[a].rank; jj += 4) {
-                  const float4 h4 = *reinterpret_cast<const float4*>(hrow + jj);
+              // eight columns at a time: sum_j h[j] B[o, j] in fp32, then added once (B rows
+              // are read by every thread of the warp: broadcast, L1-resident)
 #pragma unroll
-                  for (int i = 0; i < 32; ++i) {
-                    if (i < nc) {
-                      const float4 b4 = __ldg(reinterpret_cast<const float4*>(Bm + i * ldb + jj));
-                      v[i] = fmaf(h4.x, b4.x, v[i]);
-                      v[i] = fmaf(h4.y, b4.y, v[i]);
-                      v[i] = fmaf(h4.z, b4.z, v[i]);
-                      v[i] = fmaf(h4.w, b4.w, v[i]);
+              for (int g8 = 0; g8 < 4; ++g8) {
+                float dsum[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dsum[i] = 0.f;
+                if (p.ad32[a].vec4) {
+#pragma unroll 1
+                  for (int jj = 0; jj < p.ad32[a].rank; jj += 4) {
+                    const float4 h4 = *reinterpret_cast<const float4*>(hrow + jj);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                      if (g8 * 8 + i < nc) {
+                        const float4 b4 = __ldg(reinterpret_cast<const float4*>(Bm + (g8 * 8 + i) * ldb + jj));
+                        dsum[i] = fmaf(h4.x, b4.x, dsum[i]);
+                        dsum[i] = fmaf(h4.y, b4.y, dsum[i]);
+                        dsum[i] = fmaf(h4.z, b4.z, dsum[i]);
+                        dsum[i] = fmaf(h4.w, b4.w, dsum[i]);
+                      }
                     }
                   }
-                }
-              } else {
-                for (int jj = 0; jj < p.ad32[a].rank; ++jj) {
-                  const float h = hrow[jj];
+                } else {
+#pragma unroll 1
+                  for (int jj = 0; jj < p.ad32[a].rank; ++jj) {
+                    const float h = hrow[jj];
 #pragma unroll
-                  for (int i = 0; i < 32; ++i)
-                    if (i < nc) v[i] = fmaf(h, Bm[i * ldb + jj], v[i]);
+                    for (int i = 0; i < 8; ++i)
+                      if (g8 * 8 + i < nc) dsum[i] = fmaf(h, Bm[(g8 * 8 + i) * ldb + jj], dsum[i]);
+                  }
                 }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[g8 * 8 + i] += dsum[i];
               }
             }
           }
@@ -768,12 +725,23 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     int wb = 0;
     uint32_t wphase = 0;
     bool ok = true;
-    Sched sc{group, -1, 0, -1};
-    while (ok && sched_next(sc, p, q_in_group, ngroups, nchunks)) {
-      const int L = sc.L;
-      const Tile t = decode_tile(p, L);
+    ItemIter iter{0, pair};
+    Item it;
+    while (ok && next_item(iter, p, pair, npairs, it)) {
+      // stages that carry no codes (rank K steps, second contraction) still complete
+      // their code barrier: waiting on it keeps every stage's phase count exact
+      auto skip = [&](int n) {
+        for (int i = 0; i < n && ok; ++i) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&raw_full[stage], phase, abort_flag, tmo, status));
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
+      };
+      if (it.rank) {
+        for (int kb = 0; kb < p.k_blocks && ok; ++kb) skip(2);
+        continue;
+      }
+      const Tile& t = it.t;
       const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
-      const bool lora = a1 > a0;
       const int wrow = t.g * p.out_g + t.j * kBN + static_cast<int>(cta) * 128 + r;
       const bool wrow_ok = wrow < p.N;
       const float* am_row = p.absmax + static_cast<long long>(wrow_ok ? wrow : 0) * kb64;
@@ -818,15 +786,8 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         if (++wb == kWRing) { wb = 0; wphase ^= 1; }
       }
       if (!ok) break;
-      if (lora) {
-        // the second-contraction stages carry no codes; the producer still arrives on
-        // their code barrier, and waiting here keeps every stage's phase count exact
-        for (int a = a0; a < a1 && ok; ++a)
-          for (int c = 0; c < p.ad[a].nchunks && ok; ++c) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&raw_full[stage], phase, abort_flag, tmo, status));
-            if (++stage == S) { stage = 0; phase ^= 1; }
-          }
-      }
+      for (int a = a0; a < a1 && ok; ++a)
+        for (int c = 0; c < p.ad[a].nchunks && ok; ++c) skip(2);
     }
   }
 
@@ -861,7 +822,7 @@ cudaLaunchConfig_t pair_config(int grid, size_t smem_bytes, cudaStream_t stream,
 
 template <bool kNF4>
 int max_pairs_impl(size_t smem_bytes) {
-  cudaError_t e = cudaFuncSetAttribute(tc_fused_fwd_kernel<kNF4>,
+  cudaError_t e = cudaFuncSetAttribute(tc_fused_fwd_kernel<kNF4, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   if (e != cudaSuccess) {
     set_last_cuda_error(e);
@@ -870,7 +831,7 @@ int max_pairs_impl(size_t smem_bytes) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pair_config<kNF4>(2 * 256, smem_bytes, nullptr, attr);
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, tc_fused_fwd_kernel<kNF4>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, tc_fused_fwd_kernel<kNF4, false>, &cfg);
   if (e != cudaSuccess || n <= 0) {
     if (e != cudaSuccess) set_last_cuda_error(e);
     n = device_sm_count() / 2;
@@ -878,10 +839,10 @@ int max_pairs_impl(size_t smem_bytes) {
   return n;
 }
 
-template <bool kNF4>
+template <bool kNF4, bool kF32>
 int launch_impl(const TcMaps& maps, const TcParams& p, int grid, size_t smem_bytes,
                 cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(tc_fused_fwd_kernel<kNF4>,
+  cudaError_t e = cudaFuncSetAttribute(tc_fused_fwd_kernel<kNF4, kF32>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   if (e != cudaSuccess) {
     set_last_cuda_error(e);
@@ -889,7 +850,7 @@ int launch_impl(const TcMaps& maps, const TcParams& p, int grid, size_t smem_byt
   }
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pair_config<kNF4>(grid, smem_bytes, stream, attr);
-  e = cudaLaunchKernelEx(&cfg, tc_fused_fwd_kernel<kNF4>, maps, p);
+  e = cudaLaunchKernelEx(&cfg, tc_fused_fwd_kernel<kNF4, kF32>, maps, p);
   if (e != cudaSuccess) {
     set_last_cuda_error(e);
     return WP_ERR_CUDA;
@@ -916,8 +877,12 @@ int tc_max_pairs(size_t smem_bytes, bool nf4) {
 
 int launch_tc_fwd(const TcMaps& maps, const TcParams& p, int grid, size_t smem_bytes,
                   cudaStream_t stream, bool nf4) {
-  return nf4 ? launch_impl<true>(maps, p, grid, smem_bytes, stream)
-             : launch_impl<false>(maps, p, grid, smem_bytes, stream);
+  const bool f32 = p.n_ad32 > 0;
+  if (nf4)
+    return f32 ? launch_impl<true, true>(maps, p, grid, smem_bytes, stream)
+               : launch_impl<true, false>(maps, p, grid, smem_bytes, stream);
+  return f32 ? launch_impl<false, true>(maps, p, grid, smem_bytes, stream)
+             : launch_impl<false, false>(maps, p, grid, smem_bytes, stream);
 }
 
 int tc_fwd_status(int reset) {
