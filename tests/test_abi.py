@@ -115,11 +115,12 @@ def test_workspace_sizes(lib):
     X, W = _m(1000, 128), _m(256, 128)
     arr = (wpg.WpAdapter * 2)(_ad(8, 128, 256), _ad(16, 128, 256, dtype=wpg.WP_FP32))
     # tensor-core path: the fp32 adapter's s * X A^T (1000 x 16 fp32, for the CUDA-core
-    # route), its bf16 pieces (A: 3 x 16 x 128, B: 256 x 6 x 16), the H~ rows of both
-    # adapters (1000 x (16 + 96) bf16) and one flag per 256-row block (4, padded to 256 B)
+    # route), its bf16 B pieces (256 x 6 x 16), the H~ rows of both adapters
+    # (1000 x (16 + 96) bf16), one flag per 256-row block (4, padded to 256 B) and the
+    # packed A rows of the rank item ((16 + 3 x 16) x 128 bf16)
     assert (lib.lora_workspace_size(0, ctypes.byref(X), ctypes.byref(W), arr, 2)
-            == 64000 + 12288 + 49152 + 224000 + 256)
-    assert lib.lora_workspace_size(0, ctypes.byref(X), ctypes.byref(W), arr, 1) == 32000 + 256
+            == 64000 + 49152 + 224000 + 256 + 16384)
+    assert lib.lora_workspace_size(0, ctypes.byref(X), ctypes.byref(W), arr, 1) == 32000 + 256 + 4096
     assert lib.lora_workspace_size(0, ctypes.byref(X), ctypes.byref(W), arr, 0) == 0
     Xf = _m(1000, 128, wpg.WP_FP32)
     # fp32 path: every adapter's s * X A^T, 1000 x 24 fp32, rounded up to 256 bytes

@@ -119,16 +119,15 @@ struct FwdPlan {
   bool tc = false;        // tensor-core path
   int rank32_total = 0;   // fp32 adapters' total rank (tensor-core path)
   int rank_all = 0;       // all adapters' total rank (fp32 path)
-  size_t split_bytes = 0; // bf16 pieces of the fp32 adapters (tensor-core path)
+  size_t split_bytes = 0; // bf16 B pieces of the fp32 adapters (tensor-core path)
   int htilde_cols = 0;    // H~ columns, at most (tensor-core path)
+  int rank_cols = 0;      // rank-item columns, at most (tensor-core path)
+  size_t pack_bytes = 0;  // packed A rows of the rank item (tensor-core path)
 };
 
 // FP32 adapters on the tensor-core path travel as three bf16 pieces per factor: rank
 // padded to rp (16), A pieces [3 rp, round8(K)], B pieces [out, 6 rp].
 int split_rp(long long r) { return static_cast<int>((r + 15) / 16 * 16); }
-size_t split_a_bytes(long long r, long long K) {
-  return round256(static_cast<size_t>(3 * split_rp(r)) * static_cast<size_t>((K + 7) / 8 * 8) * 2);
-}
 size_t split_b_bytes(long long r, long long out) {
   return round256(static_cast<size_t>(out) * 6 * split_rp(r) * 2);
 }
@@ -141,12 +140,16 @@ int plan_fwd(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int n, FwdP
     plan->rank_all += r;
     if (ad[i].A.dtype == WP_FP32) {
       plan->rank32_total += r;
-      plan->split_bytes += split_a_bytes(r, ad[i].A.cols) + split_b_bytes(r, ad[i].B.rows);
+      plan->split_bytes += split_b_bytes(r, ad[i].B.rows);
       plan->htilde_cols += 6 * split_rp(r);
+      plan->rank_cols += 3 * split_rp(r);
     } else {
       plan->htilde_cols += static_cast<int>((r + 15) / 16 * 16);
+      plan->rank_cols += static_cast<int>((r + 15) / 16 * 16);
     }
   }
+  plan->pack_bytes = round256(static_cast<size_t>(std::min(plan->rank_cols, kHCols)) *
+                              static_cast<size_t>((X->cols + 7) / 8 * 8) * 2);
   return WP_OK;
 }
 
@@ -156,7 +159,7 @@ size_t fwd_workspace(const wp_mat* X, const FwdPlan& plan) {
     if (plan.htilde_cols == 0) return 0;
     const size_t m_tiles = (T + kPairM - 1) / kPairM;
     return round256(T * plan.rank32_total * 4) + plan.split_bytes +
-           round256(T * plan.htilde_cols * 2) + round256(m_tiles * 4);
+           round256(T * plan.htilde_cols * 2) + round256(m_tiles * 4) + plan.pack_bytes;
   }
   return plan.rank_all ? round256(T * plan.rank_all * 4) : 0;
 }
@@ -262,6 +265,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   p.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
   p.has_base = W ? 1 : 0;
   p.bias = bias ? bias->data : nullptr; p.bias_f32 = bias && bias->dtype == WP_FP32;
+  p.bias_vec = bias && aligned16(bias->data) ? 1 : 0;
   p.Y = Y->data; p.ldy = Y->ld; p.y_f32 = Y->dtype == WP_FP32;
   p.timeout_ns = 2000000000ull;
 
@@ -290,15 +294,16 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     }
     split3 = n32 > 0 && n16 + n32 <= kMaxAd && width <= kHCols && !h_out;
   }
-  // workspace: [fp32 s X A^T | bf16 pieces | H~ | row-block flags]
+  // workspace: [fp32 s X A^T | bf16 B pieces | H~ | row-block flags | packed A rows]
   const size_t h32_bytes = round256(static_cast<size_t>(T) * plan.rank32_total * 4);
   size_t split_off = h32_bytes;
   const size_t hq_off = h32_bytes + plan.split_bytes;
   const size_t flags_off = hq_off + round256(static_cast<size_t>(T) * plan.htilde_cols * 2);
-  struct SplitJob { const wp_adapter* a; int rp, out; uint16_t* As; uint16_t* Bs; int lda_s; };
-  SplitJob jobs[kMaxAd];
-  int n_jobs = 0;
-  const void* amap_ptr[kMaxAd]; long long amap_rows[kMaxAd], amap_ld[kMaxAd];
+  const size_t pack_off = flags_off + round256((static_cast<size_t>(T) + kPairM - 1) / kPairM * 4);
+  PackParams pk{};
+  pk.K = static_cast<int>(K);
+  pk.ldk = static_cast<int>((K + 7) / 8 * 8);
+  pk.Ap = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + pack_off);
   const void* bmap_ptr[kMaxAd]; long long bmap_cols[kMaxAd], bmap_ld[kMaxAd];
   int hcols = 0;                           // H~ columns: every adapter packed, 16-aligned
   for (int g = 0; g < G; ++g) {
@@ -310,21 +315,18 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
       const int r = static_cast<int>(a.A.rows);
       if (a.A.dtype == WP_FP32 && split3) {
         TcAdapter& d = p.ad[p.n_ad];
+        PackAdapter& q = pk.ad[p.n_ad];
         const int rp = split_rp(r);
-        SplitJob& j = jobs[n_jobs++];
-        j.a = &a; j.rp = rp; j.out = static_cast<int>(a.B.rows);
-        j.lda_s = static_cast<int>((K + 7) / 8 * 8);
-        j.As = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + split_off);
-        split_off += split_a_bytes(r, K);
-        j.Bs = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + split_off);
+        q.A = a.A.data; q.lda = a.A.ld; q.dtype = WP_FP32; q.r = r; q.rp = rp; q.split3 = 1;
+        q.B = static_cast<const float*>(a.B.data); q.ldb = a.B.ld; q.out = static_cast<int>(a.B.rows);
+        q.Bs = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + split_off);
         split_off += split_b_bytes(r, a.B.rows);
         d.group = g; d.rank = 6 * rp; d.rpad16 = 6 * rp; d.pw = 3 * rp; d.split3 = 1;
         d.nchunks = (6 * rp + 63) / 64; d.s = s_of[i];
         d.hout_off = hout_of[i];
         d.toff = hcols;
         hcols += d.rpad16;
-        amap_ptr[p.n_ad] = j.As; amap_rows[p.n_ad] = 3 * rp; amap_ld[p.n_ad] = j.lda_s;
-        bmap_ptr[p.n_ad] = j.Bs; bmap_cols[p.n_ad] = 6 * rp; bmap_ld[p.n_ad] = 6 * rp;
+        bmap_ptr[p.n_ad] = q.Bs; bmap_cols[p.n_ad] = 6 * rp; bmap_ld[p.n_ad] = 6 * rp;
         ++p.n_ad;
         continue;
       }
@@ -341,55 +343,39 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
       }
       if (p.n_ad >= kMaxAd) return WP_ERR_UNSUPPORTED;
       if (r > kHCols) return WP_ERR_UNSUPPORTED;
-      if (!aligned16(a.A.data) || a.A.ld % 8 || !aligned16(a.B.data) || a.B.ld % 8)
-        return WP_ERR_ALIGN;
+      if (!aligned16(a.B.data) || a.B.ld % 8) return WP_ERR_ALIGN;
       TcAdapter& d = p.ad[p.n_ad];
+      PackAdapter& q = pk.ad[p.n_ad];
       d.group = g; d.rank = r; d.rpad16 = (r + 15) / 16 * 16; d.pw = d.rpad16; d.split3 = 0;
       d.nchunks = (r + 63) / 64; d.s = s_of[i];
       d.hout_off = hout_of[i];
       d.toff = hcols;
       hcols += d.rpad16;
-      amap_ptr[p.n_ad] = a.A.data; amap_rows[p.n_ad] = r; amap_ld[p.n_ad] = a.A.ld;
+      q.A = a.A.data; q.lda = a.A.ld; q.dtype = WP_BF16; q.r = r; q.rp = d.pw; q.split3 = 0;
       bmap_ptr[p.n_ad] = a.B.data; bmap_cols[p.n_ad] = r; bmap_ld[p.n_ad] = a.B.ld;
       ++p.n_ad;
     }
   }
   p.ad_begin[G] = p.n_ad;
   if (p.n_ad > 0) {
-    // Rank columns of the pair's MMA (N = htot): each CTA supplies the A rows of its half.
-    // Whole adapters per CTA (largest first, onto the lighter CTA) when that is no wider
-    // than splitting every adapter across both halves; else split them all.
-    int order[kMaxAd];
-    for (int k = 0; k < p.n_ad; ++k) order[k] = k;
-    std::sort(order, order + p.n_ad, [&](int x, int y) { return p.ad[x].pw > p.ad[y].pw; });
-    int load[2] = {0, 0};
-    int sum_pw = 0;
-    for (int k = 0; k < p.n_ad; ++k) {
-      TcAdapter& d = p.ad[order[k]];
-      d.cta = load[1] < load[0] ? 1 : 0;
-      d.hoff = load[d.cta];              // relative to the CTA's half, fixed up below
-      load[d.cta] += d.pw;
-      sum_pw += d.pw;
-    }
-    int half = std::max(load[0], load[1]);
-    if (2 * half <= sum_pw) {
-      for (int k = 0; k < p.n_ad; ++k) {
-        p.ad[k].hoff += p.ad[k].cta * half;
-        p.ad[k].hoff2 = p.ad[k].hoff + p.ad[k].pw / 2;
-      }
-    } else {
-      // each CTA loads half of every adapter's rows at the same place in its half
-      half = sum_pw / 2;
-      int off = 0;
-      for (int k = 0; k < p.n_ad; ++k) {
-        p.ad[k].cta = 2;
-        p.ad[k].hoff = off;
-        p.ad[k].hoff2 = half + off;
-        off += p.ad[k].pw / 2;
-      }
-    }
+    // Rank columns of the pair's MMA (N = htot = sum of pw): each CTA supplies half of
+    // every adapter's packed A rows, so both halves are equally wide
+    int half = 0;
+    for (int k = 0; k < p.n_ad; ++k) half += p.ad[k].pw / 2;
     if (2 * half > kHCols) return WP_ERR_UNSUPPORTED;
+    for (int k = 0, off = 0; k < p.n_ad; ++k) {
+      p.ad[k].hoff = off;
+      p.ad[k].hoff2 = half + off;
+      pk.ad[k].pw = p.ad[k].pw;
+      pk.ad[k].hoff = p.ad[k].hoff;
+      pk.ad[k].hoff2 = p.ad[k].hoff2;
+      off += p.ad[k].pw / 2;
+    }
     p.htot = 2 * half;
+    pk.n_ad = p.n_ad;
+    pk.half = half;
+    pk.flags = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + flags_off);
+    pk.n_flags = p.m_tiles;
     p.hq = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + hq_off);
     p.hq_ld = hcols;
     p.flags = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + flags_off);
@@ -439,11 +425,11 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     rc = make_map_bf16(&maps.hq, p.hq, p.hq_ld, T, p.hq_ld, 64, kBM);
     if (rc != WP_OK) return rc;
   }
-  for (int k = 0; k < p.n_ad; ++k) {
-    // rank item: the whole adapter from one CTA, or half of its rows from each
-    rc = make_map_bf16(&maps.a[k], amap_ptr[k], K, amap_rows[k], amap_ld[k], kBK,
-                       p.ad[k].cta != 2 ? p.ad[k].pw : p.ad[k].pw / 2);
+  if (p.n_ad > 0) {
+    rc = make_map_bf16(&maps.ap, pk.Ap, K, p.htot, pk.ldk, kBK, p.htot / 2);
     if (rc != WP_OK) return rc;
+  }
+  for (int k = 0; k < p.n_ad; ++k) {
     rc = make_map_bf16(&maps.b[k], bmap_ptr[k], bmap_cols[k], out_g, bmap_ld[k], 64, 128);
     if (rc != WP_OK) return rc;
   }
@@ -452,19 +438,9 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     rc = launch_h32(hp, stream);
     if (rc != WP_OK) return rc;
   }
-  for (int k = 0; k < n_jobs; ++k) {
-    const SplitJob& j = jobs[k];
-    rc = launch_split3(static_cast<const float*>(j.a->A.data), j.a->A.ld, static_cast<int>(j.a->A.rows),
-                       static_cast<int>(K), j.rp, j.As, j.lda_s, static_cast<const float*>(j.a->B.data),
-                       j.a->B.ld, j.out, j.Bs, stream);
-    if (rc != WP_OK) return rc;
-  }
   if (p.n_ad > 0) {
-    cudaError_t e = cudaMemsetAsync(p.flags, 0, static_cast<size_t>(p.m_tiles) * 4, stream);
-    if (e != cudaSuccess) {
-      set_last_cuda_error(e);
-      return WP_ERR_CUDA;
-    }
+    rc = launch_rank_pack(pk, stream);
+    if (rc != WP_OK) return rc;
   }
   int pairs = tc_max_pairs(smem, nf4);
   if (pairs <= 0) return WP_ERR_CUDA;
@@ -525,12 +501,27 @@ bool bwd_layout(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int G, B
   }
   L->part = off;
   off += round256(max_part * 4);
-  // workspace of the forward call that computes dX (H~ of dY B_g and its row-block flags)
-  int hcols = 0;
-  for (int g = 0; g < G; ++g) hcols += static_cast<int>((ad[g].A.rows + 15) / 16 * 16);
-  L->fwd = off;
-  L->fwd_bytes = round256(T * hcols * 2) + round256((T + kPairM - 1) / kPairM * 4);
-  off += L->fwd_bytes;
+  // workspace of the forward call that computes dX: X := dY [T, Ntot], W := W^T, adapter g
+  // A := B_g^T padded to [r_g, Ntot] (bf16), B := A_g^T [K, r_g]
+  {
+    const wp_mat dy{nullptr, WP_BF16, static_cast<int64_t>(T), static_cast<int64_t>(Ntot),
+                    static_cast<int64_t>(Ntot), nullptr};
+    const wp_mat wt{nullptr, WP_BF16, static_cast<int64_t>(K), static_cast<int64_t>(Ntot),
+                    static_cast<int64_t>(Ntot), nullptr};
+    wp_adapter fa[kMaxGroups];
+    for (int g = 0; g < G; ++g) {
+      const int64_t r = ad[g].A.rows;
+      fa[g].A = wp_mat{nullptr, WP_BF16, r, static_cast<int64_t>(Ntot), static_cast<int64_t>(Ntot), nullptr};
+      fa[g].B = wp_mat{nullptr, WP_BF16, static_cast<int64_t>(K), r, r, nullptr};
+      fa[g].alpha = ad[g].alpha;
+      fa[g].strength = ad[g].strength;
+    }
+    FwdPlan plan;
+    plan_fwd(&dy, &wt, fa, G, &plan);
+    L->fwd = off;
+    L->fwd_bytes = fwd_workspace(&dy, plan);
+    off += L->fwd_bytes;
+  }
   L->total = off;
   return true;
 }

@@ -40,11 +40,9 @@ struct TcAdapter {
                    // an FP32 adapter carried as bf16 pieces, 6 * rp (the width of its H~)
   int pw;          // rank-pass columns: rpad16, or 3 * rp for an FP32 adapter (X a_i^T, i=1..3)
   int split3;      // FP32 adapter as three bf16 pieces (rp = pw / 3 ranks per piece)
-  int hoff;        // TMEM column of rank-pass columns [0, pw/2) of this adapter
-  int hoff2;       // TMEM column of columns [pw/2, pw) (hoff + pw/2 unless split)
+  int hoff;        // rank columns [0, pw/2) of this adapter: TMEM column = packed A row
+  int hoff2;       // rank columns [pw/2, pw): TMEM column = packed A row (htot/2 + hoff)
   int toff;        // first column of this adapter's H~ (multiple of 16)
-  int cta;         // rank pass: the CTA of the pair that loads all A rows (0, 1), or 2 when
-                   // each CTA loads half of them (the adapter is split between the halves)
   int nchunks;     // ceil(r / 64)
   int hout_off;    // column of this adapter's s * X A^T in TcParams::h_out (if stored)
   float s;         // combined scale, fp32
@@ -85,6 +83,7 @@ struct TcParams {
   int h32_cols;
   const void* bias;            // [N] or null
   int bias_f32;
+  int bias_vec;                // bias 16-byte aligned: 16-byte loads of full sub-chunks
   void* Y;
   long long ldy;
   int y_f32;
@@ -98,7 +97,7 @@ struct TcMaps {
   CUtensorMap wq;                // 4-bit W codes: [N rows, K/2 bytes], boxes of 128 x 32 bytes
   CUtensorMap am;                // 4-bit W block scales: [N rows, K/64] fp32, boxes of 128 x 4
   CUtensorMap hq;                // H~ [T rows, hq_ld], boxes of 128 rows x 64 ranks
-  CUtensorMap a[kMaxAd];
+  CUtensorMap ap;                // packed A rows [htot, K]: boxes of htot/2 rows x 64
   CUtensorMap b[kMaxAd];
 };
 
@@ -146,11 +145,27 @@ struct H32Params {
 };
 int launch_h32(const H32Params& p, cudaStream_t stream);
 
-// An FP32 adapter (A [r, K], B [out, r], fp32) as bf16 pieces x = x1 + x2 + x3 (each the
-// bf16 rounding of what the previous ones leave): As [3 rp, lda_s] = [a1; a2; a3] and
-// Bs [out, 6 rp] = [b1 b2 b1 b3 b2 b1], rows / columns past r zero.
-int launch_split3(const float* A, long long lda, int r, int K, int rp, uint16_t* As, int lda_s,
-                  const float* B, long long ldb, int out, uint16_t* Bs, cudaStream_t stream);
+// Operands of the rank item, packed once per call.  Ap [htot, ldk] bf16 holds every
+// adapter's A rows as the pair's MMA reads them: rows [0, htot/2) feed CTA 0 (rank columns
+// [0, pw/2) of each adapter, from row hoff), rows [htot/2, htot) feed CTA 1 (columns
+// [pw/2, pw), from row hoff2).  A bf16 adapter's column j is its row j (zero past r).  An
+// FP32 adapter (A [r, K], B [out, r]) rides as bf16 pieces x = x1 + x2 + x3, each the
+// rounding of what the previous ones leave: its column i * rp + j is piece i + 1 of its
+// row j, and its B becomes Bs [out, 6 rp] = [b1 b2 b1 b3 b2 b1].
+struct PackAdapter {
+  const void* A; long long lda; int dtype;
+  int r, pw, rp, hoff, hoff2, split3;
+  const float* B; long long ldb; int out; uint16_t* Bs;   // FP32 adapters only
+};
+struct PackParams {
+  int n_ad, K, ldk, half;
+  int rows_total;                // set by launch_rank_pack
+  uint16_t* Ap;
+  uint32_t* flags;               // row-block flags of the forward kernel, cleared here
+  int n_flags;
+  PackAdapter ad[kMaxAd];
+};
+int launch_rank_pack(const PackParams& p, cudaStream_t stream);
 
 // ------------------------------------------------------------------ backward helpers
 struct NF4Table {

@@ -352,36 +352,84 @@ __device__ __forceinline__ void split3_bf16(float x, uint16_t* h) {
 
 }  // namespace
 
-// Grid-stride over the As elements, then over the Bs elements.
-__global__ void split3_kernel(const float* A, long long lda, int r, int K, int rp, uint16_t* As,
-                              int lda_s, const float* B, long long ldb, int out, uint16_t* Bs) {
-  const long long na = static_cast<long long>(rp) * lda_s;
-  const long long nb = static_cast<long long>(out) * rp;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < na + nb;
-       e += stride) {
-    uint16_t h[3] = {0, 0, 0};
-    if (e < na) {
-      const int j = static_cast<int>(e / lda_s), k = static_cast<int>(e % lda_s);
-      if (j < r && k < K) split3_bf16(A[j * lda + k], h);
+// One block per row: rows [0, 2 half) are the packed A rows, the rest the B-piece rows of
+// the FP32 adapters (adapter by adapter); threads take 8 consecutive elements each.
+// Block 0 also clears the row-block flags of the forward kernel that follows.
+__global__ void __launch_bounds__(256) rank_pack_kernel(const PackParams p) {
+  const int htot = 2 * p.half;
+  if (blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i < p.n_flags; i += blockDim.x) p.flags[i] = 0u;
+  for (int vr = blockIdx.y; vr < p.rows_total; vr += gridDim.y) {
+    if (vr < htot) {
+      // packed A row pr: find the adapter and rank column it holds
+      const int pr = vr;
+      int da = -1, u = 0;
+      for (int a = 0; a < p.n_ad; ++a) {
+        const int base = pr < p.half ? p.ad[a].hoff : p.ad[a].hoff2;
+        if (pr >= base && pr < base + p.ad[a].pw / 2) {
+          da = a;
+          u = pr - base + (pr < p.half ? 0 : p.ad[a].pw / 2);
+        }
+      }
+      const bool split3 = da >= 0 && p.ad[da].split3;
+      const int i = split3 ? u / p.ad[da].rp : 0;
+      const int j = split3 ? u % p.ad[da].rp : u;
+      const bool live = da >= 0 && j < p.ad[da].r;
+      const void* srcA = live ? p.ad[da].A : nullptr;
+      const long long lda = live ? p.ad[da].lda : 0;
+      uint16_t* dst = p.Ap + static_cast<long long>(pr) * p.ldk;
+      for (int k0 = (blockIdx.x * blockDim.x + threadIdx.x) * 8; k0 < p.ldk; k0 += gridDim.x * blockDim.x * 8) {
+        uint16_t h8[8];
+        if (!live) {
 #pragma unroll
-      for (int i = 0; i < 3; ++i) As[(static_cast<long long>(i) * rp + j) * lda_s + k] = h[i];
+          for (int e = 0; e < 8; ++e) h8[e] = 0;
+        } else if (split3) {
+          const float* src = static_cast<const float*>(srcA) + j * lda;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            uint16_t h[3] = {0, 0, 0};
+            if (k0 + e < p.K) split3_bf16(src[k0 + e], h);
+            h8[e] = h[i];
+          }
+        } else {
+          const uint16_t* src = static_cast<const uint16_t*>(srcA) + j * lda;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) h8[e] = k0 + e < p.K ? src[k0 + e] : uint16_t(0);
+        }
+        uint4 w;
+        w.x = h8[0] | (uint32_t(h8[1]) << 16); w.y = h8[2] | (uint32_t(h8[3]) << 16);
+        w.z = h8[4] | (uint32_t(h8[5]) << 16); w.w = h8[6] | (uint32_t(h8[7]) << 16);
+        *reinterpret_cast<uint4*>(dst + k0) = w;     // ldk % 8 == 0, Ap 16-byte aligned
+      }
     } else {
-      const long long f = e - na;
-      const int o = static_cast<int>(f / rp), j = static_cast<int>(f % rp);
-      if (j < r) split3_bf16(B[o * ldb + j], h);
-      uint16_t* row = Bs + static_cast<long long>(o) * 6 * rp;
-      row[j] = h[0]; row[rp + j] = h[1]; row[2 * rp + j] = h[0];
-      row[3 * rp + j] = h[2]; row[4 * rp + j] = h[1]; row[5 * rp + j] = h[0];
+      // B-piece row: (adapter, output row o) in order
+      int f = vr - htot;
+      for (int a = 0; a < p.n_ad; ++a) {
+        const PackAdapter& d = p.ad[a];
+        if (!d.split3) continue;
+        if (f >= d.out) { f -= d.out; continue; }
+        const int rp = d.rp;
+        uint16_t* row = d.Bs + static_cast<long long>(f) * 6 * rp;
+        for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < rp; j += gridDim.x * blockDim.x) {
+          uint16_t h[3] = {0, 0, 0};
+          if (j < d.r) split3_bf16(d.B[f * d.ldb + j], h);
+          row[j] = h[0]; row[rp + j] = h[1]; row[2 * rp + j] = h[0];
+          row[3 * rp + j] = h[2]; row[4 * rp + j] = h[1]; row[5 * rp + j] = h[0];
+        }
+        break;
+      }
     }
   }
 }
 
-int launch_split3(const float* A, long long lda, int r, int K, int rp, uint16_t* As, int lda_s,
-                  const float* B, long long ldb, int out, uint16_t* Bs, cudaStream_t stream) {
-  const long long n = static_cast<long long>(rp) * lda_s + static_cast<long long>(out) * rp;
-  const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, 4LL * device_sm_count()));
-  split3_kernel<<<blocks, 256, 0, stream>>>(A, lda, r, K, rp, As, lda_s, B, ldb, out, Bs);
+int launch_rank_pack(const PackParams& p0, cudaStream_t stream) {
+  PackParams p = p0;
+  p.rows_total = 2 * p.half;
+  for (int a = 0; a < p.n_ad; ++a)
+    if (p.ad[a].split3) p.rows_total += p.ad[a].out;
+  if (p.rows_total == 0 && p.n_flags == 0) return WP_OK;
+  dim3 grid(std::max(1, std::min((p.ldk + 2047) / 2048, 4)), std::max(1, std::min(p.rows_total, 65535)));
+  rank_pack_kernel<<<grid, 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_last_cuda_error(e);

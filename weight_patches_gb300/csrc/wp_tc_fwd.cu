@@ -190,7 +190,10 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&maps.x);
     if (p.has_base) tma_prefetch_desc(kNF4 ? &maps.wq : &maps.w);
-    if (p.n_ad > 0) tma_prefetch_desc(&maps.hq);
+    if (p.n_ad > 0) {
+      tma_prefetch_desc(&maps.hq);
+      tma_prefetch_desc(&maps.ap);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, 512);
@@ -230,17 +233,14 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         ++issued[stage];
         if (++stage == S) { stage = 0; phase ^= 1; }
       };
-      uint32_t rank_tx = 0;                     // A rows of every adapter, both CTAs
-      for (int a = 0; a < p.n_ad; ++a) rank_tx += p.ad[a].pw * 128;
+      const uint32_t rank_tx = static_cast<uint32_t>(p.htot) * 128;   // packed A rows, both CTAs
       const int half = p.htot >> 1;
       ItemIter iter{0, pair};
       Item it;
       while (ok && next_item(iter, p, pair, npairs, it)) {
         const int x_row = it.m * kPairM + static_cast<int>(cta) * kBM;
         if (it.rank) {
-          // X rows of the block and every adapter's A rows.  An adapter is loaded whole by
-          // one CTA of the pair into its half of the rank columns, or split between them;
-          // rows of a half that no adapter fills are not loaded (their columns are unread).
+          // X rows of the block and this CTA's half of the packed A rows (one box each)
           for (int kb = 0; kb < p.k_blocks; ++kb) {
             uint8_t* st;
             uint32_t fb;
@@ -253,17 +253,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               if (!(ok = claim(rank_tx, st, fb))) break;
               ra = st;
             }
-            for (int a = 0; a < p.n_ad; ++a) {
-              const TcAdapter& d = p.ad[a];
-              if (d.cta == 2) {
-                const int col = cta ? d.hoff2 : d.hoff;
-                tma_load_2d_pair_hint(ra + (col - static_cast<int>(cta) * half) * 128, &maps.a[a],
-                                      kb * kBK, static_cast<int>(cta) * (d.pw >> 1), fb, keep);
-              } else if (d.cta == static_cast<int>(cta)) {
-                tma_load_2d_pair_hint(ra + (d.hoff - static_cast<int>(cta) * half) * 128, &maps.a[a],
-                                      kb * kBK, 0, fb, keep);
-              }
-            }
+            tma_load_2d_pair_hint(ra, &maps.ap, kb * kBK, static_cast<int>(cta) * half, fb, keep);
             if (kNF4) mbar_arrive(&raw_full[stage]);
             advance();
           }
@@ -271,6 +261,9 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         }
         const Tile& t = it.t;
         const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
+        // the block's flag, read (acquire) before the base K loop: the read's latency is
+        // covered by the stages already queued for the MMA, and the flag is usually set
+        const uint32_t peek = a1 > a0 ? ld_acquire_gpu(p.flags + t.m) : 0u;
         if (p.has_base) {
           const int w_row = t.g * p.out_g + t.j * kBN + static_cast<int>(cta) * 128;
           for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -295,7 +288,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         }
         if (a1 > a0) {
           // second contraction: H~ of this row block (written by its rank item) and B
-          if (!(ok = flag_wait(p.flags + t.m, 2u, abort_flag, tmo, status))) break;
+          if (peek < 2u && !(ok = flag_wait(p.flags + t.m, 2u, abort_flag, tmo, status))) break;
           fence_proxy_async_global();
           const int b_row = t.j * kBN + static_cast<int>(cta) * 128;
           for (int a = a0; a < a1 && ok; ++a) {
@@ -539,9 +532,9 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(acc_empty_l[b]);
-        // H~ rows visible to the TMA loads of other pairs, then count this CTA in
+        // H~ rows visible to the TMA loads of other pairs: every thread orders its stores
+        // for the async proxy, the barrier gathers them, and one release counts this CTA in
         fence_proxy_async_global();
-        __threadfence();
         named_bar_sync(1, 128);
         if (elected) red_release_gpu_add(p.flags + it.m, 1u);
         ++nuse[b];
@@ -597,16 +590,39 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
           }
           const int nc = min(32, ncols - c0);               // valid columns of the sub-chunk
           if (p.bias && nc > 0) {
+            // 16-byte loads of the 32 bias values (the same for every row: broadcast)
+            // where they all exist and the bias is aligned, single values otherwise
             if (p.bias_f32) {
               const float* bp = static_cast<const float*>(p.bias) + gcol + c0;
+              if (nc == 32 && p.bias_vec) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (i < nc) v[i] += bp[i];
+                for (int i = 0; i < 8; ++i) {
+                  const float4 b4 = __ldg(reinterpret_cast<const float4*>(bp) + i);
+                  v[4 * i] += b4.x; v[4 * i + 1] += b4.y; v[4 * i + 2] += b4.z; v[4 * i + 3] += b4.w;
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (i < nc) v[i] += bp[i];
+              }
             } else {
               const uint16_t* bp = static_cast<const uint16_t*>(p.bias) + gcol + c0;
+              if (nc == 32 && p.bias_vec) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (i < nc) v[i] += bf16_to_f32(bp[i]);
+                for (int i = 0; i < 4; ++i) {
+                  const uint4 b8 = __ldg(reinterpret_cast<const uint4*>(bp) + i);
+                  const uint32_t w[4] = {b8.x, b8.y, b8.z, b8.w};
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    v[8 * i + 2 * k] += u2f(w[k] << 16);
+                    v[8 * i + 2 * k + 1] += u2f(w[k] & 0xffff0000u);
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (i < nc) v[i] += bf16_to_f32(bp[i]);
+              }
             }
           }
           if (kF32 && p.n_ad32 > 0 && row_ok && nc > 0) {
