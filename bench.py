@@ -42,6 +42,11 @@ def flops_of(lin) -> float:
     return 2.0 * T * (K * out + sum(p.rank * (K + og) for p in lin.patches))
 
 
+# Kernels of this library per fused step on the bench workload: rank_pack_kernel (packs the
+# adapters' A rows for the rank items, clears the row-block flags) and tc_fused_fwd_kernel.
+LAUNCHES_PER_STEP = 2
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -228,13 +233,16 @@ def run_fused(args):
                    "parallelism": f"replicas x{ws} (token-local, no collective)"},
         "roofline": {"bound": "tensor", "achieved": round(per_launch_tflops, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(per_launch_tflops / peak, 4), "traffic": captured_traffic(),
-                     "peak_source": f"{peak_kind} bf16 burst"},
+                     "peak_source": f"{peak_kind} bf16 burst",
+                     "timing": "CUDA events over the timed steps; a step is the rank-operand pack "
+                               "kernel plus the fused kernel, so this slightly understates the fused "
+                               "kernel's own rate"},
         "overhead": {"vs_cublas_base_gemm": round(ms_step / base_ms - 1.0, 4),
                      "vs_own_base_kernel": round(ms_step / own_base_ms - 1.0, 4),
                      "cublas_base_ms": round(base_ms, 5), "own_base_ms": round(own_base_ms, 5)},
         "e2e": {"value": round(ws * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * LAUNCHES_PER_STEP,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
