@@ -108,17 +108,21 @@ enum { WP_OP_FWD = 0, WP_OP_FWD_GROUPED = 1, WP_OP_BWD = 2 };
  *   W        [out, in], WP_BF16 or WP_NF4 with a bf16 X, WP_FP32 with an fp32 X;
  *            NULL computes the low-rank delta only.
  *   bias     [1, out] WP_BF16 or WP_FP32, or NULL; added in the epilogue.
- *   adapters n_adapters patches (0..8); bf16 adapters on a bf16 X run on the tensor
- *            cores, FP32 adapters run in FP32 on the CUDA cores and are added to the
- *            same FP32 accumulator before the single output rounding.
+ *   adapters n_adapters patches (0..12); bf16 adapters on a bf16 X run on the tensor
+ *            cores.  FP32 adapters on a bf16 X run there too, as three bf16 pieces per
+ *            factor (every product above 2^-24 of the leading one is kept), when the
+ *            call's rank columns allow; otherwise they run in FP32 on the CUDA cores.
+ *            Either way their terms join the same FP32 accumulator before the single
+ *            output rounding.
  *   Y        [T, out] WP_BF16 or WP_FP32, ld >= out; must not overlap the inputs.
  *   workspace device scratch of at least lora_workspace_size(WP_OP_FWD, ...) bytes
  *            (may be NULL when that size is 0).
  * Alignment (tensor-core path): every base pointer 16-byte aligned, every ld a
  * multiple of 8 elements (bf16) / 4 (fp32), in % 8 == 0, out % 8 == 0.
- * Limits: the bf16 adapters of one call fit 256 tensor-memory columns, counting
- * each adapter as ceil(r / 64) * 64 columns; r <= 256 per adapter; FP32 adapters
- * total r <= 64.
+ * Limits (tensor-core path): at most 8 adapters on the tensor cores, whose rank
+ * columns fit one 256-column accumulator: a bf16 adapter counts ceil(r / 16) * 16
+ * columns, an FP32 adapter as pieces 3 * ceil(r / 16) * 16 (FP32 adapters that do not
+ * fit take the CUDA-core route, at most 4 of them).
  */
 int lora_linear_fwd(const wp_mat* X, const wp_mat* W, const wp_mat* bias,
                     const wp_adapter* adapters, int32_t n_adapters, double request_scale,
@@ -150,6 +154,8 @@ int lora_linear_fwd_grouped(const wp_mat* X, const wp_mat* W_stacked, const wp_m
  *   X [T, in] WP_BF16; W [G*out_g, in] WP_BF16 or WP_NF4; dY [T, G*out_g] WP_BF16.
  *   dX: WP_BF16 or WP_FP32 output, or NULL to skip; dA[g], dB[g]: WP_FP32 outputs.
  *   dA/dB are overwritten (not accumulated).
+ * Limits: bf16 adapters, r_g <= 64 each, sum over groups of ceil(r_g / 16) * 16 <= 256;
+ * in % 8 == 0 and out_g % 8 == 0.
  */
 int lora_linear_bwd(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int32_t n_groups,
                     const wp_adapter* adapters, double request_scale, const wp_out* dX,

@@ -546,7 +546,7 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
     if (dX->rows != T || dX->cols != K) return WP_ERR_SHAPE;
   }
   float s_of[kMaxGroups];
-  int chunks = 0;
+  int rank_cols = 0;                 // the dX forward's rank-item width
   for (int g = 0; g < G; ++g) {
     const wp_adapter& a = ad[g];
     if (!valid_input(&a.A, false) || !valid_input(&a.B, false)) return WP_ERR_INVALID;
@@ -559,14 +559,14 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
     const double s = a.alpha / static_cast<double>(r) * a.strength * request_scale;
     if (!std::isfinite(s) || !std::isfinite(static_cast<float>(s))) return WP_ERR_INVALID;
     s_of[g] = static_cast<float>(s);
-    chunks += static_cast<int>((r + 63) / 64);
+    rank_cols += static_cast<int>((r + 15) / 16 * 16);
     const wp_out& da = dA[g];
     const wp_out& db = dB[g];
     if (!valid_output(&da) || !valid_output(&db)) return WP_ERR_INVALID;
     if (da.dtype != WP_FP32 || db.dtype != WP_FP32) return WP_ERR_DTYPE;
     if (da.rows != r || da.cols != K || db.rows != og || db.cols != r) return WP_ERR_SHAPE;
   }
-  if (chunks * 64 > kHCols) return WP_ERR_UNSUPPORTED;
+  if (rank_cols > kHCols) return WP_ERR_UNSUPPORTED;
   BwdLayout L;
   if (!bwd_layout(X, W, ad, G, &L)) return WP_ERR_INVALID;
   if (!workspace || ws_bytes < L.total) return WP_ERR_WORKSPACE;
