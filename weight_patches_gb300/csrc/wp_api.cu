@@ -164,13 +164,17 @@ size_t fwd_workspace(const wp_mat* X, const FwdPlan& plan) {
   return plan.rank_all ? round256(T * plan.rank_all * 4) : 0;
 }
 
+// h_out (optional): s * X A^T of the tensor-core adapters in fp32, [T, h_out_ld], adapters in
+// call order.  rank_only: only the rank items run (no output tiles, Y unused and may be
+// null, W must be null, the adapters' B are not read); used by the backward.
 int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool grouped,
              const wp_adapter* adapters, int n_adapters, double request_scale, const wp_out* Y,
              void* workspace, size_t ws_bytes, cudaStream_t stream, float* h_out = nullptr,
-             int h_out_ld = 0) {
+             int h_out_ld = 0, bool rank_only = false) {
   if (!valid_input(X, false)) return WP_ERR_INVALID;
   if (W && !valid_input(W, true)) return WP_ERR_INVALID;
-  if (!valid_output(Y)) return WP_ERR_INVALID;
+  if (rank_only ? (W || bias || !h_out || n_adapters < 1 || X->dtype != WP_BF16) : !valid_output(Y))
+    return WP_ERR_INVALID;
   if (!std::isfinite(request_scale)) return WP_ERR_INVALID;
   if (n_adapters < 0 || n_adapters > kMaxAd + kMaxAd32) return WP_ERR_UNSUPPORTED;
   if (n_adapters > 0 && !adapters) return WP_ERR_INVALID;
@@ -178,9 +182,9 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   if (!grouped) G = 1;
 
   const long long T = X->rows, K = X->cols;
-  const long long N = W ? W->rows : Y->cols;
+  const long long N = W ? W->rows : rank_only ? G * adapters[0].B.rows : Y->cols;
   if (W && W->cols != K) return WP_ERR_SHAPE;
-  if (Y->rows != T || Y->cols != N) return WP_ERR_SHAPE;
+  if (!rank_only && (Y->rows != T || Y->cols != N)) return WP_ERR_SHAPE;
   if (N % G) return WP_ERR_SHAPE;
   const long long out_g = N / G;
   if (W && W->dtype == WP_NF4 && (K % 64 != 0 || W->ld != K)) return WP_ERR_SHAPE;
@@ -249,7 +253,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   const bool nf4 = W && W->dtype == WP_NF4;
   if (!aligned16(X->data) || X->ld % 8) return WP_ERR_ALIGN;
   if (W && (!aligned16(W->data) || W->ld % 8)) return WP_ERR_ALIGN;
-  if (!aligned16(Y->data) || Y->ld % (Y->dtype == WP_BF16 ? 8 : 4)) return WP_ERR_ALIGN;
+  if (!rank_only && (!aligned16(Y->data) || Y->ld % (Y->dtype == WP_BF16 ? 8 : 4))) return WP_ERR_ALIGN;
   if (out_g % 8) return WP_ERR_ALIGN;
 
   TcParams p{};
@@ -261,12 +265,12 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   p.m_tiles = static_cast<int>((T + kPairM - 1) / kPairM);
   const long long total = static_cast<long long>(p.m_tiles) * G * p.nt_g;
   if (total > 0x7FFFFFFFLL) return WP_ERR_UNSUPPORTED;
-  p.total_tiles = static_cast<int>(total);
+  p.total_tiles = rank_only ? 0 : static_cast<int>(total);
   p.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
   p.has_base = W ? 1 : 0;
   p.bias = bias ? bias->data : nullptr; p.bias_f32 = bias && bias->dtype == WP_FP32;
   p.bias_vec = bias && aligned16(bias->data) ? 1 : 0;
-  p.Y = Y->data; p.ldy = Y->ld; p.y_f32 = Y->dtype == WP_FP32;
+  if (!rank_only) { p.Y = Y->data; p.ldy = Y->ld; p.y_f32 = Y->dtype == WP_FP32; }
   p.timeout_ns = 2000000000ull;
 
   // Plan the adapters (host only; every rejection happens before any CUDA call).
@@ -343,7 +347,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
       }
       if (p.n_ad >= kMaxAd) return WP_ERR_UNSUPPORTED;
       if (r > kHCols) return WP_ERR_UNSUPPORTED;
-      if (!aligned16(a.B.data) || a.B.ld % 8) return WP_ERR_ALIGN;
+      if (!rank_only && (!aligned16(a.B.data) || a.B.ld % 8)) return WP_ERR_ALIGN;
       TcAdapter& d = p.ad[p.n_ad];
       PackAdapter& q = pk.ad[p.n_ad];
       d.group = g; d.rank = r; d.rpad16 = (r + 15) / 16 * 16; d.pw = d.rpad16; d.split3 = 0;
@@ -419,8 +423,10 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     rc = make_map_bf16(&maps.w, W->data, K, N, W->ld, kBK, 128);
     if (rc != WP_OK) return rc;
   }
-  rc = make_map(&maps.y, Y->dtype, Y->data, N, T, Y->ld, Y->dtype == WP_FP32 ? 32 : 64, kBM);
-  if (rc != WP_OK) return rc;
+  if (!rank_only) {
+    rc = make_map(&maps.y, Y->dtype, Y->data, N, T, Y->ld, Y->dtype == WP_FP32 ? 32 : 64, kBM);
+    if (rc != WP_OK) return rc;
+  }
   if (p.n_ad > 0) {
     rc = make_map_bf16(&maps.hq, p.hq, p.hq_ld, T, p.hq_ld, 64, kBM);
     if (rc != WP_OK) return rc;
@@ -429,7 +435,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     rc = make_map_bf16(&maps.ap, pk.Ap, K, p.htot, pk.ldk, kBK, p.htot / 2);
     if (rc != WP_OK) return rc;
   }
-  for (int k = 0; k < p.n_ad; ++k) {
+  for (int k = 0; k < p.n_ad && !rank_only; ++k) {
     rc = make_map_bf16(&maps.b[k], bmap_ptr[k], bmap_cols[k], out_g, bmap_ld[k], 64, 128);
     if (rc != WP_OK) return rc;
   }
@@ -444,7 +450,8 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   }
   int pairs = tc_max_pairs(smem, nf4);
   if (pairs <= 0) return WP_ERR_CUDA;
-  if (pairs > p.total_tiles) pairs = p.total_tiles;
+  const int work = rank_only ? p.m_tiles : p.total_tiles;
+  if (pairs > work) pairs = work;
   // rank items two rounds of tiles ahead, or one when the X rows of two rounds would not
   // stay in L2 until their tiles come
   const double x_two_rounds = 2.0 * pairs / (G * p.nt_g) * kPairM * static_cast<double>(K) * 2;
@@ -518,8 +525,11 @@ bool bwd_layout(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int G, B
     }
     FwdPlan plan;
     plan_fwd(&dy, &wt, fa, G, &plan);
+    // and of the rank-items-only call that computes H = X A_g^T (X [T, in], A_g as given)
+    FwdPlan hplan;
+    plan_fwd(X, nullptr, ad, G, &hplan);
     L->fwd = off;
-    L->fwd_bytes = fwd_workspace(&dy, plan);
+    L->fwd_bytes = std::max(fwd_workspace(&dy, plan), fwd_workspace(X, hplan));
     off += L->fwd_bytes;
   }
   L->total = off;
@@ -537,6 +547,7 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
   const long long T = X->rows, K = X->cols, Ntot = W->rows;
   if (W->cols != K || dY->rows != T || dY->cols != Ntot || Ntot % G) return WP_ERR_SHAPE;
   if (W->dtype == WP_NF4 && (K % 64 || W->ld != K)) return WP_ERR_SHAPE;
+  if (W->dtype == WP_NF4 && !aligned16(W->data)) return WP_ERR_ALIGN;   // 4-byte code loads
   const long long og = Ntot / G;
   if (K % 8 || og % 8 || Ntot % 8) return WP_ERR_ALIGN;
   if (!aligned16(X->data) || X->ld % 8 || !aligned16(dY->data) || dY->ld % 8) return WP_ERR_ALIGN;
@@ -612,35 +623,30 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
     fwd_ad[g].strength = a.strength;
   }
 
-  // 3. H = X A_g^T (fp32, for dB)
-  H32Params hp{};
-  hp.T = static_cast<int>(T); hp.K = static_cast<int>(K);
-  hp.X = X->data; hp.x_dtype = WP_BF16; hp.ldx = X->ld;
-  hp.n_ad = G; hp.H = H; hp.h_cols = L.R;
-  for (int g = 0; g < G; ++g) {
-    hp.A[g] = ad[g].A.data; hp.a_dtype[g] = WP_BF16; hp.lda[g] = ad[g].A.ld;
-    hp.rank[g] = static_cast<int>(ad[g].A.rows); hp.h_off[g] = L.roff[g]; hp.s[g] = 1.0f;
+  // 3. H = X A_g^T (fp32, for dB): rank items only, on the tensor cores (s = 1)
+  {
+    wp_adapter h_ad[kMaxGroups];
+    for (int g = 0; g < G; ++g) {
+      h_ad[g] = ad[g];
+      h_ad[g].alpha = static_cast<double>(ad[g].A.rows);
+      h_ad[g].strength = 1.0;
+    }
+    rc = fwd_impl(X, nullptr, nullptr, G, G > 1, h_ad, G, 1.0, nullptr, ws + L.fwd, L.fwd_bytes,
+                  stream, H, L.R, /*rank_only=*/true);
+    if (rc != WP_OK) return rc;
   }
-  rc = launch_h32(hp, stream);
-  if (rc != WP_OK) return rc;
 
   // 4. dX = dY W + sum_g s_g (dY B_g) A_g on the fused tensor-core kernel, which also
-  //    leaves s_g dY B_g (fp32) in Gs; without dX, Gs comes from the fp32 projection
+  //    leaves s_g dY B_g (fp32) in Gs; without dX, a rank-items-only call computes Gs
   const wp_mat Wt_m{Wt, WP_BF16, K, Ntot, Ntot, nullptr};
   if (dX) {
     rc = fwd_impl(dY, &Wt_m, nullptr, 1, false, fwd_ad, G, request_scale, dX, ws + L.fwd,
                   L.fwd_bytes, stream, Gs, L.R);
     if (rc != WP_OK) return rc;
   } else {
-    H32Params gp{};
-    gp.T = static_cast<int>(T); gp.K = static_cast<int>(Ntot);
-    gp.X = dY->data; gp.x_dtype = WP_BF16; gp.ldx = dY->ld;
-    gp.n_ad = G; gp.H = Gs; gp.h_cols = L.R;
-    for (int g = 0; g < G; ++g) {
-      gp.A[g] = fwd_ad[g].A.data; gp.a_dtype[g] = WP_BF16; gp.lda[g] = Ntot;
-      gp.rank[g] = static_cast<int>(ad[g].A.rows); gp.h_off[g] = L.roff[g]; gp.s[g] = s_of[g];
-    }
-    rc = launch_h32(gp, stream);
+    // s_g dY B_g alone: rank items only
+    rc = fwd_impl(dY, nullptr, nullptr, 1, false, fwd_ad, G, request_scale, nullptr, ws + L.fwd,
+                  L.fwd_bytes, stream, Gs, L.R, /*rank_only=*/true);
     if (rc != WP_OK) return rc;
   }
 
