@@ -17,6 +17,7 @@
 #include <cstdint>
 
 #include "wp_internal.h"
+#include "wp_ptx.cuh"
 
 namespace wp {
 
@@ -356,6 +357,9 @@ __device__ __forceinline__ void split3_bf16(float x, uint16_t* h) {
 // the FP32 adapters (adapter by adapter); threads take 8 consecutive elements each.
 // Block 0 also clears the row-block flags of the forward kernel that follows.
 __global__ void __launch_bounds__(256) rank_pack_kernel(const PackParams p) {
+  // the fused kernel that follows may start its set-up now; it waits for this grid to
+  // finish before it touches the packed rows, the B pieces or the flags
+  grid_launch_dependents();
   const int htot = 2 * p.half;
   if (blockIdx.x == 0 && blockIdx.y == 0)
     for (int i = threadIdx.x; i < p.n_flags; i += blockDim.x) p.flags[i] = 0u;

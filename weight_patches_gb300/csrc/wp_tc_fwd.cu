@@ -67,9 +67,10 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, int L) {
 }
 
 // Work items of one pair.  Output tiles are dealt round-robin: round k of pair q is tile
-// q + k * npairs.  The rank item of row block m belongs to pair m mod npairs and runs at
-// the start of that pair's round r(m) - rlead, where r(m) = floor(m * tpb / npairs) is
-// the first round that can hold a tile of m (or as soon as the pair has no tiles left).
+// q + k * npairs.  The rank item of row block m belongs to pair (m + total_tiles) mod npairs
+// (so the pairs with one tile fewer take rank items first) and runs at the start of that
+// pair's round r(m) - rlead, where r(m) = floor(m * tpb / npairs) is the first round that
+// can hold a tile of m (or as soon as the pair has no tiles left).
 // A tile of round k waits only for rank items of rounds < k, and every pair walks its
 // items in order, so the schedule cannot deadlock while all pairs are resident.
 struct Item {
@@ -82,6 +83,11 @@ struct ItemIter {
   int k;        // next tile round of this pair
   int m_next;   // next row block whose rank item this pair owns
 };
+
+__device__ __forceinline__ ItemIter item_iter_begin(const TcParams& p, int pair, int npairs) {
+  const int first = ((pair - p.total_tiles) % npairs + npairs) % npairs;
+  return ItemIter{0, first};
+}
 
 __device__ __forceinline__ bool next_item(ItemIter& s, const TcParams& p, int pair, int npairs,
                                           Item& it) {
@@ -234,8 +240,11 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         if (++stage == S) { stage = 0; phase ^= 1; }
       };
       const uint32_t rank_tx = static_cast<uint32_t>(p.htot) * 128;   // packed A rows, both CTAs
+      // the operands packed by the kernel launched just before (packed A rows, B pieces,
+      // cleared flags) are read only after that kernel has finished
+      if (p.n_ad > 0) grid_dependency_wait();
       const int half = p.htot >> 1;
-      ItemIter iter{0, pair};
+      ItemIter iter = item_iter_begin(p, pair, npairs);
       Item it;
       while (ok && next_item(iter, p, pair, npairs, it)) {
         const int x_row = it.m * kPairM + static_cast<int>(cta) * kBM;
@@ -358,7 +367,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         mma_commit_pair_mc(&empty[s0], kBothCtas);
         if (kNF4) mma_commit_pair_mc(&empty[s1], kBothCtas);
       };
-      ItemIter iter{0, pair};
+      ItemIter iter = item_iter_begin(p, pair, npairs);
       Item it;
       while (next_item(iter, p, pair, npairs, it)) {
         const int a0 = it.rank ? 0 : p.ad_begin[it.t.g];
@@ -448,7 +457,8 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     uint32_t nuse[2] = {0, 0};
     int count = 0;
     uint32_t sidx = 0;                              // staging chunks issued so far
-    ItemIter iter{0, pair};
+    if (p.n_ad > 0) grid_dependency_wait();          // rank items release flags cleared by it
+    ItemIter iter = item_iter_begin(p, pair, npairs);
     Item it;
     while (next_item(iter, p, pair, npairs, it)) {
       const int b = count & 1;
@@ -741,7 +751,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     int wb = 0;
     uint32_t wphase = 0;
     bool ok = true;
-    ItemIter iter{0, pair};
+    ItemIter iter = item_iter_begin(p, pair, npairs);
     Item it;
     while (ok && next_item(iter, p, pair, npairs, it)) {
       // stages that carry no codes (rank K steps, second contraction) still complete
@@ -819,9 +829,11 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
 
 namespace {
 
+// attr must hold 2 entries; `pdl` lets the kernel start while the previous kernel of the
+// stream (the operand pack) is still running.
 template <bool kNF4>
 cudaLaunchConfig_t pair_config(int grid, size_t smem_bytes, cudaStream_t stream,
-                               cudaLaunchAttribute* attr) {
+                               cudaLaunchAttribute* attr, bool pdl = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kNF4 ? kTcThreadsNF4 : kTcThreads);
@@ -833,6 +845,11 @@ cudaLaunchConfig_t pair_config(int grid, size_t smem_bytes, cudaStream_t stream,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (pdl) {
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+  }
   return cfg;
 }
 
@@ -844,7 +861,7 @@ int max_pairs_impl(size_t smem_bytes) {
     set_last_cuda_error(e);
     return 0;
   }
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config<kNF4>(2 * 256, smem_bytes, nullptr, attr);
   int n = 0;
   e = cudaOccupancyMaxActiveClusters(&n, tc_fused_fwd_kernel<kNF4, false>, &cfg);
@@ -864,8 +881,8 @@ int launch_impl(const TcMaps& maps, const TcParams& p, int grid, size_t smem_byt
     set_last_cuda_error(e);
     return WP_ERR_CUDA;
   }
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pair_config<kNF4>(grid, smem_bytes, stream, attr);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pair_config<kNF4>(grid, smem_bytes, stream, attr, p.n_ad > 0);
   e = cudaLaunchKernelEx(&cfg, tc_fused_fwd_kernel<kNF4, kF32>, maps, p);
   if (e != cudaSuccess) {
     set_last_cuda_error(e);
