@@ -284,10 +284,11 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               // this CTA's codes complete on its own barrier; the dequantisation warps
               // turn them into the bf16 tile the MMA reads
               mbar_arrive_expect_tx(&raw_full[stage], kRawBytes + (p.am_tma ? kAmBytes : 0));
-              tma_load_2d(st + kATileBytes, &maps.wq, kb * (kBK / 2), w_row, &raw_full[stage]);
+              tma_load_2d_hint(st + kATileBytes, &maps.wq, kb * (kBK / 2), w_row, &raw_full[stage], keep);
               // the block scales of this K step and the next three (16-byte boxes)
               if (p.am_tma)
-                tma_load_2d(st + kATileBytes + kRawBytes, &maps.am, kb & ~3, w_row, &raw_full[stage]);
+                tma_load_2d_hint(st + kATileBytes + kRawBytes, &maps.am, kb & ~3, w_row, &raw_full[stage],
+                                 keep);
             } else {
               tma_load_2d_pair_hint(st + kATileBytes, &maps.w, kb * kBK, w_row, fb, keep);
             }
@@ -739,9 +740,9 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     const int d = threadIdx.x - 192;
     const int r = d >> 1;
     const int hh = d & 1;
-    const uint32_t wfull_l[kWRing] = {mapa_shared(smem_u32(&wfull[0]), 0),
-                                      mapa_shared(smem_u32(&wfull[1]), 0),
-                                      mapa_shared(smem_u32(&wfull[2]), 0)};
+    uint32_t wfull_l[kWRing];
+#pragma unroll
+    for (int w = 0; w < kWRing; ++w) wfull_l[w] = mapa_shared(smem_u32(&wfull[w]), 0);
     float lv[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) lv[i] = p.nf4_code[i];
