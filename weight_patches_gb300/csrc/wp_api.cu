@@ -38,8 +38,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 2-D bf16 tensor map over a row-major [outer, inner] matrix with row pitch ld
 // (elements), 128-byte swizzled boxes of {box_inner, box_outer}; out-of-range
 // elements read as zero.
+// swizzle: 128 or 64 (the box's inner extent must then be 128 or 64 bytes) or 0 (none)
 int make_map(CUtensorMap* m, int dtype, const void* ptr, long long inner, long long outer,
-             long long ld, int box_inner, int box_outer, bool swizzle128 = true) {
+             long long ld, int box_inner, int box_outer, int swizzle = 128) {
   auto fn = encode_fn();
   if (!fn) {
     g_last_error = "cuTensorMapEncodeTiled unavailable";
@@ -53,7 +54,9 @@ int make_map(CUtensorMap* m, int dtype, const void* ptr, long long inner, long l
   CUresult r = fn(m, dtype == WP_FP32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                   2, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  swizzle == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                  : swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                  : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char buf[96];
@@ -415,7 +418,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     // block scales [N, K/64] by TMA when a row of them is a multiple of 16 bytes
     p.am_tma = (K % 256 == 0 && aligned16(W->absmax)) ? 1 : 0;
     if (p.am_tma) {
-      rc = make_map(&maps.am, WP_FP32, W->absmax, K / 64, N, K / 64, 4, 128, /*swizzle128=*/false);
+      rc = make_map(&maps.am, WP_FP32, W->absmax, K / 64, N, K / 64, 4, 128, /*swizzle=*/0);
       if (rc != WP_OK) return rc;
     }
     nf4_codebook_host(p.nf4_code);
@@ -428,7 +431,11 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     if (rc != WP_OK) return rc;
   }
   if (p.n_ad > 0) {
+    // H~ and B chunks of 64 ranks (128-byte swizzle), or of 32 when at most 32 remain
+    // (64-byte swizzle, half the bytes)
     rc = make_map_bf16(&maps.hq, p.hq, p.hq_ld, T, p.hq_ld, 64, kBM);
+    if (rc != WP_OK) return rc;
+    rc = make_map(&maps.hq32, WP_BF16, p.hq, p.hq_ld, T, p.hq_ld, 32, kBM, 64);
     if (rc != WP_OK) return rc;
   }
   if (p.n_ad > 0) {
@@ -437,6 +444,8 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   }
   for (int k = 0; k < p.n_ad && !rank_only; ++k) {
     rc = make_map_bf16(&maps.b[k], bmap_ptr[k], bmap_cols[k], out_g, bmap_ld[k], 64, 128);
+    if (rc != WP_OK) return rc;
+    rc = make_map(&maps.b32[k], WP_BF16, bmap_ptr[k], bmap_cols[k], out_g, bmap_ld[k], 32, 128, 64);
     if (rc != WP_OK) return rc;
   }
 

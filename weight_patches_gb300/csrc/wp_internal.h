@@ -97,8 +97,10 @@ struct TcMaps {
   CUtensorMap wq;                // 4-bit W codes: [N rows, K/2 bytes], boxes of 128 x 32 bytes
   CUtensorMap am;                // 4-bit W block scales: [N rows, K/64] fp32, boxes of 128 x 4
   CUtensorMap hq;                // H~ [T rows, hq_ld], boxes of 128 rows x 64 ranks
+  CUtensorMap hq32;              // the same with boxes of 128 rows x 32 ranks (64-byte swizzle)
   CUtensorMap ap;                // packed A rows [htot, K]: boxes of htot/2 rows x 64
   CUtensorMap b[kMaxAd];
+  CUtensorMap b32[kMaxAd];       // B with boxes of 128 rows x 32 ranks (64-byte swizzle)
 };
 
 // Number of CTA pairs that can be resident at once for this shared-memory size.

@@ -415,6 +415,18 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
+// The same for rows of 64 bytes (32 bf16 along K) in the 64-byte swizzle layout: 8-row
+// groups of 512 bytes.
+__device__ __forceinline__ uint64_t sw64_kmajor_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);          // start address
+  d |= static_cast<uint64_t>(1) << 16;                              // LBO (unused here)
+  d |= static_cast<uint64_t>(512 >> 4) << 32;                       // SBO: 8-row group stride
+  d |= static_cast<uint64_t>(1) << 46;                              // descriptor version
+  d |= static_cast<uint64_t>(4) << 61;                              // 64-byte swizzle
+  return d;
+}
+
 // Instruction descriptor: kind::f16, bf16 A and B, fp32 D, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
   return (1u << 4)              // D = f32

@@ -303,18 +303,21 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
           const int b_row = t.j * kBN + static_cast<int>(cta) * 128;
           for (int a = a0; a < a1 && ok; ++a) {
             for (int c = 0; c < p.ad[a].nchunks; ++c) {
+              // a chunk with at most 32 ranks left travels in 32-rank boxes (half the bytes)
+              const bool narrow = p.ad[a].rpad16 - 64 * c <= 32;
+              const uint32_t box = narrow ? kATileBytes / 2 : kATileBytes;   // per CTA, per operand
               uint8_t* st;
               uint32_t fb;
-              if (!(ok = claim((kNF4 ? 2u : 4u) * kATileBytes, st, fb))) break;
-              tma_load_2d_pair_hint(st, &maps.hq, p.ad[a].toff + 64 * c, x_row, fb, keep);
+              if (!(ok = claim((kNF4 ? 2u : 4u) * box, st, fb))) break;
+              tma_load_2d_pair_hint(st, narrow ? &maps.hq32 : &maps.hq, p.ad[a].toff + 64 * c, x_row, fb, keep);
               uint8_t* bs = st + kATileBytes;
               if (kNF4) {
                 mbar_arrive(&raw_full[stage]);
                 advance();
-                if (!(ok = claim(2u * kBHalfBytes, st, fb))) break;
+                if (!(ok = claim(2u * box, st, fb))) break;
                 bs = st;
               }
-              tma_load_2d_pair_hint(bs, &maps.b[a], c * 64, b_row, fb, keep);
+              tma_load_2d_pair_hint(bs, narrow ? &maps.b32[a] : &maps.b[a], c * 64, b_row, fb, keep);
               if (kNF4) mbar_arrive(&raw_full[stage]);
               advance();
             }
@@ -418,8 +421,9 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               uint32_t h_st, b_st;
               if (!(ok = take(h_st, b_st))) break;
               const int kext = min(64, p.ad[a].rpad16 - 64 * c);
-              const uint64_t hd = sw128_kmajor_desc(h_st);
-              const uint64_t bd = sw128_kmajor_desc(b_st);
+              const bool narrow = kext <= 32;              // 32-rank boxes, 64-byte swizzle
+              const uint64_t hd = narrow ? sw64_kmajor_desc(h_st) : sw128_kmajor_desc(h_st);
+              const uint64_t bd = narrow ? sw64_kmajor_desc(b_st) : sw128_kmajor_desc(b_st);
               for (int kk = 0; kk < kext / 16; ++kk)
                 mma_bf16_pair(acc_t, hd + 2 * kk, bd + 2 * kk, idesc_acc, (accum || kk > 0) ? 1u : 0u);
               accum = true;
