@@ -196,15 +196,16 @@ def run_fused(args):
     base_ms = timed(lambda: torch.matmul(X, Wt, out=Y0), kb, 5) / kb
     own_base_ms = timed(lambda: wpg.lora_linear_fwd(X, W, None, [], out=Y0), kb, 5) / kb
 
-    # end to end through the public API with host buffers: pinned X in, Y out
+    # end to end through the public API with host buffers: pinned X in, Y out; the
+    # host-buffer entry point moves row chunks in and out while it computes
     Xh = X.cpu().pin_memory()
     Yh = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
-    Xd = torch.empty_like(X)
+    ws_host = torch.empty(wpg.lora_workspace_size(wpg.WP_OP_FWD_HOST, Xh, W, ads), dtype=torch.uint8,
+                          device=dev)
 
     def e2e_step():
-        Xd.copy_(Xh, non_blocking=True)
-        wpg.lora_linear_fwd_grouped(Xd, W, None, ads, lin.request_scale, out=Y)
-        Yh.copy_(Y, non_blocking=True)
+        wpg.lora_linear_fwd_host(Xh, W, None, ads, lin.request_scale, out=Yh, grouped=True,
+                                 workspace=ws_host)
 
     ke = max(5, min(args.steps, 50))
     e2e_ms = timed(e2e_step, ke, 3) / ke

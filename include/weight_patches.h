@@ -97,7 +97,7 @@ typedef struct wp_adapter {
 } wp_adapter;
 
 /* Operation ids for lora_workspace_size(). */
-enum { WP_OP_FWD = 0, WP_OP_FWD_GROUPED = 1, WP_OP_BWD = 2 };
+enum { WP_OP_FWD = 0, WP_OP_FWD_GROUPED = 1, WP_OP_BWD = 2, WP_OP_FWD_HOST = 3 };
 
 /*
  * lora_linear_fwd -- Y = X W^T + bias + sum_p s_p (X A_p^T) B_p^T.
@@ -142,6 +142,30 @@ int lora_linear_fwd_grouped(const wp_mat* X, const wp_mat* W_stacked, const wp_m
                             int32_t n_groups, const wp_adapter* adapters, double request_scale,
                             const wp_out* Y, void* workspace, size_t workspace_bytes,
                             void* stream);
+
+/*
+ * lora_linear_fwd_host -- lora_linear_fwd (n_groups == 0) or lora_linear_fwd_grouped
+ * (n_groups >= 1) with X and Y in host memory, for callers whose activations live on the
+ * host.  A deployment variant with no counterpart in the pages.
+ *
+ * The rows are processed in chunks of 4096: the host-to-device copy of chunk i + 1, the
+ * forward of chunk i and the device-to-host copy of chunk i - 1 run at the same time on
+ * three streams owned by the library (created on the first call per device); the call
+ * returns at once and `stream` waits for the whole operation.  X and Y should be pinned
+ * (page-locked) for the copies to overlap; pageable memory works, serialised.
+ *   X_host  [T, in] WP_BF16 (or WP_FP32 for the all-FP32 layer), host pointer.
+ *   W, bias, adapters, request_scale: as lora_linear_fwd / lora_linear_fwd_grouped (device).
+ *   Y_host  [T, out] WP_BF16 or WP_FP32, host pointer, ld >= out.
+ *   workspace  device scratch of at least lora_workspace_size(WP_OP_FWD_HOST, X_host, W,
+ *              adapters, n_adapters) bytes: two device chunks of X and of Y, and the
+ *              forward's own scratch for one chunk.
+ * Errors as lora_linear_fwd; a failure found after copies were queued still returns its
+ * status, and `stream` then does not wait for the internal streams.
+ */
+int lora_linear_fwd_host(const wp_mat* X_host, const wp_mat* W, const wp_mat* bias,
+                         int32_t n_groups, const wp_adapter* adapters, int32_t n_adapters,
+                         double request_scale, const wp_out* Y_host, void* workspace,
+                         size_t workspace_bytes, void* stream);
 
 /*
  * lora_linear_bwd -- closed-form gradients of Y = X W_g^T + s_g (X A_g^T) B_g^T over

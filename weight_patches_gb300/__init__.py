@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_HERE, "libweight_patches_gb300.so")
 
 WP_BF16, WP_FP32, WP_NF4 = 0, 1, 2
 WP_PATCH_ADD, WP_PATCH_SET = 0, 1
-WP_OP_FWD, WP_OP_FWD_GROUPED, WP_OP_BWD = 0, 1, 2
+WP_OP_FWD, WP_OP_FWD_GROUPED, WP_OP_BWD, WP_OP_FWD_HOST = 0, 1, 2, 3
 STATUS = {0: "WP_OK", -1: "WP_ERR_INVALID", -2: "WP_ERR_SHAPE", -3: "WP_ERR_DTYPE",
           -4: "WP_ERR_ALIGN", -5: "WP_ERR_WORKSPACE", -6: "WP_ERR_CUDA", -7: "WP_ERR_TIMEOUT",
           -8: "WP_ERR_UNSUPPORTED"}
@@ -73,6 +73,7 @@ def _load():
     lib.lora_linear_fwd.argtypes = [pm, pm, pm, pa, I32, D, po, P, SZ, P]
     lib.lora_linear_fwd_grouped.argtypes = [pm, pm, pm, I32, pa, D, po, P, SZ, P]
     lib.lora_linear_fwd_noalloc.argtypes = [pm, pm, pm, pa, I32, D, po, P]
+    lib.lora_linear_fwd_host.argtypes = [pm, pm, pm, I32, pa, I32, D, po, P, SZ, P]
     lib.lora_linear_bwd.argtypes = [pm, pm, pm, I32, pa, D, po, po, po, P, SZ, P]
     lib.lora_dense_patch.argtypes = [P, I32, I64, P, I32, I64, I32, D, P]
     lib.lora_workspace_size.argtypes = [I32, pm, pm, pa, I32]
@@ -84,7 +85,7 @@ def _load():
     lib.lora_nf4_codebook.restype = None
     lib.lora_last_cuda_error.restype = ctypes.c_char_p
     for name in ("lora_linear_fwd", "lora_linear_fwd_grouped", "lora_linear_bwd", "lora_dense_patch",
-                 "lora_device_status", "lora_linear_fwd_noalloc"):
+                 "lora_device_status", "lora_linear_fwd_noalloc", "lora_linear_fwd_host"):
         getattr(lib, name).restype = ctypes.c_int
     _LIB = lib
     return lib
@@ -211,6 +212,30 @@ def lora_linear_fwd_grouped(X: torch.Tensor, W_stacked, bias: Optional[torch.Ten
                                          ws.data_ptr() if ws is not None else None, nbytes,
                                          _stream(X.device))
     _check(st, "lora_linear_fwd_grouped")
+    return out
+
+
+def lora_linear_fwd_host(X_host: torch.Tensor, W, bias: Optional[torch.Tensor], adapters: Sequence[Adapter],
+                         request_scale: float = 1.0, out: Optional[torch.Tensor] = None,
+                         out_dtype: torch.dtype = torch.bfloat16, grouped: bool = False,
+                         workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The forward with X and the result in host memory (pin both for the copies to overlap
+    the compute): rows go through the device in chunks, copies and kernels overlapped.
+    ``grouped`` selects the stacked column-group form (one adapter per group)."""
+    if isinstance(W, NF4Weight):
+        device, n = W.packed.device, W.rows
+    elif W is not None:
+        device, n = W.device, W.shape[0]
+    else:
+        device, n = adapters[0].A.device, adapters[0].B.shape[0]
+    if out is None:
+        out = torch.empty(X_host.shape[0], n, dtype=out_dtype, pin_memory=True)
+    xm, wm, bm, arr, ym = _mat(X_host), _mat(W), _mat(bias), _adapters(adapters), _out(out)
+    ws, nbytes = _workspace(WP_OP_FWD_HOST, xm, wm, arr, len(adapters), device, workspace)
+    st = _load().lora_linear_fwd_host(ctypes.byref(xm), _ref(wm), _ref(bm), len(adapters) if grouped else 0,
+                                      arr, len(adapters), float(request_scale), ctypes.byref(ym),
+                                      ws.data_ptr() if ws is not None else None, nbytes, _stream(device))
+    _check(st, "lora_linear_fwd_host")
     return out
 
 

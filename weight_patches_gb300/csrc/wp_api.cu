@@ -682,6 +682,145 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
   return WP_OK;
 }
 
+// ------------------------------------------------------------------ host-buffer forward
+// Workspace of lora_linear_fwd_host, in order (each region 256-byte aligned): X chunks
+// [2][chunk, in] | Y chunks [2][chunk, out] (fp32-sized, whatever Y's type) | the
+// forward's scratch for one chunk.
+constexpr long long kHostChunkRows = 4096;
+
+struct HostLayout {
+  size_t x[2], y[2], fwd, fwd_bytes, total;
+  long long chunk, out;
+};
+
+bool host_layout(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int n, HostLayout* L) {
+  if (!X || X->rows < 0 || X->cols <= 0) return false;
+  // out features: W's rows, or for a delta-only layer (no W, one group) the adapters' B rows
+  const long long out = W ? W->rows : (n > 0 && ad ? ad[0].B.rows : 0);
+  if (out <= 0) return false;
+  L->out = out;
+  L->chunk = std::min(kHostChunkRows, std::max<long long>(X->rows, 1));
+  const size_t xs = static_cast<size_t>(X->dtype == WP_FP32 ? 4 : 2);
+  size_t off = 0;
+  for (int b = 0; b < 2; ++b) {
+    L->x[b] = off;
+    off += round256(static_cast<size_t>(L->chunk) * X->cols * xs);
+  }
+  for (int b = 0; b < 2; ++b) {
+    L->y[b] = off;
+    off += round256(static_cast<size_t>(L->chunk) * out * 4);
+  }
+  wp_mat xc = *X;
+  xc.rows = L->chunk;
+  xc.ld = X->cols;
+  FwdPlan plan;
+  plan_fwd(&xc, W, ad, n, &plan);
+  L->fwd = off;
+  L->fwd_bytes = fwd_workspace(&xc, plan);
+  off += L->fwd_bytes;
+  L->total = off;
+  return true;
+}
+
+// Library-owned streams and events of the host-buffer forward, per device.
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t h2d = nullptr, cmp = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, done_c = nullptr, done_d = nullptr;
+  cudaEvent_t x_ready[2] = {}, x_free[2] = {}, y_ready[2] = {}, y_free[2] = {};
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipe[64];
+
+int host_pipe(HostPipe** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    return WP_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= 64) return WP_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.ready) {
+    cudaStream_t* ss[3] = {&hp.h2d, &hp.cmp, &hp.d2h};
+    for (cudaStream_t* sp : ss) {
+      e = cudaStreamCreateWithFlags(sp, cudaStreamNonBlocking);
+      if (e != cudaSuccess) { set_last_cuda_error(e); return WP_ERR_CUDA; }
+    }
+    cudaEvent_t* es[11] = {&hp.start, &hp.done_c, &hp.done_d, &hp.x_ready[0], &hp.x_ready[1],
+                           &hp.x_free[0], &hp.x_free[1], &hp.y_ready[0], &hp.y_ready[1],
+                           &hp.y_free[0], &hp.y_free[1]};
+    for (cudaEvent_t* ep : es) {
+      e = cudaEventCreateWithFlags(ep, cudaEventDisableTiming);
+      if (e != cudaSuccess) { set_last_cuda_error(e); return WP_ERR_CUDA; }
+    }
+    hp.ready = true;
+  }
+  *out = &hp;
+  return WP_OK;
+}
+
+int host_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int n_groups,
+              const wp_adapter* adapters, int n_adapters, double request_scale, const wp_out* Y,
+              void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (!valid_input(X, false) || !valid_output(Y)) return WP_ERR_INVALID;
+  if (n_groups < 0 || n_adapters < 0 || (n_adapters > 0 && !adapters)) return WP_ERR_INVALID;
+  if (n_groups > 0 && (!W || n_adapters != n_groups)) return WP_ERR_INVALID;
+  if (Y->rows != X->rows) return WP_ERR_SHAPE;
+  HostLayout L;
+  if (!host_layout(X, W, adapters, n_adapters, &L)) return WP_ERR_INVALID;
+  if (Y->cols != L.out) return WP_ERR_SHAPE;
+  if (!workspace || ws_bytes < L.total) return WP_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return WP_ERR_ALIGN;
+  const long long T = X->rows, K = X->cols, N = Y->cols;
+  if (T == 0) return WP_OK;
+  HostPipe* hp = nullptr;
+  int rc = host_pipe(&hp);
+  if (rc != WP_OK) return rc;
+  char* ws = static_cast<char*>(workspace);
+  const size_t xs = X->dtype == WP_FP32 ? 4 : 2, ys = Y->dtype == WP_FP32 ? 4 : 2;
+  auto fail = [](cudaError_t e) { set_last_cuda_error(e); return WP_ERR_CUDA; };
+  cudaError_t e = cudaEventRecord(hp->start, stream);
+  if (e != cudaSuccess) return fail(e);
+  for (cudaStream_t s2 : {hp->h2d, hp->cmp, hp->d2h})
+    if ((e = cudaStreamWaitEvent(s2, hp->start, 0)) != cudaSuccess) return fail(e);
+  const long long nchunks = (T + L.chunk - 1) / L.chunk;
+  for (long long i = 0; i < nchunks; ++i) {
+    const int b = static_cast<int>(i & 1);
+    const long long r0 = i * L.chunk, rows = std::min(L.chunk, T - r0);
+    void* xd = ws + L.x[b];
+    void* yd = ws + L.y[b];
+    // chunk i in: after the forward of chunk i - 2 has read this X buffer
+    if (i >= 2 && (e = cudaStreamWaitEvent(hp->h2d, hp->x_free[b], 0)) != cudaSuccess) return fail(e);
+    e = cudaMemcpy2DAsync(xd, K * xs, static_cast<const char*>(X->data) + r0 * X->ld * xs, X->ld * xs,
+                          K * xs, rows, cudaMemcpyDefault, hp->h2d);
+    if (e != cudaSuccess) return fail(e);
+    if ((e = cudaEventRecord(hp->x_ready[b], hp->h2d)) != cudaSuccess) return fail(e);
+    // forward of chunk i: after its X landed and chunk i - 2's Y left this Y buffer
+    if ((e = cudaStreamWaitEvent(hp->cmp, hp->x_ready[b], 0)) != cudaSuccess) return fail(e);
+    if (i >= 2 && (e = cudaStreamWaitEvent(hp->cmp, hp->y_free[b], 0)) != cudaSuccess) return fail(e);
+    const wp_mat xc{xd, X->dtype, rows, K, K, nullptr};
+    const wp_out yc{yd, Y->dtype, rows, N, N};
+    rc = fwd_impl(&xc, W, bias, n_groups > 0 ? n_groups : 1, n_groups > 0, adapters, n_adapters,
+                  request_scale, &yc, ws + L.fwd, L.fwd_bytes, hp->cmp);
+    if (rc != WP_OK) return rc;
+    if ((e = cudaEventRecord(hp->x_free[b], hp->cmp)) != cudaSuccess) return fail(e);
+    if ((e = cudaEventRecord(hp->y_ready[b], hp->cmp)) != cudaSuccess) return fail(e);
+    // chunk i out
+    if ((e = cudaStreamWaitEvent(hp->d2h, hp->y_ready[b], 0)) != cudaSuccess) return fail(e);
+    e = cudaMemcpy2DAsync(static_cast<char*>(Y->data) + r0 * Y->ld * ys, Y->ld * ys, yd, N * ys, N * ys,
+                          rows, cudaMemcpyDefault, hp->d2h);
+    if (e != cudaSuccess) return fail(e);
+    if ((e = cudaEventRecord(hp->y_free[b], hp->d2h)) != cudaSuccess) return fail(e);
+  }
+  if ((e = cudaEventRecord(hp->done_c, hp->cmp)) != cudaSuccess) return fail(e);
+  if ((e = cudaEventRecord(hp->done_d, hp->d2h)) != cudaSuccess) return fail(e);
+  if ((e = cudaStreamWaitEvent(stream, hp->done_c, 0)) != cudaSuccess) return fail(e);
+  if ((e = cudaStreamWaitEvent(stream, hp->done_d, 0)) != cudaSuccess) return fail(e);
+  return WP_OK;
+}
+
 }  // namespace
 
 void set_last_cuda_error(cudaError_t e) { g_last_error = cudaGetErrorString(e); }
@@ -754,7 +893,19 @@ size_t lora_workspace_size(int32_t op, const wp_mat* X, const wp_mat* W,
     BwdLayout L;
     return bwd_layout(X, W, adapters, n_adapters, &L) ? L.total : 0;
   }
+  if (op == WP_OP_FWD_HOST) {
+    HostLayout L;
+    return host_layout(X, W, adapters, n_adapters, &L) ? L.total : 0;
+  }
   return 0;
+}
+
+int lora_linear_fwd_host(const wp_mat* X_host, const wp_mat* W, const wp_mat* bias,
+                         int32_t n_groups, const wp_adapter* adapters, int32_t n_adapters,
+                         double request_scale, const wp_out* Y_host, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  return host_impl(X_host, W, bias, n_groups, adapters, n_adapters, request_scale, Y_host,
+                   workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 const char* lora_status_string(int status) {
