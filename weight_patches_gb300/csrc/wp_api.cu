@@ -396,9 +396,9 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   }
   hp.H = static_cast<float*>(workspace); hp.h_cols = h_off;
 
-  // stage: X rows | bf16 W half (or 4-bit codes + block scales)
-  p.stage_bytes = kATileBytes + (nf4 ? kRawBytes + kAmBytes : kBHalfBytes);
-  const size_t fixed = 1024 + (nf4 ? static_cast<size_t>(kWRing) * kBHalfBytes : 0) + 2 * kStgBytes + 512;
+  // stage: X rows | W half (bf16, or the dequantised 4-bit tile) [| 4-bit codes | block scales]
+  p.stage_bytes = kATileBytes + kBHalfBytes + (nf4 ? kRawBytes + kAmBytes : 0);
+  const size_t fixed = 1024 + 2 * kStgBytes + 512;
   int stages = static_cast<int>((kSmemLimit - fixed) / p.stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return WP_ERR_UNSUPPORTED;

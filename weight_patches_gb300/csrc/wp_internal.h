@@ -26,10 +26,11 @@ constexpr int kATileBytes = kBM * kBK * 2;      // 16 KiB: this CTA's X rows
 constexpr int kBHalfBytes = 128 * kBK * 2;      // 16 KiB: this CTA's half of a B tile
 constexpr int kStgBytes = kBM * 128;            // output staging: 128 rows x 128 bytes
 constexpr int kTcThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kTcThreadsNF4 = 448;  // + warps 6..13: 4-bit dequantisation
+// 4-bit W: warp 0 TMA, warp 1 MMA (warps 2..3 idle), warps 4..7 epilogue, warps 8..23
+// dequantisation in two groups of 8 warps that take alternate K steps
+constexpr int kTcThreadsNF4 = 768;
 constexpr int kRawBytes = 128 * 32;             // 4-bit codes of 128 rows x 64 K per stage
 constexpr int kAmBytes = 128 * 4 * 4;           // block scales of 128 rows x 4 K steps
-constexpr int kWRing = 3;                       // dequantised weight tiles in flight
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 227 * 1024;
 

@@ -151,23 +151,21 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
   const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base_addr - raw_addr);
 
-  // Stage s: [X rows (or H~ rows) 16 KiB | bf16 W half (or B) 16 KiB], or with a 4-bit W
-  // [X 16 KiB | codes 4 KiB | block scales 2 KiB]; a step with two bf16 operands other
-  // than W (rank K step, second contraction) then takes two stages, one per operand.
+  // Stage s: [X rows (or H~ rows) 16 KiB | W half (or B) 16 KiB]; with a 4-bit W it also
+  // holds [codes 4 KiB | block scales 2 KiB] and its W half is the dequantised tile.
   const int S = p.stages;
   const int SB = p.stage_bytes;
-  uint8_t* wring = sbase + S * SB;                      // 4-bit W: dequantised tiles
-  uint8_t* stg = wring + (kNF4 ? kWRing * kBHalfBytes : 0);   // 2 output staging buffers
+  uint8_t* stg = sbase + S * SB;                        // 2 output staging buffers
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg + 2 * kStgBytes);
   uint64_t* full = bars;                  // [S]  leader: TMA bytes of both CTAs landed
   uint64_t* empty = bars + S;             // [S]  both: the pair MMAs consumed the stage
   uint64_t* acc_full = bars + 2 * S;      // [2]  both: accumulator buffer ready
   uint64_t* acc_empty = acc_full + 2;     // [2]  leader: both epilogues drained it
   uint64_t* drain = acc_full + 4;         //      leader: every MMA issued has finished
-  uint64_t* raw_full = acc_full + 5;      // [S]  4-bit W, local: this CTA's codes landed
-  uint64_t* wfull = raw_full + S;         // [kWRing] leader: both CTAs' tiles dequantised
-  uint64_t* wempty = wfull + kWRing;      // [kWRing] both: the MMAs consumed the tile
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty + kWRing);
+  uint64_t* raw_full = acc_full + 5;      // [S]  4-bit W, local: this CTA's X, codes, scales landed
+  uint64_t* wfull = raw_full + S;         // [S]  4-bit W, leader: every dequantisation warp of both
+                                          //      CTAs is done with this use (tile written if any)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wfull + S);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -180,16 +178,13 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
       mbar_init(&raw_full[s], 1);
+      mbar_init(&wfull[s], 32);           // 16 dequantisation warps x 2 CTAs
     }
     mbar_init(&acc_full[0], 1);
     mbar_init(&acc_full[1], 1);
     mbar_init(&acc_empty[0], 8);          // 4 epilogue warps x 2 CTAs
     mbar_init(&acc_empty[1], 8);
     mbar_init(drain, 1);
-    for (int w = 0; w < kWRing; ++w) {
-      mbar_init(&wfull[w], 16);           // 8 dequantisation warps x 2 CTAs
-      mbar_init(&wempty[w], 1);
-    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -211,12 +206,20 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // 4-bit W: 24 warps launched at 80 registers (768 x 80 = 61440 in all); the warpgroups
+  // re-balance that exact total: TMA/MMA 128 x 56, epilogue 128 x 136, dequantisation
+  // 512 x 72
+  // 512 x 72 (each warpgroup runs one setmaxnreg at the top of its role branch)
+  constexpr int kEpiWarp0 = kNF4 ? 4 : 2;              // first of the 4 epilogue warps
+
   // Pair `pair` takes items pair, pair + npairs, pair + 2 npairs, ...
   const int npairs = static_cast<int>(gridDim.x >> 1);
   const int pair = static_cast<int>(blockIdx.x >> 1);
   const uint64_t tmo = p.timeout_ns;
   int* status = &g_tc_status;
 
+  if (warp < kEpiWarp0) {
+  if (kNF4) regs_dec<56>();                           // warpgroup 0: TMA, MMA, 2 idle warps
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
@@ -253,17 +256,10 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
           for (int kb = 0; kb < p.k_blocks; ++kb) {
             uint8_t* st;
             uint32_t fb;
-            if (!(ok = claim(kNF4 ? 2u * kATileBytes : 2u * kATileBytes + rank_tx, st, fb))) break;
+            if (!(ok = claim(2u * kATileBytes + rank_tx, st, fb))) break;
             tma_load_2d_pair(st, &maps.x, kb * kBK, x_row, fb);
-            uint8_t* ra = st + kATileBytes;
-            if (kNF4) {
-              mbar_arrive(&raw_full[stage]);      // no codes in this stage
-              advance();
-              if (!(ok = claim(rank_tx, st, fb))) break;
-              ra = st;
-            }
-            tma_load_2d_pair_hint(ra, &maps.ap, kb * kBK, static_cast<int>(cta) * half, fb, keep);
-            if (kNF4) mbar_arrive(&raw_full[stage]);
+            tma_load_2d_pair_hint(st + kATileBytes, &maps.ap, kb * kBK, static_cast<int>(cta) * half, fb, keep);
+            if (kNF4) mbar_arrive(&raw_full[stage]);   // no codes in this stage (keeps its phase)
             advance();
           }
           continue;
@@ -278,18 +274,20 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
           for (int kb = 0; kb < p.k_blocks; ++kb) {
             uint8_t* st;
             uint32_t fb;
-            if (!(ok = claim((kNF4 ? 2u : 4u) * kATileBytes, st, fb))) break;
-            tma_load_2d_pair(st, &maps.x, kb * kBK, x_row, fb);
+            // 4-bit W: the leader's full barrier only keeps its phase; this CTA's X rows,
+            // codes and block scales complete on its own barrier, the dequantisation warps
+            // turn the codes into the bf16 tile and tell the MMA (wfull)
+            if (!(ok = claim(kNF4 ? 0u : 4u * kATileBytes, st, fb))) break;
             if (kNF4) {
-              // this CTA's codes complete on its own barrier; the dequantisation warps
-              // turn them into the bf16 tile the MMA reads
-              mbar_arrive_expect_tx(&raw_full[stage], kRawBytes + (p.am_tma ? kAmBytes : 0));
-              tma_load_2d_hint(st + kATileBytes, &maps.wq, kb * (kBK / 2), w_row, &raw_full[stage], keep);
+              uint8_t* raw = st + 2 * kATileBytes;
+              mbar_arrive_expect_tx(&raw_full[stage], kATileBytes + kRawBytes + (p.am_tma ? kAmBytes : 0));
+              tma_load_2d(st, &maps.x, kb * kBK, x_row, &raw_full[stage]);
+              tma_load_2d_hint(raw, &maps.wq, kb * (kBK / 2), w_row, &raw_full[stage], keep);
               // the block scales of this K step and the next three (16-byte boxes)
               if (p.am_tma)
-                tma_load_2d_hint(st + kATileBytes + kRawBytes, &maps.am, kb & ~3, w_row, &raw_full[stage],
-                                 keep);
+                tma_load_2d_hint(raw + kRawBytes, &maps.am, kb & ~3, w_row, &raw_full[stage], keep);
             } else {
+              tma_load_2d_pair(st, &maps.x, kb * kBK, x_row, fb);
               tma_load_2d_pair_hint(st + kATileBytes, &maps.w, kb * kBK, w_row, fb, keep);
             }
             advance();
@@ -308,30 +306,32 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               const uint32_t box = narrow ? kATileBytes / 2 : kATileBytes;   // per CTA, per operand
               uint8_t* st;
               uint32_t fb;
-              if (!(ok = claim((kNF4 ? 2u : 4u) * box, st, fb))) break;
+              if (!(ok = claim(4u * box, st, fb))) break;
               tma_load_2d_pair_hint(st, narrow ? &maps.hq32 : &maps.hq, p.ad[a].toff + 64 * c, x_row, fb, keep);
-              uint8_t* bs = st + kATileBytes;
-              if (kNF4) {
-                mbar_arrive(&raw_full[stage]);
-                advance();
-                if (!(ok = claim(2u * box, st, fb))) break;
-                bs = st;
-              }
-              tma_load_2d_pair_hint(bs, narrow ? &maps.b32[a] : &maps.b[a], c * 64, b_row, fb, keep);
-              if (kNF4) mbar_arrive(&raw_full[stage]);
+              tma_load_2d_pair_hint(st + kATileBytes, narrow ? &maps.b32[a] : &maps.b[a], c * 64, b_row, fb,
+                                    keep);
+              if (kNF4) mbar_arrive(&raw_full[stage]);   // keeps its phase
               advance();
             }
           }
         }
       }
-      if (!ok && leader) {
-        // Wait (bounded) for the copies put in flight before the CTA exits.
+      if (!ok) {
+        // Wait (bounded) for the copies put in flight before the CTA exits: the pair's
+        // copies complete on the leader's barriers, a 4-bit W's local ones on raw_full.
         for (int s = 0; s < S; ++s) {
           if (issued[s] == 0) continue;
           const uint32_t par = static_cast<uint32_t>((issued[s] - 1) & 1);
-          const uint32_t a = smem_u32(&full[s]);
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait_cluster(a, par) && globaltimer_ns() - t0 < 100000000ull) {
+          if (leader) {
+            const uint32_t a = smem_u32(&full[s]);
+            while (!mbar_try_wait_cluster(a, par) && globaltimer_ns() - t0 < 100000000ull) {
+            }
+          }
+          if (kNF4) {
+            const uint32_t a = smem_u32(&raw_full[s]);
+            while (!mbar_try_wait(a, par) && globaltimer_ns() - t0 < 100000000ull) {
+            }
           }
         }
       }
@@ -341,36 +341,28 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
-      int wb = 0;
-      uint32_t wphase = 0;
       uint32_t nuse[2] = {0, 0};
       int count = 0;
       const uint32_t idesc_acc = idesc_bf16_f32(kPairM, kBN);
       const uint32_t idesc_h = idesc_bf16_f32(kPairM, p.htot > 0 ? p.htot : 16);
       const uint32_t stage_base = smem_u32(sbase);
-      const uint32_t wring_base = smem_u32(wring);
       bool ok = true;
-      // Operands of a step with two bf16 operands: A in this stage's first slot, B in
-      // its second slot (bf16 W) or in the next stage's first slot (4-bit W).
-      int s0 = 0, s1 = 0;
+      // Operands of a step: A in the stage's first slot, B in its second slot.  A base K
+      // step of a 4-bit W waits for the dequantisation warps (wfull: tile written, X
+      // landed in both CTAs); every other step waits for the TMA bytes (full) and, with a
+      // 4-bit W, for wfull too, which keeps every dequantisation warp in step.
+      int s0 = 0;
       auto take = [&](uint32_t& a_st, uint32_t& b_st) -> bool {
         if (!mbar_wait(&full[stage], phase, abort_flag, tmo, status)) return false;
+        if (kNF4 && !mbar_wait_cluster(&wfull[stage], phase, abort_flag, tmo, status)) return false;
         s0 = stage;
         if (++stage == S) { stage = 0; phase ^= 1; }
-        if (kNF4) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, tmo, status)) return false;
-          s1 = stage;
-          if (++stage == S) { stage = 0; phase ^= 1; }
-        }
         tc_fence_after();
         a_st = stage_base + s0 * SB;
-        b_st = kNF4 ? stage_base + s1 * SB : a_st + kATileBytes;
+        b_st = a_st + kATileBytes;
         return true;
       };
-      auto give_back = [&]() {
-        mma_commit_pair_mc(&empty[s0], kBothCtas);
-        if (kNF4) mma_commit_pair_mc(&empty[s1], kBothCtas);
-      };
+      auto give_back = [&]() { mma_commit_pair_mc(&empty[s0], kBothCtas); };
       ItemIter iter = item_iter_begin(p, pair, npairs);
       Item it;
       while (next_item(iter, p, pair, npairs, it)) {
@@ -397,22 +389,18 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         } else {
           if (p.has_base) {
             for (int kb = 0; kb < p.k_blocks; ++kb) {
-              if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
-              if (kNF4 && !(ok = mbar_wait_cluster(&wfull[wb], wphase, abort_flag, tmo, status)))
+              if (!(ok = kNF4 ? mbar_wait_cluster(&wfull[stage], phase, abort_flag, tmo, status)
+                              : mbar_wait(&full[stage], phase, abort_flag, tmo, status)))
                 break;
               tc_fence_after();
               const uint32_t st = stage_base + stage * SB;
               const uint64_t ad = sw128_kmajor_desc(st);
-              const uint64_t bd = sw128_kmajor_desc(kNF4 ? wring_base + wb * kBHalfBytes : st + kATileBytes);
+              const uint64_t bd = sw128_kmajor_desc(st + kATileBytes);
 #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk)
                 mma_bf16_pair(acc_t, ad + 2 * kk, bd + 2 * kk, idesc_acc, (kb | kk) != 0 ? 1u : 0u);
               mma_commit_pair_mc(&empty[stage], kBothCtas);
               if (++stage == S) { stage = 0; phase ^= 1; }
-              if (kNF4) {
-                mma_commit_pair_mc(&wempty[wb], kBothCtas);
-                if (++wb == kWRing) { wb = 0; wphase ^= 1; }
-              }
             }
           }
           bool accum = p.has_base != 0;
@@ -443,7 +431,9 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       while (!mbar_try_wait_cluster(a, 0) && globaltimer_ns() - t0 < 100000000ull) {
       }
     }
-  } else if (warp < 6) {
+  }
+  } else if (warp < kEpiWarp0 + 4) {
+    if (kNF4) regs_inc<136>();
     // ------------------------------------------------------------ epilogue (4 warps)
     // Output chunks of 128 bytes per row (64 bf16 or 32 fp32 columns) are staged in two
     // 128-byte-swizzled shared buffers and written by TMA bulk stores (evict-first in L2);
@@ -454,7 +444,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     const int row_in_cta = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t stg_addr = smem_u32(stg);
-    const bool elected = threadIdx.x == 64;
+    const bool elected = threadIdx.x == kEpiWarp0 * 32;
     const uint32_t acc_empty_l[2] = {mapa_shared(smem_u32(&acc_empty[0]), 0),
                                      mapa_shared(smem_u32(&acc_empty[1]), 0)};
     const uint64_t stream_out = l2_evict_first();   // Y is written once: keep X and W in L2
@@ -735,40 +725,43 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     }
     if (elected) bulk_wait_all();
   } else if (kNF4) {
+    regs_dec<72>();
     // ------------------------------------------------------------ 4-bit dequantisation
-    // Thread d of 256 owns row d/2 of this CTA's 128 weight rows and half (32 elements) of
-    // each 64-element K step.  For every (row, K step) -- one 64-element absmax block --
+    // Two groups of 256 threads take alternate base K steps (the CTA's running count of
+    // them).  Thread d of a group owns row d/2 of this CTA's 128 weight rows and half (32
+    // elements) of the K step.  For every (row, K step) -- one 64-element absmax block --
     // it builds the 16 bf16 values bf16(fl32(level[i]) * absmax) in registers, split into
     // low-byte and high-byte planes, and looks its codes up four at a time with byte
-    // permutes; the result is written in the 128-byte swizzle K-major layout.
-    const int d = threadIdx.x - 192;
+    // permutes; the result goes to the stage's W slot in the 128-byte swizzle K-major
+    // layout.  That slot is free as soon as the stage's codes have landed: the producer
+    // waited for the MMAs to release the stage before it loaded them.  Every warp waits on
+    // every use of every stage (so that no parity wait can pass a phase that has not
+    // completed yet) and then arrives on the stage's wfull, after its tile if the use is
+    // one of its group's K steps; the MMA waits for all 32 arrivals of every use, so that
+    // no warp can fall two phases behind either.
+    const int group = (threadIdx.x - 256) >> 8;
+    const int d = (threadIdx.x - 256) & 255;
     const int r = d >> 1;
     const int hh = d & 1;
-    uint32_t wfull_l[kWRing];
-#pragma unroll
-    for (int w = 0; w < kWRing; ++w) wfull_l[w] = mapa_shared(smem_u32(&wfull[w]), 0);
+    uint32_t kc = 0;                                  // base K steps seen by this CTA
+    const uint32_t wfull_l0 = mapa_shared(smem_u32(&wfull[0]), 0);   // leader's barriers
     float lv[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) lv[i] = p.nf4_code[i];
     const int kb64 = p.K / 64;
     int stage = 0;
     uint32_t phase = 0;
-    int wb = 0;
-    uint32_t wphase = 0;
     bool ok = true;
+    auto pass = [&]() {                               // a stage use this warp does not fill
+      ok = __all_sync(0xffffffffu, mbar_wait(&raw_full[stage], phase, abort_flag, tmo, status));
+      if (ok && lane == 0) mbar_arrive_remote(wfull_l0 + 8u * stage);
+      if (++stage == S) { stage = 0; phase ^= 1; }
+    };
     ItemIter iter = item_iter_begin(p, pair, npairs);
     Item it;
     while (ok && next_item(iter, p, pair, npairs, it)) {
-      // stages that carry no codes (rank K steps, second contraction) still complete
-      // their code barrier: waiting on it keeps every stage's phase count exact
-      auto skip = [&](int n) {
-        for (int i = 0; i < n && ok; ++i) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&raw_full[stage], phase, abort_flag, tmo, status));
-          if (++stage == S) { stage = 0; phase ^= 1; }
-        }
-      };
       if (it.rank) {
-        for (int kb = 0; kb < p.k_blocks && ok; ++kb) skip(2);
+        for (int kb = 0; kb < p.k_blocks && ok; ++kb) pass();
         continue;
       }
       const Tile& t = it.t;
@@ -776,16 +769,18 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       const int wrow = t.g * p.out_g + t.j * kBN + static_cast<int>(cta) * 128 + r;
       const bool wrow_ok = wrow < p.N;
       const float* am_row = p.absmax + static_cast<long long>(wrow_ok ? wrow : 0) * kb64;
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
+      for (int kb = 0; kb < p.k_blocks && ok; ++kb, ++kc) {
+        if (static_cast<int>(kc & 1u) != group) {       // the other group's K step
+          pass();
+          continue;
+        }
         ok = mbar_wait(&raw_full[stage], phase, abort_flag, tmo, status);
-        ok = ok && mbar_wait_cluster(&wempty[wb], wphase ^ 1, abort_flag, tmo, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const uint8_t* raw = sbase + stage * SB + 2 * kATileBytes;   // codes | block scales
         // block scale: from the stage (TMA, no global load left in flight when this warp
         // releases the tile to the peer CTA) or, for K % 256 != 0, straight from memory
-        const float am = p.am_tma
-                             ? reinterpret_cast<const float*>(sbase + stage * SB + kATileBytes +
-                                                              kRawBytes)[r * 4 + (kb & 3)]
-                             : (wrow_ok ? __ldg(am_row + kb) : 0.f);
+        const float am = p.am_tma ? reinterpret_cast<const float*>(raw + kRawBytes)[r * 4 + (kb & 3)]
+                                  : (wrow_ok ? __ldg(am_row + kb) : 0.f);
         // table: entries 2k, 2k+1 packed in e[k]; byte planes lo/hi of entries 4j..4j+3
         uint32_t e[8];
 #pragma unroll
@@ -796,10 +791,9 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
           lo[j] = prmt(e[2 * j], e[2 * j + 1], 0x6420u);
           hi[j] = prmt(e[2 * j], e[2 * j + 1], 0x7531u);
         }
-        const uint8_t* codes = sbase + stage * SB + kATileBytes + r * 32 + hh * 16;
-        const uint4 cw4 = *reinterpret_cast<const uint4*>(codes);
+        const uint4 cw4 = *reinterpret_cast<const uint4*>(raw + r * 32 + hh * 16);
         const uint32_t cwords[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
-        const uint32_t dst = smem_u32(wring) + wb * kBHalfBytes + r * 128;
+        const uint32_t dst = smem_u32(sbase + stage * SB + kATileBytes) + r * 128;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           // 4 bytes = 8 codes of consecutive elements
@@ -812,13 +806,12 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(wfull_l[wb]);
+        if (lane == 0) mbar_arrive_remote(wfull_l0 + 8u * stage);
         if (++stage == S) { stage = 0; phase ^= 1; }
-        if (++wb == kWRing) { wb = 0; wphase ^= 1; }
       }
       if (!ok) break;
       for (int a = a0; a < a1 && ok; ++a)
-        for (int c = 0; c < p.ad[a].nchunks && ok; ++c) skip(2);
+        for (int c = 0; c < p.ad[a].nchunks && ok; ++c) pass();
     }
   }
 
