@@ -265,7 +265,10 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   p.T = static_cast<int>(T); p.K = static_cast<int>(K); p.N = static_cast<int>(N);
   p.out_g = static_cast<int>(out_g); p.G = G;
   p.nt_g = static_cast<int>((out_g + kBN - 1) / kBN);
-  p.m_tiles = static_cast<int>((T + kPairM - 1) / kPairM);
+  // a 4-bit W's tile is two 256-row halves sharing each dequantised weight tile
+  p.m_shift = nf4 ? 1 : 0;
+  p.r_blocks = static_cast<int>((T + kPairM - 1) / kPairM);
+  p.m_tiles = static_cast<int>((T + (kPairM << p.m_shift) - 1) / (kPairM << p.m_shift));
   const long long total = static_cast<long long>(p.m_tiles) * G * p.nt_g;
   if (total > 0x7FFFFFFFLL) return WP_ERR_UNSUPPORTED;
   p.total_tiles = rank_only ? 0 : static_cast<int>(total);
@@ -382,7 +385,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     pk.n_ad = p.n_ad;
     pk.half = half;
     pk.flags = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + flags_off);
-    pk.n_flags = p.m_tiles;
+    pk.n_flags = p.r_blocks;
     p.hq = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + hq_off);
     p.hq_ld = hcols;
     p.flags = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + flags_off);
@@ -396,8 +399,10 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   }
   hp.H = static_cast<float*>(workspace); hp.h_cols = h_off;
 
-  // stage: X rows | W half (bf16, or the dequantised 4-bit tile) [| 4-bit codes | block scales]
-  p.stage_bytes = kATileBytes + kBHalfBytes + (nf4 ? kRawBytes + kAmBytes : 0);
+  // stage: X rows (both halves' for a 4-bit W) | W half (bf16, or the dequantised 4-bit tile)
+  // [| 4-bit codes | block scales]
+  p.stage_bytes = nf4 ? kMHalvesNF4 * kATileBytes + kBHalfBytes + kRawBytes + kAmBytes
+                      : kATileBytes + kBHalfBytes;
   const size_t fixed = 1024 + 2 * kStgBytes + 512;
   int stages = static_cast<int>((kSmemLimit - fixed) / p.stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
@@ -459,11 +464,11 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   }
   int pairs = tc_max_pairs(smem, nf4);
   if (pairs <= 0) return WP_ERR_CUDA;
-  const int work = rank_only ? p.m_tiles : p.total_tiles;
+  const int work = rank_only ? p.r_blocks : p.total_tiles;
   if (pairs > work) pairs = work;
   // rank items two rounds of tiles ahead, or one when the X rows of two rounds would not
   // stay in L2 until their tiles come
-  const double x_two_rounds = 2.0 * pairs / (G * p.nt_g) * kPairM * static_cast<double>(K) * 2;
+  const double x_two_rounds = 2.0 * pairs / (G * p.nt_g) * (kPairM << p.m_shift) * static_cast<double>(K) * 2;
   p.rlead = x_two_rounds <= 48.0 * (1 << 20) ? 2 : 1;
   return launch_tc_fwd(maps, p, 2 * pairs, smem, stream, nf4);
 }

@@ -29,6 +29,9 @@ constexpr int kTcThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilog
 // 4-bit W: warp 0 TMA, warp 1 MMA (warps 2..3 idle), warps 4..7 epilogue, warps 8..23
 // dequantisation in two groups of 8 warps that take alternate K steps
 constexpr int kTcThreadsNF4 = 768;
+// 4-bit W: a pair tile covers 2 x 256 token rows (two accumulators of 256 TMEM columns,
+// one buffer), so every dequantised weight tile feeds two MMAs
+constexpr int kMHalvesNF4 = 2;
 constexpr int kRawBytes = 128 * 32;             // 4-bit codes of 128 rows x 64 K per stage
 constexpr int kAmBytes = 128 * 4 * 4;           // block scales of 128 rows x 4 K steps
 constexpr int kMaxStages = 8;
@@ -61,21 +64,25 @@ struct TcAdapter32 {
 struct TcParams {
   int T, K, N;                 // tokens, in_features, total out_features
   int out_g, G, nt_g;          // group width, groups, N-tiles per group
-  int m_tiles, total_tiles, k_blocks;   // m_tiles counts 256-row pair blocks
+  int m_tiles, total_tiles, k_blocks;   // m_tiles counts tile rows (256 << m_shift token rows)
+  int r_blocks;                // 256-row blocks: one rank item and one flag each
+  int m_shift;                 // 4-bit W: 1 (a tile is two 256-row halves that share the
+                               // dequantised weight tile), else 0
   int rlead;                   // rank items run this many rounds of tiles ahead of their tiles
   int has_base;
   int n_ad;                    // adapters on the tensor cores (bf16, or FP32 as pieces)
   int ad_begin[kMaxGroups + 1];
   int htot;                    // rank-item MMA width: twice the larger CTA half (<= 256)
   int stages;
-  int stage_bytes;             // bf16 W: 32 KiB; 4-bit W: 16 KiB + 4 KiB codes + 2 KiB scales
+  int stage_bytes;             // bf16 W: 32 KiB; 4-bit W: 2 x 16 KiB X + 16 KiB W + 4 KiB codes
+                               // + 2 KiB scales
   const float* absmax;         // 4-bit W: [N * K / 64] fp32 block scales
   int am_tma;                  // 4-bit W: block scales arrive by TMA with the codes
   float nf4_code[16];          // 4-bit W: the NormalFloat levels
   TcAdapter ad[kMaxAd];
   uint16_t* hq;                // [T, hq_ld] bf16: H~ = s X A^T of every adapter (toff columns)
   int hq_ld;
-  uint32_t* flags;             // [m_tiles]: 2 once both CTAs wrote the block's H~ rows
+  uint32_t* flags;             // [r_blocks]: 2 once both CTAs wrote the block's H~ rows
   int n_ad32;                  // fp32 adapters (epilogue FFMA)
   TcAdapter32 ad32[kMaxAd32];
   float* h_out;                // optional [T, h_out_ld] fp32: s * X A^T of the bf16 adapters

@@ -92,8 +92,9 @@ __device__ __forceinline__ ItemIter item_iter_begin(const TcParams& p, int pair,
 __device__ __forceinline__ bool next_item(ItemIter& s, const TcParams& p, int pair, int npairs,
                                           Item& it) {
   const int tile_pos = pair + s.k * npairs;
-  if (p.n_ad > 0 && s.m_next < p.m_tiles) {
-    const int due = static_cast<int>((static_cast<long long>(s.m_next) * p.G * p.nt_g) / npairs) - p.rlead;
+  if (p.n_ad > 0 && s.m_next < p.r_blocks) {
+    const int due =
+        static_cast<int>((static_cast<long long>(s.m_next >> p.m_shift) * p.G * p.nt_g) / npairs) - p.rlead;
     if (due <= s.k || tile_pos >= p.total_tiles) {
       it.rank = true;
       it.m = s.m_next;
@@ -211,6 +212,10 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
   // 512 x 72
   // 512 x 72 (each warpgroup runs one setmaxnreg at the top of its role branch)
   constexpr int kEpiWarp0 = kNF4 ? 4 : 2;              // first of the 4 epilogue warps
+  // token rows per pair tile: kMH halves of 256 rows, each with its own accumulator; a
+  // 4-bit W's stage holds both halves' X rows ahead of the weight slot
+  constexpr int kMH = kNF4 ? kMHalvesNF4 : 1;
+  constexpr int kXBytes = kMH * kATileBytes;
 
   // Pair `pair` takes items pair, pair + npairs, pair + 2 npairs, ...
   const int npairs = static_cast<int>(gridDim.x >> 1);
@@ -250,8 +255,8 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       ItemIter iter = item_iter_begin(p, pair, npairs);
       Item it;
       while (ok && next_item(iter, p, pair, npairs, it)) {
-        const int x_row = it.m * kPairM + static_cast<int>(cta) * kBM;
         if (it.rank) {
+          const int x_row = it.m * kPairM + static_cast<int>(cta) * kBM;
           // X rows of the block and this CTA's half of the packed A rows (one box each)
           for (int kb = 0; kb < p.k_blocks; ++kb) {
             uint8_t* st;
@@ -266,9 +271,15 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         }
         const Tile& t = it.t;
         const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
-        // the block's flag, read (acquire) before the base K loop: the read's latency is
-        // covered by the stages already queued for the MMA, and the flag is usually set
-        const uint32_t peek = a1 > a0 ? ld_acquire_gpu(p.flags + t.m) : 0u;
+        // this CTA's X rows of the tile's first half; half h starts h * 256 rows further
+        const int x_row = t.m * (kPairM * kMH) + static_cast<int>(cta) * kBM;
+        const int blk0 = t.m * kMH;                           // the tile's 256-row blocks
+        const int nblk = min(kMH, p.r_blocks - blk0);
+        // the blocks' flags, read (acquire) before the base K loop: the read's latency is
+        // covered by the stages already queued for the MMA, and the flags are usually set
+        uint32_t peek = 2u;
+        if (a1 > a0)
+          for (int h = 0; h < nblk; ++h) peek = min(peek, ld_acquire_gpu(p.flags + blk0 + h));
         if (p.has_base) {
           const int w_row = t.g * p.out_g + t.j * kBN + static_cast<int>(cta) * 128;
           for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -279,9 +290,10 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
             // turn the codes into the bf16 tile and tell the MMA (wfull)
             if (!(ok = claim(kNF4 ? 0u : 4u * kATileBytes, st, fb))) break;
             if (kNF4) {
-              uint8_t* raw = st + 2 * kATileBytes;
-              mbar_arrive_expect_tx(&raw_full[stage], kATileBytes + kRawBytes + (p.am_tma ? kAmBytes : 0));
-              tma_load_2d(st, &maps.x, kb * kBK, x_row, &raw_full[stage]);
+              uint8_t* raw = st + kXBytes + kBHalfBytes;
+              mbar_arrive_expect_tx(&raw_full[stage], kXBytes + kRawBytes + (p.am_tma ? kAmBytes : 0));
+              for (int h = 0; h < kMH; ++h)
+                tma_load_2d(st + h * kATileBytes, &maps.x, kb * kBK, x_row + h * kPairM, &raw_full[stage]);
               tma_load_2d_hint(raw, &maps.wq, kb * (kBK / 2), w_row, &raw_full[stage], keep);
               // the block scales of this K step and the next three (16-byte boxes)
               if (p.am_tma)
@@ -295,8 +307,11 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
           if (!ok) break;
         }
         if (a1 > a0) {
-          // second contraction: H~ of this row block (written by its rank item) and B
-          if (peek < 2u && !(ok = flag_wait(p.flags + t.m, 2u, abort_flag, tmo, status))) break;
+          // second contraction: H~ of the tile's rows (written by the rank items of its
+          // blocks) and B
+          for (int h = 0; h < nblk && ok && peek < 2u; ++h)
+            ok = flag_wait(p.flags + blk0 + h, 2u, abort_flag, tmo, status);
+          if (!ok) break;
           fence_proxy_async_global();
           const int b_row = t.j * kBN + static_cast<int>(cta) * 128;
           for (int a = a0; a < a1 && ok; ++a) {
@@ -306,10 +321,11 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               const uint32_t box = narrow ? kATileBytes / 2 : kATileBytes;   // per CTA, per operand
               uint8_t* st;
               uint32_t fb;
-              if (!(ok = claim(4u * box, st, fb))) break;
-              tma_load_2d_pair_hint(st, narrow ? &maps.hq32 : &maps.hq, p.ad[a].toff + 64 * c, x_row, fb, keep);
-              tma_load_2d_pair_hint(st + kATileBytes, narrow ? &maps.b32[a] : &maps.b[a], c * 64, b_row, fb,
-                                    keep);
+              if (!(ok = claim(2u * (kMH + 1) * box, st, fb))) break;
+              for (int h = 0; h < kMH; ++h)
+                tma_load_2d_pair_hint(st + h * kATileBytes, narrow ? &maps.hq32 : &maps.hq, p.ad[a].toff + 64 * c,
+                                      x_row + h * kPairM, fb, keep);
+              tma_load_2d_pair_hint(st + kXBytes, narrow ? &maps.b32[a] : &maps.b[a], c * 64, b_row, fb, keep);
               if (kNF4) mbar_arrive(&raw_full[stage]);   // keeps its phase
               advance();
             }
@@ -352,14 +368,13 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       // landed in both CTAs); every other step waits for the TMA bytes (full) and, with a
       // 4-bit W, for wfull too, which keeps every dequantisation warp in step.
       int s0 = 0;
-      auto take = [&](uint32_t& a_st, uint32_t& b_st) -> bool {
+      auto take = [&](uint32_t& st) -> bool {
         if (!mbar_wait(&full[stage], phase, abort_flag, tmo, status)) return false;
         if (kNF4 && !mbar_wait_cluster(&wfull[stage], phase, abort_flag, tmo, status)) return false;
         s0 = stage;
         if (++stage == S) { stage = 0; phase ^= 1; }
         tc_fence_after();
-        a_st = stage_base + s0 * SB;
-        b_st = a_st + kATileBytes;
+        st = stage_base + s0 * SB;
         return true;
       };
       auto give_back = [&]() { mma_commit_pair_mc(&empty[s0], kBothCtas); };
@@ -369,7 +384,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         const int a0 = it.rank ? 0 : p.ad_begin[it.t.g];
         const int a1 = it.rank ? 0 : p.ad_begin[it.t.g + 1];
         if (!it.rank && !(p.has_base || a1 > a0)) continue;   // bias-only tile: no MMA
-        const int b = count & 1;
+        const int b = kNF4 ? 0 : (count & 1);   // a 4-bit W's tile fills all 512 columns
         if (!(ok = mbar_wait_cluster(&acc_empty[b], (nuse[b] & 1) ^ 1, abort_flag, tmo, status)))
           break;
         tc_fence_after();
@@ -377,10 +392,10 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         if (it.rank) {
           // one MMA per K step covers every adapter: N = htot rank columns
           for (int kb = 0; kb < p.k_blocks; ++kb) {
-            uint32_t a_st, b_st;
-            if (!(ok = take(a_st, b_st))) break;
-            const uint64_t ad = sw128_kmajor_desc(a_st);
-            const uint64_t rd = sw128_kmajor_desc(b_st);
+            uint32_t st;
+            if (!(ok = take(st))) break;
+            const uint64_t ad = sw128_kmajor_desc(st);
+            const uint64_t rd = sw128_kmajor_desc(st + kATileBytes);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
               mma_bf16_pair(acc_t, ad + 2 * kk, rd + 2 * kk, idesc_h, (kb | kk) != 0 ? 1u : 0u);
@@ -394,11 +409,13 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
                 break;
               tc_fence_after();
               const uint32_t st = stage_base + stage * SB;
-              const uint64_t ad = sw128_kmajor_desc(st);
-              const uint64_t bd = sw128_kmajor_desc(st + kATileBytes);
+              const uint64_t bd = sw128_kmajor_desc(st + kXBytes);
 #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk)
-                mma_bf16_pair(acc_t, ad + 2 * kk, bd + 2 * kk, idesc_acc, (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+                for (int h = 0; h < kMH; ++h)
+                  mma_bf16_pair(acc_t + h * kBN, sw128_kmajor_desc(st + h * kATileBytes) + 2 * kk, bd + 2 * kk,
+                                idesc_acc, (kb | kk) != 0 ? 1u : 0u);
               mma_commit_pair_mc(&empty[stage], kBothCtas);
               if (++stage == S) { stage = 0; phase ^= 1; }
             }
@@ -406,14 +423,17 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
           bool accum = p.has_base != 0;
           for (int a = a0; a < a1 && ok; ++a) {
             for (int c = 0; c < p.ad[a].nchunks; ++c) {
-              uint32_t h_st, b_st;
-              if (!(ok = take(h_st, b_st))) break;
+              uint32_t st;
+              if (!(ok = take(st))) break;
               const int kext = min(64, p.ad[a].rpad16 - 64 * c);
               const bool narrow = kext <= 32;              // 32-rank boxes, 64-byte swizzle
-              const uint64_t hd = narrow ? sw64_kmajor_desc(h_st) : sw128_kmajor_desc(h_st);
-              const uint64_t bd = narrow ? sw64_kmajor_desc(b_st) : sw128_kmajor_desc(b_st);
+              auto desc = [&](uint32_t addr) { return narrow ? sw64_kmajor_desc(addr) : sw128_kmajor_desc(addr); };
+              const uint64_t bd = desc(st + kXBytes);
               for (int kk = 0; kk < kext / 16; ++kk)
-                mma_bf16_pair(acc_t, hd + 2 * kk, bd + 2 * kk, idesc_acc, (accum || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int h = 0; h < kMH; ++h)
+                  mma_bf16_pair(acc_t + h * kBN, desc(st + h * kATileBytes) + 2 * kk, bd + 2 * kk, idesc_acc,
+                                (accum || kk > 0) ? 1u : 0u);
               accum = true;
               give_back();
             }
@@ -456,7 +476,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     ItemIter iter = item_iter_begin(p, pair, npairs);
     Item it;
     while (next_item(iter, p, pair, npairs, it)) {
-      const int b = count & 1;
+      const int b = kNF4 ? 0 : (count & 1);
       if (it.rank) {
         // s X A^T of every adapter -> bf16 H~ rows of this block in global memory (and
         // the fp32 values in h_out when asked), then the block's flag
@@ -555,12 +575,14 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         tc_fence_after();
       }
 
-      const int row0 = t.m * kPairM + static_cast<int>(cta) * kBM;
-      const int row = row0 + row_in_cta;
-      const bool row_ok = row < p.T;
-      const uint32_t acc_t = tmem + b * kBN;
       // valid chunks of this tile (the last tile of a group may be partial)
       const int nchunk = min(kBN / cw, (p.out_g - t.j * kBN + cw - 1) / cw);
+#pragma unroll 1
+      for (int h = 0; h < kMH; ++h) {
+      const int row0 = t.m * (kPairM * kMH) + h * kPairM + static_cast<int>(cta) * kBM;
+      const int row = row0 + row_in_cta;
+      const bool row_ok = row < p.T;
+      const uint32_t acc_t = tmem + (b + h) * kBN;
 #pragma unroll 1
       for (int c = 0; c < nchunk; ++c) {
         const int cig = t.j * kBN + c * cw;                 // first column, within the group
@@ -583,7 +605,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
             tmem_ld32(acc_t + lane_base + c * cw + c0, r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = u2f(r[i]);
-            if (c == nchunk - 1 && sub == cw / 32 - 1) {
+            if (h == kMH - 1 && c == nchunk - 1 && sub == cw / 32 - 1) {
               // the accumulator is fully in registers: hand it back to the MMA
               tc_fence_before();
               __syncwarp();
@@ -711,12 +733,13 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         if (full_chunk) {
           fence_proxy_async_smem();
           named_bar_sync(1, 128);
-          if (elected) {
+          if (elected && row0 < p.T) {                     // no store of rows past the end
             tma_store_2d_hint(&maps.y, gcol, row0, stg + (sidx & 1) * kStgBytes, stream_out);
             bulk_commit();
           }
           ++sidx;
         }
+      }
       }
       if (any_mma) {
         ++nuse[b];
@@ -776,7 +799,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         }
         ok = mbar_wait(&raw_full[stage], phase, abort_flag, tmo, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        const uint8_t* raw = sbase + stage * SB + 2 * kATileBytes;   // codes | block scales
+        const uint8_t* raw = sbase + stage * SB + kXBytes + kBHalfBytes;   // codes | block scales
         // block scale: from the stage (TMA, no global load left in flight when this warp
         // releases the tile to the peer CTA) or, for K % 256 != 0, straight from memory
         const float am = p.am_tma ? reinterpret_cast<const float*>(raw + kRawBytes)[r * 4 + (kb & 3)]
@@ -793,7 +816,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         }
         const uint4 cw4 = *reinterpret_cast<const uint4*>(raw + r * 32 + hh * 16);
         const uint32_t cwords[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
-        const uint32_t dst = smem_u32(sbase + stage * SB + kATileBytes) + r * 128;
+        const uint32_t dst = smem_u32(sbase + stage * SB + kXBytes) + r * 128;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           // 4 bytes = 8 codes of consecutive elements
