@@ -401,14 +401,23 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
 
   // stage: X rows (both halves' for a 4-bit W) | W half (bf16, or the dequantised 4-bit tile)
   // [| 4-bit codes | block scales]
-  p.stage_bytes = nf4 ? kMHalvesNF4 * kATileBytes + kBHalfBytes + kRawBytes + kAmBytes
-                      : kATileBytes + kBHalfBytes;
+  p.stage_bytes = nf4 ? kMHalvesNF4 * kATileBytes + kBHalfBytes : kATileBytes + kBHalfBytes;
   const size_t fixed = 1024 + 2 * kStgBytes + 512;
   int stages = static_cast<int>((kSmemLimit - fixed) / p.stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
-  if (stages < 2) return WP_ERR_UNSUPPORTED;
+  // 4-bit W: three stages, the rest of shared memory holds the codes ring
+  if (nf4) stages = 3;
   p.stages = stages;
-  const size_t smem = fixed + static_cast<size_t>(stages) * p.stage_bytes;
+  p.code_slots = 0;
+  if (nf4) {
+    const size_t left = kSmemLimit - fixed - static_cast<size_t>(stages) * p.stage_bytes;
+    p.code_slots = static_cast<int>(left / kCodeSlotBytes);
+    if (p.code_slots > kMaxCodeSlots) p.code_slots = kMaxCodeSlots;
+    if (p.code_slots < 2 || p.code_slots % 2) return WP_ERR_UNSUPPORTED;   // even: one group per slot
+  }
+  if (stages < 2) return WP_ERR_UNSUPPORTED;
+  const size_t smem = fixed + static_cast<size_t>(stages) * p.stage_bytes +
+                      static_cast<size_t>(p.code_slots) * kCodeSlotBytes;
 
   // Tensor maps (driver calls from here on).
   // Each CTA of a pair loads 128 rows of X, 128 rows of the weight tile, its share of the

@@ -34,6 +34,8 @@ constexpr int kTcThreadsNF4 = 768;
 constexpr int kMHalvesNF4 = 2;
 constexpr int kRawBytes = 128 * 32;             // 4-bit codes of 128 rows x 64 K per stage
 constexpr int kAmBytes = 128 * 4 * 4;           // block scales of 128 rows x 4 K steps
+constexpr int kCodeSlotBytes = kRawBytes + kAmBytes;
+constexpr int kMaxCodeSlots = 8;
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 227 * 1024;
 
@@ -74,8 +76,9 @@ struct TcParams {
   int ad_begin[kMaxGroups + 1];
   int htot;                    // rank-item MMA width: twice the larger CTA half (<= 256)
   int stages;
-  int stage_bytes;             // bf16 W: 32 KiB; 4-bit W: 2 x 16 KiB X + 16 KiB W + 4 KiB codes
-                               // + 2 KiB scales
+  int stage_bytes;             // bf16 W: 32 KiB; 4-bit W: 2 x 16 KiB X + 16 KiB dequantised W
+  int code_slots;              // 4-bit W: ring of [4 KiB codes | 2 KiB block scales] slots, loaded
+                               // ahead of the stages
   const float* absmax;         // 4-bit W: [N * K / 64] fp32 block scales
   int am_tma;                  // 4-bit W: block scales arrive by TMA with the codes
   float nf4_code[16];          // 4-bit W: the NormalFloat levels

@@ -156,17 +156,20 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
   // holds [codes 4 KiB | block scales 2 KiB] and its W half is the dequantised tile.
   const int S = p.stages;
   const int SB = p.stage_bytes;
-  uint8_t* stg = sbase + S * SB;                        // 2 output staging buffers
+  const int R = kNF4 ? p.code_slots : 0;                // 4-bit W: codes ring
+  uint8_t* codes = sbase + S * SB;                      // [R] codes | block scales
+  uint8_t* stg = codes + R * kCodeSlotBytes;            // 2 output staging buffers
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg + 2 * kStgBytes);
   uint64_t* full = bars;                  // [S]  leader: TMA bytes of both CTAs landed
   uint64_t* empty = bars + S;             // [S]  both: the pair MMAs consumed the stage
   uint64_t* acc_full = bars + 2 * S;      // [2]  both: accumulator buffer ready
   uint64_t* acc_empty = acc_full + 2;     // [2]  leader: both epilogues drained it
   uint64_t* drain = acc_full + 4;         //      leader: every MMA issued has finished
-  uint64_t* raw_full = acc_full + 5;      // [S]  4-bit W, local: this CTA's X, codes, scales landed
-  uint64_t* wfull = raw_full + S;         // [S]  4-bit W, leader: every dequantisation warp of both
+  uint64_t* wfull = acc_full + 5;         // [S]  4-bit W, leader: every dequantisation warp of both
                                           //      CTAs is done with this use (tile written if any)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wfull + S);
+  uint64_t* code_full = wfull + S;        // [R]  4-bit W, local: a codes slot landed
+  uint64_t* code_empty = code_full + R;   // [R]  4-bit W, local: its dequantisation group is done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(code_empty + R);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -178,8 +181,11 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&raw_full[s], 1);
       mbar_init(&wfull[s], 32);           // 16 dequantisation warps x 2 CTAs
+    }
+    for (int s = 0; s < R; ++s) {
+      mbar_init(&code_full[s], 1);
+      mbar_init(&code_empty[s], 8);       // the 8 warps of one dequantisation group
     }
     mbar_init(&acc_full[0], 1);
     mbar_init(&acc_full[1], 1);
@@ -248,6 +254,35 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         if (++stage == S) { stage = 0; phase ^= 1; }
       };
       const uint32_t rank_tx = static_cast<uint32_t>(p.htot) * 128;   // packed A rows, both CTAs
+      // 4-bit W: this CTA's codes and block scales of every base K step, in order, run
+      // through their own ring up to R - 1 steps ahead of the stages (a second walk over the
+      // same items), so that the dequantisation of a step waits only for its weight slot
+      ItemIter citer = item_iter_begin(p, pair, npairs);
+      Item cit;
+      int c_kb = p.k_blocks, c_wrow = 0;
+      uint32_t c_issued = 0;
+      bool c_more = kNF4;
+      auto issue_codes = [&]() -> bool {
+        while (c_kb == p.k_blocks) {
+          if (!next_item(citer, p, pair, npairs, cit)) { c_more = false; return true; }
+          if (!cit.rank) {
+            c_kb = 0;
+            c_wrow = cit.t.g * p.out_g + cit.t.j * kBN + static_cast<int>(cta) * 128;
+          }
+        }
+        const uint32_t slot = c_issued % static_cast<uint32_t>(R);
+        // free once the group that dequantised the slot's previous step is done with it
+        if (!mbar_wait(&code_empty[slot], ((c_issued / R) & 1u) ^ 1u, abort_flag, tmo, status)) return false;
+        uint8_t* cs = codes + slot * kCodeSlotBytes;
+        mbar_arrive_expect_tx(&code_full[slot], kRawBytes + (p.am_tma ? kAmBytes : 0));
+        tma_load_2d_hint(cs, &maps.wq, c_kb * (kBK / 2), c_wrow, &code_full[slot], keep);
+        // the block scales of this K step and the next three (16-byte boxes)
+        if (p.am_tma) tma_load_2d_hint(cs + kRawBytes, &maps.am, c_kb & ~3, c_wrow, &code_full[slot], keep);
+        ++c_kb;
+        ++c_issued;
+        return true;
+      };
+      for (int i = 0; i < R - 1 && c_more && ok; ++i) ok = issue_codes();
       // the operands packed by the kernel launched just before (packed A rows, B pieces,
       // cleared flags) are read only after that kernel has finished
       if (p.n_ad > 0) grid_dependency_wait();
@@ -264,7 +299,6 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
             if (!(ok = claim(2u * kATileBytes + rank_tx, st, fb))) break;
             tma_load_2d_pair(st, &maps.x, kb * kBK, x_row, fb);
             tma_load_2d_pair_hint(st + kATileBytes, &maps.ap, kb * kBK, static_cast<int>(cta) * half, fb, keep);
-            if (kNF4) mbar_arrive(&raw_full[stage]);   // no codes in this stage (keeps its phase)
             advance();
           }
           continue;
@@ -285,19 +319,15 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
           for (int kb = 0; kb < p.k_blocks; ++kb) {
             uint8_t* st;
             uint32_t fb;
-            // 4-bit W: the leader's full barrier only keeps its phase; this CTA's X rows,
-            // codes and block scales complete on its own barrier, the dequantisation warps
-            // turn the codes into the bf16 tile and tell the MMA (wfull)
-            if (!(ok = claim(kNF4 ? 0u : 4u * kATileBytes, st, fb))) break;
+            // 4-bit W: only the X rows of both halves come with the stage; the
+            // dequantisation warps write the weight slot (wfull) from the codes ring
+            if (!(ok = claim(kNF4 ? 2u * kXBytes : 4u * kATileBytes, st, fb))) break;
             if (kNF4) {
-              uint8_t* raw = st + kXBytes + kBHalfBytes;
-              mbar_arrive_expect_tx(&raw_full[stage], kXBytes + kRawBytes + (p.am_tma ? kAmBytes : 0));
               for (int h = 0; h < kMH; ++h)
-                tma_load_2d(st + h * kATileBytes, &maps.x, kb * kBK, x_row + h * kPairM, &raw_full[stage]);
-              tma_load_2d_hint(raw, &maps.wq, kb * (kBK / 2), w_row, &raw_full[stage], keep);
-              // the block scales of this K step and the next three (16-byte boxes)
-              if (p.am_tma)
-                tma_load_2d_hint(raw + kRawBytes, &maps.am, kb & ~3, w_row, &raw_full[stage], keep);
+                tma_load_2d_pair(st + h * kATileBytes, &maps.x, kb * kBK, x_row + h * kPairM, fb);
+              advance();
+              if (c_more && !(ok = issue_codes())) break;   // the step R - 1 ahead
+              continue;
             } else {
               tma_load_2d_pair(st, &maps.x, kb * kBK, x_row, fb);
               tma_load_2d_pair_hint(st + kATileBytes, &maps.w, kb * kBK, w_row, fb, keep);
@@ -326,7 +356,6 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
                 tma_load_2d_pair_hint(st + h * kATileBytes, narrow ? &maps.hq32 : &maps.hq, p.ad[a].toff + 64 * c,
                                       x_row + h * kPairM, fb, keep);
               tma_load_2d_pair_hint(st + kXBytes, narrow ? &maps.b32[a] : &maps.b[a], c * 64, b_row, fb, keep);
-              if (kNF4) mbar_arrive(&raw_full[stage]);   // keeps its phase
               advance();
             }
           }
@@ -334,20 +363,21 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       }
       if (!ok) {
         // Wait (bounded) for the copies put in flight before the CTA exits: the pair's
-        // copies complete on the leader's barriers, a 4-bit W's local ones on raw_full.
+        // copies complete on the leader's barriers, a 4-bit W's codes on code_full.
         for (int s = 0; s < S; ++s) {
-          if (issued[s] == 0) continue;
+          if (issued[s] == 0 || !leader) continue;
           const uint32_t par = static_cast<uint32_t>((issued[s] - 1) & 1);
           const uint64_t t0 = globaltimer_ns();
-          if (leader) {
-            const uint32_t a = smem_u32(&full[s]);
-            while (!mbar_try_wait_cluster(a, par) && globaltimer_ns() - t0 < 100000000ull) {
-            }
+          const uint32_t a = smem_u32(&full[s]);
+          while (!mbar_try_wait_cluster(a, par) && globaltimer_ns() - t0 < 100000000ull) {
           }
-          if (kNF4) {
-            const uint32_t a = smem_u32(&raw_full[s]);
-            while (!mbar_try_wait(a, par) && globaltimer_ns() - t0 < 100000000ull) {
-            }
+        }
+        for (int s = 0; s < R; ++s) {
+          const uint32_t n = c_issued / R + (static_cast<uint32_t>(s) < c_issued % R ? 1u : 0u);
+          if (n == 0) continue;
+          const uint64_t t0 = globaltimer_ns();
+          const uint32_t a = smem_u32(&code_full[s]);
+          while (!mbar_try_wait(a, (n - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
           }
         }
       }
@@ -363,10 +393,10 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       const uint32_t idesc_h = idesc_bf16_f32(kPairM, p.htot > 0 ? p.htot : 16);
       const uint32_t stage_base = smem_u32(sbase);
       bool ok = true;
-      // Operands of a step: A in the stage's first slot, B in its second slot.  A base K
-      // step of a 4-bit W waits for the dequantisation warps (wfull: tile written, X
-      // landed in both CTAs); every other step waits for the TMA bytes (full) and, with a
-      // 4-bit W, for wfull too, which keeps every dequantisation warp in step.
+      // Operands of a step: A (X or H~ rows of each half) first, then B.  Every step
+      // waits for the TMA bytes of both CTAs (full) and, with a 4-bit W, for the
+      // dequantisation warps (wfull: the weight tile of a base step is written; on the
+      // other steps it keeps every dequantisation warp in step).
       int s0 = 0;
       auto take = [&](uint32_t& st) -> bool {
         if (!mbar_wait(&full[stage], phase, abort_flag, tmo, status)) return false;
@@ -404,11 +434,8 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         } else {
           if (p.has_base) {
             for (int kb = 0; kb < p.k_blocks; ++kb) {
-              if (!(ok = kNF4 ? mbar_wait_cluster(&wfull[stage], phase, abort_flag, tmo, status)
-                              : mbar_wait(&full[stage], phase, abort_flag, tmo, status)))
-                break;
-              tc_fence_after();
-              const uint32_t st = stage_base + stage * SB;
+              uint32_t st;
+              if (!(ok = take(st))) break;
               const uint64_t bd = sw128_kmajor_desc(st + kXBytes);
 #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk)
@@ -416,8 +443,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
                 for (int h = 0; h < kMH; ++h)
                   mma_bf16_pair(acc_t + h * kBN, sw128_kmajor_desc(st + h * kATileBytes) + 2 * kk, bd + 2 * kk,
                                 idesc_acc, (kb | kk) != 0 ? 1u : 0u);
-              mma_commit_pair_mc(&empty[stage], kBothCtas);
-              if (++stage == S) { stage = 0; phase ^= 1; }
+              give_back();
             }
           }
           bool accum = p.has_base != 0;
@@ -756,12 +782,12 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     // it builds the 16 bf16 values bf16(fl32(level[i]) * absmax) in registers, split into
     // low-byte and high-byte planes, and looks its codes up four at a time with byte
     // permutes; the result goes to the stage's W slot in the 128-byte swizzle K-major
-    // layout.  That slot is free as soon as the stage's codes have landed: the producer
-    // waited for the MMAs to release the stage before it loaded them.  Every warp waits on
-    // every use of every stage (so that no parity wait can pass a phase that has not
-    // completed yet) and then arrives on the stage's wfull, after its tile if the use is
-    // one of its group's K steps; the MMA waits for all 32 arrivals of every use, so that
-    // no warp can fall two phases behind either.
+    // layout.  The codes come from their own ring (loaded ahead), so a step waits only for
+    // its slot: free once the MMAs released the stage's previous use (empty).  Every warp
+    // waits on every use of every stage (so that no parity wait can pass a phase that has
+    // not completed yet) and then arrives on the stage's wfull, after its tile if the use
+    // is one of its group's K steps; the MMA waits for all 32 arrivals of every use, so
+    // that no warp can fall two phases behind either.
     const int group = (threadIdx.x - 256) >> 8;
     const int d = (threadIdx.x - 256) & 255;
     const int r = d >> 1;
@@ -775,8 +801,11 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    auto slot_free = [&]() {                          // the stage's previous use released
+      return mbar_wait_cluster(&empty[stage], phase ^ 1, abort_flag, tmo, status);
+    };
     auto pass = [&]() {                               // a stage use this warp does not fill
-      ok = __all_sync(0xffffffffu, mbar_wait(&raw_full[stage], phase, abort_flag, tmo, status));
+      ok = __all_sync(0xffffffffu, slot_free());
       if (ok && lane == 0) mbar_arrive_remote(wfull_l0 + 8u * stage);
       if (++stage == S) { stage = 0; phase ^= 1; }
     };
@@ -797,9 +826,10 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
           pass();
           continue;
         }
-        ok = mbar_wait(&raw_full[stage], phase, abort_flag, tmo, status);
+        const uint32_t slot = kc % static_cast<uint32_t>(R);   // its codes in the ring
+        ok = slot_free() && mbar_wait(&code_full[slot], (kc / R) & 1u, abort_flag, tmo, status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        const uint8_t* raw = sbase + stage * SB + kXBytes + kBHalfBytes;   // codes | block scales
+        const uint8_t* raw = codes + slot * kCodeSlotBytes;                // codes | block scales
         // block scale: from the stage (TMA, no global load left in flight when this warp
         // releases the tile to the peer CTA) or, for K % 256 != 0, straight from memory
         const float am = p.am_tma ? reinterpret_cast<const float*>(raw + kRawBytes)[r * 4 + (kb & 3)]
@@ -829,7 +859,10 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(wfull_l0 + 8u * stage);
+        if (lane == 0) {
+          mbar_arrive_remote(wfull_l0 + 8u * stage);
+          mbar_arrive(&code_empty[slot]);
+        }
         if (++stage == S) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
