@@ -16,10 +16,12 @@ Modules
   dense_patch  ``.diff`` / ``.diff_b`` additive deltas and ``.set_weight`` replacement
   lora         forward (single, multi-patch, grouped), closed-form backward, and the
                unfused bf16 reference chain used by the accuracy gate
+  swiglu       the SwiGLU activation around the LoRA MLP and its backward, and the
+               whole MLP's forward and closed-form gradients
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test against
 something other than itself (brute force, closed forms, invariants, library
 special cases); none is "parity unpinned" except the claim that the NF4 codebook is
 bit-identical to the one bitsandbytes ships (see ``nf4``).
 """
-from . import numerics, nf4, dense_patch, lora  # noqa: F401
+from . import numerics, nf4, dense_patch, lora, swiglu  # noqa: F401
