@@ -97,7 +97,7 @@ typedef struct wp_adapter {
 } wp_adapter;
 
 /* Operation ids for lora_workspace_size(). */
-enum { WP_OP_FWD = 0, WP_OP_FWD_GROUPED = 1, WP_OP_BWD = 2, WP_OP_FWD_HOST = 3 };
+enum { WP_OP_FWD = 0, WP_OP_FWD_GROUPED = 1, WP_OP_BWD = 2, WP_OP_FWD_HOST = 3, WP_OP_SWIGLU_FWD = 4 };
 
 /*
  * lora_linear_fwd -- Y = X W^T + bias + sum_p s_p (X A_p^T) B_p^T.
@@ -166,6 +166,45 @@ int lora_linear_fwd_host(const wp_mat* X_host, const wp_mat* W, const wp_mat* bi
                          int32_t n_groups, const wp_adapter* adapters, int32_t n_adapters,
                          double request_scale, const wp_out* Y_host, void* workspace,
                          size_t workspace_bytes, void* stream);
+
+/*
+ * lora_swiglu_fwd -- the front half of a SwiGLU LoRA MLP in one pass: the gate and up
+ * LoRA linears and the activation,
+ *     e = X W_gate^T + bias_gate + s_g (X A_g^T) B_g^T,
+ *     g = X W_up^T   + bias_up   + s_u (X A_u^T) B_u^T,
+ *     h = silu(e) g,   silu(e) = e / (1 + exp(-e)).
+ * (Unsloth fast_lora walkthrough, section 4, LoRA_MLP forward: e and g by two LoRA
+ *  matmuls, h by the SwiGLU kernel, e and g kept for the backward.)
+ *   X [T, in] WP_BF16; W_gate_up [2F, in] WP_BF16 or WP_NF4, gate rows 0..F-1 then up
+ *   rows F..2F-1; bias [2F] (gate then up) or NULL; adapters[0] the gate adapter
+ *   (B [F, r]), adapters[1] the up adapter (strength 0 disables one); bf16 adapters, or
+ *   FP32 ones small enough to ride as bf16 pieces.
+ *   H [T, F] WP_BF16 output.  EG [T, 2F] WP_BF16 or NULL: receives e | g.
+ * e and g are rounded to bf16 once (EG holds exactly those values, bit-equal to
+ * lora_linear_fwd_grouped with n_groups = 2), h = bf16(silu(e) * g) from them, so the
+ * h that lora_swiglu_bwd recomputes from EG is bit-equal to H.
+ *   workspace: lora_workspace_size(WP_OP_SWIGLU_FWD, X, W_gate_up, adapters, 2) bytes.
+ * Limits: as lora_linear_fwd_grouped; F % 8 == 0.  Errors as lora_linear_fwd.
+ */
+int lora_swiglu_fwd(const wp_mat* X, const wp_mat* W_gate_up, const wp_mat* bias,
+                    const wp_adapter* adapters, double request_scale, const wp_out* H,
+                    const wp_out* EG, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * lora_swiglu_bwd -- the SwiGLU step of the LoRA MLP backward, elementwise.  From the
+ * gradient dH at h (the dX of the down projection) and the saved e | g:
+ *     f = silu(e),  dg = dH f,  de = dH g sigmoid(e) (1 + e (1 - sigmoid(e))),
+ * and, when H is given, h = f g again (for the down adapter's gradients).
+ * (Unsloth fast_lora walkthrough, section 4, LoRA_MLP backward: one kernel gives h and
+ *  the gradients at g and e.)
+ *   dH [T, F], EG [T, 2F] WP_BF16 inputs; dEG [T, 2F] WP_BF16 output, de | dg (the
+ *   stacked output gradient for the grouped gate/up backward); H [T, F] WP_BF16 or NULL.
+ * Every product is one float32 rounding, each output one bf16 rounding.
+ * Errors: WP_ERR_SHAPE, WP_ERR_DTYPE (not bf16), WP_ERR_ALIGN (16-byte bases, F and
+ * row pitches multiples of 8 elements).  Outputs must not overlap the inputs.
+ */
+int lora_swiglu_bwd(const wp_mat* dH, const wp_mat* EG, const wp_out* dEG, const wp_out* H,
+                    void* stream);
 
 /*
  * lora_linear_bwd -- closed-form gradients of Y = X W_g^T + s_g (X A_g^T) B_g^T over

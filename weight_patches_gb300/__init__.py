@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_HERE, "libweight_patches_gb300.so")
 
 WP_BF16, WP_FP32, WP_NF4 = 0, 1, 2
 WP_PATCH_ADD, WP_PATCH_SET = 0, 1
-WP_OP_FWD, WP_OP_FWD_GROUPED, WP_OP_BWD, WP_OP_FWD_HOST = 0, 1, 2, 3
+WP_OP_FWD, WP_OP_FWD_GROUPED, WP_OP_BWD, WP_OP_FWD_HOST, WP_OP_SWIGLU_FWD = 0, 1, 2, 3, 4
 STATUS = {0: "WP_OK", -1: "WP_ERR_INVALID", -2: "WP_ERR_SHAPE", -3: "WP_ERR_DTYPE",
           -4: "WP_ERR_ALIGN", -5: "WP_ERR_WORKSPACE", -6: "WP_ERR_CUDA", -7: "WP_ERR_TIMEOUT",
           -8: "WP_ERR_UNSUPPORTED"}
@@ -75,6 +75,8 @@ def _load():
     lib.lora_linear_fwd_noalloc.argtypes = [pm, pm, pm, pa, I32, D, po, P]
     lib.lora_linear_fwd_host.argtypes = [pm, pm, pm, I32, pa, I32, D, po, P, SZ, P]
     lib.lora_linear_bwd.argtypes = [pm, pm, pm, I32, pa, D, po, po, po, P, SZ, P]
+    lib.lora_swiglu_fwd.argtypes = [pm, pm, pm, pa, D, po, po, P, SZ, P]
+    lib.lora_swiglu_bwd.argtypes = [pm, pm, po, po, P]
     lib.lora_dense_patch.argtypes = [P, I32, I64, P, I32, I64, I32, D, P]
     lib.lora_workspace_size.argtypes = [I32, pm, pm, pa, I32]
     lib.lora_workspace_size.restype = SZ
@@ -213,6 +215,44 @@ def lora_linear_fwd_grouped(X: torch.Tensor, W_stacked, bias: Optional[torch.Ten
                                          _stream(X.device))
     _check(st, "lora_linear_fwd_grouped")
     return out
+
+
+def lora_swiglu_fwd(X: torch.Tensor, W_gate_up, bias: Optional[torch.Tensor], adapters: Sequence[Adapter],
+                    request_scale: float = 1.0, out: Optional[torch.Tensor] = None,
+                    eg: Optional[torch.Tensor] = None, save_eg: bool = False,
+                    workspace: Optional[torch.Tensor] = None):
+    """SwiGLU front half: h = silu(e) g with e, g the gate and up LoRA linears of the stacked
+    ``W_gate_up`` ([2F, in]; ``adapters`` = [gate, up]).  Returns h, or (h, eg) when
+    ``save_eg`` or ``eg`` is given (eg = e | g, [T, 2F], what the backward needs)."""
+    n2 = W_gate_up.rows if isinstance(W_gate_up, NF4Weight) else W_gate_up.shape[0]
+    if out is None:
+        out = torch.empty(X.shape[0], n2 // 2, dtype=torch.bfloat16, device=X.device)
+    if eg is None and save_eg:
+        eg = torch.empty(X.shape[0], n2, dtype=torch.bfloat16, device=X.device)
+    xm, wm, bm, arr, hm = _mat(X), _mat(W_gate_up), _mat(bias), _adapters(adapters), _out(out)
+    egm = _out(eg) if eg is not None else None
+    ws, nbytes = _workspace(WP_OP_SWIGLU_FWD, xm, wm, arr, len(adapters), X.device, workspace)
+    st = _load().lora_swiglu_fwd(ctypes.byref(xm), ctypes.byref(wm), _ref(bm), arr, float(request_scale),
+                                 ctypes.byref(hm), _ref(egm), ws.data_ptr() if ws is not None else None,
+                                 nbytes, _stream(X.device))
+    _check(st, "lora_swiglu_fwd")
+    return (out, eg) if eg is not None else out
+
+
+def lora_swiglu_bwd(dH: torch.Tensor, eg: torch.Tensor, deg: Optional[torch.Tensor] = None,
+                    h: Optional[torch.Tensor] = None, want_h: bool = False):
+    """SwiGLU backward: from the gradient at h and the saved e | g, de | dg ([T, 2F], the
+    stacked gate/up output gradient); with ``want_h`` (or ``h``) also h recomputed.
+    Returns deg, or (deg, h)."""
+    if deg is None:
+        deg = torch.empty_like(eg)
+    if h is None and want_h:
+        h = torch.empty_like(dH)
+    hm = _out(h) if h is not None else None
+    st = _load().lora_swiglu_bwd(ctypes.byref(_mat(dH)), ctypes.byref(_mat(eg)), ctypes.byref(_out(deg)),
+                                 _ref(hm), _stream(dH.device))
+    _check(st, "lora_swiglu_bwd")
+    return (deg, h) if h is not None else deg
 
 
 def lora_linear_fwd_host(X_host: torch.Tensor, W, bias: Optional[torch.Tensor], adapters: Sequence[Adapter],

@@ -173,7 +173,8 @@ size_t fwd_workspace(const wp_mat* X, const FwdPlan& plan) {
 int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool grouped,
              const wp_adapter* adapters, int n_adapters, double request_scale, const wp_out* Y,
              void* workspace, size_t ws_bytes, cudaStream_t stream, float* h_out = nullptr,
-             int h_out_ld = 0, bool rank_only = false) {
+             int h_out_ld = 0, bool rank_only = false, bool swiglu = false,
+             const wp_out* eg = nullptr) {
   if (!valid_input(X, false)) return WP_ERR_INVALID;
   if (W && !valid_input(W, true)) return WP_ERR_INVALID;
   if (rank_only ? (W || bias || !h_out || n_adapters < 1 || X->dtype != WP_BF16) : !valid_output(Y))
@@ -183,11 +184,15 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   if (n_adapters > 0 && !adapters) return WP_ERR_INVALID;
   if (grouped && (G < 1 || G > kMaxGroups || n_adapters != G)) return WP_ERR_INVALID;
   if (!grouped) G = 1;
+  // SwiGLU front half: the gate and up groups of a stacked W, h = silu(e) g out
+  if (swiglu && (!W || !grouped || G != 2 || rank_only || Y->dtype != WP_BF16)) return WP_ERR_INVALID;
+  if (eg && (!swiglu || !valid_output(eg) || eg->dtype != WP_BF16)) return WP_ERR_INVALID;
 
   const long long T = X->rows, K = X->cols;
   const long long N = W ? W->rows : rank_only ? G * adapters[0].B.rows : Y->cols;
   if (W && W->cols != K) return WP_ERR_SHAPE;
-  if (!rank_only && (Y->rows != T || Y->cols != N)) return WP_ERR_SHAPE;
+  if (!rank_only && (Y->rows != T || Y->cols != (swiglu ? N / 2 : N))) return WP_ERR_SHAPE;
+  if (eg && (eg->rows != T || eg->cols != N)) return WP_ERR_SHAPE;
   if (N % G) return WP_ERR_SHAPE;
   const long long out_g = N / G;
   if (W && W->dtype == WP_NF4 && (K % 64 != 0 || W->ld != K)) return WP_ERR_SHAPE;
@@ -222,6 +227,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   if (!plan.tc) {
     // ------------------------------------------------------------- exact FP32 path
     if (W && W->dtype == WP_NF4) return WP_ERR_DTYPE;
+    if (swiglu) return WP_ERR_DTYPE;
     F32Params fp{};
     fp.T = static_cast<int>(T); fp.K = static_cast<int>(K); fp.N = static_cast<int>(N);
     fp.X = X->data; fp.x_dtype = X->dtype; fp.ldx = X->ld;
@@ -258,6 +264,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   if (W && (!aligned16(W->data) || W->ld % 8)) return WP_ERR_ALIGN;
   if (!rank_only && (!aligned16(Y->data) || Y->ld % (Y->dtype == WP_BF16 ? 8 : 4))) return WP_ERR_ALIGN;
   if (out_g % 8) return WP_ERR_ALIGN;
+  if (eg && (!aligned16(eg->data) || eg->ld % 8)) return WP_ERR_ALIGN;
 
   TcParams p{};
   TcMaps maps;
@@ -367,6 +374,17 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     }
   }
   p.ad_begin[G] = p.n_ad;
+  if (swiglu) {
+    // one kind of tile: 128 gate and the same 128 up columns, every adapter applied (each
+    // to its own half of the tile)
+    if (p.n_ad32 > 0) return WP_ERR_UNSUPPORTED;
+    p.swiglu = 1;
+    p.G = 1;
+    p.nt_g = static_cast<int>((out_g + 127) / 128);
+    p.total_tiles = p.m_tiles * p.nt_g;
+    p.ad_begin[1] = p.n_ad;
+    if (eg) { p.eg = static_cast<uint16_t*>(eg->data); p.ld_eg = eg->ld; }
+  }
   if (p.n_ad > 0) {
     // Rank columns of the pair's MMA (N = htot = sum of pw): each CTA supplies half of
     // every adapter's packed A rows, so both halves are equally wide
@@ -441,7 +459,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     if (rc != WP_OK) return rc;
   }
   if (!rank_only) {
-    rc = make_map(&maps.y, Y->dtype, Y->data, N, T, Y->ld, Y->dtype == WP_FP32 ? 32 : 64, kBM);
+    rc = make_map(&maps.y, Y->dtype, Y->data, swiglu ? out_g : N, T, Y->ld, Y->dtype == WP_FP32 ? 32 : 64, kBM);
     if (rc != WP_OK) return rc;
   }
   if (p.n_ad > 0) {
@@ -873,6 +891,39 @@ int lora_linear_fwd_grouped(const wp_mat* X, const wp_mat* W_stacked, const wp_m
                   workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
+int lora_swiglu_fwd(const wp_mat* X, const wp_mat* W_gate_up, const wp_mat* bias,
+                    const wp_adapter* adapters, double request_scale, const wp_out* H,
+                    const wp_out* EG, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!W_gate_up || !H) return WP_ERR_INVALID;
+  return fwd_impl(X, W_gate_up, bias, 2, true, adapters, 2, request_scale, H, workspace,
+                  workspace_bytes, static_cast<cudaStream_t>(stream), nullptr, 0, false, true, EG);
+}
+
+int lora_swiglu_bwd(const wp_mat* dH, const wp_mat* EG, const wp_out* dEG, const wp_out* H,
+                    void* stream) {
+  if (!dH || !EG || !dEG) return WP_ERR_INVALID;
+  if (!dH->data || !EG->data || !dEG->data || (H && !H->data)) return WP_ERR_INVALID;
+  if (dH->dtype != WP_BF16 || EG->dtype != WP_BF16 || dEG->dtype != WP_BF16 ||
+      (H && H->dtype != WP_BF16))
+    return WP_ERR_DTYPE;
+  const long long T = dH->rows, F = dH->cols;
+  if (T < 0 || F < 0 || EG->rows != T || EG->cols != 2 * F || dEG->rows != T || dEG->cols != 2 * F ||
+      (H && (H->rows != T || H->cols != F)))
+    return WP_ERR_SHAPE;
+  if (dH->ld < F || EG->ld < 2 * F || dEG->ld < 2 * F || (H && H->ld < F)) return WP_ERR_SHAPE;
+  if (F % 8 || dH->ld % 8 || EG->ld % 8 || dEG->ld % 8 || (H && H->ld % 8) || !aligned16(dH->data) ||
+      !aligned16(EG->data) || !aligned16(dEG->data) || (H && !aligned16(H->data)))
+    return WP_ERR_ALIGN;
+  if (T * F == 0) return WP_OK;
+  SwigluBwdParams q{};
+  q.T = T; q.F = F;
+  q.dh = static_cast<const uint16_t*>(dH->data); q.ld_dh = dH->ld;
+  q.eg = static_cast<const uint16_t*>(EG->data); q.ld_eg = EG->ld;
+  q.deg = static_cast<uint16_t*>(dEG->data); q.ld_deg = dEG->ld;
+  q.h = H ? static_cast<uint16_t*>(H->data) : nullptr; q.ld_h = H ? H->ld : 0;
+  return launch_swiglu_bwd(q, static_cast<cudaStream_t>(stream));
+}
+
 int lora_linear_bwd(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int32_t n_groups,
                     const wp_adapter* adapters, double request_scale, const wp_out* dX,
                     const wp_out* dA, const wp_out* dB, void* workspace,
@@ -898,7 +949,7 @@ int lora_dense_patch(void* param, int32_t param_dtype, int64_t param_numel, cons
 size_t lora_workspace_size(int32_t op, const wp_mat* X, const wp_mat* W,
                            const wp_adapter* adapters, int32_t n_adapters) {
   if (!X || n_adapters < 0 || (n_adapters > 0 && !adapters)) return 0;
-  if (op == WP_OP_FWD || op == WP_OP_FWD_GROUPED) {
+  if (op == WP_OP_FWD || op == WP_OP_FWD_GROUPED || op == WP_OP_SWIGLU_FWD) {
     FwdPlan plan;
     plan_fwd(X, W, adapters, n_adapters, &plan);
     return fwd_workspace(X, plan);

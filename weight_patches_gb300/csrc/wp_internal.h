@@ -98,6 +98,12 @@ struct TcParams {
   void* Y;
   long long ldy;
   int y_f32;
+  // SwiGLU front half: every tile holds 128 gate columns (CTA 0's weight rows) and the same
+  // 128 up columns (CTA 1's); Y is h = silu(e) g [T, out_g]; eg, when set, receives the
+  // bf16 e | g [T, 2 out_g] that the backward needs
+  int swiglu;
+  uint16_t* eg;
+  long long ld_eg;
   unsigned long long timeout_ns;
 };
 
@@ -115,6 +121,17 @@ struct TcMaps {
 };
 
 // Number of CTA pairs that can be resident at once for this shared-memory size.
+// SwiGLU backward, elementwise: from the gradient at h and the saved e | g, the gradients
+// at e and g (written as de | dg, the stacked gate/up output gradient) and h itself
+struct SwigluBwdParams {
+  long long T, F;
+  const uint16_t* dh; long long ld_dh;
+  const uint16_t* eg; long long ld_eg;
+  uint16_t* deg; long long ld_deg;
+  uint16_t* h; long long ld_h;       // optional
+};
+int launch_swiglu_bwd(const SwigluBwdParams& q, cudaStream_t stream);
+
 int tc_max_pairs(size_t smem_bytes, bool nf4);
 int launch_tc_fwd(const TcMaps& maps, const TcParams& p, int grid, size_t smem_bytes,
                   cudaStream_t stream, bool nf4);

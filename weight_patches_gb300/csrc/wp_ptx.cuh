@@ -469,4 +469,18 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, ui
                : "memory");
 }
 
+// ---------------------------------------------------------------- SwiGLU activation
+// Unsloth fast_lora walkthrough, section 4 (LoRA_MLP): h = f(e) g with the SiLU gate
+// f(e) = e sigmoid(e).  One definition for the fused forward epilogue and the backward
+// kernel, so that the h the backward recomputes from the saved bf16 e and g is the very
+// value the forward wrote.  sigmoid(e) = 1 / (1 + exp(-e)); for e below about -88 the
+// exponential overflows to +inf and both functions return 0 (the true values are below
+// 1e-36 in magnitude).
+__device__ __forceinline__ float sigmoid_f32(float e) {
+  return __fdividef(1.0f, __fadd_rn(1.0f, __expf(-e)));
+}
+__device__ __forceinline__ float silu_f32(float e) {
+  return __fdividef(e, __fadd_rn(1.0f, __expf(-e)));
+}
+
 }  // namespace wp

@@ -140,6 +140,17 @@ __device__ __forceinline__ void lookup4(uint32_t codes, const uint32_t (&lo)[4],
 
 constexpr uint16_t kBothCtas = 0x3;
 
+// First weight row of this CTA's half of tile t: 128 consecutive rows of the tile's column
+// group, or, for the SwiGLU front half, the tile's 128 gate rows (CTA 0) or up rows (CTA 1)
+__device__ __forceinline__ int weight_row(const TcParams& p, const Tile& t, uint32_t cta) {
+  return p.swiglu ? (cta ? p.out_g : 0) + t.j * 128 : t.g * p.out_g + t.j * kBN + static_cast<int>(cta) * 128;
+}
+
+__device__ __forceinline__ float bias_at(const TcParams& p, int col) {
+  return p.bias_f32 ? static_cast<const float*>(p.bias)[col]
+                    : bf16_to_f32(static_cast<const uint16_t*>(p.bias)[col]);
+}
+
 }  // namespace
 
 // kF32: the epilogue also adds FP32 adapters by FFMA (those too wide to ride as bf16
@@ -156,9 +167,9 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
   // holds [codes 4 KiB | block scales 2 KiB] and its W half is the dequantised tile.
   const int S = p.stages;
   const int SB = p.stage_bytes;
-  const int R = kNF4 ? p.code_slots : 0;                // 4-bit W: codes ring
+  const int R = kNF4 ? p.code_slots : 1;                // 4-bit W: codes ring slots
   uint8_t* codes = sbase + S * SB;                      // [R] codes | block scales
-  uint8_t* stg = codes + R * kCodeSlotBytes;            // 2 output staging buffers
+  uint8_t* stg = codes + (kNF4 ? R * kCodeSlotBytes : 0);   // 2 output staging buffers
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg + 2 * kStgBytes);
   uint64_t* full = bars;                  // [S]  leader: TMA bytes of both CTAs landed
   uint64_t* empty = bars + S;             // [S]  both: the pair MMAs consumed the stage
@@ -267,7 +278,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
           if (!next_item(citer, p, pair, npairs, cit)) { c_more = false; return true; }
           if (!cit.rank) {
             c_kb = 0;
-            c_wrow = cit.t.g * p.out_g + cit.t.j * kBN + static_cast<int>(cta) * 128;
+            c_wrow = weight_row(p, cit.t, cta);
           }
         }
         const uint32_t slot = c_issued % static_cast<uint32_t>(R);
@@ -315,7 +326,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         if (a1 > a0)
           for (int h = 0; h < nblk; ++h) peek = min(peek, ld_acquire_gpu(p.flags + blk0 + h));
         if (p.has_base) {
-          const int w_row = t.g * p.out_g + t.j * kBN + static_cast<int>(cta) * 128;
+          const int w_row = weight_row(p, t, cta);
           for (int kb = 0; kb < p.k_blocks; ++kb) {
             uint8_t* st;
             uint32_t fb;
@@ -343,8 +354,11 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
             ok = flag_wait(p.flags + blk0 + h, 2u, abort_flag, tmo, status);
           if (!ok) break;
           fence_proxy_async_global();
-          const int b_row = t.j * kBN + static_cast<int>(cta) * 128;
           for (int a = a0; a < a1 && ok; ++a) {
+            // SwiGLU: an adapter's B rows go to the CTA of its own half; the other CTA's
+            // box starts past the last row, so TMA fills it with zeros
+            const int b_row = !p.swiglu ? t.j * kBN + static_cast<int>(cta) * 128
+                              : p.ad[a].group == static_cast<int>(cta) ? t.j * 128 : p.out_g + t.j * 128;
             for (int c = 0; c < p.ad[a].nchunks; ++c) {
               // a chunk with at most 32 ranks left travels in 32-rank boxes (half the bytes)
               const bool narrow = p.ad[a].rpad16 - 64 * c <= 32;
@@ -600,6 +614,95 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         if (named_bar_any(!ok, 2, 128)) break;
         tc_fence_after();
       }
+      if (p.swiglu) {
+        // SwiGLU front half: accumulator columns [0, 128) hold e (gate) and [128, 256) g
+        // (up) of the same output columns.  e and g are rounded to bf16 once -- they are
+        // the two linears' outputs, written to eg when asked -- and h = silu(e) g is
+        // rounded once; h chunks of 64 columns go out like the plain output.
+        const int ncol = min(128, p.out_g - t.j * 128);
+        const int nch = (ncol + 63) / 64;
+#pragma unroll 1
+        for (int h = 0; h < kMH; ++h) {
+          const int row0 = t.m * (kPairM * kMH) + h * kPairM + static_cast<int>(cta) * kBM;
+          const int row = row0 + row_in_cta;
+          const bool row_ok = row < p.T;
+          const uint32_t acc_t = tmem + (b + h) * kBN;
+#pragma unroll 1
+          for (int c = 0; c < nch; ++c) {
+            const int cig = t.j * 128 + c * 64;            // first h column of the chunk
+            const int ncols = min(64, p.out_g - cig);
+            const bool full_chunk = ncols == 64;
+            const uint32_t buf = stg_addr + (sidx & 1) * kStgBytes;
+            if (full_chunk) {
+              if (sidx >= 2 && elected) bulk_wait_read_le1();
+              named_bar_sync(1, 128);
+            }
+#pragma unroll 1
+            for (int sub = 0; sub < 2; ++sub) {
+              const int c0 = c * 64 + sub * 32;            // column within the tile's 128
+              uint32_t re[32], rg[32];
+              tmem_ld32(acc_t + lane_base + c0, re);
+              tmem_ld32(acc_t + lane_base + 128 + c0, rg);
+              if (h == kMH - 1 && c == nch - 1 && sub == 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(acc_empty_l[b]);
+              }
+              const int nc = min(32, ncols - sub * 32);
+              const int col = cig + sub * 32;              // first column of the sub-chunk
+              uint32_t eb[16], gb[16], hb[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float e0 = u2f(re[2 * i]), e1 = u2f(re[2 * i + 1]);
+                float g0 = u2f(rg[2 * i]), g1 = u2f(rg[2 * i + 1]);
+                if (p.bias && 2 * i < nc) {
+                  e0 += bias_at(p, col + 2 * i); e1 += bias_at(p, col + 2 * i + 1);
+                  g0 += bias_at(p, p.out_g + col + 2 * i); g1 += bias_at(p, p.out_g + col + 2 * i + 1);
+                }
+                eb[i] = pack_bf16x2(e0, e1);
+                gb[i] = pack_bf16x2(g0, g1);
+                hb[i] = pack_bf16x2(__fmul_rn(silu_f32(u2f(eb[i] << 16)), u2f(gb[i] << 16)),
+                                    __fmul_rn(silu_f32(u2f(eb[i] & 0xffff0000u)), u2f(gb[i] & 0xffff0000u)));
+              }
+              if (p.eg && row_ok) {
+                uint16_t* pe = p.eg + static_cast<long long>(row) * p.ld_eg + col;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  if (u * 8 < nc) {
+                    st_global_v4_hint(pe + u * 8, eb[4 * u], eb[4 * u + 1], eb[4 * u + 2], eb[4 * u + 3], stream_out);
+                    st_global_v4_hint(pe + p.out_g + u * 8, gb[4 * u], gb[4 * u + 1], gb[4 * u + 2], gb[4 * u + 3],
+                                      stream_out);
+                  }
+              }
+              if (full_chunk) {
+                const uint32_t rowb = buf + row_in_cta * 128;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  st_shared_v4(rowb + (((sub * 4 + u) ^ (row_in_cta & 7)) * 16), hb[4 * u], hb[4 * u + 1],
+                               hb[4 * u + 2], hb[4 * u + 3]);
+              } else if (row_ok) {
+                uint16_t* y = static_cast<uint16_t*>(p.Y) + static_cast<long long>(row) * p.ldy + col;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  if (u * 8 < nc)
+                    st_global_v4_hint(y + u * 8, hb[4 * u], hb[4 * u + 1], hb[4 * u + 2], hb[4 * u + 3], stream_out);
+              }
+            }
+            if (full_chunk) {
+              fence_proxy_async_smem();
+              named_bar_sync(1, 128);
+              if (elected && row0 < p.T) {
+                tma_store_2d_hint(&maps.y, cig, row0, stg + (sidx & 1) * kStgBytes, stream_out);
+                bulk_commit();
+              }
+              ++sidx;
+            }
+          }
+        }
+        ++nuse[b];
+        ++count;
+        continue;
+      }
 
       // valid chunks of this tile (the last tile of a group may be partial)
       const int nchunk = min(kBN / cw, (p.out_g - t.j * kBN + cw - 1) / cw);
@@ -818,7 +921,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       }
       const Tile& t = it.t;
       const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
-      const int wrow = t.g * p.out_g + t.j * kBN + static_cast<int>(cta) * 128 + r;
+      const int wrow = weight_row(p, t, cta) + r;
       const bool wrow_ok = wrow < p.N;
       const float* am_row = p.absmax + static_cast<long long>(wrow_ok ? wrow : 0) * kb64;
       for (int kb = 0; kb < p.k_blocks && ok; ++kb, ++kc) {
