@@ -641,8 +641,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
             for (int sub = 0; sub < 2; ++sub) {
               const int c0 = c * 64 + sub * 32;            // column within the tile's 128
               uint32_t re[32], rg[32];
-              tmem_ld32(acc_t + lane_base + c0, re);
-              tmem_ld32(acc_t + lane_base + 128 + c0, rg);
+              tmem_ld32x2(acc_t + lane_base + c0, re, acc_t + lane_base + 128 + c0, rg);
               if (h == kMH - 1 && c == nch - 1 && sub == 1) {
                 tc_fence_before();
                 __syncwarp();
