@@ -1,0 +1,115 @@
+"""The small-token path (the weight streamed once over every SM, swapped MMAs, K split,
+one reduction pass; 4-bit weights up to 64 tokens, bf16 weights up to 4) against the FP64
+oracle with the bf16 accuracy gate.  Token counts just past the bf16 limit check the
+hand-over to the general path.
+
+InvokeAI sidecar-patch article, section 五: quantised layers under few tokens go through a
+small-batch kernel; here both bf16 and 4-bit weights do, with the LoRA terms fused in.
+Covered: one token, ragged token counts, ragged weight rows, 4-bit weights with and
+without TMA-fed block scales, stacked column groups, delta-only layers, several adapters,
+bias, fp32 output, zero strength, and full-size layers of the workloads (sampled output
+columns)."""
+import numpy as np
+import pytest
+import torch
+
+import weight_patches_gb300 as wpg
+import workloads
+from oracle import lora as olora
+from oracle.numerics import relative_rms, to_f64
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+BF16_TOL = 4e-3
+
+
+def _layer(T, K, N, ranks, kind="bf16", bias=None, groups=1, strengths=None, seed=0, with_w=True):
+    rng = np.random.default_rng(seed)
+    X = workloads.draw(rng, T, K, 1.0)
+    W = None
+    if with_w:
+        W = workloads.draw_nf4(rng, N, K) if kind == "nf4" else workloads.draw(rng, N, K, (1.0 / K) ** 0.5)
+    b = None
+    if bias is not None:
+        b = workloads.draw(rng, 1, N, 0.01, kind=bias)
+    og = N // groups
+    strengths = strengths or [1.0] * len(ranks)
+    patches = [workloads.Patch(workloads.draw(rng, r, K, (1.0 / K) ** 0.5),
+                               workloads.draw(rng, og if groups > 1 else N, r, 0.02), float(r), st)
+               for r, st in zip(ranks, strengths)]
+    return workloads.Linear(f"small_{kind}", X, W, b, patches, groups=groups)
+
+
+def _check(lin, out_dtype=torch.bfloat16):
+    Y = gu.run_fwd(lin, out_dtype=out_dtype)
+    assert wpg.lora_device_status() == 0
+    err, chain = gu.errors(lin, Y)
+    assert err <= BF16_TOL, err
+    assert err <= chain, (err, chain)
+    return Y
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 16])
+def test_bf16_weight(T):
+    _check(_layer(T, 256, 320, [16], bias="bf16", seed=T))
+
+
+@pytest.mark.parametrize("T,K,N", [(1, 512, 384), (33, 512, 384), (20, 320, 200), (64, 256, 264)])
+def test_nf4_weight(T, K, N):
+    # K = 512: block scales by TMA; K = 320: block scales loaded by the dequantisation warps
+    _check(_layer(T, K, N, [16], kind="nf4", seed=T + K))
+
+
+def test_grouped_qkv():
+    _check(_layer(3, 320, 3 * 320, [32, 32, 32], groups=3, seed=3))
+
+
+def test_grouped_nf4():
+    _check(_layer(40, 256, 2 * 320, [16, 16], kind="nf4", groups=2, seed=8))
+
+
+def test_delta_only():
+    _check(_layer(2, 256, 264, [8], with_w=False, seed=5))
+
+
+def test_several_adapters_fp32_out():
+    lin = _layer(4, 384, 384, [8, 40, 128], bias="fp32", strengths=[1.0, 0.6, -0.3], seed=6)
+    _check(lin, out_dtype=torch.float32)
+
+
+def test_zero_strength_equals_base():
+    lin = _layer(3, 256, 320, [16], strengths=[0.0], seed=7)
+    X, W = gu.dev(lin.X), gu.dev(lin.W)
+    y0 = wpg.lora_linear_fwd(X, W, None, gu.adapters(lin))
+    y1 = wpg.lora_linear_fwd(X, W, None, [])
+    torch.cuda.synchronize()
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+
+
+@pytest.mark.parametrize("cfg,T", [("c1", 4), ("c3", 1), ("c3", 64)])
+def test_full_size_layers(cfg, T):
+    """Full-size weights of the workloads with few tokens; the oracle checks 256 sampled
+    output columns (weight rows decoded one block at a time)."""
+    lin = workloads.config1("full") if cfg == "c1" else workloads.config3("full")[0]
+    X = lin.X.slice_rows(0, T)
+    small = workloads.Linear(lin.name, X, lin.W, lin.bias, lin.patches, lin.request_scale, lin.groups)
+    Y = gu.run_fwd(small)
+    assert wpg.lora_device_status() == 0
+    got = gu.to_f64(Y)
+    N = lin.W.rows
+    og = N // lin.groups
+    rng = np.random.default_rng(99)
+    cols = np.sort(rng.choice(N, 256, replace=False))
+    Xf = to_f64(X)
+    bias = to_f64(lin.bias).reshape(-1) if lin.bias is not None else None
+    want = np.empty((T, len(cols)))
+    for k, c in enumerate(cols):
+        w = to_f64(lin.W.slice_rows(int(c), int(c) + 1))[0]
+        y = Xf @ w + (bias[c] if bias is not None else 0.0)
+        g = c // og if lin.groups > 1 else 0
+        p = olora.decode_patch(lin.patches[g])
+        s = olora.combined_scale(p.alpha, p.rank, p.strength, lin.request_scale)
+        y = y + s * ((Xf @ p.A.T) @ p.B[c - g * og])
+        want[:, k] = y
+    assert relative_rms(got[:, cols], want) <= BF16_TOL

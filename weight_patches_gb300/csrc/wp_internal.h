@@ -132,6 +132,66 @@ struct SwigluBwdParams {
 };
 int launch_swiglu_bwd(const SwigluBwdParams& q, cudaStream_t stream);
 
+// ------------------------------------------------------------------ small-token path
+// T <= 64 tokens: Y^T = W X^T with the weight rows as the 128-row MMA operand and the
+// tokens (rounded up to 16) as its width, single-CTA tcgen05; the adapters' A rows
+// (laid out one adapter after another at 16-aligned offsets) ride as extra row blocks, so X A^T comes
+// out of the same pass.  K is split so that the units fill the SMs; a second kernel sums
+// the splits, forms H~ = bf16(s X A^T), adds the bias and H~ B^T and rounds once.
+constexpr int kSkinnyMaxT = 64;
+constexpr int kSkinnyThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kSkinnyThreadsNF4 = 704;    // + warps 6..21 dequantisation (two groups of 8)
+constexpr int kSkinnyXBytes = kSkinnyMaxT * 128;   // X rows of a stage (64 rows x 64 K bf16)
+
+struct SkinnyParams {
+  int T, Tp;                   // tokens and the MMA width (T rounded up to 16)
+  int K, k_blocks;
+  int N;                       // output columns: weight rows, and the first A-row column
+  int nbW, nbA;                // 128-row blocks of W and of the A rows
+  int R16;                     // A rows: adapter i at rows [a_off[i], a_off[i] + ceil16(r_i))
+  int n_ad;
+  int a_off[kMaxAd + 1];       // a_off[n_ad] = R16
+  int splits, kb_per_split, units;
+  int am_tma;
+  const float* absmax;
+  float nf4_code[16];
+  float* part;                 // [splits][T][ldp] fp32: W rows, then the A rows at N
+  long long ldp;
+  int stages, stage_bytes;
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+struct SkinnyMaps {
+  CUtensorMap x, w, wq, am;
+  CUtensorMap a[kMaxAd];       // adapter A [r, in], boxes of 16 rows x 64 K (rows past r read 0)
+};
+
+struct SkinnyReduceParams {
+  int T, N, out_g, R16, splits, has_w;
+  long long ldp;
+  const float* part;
+  const void* bias;
+  int bias_f32;
+  int n_ad;
+  struct Ad {
+    int group, rank, toff;
+    int vec;                   // B rows 16-byte aligned: loaded 8 ranks at a time
+    float s;
+    const uint16_t* B;
+    long long ldb;
+  } ad[kMaxAd];
+  void* Y;
+  long long ldy;
+  int y_f32;
+};
+
+int launch_skinny(const SkinnyMaps& maps, const SkinnyParams& p, size_t smem_bytes, bool nf4,
+                  cudaStream_t stream);
+int launch_skinny_reduce(const SkinnyReduceParams& q, cudaStream_t stream);
+int skinny_grid_ctas(size_t smem_bytes, bool nf4);
+int* tc_status_ptr();
+
 int tc_max_pairs(size_t smem_bytes, bool nf4);
 int launch_tc_fwd(const TcMaps& maps, const TcParams& p, int grid, size_t smem_bytes,
                   cudaStream_t stream, bool nf4);

@@ -44,6 +44,7 @@
 #include <cuda_runtime.h>
 
 #include "wp_internal.h"
+#include "wp_nf4.cuh"
 #include "wp_ptx.cuh"
 
 namespace wp {
@@ -114,29 +115,6 @@ __device__ __forceinline__ bool next_item(ItemIter& s, const TcParams& p, int pa
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(uint32_t(h) << 16); }
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-
-// Four 4-bit codes -> four bf16 values from a 16-entry table split into byte planes:
-// lo[j] / hi[j] hold the low / high bytes of entries 4j..4j+3.  `codes` is 16 bits of the
-// packed stream as stored (byte k: element 2k in the high nibble), so its nibbles, low
-// to high, are the codes of elements 1, 0, 3, 2.  Each plane is looked up in both
-// half-tables (3-bit byte selects); a fourth permute keeps, per byte, the half the code's
-// bit 3 points at; the last two permutes interleave the planes back into element order.
-// Returns the words holding elements (0, 1) and (2, 3).
-__device__ __forceinline__ void lookup4(uint32_t codes, const uint32_t (&lo)[4], const uint32_t (&hi)[4],
-                                        uint32_t& out01, uint32_t& out23) {
-  const uint32_t sel3 = codes & 0x7777u;
-  const uint32_t pick = 0x3210u | ((codes >> 1) & 0x4444u);     // byte i from the upper half-table if code >= 8
-  const uint32_t l = prmt(prmt(lo[0], lo[1], sel3), prmt(lo[2], lo[3], sel3), pick);
-  const uint32_t h = prmt(prmt(hi[0], hi[1], sel3), prmt(hi[2], hi[3], sel3), pick);
-  out01 = prmt(l, h, 0x4051u);
-  out23 = prmt(l, h, 0x6273u);
-}
 
 constexpr uint16_t kBothCtas = 0x3;
 
@@ -936,29 +914,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         // releases the tile to the peer CTA) or, for K % 256 != 0, straight from memory
         const float am = p.am_tma ? reinterpret_cast<const float*>(raw + kRawBytes)[r * 4 + (kb & 3)]
                                   : (wrow_ok ? __ldg(am_row + kb) : 0.f);
-        // table: entries 2k, 2k+1 packed in e[k]; byte planes lo/hi of entries 4j..4j+3
-        uint32_t e[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) e[k] = pack_bf16x2(lv[2 * k] * am, lv[2 * k + 1] * am);
-        uint32_t lo[4], hi[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          lo[j] = prmt(e[2 * j], e[2 * j + 1], 0x6420u);
-          hi[j] = prmt(e[2 * j], e[2 * j + 1], 0x7531u);
-        }
-        const uint4 cw4 = *reinterpret_cast<const uint4*>(raw + r * 32 + hh * 16);
-        const uint32_t cwords[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
-        const uint32_t dst = smem_u32(sbase + stage * SB + kXBytes) + r * 128;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          // 4 bytes = 8 codes of consecutive elements
-          const uint32_t c = cwords[u];
-          uint32_t o0, o1, o2, o3;
-          lookup4(c & 0xFFFFu, lo, hi, o0, o1);
-          lookup4(c >> 16, lo, hi, o2, o3);
-          const int unit = hh * 4 + u;                    // 16-byte unit = 8 elements
-          st_shared_v4(dst + ((unit ^ (r & 7)) * 16), o0, o1, o2, o3);
-        }
+        nf4_dequant_half_row(raw + r * 32 + hh * 16, am, lv, smem_u32(sbase + stage * SB + kXBytes), r, hh);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -1072,6 +1028,12 @@ int launch_tc_fwd(const TcMaps& maps, const TcParams& p, int grid, size_t smem_b
                : launch_impl<true, false>(maps, p, grid, smem_bytes, stream);
   return f32 ? launch_impl<false, true>(maps, p, grid, smem_bytes, stream)
              : launch_impl<false, false>(maps, p, grid, smem_bytes, stream);
+}
+
+int* tc_status_ptr() {
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_tc_status) != cudaSuccess) return nullptr;
+  return static_cast<int*>(ptr);
 }
 
 int tc_fwd_status(int reset) {
