@@ -1,0 +1,91 @@
+"""LoRA merge into the base weight (oracle side).
+
+Test infrastructure only; see the package docstring.
+
+piper-offload docs, "LoRA merge" and "Quantized weight support": merging bakes the
+adapters into the weight in place -- a plain floating-point weight takes an ``addmm_``
+update, a bitsandbytes NF4 weight is dequantised, takes every LoRA of the target as one
+staged low-rank update and is re-encoded once; the re-encoding is stochastic by default
+and deterministic round-to-nearest on request (the deterministic form is the one here).
+The update of one adapter is s (B A) with s = alpha / r * strength * scale (the PEFT
+convention the rest of the library uses).
+
+Readings (the pages fix the flow, not the arithmetic):
+  * every adapter of a call is one update, accumulated exactly and rounded once:
+    W' = round(W + sum_p s_p B_p A_p);
+  * bf16 weight: round to nearest even;
+  * NF4 weight: W_eff = bf16(fl32(level[q]) * absmax) as in the forward; u = W_eff + update;
+    per 64-element block absmax' = max |u|, and each element's code is the nearest level of
+    u / absmax' -- decided, like the kernel, in float32: x = fl32(fl32(u) / absmax'), code =
+    the number of midpoints fl32((level[k] + level[k+1]) / 2) below x (a value on a midpoint
+    takes the lower code); an all-zero block keeps scale 0 and the code of level 0 (index 7).
+
+Pinned by ``tests/test_oracle_merge.py``: brute force (exhaustive argmin over the 16
+levels), the dequantise-requantise round trip on blocks that hold level +-1, merge and
+unmerge returning the weight within one rounding, zero strength leaving it unchanged,
+and the merged weight reproducing the unmerged forward (the forward is linear, Unsloth
+fast_lora walkthrough, section 2).
+"""
+from __future__ import annotations
+
+from typing import Sequence
+
+import numpy as np
+
+from . import nf4 as onf4
+from .lora import DecodedPatch, combined_scale
+from .numerics import f64_to_bf16_value
+
+
+def update(patches: Sequence[DecodedPatch], scale: float) -> np.ndarray:
+    """sum_p s_p B_p A_p in float64."""
+    U = None
+    for p in patches:
+        s = combined_scale(p.alpha, p.rank, p.strength, scale)
+        d = s * (p.B @ p.A)
+        U = d if U is None else U + d
+    return U
+
+
+def merge_bf16_values(W: np.ndarray, patches: Sequence[DecodedPatch], scale: float) -> np.ndarray:
+    """The merged bf16 weight (as float64 values) from the float64 values of the old one."""
+    return f64_to_bf16_value(W + update(patches, scale))
+
+
+def midpoints_f32() -> np.ndarray:
+    """The 15 decision points between consecutive levels, in float32."""
+    lv = onf4.codebook_f32()
+    return ((lv[:-1] + lv[1:]).astype(np.float32) * np.float32(0.5)).astype(np.float32)
+
+
+def quantize_blocks(u: np.ndarray):
+    """float32 [rows, cols] (cols % 64 == 0) -> (codes uint8 [rows, cols], absmax float32
+    [rows * cols / 64], x float32 [rows, cols]): the requantisation rule of the module
+    docstring, in float32."""
+    u = np.asarray(u, dtype=np.float32)
+    rows, cols = u.shape
+    b = u.reshape(-1, onf4.BLOCK)
+    m = np.max(np.abs(b), axis=1).astype(np.float32)
+    safe = np.where(m > 0, m, np.float32(1.0)).astype(np.float32)
+    x = (b / safe[:, None]).astype(np.float32)
+    mid = midpoints_f32()
+    codes = np.sum(x[:, :, None] > mid[None, None, :], axis=2).astype(np.uint8)
+    codes[m == 0] = 7
+    return codes.reshape(rows, cols), m, x.reshape(rows, cols)
+
+
+def nearest_level_brute(x: np.ndarray) -> np.ndarray:
+    """argmin_k |x - level[k]| over the 16 float32 levels (ties to the lower index), by
+    exhaustive comparison; the pin of the midpoint rule."""
+    lv = onf4.codebook_f32().astype(np.float64)
+    d = np.abs(np.asarray(x, dtype=np.float64)[..., None] - lv)
+    return np.argmin(d, axis=-1).astype(np.uint8)
+
+
+def merge_nf4(packed: np.ndarray, absmax: np.ndarray, rows: int, cols: int,
+              patches: Sequence[DecodedPatch], scale: float):
+    """(codes uint8 [rows, cols], absmax' float32, x float32): the requantised merge, with
+    u = fl32(W_eff + update) taken to float32 once before the float32 decisions."""
+    W = onf4.dequant_f64(packed, absmax, rows, cols)
+    u = (W + update(patches, scale)).astype(np.float32)
+    return quantize_blocks(u)
