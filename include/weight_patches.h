@@ -97,7 +97,7 @@ typedef struct wp_adapter {
 } wp_adapter;
 
 /* Operation ids for lora_workspace_size(). */
-enum { WP_OP_FWD = 0, WP_OP_FWD_GROUPED = 1, WP_OP_BWD = 2, WP_OP_FWD_HOST = 3, WP_OP_SWIGLU_FWD = 4 };
+enum { WP_OP_FWD = 0, WP_OP_FWD_GROUPED = 1, WP_OP_BWD = 2, WP_OP_FWD_HOST = 3, WP_OP_SWIGLU_FWD = 4, WP_OP_MERGE = 5 };
 
 /*
  * lora_linear_fwd -- Y = X W^T + bias + sum_p s_p (X A_p^T) B_p^T.
@@ -166,6 +166,26 @@ int lora_linear_fwd_host(const wp_mat* X_host, const wp_mat* W, const wp_mat* bi
                          int32_t n_groups, const wp_adapter* adapters, int32_t n_adapters,
                          double request_scale, const wp_out* Y_host, void* workspace,
                          size_t workspace_bytes, void* stream);
+
+/*
+ * lora_merge -- bake adapters into the base weight in place (piper-offload docs, "LoRA
+ * merge" and "Quantized weight support"; the PEFT merge):
+ *     W <- W + sum_p s_p B_p A_p,   s_p = alpha_p / r_p * strength_p * scale,
+ * every adapter of the call taken as one update, accumulated in fp32 and rounded once:
+ *   W WP_BF16 [out, in] (device): bf16_rne(fl32(W) + ...);
+ *   W WP_NF4 (codes [out, in/2] and absmax [out*in/64], device, both rewritten): dequantised
+ *     to W_eff, the update added in fp32, re-encoded with deterministic round-to-nearest: per
+ *     64-element block absmax' = max |u|, code = the nearest level of u / absmax' (a value on
+ *     a midpoint between two levels takes the lower code), an all-zero block keeps scale 0.
+ *   adapters: bf16 A [r, in], B [out, r]; strength 0 skips one; scale -1 undoes an earlier
+ *   merge of the same adapters up to the roundings.
+ *   workspace: lora_workspace_size(WP_OP_MERGE, NULL, W, adapters, n) bytes (A^T copies, and
+ *   an fp32 [out, in] buffer for a 4-bit W or several adapters).
+ * Errors: WP_ERR_SHAPE, WP_ERR_DTYPE (fp32 adapters), WP_ERR_ALIGN (bf16 W rows must be
+ * 16-byte aligned), WP_ERR_WORKSPACE.  With no non-zero adapter nothing is launched.
+ */
+int lora_merge(const wp_mat* W, const wp_adapter* adapters, int32_t n_adapters, double scale,
+               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * lora_swiglu_fwd -- the front half of a SwiGLU LoRA MLP in one pass: the gate and up

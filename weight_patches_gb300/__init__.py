@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_HERE, "libweight_patches_gb300.so")
 
 WP_BF16, WP_FP32, WP_NF4 = 0, 1, 2
 WP_PATCH_ADD, WP_PATCH_SET = 0, 1
-WP_OP_FWD, WP_OP_FWD_GROUPED, WP_OP_BWD, WP_OP_FWD_HOST, WP_OP_SWIGLU_FWD = 0, 1, 2, 3, 4
+WP_OP_FWD, WP_OP_FWD_GROUPED, WP_OP_BWD, WP_OP_FWD_HOST, WP_OP_SWIGLU_FWD, WP_OP_MERGE = 0, 1, 2, 3, 4, 5
 STATUS = {0: "WP_OK", -1: "WP_ERR_INVALID", -2: "WP_ERR_SHAPE", -3: "WP_ERR_DTYPE",
           -4: "WP_ERR_ALIGN", -5: "WP_ERR_WORKSPACE", -6: "WP_ERR_CUDA", -7: "WP_ERR_TIMEOUT",
           -8: "WP_ERR_UNSUPPORTED"}
@@ -76,6 +76,7 @@ def _load():
     lib.lora_linear_fwd_host.argtypes = [pm, pm, pm, I32, pa, I32, D, po, P, SZ, P]
     lib.lora_linear_bwd.argtypes = [pm, pm, pm, I32, pa, D, po, po, po, P, SZ, P]
     lib.lora_swiglu_fwd.argtypes = [pm, pm, pm, pa, D, po, po, P, SZ, P]
+    lib.lora_merge.argtypes = [pm, pa, I32, D, P, SZ, P]
     lib.lora_swiglu_bwd.argtypes = [pm, pm, po, po, P]
     lib.lora_dense_patch.argtypes = [P, I32, I64, P, I32, I64, I32, D, P]
     lib.lora_workspace_size.argtypes = [I32, pm, pm, pa, I32]
@@ -174,7 +175,7 @@ def _workspace(op, xm, wm, arr, n, device, workspace):
 
 def lora_workspace_size(op: int, X, W, adapters: Sequence[Adapter]) -> int:
     xm, wm, arr = _mat(X), _mat(W), _adapters(adapters)
-    return _load().lora_workspace_size(op, ctypes.byref(xm), _ref(wm), arr, len(adapters))
+    return _load().lora_workspace_size(op, _ref(xm), _ref(wm), arr, len(adapters))
 
 
 def _out_features(X, W, adapters):
@@ -215,6 +216,22 @@ def lora_linear_fwd_grouped(X: torch.Tensor, W_stacked, bias: Optional[torch.Ten
                                          _stream(X.device))
     _check(st, "lora_linear_fwd_grouped")
     return out
+
+
+def lora_merge(W, adapters: Sequence[Adapter], scale: float = 1.0, workspace: Optional[torch.Tensor] = None):
+    """Bake the adapters into W in place: W <- W + sum_p s_p B_p A_p (s_p = alpha/r * strength
+    * scale), accumulated in fp32 and rounded once; a 4-bit ``NF4Weight`` is requantised
+    (round to nearest).  Returns W."""
+    wm, arr = _mat(W), _adapters(adapters)
+    device = W.packed.device if isinstance(W, NF4Weight) else W.device
+    need = _load().lora_workspace_size(WP_OP_MERGE, None, ctypes.byref(wm), arr, len(adapters))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    nbytes = workspace.numel() if workspace is not None else 0
+    st = _load().lora_merge(ctypes.byref(wm), arr, len(adapters), float(scale),
+                            workspace.data_ptr() if workspace is not None else None, nbytes, _stream(device))
+    _check(st, "lora_merge")
+    return W
 
 
 def lora_swiglu_fwd(X: torch.Tensor, W_gate_up, bias: Optional[torch.Tensor], adapters: Sequence[Adapter],

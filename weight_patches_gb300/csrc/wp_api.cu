@@ -1025,6 +1025,158 @@ int device_sm_count() {
   return cached[dev];
 }
 
+// ------------------------------------------------------------------ merge
+// piper-offload docs, "LoRA merge": W <- W + sum_p s_p B_p A_p in place, every LoRA of the
+// target taken as one update and rounded (re-encoded, for a 4-bit weight) once.  Each
+// adapter's product runs on the fused kernel's base path with B_p as the token operand
+// [out, r] and A_p^T as the weight [in, r] (K = r), its epilogue computing s * acc + R:
+//   bf16 W, one adapter:  R = W, written back to W;
+//   bf16 W, several:      U = s_1 acc_1 + W (fp32), U = s_p acc_p + U, W = s_n acc_n + U;
+//   4-bit W:              U = fl32(W_eff), U = s_p acc_p + U for every adapter, requantise.
+// Workspace, each region 256-byte aligned: per adapter A^T [in, r8] bf16 and, when B's rows
+// are not 16-byte aligned, a copy of B [out, r8]; the fp32 U [out, in] when needed.
+struct MergeLayout {
+  size_t at[kMaxAd], bp[kMaxAd], u, total;
+  bool copy_b[kMaxAd];
+  bool need_u;
+  int n_eff;
+};
+
+bool merge_layout(const wp_mat* W, const wp_adapter* ad, int n, double scale, MergeLayout* L) {
+  *L = MergeLayout{};
+  if (!W || n < 0 || n > kMaxAd || (n > 0 && !ad)) return false;
+  const long long out = W->rows, in = W->cols;
+  size_t off = 0;
+  for (int i = 0; i < n; ++i) {
+    const long long r = ad[i].A.rows, r8 = (r + 7) / 8 * 8;
+    const double s = ad[i].alpha / static_cast<double>(r > 0 ? r : 1) * ad[i].strength * scale;
+    if (static_cast<float>(s) != 0.0f) ++L->n_eff;
+    L->at[i] = off;
+    off += round256(static_cast<size_t>(in) * r8 * 2);
+    L->copy_b[i] = !aligned16(ad[i].B.data) || ad[i].B.ld % 8 != 0;
+    L->bp[i] = off;
+    if (L->copy_b[i]) off += round256(static_cast<size_t>(out) * r8 * 2);
+  }
+  L->need_u = W->dtype == WP_NF4 || L->n_eff > 1;
+  L->u = off;
+  if (L->need_u) off += round256(static_cast<size_t>(out) * in * 4);
+  L->total = L->n_eff > 0 ? off : 0;
+  return true;
+}
+
+// One product pass: Y = s * (P Q^T) + R, P [rows, r] and Q [cols, r] K-major bf16.
+int merge_pass(const void* P, long long ldp, const void* Q, long long ldq, long long rows, long long cols, int r,
+               float s, const void* R, bool r_f32, long long ldr, void* Y, bool y_f32, long long ldy,
+               cudaStream_t stream) {
+  TcParams p{};
+  TcMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  p.T = static_cast<int>(rows); p.K = r; p.N = static_cast<int>(cols);
+  p.out_g = p.N; p.G = 1;
+  p.nt_g = (p.N + kBN - 1) / kBN;
+  p.m_shift = 0;
+  p.r_blocks = (p.T + kPairM - 1) / kPairM;
+  p.m_tiles = p.r_blocks;
+  p.total_tiles = p.m_tiles * p.nt_g;
+  p.k_blocks = (r + kBK - 1) / kBK;
+  p.has_base = 1;
+  p.Y = Y; p.ldy = ldy; p.y_f32 = y_f32 ? 1 : 0;
+  p.acc_scale = s; p.resid = R; p.ld_resid = ldr; p.resid_f32 = r_f32 ? 1 : 0;
+  p.timeout_ns = 2000000000ull;
+  p.stage_bytes = kATileBytes + kBHalfBytes;
+  const size_t fixed = 1024 + 2 * kStgBytes + 512;
+  p.stages = std::min<int>(kMaxStages, static_cast<int>((kSmemLimit - fixed) / p.stage_bytes));
+  const size_t smem = fixed + static_cast<size_t>(p.stages) * p.stage_bytes;
+  int rc = make_map_bf16(&maps.x, P, r, rows, ldp, kBK, kBM);
+  if (rc != WP_OK) return rc;
+  rc = make_map_bf16(&maps.w, Q, r, cols, ldq, kBK, 128);
+  if (rc != WP_OK) return rc;
+  rc = make_map(&maps.y, y_f32 ? WP_FP32 : WP_BF16, Y, cols, rows, ldy, y_f32 ? 32 : 64, kBM);
+  if (rc != WP_OK) return rc;
+  int pairs = tc_max_pairs(smem, false);
+  if (pairs <= 0) return WP_ERR_CUDA;
+  if (pairs > p.total_tiles) pairs = p.total_tiles;
+  p.rlead = 1;
+  return launch_tc_fwd(maps, p, 2 * pairs, smem, stream, false);
+}
+
+int merge_impl(const wp_mat* W, const wp_adapter* ad, int n, double scale, void* workspace, size_t ws_bytes,
+               cudaStream_t stream) {
+  if (!W || !W->data || W->rows <= 0 || W->cols <= 0) return WP_ERR_INVALID;
+  if (W->dtype != WP_BF16 && W->dtype != WP_NF4) return WP_ERR_DTYPE;
+  if (!std::isfinite(scale)) return WP_ERR_INVALID;
+  if (n < 0 || n > kMaxAd) return WP_ERR_UNSUPPORTED;
+  if (n > 0 && !ad) return WP_ERR_INVALID;
+  const long long out = W->rows, in = W->cols;
+  if (out > 0x7FFFFFFFLL || in > 0x7FFFFFFFLL) return WP_ERR_UNSUPPORTED;
+  const bool nf4 = W->dtype == WP_NF4;
+  if (nf4 ? (in % 64 != 0 || W->ld != in || !W->absmax || !aligned16(W->absmax) || !aligned16(W->data))
+          : (W->ld < in || W->ld % 8 != 0 || in % 8 != 0 || !aligned16(W->data)))
+    return nf4 ? WP_ERR_SHAPE : WP_ERR_ALIGN;
+  float s_of[kMaxAd];
+  for (int i = 0; i < n; ++i) {
+    const wp_adapter& a = ad[i];
+    if (!a.A.data || !a.B.data) return WP_ERR_INVALID;
+    if (a.A.dtype != WP_BF16 || a.B.dtype != WP_BF16) return WP_ERR_DTYPE;
+    const long long r = a.A.rows;
+    if (r <= 0 || r > 0x7FFFFFFFLL) return WP_ERR_INVALID;
+    if (a.A.cols != in || a.B.rows != out || a.B.cols != r || a.A.ld < in || a.B.ld < r) return WP_ERR_SHAPE;
+    if (!std::isfinite(a.alpha) || !std::isfinite(a.strength)) return WP_ERR_INVALID;
+    const double s = a.alpha / static_cast<double>(r) * a.strength * scale;
+    if (!std::isfinite(s) || !std::isfinite(static_cast<float>(s))) return WP_ERR_INVALID;
+    s_of[i] = static_cast<float>(s);
+  }
+  MergeLayout L;
+  if (!merge_layout(W, ad, n, scale, &L)) return WP_ERR_INVALID;
+  if (L.n_eff == 0) return WP_OK;                 // nothing to add: the weight stays bit-identical
+  if (!workspace || ws_bytes < L.total) return WP_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return WP_ERR_ALIGN;
+  char* ws = static_cast<char*>(workspace);
+  float* U = reinterpret_cast<float*>(ws + L.u);
+  void* wdata = const_cast<void*>(W->data);        // the weight is updated in place
+  NF4Table tab;
+  int rc = WP_OK;
+  if (nf4) {
+    nf4_codebook_host(tab.level);
+    rc = launch_nf4_to_f32(W->data, W->absmax, out * in, tab, U, stream);
+    if (rc != WP_OK) return rc;
+  }
+  int done = 0;
+  for (int i = 0; i < n; ++i) {
+    if (s_of[i] == 0.0f) continue;
+    const wp_adapter& a = ad[i];
+    const int r = static_cast<int>(a.A.rows);
+    const long long r8 = (r + 7) / 8 * 8;
+    uint16_t* at = reinterpret_cast<uint16_t*>(ws + L.at[i]);
+    rc = launch_transpose_bf16(a.A.data, a.A.ld, r, static_cast<int>(in), at, r8, stream);
+    if (rc != WP_OK) return rc;
+    const void* bp = a.B.data;
+    long long ldb = a.B.ld;
+    if (L.copy_b[i]) {
+      bp = ws + L.bp[i];
+      ldb = r8;
+      if (cudaMemcpy2DAsync(ws + L.bp[i], r8 * 2, a.B.data, a.B.ld * 2, static_cast<size_t>(r) * 2, out,
+                            cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+        return record_cuda();
+    }
+    ++done;
+    const bool first = done == 1, last = done == L.n_eff;
+    if (nf4) {
+      rc = merge_pass(bp, ldb, at, r8, out, in, r, s_of[i], U, true, in, U, true, in, stream);
+    } else if (L.n_eff == 1) {
+      rc = merge_pass(bp, ldb, at, r8, out, in, r, s_of[i], wdata, false, W->ld, wdata, false, W->ld, stream);
+    } else {
+      const void* R = first ? W->data : static_cast<const void*>(U);
+      void* Y = last ? wdata : static_cast<void*>(U);
+      rc = merge_pass(bp, ldb, at, r8, out, in, r, s_of[i], R, !first, first ? W->ld : in, Y, !last,
+                      last ? W->ld : in, stream);
+    }
+    if (rc != WP_OK) return rc;
+  }
+  if (nf4) rc = launch_nf4_requant(U, out * in, tab, wdata, const_cast<float*>(W->absmax), stream);
+  return rc;
+}
+
 }  // namespace wp
 
 using namespace wp;
@@ -1045,6 +1197,11 @@ int lora_linear_fwd_grouped(const wp_mat* X, const wp_mat* W_stacked, const wp_m
   if (!W_stacked) return WP_ERR_INVALID;
   return fwd_impl(X, W_stacked, bias, n_groups, true, adapters, n_groups, request_scale, Y,
                   workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int lora_merge(const wp_mat* W, const wp_adapter* adapters, int32_t n_adapters, double scale, void* workspace,
+               size_t workspace_bytes, void* stream) {
+  return merge_impl(W, adapters, n_adapters, scale, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 int lora_swiglu_fwd(const wp_mat* X, const wp_mat* W_gate_up, const wp_mat* bias,
@@ -1104,6 +1261,10 @@ int lora_dense_patch(void* param, int32_t param_dtype, int64_t param_numel, cons
 
 size_t lora_workspace_size(int32_t op, const wp_mat* X, const wp_mat* W,
                            const wp_adapter* adapters, int32_t n_adapters) {
+  if (op == WP_OP_MERGE) {
+    MergeLayout L;
+    return merge_layout(W, adapters, n_adapters, 1.0, &L) ? L.total : 0;
+  }
   if (!X || n_adapters < 0 || (n_adapters > 0 && !adapters)) return 0;
   if (op == WP_OP_FWD || op == WP_OP_FWD_GROUPED || op == WP_OP_SWIGLU_FWD) {
     FwdPlan plan;

@@ -95,6 +95,12 @@ struct TcParams {
   const void* bias;            // [N] or null
   int bias_f32;
   int bias_vec;                // bias 16-byte aligned: 16-byte loads of full sub-chunks
+  // merge: the accumulator times acc_scale plus a per-element residual R [T, N] (bf16 or
+  // fp32, may be Y itself: each element is read by the thread that writes it), in fp32
+  float acc_scale;
+  const void* resid;
+  long long ld_resid;
+  int resid_f32;
   void* Y;
   long long ldy;
   int y_f32;
@@ -261,6 +267,11 @@ int launch_rank_pack(const PackParams& p, cudaStream_t stream);
 struct NF4Table {
   float level[16];
 };
+// LoRA merge into a 4-bit weight (wp_merge.cu): W_eff as fp32, and the requantisation
+int launch_nf4_to_f32(const void* codes, const float* absmax, long long numel, const NF4Table& tab, float* U,
+                      cudaStream_t stream);
+int launch_nf4_requant(const float* U, long long numel, const NF4Table& tab, void* codes, float* absmax,
+                       cudaStream_t stream);
 int launch_transpose_bf16(const void* src, long long ld_s, int R, int C, void* dst, long long ld_d,
                           cudaStream_t stream);
 int launch_nf4_dequant_t(const void* codes, const float* absmax, int N, int K, const NF4Table& tab,

@@ -722,6 +722,37 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
           }
           const int nc = min(32, ncols - c0);               // valid columns of the sub-chunk
+          if (p.resid && row_ok && nc > 0) {
+            // merge: s * acc + R, two fp32 roundings, R read with 16-byte loads (the row
+            // pitch and the sub-chunk start are multiples of 8 elements)
+            if (p.resid_f32) {
+              const float* rp = static_cast<const float*>(p.resid) + static_cast<long long>(row) * p.ld_resid + gcol + c0;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                if (4 * i < nc) {
+                  const float4 r4 = *reinterpret_cast<const float4*>(rp + 4 * i);
+                  v[4 * i] = __fadd_rn(__fmul_rn(v[4 * i], p.acc_scale), r4.x);
+                  v[4 * i + 1] = __fadd_rn(__fmul_rn(v[4 * i + 1], p.acc_scale), r4.y);
+                  v[4 * i + 2] = __fadd_rn(__fmul_rn(v[4 * i + 2], p.acc_scale), r4.z);
+                  v[4 * i + 3] = __fadd_rn(__fmul_rn(v[4 * i + 3], p.acc_scale), r4.w);
+                }
+              }
+            } else {
+              const uint16_t* rp = static_cast<const uint16_t*>(p.resid) + static_cast<long long>(row) * p.ld_resid + gcol + c0;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                if (8 * i < nc) {
+                  const uint4 r8 = *reinterpret_cast<const uint4*>(rp + 8 * i);
+                  const uint32_t w[4] = {r8.x, r8.y, r8.z, r8.w};
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    v[8 * i + 2 * k] = __fadd_rn(__fmul_rn(v[8 * i + 2 * k], p.acc_scale), u2f(w[k] << 16));
+                    v[8 * i + 2 * k + 1] = __fadd_rn(__fmul_rn(v[8 * i + 2 * k + 1], p.acc_scale), u2f(w[k] & 0xffff0000u));
+                  }
+                }
+              }
+            }
+          }
           if (p.bias && nc > 0) {
             // 16-byte loads of the 32 bias values (the same for every row: broadcast)
             // where they all exist and the bias is aligned, single values otherwise
