@@ -70,4 +70,33 @@ __device__ __forceinline__ void nf4_dequant_half_row(const uint8_t* codes16, flo
   }
 }
 
+// All 64 elements of one block: row `r` of the tile, one table for the 64 codes.
+__device__ __forceinline__ void nf4_dequant_row(const uint8_t* codes32, float am, const float (&lv)[16],
+                                                uint32_t tile, int r) {
+  uint32_t e[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) e[k] = pack_bf16x2(lv[2 * k] * am, lv[2 * k + 1] * am);
+  uint32_t lo[4], hi[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    lo[j] = prmt(e[2 * j], e[2 * j + 1], 0x6420u);
+    hi[j] = prmt(e[2 * j], e[2 * j + 1], 0x7531u);
+  }
+  const uint32_t dst = tile + r * 128;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint4 cw4 = *reinterpret_cast<const uint4*>(codes32 + half * 16);
+    const uint32_t cwords[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t c = cwords[u];
+      uint32_t o0, o1, o2, o3;
+      lookup4(c & 0xFFFFu, lo, hi, o0, o1);
+      lookup4(c >> 16, lo, hi, o2, o3);
+      const int unit = half * 4 + u;
+      st_shared_v4(dst + ((unit ^ (r & 7)) * 16), o0, o1, o2, o3);
+    }
+  }
+}
+
 }  // namespace wp

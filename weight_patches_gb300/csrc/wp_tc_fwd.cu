@@ -136,6 +136,13 @@ __device__ __forceinline__ float bias_at(const TcParams& p, int col) {
 template <bool kNF4, bool kF32>
 __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     tc_fused_fwd_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
+  constexpr int kEpiWarp0 = kNF4 ? 4 : 2;              // first epilogue warp
+  constexpr int kEpiWarps = kNF4 ? 8 : 4;              // 4-bit W: one warpgroup per M half
+  constexpr int kDeqWarp0 = kEpiWarp0 + kEpiWarps;     // 4-bit W: 12 dequantisation warps
+  // token rows per pair tile: kMH halves of 256 rows, each with its own accumulator; a
+  // 4-bit W's stage holds both halves' X rows ahead of the weight slot
+  constexpr int kMH = kNF4 ? kMHalvesNF4 : 1;
+  constexpr int kXBytes = kMH * kATileBytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
@@ -170,16 +177,16 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&wfull[s], 32);           // 16 dequantisation warps x 2 CTAs
+      mbar_init(&wfull[s], 24);           // 12 dequantisation warps x 2 CTAs
     }
     for (int s = 0; s < R; ++s) {
       mbar_init(&code_full[s], 1);
-      mbar_init(&code_empty[s], 8);       // the 8 warps of one dequantisation group
+      mbar_init(&code_empty[s], 4);       // the 4 warps of one dequantisation group
     }
     mbar_init(&acc_full[0], 1);
     mbar_init(&acc_full[1], 1);
-    mbar_init(&acc_empty[0], 8);          // 4 epilogue warps x 2 CTAs
-    mbar_init(&acc_empty[1], 8);
+    mbar_init(&acc_empty[0], 2 * kEpiWarps);   // every epilogue warp of both CTAs
+    mbar_init(&acc_empty[1], 2 * kEpiWarps);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -203,14 +210,8 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   // 4-bit W: 24 warps launched at 80 registers (768 x 80 = 61440 in all); the warpgroups
-  // re-balance that exact total: TMA/MMA 128 x 56, epilogue 128 x 136, dequantisation
-  // 512 x 72
-  // 512 x 72 (each warpgroup runs one setmaxnreg at the top of its role branch)
-  constexpr int kEpiWarp0 = kNF4 ? 4 : 2;              // first of the 4 epilogue warps
-  // token rows per pair tile: kMH halves of 256 rows, each with its own accumulator; a
-  // 4-bit W's stage holds both halves' X rows ahead of the weight slot
-  constexpr int kMH = kNF4 ? kMHalvesNF4 : 1;
-  constexpr int kXBytes = kMH * kATileBytes;
+  // re-balance that exact total: TMA/MMA 128 x 56, epilogue 256 x 104, dequantisation
+  // 384 x 72 (each warpgroup runs one setmaxnreg at the top of its role branch)
 
   // Pair `pair` takes items pair, pair + npairs, pair + 2 npairs, ...
   const int npairs = static_cast<int>(gridDim.x >> 1);
@@ -470,19 +471,34 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       }
     }
   }
-  } else if (warp < kEpiWarp0 + 4) {
-    if (kNF4) regs_inc<136>();
-    // ------------------------------------------------------------ epilogue (4 warps)
-    // Output chunks of 128 bytes per row (64 bf16 or 32 fp32 columns) are staged in two
+  } else if (warp < kDeqWarp0) {
+    if (kNF4) regs_inc<104>();
+    // ------------------------------------------------------------ epilogue
+    // Output chunks of 128 bytes per row (64 bf16 or 32 fp32 columns) are staged in
     // 128-byte-swizzled shared buffers and written by TMA bulk stores (evict-first in L2);
-    // a partial chunk at the end of a column group is written with plain stores.  Every
-    // wait outcome is OR-reduced over the four warps so that they always leave together
-    // and never strand each other at a named barrier.
+    // a partial chunk at the end of a column group is written with plain stores.  bf16 W:
+    // one warpgroup, two staging buffers used in turn.  4-bit W: warpgroup eg drains M
+    // half eg of a tile through its own buffer, the other half at the same time (the tile
+    // holds all of tensor memory, so the MMAs wait for both); rank items are read by
+    // warpgroup 0.  Every wait outcome is OR-reduced over a warpgroup so that its warps
+    // always leave together and never strand each other at a named barrier.
+    const int eg = (warp - kEpiWarp0) >> 2;  // epilogue warpgroup
+    const uint32_t bar_main = 1 + 2 * eg, bar_any = 2 + 2 * eg;
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
     const int row_in_cta = q * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t stg_addr = smem_u32(stg);
-    const bool elected = threadIdx.x == kEpiWarp0 * 32;
+    const bool elected = threadIdx.x == (kEpiWarp0 + 4 * eg) * 32;
+    const int h_begin = kNF4 ? eg : 0, h_end = kNF4 ? eg + 1 : kMH;   // M halves drained here
+    // staging buffer of chunk sidx, and the wait before reusing it
+    auto stg_index = [&](uint32_t sidx) -> int { return kNF4 ? eg : static_cast<int>(sidx & 1); };
+    auto stg_free = [&](uint32_t sidx) {
+      if (kNF4) {
+        if (sidx >= 1 && elected) bulk_wait_read_0();
+      } else if (sidx >= 2 && elected) {
+        bulk_wait_read_le1();
+      }
+    };
     const uint32_t acc_empty_l[2] = {mapa_shared(smem_u32(&acc_empty[0]), 0),
                                      mapa_shared(smem_u32(&acc_empty[1]), 0)};
     const uint64_t stream_out = l2_evict_first();   // Y is written once: keep X and W in L2
@@ -495,11 +511,23 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     Item it;
     while (next_item(iter, p, pair, npairs, it)) {
       const int b = kNF4 ? 0 : (count & 1);
+      if (it.rank && eg == 1) {
+        // 4-bit W: warpgroup 1 has no rows of the rank item to read; it only counts the
+        // item off the accumulator buffer, after the MMAs filled it
+        const bool okw = mbar_wait_cluster(&acc_full[b], nuse[b] & 1, abort_flag, tmo, status);
+        if (named_bar_any(!okw, bar_any, 128)) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_l[b]);
+        ++nuse[b];
+        ++count;
+        continue;
+      }
       if (it.rank) {
         // s X A^T of every adapter -> bf16 H~ rows of this block in global memory (and
         // the fp32 values in h_out when asked), then the block's flag
         const bool okw = mbar_wait_cluster(&acc_full[b], nuse[b] & 1, abort_flag, tmo, status);
-        if (named_bar_any(!okw, 2, 128)) break;
+        if (named_bar_any(!okw, bar_any, 128)) break;
         tc_fence_after();
         const uint32_t h_t = tmem + b * kBN;
         const int row = it.m * kPairM + static_cast<int>(cta) * kBM + row_in_cta;
@@ -578,7 +606,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         // H~ rows visible to the TMA loads of other pairs: every thread orders its stores
         // for the async proxy, the barrier gathers them, and one release counts this CTA in
         fence_proxy_async_global();
-        named_bar_sync(1, 128);
+        named_bar_sync(bar_main, 128);
         if (elected) red_release_gpu_add(p.flags + it.m, 1u);
         ++nuse[b];
         ++count;
@@ -589,7 +617,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       const bool any_mma = p.has_base || a1 > a0;
       if (any_mma) {
         const bool ok = mbar_wait_cluster(&acc_full[b], nuse[b] & 1, abort_flag, tmo, status);
-        if (named_bar_any(!ok, 2, 128)) break;
+        if (named_bar_any(!ok, bar_any, 128)) break;
         tc_fence_after();
       }
       if (p.swiglu) {
@@ -600,7 +628,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         const int ncol = min(128, p.out_g - t.j * 128);
         const int nch = (ncol + 63) / 64;
 #pragma unroll 1
-        for (int h = 0; h < kMH; ++h) {
+        for (int h = h_begin; h < h_end; ++h) {
           const int row0 = t.m * (kPairM * kMH) + h * kPairM + static_cast<int>(cta) * kBM;
           const int row = row0 + row_in_cta;
           const bool row_ok = row < p.T;
@@ -610,26 +638,27 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
             const int cig = t.j * 128 + c * 64;            // first h column of the chunk
             const int ncols = min(64, p.out_g - cig);
             const bool full_chunk = ncols == 64;
-            const uint32_t buf = stg_addr + (sidx & 1) * kStgBytes;
+            const uint32_t buf = stg_addr + stg_index(sidx) * kStgBytes;
             if (full_chunk) {
-              if (sidx >= 2 && elected) bulk_wait_read_le1();
-              named_bar_sync(1, 128);
+              stg_free(sidx);
+              named_bar_sync(bar_main, 128);
             }
+            // 16 columns at a time: e and g under one TMEM wait
 #pragma unroll 1
-            for (int sub = 0; sub < 2; ++sub) {
-              const int c0 = c * 64 + sub * 32;            // column within the tile's 128
-              uint32_t re[32], rg[32];
-              tmem_ld32x2(acc_t + lane_base + c0, re, acc_t + lane_base + 128 + c0, rg);
-              if (h == kMH - 1 && c == nch - 1 && sub == 1) {
+            for (int sub = 0; sub < 4; ++sub) {
+              const int c0 = c * 64 + sub * 16;            // column within the tile's 128
+              uint32_t re[16], rg[16];
+              tmem_ld16x2(acc_t + lane_base + c0, re, acc_t + lane_base + 128 + c0, rg);
+              if (h == h_end - 1 && c == nch - 1 && sub == 3) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(acc_empty_l[b]);
               }
-              const int nc = min(32, ncols - sub * 32);
-              const int col = cig + sub * 32;              // first column of the sub-chunk
-              uint32_t eb[16], gb[16], hb[16];
+              const int nc = min(16, ncols - sub * 16);
+              const int col = cig + sub * 16;              // first column of the sub-chunk
+              uint32_t eb[8], gb[8], hb[8];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
+              for (int i = 0; i < 8; ++i) {
                 float e0 = u2f(re[2 * i]), e1 = u2f(re[2 * i + 1]);
                 float g0 = u2f(rg[2 * i]), g1 = u2f(rg[2 * i + 1]);
                 if (p.bias && 2 * i < nc) {
@@ -644,7 +673,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               if (p.eg && row_ok) {
                 uint16_t* pe = p.eg + static_cast<long long>(row) * p.ld_eg + col;
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+                for (int u = 0; u < 2; ++u)
                   if (u * 8 < nc) {
                     st_global_v4_hint(pe + u * 8, eb[4 * u], eb[4 * u + 1], eb[4 * u + 2], eb[4 * u + 3], stream_out);
                     st_global_v4_hint(pe + p.out_g + u * 8, gb[4 * u], gb[4 * u + 1], gb[4 * u + 2], gb[4 * u + 3],
@@ -654,22 +683,22 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               if (full_chunk) {
                 const uint32_t rowb = buf + row_in_cta * 128;
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                  st_shared_v4(rowb + (((sub * 4 + u) ^ (row_in_cta & 7)) * 16), hb[4 * u], hb[4 * u + 1],
+                for (int u = 0; u < 2; ++u)
+                  st_shared_v4(rowb + (((sub * 2 + u) ^ (row_in_cta & 7)) * 16), hb[4 * u], hb[4 * u + 1],
                                hb[4 * u + 2], hb[4 * u + 3]);
               } else if (row_ok) {
                 uint16_t* y = static_cast<uint16_t*>(p.Y) + static_cast<long long>(row) * p.ldy + col;
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+                for (int u = 0; u < 2; ++u)
                   if (u * 8 < nc)
                     st_global_v4_hint(y + u * 8, hb[4 * u], hb[4 * u + 1], hb[4 * u + 2], hb[4 * u + 3], stream_out);
               }
             }
             if (full_chunk) {
               fence_proxy_async_smem();
-              named_bar_sync(1, 128);
+              named_bar_sync(bar_main, 128);
               if (elected && row0 < p.T) {
-                tma_store_2d_hint(&maps.y, cig, row0, stg + (sidx & 1) * kStgBytes, stream_out);
+                tma_store_2d_hint(&maps.y, cig, row0, stg + stg_index(sidx) * kStgBytes, stream_out);
                 bulk_commit();
               }
               ++sidx;
@@ -684,7 +713,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       // valid chunks of this tile (the last tile of a group may be partial)
       const int nchunk = min(kBN / cw, (p.out_g - t.j * kBN + cw - 1) / cw);
 #pragma unroll 1
-      for (int h = 0; h < kMH; ++h) {
+      for (int h = h_begin; h < h_end; ++h) {
       const int row0 = t.m * (kPairM * kMH) + h * kPairM + static_cast<int>(cta) * kBM;
       const int row = row0 + row_in_cta;
       const bool row_ok = row < p.T;
@@ -695,11 +724,11 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         const int ncols = min(cw, p.out_g - cig);           // uniform across the warps
         const int gcol = t.g * p.out_g + cig;
         const bool full_chunk = ncols == cw;
-        const uint32_t buf = stg_addr + (sidx & 1) * kStgBytes;
+        const uint32_t buf = stg_addr + stg_index(sidx) * kStgBytes;
         if (full_chunk) {
-          // the staging buffer is free once the bulk store two chunks back has read it
-          if (sidx >= 2 && elected) bulk_wait_read_le1();
-          named_bar_sync(1, 128);
+          // the staging buffer is free once the bulk store that last used it has read it
+          stg_free(sidx);
+          named_bar_sync(bar_main, 128);
         }
         // 32 columns at a time: TMEM -> registers -> bias / FP32 adapters -> staging
 #pragma unroll 1
@@ -711,7 +740,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
             tmem_ld32(acc_t + lane_base + c * cw + c0, r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = u2f(r[i]);
-            if (h == kMH - 1 && c == nchunk - 1 && sub == cw / 32 - 1) {
+            if (h == h_end - 1 && c == nchunk - 1 && sub == cw / 32 - 1) {
               // the accumulator is fully in registers: hand it back to the MMA
               tc_fence_before();
               __syncwarp();
@@ -869,9 +898,9 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         }
         if (full_chunk) {
           fence_proxy_async_smem();
-          named_bar_sync(1, 128);
+          named_bar_sync(bar_main, 128);
           if (elected && row0 < p.T) {                     // no store of rows past the end
-            tma_store_2d_hint(&maps.y, gcol, row0, stg + (sidx & 1) * kStgBytes, stream_out);
+            tma_store_2d_hint(&maps.y, gcol, row0, stg + stg_index(sidx) * kStgBytes, stream_out);
             bulk_commit();
           }
           ++sidx;
@@ -887,22 +916,19 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
   } else if (kNF4) {
     regs_dec<72>();
     // ------------------------------------------------------------ 4-bit dequantisation
-    // Two groups of 256 threads take alternate base K steps (the CTA's running count of
-    // them).  Thread d of a group owns row d/2 of this CTA's 128 weight rows and half (32
-    // elements) of the K step.  For every (row, K step) -- one 64-element absmax block --
-    // it builds the 16 bf16 values bf16(fl32(level[i]) * absmax) in registers, split into
-    // low-byte and high-byte planes, and looks its codes up four at a time with byte
-    // permutes; the result goes to the stage's W slot in the 128-byte swizzle K-major
-    // layout.  The codes come from their own ring (loaded ahead), so a step waits only for
+    // Three groups of 128 threads take every third base K step (the CTA's running count
+    // of them).  Thread d of a group owns row d of this CTA's 128 weight rows: for every
+    // (row, K step) -- one 64-element absmax block -- it builds the 16 bf16 values
+    // bf16(fl32(level[i]) * absmax) in registers, split into low-byte and high-byte planes,
+    // and looks its 64 codes up four at a time with byte permutes; the result goes to the
+    // stage's W slot in the 128-byte swizzle K-major layout.  The codes come from their own ring (loaded ahead), so a step waits only for
     // its slot: free once the MMAs released the stage's previous use (empty).  Every warp
     // waits on every use of every stage (so that no parity wait can pass a phase that has
     // not completed yet) and then arrives on the stage's wfull, after its tile if the use
-    // is one of its group's K steps; the MMA waits for all 32 arrivals of every use, so
+    // is one of its group's K steps; the MMA waits for all 24 arrivals of every use, so
     // that no warp can fall two phases behind either.
-    const int group = (threadIdx.x - 256) >> 8;
-    const int d = (threadIdx.x - 256) & 255;
-    const int r = d >> 1;
-    const int hh = d & 1;
+    const int group = (threadIdx.x - kDeqWarp0 * 32) >> 7;
+    const int r = (threadIdx.x - kDeqWarp0 * 32) & 127;
     uint32_t kc = 0;                                  // base K steps seen by this CTA
     const uint32_t wfull_l0 = mapa_shared(smem_u32(&wfull[0]), 0);   // leader's barriers
     float lv[16];
@@ -933,7 +959,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       const bool wrow_ok = wrow < p.N;
       const float* am_row = p.absmax + static_cast<long long>(wrow_ok ? wrow : 0) * kb64;
       for (int kb = 0; kb < p.k_blocks && ok; ++kb, ++kc) {
-        if (static_cast<int>(kc & 1u) != group) {       // the other group's K step
+        if (static_cast<int>(kc % 3u) != group) {       // another group's K step
           pass();
           continue;
         }
@@ -945,7 +971,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         // releases the tile to the peer CTA) or, for K % 256 != 0, straight from memory
         const float am = p.am_tma ? reinterpret_cast<const float*>(raw + kRawBytes)[r * 4 + (kb & 3)]
                                   : (wrow_ok ? __ldg(am_row + kb) : 0.f);
-        nf4_dequant_half_row(raw + r * 32 + hh * 16, am, lv, smem_u32(sbase + stage * SB + kXBytes), r, hh);
+        nf4_dequant_row(raw + r * 32, am, lv, smem_u32(sbase + stage * SB + kXBytes), r);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
