@@ -146,7 +146,7 @@ int launch_swiglu_bwd(const SwigluBwdParams& q, cudaStream_t stream);
 // the splits, forms H~ = bf16(s X A^T), adds the bias and H~ B^T and rounds once.
 constexpr int kSkinnyMaxT = 64;
 constexpr int kSkinnyThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kSkinnyThreadsNF4 = 704;    // + warps 6..21 dequantisation (two groups of 8)
+constexpr int kSkinnyThreadsNF4 = 704;    // + warps 6..21 dequantisation (four groups of 4)
 constexpr int kSkinnyXBytes = kSkinnyMaxT * 128;   // X rows of a stage (64 rows x 64 K bf16)
 
 struct SkinnyParams {

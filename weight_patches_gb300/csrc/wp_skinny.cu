@@ -14,8 +14,8 @@
 // range); K is split so that the units fill the machine.  Per CTA: warp 0 issues the TMA
 // loads, warp 1 the single-CTA MMAs (two 64-column accumulators in tensor memory, so the
 // epilogue of one unit overlaps the next), warps 2..5 write fp32 partial sums, and with a
-// 4-bit weight warps 6..21 dequantise the tiles in shared memory, two groups of eight
-// taking alternate K steps (as the large-T kernel does).  The second kernel, one block per (token, 256 output columns), sums the K splits
+// 4-bit weight warps 6..21 dequantise the tiles in shared memory, four groups of four
+// taking every fourth K step, a thread per weight row (as the large-T kernel does).  The second kernel, one block per (token, 256 output columns), sums the K splits
 // in a fixed order, forms the token's H~ = bf16(s X A^T), adds the bias and H~ B^T in
 // fp32 and rounds once.
 #include <cuda.h>
@@ -241,14 +241,12 @@ __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
     }
   } else if (kNF4) {
     // ------------------------------------------------------------ 4-bit dequantisation
-    // two groups of 256 threads take alternate K steps of the weight blocks; thread d of a
-    // group owns row d/2 of the block and half (32 elements) of the K step.  Every warp
-    // waits on every stage use and arrives on its wfull, after its tile if the use is one
-    // of its group's, so that no parity wait can pass or fall behind a phase
-    const int group = (threadIdx.x - kSkinnyThreads) >> 8;
-    const int d = (threadIdx.x - kSkinnyThreads) & 255;
-    const int r = d >> 1;
-    const int hh = d & 1;
+    // four groups of 128 threads take every fourth K step of the weight blocks; thread r
+    // of a group owns row r of the block (one 64-element absmax block per K step).  Every
+    // warp waits on every stage use and arrives on its wfull, after its tile if the use is
+    // one of its group's, so that no parity wait can pass or fall behind a phase
+    const int group = (threadIdx.x - kSkinnyThreads) >> 7;
+    const int r = (threadIdx.x - kSkinnyThreads) & 127;
     uint32_t kc = 0;                                 // weight-block K steps seen
     float lv[16];
 #pragma unroll
@@ -264,13 +262,13 @@ __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
       for (int kb = t.kb0; kb < t.kb1; ++kb) {
         ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_flag, tmo, status));
         if (!ok) break;
-        const bool mine = !t.a_blk && static_cast<int>(kc++ & 1u) == group;
+        const bool mine = !t.a_blk && static_cast<int>(kc++ & 3u) == group;
         if (mine) {
           uint8_t* st = sbase + stage * SB;
           const uint8_t* raw = st + kWTileBytes + kSkinnyXBytes;
           const float am = p.am_tma ? reinterpret_cast<const float*>(raw + kRawBytes)[r * 4 + (kb & 3)]
                                     : (wrow_ok ? __ldg(p.absmax + static_cast<long long>(wrow) * kb64 + kb) : 0.f);
-          nf4_dequant_half_row(raw + r * 32 + hh * 16, am, lv, smem_u32(st), r, hh);
+          nf4_dequant_row(raw + r * 32, am, lv, smem_u32(st), r);
           fence_proxy_async_smem();
         }
         __syncwarp();
