@@ -141,6 +141,7 @@ def run_fused(args):
     torch.cuda.set_device(dev)
 
     import weight_patches_gb300 as wpg
+    from weight_patches_gb300 import data_parallel as wdp
     import workloads
 
     lin = workloads.config1("full")
@@ -176,9 +177,7 @@ def run_fused(args):
         barrier()
         ms = e0.elapsed_time(e1)
         if ws > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+            ms = wdp.max_over_ranks(ms, device=dev)      # the whole job waits for its slowest rank
         return ms
 
     vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
