@@ -8,8 +8,8 @@
 // round-to-nearest float32 operations (explicit __fmul_rn / __fadd_rn, so the
 // compiler cannot contract them into an FMA) and the cast back to bf16 is
 // round-to-nearest-even, which makes the result bit-exact against the float32
-// definition.  The kernel is HBM-bound: 16-byte vector loads and stores, a grid of a
-// few CTAs per SM striding over the tensor.
+// definition.  The kernel is HBM-bound: 16-byte vector loads and stores, four of each in
+// flight per thread, a grid of a few CTAs per SM striding over the tensor.
 #include <cuda_runtime.h>
 
 #include "wp_internal.h"
@@ -36,27 +36,43 @@ __device__ __forceinline__ float combine(float p, float d, float k, int kind) {
 
 }  // namespace
 
-// bf16 parameter, bf16 payload, 8 elements (16 bytes) per thread per step.
+__device__ __forceinline__ uint4 patch8(uint4 d, uint4 pv, int kind, float k) {
+  const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
+  const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float d_lo = __uint_as_float(dw[w] << 16), d_hi = __uint_as_float(dw[w] & 0xFFFF0000u);
+    const float p_lo = __uint_as_float(pw[w] << 16), p_hi = __uint_as_float(pw[w] & 0xFFFF0000u);
+    const uint16_t lo = to_bf16(combine(p_lo, d_lo, k, kind));
+    const uint16_t hi = to_bf16(combine(p_hi, d_hi, k, kind));
+    out[w] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// bf16 parameter, bf16 payload, 8 elements (16 bytes) per vector; each thread keeps four
+// vectors of each operand in flight (their loads issued before any arithmetic).
 __global__ void __launch_bounds__(256) dense_patch_bf16_vec(uint16_t* __restrict__ param,
                                                             const uint16_t* __restrict__ payload,
                                                             long long n8, int kind, float k) {
   const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
-    const uint4 d = reinterpret_cast<const uint4*>(payload)[i];
-    uint4 pv = make_uint4(0, 0, 0, 0);
-    if (kind == WP_PATCH_ADD) pv = reinterpret_cast<const uint4*>(param)[i];
-    const uint32_t dw[4] = {d.x, d.y, d.z, d.w};
-    const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
-    uint32_t out[4];
+  const uint4* src = reinterpret_cast<const uint4*>(payload);
+  uint4* dst = reinterpret_cast<uint4*>(param);
+  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n8; i += 4 * stride) {
+    uint4 d[4], pv[4];
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float d_lo = __uint_as_float(dw[w] << 16), d_hi = __uint_as_float(dw[w] & 0xFFFF0000u);
-      const float p_lo = __uint_as_float(pw[w] << 16), p_hi = __uint_as_float(pw[w] & 0xFFFF0000u);
-      const uint16_t lo = to_bf16(combine(p_lo, d_lo, k, kind));
-      const uint16_t hi = to_bf16(combine(p_hi, d_hi, k, kind));
-      out[w] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    for (int u = 0; u < 4; ++u) {
+      d[u] = src[i + u * stride];
+      pv[u] = kind == WP_PATCH_ADD ? dst[i + u * stride] : make_uint4(0, 0, 0, 0);
     }
-    reinterpret_cast<uint4*>(param)[i] = make_uint4(out[0], out[1], out[2], out[3]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) dst[i + u * stride] = patch8(d[u], pv[u], kind, k);
+  }
+  for (; i < n8; i += stride) {
+    const uint4 pv = kind == WP_PATCH_ADD ? dst[i] : make_uint4(0, 0, 0, 0);
+    dst[i] = patch8(src[i], pv, kind, k);
   }
 }
 
