@@ -71,7 +71,8 @@ def _free_port():
 
 def test_two_gloo_ranks_match_the_whole_batch():
     world = 2
-    with mp.Manager() as m:
+    # every process here starts by spawn (no fork after a CUDA context may exist)
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.spawn(_worker, args=(world, _free_port(), results), nprocs=world, join=True)
         res = dict(results)

@@ -665,7 +665,22 @@ struct BwdLayout {
   int r8[kMaxGroups];
   int roff[kMaxGroups];
   int R;
+  // dA / dB on the tensor cores (when the pieces fit N = 256): the bf16 pieces of H and of
+  // s G [T, tokN], and the token-split partial sums
+  bool tok;
+  int tokN, R16, roff16[kMaxGroups], splits_a, splits_b;
+  size_t hp, gp, tpart;
 };
+
+// Token splits of a contraction with m_tiles 256-row blocks over k_blocks 64-token steps: about
+// one unit per SM, at least 8 steps per unit.
+int tok_splits(int m_tiles, int k_blocks) {
+  const int sms = device_sm_count();
+  int s = (sms + m_tiles - 1) / m_tiles;
+  const int cap = std::max(1, k_blocks / 8);
+  if (s > cap) s = cap;
+  return s < 1 ? 1 : s;
+}
 
 bool bwd_layout(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int G, BwdLayout* L) {
   if (!X || !W || !ad || G < 1 || G > kMaxGroups) return false;
@@ -705,6 +720,25 @@ bool bwd_layout(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int G, B
   }
   L->part = off;
   off += round256(max_part * 4);
+  L->R16 = 0;
+  for (int g = 0; g < G; ++g) {
+    L->roff16[g] = L->R16;
+    L->R16 += static_cast<int>((ad[g].A.rows + 15) / 16 * 16);
+  }
+  L->tok = 2 * L->R16 <= 256 && K % 8 == 0 && Ntot % 8 == 0;
+  if (L->tok) {
+    L->tokN = 2 * L->R16 <= 128 ? 128 : 256;
+    const int kbt = static_cast<int>((T + 63) / 64);
+    L->splits_a = tok_splits(static_cast<int>((K + 255) / 256), kbt);
+    L->splits_b = tok_splits(static_cast<int>((Ntot + 255) / 256), kbt);
+    L->hp = off;
+    off += round256(T * L->tokN * 2);
+    L->gp = off;
+    off += round256(T * L->tokN * 2);
+    L->tpart = off;
+    off += round256(std::max(static_cast<size_t>(L->splits_a) * K, static_cast<size_t>(L->splits_b) * Ntot) *
+                    L->tokN * 4);
+  }
   // workspace of the forward call that computes dX: X := dY [T, Ntot], W := W^T, adapter g
   // A := B_g^T padded to [r_g, Ntot] (bf16), B := A_g^T [K, r_g]
   {
@@ -847,7 +881,76 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
     if (rc != WP_OK) return rc;
   }
 
-  // 5. dA_g = (s_g G_g)^T X  and  dB_g = s_g dY_g^T H_g  (exact zeros when s_g == 0)
+  // 5. dA_g = (s_g G_g)^T X  and  dB_g = s_g dY_g^T H_g  (exact zeros when s_g == 0): on the
+  //    tensor cores as token contractions with the fp32 H and s G as two bf16 pieces each,
+  //    or, when the pieces do not fit, by the split-T FFMA reduction below
+  if (L.tok) {
+    bool any = false;
+    for (int g = 0; g < G; ++g) any = any || s_of[g] != 0.0f;
+    TokPieceMap pm{};
+    pm.G = G; pm.R16 = L.R16;
+    for (int g = 0; g < G; ++g) {
+      pm.roff16[g] = L.roff16[g]; pm.off[g] = L.roff[g]; pm.r[g] = static_cast<int>(ad[g].A.rows);
+    }
+    uint16_t* Hp = reinterpret_cast<uint16_t*>(ws + L.hp);
+    uint16_t* Gp = reinterpret_cast<uint16_t*>(ws + L.gp);
+    float* tpart = reinterpret_cast<float*>(ws + L.tpart);
+    const int N = L.tokN;
+    const int Ti = static_cast<int>(T);
+    if (any) {
+      rc = launch_pieces(H, L.R, Ti, N, pm, Hp, stream);
+      if (rc == WP_OK) rc = launch_pieces(Gs, L.R, Ti, N, pm, Gp, stream);
+      if (rc != WP_OK) return rc;
+    }
+    TokGemmParams tp{};
+    tp.T = Ti; tp.N = N; tp.k_blocks = (Ti + 63) / 64;
+    tp.part = tpart;
+    tp.status = tc_status_ptr();
+    tp.timeout_ns = 2000000000ull;
+    if (!tp.status) return record_cuda();
+    const size_t sb = 2 * 64 * 128 + static_cast<size_t>(N) / 2 * 128;
+    tp.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - 1024 - 256) / sb));
+    const size_t smem = 1024 + tp.stages * sb + 256;
+    const int max_pairs = tokgemm_max_pairs(smem);
+    if (max_pairs <= 0) return WP_ERR_CUDA;
+    // (A, M, splits, then per group: finish into dB_g rows or dA_g transposed)
+    for (int pass = 0; pass < 2 && any; ++pass) {
+      const bool db = pass == 0;
+      TokGemmMaps tm;
+      std::memset(&tm, 0, sizeof(tm));
+      const long long M = db ? Ntot : K;
+      tp.M = static_cast<int>(M);
+      tp.m_tiles = static_cast<int>((M + 255) / 256);
+      tp.splits = db ? L.splits_b : L.splits_a;
+      tp.kb_per_split = (tp.k_blocks + tp.splits - 1) / tp.splits;
+      tp.splits = (tp.k_blocks + tp.kb_per_split - 1) / tp.kb_per_split;
+      tp.units = tp.m_tiles * tp.splits;
+      rc = db ? make_map_bf16(&tm.a, dY->data, Ntot, T, dY->ld, 64, 64)
+              : make_map_bf16(&tm.a, X->data, K, T, X->ld, 64, 64);
+      if (rc == WP_OK) rc = make_map_bf16(&tm.b, db ? Hp : Gp, N, T, N, 64, 64);
+      if (rc != WP_OK) return rc;
+      rc = launch_tokgemm(tm, tp, std::min(max_pairs, tp.units), smem, stream);
+      if (rc != WP_OK) return rc;
+      for (int g = 0; g < G; ++g) {
+        const int r = static_cast<int>(ad[g].A.rows);
+        if (s_of[g] == 0.0f) continue;
+        rc = db ? launch_tok_finish(tpart, tp.M, N, tp.splits, L.R16, L.roff16[g], r, static_cast<int>(g * og),
+                                    static_cast<int>(og), s_of[g], static_cast<float*>(dB[g].data), dB[g].ld,
+                                    false, stream)
+                : launch_tok_finish(tpart, tp.M, N, tp.splits, L.R16, L.roff16[g], r, 0, static_cast<int>(K), 1.0f,
+                                    static_cast<float*>(dA[g].data), dA[g].ld, true, stream);
+        if (rc != WP_OK) return rc;
+      }
+    }
+    for (int g = 0; g < G; ++g) {
+      if (s_of[g] != 0.0f) continue;
+      for (const wp_out* o : {&dA[g], &dB[g]}) {
+        cudaError_t e = cudaMemset2DAsync(o->data, o->ld * 4, 0, o->cols * 4, o->rows, stream);
+        if (e != cudaSuccess) { set_last_cuda_error(e); return WP_ERR_CUDA; }
+      }
+    }
+    return WP_OK;
+  }
   for (int g = 0; g < G; ++g) {
     const int r = static_cast<int>(ad[g].A.rows);
     if (s_of[g] == 0.0f) {

@@ -267,6 +267,32 @@ int launch_rank_pack(const PackParams& p, cudaStream_t stream);
 struct NF4Table {
   float level[16];
 };
+// Token contractions for the backward's dA / dB on the tensor cores (wp_tokgemm.cu):
+// part[split][m][n] = sum over the split's tokens t of A[t, m] B[t, n]
+struct TokGemmParams {
+  int T, M, N;                 // tokens, rows of D (A's columns), columns (128 or 256)
+  int m_tiles, splits, kb_per_split, k_blocks, units;
+  float* part;                 // [splits][M][N] fp32
+  int stages;
+  int* status;
+  unsigned long long timeout_ns;
+};
+struct TokGemmMaps {
+  CUtensorMap a, b;            // A [T, M], B [T, N]: boxes of 64 tokens x 64 columns, 128-byte swizzle
+};
+// column map of the rank-wide operand's bf16 pieces (see launch_pieces)
+struct TokPieceMap {
+  int G, R16;
+  int roff16[kMaxGroups], off[kMaxGroups], r[kMaxGroups];
+};
+int tokgemm_max_pairs(size_t smem_bytes);
+int launch_tokgemm(const TokGemmMaps& maps, const TokGemmParams& p, int pairs, size_t smem_bytes,
+                   cudaStream_t stream);
+int launch_pieces(const float* src, long long ld, int T, int N, const TokPieceMap& pm, uint16_t* dst,
+                  cudaStream_t stream);
+int launch_tok_finish(const float* part, int M, int N, int splits, int R16, int roff16, int r, int row0, int rows,
+                      float scale, float* out, long long ldo, bool transposed, cudaStream_t stream);
+
 // LoRA merge into a 4-bit weight (wp_merge.cu): W_eff as fp32, and the requantisation
 int launch_nf4_to_f32(const void* codes, const float* absmax, long long numel, const NF4Table& tab, float* U,
                       cudaStream_t stream);
