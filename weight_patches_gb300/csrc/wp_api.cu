@@ -135,6 +135,7 @@ struct FwdPlan {
 struct SkinnyPlan {
   bool use = false;
   int Tp = 0, nbW = 0, nbA = 0, R16 = 0, splits = 1, kbps = 1, units = 0, k_blocks = 0;
+  int kkb = 1;                 // 64-wide K blocks per pipeline step
   long long N = 0;
   size_t part_bytes = 0;
 };
@@ -168,6 +169,9 @@ bool plan_skinny(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int n, 
   sp->nbA = (R16 + 127) / 128;
   const int rows = sp->nbW + sp->nbA;
   sp->k_blocks = static_cast<int>((K + kBK - 1) / kBK);
+  // a 4-bit weight goes two K blocks per step: half the hand-offs between the kernel's
+  // roles per byte of weight
+  sp->kkb = (W && W->dtype == WP_NF4) ? 2 : 1;
   const int grid = device_sm_count();
   double best = 1e30;
   for (int sp_try = 1; sp_try <= 8; ++sp_try) {
@@ -177,6 +181,7 @@ bool plan_skinny(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int n, 
     if (waste < best - 0.02) { best = waste; sp->splits = sp_try; }
   }
   sp->kbps = (sp->k_blocks + sp->splits - 1) / sp->splits;
+  sp->kbps = (sp->kbps + sp->kkb - 1) / sp->kkb * sp->kkb;
   sp->splits = (sp->k_blocks + sp->kbps - 1) / sp->kbps;
   sp->units = rows * sp->splits;
   sp->part_bytes = round256(static_cast<size_t>(sp->splits) * T * (N + R16) * 4);
@@ -282,21 +287,48 @@ int skinny_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, boo
   p.T = static_cast<int>(T); p.Tp = sp.Tp; p.K = static_cast<int>(K); p.k_blocks = sp.k_blocks;
   p.N = static_cast<int>(N);              // the A rows' partial sums start at column N
   p.nbW = sp.nbW; p.nbA = sp.nbA; p.R16 = sp.R16;
-  p.splits = sp.splits; p.kb_per_split = sp.kbps; p.units = sp.units;
+  p.splits = sp.splits; p.kb_per_split = sp.kbps; p.units = sp.units; p.kkb = sp.kkb;
   p.part = part; p.ldp = q.ldp;
   p.status = tc_status_ptr();
   p.timeout_ns = 2000000000ull;
   if (!p.status) return record_cuda();
-  p.stage_bytes = 16384 + kSkinnyXBytes + (nf4 ? kRawBytes + kAmBytes : 0);
-  p.stages = std::min<int>(kMaxStages, static_cast<int>((kSmemLimit - 1024 - 256) / p.stage_bytes));
-  const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + 256;
+  // barriers (3 per stage, 1 per code slot, 5 more), the TMEM address, the abort flag and
+  // the per-slot copy counts
+  const size_t bar_bytes = 1024;
+  size_t smem = 0;
+  if (nf4) {
+    // stage = [kkb W tiles | kkb boxes of Tp X rows]; one K block per step: 8 stages (two
+    // per dequantisation group) while the codes ring keeps at least 8 slots, else 4; two
+    // K blocks per step: 4 stages, and the block scales come from global memory when a ring
+    // of at least 4 slots has no room for them
+    const int kkb = sp.kkb;
+    p.stage_bytes = kkb * (kWTileBytesSkinny + sp.Tp * 128);
+    p.am_tma = (K % 256 == 0 && aligned16(W->absmax)) ? 1 : 0;
+    const size_t avail = kSmemLimit - 1024 - bar_bytes;
+    if (kkb == 2 && (avail - 4 * static_cast<size_t>(p.stage_bytes)) /
+                            (static_cast<size_t>(kkb) * kRawBytes + kAmBytes) < 4)
+      p.am_tma = 0;
+    const size_t slot = static_cast<size_t>(kkb) * kRawBytes + (p.am_tma ? kAmBytes : 0);
+    p.stages = 4;
+    if (kkb == 1 && (avail - 8 * static_cast<size_t>(p.stage_bytes)) / slot >= 8) p.stages = 8;
+    p.code_slots = static_cast<int>(
+        std::min<size_t>(kSkinnyCodeSlots, (avail - static_cast<size_t>(p.stages) * p.stage_bytes) / slot));
+    if (p.code_slots < p.stages) return WP_ERR_UNSUPPORTED;
+    smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + static_cast<size_t>(p.code_slots) * slot +
+           bar_bytes;
+  } else {
+    p.stage_bytes = kWTileBytesSkinny + kSkinnyXBytes;
+    p.stages = std::min<int>(kMaxStages, static_cast<int>((kSmemLimit - 1024 - bar_bytes) / p.stage_bytes));
+    p.code_slots = 0;
+    smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + bar_bytes;
+  }
+  if (smem > static_cast<size_t>(kSmemLimit)) return WP_ERR_UNSUPPORTED;
   int rc = make_map_bf16(&maps.x, X->data, K, T, X->ld, kBK, sp.Tp);
   if (rc != WP_OK) return rc;
   if (nf4) {
-    rc = make_map_u8(&maps.wq, W->data, K / 2, N, K / 2, kBK / 2, 128);
+    rc = make_map_u8(&maps.wq, W->data, K / 2, N, K / 2, sp.kkb * kBK / 2, 128);
     if (rc != WP_OK) return rc;
     p.absmax = W->absmax;
-    p.am_tma = (K % 256 == 0 && aligned16(W->absmax)) ? 1 : 0;
     if (p.am_tma) {
       rc = make_map(&maps.am, WP_FP32, W->absmax, K / 64, N, K / 64, 4, 128, /*swizzle=*/0);
       if (rc != WP_OK) return rc;

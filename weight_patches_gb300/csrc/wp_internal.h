@@ -148,6 +148,8 @@ constexpr int kSkinnyMaxT = 64;
 constexpr int kSkinnyThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kSkinnyThreadsNF4 = 704;    // + warps 6..21 dequantisation (four groups of 4)
 constexpr int kSkinnyXBytes = kSkinnyMaxT * 128;   // X rows of a stage (64 rows x 64 K bf16)
+constexpr int kWTileBytesSkinny = 128 * 64 * 2;   // 128 weight (or A) rows x 64 K, bf16
+constexpr int kSkinnyCodeSlots = 16;      // 4-bit W: most slots of the codes ring
 
 struct SkinnyParams {
   int T, Tp;                   // tokens and the MMA width (T rounded up to 16)
@@ -158,12 +160,15 @@ struct SkinnyParams {
   int n_ad;
   int a_off[kMaxAd + 1];       // a_off[n_ad] = R16
   int splits, kb_per_split, units;
+  int kkb;                     // 64-wide K blocks per step (1, or 2 with a 4-bit W); kb_per_split
+                               // is a multiple of it
   int am_tma;
   const float* absmax;
   float nf4_code[16];
   float* part;                 // [splits][T][ldp] fp32: W rows, then the A rows at N
   long long ldp;
-  int stages, stage_bytes;
+  int stages, stage_bytes;     // 4-bit W: 4 or 8 stages (stage s written by group s % 4)
+  int code_slots;              // 4-bit W: slots of the codes ring (0 for bf16)
   int* status;
   unsigned long long timeout_ns;
 };

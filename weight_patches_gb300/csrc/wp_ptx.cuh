@@ -47,11 +47,41 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity (no suspend, unlike try_wait).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// Wall-clock budget of a polling loop.  Reading %globaltimer costs far more than a
+// shared-memory poll (its value moves in 256 ns steps on these parts), so the clock is
+// read only on every 256th poll, and the budget counts from the first such read.
+struct SpinBudget {
+  uint64_t t0 = 0;
+  uint32_t n = 0;
+  __device__ __forceinline__ bool spent(uint64_t timeout_ns) {
+    if ((++n & 255u) != 0) return false;
+    const uint64_t now = globaltimer_ns();
+    if (n == 256u) {
+      t0 = now;
+      return false;
+    }
+    return now - t0 > timeout_ns;
+  }
+};
 
 // Bounded wait for the phase with the given parity.  Returns false when the wall-clock
 // budget runs out (then it raises the CTA's abort flag and records WP_ERR_TIMEOUT in
@@ -61,11 +91,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
                                           uint64_t timeout_ns, int* status) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t n = 0;
+  SpinBudget budget;
   while (!mbar_try_wait(a, parity)) {
     if (*abort_flag) return false;
-    if ((++n & 63u) == 0 && globaltimer_ns() - t0 > timeout_ns) {
+    if (budget.spent(timeout_ns)) {
       *abort_flag = 1;
       atomicExch(status, kErrTimeout);
       return false;
@@ -93,11 +122,10 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
                                                   int* status) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait_cluster(a, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t n = 0;
+  SpinBudget budget;
   while (!mbar_try_wait_cluster(a, parity)) {
     if (*abort_flag) return false;
-    if ((++n & 63u) == 0 && globaltimer_ns() - t0 > timeout_ns) {
+    if (budget.spent(timeout_ns)) {
       *abort_flag = 1;
       atomicExch(status, kErrTimeout);
       return false;
@@ -243,6 +271,20 @@ __device__ __forceinline__ bool named_bar_any(bool v, uint32_t id, uint32_t n) {
   return r != 0;
 }
 
+// Named barrier that also returns whether every participating thread passed `v` true.
+__device__ __forceinline__ bool named_bar_all(bool v, uint32_t id, uint32_t n) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
 // Make generic-proxy writes to shared memory visible to the async proxy (TMA, MMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -283,10 +325,10 @@ __device__ __forceinline__ bool flag_wait(const uint32_t* flag, uint32_t target,
                                           volatile int* abort_flag, uint64_t timeout_ns,
                                           int* status) {
   if (ld_acquire_gpu(flag) >= target) return true;
-  const uint64_t t0 = globaltimer_ns();
+  SpinBudget budget;
   while (ld_acquire_gpu(flag) < target) {
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > timeout_ns) {
+    if (budget.spent(timeout_ns)) {
       *abort_flag = 1;
       atomicExch(status, kErrTimeout);
       return false;

@@ -10,14 +10,19 @@
 // and the tokens, rounded up to 16, as its width; the A rows of every adapter, one
 // adapter after another at 16-aligned row offsets (16-row TMA boxes straight from each
 // adapter, zero past its rank), ride as extra row blocks, so X A^T comes out of the same
-// pass.  A unit of work is (128-row block, K
-// range); K is split so that the units fill the machine.  Per CTA: warp 0 issues the TMA
-// loads, warp 1 the single-CTA MMAs (two 64-column accumulators in tensor memory, so the
-// epilogue of one unit overlaps the next), warps 2..5 write fp32 partial sums, and with a
-// 4-bit weight warps 6..21 dequantise the tiles in shared memory, four groups of four
-// taking every fourth K step, a thread per weight row (as the large-T kernel does).  The second kernel, one block per (token, 256 output columns), sums the K splits
-// in a fixed order, forms the token's H~ = bf16(s X A^T), adds the bias and H~ B^T in
-// fp32 and rounds once.
+// pass.  A unit of work is (128-row block, K range); K is split so that the units fill
+// the machine.  Per CTA: warp 0 issues the TMA loads, warp 1 the single-CTA MMAs (two
+// 64-column accumulators in tensor memory, so the epilogue of one unit overlaps the
+// next), warps 2..5 write fp32 partial sums, and with a 4-bit weight warps 6..21
+// dequantise the tiles in shared memory: four groups of four warps, a thread per weight
+// row, each group owning the stages of every fourth step.  A 4-bit step covers two K
+// blocks: every hand-off between the roles (a barrier round trip of a few hundred cycles
+// on this part) then moves twice the weight.  The 4-bit codes travel in a ring of their
+// own that each group refills, as soon as it has read a slot, with the codes of the step
+// a ring's length ahead, so the weight stream never waits on the producer.  The second
+// kernel, one block per (16 tokens, 256 output columns), sums the K splits in a fixed
+// order, forms the tokens' H~ = bf16(s X A^T), adds the bias and H~ B^T in fp32 and
+// rounds once.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -46,6 +51,38 @@ __device__ __forceinline__ Unit unit_of(const SkinnyParams& p, int u) {
   return t;
 }
 
+// Walks the weight steps of a CTA in issue order (its weight units come before its units of
+// A rows, so the walk ends at the first A unit).
+struct WIter {
+  int u, kb, kb1, rb;
+  bool more;
+};
+
+__device__ __forceinline__ void witer_unit(const SkinnyParams& p, WIter& it) {
+  it.more = false;
+  if (it.u < p.units) {
+    const Unit t = unit_of(p, it.u);
+    it.more = !t.a_blk;
+    it.kb = t.kb0;
+    it.kb1 = t.kb1;
+    it.rb = t.rb;
+  }
+}
+
+__device__ __forceinline__ void witer_start(const SkinnyParams& p, WIter& it) {
+  it.u = blockIdx.x;
+  witer_unit(p, it);
+}
+
+__device__ __forceinline__ void witer_next(const SkinnyParams& p, WIter& it) {
+  if (!it.more) return;
+  it.kb += p.kkb;
+  if (it.kb >= it.kb1) {
+    it.u += gridDim.x;
+    witer_unit(p, it);
+  }
+}
+
 template <bool kNF4>
 __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
     skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constant__ SkinnyParams p) {
@@ -54,19 +91,32 @@ __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
   const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base_addr - raw_addr);
 
-  // stage: [W (or A) rows 16 KiB | X rows 8 KiB | 4-bit codes 4 KiB | block scales 2 KiB]
+  // A step covers kkb 64-wide K blocks (1, or 2 with a 4-bit W).  stage = [kkb W (or A)
+  // tiles of 16 KiB | kkb boxes of Tp X rows].  bf16 W: all of it comes by TMA.  4-bit W:
+  // the W tiles are written by the stage's dequantisation group (stage s belongs to group
+  // s % 4, S is 4 or 8), and the codes travel in a ring of slots [4-bit codes, kkb x 4 KiB |
+  // block scales 2 KiB] that the groups refill themselves, R weight steps ahead of the one
+  // they have just read.
   const int S = p.stages;
   const int SB = p.stage_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + S * SB);
-  uint64_t* full = bars;                  // [S] TMA bytes landed
+  const int kkb = kNF4 ? p.kkb : 1;
+  const int XB = p.Tp * 128;                    // one box of X rows
+  const int x_off = kkb * kWTileBytes;          // X boxes within a stage
+  const int CSB = kkb * kRawBytes + (p.am_tma ? kAmBytes : 0);   // one code slot
+  const int R = kNF4 ? p.code_slots : 1;
+  uint8_t* codes = sbase + S * SB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(codes + (kNF4 ? R * CSB : 0));
+  uint64_t* full = bars;                  // [S] TMA bytes landed: X, and W (bf16) or A rows
   uint64_t* empty = bars + S;             // [S] the MMAs are done with the stage
-  uint64_t* wfull = bars + 2 * S;         // [S] 4-bit W: every dequantisation warp is done
-                                          //     with this use (tile written if any)
-  uint64_t* acc_full = bars + 3 * S;      // [2] accumulator ready
+  uint64_t* wfull = bars + 2 * S;         // [S] 4-bit: the owning group has written the tile
+                                          //     (or has nothing to write) and seen `full`
+  uint64_t* code_full = bars + 3 * S;     // [R] 4-bit: codes (and scales) landed
+  uint64_t* acc_full = code_full + R;     // [2] accumulator ready
   uint64_t* acc_empty = acc_full + 2;     // [2] the epilogue has read it
   uint64_t* drain = acc_full + 4;         //     every MMA issued has finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* c_uses = tmem_slot + 2;       // [R] 4-bit: copies issued into each code slot
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -74,8 +124,13 @@ __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&wfull[s], 16);           // 16 dequantisation warps
+      mbar_init(&wfull[s], 4);            // the 4 warps of the stage's dequantisation group
     }
+    if (kNF4)
+      for (int c = 0; c < R; ++c) {
+        mbar_init(&code_full[c], 1);
+        c_uses[c] = 0;
+      }
     mbar_init(&acc_full[0], 1);
     mbar_init(&acc_full[1], 1);
     mbar_init(&acc_empty[0], 4);          // 4 epilogue warps
@@ -98,66 +153,88 @@ __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
   // whole of this grid (partial sums included)
   if (threadIdx.x == 0) grid_launch_dependents();
 
+  // the A rows of A block `a0`: the 16-row pieces of the adapters inside it (rows of the
+  // block that no adapter covers are never read by the epilogue)
+  auto a_block_bytes = [&](int a0) {
+    uint32_t bytes = 0;
+    for (int i = 0; i < p.n_ad; ++i) {
+      const int lo = max(a0, p.a_off[i]), hi = min(a0 + 128, p.a_off[i + 1]);
+      if (hi > lo) bytes += static_cast<uint32_t>(hi - lo) * 128;
+    }
+    return bytes;
+  };
+  auto load_a_block = [&](uint8_t* dst, int a0, int kb, uint64_t* bar, uint64_t hint) {
+    for (int i = 0; i < p.n_ad; ++i) {
+      const int lo = max(a0, p.a_off[i]), hi = min(a0 + 128, p.a_off[i + 1]);
+      for (int r0 = lo; r0 < hi; r0 += 16)
+        tma_load_2d_hint(dst + (r0 - a0) * 128, &maps.a[i], kb * kBK, r0 - p.a_off[i], bar, hint);
+    }
+  };
+  // bounded wait for the copies of a barrier's last armed phase (after an abort)
+  auto settle = [](uint64_t* bar, uint32_t uses) {
+    if (uses == 0) return;
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(a, (uses - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
+    }
+  };
+
+  // the codes (and block scales) of weight step (rb, kb) into code slot c
+  // (one box of kkb K blocks; the scale box of 4 blocks holds both of a 2-block step, which
+  // starts at an even block)
+  auto load_codes = [&](int c, int rb, int kb, uint64_t hint) {
+    uint8_t* cs = codes + c * CSB;
+    ++c_uses[c];
+    mbar_arrive_expect_tx(&code_full[c], kkb * kRawBytes + (p.am_tma ? kAmBytes : 0));
+    tma_load_2d_hint(cs, &maps.wq, kb * (kBK / 2), rb * 128, &code_full[c], hint);
+    if (p.am_tma) tma_load_2d_hint(cs + kkb * kRawBytes, &maps.am, kb & ~3, rb * 128, &code_full[c], hint);
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t keep = l2_evict_last();      // X and the A rows: read by every CTA
       const uint64_t once = l2_evict_first();     // the weight: read once
+      bool ok = true;
+      if (kNF4) {
+        // the first R weight steps' codes; the dequantisation groups issue the rest
+        WIter c;
+        witer_start(p, c);
+        for (int i = 0; i < R && c.more; ++i) {
+          load_codes(i, c.rb, c.kb, once);
+          witer_next(p, c);
+        }
+      }
       int stage = 0;
       uint32_t phase = 0;
-      int issued[kMaxStages];
+      uint32_t issued[kMaxStages];
       for (int s = 0; s < kMaxStages; ++s) issued[s] = 0;
-      bool ok = true;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
         const Unit t = unit_of(p, u);
-        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+        for (int kb = t.kb0; kb < t.kb1; kb += kkb) {
           if (!(ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, tmo, status))) break;
           uint8_t* st = sbase + stage * SB;
-          const bool codes = kNF4 && !t.a_blk;
-          // A block: the 16-row pieces of the adapters inside it (rows of the block that no
-          // adapter covers are never read by the epilogue)
           const int a0 = (t.rb - p.nbW) * 128;
-          uint32_t a_bytes = 0;
-          if (t.a_blk)
-            for (int i = 0; i < p.n_ad; ++i) {
-              const int lo = max(a0, p.a_off[i]), hi = min(a0 + 128, p.a_off[i + 1]);
-              if (hi > lo) a_bytes += static_cast<uint32_t>(hi - lo) * 128;
-            }
-          const uint32_t tx = static_cast<uint32_t>(p.Tp) * 128 +
-                              (codes ? kRawBytes + (p.am_tma ? kAmBytes : 0) : t.a_blk ? a_bytes : kWTileBytes);
+          // K blocks past K (the second block of a last 2-block step) read as zeros
+          const uint32_t tx = static_cast<uint32_t>(kkb) *
+                              (static_cast<uint32_t>(XB) +
+                               (t.a_blk ? a_block_bytes(a0) : kNF4 ? 0u : static_cast<uint32_t>(kWTileBytes)));
           mbar_arrive_expect_tx(&full[stage], tx);
-          tma_load_2d_hint(st + kWTileBytes, &maps.x, kb * kBK, 0, &full[stage], keep);
-          if (t.a_blk) {
-            for (int i = 0; i < p.n_ad; ++i) {
-              const int lo = max(a0, p.a_off[i]), hi = min(a0 + 128, p.a_off[i + 1]);
-              for (int r0 = lo; r0 < hi; r0 += 16)
-                tma_load_2d_hint(st + (r0 - a0) * 128, &maps.a[i], kb * kBK, r0 - p.a_off[i], &full[stage], keep);
-            }
-          } else if (codes) {
-            uint8_t* raw = st + kWTileBytes + kSkinnyXBytes;
-            tma_load_2d_hint(raw, &maps.wq, kb * (kBK / 2), t.rb * 128, &full[stage], once);
-            if (p.am_tma) tma_load_2d_hint(raw + kRawBytes, &maps.am, kb & ~3, t.rb * 128, &full[stage], once);
-          } else {
-            tma_load_2d_hint(st, &maps.w, kb * kBK, t.rb * 128, &full[stage], once);
+          for (int h = 0; h < kkb; ++h) {
+            tma_load_2d_hint(st + x_off + h * XB, &maps.x, (kb + h) * kBK, 0, &full[stage], keep);
+            if (t.a_blk) load_a_block(st + h * kWTileBytes, a0, kb + h, &full[stage], keep);
+            else if (!kNF4) tma_load_2d_hint(st + h * kWTileBytes, &maps.w, (kb + h) * kBK, t.rb * 128, &full[stage], once);
           }
           ++issued[stage];
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
-      if (!ok) {
-        // wait (bounded) for the copies in flight before the CTA exits
-        for (int s = 0; s < S; ++s) {
-          if (issued[s] == 0) continue;
-          const uint32_t a = smem_u32(&full[s]);
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(a, static_cast<uint32_t>((issued[s] - 1) & 1)) &&
-                 globaltimer_ns() - t0 < 100000000ull) {
-          }
-        }
-      }
+      if (!ok)
+        for (int s = 0; s < S; ++s) settle(&full[s], issued[s]);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // waits for the stage's TMA bytes and, with a 4-bit W, for its dequantisation group
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -171,16 +248,18 @@ __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
         const int b = count & 1;
         if (!(ok = mbar_wait(&acc_empty[b], (nuse[b] & 1) ^ 1, abort_flag, tmo, status))) break;
         tc_fence_after();
-        for (int kb = t.kb0; kb < t.kb1; ++kb) {
-          if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
+        for (int kb = t.kb0; kb < t.kb1; kb += kkb) {
           if (kNF4 && !(ok = mbar_wait(&wfull[stage], phase, abort_flag, tmo, status))) break;
+          if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
           tc_fence_after();
           const uint32_t st = stage_base + stage * SB;
-          const uint64_t ad = sw128_kmajor_desc(st);
-          const uint64_t bd = sw128_kmajor_desc(st + kWTileBytes);
+          for (int h = 0; h < kkb; ++h) {
+            const uint64_t ad = sw128_kmajor_desc(st + h * kWTileBytes);
+            const uint64_t bd = sw128_kmajor_desc(st + x_off + h * XB);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_bf16(tmem + b * 64, ad + 2 * kk, bd + 2 * kk, idesc, (kb > t.kb0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_bf16(tmem + b * 64, ad + 2 * kk, bd + 2 * kk, idesc, (kb > t.kb0 || h > 0 || kk > 0) ? 1u : 0u);
+          }
           mma_commit(&empty[stage]);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
@@ -241,45 +320,85 @@ __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
     }
   } else if (kNF4) {
     // ------------------------------------------------------------ 4-bit dequantisation
-    // four groups of 128 threads take every fourth K step of the weight blocks; thread r
-    // of a group owns row r of the block (one 64-element absmax block per K step).  Every
-    // warp waits on every stage use and arrives on its wfull, after its tile if the use is
-    // one of its group's, so that no parity wait can pass or fall behind a phase
+    // Four groups of 128 threads; step j belongs to group j % 4, and so do all the uses of
+    // its stage j % S (S is 4 or 8), so each group's waits see every phase of its stages'
+    // barriers.  Thread r of a group owns row r of the step: kkb 64-element blocks.  A
+    // weight step's codes sit in the ring slot of its weight-step index; once the whole
+    // group has read them, the group's elected thread refills the slot with the codes of
+    // the weight step R further on.  That slot's previous use is R >= S steps back, and the
+    // stage wait has already seen the MMAs of every step S back, so the parity wait on the
+    // slot cannot pass on a stale phase.  Lane 0 of each warp polls and the warp follows;
+    // every exit is decided by a vote of the whole group, so no warp can leave the others
+    // waiting at the group's named barrier.
     const int group = (threadIdx.x - kSkinnyThreads) >> 7;
     const int r = (threadIdx.x - kSkinnyThreads) & 127;
-    uint32_t kc = 0;                                 // weight-block K steps seen
+    const uint32_t gbar = 1u + static_cast<uint32_t>(group);      // named barrier of the group
     float lv[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) lv[i] = p.nf4_code[i];
     const int kb64 = p.K / 64;
-    int stage = 0;
-    uint32_t phase = 0;
+    const uint64_t once = l2_evict_first();
+    auto wait0 = [&](uint64_t* bar, uint32_t par) -> bool {
+      bool w = true;
+      if (lane == 0) w = mbar_wait(bar, par, abort_flag, tmo, status);
+      __syncwarp();
+      return __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+    };
+    uint32_t j = 0;                                  // steps seen
+    int s = 0;                                       // the next step's stage and its use parity
+    uint32_t spar = 0;
+    int cslot = 0;                                   // the next weight step's code slot and parity
+    uint32_t cpar = 0;
+    WIter ahead;                                     // the weight step R after the next one
+    witer_start(p, ahead);
+    for (int i = 0; i < R; ++i) witer_next(p, ahead);
     bool ok = true;
     for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
       const Unit t = unit_of(p, u);
       const int wrow = t.rb * 128 + r;
       const bool wrow_ok = !t.a_blk && wrow < p.N;
-      for (int kb = t.kb0; kb < t.kb1; ++kb) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_flag, tmo, status));
-        if (!ok) break;
-        const bool mine = !t.a_blk && static_cast<int>(kc++ & 3u) == group;
-        if (mine) {
-          uint8_t* st = sbase + stage * SB;
-          const uint8_t* raw = st + kWTileBytes + kSkinnyXBytes;
-          const float am = p.am_tma ? reinterpret_cast<const float*>(raw + kRawBytes)[r * 4 + (kb & 3)]
-                                    : (wrow_ok ? __ldg(p.absmax + static_cast<long long>(wrow) * kb64 + kb) : 0.f);
-          nf4_dequant_row(raw + r * 32, am, lv, smem_u32(st), r);
+      for (int kb = t.kb0; kb < t.kb1; kb += kkb) {
+        const int st = s;
+        const uint32_t st_par = spar;
+        const int slot = cslot;
+        const uint32_t slot_par = cpar;
+        const bool mine = static_cast<int>(j & 3u) == group;
+        ++j;
+        if (++s == S) { s = 0; spar ^= 1u; }
+        if (!t.a_blk && ++cslot == R) { cslot = 0; cpar ^= 1u; }
+        if (!mine) {
+          if (!t.a_blk) witer_next(p, ahead);
+          continue;
+        }
+        bool w = wait0(&empty[st], st_par ^ 1u);
+        if (!t.a_blk) w = w && wait0(&code_full[slot], slot_par);
+        if (!(ok = named_bar_all(w, gbar, 128))) break;
+        if (!t.a_blk) {
+          const uint8_t* cs = codes + slot * CSB;
+          const uint32_t tile = smem_u32(sbase + st * SB);
+          for (int h = 0; h < kkb; ++h) {
+            // a block past K (K blocks odd, last 2-block step) reads zero codes and scale
+            const int k = kb + h;
+            const float am = p.am_tma ? reinterpret_cast<const float*>(cs + kkb * kRawBytes)[r * 4 + (k & 3)]
+                                      : (wrow_ok && k < kb64 ? __ldg(p.absmax + static_cast<long long>(wrow) * kb64 + k) : 0.f);
+            nf4_dequant_row(cs + r * (32 * kkb) + h * 32, am, lv, tile + h * kWTileBytes, r);
+          }
           fence_proxy_async_smem();
+          named_bar_sync(gbar, 128);                 // the slot is read and the tiles written
+          if (r == 0 && ahead.more) load_codes(slot, ahead.rb, ahead.kb, once);
+          witer_next(p, ahead);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&wfull[stage]);
-        if (++stage == S) { stage = 0; phase ^= 1; }
+        if (lane == 0) mbar_arrive(&wfull[st]);
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  // after an abort: the last copy into each code slot may still be in flight
+  if (kNF4 && threadIdx.x == 0 && *abort_flag)
+    for (int c = 0; c < R; ++c) settle(&code_full[c], c_uses[c]);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 128);
