@@ -69,8 +69,10 @@ int make_map(CUtensorMap* m, int dtype, const void* ptr, long long inner, long l
 
 // 2-D byte tensor map (4-bit codes, two per byte) without swizzle: boxes of
 // {box_inner bytes, box_outer rows}, rows box_inner bytes apart in shared memory.
+// Byte tensor map; swizzle 32 or 64 stores each box row's 16-byte units swizzled like
+// the bf16 tiles (the 4-bit codes, so that a quarter-warp's rows read different banks).
 int make_map_u8(CUtensorMap* m, const void* ptr, long long inner_bytes, long long outer,
-                long long ld_bytes, int box_inner, int box_outer) {
+                long long ld_bytes, int box_inner, int box_outer, int swizzle = 0) {
   auto fn = encode_fn();
   if (!fn) {
     g_last_error = "cuTensorMapEncodeTiled unavailable";
@@ -81,7 +83,10 @@ int make_map_u8(CUtensorMap* m, const void* ptr, long long inner_bytes, long lon
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle == 64   ? CU_TENSOR_MAP_SWIZZLE_64B
+                  : swizzle == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                  : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char buf[96];
@@ -326,7 +331,7 @@ int skinny_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, boo
   int rc = make_map_bf16(&maps.x, X->data, K, T, X->ld, kBK, sp.Tp);
   if (rc != WP_OK) return rc;
   if (nf4) {
-    rc = make_map_u8(&maps.wq, W->data, K / 2, N, K / 2, sp.kkb * kBK / 2, 128);
+    rc = make_map_u8(&maps.wq, W->data, K / 2, N, K / 2, sp.kkb * kBK / 2, 128, sp.kkb * 32);
     if (rc != WP_OK) return rc;
     p.absmax = W->absmax;
     if (p.am_tma) {
@@ -632,7 +637,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   if (rc != WP_OK) return rc;
   if (nf4) {
     // codes: [N rows, K/2 bytes]; each CTA loads 128 rows x 32 bytes (64 elements) per K step
-    rc = make_map_u8(&maps.wq, W->data, K / 2, N, K / 2, kBK / 2, 128);
+    rc = make_map_u8(&maps.wq, W->data, K / 2, N, K / 2, kBK / 2, 128, 32);
     if (rc != WP_OK) return rc;
     p.absmax = W->absmax;
     // block scales [N, K/64] by TMA when a row of them is a multiple of 16 bytes

@@ -41,13 +41,15 @@ __device__ __forceinline__ void lookup4(uint32_t sel, uint32_t pick, const uint3
 }
 
 // All 64 elements of one block: row `r` of the tile, one table for the 64 codes.
-// `codes32` points at the row's 32 code bytes, `am` is the block's scale, `lv` the 16
-// levels, `tile` the shared-memory address of the tile (row r at r * 128 bytes, 16-byte
-// unit u stored at unit u ^ (r & 7): the 128-byte swizzle, K-major).  Rows r with bit 2
-// set read their second 16 code bytes first, so that the eight rows of a quarter-warp
-// load hit eight different bank groups.
-__device__ __forceinline__ void nf4_dequant_row(const uint8_t* codes32, float am, const float (&lv)[16],
-                                                uint32_t tile, int r) {
+// `row` points at the row's codes in shared memory as the copy engine swizzled them: the
+// block's two 16-byte halves are the row's 16-byte units unit0 and unit0 + 1, stored at
+// unit ^ swz (the 32-byte swizzle of 32-byte rows: swz = (r >> 2) & 1; the 64-byte swizzle
+// of 64-byte rows: swz = (r >> 1) & 3), which spreads the rows of a quarter-warp load over
+// eight bank groups.  `am` is the block's scale, `lv` the 16 levels, `tile` the shared-
+// memory address of the tile (row r at r * 128 bytes, 16-byte unit u stored at unit
+// u ^ (r & 7): the 128-byte swizzle, K-major).
+__device__ __forceinline__ void nf4_dequant_row(const uint8_t* row, int unit0, int swz, float am,
+                                                const float (&lv)[16], uint32_t tile, int r) {
   uint32_t e[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) e[k] = pack_bf16x2(lv[2 * k] * am, lv[2 * k + 1] * am);
@@ -58,11 +60,9 @@ __device__ __forceinline__ void nf4_dequant_row(const uint8_t* codes32, float am
     hi[j] = prmt(e[2 * j], e[2 * j + 1], 0x7531u);
   }
   const uint32_t dst = tile + r * 128;
-  const int hs = (r >> 2) & 1;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int half = i ^ hs;
-    const uint4 cw4 = *reinterpret_cast<const uint4*>(codes32 + half * 16);
+  for (int half = 0; half < 2; ++half) {
+    const uint4 cw4 = *reinterpret_cast<const uint4*>(row + (((unit0 + half) ^ swz) << 4));
     const uint32_t cwords[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {

@@ -381,7 +381,8 @@ __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
             const int k = kb + h;
             const float am = p.am_tma ? reinterpret_cast<const float*>(cs + kkb * kRawBytes)[r * 4 + (k & 3)]
                                       : (wrow_ok && k < kb64 ? __ldg(p.absmax + static_cast<long long>(wrow) * kb64 + k) : 0.f);
-            nf4_dequant_row(cs + r * (32 * kkb) + h * 32, am, lv, tile + h * kWTileBytes, r);
+            nf4_dequant_row(cs + r * (32 * kkb), 2 * h, kkb == 2 ? (r >> 1) & 3 : (r >> 2) & 1, am, lv,
+                            tile + h * kWTileBytes, r);
           }
           fence_proxy_async_smem();
           named_bar_sync(gbar, 128);                 // the slot is read and the tiles written

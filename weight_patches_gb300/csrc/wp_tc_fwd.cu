@@ -971,7 +971,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         // releases the tile to the peer CTA) or, for K % 256 != 0, straight from memory
         const float am = p.am_tma ? reinterpret_cast<const float*>(raw + kRawBytes)[r * 4 + (kb & 3)]
                                   : (wrow_ok ? __ldg(am_row + kb) : 0.f);
-        nf4_dequant_row(raw + r * 32, am, lv, smem_u32(sbase + stage * SB + kXBytes), r);
+        nf4_dequant_row(raw + r * 32, 0, (r >> 2) & 1, am, lv, smem_u32(sbase + stage * SB + kXBytes), r);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
