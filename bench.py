@@ -56,6 +56,16 @@ def measured_peaks():
     return 1900.0, 6800.0, "fallback"
 
 
+def measured_sustained_bf16():
+    """cuBLAS bf16 rate held for seconds under the power cap (the default timed loop runs
+    about 0.3 s of back-to-back launches, long enough for the cap to act), or None."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        return json.load(f).get("bf16_tflops_sustained")
+
+
 def captured_traffic():
     """DRAM bytes per launch of the fused kernel from the committed ncu summary, or None
     when the kernel source changed since that capture."""
@@ -212,6 +222,7 @@ def run_fused(args):
     d2h = Y.numel() * Y.element_size()
 
     peak, hbm, peak_kind = measured_peaks()
+    sustained = measured_sustained_bf16()
     tflops = ws * flops / (ms_step * 1e-3) / 1e12
     per_launch_tflops = flops / (ms_step * 1e-3) / 1e12
     out = {
@@ -234,6 +245,7 @@ def run_fused(args):
         "roofline": {"bound": "tensor", "achieved": round(per_launch_tflops, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(per_launch_tflops / peak, 4), "traffic": captured_traffic(),
                      "peak_source": f"{peak_kind} bf16 burst",
+                     "frac_of_sustained": (round(per_launch_tflops / sustained, 4) if sustained else None),
                      "timing": "CUDA events over the timed steps; a step is the rank-operand pack "
                                "kernel plus the fused kernel, so this slightly understates the fused "
                                "kernel's own rate"},
