@@ -21,6 +21,11 @@ Sources:
   * Unsloth fast_lora walkthrough, section 2: the forward is linear,
     out = X (W + s A B)^T in its transposed naming, and the backward has closed forms
     for dX, dA, dB (section 4, ``LoRA_MLP`` / ``LoRA_QKV``).
+  * piper-offload docs, "LoRA merge": older PEFT/Wan adapters may carry a vector beside A
+    and B (their lora_B.bias); routed mode applies it as part of the output residual, merge
+    mode adds it to the module's bias with the same adapter strength.  Reading: the vector
+    is scaled by the adapter's own s, so a patch contributes s ((X A^T) B^T + bias_B), as
+    the second factor's bias of a PEFT adapter does.
 
 Everything is exact FP64 on exactly decoded inputs; ``numpy.matmul`` is the only
 library step.  ``unfused_bf16_chain`` is not the definition: it simulates the
@@ -44,6 +49,7 @@ class DecodedPatch:
     alpha: float
     strength: float
     fp32_adapter: bool = False
+    bias_B: Optional[np.ndarray] = None   # [out] float64: the legacy vector, or None
 
     @property
     def rank(self) -> int:
@@ -57,10 +63,13 @@ def combined_scale(alpha: float, rank: int, strength: float, request_scale: floa
 
 
 def lora_delta(X: np.ndarray, p: DecodedPatch, request_scale: float) -> np.ndarray:
-    """s (X A^T) B^T for one patch."""
+    """s ((X A^T) B^T + bias_B) for one patch (bias_B, the legacy vector, if it has one)."""
     s = combined_scale(p.alpha, p.rank, p.strength, request_scale)
     H = X @ p.A.T
-    return s * (H @ p.B.T)
+    D = H @ p.B.T
+    if p.bias_B is not None:
+        D = D + np.asarray(p.bias_B, dtype=np.float64).reshape(1, -1)
+    return s * D
 
 
 def linear_fwd(X: np.ndarray, W: Optional[np.ndarray], bias: Optional[np.ndarray],
@@ -156,7 +165,8 @@ def unfused_bf16_chain(X: np.ndarray, W: Optional[np.ndarray], bias: Optional[np
     chain materialises is rounded to bf16.
 
         base = bf16(X W^T + bias)                 (bias in the base GEMM, one GPU)
-        t    = bf16(X A^T);  d = bf16(t B^T)
+        t    = bf16(X A^T);  d = bf16(t B^T)      (d = bf16(t B^T + bias_B) for a legacy
+                                                   vector: the second factor's own bias)
         d    = bf16(d * alpha/r); d = bf16(d * strength); d = bf16(d * request_scale)
         Y    = bf16(Y + d)                        (patch after patch, in order)
 
@@ -178,13 +188,14 @@ def unfused_bf16_chain(X: np.ndarray, W: Optional[np.ndarray], bias: Optional[np
         sl = column_slices[i] if column_slices is not None else slice(None)
         scales = [np.float64(np.float32(p.alpha / p.rank)), np.float64(np.float32(p.strength)),
                   np.float64(np.float32(request_scale))]
+        vb = 0.0 if p.bias_B is None else np.asarray(p.bias_B, dtype=np.float64).reshape(1, -1)
         if p.fp32_adapter:
-            d = (X @ p.A.T) @ p.B.T
+            d = (X @ p.A.T) @ p.B.T + vb
             for c in scales:
                 d = d * c
         else:
             t = rnd(X @ p.A.T)
-            d = rnd(t @ p.B.T)
+            d = rnd(t @ p.B.T + vb)
             for c in scales:
                 if c != 1.0:
                     d = rnd(d * c)

@@ -20,6 +20,12 @@ Readings (the pages fix the flow, not the arithmetic):
     the number of midpoints fl32((level[k] + level[k+1]) / 2) below x (a value on a midpoint
     takes the lower code); an all-zero block keeps scale 0 and the code of level 0 (index 7).
 
+Legacy adapter bias vectors (the lora_B.bias older adapters carry; piper-offload docs,
+"LoRA merge": merge mode adds the vector to the module's dense bias with the same adapter
+strength) follow the dense bias patch's arithmetic (FastVideo DenseLoRAPatch.apply_to:
+cast(fp32(param) + fp32(payload) * k)) with k = s_p, all of a call's vectors summed in
+float32 in call order and the sum cast once (one update, as for the weight).
+
 Pinned by ``tests/test_oracle_merge.py``: brute force (exhaustive argmin over the 16
 levels), the dequantise-requantise round trip on blocks that hold level +-1, merge and
 unmerge returning the weight within one rounding, zero strength leaving it unchanged,
@@ -50,6 +56,24 @@ def update(patches: Sequence[DecodedPatch], scale: float) -> np.ndarray:
 def merge_bf16_values(W: np.ndarray, patches: Sequence[DecodedPatch], scale: float) -> np.ndarray:
     """The merged bf16 weight (as float64 values) from the float64 values of the old one."""
     return f64_to_bf16_value(W + update(patches, scale))
+
+
+def merge_bias_values(bias: np.ndarray, patches: Sequence[DecodedPatch], scale: float,
+                      bf16: bool) -> np.ndarray:
+    """The merged bias (float64 values) from the old one: v = fl32(bias), then for each
+    patch with a legacy vector v = fl32(v + fl32(fl32(s_p) * fl32(vec))), then the bias's
+    own dtype (bf16 round to nearest even, or float32 as is)."""
+    v = np.asarray(bias, dtype=np.float64).astype(np.float32)
+    for p in patches:
+        if p.bias_B is None:
+            continue
+        s = np.float32(combined_scale(p.alpha, p.rank, p.strength, scale))
+        if s == 0:
+            continue
+        term = (s * np.asarray(p.bias_B, dtype=np.float64).astype(np.float32)).astype(np.float32)
+        v = (v + term).astype(np.float32)
+    v = v.astype(np.float64)
+    return f64_to_bf16_value(v) if bf16 else v
 
 
 def midpoints_f32() -> np.ndarray:
