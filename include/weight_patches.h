@@ -88,12 +88,19 @@ typedef struct wp_out {
 /* One low-rank patch.  A [r, in], B [out, r] (for grouped calls, out = the group's
  * width); both WP_BF16, or both WP_FP32 for an FP32 adapter.  The combined scale
  * s = alpha / r * strength * request_scale is formed on the host in double and
- * rounded once to fp32; an adapter whose s is exactly +-0 contributes nothing. */
+ * rounded once to fp32; an adapter whose s is exactly +-0 contributes nothing.
+ * bias_B: the optional vector older PEFT/Wan adapters carry beside A and B (their
+ * lora_B.bias; piper-offload docs, "LoRA merge"), [out] contiguous on the device,
+ * WP_BF16 or WP_FP32 (bias_B_dtype), or NULL.  The forwards add s * bias_B to the
+ * adapter's output columns (also when the layer has no bias of its own); lora_merge adds
+ * it to the module's bias; the backward's dX, dA and dB do not depend on it. */
 typedef struct wp_adapter {
   wp_mat A;
   wp_mat B;
   double alpha;
   double strength;
+  const void* bias_B;
+  int32_t bias_B_dtype;
 } wp_adapter;
 
 /* Operation ids for lora_workspace_size(). */
@@ -107,7 +114,10 @@ enum { WP_OP_FWD = 0, WP_OP_FWD_GROUPED = 1, WP_OP_BWD = 2, WP_OP_FWD_HOST = 3, 
  *   X        [T, in], WP_BF16 (tensor-core path) or WP_FP32 (exact FP32 path).
  *   W        [out, in], WP_BF16 or WP_NF4 with a bf16 X, WP_FP32 with an fp32 X;
  *            NULL computes the low-rank delta only.
- *   bias     [1, out] WP_BF16 or WP_FP32, or NULL; added in the epilogue.
+ *   bias     [1, out] WP_BF16 or WP_FP32, or NULL; added in the epilogue.  With adapters
+ *            that carry a legacy bias_B (and a non-zero s), bias + sum_p s_p bias_B_p is
+ *            first formed in fp32 in the workspace (the first ceil256(4 out) bytes) and
+ *            that vector is what the epilogue adds.
  *   adapters n_adapters patches (0..12); bf16 adapters on a bf16 X run on the tensor
  *            cores.  FP32 adapters on a bf16 X run there too, as three bf16 pieces per
  *            factor (every product above 2^-24 of the leading one is kept), when the
@@ -171,6 +181,7 @@ int lora_linear_fwd_host(const wp_mat* X_host, const wp_mat* W, const wp_mat* bi
  * lora_merge -- bake adapters into the base weight in place (piper-offload docs, "LoRA
  * merge" and "Quantized weight support"; the PEFT merge):
  *     W <- W + sum_p s_p B_p A_p,   s_p = alpha_p / r_p * strength_p * scale,
+ *     bias <- bias + sum_p s_p bias_B_p   (adapters that carry the legacy vector),
  * every adapter of the call taken as one update, accumulated in fp32 and rounded once:
  *   W WP_BF16 [out, in] (device): bf16_rne(fl32(W) + ...);
  *   W WP_NF4 (codes [out, in/2] and absmax [out*in/64], device, both rewritten): dequantised
@@ -181,11 +192,16 @@ int lora_linear_fwd_host(const wp_mat* X_host, const wp_mat* W, const wp_mat* bi
  *   merge of the same adapters up to the roundings.
  *   workspace: lora_workspace_size(WP_OP_MERGE, NULL, W, adapters, n) bytes (A^T copies, and
  *   an fp32 [out, in] buffer for a 4-bit W or several adapters).
+ *   bias: the module's bias [out] (WP_BF16 or WP_FP32, device, rewritten in place) or NULL.
+ *   The legacy vectors are added in fp32 in call order (each term fl32(s_p * v)) and the
+ *   sum rounded once to the bias's dtype; for one adapter that is the dense patch's add.
  * Errors: WP_ERR_SHAPE, WP_ERR_DTYPE (fp32 adapters), WP_ERR_ALIGN (bf16 W rows must be
- * 16-byte aligned), WP_ERR_WORKSPACE.  With no non-zero adapter nothing is launched.
+ * 16-byte aligned), WP_ERR_WORKSPACE; WP_ERR_INVALID, before anything is written, when an
+ * adapter with a non-zero s carries a legacy vector and bias is NULL (the merge does not
+ * create a bias the module does not have).  With no non-zero adapter nothing is launched.
  */
-int lora_merge(const wp_mat* W, const wp_adapter* adapters, int32_t n_adapters, double scale,
-               void* workspace, size_t workspace_bytes, void* stream);
+int lora_merge(const wp_mat* W, const wp_out* bias, const wp_adapter* adapters, int32_t n_adapters,
+               double scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * lora_swiglu_fwd -- the front half of a SwiGLU LoRA MLP in one pass: the gate and up

@@ -206,8 +206,10 @@ def unfused_bf16_chain(X: np.ndarray, W: Optional[np.ndarray], bias: Optional[np
 def decode_patch(p) -> DecodedPatch:
     """A ``workloads.Patch`` decoded to exact float64."""
     from .numerics import to_f64
+    vb = getattr(p, "bias_B", None)
     return DecodedPatch(to_f64(p.A), to_f64(p.B), float(p.alpha), float(p.strength),
-                        fp32_adapter=(p.A.kind == "fp32" and p.B.kind == "fp32"))
+                        fp32_adapter=(p.A.kind == "fp32" and p.B.kind == "fp32"),
+                        bias_B=None if vb is None else to_f64(vb).reshape(-1))
 
 
 def decode_linear(lin, rows=None):

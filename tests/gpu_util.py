@@ -20,7 +20,9 @@ def dev(mat):
 
 
 def adapters(lin):
-    return [wpg.Adapter(dev(p.A), dev(p.B), p.alpha, p.strength) for p in lin.patches]
+    return [wpg.Adapter(dev(p.A), dev(p.B), p.alpha, p.strength,
+                        dev(p.bias_B).reshape(-1) if getattr(p, "bias_B", None) is not None else None)
+            for p in lin.patches]
 
 
 def run_fwd(lin, out_dtype=torch.bfloat16, with_base=True, request_scale=None):

@@ -44,7 +44,7 @@ class WpOut(ctypes.Structure):
 
 class WpAdapter(ctypes.Structure):
     _fields_ = [("A", WpMat), ("B", WpMat), ("alpha", ctypes.c_double),
-                ("strength", ctypes.c_double)]
+                ("strength", ctypes.c_double), ("bias_B", ctypes.c_void_p), ("bias_B_dtype", ctypes.c_int32)]
 
 
 class WeightPatchesError(RuntimeError):
@@ -76,7 +76,7 @@ def _load():
     lib.lora_linear_fwd_host.argtypes = [pm, pm, pm, I32, pa, I32, D, po, P, SZ, P]
     lib.lora_linear_bwd.argtypes = [pm, pm, pm, I32, pa, D, po, po, po, P, SZ, P]
     lib.lora_swiglu_fwd.argtypes = [pm, pm, pm, pa, D, po, po, P, SZ, P]
-    lib.lora_merge.argtypes = [pm, pa, I32, D, P, SZ, P]
+    lib.lora_merge.argtypes = [pm, po, pa, I32, D, P, SZ, P]
     lib.lora_swiglu_bwd.argtypes = [pm, pm, po, po, P]
     lib.lora_dense_patch.argtypes = [P, I32, I64, P, I32, I64, I32, D, P]
     lib.lora_workspace_size.argtypes = [I32, pm, pm, pa, I32]
@@ -113,12 +113,16 @@ class NF4Weight:
 
 @dataclass
 class Adapter:
-    """One low-rank patch: A [r, in], B [out, r] (bf16, or fp32 for an FP32 adapter)."""
+    """One low-rank patch: A [r, in], B [out, r] (bf16, or fp32 for an FP32 adapter), and the
+    optional legacy ``bias_B`` [out] (bf16 or fp32) older adapters carry as lora_B.bias: the
+    forwards add s * bias_B to the patch's output columns, ``lora_merge`` adds it to the
+    module's bias."""
 
     A: torch.Tensor
     B: torch.Tensor
     alpha: float
     strength: float = 1.0
+    bias_B: Optional[torch.Tensor] = None
 
 
 _DT = {torch.bfloat16: WP_BF16, torch.float32: WP_FP32}
@@ -147,7 +151,12 @@ def _out(t: torch.Tensor) -> WpOut:
 def _adapters(adapters: Sequence[Adapter]):
     arr = (WpAdapter * max(1, len(adapters)))()
     for i, a in enumerate(adapters):
-        arr[i] = WpAdapter(_mat(a.A), _mat(a.B), float(a.alpha), float(a.strength))
+        vb = getattr(a, "bias_B", None)
+        if vb is not None and not vb.is_contiguous():
+            raise ValueError("bias_B must be contiguous")
+        arr[i] = WpAdapter(_mat(a.A), _mat(a.B), float(a.alpha), float(a.strength),
+                           vb.data_ptr() if vb is not None else None,
+                           _DT[vb.dtype] if vb is not None else WP_BF16)
     return arr
 
 
@@ -218,17 +227,25 @@ def lora_linear_fwd_grouped(X: torch.Tensor, W_stacked, bias: Optional[torch.Ten
     return out
 
 
-def lora_merge(W, adapters: Sequence[Adapter], scale: float = 1.0, workspace: Optional[torch.Tensor] = None):
+def lora_merge(W, adapters: Sequence[Adapter], scale: float = 1.0, workspace: Optional[torch.Tensor] = None,
+               bias: Optional[torch.Tensor] = None):
     """Bake the adapters into W in place: W <- W + sum_p s_p B_p A_p (s_p = alpha/r * strength
     * scale), accumulated in fp32 and rounded once; a 4-bit ``NF4Weight`` is requantised
-    (round to nearest).  Returns W."""
+    (round to nearest).  Adapters with a legacy ``bias_B`` also update ``bias`` in place
+    (bias <- bias + sum_p s_p bias_B_p, one rounding); the call fails before writing anything
+    when such an adapter meets ``bias=None``.  Returns W."""
     wm, arr = _mat(W), _adapters(adapters)
+    bo = None
+    if bias is not None:
+        if not bias.is_contiguous():
+            raise ValueError("bias must be contiguous")
+        bo = WpOut(bias.data_ptr(), _DT[bias.dtype], 1, bias.numel(), bias.numel())
     device = W.packed.device if isinstance(W, NF4Weight) else W.device
     need = _load().lora_workspace_size(WP_OP_MERGE, None, ctypes.byref(wm), arr, len(adapters))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=device)
     nbytes = workspace.numel() if workspace is not None else 0
-    st = _load().lora_merge(ctypes.byref(wm), arr, len(adapters), float(scale),
+    st = _load().lora_merge(ctypes.byref(wm), _ref(bo), arr, len(adapters), float(scale),
                             workspace.data_ptr() if workspace is not None else None, nbytes, _stream(device))
     _check(st, "lora_merge")
     return W

@@ -132,6 +132,7 @@ struct FwdPlan {
   int rank_cols = 0;      // rank-item columns, at most (tensor-core path)
   size_t pack_bytes = 0;  // packed A rows of the rank item (tensor-core path)
   size_t skinny_bytes = 0;  // small-token path: packed A rows + K-split partial sums
+  size_t fold_bytes = 0;  // the fp32 bias with the adapters' legacy vectors folded in
 };
 
 // Small-token path (T <= 64, bf16 X and adapters, bf16 or 4-bit W): the fp32 partial sums
@@ -221,6 +222,15 @@ int plan_fwd(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int n, FwdP
                               static_cast<size_t>((X->cols + 7) / 8 * 8) * 2);
   SkinnyPlan sp;
   if (plan_skinny(X, W, ad, n, &sp)) plan->skinny_bytes = sp.part_bytes;
+  // legacy adapter bias vectors: an fp32 [out] vector ahead of everything else (out bounded
+  // by the sum of the adapters' B rows when there is no W)
+  bool legacy = false;
+  long long nb = W ? W->rows : 0;
+  for (int i = 0; i < n; ++i) {
+    legacy = legacy || ad[i].bias_B != nullptr;
+    if (!W) nb += ad[i].B.rows;
+  }
+  plan->fold_bytes = legacy ? round256(static_cast<size_t>(nb) * 4) : 0;
   return WP_OK;
 }
 
@@ -235,9 +245,9 @@ size_t fwd_workspace(const wp_mat* X, const FwdPlan& plan, bool min_only = false
       tc = round256(T * plan.rank32_total * 4) + plan.split_bytes + round256(T * plan.htilde_cols * 2) +
            round256(m_tiles * 4) + plan.pack_bytes;
     }
-    return min_only ? tc : std::max(tc, plan.skinny_bytes);
+    return plan.fold_bytes + (min_only ? tc : std::max(tc, plan.skinny_bytes));
   }
-  return plan.rank_all ? round256(T * plan.rank_all * 4) : 0;
+  return plan.fold_bytes + (plan.rank_all ? round256(T * plan.rank_all * 4) : 0);
 }
 
 // The last CUDA error, recorded for lora_last_cuda_error, as a status.
@@ -402,12 +412,46 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     s_of[i] = static_cast<float>(s);
   }
 
+  // legacy adapter bias vectors (older adapters' lora_B.bias), folded with the layer's own
+  // bias into one fp32 vector that the epilogue adds instead
+  BiasFoldParams fold{};
+  for (int i = 0; i < n_adapters; ++i) {
+    const wp_adapter& a = adapters[i];
+    if (!a.bias_B) continue;
+    if (a.bias_B_dtype != WP_BF16 && a.bias_B_dtype != WP_FP32) return WP_ERR_DTYPE;
+    if (rank_only || s_of[i] == 0.0f) continue;
+    const int g = grouped ? i : 0;
+    BiasFoldParams::Vec& v = fold.ad[fold.n++];
+    v.v = a.bias_B;
+    v.dtype = a.bias_B_dtype;
+    v.s = s_of[i];
+    v.col0 = static_cast<int>(g * out_g);
+    v.cols = static_cast<int>(grouped ? out_g : N);
+  }
+
   FwdPlan plan;
   plan_fwd(X, W, adapters, n_adapters, &plan);
   const size_t need = fwd_workspace(X, plan, /*min_only=*/true);
   if (need > 0 && (!workspace || ws_bytes < need)) return WP_ERR_WORKSPACE;
   if (need > 0 && !aligned16(workspace)) return WP_ERR_ALIGN;
+  wp_mat folded_bias{};
+  if (fold.n > 0) {
+    // the first plan.fold_bytes of the workspace (at least 4 N bytes); the paths below get
+    // the rest
+    fold.out = static_cast<float*>(workspace);
+    fold.bias = bias ? const_cast<void*>(bias->data) : nullptr;
+    fold.bias_dtype = bias ? bias->dtype : WP_FP32;
+    fold.N = static_cast<int>(N);
+    folded_bias = wp_mat{workspace, WP_FP32, 1, N, N, nullptr};
+    workspace = static_cast<uint8_t*>(workspace) + plan.fold_bytes;
+    ws_bytes -= plan.fold_bytes;
+  }
   if (T == 0) return WP_OK;
+  if (fold.n > 0) {
+    const int frc = launch_bias_fold(fold, stream);
+    if (frc != WP_OK) return frc;
+    bias = &folded_bias;
+  }
 
   // a few tokens: the weight-streaming small-token path, when the workspace holds its
   // partial sums (else the general path below serves the call)
@@ -783,7 +827,7 @@ bool bwd_layout(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int G, B
                     static_cast<int64_t>(Ntot), nullptr};
     const wp_mat wt{nullptr, WP_BF16, static_cast<int64_t>(K), static_cast<int64_t>(Ntot),
                     static_cast<int64_t>(Ntot), nullptr};
-    wp_adapter fa[kMaxGroups];
+    wp_adapter fa[kMaxGroups] = {};
     for (int g = 0; g < G; ++g) {
       const int64_t r = ad[g].A.rows;
       fa[g].A = wp_mat{nullptr, WP_BF16, r, static_cast<int64_t>(Ntot), static_cast<int64_t>(Ntot), nullptr};
@@ -873,7 +917,7 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
 
   // 2. per group: B_g^T placed at the group's columns of a zero [r_g, Ntot] matrix (so
   //    dY B_hat_g^T = dY_g B_g), and A_g^T [K, r8_g]
-  wp_adapter fwd_ad[kMaxGroups];
+  wp_adapter fwd_ad[kMaxGroups] = {};             // (no legacy bias vectors: dX does not have them)
   for (int g = 0; g < G; ++g) {
     const wp_adapter& a = ad[g];
     const int r = static_cast<int>(a.A.rows);
@@ -898,6 +942,7 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
       h_ad[g] = ad[g];
       h_ad[g].alpha = static_cast<double>(ad[g].A.rows);
       h_ad[g].strength = 1.0;
+      h_ad[g].bias_B = nullptr;
     }
     rc = fwd_impl(X, nullptr, nullptr, G, G > 1, h_ad, G, 1.0, nullptr, ws + L.fwd, L.fwd_bytes,
                   stream, H, L.R, /*rank_only=*/true);
@@ -1240,8 +1285,8 @@ int merge_pass(const void* P, long long ldp, const void* Q, long long ldq, long 
   return launch_tc_fwd(maps, p, 2 * pairs, smem, stream, false);
 }
 
-int merge_impl(const wp_mat* W, const wp_adapter* ad, int n, double scale, void* workspace, size_t ws_bytes,
-               cudaStream_t stream) {
+int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n, double scale, void* workspace,
+               size_t ws_bytes, cudaStream_t stream) {
   if (!W || !W->data || W->rows <= 0 || W->cols <= 0) return WP_ERR_INVALID;
   if (W->dtype != WP_BF16 && W->dtype != WP_NF4) return WP_ERR_DTYPE;
   if (!std::isfinite(scale)) return WP_ERR_INVALID;
@@ -1253,7 +1298,13 @@ int merge_impl(const wp_mat* W, const wp_adapter* ad, int n, double scale, void*
   if (nf4 ? (in % 64 != 0 || W->ld != in || !W->absmax || !aligned16(W->absmax) || !aligned16(W->data))
           : (W->ld < in || W->ld % 8 != 0 || in % 8 != 0 || !aligned16(W->data)))
     return nf4 ? WP_ERR_SHAPE : WP_ERR_ALIGN;
+  if (bias) {
+    if (!bias->data) return WP_ERR_INVALID;
+    if (bias->dtype != WP_BF16 && bias->dtype != WP_FP32) return WP_ERR_DTYPE;
+    if (bias->rows * bias->cols != out) return WP_ERR_SHAPE;
+  }
   float s_of[kMaxAd];
+  BiasFoldParams fold{};                           // the adapters' legacy bias vectors
   for (int i = 0; i < n; ++i) {
     const wp_adapter& a = ad[i];
     if (!a.A.data || !a.B.data) return WP_ERR_INVALID;
@@ -1265,6 +1316,18 @@ int merge_impl(const wp_mat* W, const wp_adapter* ad, int n, double scale, void*
     const double s = a.alpha / static_cast<double>(r) * a.strength * scale;
     if (!std::isfinite(s) || !std::isfinite(static_cast<float>(s))) return WP_ERR_INVALID;
     s_of[i] = static_cast<float>(s);
+    if (a.bias_B) {
+      if (a.bias_B_dtype != WP_BF16 && a.bias_B_dtype != WP_FP32) return WP_ERR_DTYPE;
+      if (s_of[i] == 0.0f) continue;
+      // a legacy vector needs a bias to land in: refused before anything is written
+      if (!bias) return WP_ERR_INVALID;
+      BiasFoldParams::Vec& v = fold.ad[fold.n++];
+      v.v = a.bias_B;
+      v.dtype = a.bias_B_dtype;
+      v.s = s_of[i];
+      v.col0 = 0;
+      v.cols = static_cast<int>(out);
+    }
   }
   MergeLayout L;
   if (!merge_layout(W, ad, n, scale, &L)) return WP_ERR_INVALID;
@@ -1314,6 +1377,13 @@ int merge_impl(const wp_mat* W, const wp_adapter* ad, int n, double scale, void*
     if (rc != WP_OK) return rc;
   }
   if (nf4) rc = launch_nf4_requant(U, out * in, tab, wdata, const_cast<float*>(W->absmax), stream);
+  if (rc == WP_OK && fold.n > 0) {
+    // bias <- bias + sum_p s_p bias_B_p, rounded once to the bias's dtype
+    fold.bias = bias->data;
+    fold.bias_dtype = bias->dtype;
+    fold.N = static_cast<int>(out);
+    rc = launch_bias_fold(fold, stream);
+  }
   return rc;
 }
 
@@ -1339,9 +1409,10 @@ int lora_linear_fwd_grouped(const wp_mat* X, const wp_mat* W_stacked, const wp_m
                   workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
-int lora_merge(const wp_mat* W, const wp_adapter* adapters, int32_t n_adapters, double scale, void* workspace,
-               size_t workspace_bytes, void* stream) {
-  return merge_impl(W, adapters, n_adapters, scale, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+int lora_merge(const wp_mat* W, const wp_out* bias, const wp_adapter* adapters, int32_t n_adapters, double scale,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  return merge_impl(W, bias, adapters, n_adapters, scale, workspace, workspace_bytes,
+                    static_cast<cudaStream_t>(stream));
 }
 
 int lora_swiglu_fwd(const wp_mat* X, const wp_mat* W_gate_up, const wp_mat* bias,

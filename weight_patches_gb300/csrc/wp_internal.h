@@ -299,6 +299,25 @@ int launch_tok_finish(const float* part, int M, int N, int splits, int R16, int 
                       float scale, float* out, long long ldo, bool transposed, cudaStream_t stream);
 
 // LoRA merge into a 4-bit weight (wp_merge.cu): W_eff as fp32, and the requantisation
+// Legacy adapter bias vectors folded into one per-column vector (piper-offload docs,
+// "LoRA merge": older adapters' lora_B.bias):  v[n] = fl32(bias[n]) and then, in order,
+// v[n] = fl32(v[n] + fl32(s_p * vec_p[n - col0_p])) for each adapter p whose columns
+// [col0_p, col0_p + cols_p) hold n.  out != nullptr: v goes there in fp32 (the forward's
+// epilogue bias); else it is rounded to the bias's own dtype and written back (the merge).
+struct BiasFoldParams {
+  float* out;
+  void* bias;                  // [N] or nullptr (forward only)
+  int bias_dtype;
+  int N, n;
+  struct Vec {
+    const void* v;
+    int dtype;
+    float s;
+    int col0, cols;
+  } ad[kMaxAd + kMaxAd32];
+};
+int launch_bias_fold(const BiasFoldParams& p, cudaStream_t stream);
+
 int launch_nf4_to_f32(const void* codes, const float* absmax, long long numel, const NF4Table& tab, float* U,
                       cudaStream_t stream);
 int launch_nf4_requant(const float* U, long long numel, const NF4Table& tab, void* codes, float* absmax,

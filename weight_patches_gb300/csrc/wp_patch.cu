@@ -10,6 +10,10 @@
 // round-to-nearest-even, which makes the result bit-exact against the float32
 // definition.  The kernel is HBM-bound: 16-byte vector loads and stores, four of each in
 // flight per thread, a grid of a few CTAs per SM striding over the tensor.
+//
+// The same add folds the legacy lora_B.bias vectors of older adapters into a layer's bias
+// (bias_fold_kernel): for the forward's epilogue (kept in fp32) and for the merge (rounded
+// once to the bias's dtype).
 #include <cuda_runtime.h>
 
 #include "wp_internal.h"
@@ -49,6 +53,34 @@ __device__ __forceinline__ uint4 patch8(uint4 d, uint4 pv, int kind, float k) {
     out[w] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
   }
   return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+__global__ void __launch_bounds__(256) bias_fold_kernel(const BiasFoldParams p) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= p.N) return;
+  float v = p.bias ? widen(p.bias, p.bias_dtype, n) : 0.f;
+  for (int i = 0; i < p.n; ++i) {
+    const int j = n - p.ad[i].col0;
+    if (j >= 0 && j < p.ad[i].cols) v = combine(v, widen(p.ad[i].v, p.ad[i].dtype, j), p.ad[i].s, WP_PATCH_ADD);
+  }
+  if (p.out) {
+    p.out[n] = v;
+  } else if (p.bias_dtype == WP_FP32) {
+    static_cast<float*>(p.bias)[n] = v;
+  } else {
+    static_cast<uint16_t*>(p.bias)[n] = to_bf16(v);
+  }
+}
+
+int launch_bias_fold(const BiasFoldParams& p, cudaStream_t stream) {
+  if (p.N <= 0) return WP_OK;
+  bias_fold_kernel<<<(p.N + 255) / 256, 256, 0, stream>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    return WP_ERR_CUDA;
+  }
+  return WP_OK;
 }
 
 // bf16 parameter, bf16 payload, 8 elements (16 bytes) per vector; each thread keeps four

@@ -102,12 +102,14 @@ def draw_nf4(rng: np.random.Generator, rows: int, cols: int) -> Mat:
 
 @dataclass
 class Patch:
-    """One low-rank patch: A [r, in], B [out, r], alpha, strength (the patch weight)."""
+    """One low-rank patch: A [r, in], B [out, r], alpha, strength (the patch weight), and
+    optionally the legacy vector older adapters carry beside A and B (bias_B, [1, out])."""
 
     A: Mat
     B: Mat
     alpha: float
     strength: float
+    bias_B: Optional[Mat] = None
 
     @property
     def rank(self) -> int:
