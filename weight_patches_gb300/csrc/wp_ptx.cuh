@@ -170,6 +170,11 @@ __device__ __forceinline__ void cluster_sync() {
 }
 
 // ---------------------------------------------------------------- TMA
+// Pull one global line toward L2 (no register result, nothing to wait for).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

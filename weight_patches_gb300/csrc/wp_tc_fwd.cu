@@ -615,6 +615,26 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       const Tile& t = it.t;
       const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
       const bool any_mma = p.has_base || a1 > a0;
+      if (!kNF4 && p.resid) {
+        // merge: pull this thread's residual rows toward L2 one tile ahead of their use (the
+        // first tile's own rows too), so that they land while this tile is drained
+        auto prefetch_tile = [&](const Tile& tt) {
+          const int esz = p.resid_f32 ? 4 : 2;
+          const int nbytes = min(kBN, p.out_g - tt.j * kBN) * esz;
+          for (int h = h_begin; h < h_end; ++h) {
+            const int row = tt.m * (kPairM * kMH) + h * kPairM + static_cast<int>(cta) * kBM + row_in_cta;
+            if (row >= p.T) continue;
+            const char* rp = static_cast<const char*>(p.resid) +
+                             (static_cast<long long>(row) * p.ld_resid + tt.g * p.out_g + tt.j * kBN) * esz;
+            for (int off = 0; off < nbytes; off += 128) prefetch_l2(rp + off);
+            prefetch_l2(rp + nbytes - 1);
+          }
+        };
+        if (count == 0) prefetch_tile(t);
+        ItemIter peek = iter;                       // the iterator's state alone: a copy peeks
+        Item nx;
+        if (next_item(peek, p, pair, npairs, nx) && !nx.rank) prefetch_tile(nx.t);
+      }
       if (any_mma) {
         const bool ok = mbar_wait_cluster(&acc_full[b], nuse[b] & 1, abort_flag, tmo, status);
         if (named_bar_any(!ok, bar_any, 128)) break;
@@ -712,12 +732,29 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
 
       // valid chunks of this tile (the last tile of a group may be partial)
       const int nchunk = min(kBN / cw, (p.out_g - t.j * kBN + cw - 1) / cw);
+      // merge: the residual of 32-column sub-chunk (cc, ss) of `row` into dst (4 x 16 bytes
+      // bf16, 8 x 16 bytes fp32; the row pitch and the sub-chunk start are multiples of 8
+      // elements), issued one sub-chunk ahead of its use so its latency overlaps the work
+      const int esz_r = p.resid_f32 ? 4 : 2;
+      auto load_res = [&](int row, int cc, int ss, uint4 (&dst)[8]) {
+        const int cig2 = t.j * kBN + cc * cw + ss * 32;
+        const int n2 = min(32, p.out_g - cig2);
+        const uint4* rp = reinterpret_cast<const uint4*>(
+            static_cast<const char*>(p.resid) +
+            (static_cast<long long>(row) * p.ld_resid + t.g * p.out_g + cig2) * esz_r);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i < 2 * esz_r && i * (16 / esz_r) < n2) dst[i] = rp[i];
+      };
 #pragma unroll 1
       for (int h = h_begin; h < h_end; ++h) {
       const int row0 = t.m * (kPairM * kMH) + h * kPairM + static_cast<int>(cta) * kBM;
       const int row = row0 + row_in_cta;
       const bool row_ok = row < p.T;
       const uint32_t acc_t = tmem + (b + h) * kBN;
+      const bool res_row = !kNF4 && p.resid && row_ok;   // merges run on the bf16 instantiation
+      uint4 rnext[8], rcur[8];
+      if (res_row) load_res(row, 0, 0, rnext);
 #pragma unroll 1
       for (int c = 0; c < nchunk; ++c) {
         const int cig = t.j * kBN + c * cw;                 // first column, within the group
@@ -751,15 +788,19 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
           }
           const int nc = min(32, ncols - c0);               // valid columns of the sub-chunk
-          if (p.resid && row_ok && nc > 0) {
-            // merge: s * acc + R, two fp32 roundings, R read with 16-byte loads (the row
-            // pitch and the sub-chunk start are multiples of 8 elements)
+          if (res_row && nc > 0) {
+            // merge: s * acc + R, two fp32 roundings; this sub-chunk's R was loaded one
+            // sub-chunk ago, the next one's load goes out now
+#pragma unroll
+            for (int i = 0; i < 8; ++i) rcur[i] = rnext[i];
+            const int cn = sub + 1 < cw / 32 ? c : c + 1, sn = sub + 1 < cw / 32 ? sub + 1 : 0;
+            if (cn < nchunk && t.j * kBN + cn * cw + sn * 32 < p.out_g) load_res(row, cn, sn, rnext);
             if (p.resid_f32) {
-              const float* rp = static_cast<const float*>(p.resid) + static_cast<long long>(row) * p.ld_resid + gcol + c0;
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 if (4 * i < nc) {
-                  const float4 r4 = *reinterpret_cast<const float4*>(rp + 4 * i);
+                  const float4 r4 = make_float4(__uint_as_float(rcur[i].x), __uint_as_float(rcur[i].y),
+                                                __uint_as_float(rcur[i].z), __uint_as_float(rcur[i].w));
                   v[4 * i] = __fadd_rn(__fmul_rn(v[4 * i], p.acc_scale), r4.x);
                   v[4 * i + 1] = __fadd_rn(__fmul_rn(v[4 * i + 1], p.acc_scale), r4.y);
                   v[4 * i + 2] = __fadd_rn(__fmul_rn(v[4 * i + 2], p.acc_scale), r4.z);
@@ -767,11 +808,10 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
                 }
               }
             } else {
-              const uint16_t* rp = static_cast<const uint16_t*>(p.resid) + static_cast<long long>(row) * p.ld_resid + gcol + c0;
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 if (8 * i < nc) {
-                  const uint4 r8 = *reinterpret_cast<const uint4*>(rp + 8 * i);
+                  const uint4 r8 = rcur[i];
                   const uint32_t w[4] = {r8.x, r8.y, r8.z, r8.w};
 #pragma unroll
                   for (int k = 0; k < 4; ++k) {
