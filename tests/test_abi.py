@@ -130,3 +130,41 @@ def test_workspace_sizes(lib):
 def test_status_strings(lib):
     for code in wpg.STATUS:
         assert wpg.lora_status_string(code)
+
+
+def _ad_vec(r, n_in, n_out, vec_dtype=wpg.WP_BF16, strength=1.0):
+    a = _ad(r, n_in, n_out, strength=strength)
+    a.bias_B = FAKE
+    a.bias_B_dtype = vec_dtype
+    return a
+
+
+def test_legacy_vector_rejections(lib):
+    """Older adapters' bias vector: a bad dtype, a missing workspace for the folded bias, and
+    (merge) a vector meeting a module without a bias, all refused on the host."""
+    X, W, Y = _m(64, 128), _m(256, 128), _o(64, 256)
+    assert _fwd(lib, X, W, None, [_ad_vec(8, 128, 256, vec_dtype=wpg.WP_NF4)], Y,
+                ws=FAKE, ws_bytes=1 << 30) == -3
+    assert _fwd(lib, X, W, None, [_ad_vec(8, 128, 256)], Y) == -5
+    Wm = _m(256, 128)
+
+    def merge(ads, bias):
+        arr = (wpg.WpAdapter * max(1, len(ads)))(*ads)
+        return lib.lora_merge(ctypes.byref(Wm), ctypes.byref(bias) if bias is not None else None, arr,
+                              len(ads), 1.0, FAKE, 1 << 30, None)
+
+    assert merge([_ad_vec(8, 128, 256)], None) == -1                    # no bias to add it to
+    assert merge([_ad_vec(8, 128, 256)], _o(1, 255)) == -2              # bias numel != out
+    assert merge([_ad_vec(8, 128, 256)], wpg.WpOut(FAKE, wpg.WP_NF4, 1, 256, 256)) == -3
+    assert merge([_ad_vec(8, 128, 256, vec_dtype=7)], _o(1, 256)) == -3
+    # a vector whose s is zero asks for nothing: no bias needed, nothing launched
+    assert merge([_ad_vec(8, 128, 256, strength=0.0)], None) == 0
+
+
+def test_workspace_reserves_the_folded_bias(lib):
+    X, W = _m(1000, 128), _m(256, 128)
+    plain = (wpg.WpAdapter * 1)(_ad(8, 128, 256))
+    vec = (wpg.WpAdapter * 1)(_ad_vec(8, 128, 256))
+    a = lib.lora_workspace_size(wpg.WP_OP_FWD, ctypes.byref(X), ctypes.byref(W), plain, 1)
+    b = lib.lora_workspace_size(wpg.WP_OP_FWD, ctypes.byref(X), ctypes.byref(W), vec, 1)
+    assert b - a == 256 * 4 + (-(256 * 4) % 256)                          # fp32 [out], 256-byte rounded
