@@ -1253,6 +1253,36 @@ bool merge_layout(const wp_mat* W, const wp_adapter* ad, int n, double scale, Me
 int merge_pass(const void* P, long long ldp, const void* Q, long long ldq, long long rows, long long cols, int r,
                float s, const void* R, bool r_f32, long long ldr, void* Y, bool y_f32, long long ldy,
                cudaStream_t stream) {
+  const int nk = (r + kBK - 1) / kBK;
+  if (nk <= kMergeTileMaxK && cols % 8 == 0 && rows <= 0x7FFFFFFFLL && cols <= 0x7FFFFFFFLL) {
+    // r up to 256: a CTA per 128 x 128 output tile (merge_tile_kernel)
+    MergeTileMaps mm;
+    std::memset(&mm, 0, sizeof(mm));
+    int rc = make_map_bf16(&mm.p, P, r, rows, ldp, kBK, 128);
+    if (rc != WP_OK) return rc;
+    // residual and result of one dtype: both through the copy engine, 128-column tiles;
+    // otherwise each thread reads and writes its row, 256-column tiles
+    const bool staged = r_f32 == y_f32;
+    const int nt = staged ? 128 : (cols >= 256 ? 256 : 128);
+    rc = make_map_bf16(&mm.q, Q, r, cols, ldq, kBK, nt);
+    if (rc != WP_OK) return rc;
+    if (staged) {
+      const int dt = y_f32 ? WP_FP32 : WP_BF16, bx = y_f32 ? 32 : 64;
+      rc = make_map(&mm.r, dt, R, cols, rows, ldr, bx, 128);
+      if (rc != WP_OK) return rc;
+      rc = make_map(&mm.y, dt, Y, cols, rows, ldy, bx, 128);
+      if (rc != WP_OK) return rc;
+    }
+    MergeTileParams mp{};
+    mp.rows = static_cast<int>(rows); mp.cols = static_cast<int>(cols); mp.nk = nk; mp.s = s; mp.nt = nt;
+    mp.staged = staged ? 1 : 0;
+    mp.R = R; mp.ldr = ldr; mp.r_f32 = r_f32 ? 1 : 0;
+    mp.Y = Y; mp.ldy = ldy; mp.y_f32 = y_f32 ? 1 : 0;
+    mp.status = tc_status_ptr();
+    mp.timeout_ns = 2000000000ull;
+    if (!mp.status) return record_cuda();
+    return launch_merge_tile(mm, mp, stream);
+  }
   TcParams p{};
   TcMaps maps;
   std::memset(&maps, 0, sizeof(maps));

@@ -36,19 +36,22 @@ int check_launch() {
 
 }  // namespace
 
-// 64 x 64 tiles through shared memory; 256 threads.
+// 64 x 64 tiles through shared memory; 256 threads.  Both loops are unrolled so that a
+// thread's 16 loads are all in flight before its first shared-memory store.
 __global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* __restrict__ src,
                                                              long long ld_s, int R, int C,
                                                              uint16_t* __restrict__ dst,
                                                              long long ld_d) {
   __shared__ uint16_t tile[64][65];
   const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+#pragma unroll
   for (int i = threadIdx.x; i < 64 * 64; i += 256) {
     const int rr = i / 64, cc = i % 64;
     const int r = r0 + rr, c = c0 + cc;
     tile[rr][cc] = (r < R && c < C) ? src[(long long)r * ld_s + c] : 0;
   }
   __syncthreads();
+#pragma unroll
   for (int i = threadIdx.x; i < 64 * 64; i += 256) {
     const int cc = i / 64, rr = i % 64;
     const int r = r0 + rr, c = c0 + cc;

@@ -318,6 +318,30 @@ struct BiasFoldParams {
 };
 int launch_bias_fold(const BiasFoldParams& p, cudaStream_t stream);
 
+// One merge pass on 128 x 128 output tiles, a CTA each: Y = fl32(fl32(s * acc) + R) with
+// acc = P Q^T, P [rows, r] and Q [cols, r] bf16 K-major (r <= kMergeTileMaxK * 64), R and Y
+// [rows, cols] bf16 or fp32 (R may be Y), cols % 8 == 0, 16-byte aligned rows.
+constexpr int kMergeTileMaxK = 4;
+struct MergeTileParams {
+  int rows, cols, nk;          // output shape; 64-wide K blocks of r
+  int nt;                      // tile columns: 128 or 256 (the Q box's rows)
+  int staged;                  // R and Y of one dtype, nt = 128: R in and Y out by TMA
+  float s;
+  const void* R;
+  long long ldr;
+  int r_f32;
+  void* Y;
+  long long ldy;
+  int y_f32;
+  int* status;
+  unsigned long long timeout_ns;
+};
+struct MergeTileMaps {
+  CUtensorMap p, q;            // boxes of 64 K x 128 (P) / nt (Q) rows, 128-byte swizzle
+  CUtensorMap r, y;            // staged: boxes of 128 bytes x 128 rows, 128-byte swizzle
+};
+int launch_merge_tile(const MergeTileMaps& maps, const MergeTileParams& p, cudaStream_t stream);
+
 int launch_nf4_to_f32(const void* codes, const float* absmax, long long numel, const NF4Table& tab, float* U,
                       cudaStream_t stream);
 int launch_nf4_requant(const float* U, long long numel, const NF4Table& tab, void* codes, float* absmax,
