@@ -191,7 +191,9 @@ int lora_linear_fwd_host(const wp_mat* X_host, const wp_mat* W, const wp_mat* bi
  *   adapters: bf16 A [r, in], B [out, r]; strength 0 skips one; scale -1 undoes an earlier
  *   merge of the same adapters up to the roundings.
  *   workspace: lora_workspace_size(WP_OP_MERGE, NULL, W, adapters, n) bytes (A^T copies, and
- *   an fp32 [out, in] buffer for a 4-bit W or several adapters).
+ *   an fp32 [out, in] buffer for several adapters on a bf16 W, or for a 4-bit W with a rank
+ *   above 256; a 4-bit W with ranks up to 256 is dequantised, updated and requantised block by
+ *   block in one pass, with the same arithmetic).
  *   bias: the module's bias [out] (WP_BF16 or WP_FP32, device, rewritten in place) or NULL.
  *   The legacy vectors are added in fp32 in call order (each term fl32(s_p * v)) and the
  *   sum rounded once to the bias's dtype; for one adapter that is the dense patch's add.

@@ -1242,7 +1242,12 @@ bool merge_layout(const wp_mat* W, const wp_adapter* ad, int n, double scale, Me
     L->bp[i] = off;
     if (L->copy_b[i]) off += round256(static_cast<size_t>(out) * r8 * 2);
   }
-  L->need_u = W->dtype == WP_NF4 || L->n_eff > 1;
+  // the fp32 sum buffer: several adapters on a bf16 weight, or a 4-bit weight whose adapters
+  // do not all fit the one-pass merge (a rank above 256)
+  bool nf4_fused = W->dtype == WP_NF4;
+  for (int i = 0; i < n; ++i)
+    if ((ad[i].A.rows + kBK - 1) / kBK > kMergeTileMaxK) nf4_fused = false;
+  L->need_u = (W->dtype == WP_NF4 && !nf4_fused) || (W->dtype != WP_NF4 && L->n_eff > 1);
   L->u = off;
   if (L->need_u) off += round256(static_cast<size_t>(out) * in * 4);
   L->total = L->n_eff > 0 ? off : 0;
@@ -1262,8 +1267,9 @@ int merge_pass(const void* P, long long ldp, const void* Q, long long ldq, long 
     if (rc != WP_OK) return rc;
     // residual and result of one dtype: both through the copy engine, 128-column tiles;
     // otherwise each thread reads and writes its row, 256-column tiles
+    // (fp32 tiles 64 columns wide: two CTAs per SM still fit their 32 KiB residual tile)
     const bool staged = r_f32 == y_f32;
-    const int nt = staged ? 128 : (cols >= 256 ? 256 : 128);
+    const int nt = staged ? (y_f32 ? 64 : 128) : (cols >= 256 ? 256 : 128);
     rc = make_map_bf16(&mm.q, Q, r, cols, ldq, kBK, nt);
     if (rc != WP_OK) return rc;
     if (staged) {
@@ -1369,8 +1375,15 @@ int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n,
   void* wdata = const_cast<void*>(W->data);        // the weight is updated in place
   NF4Table tab;
   int rc = WP_OK;
-  if (nf4) {
-    nf4_codebook_host(tab.level);
+  // a 4-bit weight with every adapter's rank up to 256: one pass (merge_nf4_kernel) that
+  // dequantises, adds the adapters and requantises each block in registers
+  bool fused = nf4;
+  for (int i = 0; i < n && fused; ++i)
+    if (s_of[i] != 0.0f && (ad[i].A.rows + kBK - 1) / kBK > kMergeTileMaxK) fused = false;
+  MergeNF4Maps fm;
+  MergeNF4Params fp{};
+  if (nf4) nf4_codebook_host(tab.level);
+  if (nf4 && !fused) {
     rc = launch_nf4_to_f32(W->data, W->absmax, out * in, tab, U, stream);
     if (rc != WP_OK) return rc;
   }
@@ -1394,6 +1407,17 @@ int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n,
     }
     ++done;
     const bool first = done == 1, last = done == L.n_eff;
+    if (fused) {
+      const int k = fp.n++;
+      rc = make_map_bf16(&fm.p[k], bp, r, out, ldb, kBK, 128);
+      if (rc != WP_OK) return rc;
+      rc = make_map_bf16(&fm.q[k], at, r, in, r8, kBK, 64);
+      if (rc != WP_OK) return rc;
+      fp.nk[k] = (r + kBK - 1) / kBK;
+      fp.nk_max = std::max(fp.nk_max, fp.nk[k]);
+      fp.s[k] = s_of[i];
+      continue;
+    }
     if (nf4) {
       rc = merge_pass(bp, ldb, at, r8, out, in, r, s_of[i], U, true, in, U, true, in, stream);
     } else if (L.n_eff == 1) {
@@ -1406,7 +1430,19 @@ int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n,
     }
     if (rc != WP_OK) return rc;
   }
-  if (nf4) rc = launch_nf4_requant(U, out * in, tab, wdata, const_cast<float*>(W->absmax), stream);
+  if (fused) {
+    fp.rows = static_cast<int>(out);
+    fp.cols = static_cast<int>(in);
+    fp.codes = static_cast<uint8_t*>(wdata);
+    fp.absmax = const_cast<float*>(W->absmax);
+    fp.tab = tab;
+    fp.status = tc_status_ptr();
+    fp.timeout_ns = 2000000000ull;
+    if (!fp.status) return record_cuda();
+    rc = launch_merge_nf4(fm, fp, stream);
+  } else if (nf4) {
+    rc = launch_nf4_requant(U, out * in, tab, wdata, const_cast<float*>(W->absmax), stream);
+  }
   if (rc == WP_OK && fold.n > 0) {
     // bias <- bias + sum_p s_p bias_B_p, rounded once to the bias's dtype
     fold.bias = bias->data;

@@ -324,8 +324,8 @@ int launch_bias_fold(const BiasFoldParams& p, cudaStream_t stream);
 constexpr int kMergeTileMaxK = 4;
 struct MergeTileParams {
   int rows, cols, nk;          // output shape; 64-wide K blocks of r
-  int nt;                      // tile columns: 128 or 256 (the Q box's rows)
-  int staged;                  // R and Y of one dtype, nt = 128: R in and Y out by TMA
+  int nt;                      // tile columns: 64, 128 or 256 (the Q box's rows)
+  int staged;                  // R and Y of one dtype (nt 64 or 128): R in and Y out by TMA
   float s;
   const void* R;
   long long ldr;
@@ -341,6 +341,27 @@ struct MergeTileMaps {
   CUtensorMap r, y;            // staged: boxes of 128 bytes x 128 rows, 128-byte swizzle
 };
 int launch_merge_tile(const MergeTileMaps& maps, const MergeTileParams& p, cudaStream_t stream);
+
+// A whole 4-bit merge in one pass (ranks up to kMergeTileMaxK * 64): a CTA per 128 rows x 64
+// columns, a thread per 64-element block: W_eff = bf16(fl32(level[q]) * absmax) in registers,
+// u = fl32(fl32(s_p * acc_p) + u) for each adapter in call order (acc_p = B_p A_p on the tensor
+// cores), then the block requantised as nf4_requant_kernel does and written in place.
+struct MergeNF4Params {
+  int rows, cols;              // W [rows, cols], cols % 64 == 0
+  uint8_t* codes;              // [rows, cols / 2], rewritten
+  float* absmax;               // [rows * cols / 64], rewritten
+  NF4Table tab;
+  int n, nk_max;               // adapters (non-zero s), the most K blocks of any of them
+  int nk[kMaxAd];
+  float s[kMaxAd];
+  int* status;
+  unsigned long long timeout_ns;
+};
+struct MergeNF4Maps {
+  CUtensorMap p[kMaxAd];       // B_p [rows, r_p]: boxes of 64 K x 128 rows
+  CUtensorMap q[kMaxAd];       // A_p^T [cols, r_p]: boxes of 64 K x 64 rows
+};
+int launch_merge_nf4(const MergeNF4Maps& maps, const MergeNF4Params& p, cudaStream_t stream);
 
 int launch_nf4_to_f32(const void* codes, const float* absmax, long long numel, const NF4Table& tab, float* U,
                       cudaStream_t stream);

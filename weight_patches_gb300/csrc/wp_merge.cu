@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include "wp_internal.h"
+#include "wp_nf4.cuh"
 #include "wp_ptx.cuh"
 
 namespace wp {
@@ -76,10 +77,7 @@ __global__ void __launch_bounds__(256) nf4_requant_kernel(const float* U, long l
     for (int i = 0; i < 8; ++i) {
       uint32_t q = 7;                                   // level 0 for an all-zero block
       if (m > 0.f) {
-        const float x = __fdiv_rn(v[i], m);
-        q = 0;
-#pragma unroll
-        for (int k = 0; k < 15; ++k) q += x > mid[k] ? 1u : 0u;
+        q = nf4_code_of(__fdiv_rn(v[i], m), mid);
       }
       // element 2b in the high nibble of byte b
       c4 |= q << (8 * (i >> 1) + ((i & 1) ? 0 : 4));

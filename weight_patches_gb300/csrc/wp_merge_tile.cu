@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include "wp_internal.h"
+#include "wp_nf4.cuh"
 #include "wp_ptx.cuh"
 
 namespace wp {
@@ -32,7 +33,7 @@ __device__ __forceinline__ void lds128(uint32_t addr, uint32_t (&w)[4]) {
 constexpr int kMT = 128;                          // tile rows
 constexpr int kMTBox = kMT * kBK * 2;             // one 128-row x 64-K bf16 operand box: 16 KiB
 
-// NT: tile columns (128 or 256), the MMA's N and the tensor-memory columns a CTA holds
+// NT: tile columns (64, 128 or 256), the MMA's N and the tensor-memory columns a CTA holds
 template <int NT>
 __global__ void __launch_bounds__(128) merge_tile_kernel(const __grid_constant__ MergeTileMaps maps,
                                                          const __grid_constant__ MergeTileParams p) {
@@ -272,12 +273,198 @@ int launch_nt(const MergeTileMaps& maps, const MergeTileParams& p, cudaStream_t 
 
 }  // namespace
 
+namespace {
+
+constexpr int kMNBoxP = 128 * kBK * 2;            // 128 B_p rows x 64 K: 16 KiB
+constexpr int kMNBoxQ = 64 * kBK * 2;             // 64 A_p^T rows x 64 K: 8 KiB
+
+__device__ __forceinline__ float nf4_weff(float level, float am) {
+  // W_eff = bf16(fl32(level) * absmax), as a float
+  uint16_t h;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(level * am));
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+__global__ void __launch_bounds__(128) merge_nf4_kernel(const __grid_constant__ MergeNF4Maps maps,
+                                                        const __grid_constant__ MergeNF4Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* sbase = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* sP = sbase;                            // [nk_max] boxes of B_p rows
+  uint8_t* sQ = sbase + p.nk_max * kMNBoxP;       // [nk_max] boxes of A_p^T rows
+  uint64_t* full = reinterpret_cast<uint64_t*>(sQ + p.nk_max * kMNBoxQ);     // one phase per adapter
+  uint64_t* done = full + 1;                      // one phase per adapter
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int blk = blockIdx.x;                     // the 64-column block
+  const int row0 = blockIdx.y * 128, col0 = blk * 64;
+  if (threadIdx.x == 0) {
+    mbar_init(full, 1);
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 64);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+
+  // this thread's block: row row0 + t, columns [col0, col0 + 64), dequantised to W_eff
+  const int row = row0 + static_cast<int>(threadIdx.x);
+  const bool row_ok = row < p.rows;
+  const long long cb = static_cast<long long>(p.cols) / 64;        // blocks per row
+  uint8_t* crow = p.codes + (static_cast<long long>(row_ok ? row : 0) * p.cols + col0) / 2;
+  float u[64];
+  {
+    uint4 c0 = make_uint4(0, 0, 0, 0), c1 = make_uint4(0, 0, 0, 0);
+    float am = 0.f;
+    if (row_ok) {
+      c0 = reinterpret_cast<const uint4*>(crow)[0];
+      c1 = reinterpret_cast<const uint4*>(crow)[1];
+      am = p.absmax[static_cast<long long>(row) * cb + blk];
+    }
+    const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int w = 0; w < 8; ++w)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        // byte 4w + b: element 2(4w + b) in the high nibble, the next in the low nibble
+        const uint32_t byte = (cw[w] >> (8 * b)) & 0xffu;
+        u[8 * w + 2 * b] = nf4_weff(p.tab.level[byte >> 4], am);
+        u[8 * w + 2 * b + 1] = nf4_weff(p.tab.level[byte & 0xfu], am);
+      }
+  }
+
+  // each adapter in call order: operands by TMA, the MMAs, u = fl32(fl32(s * acc) + u).  Every
+  // thread walks every adapter (the barriers below are uniform); after an abort nothing is
+  // issued or read
+  bool ok = true;
+  uint32_t armed = 0, committed = 0;              // thread 0: phases of full / done it started
+  for (int a = 0; a < p.n; ++a) {
+    const uint32_t par = static_cast<uint32_t>(a & 1);
+    if (threadIdx.x == 0 && !*abort_flag) {
+      const uint64_t keep = l2_evict_last();
+      mbar_arrive_expect_tx(full, static_cast<uint32_t>(p.nk[a]) * (kMNBoxP + kMNBoxQ));
+      ++armed;
+      for (int kb = 0; kb < p.nk[a]; ++kb) {
+        tma_load_2d_hint(sP + kb * kMNBoxP, &maps.p[a], kb * kBK, row0, full, keep);
+        tma_load_2d_hint(sQ + kb * kMNBoxQ, &maps.q[a], kb * kBK, col0, full, keep);
+      }
+      if (mbar_wait(full, par, abort_flag, p.timeout_ns, p.status)) {
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(128, 64);
+        for (int kb = 0; kb < p.nk[a]; ++kb) {
+          const uint64_t ad = sw128_kmajor_desc(smem_u32(sP + kb * kMNBoxP));
+          const uint64_t bd = sw128_kmajor_desc(smem_u32(sQ + kb * kMNBoxQ));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+        }
+        mma_commit(done);
+        ++committed;
+      }
+    }
+    ok = ok && __all_sync(0xffffffffu, mbar_wait(done, par, abort_flag, p.timeout_ns, p.status));
+    tc_fence_after();
+    if (ok) {
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tmem + lane_base, r0);
+      tmem_ld32(tmem + lane_base + 32, r1);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        u[i] = __fadd_rn(__fmul_rn(__uint_as_float(r0[i]), p.s[a]), u[i]);
+        u[32 + i] = __fadd_rn(__fmul_rn(__uint_as_float(r1[i]), p.s[a]), u[32 + i]);
+      }
+    }
+    // tensor memory and the operand tiles are free for the next adapter
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+
+  if (ok && row_ok && !*abort_flag) {
+    // requantise the block: absmax' = max |u|, x = fl32(u / absmax'), code = the number of
+    // level midpoints x exceeds (an all-zero block keeps scale 0 and level 0's code)
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(u[i]));
+    float mid[15];
+#pragma unroll
+    for (int k = 0; k < 15; ++k) mid[k] = __fmul_rn(__fadd_rn(p.tab.level[k], p.tab.level[k + 1]), 0.5f);
+    uint32_t cw[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      uint32_t c4 = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t q = 7;
+        if (m > 0.f) {
+          q = nf4_code_of(__fdiv_rn(u[8 * w + i], m), mid);
+        }
+        c4 |= q << (8 * (i >> 1) + ((i & 1) ? 0 : 4));
+      }
+      cw[w] = c4;
+    }
+    reinterpret_cast<uint4*>(crow)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    reinterpret_cast<uint4*>(crow)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    p.absmax[static_cast<long long>(row) * cb + blk] = m;
+  }
+
+  if (threadIdx.x == 0 && *abort_flag) {
+    // after a timed-out wait: the last copies and MMAs started finish before the exit
+    const uint64_t t0 = globaltimer_ns();
+    if (armed > 0)
+      while (!mbar_try_wait(smem_u32(full), (armed - 1) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
+      }
+    if (committed > 0)
+      while (!mbar_try_wait(smem_u32(done), (committed - 1) & 1u) && globaltimer_ns() - t0 < 200000000ull) {
+      }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+}
+
+}  // namespace
+
+int launch_merge_nf4(const MergeNF4Maps& maps, const MergeNF4Params& p, cudaStream_t stream) {
+  if (p.rows <= 0 || p.cols <= 0 || p.n <= 0) return WP_OK;
+  if (p.n > kMaxAd || p.nk_max < 1 || p.nk_max > kMergeTileMaxK || p.cols % 64 != 0) return WP_ERR_UNSUPPORTED;
+  size_t smem = 1024 + static_cast<size_t>(p.nk_max) * (kMNBoxP + kMNBoxQ) + 64;
+  const size_t floor = 228 * 1024 / 8 - 1024;    // at most 8 CTAs of 64 TMEM columns per SM
+  if (smem < floor) smem = floor;
+  cudaError_t e = cudaFuncSetAttribute(merge_nf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e == cudaSuccess) {
+    const dim3 grid(p.cols / 64, (p.rows + 127) / 128);
+    merge_nf4_kernel<<<grid, 128, smem, stream>>>(maps, p);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    return WP_ERR_CUDA;
+  }
+  return WP_OK;
+}
+
 int launch_merge_tile(const MergeTileMaps& maps, const MergeTileParams& p, cudaStream_t stream) {
   if (p.rows <= 0 || p.cols <= 0) return WP_OK;
-  if (p.nk < 1 || p.nk > kMergeTileMaxK || p.cols % 8 != 0 || (p.nt != 128 && p.nt != 256) ||
-      (p.staged && (p.nt != 128 || p.r_f32 != p.y_f32)))
+  if (p.nk < 1 || p.nk > kMergeTileMaxK || p.cols % 8 != 0 || (p.nt != 64 && p.nt != 128 && p.nt != 256) ||
+      (p.staged && (p.nt == 256 || p.r_f32 != p.y_f32)))
     return WP_ERR_UNSUPPORTED;
-  return p.nt == 256 ? launch_nt<256>(maps, p, stream) : launch_nt<128>(maps, p, stream);
+  return p.nt == 256 ? launch_nt<256>(maps, p, stream)
+       : p.nt == 128 ? launch_nt<128>(maps, p, stream)
+                     : launch_nt<64>(maps, p, stream);
 }
 
 }  // namespace wp

@@ -79,4 +79,17 @@ __device__ __forceinline__ void nf4_dequant_row(const uint8_t* row, int unit0, i
   }
 }
 
+// The 4-bit code of x = u / absmax' (the nearest level): the number of level midpoints
+// mid[k] = fl32((level[k] + level[k+1]) / 2) below x, a value on a midpoint taking the lower
+// code; found by binary search over the increasing midpoints (four comparisons).
+__device__ __forceinline__ uint32_t nf4_code_of(float x, const float (&mid)[15]) {
+  uint32_t q = x > mid[7] ? 8u : 0u;
+  q += x > (q ? mid[11] : mid[3]) ? 4u : 0u;
+  const float t2 = (q & 8u) ? ((q & 4u) ? mid[13] : mid[9]) : ((q & 4u) ? mid[5] : mid[1]);
+  q += x > t2 ? 2u : 0u;
+  const float t10 = (q & 2u) ? ((q & 4u) ? mid[6] : mid[2]) : ((q & 4u) ? mid[4] : mid[0]);
+  const float t11 = (q & 2u) ? ((q & 4u) ? mid[14] : mid[10]) : ((q & 4u) ? mid[12] : mid[8]);
+  return q + (x > ((q & 8u) ? t11 : t10) ? 1u : 0u);
+}
+
 }  // namespace wp
