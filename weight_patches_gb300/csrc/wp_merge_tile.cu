@@ -278,13 +278,6 @@ namespace {
 constexpr int kMNBoxP = 128 * kBK * 2;            // 128 B_p rows x 64 K: 16 KiB
 constexpr int kMNBoxQ = 64 * kBK * 2;             // 64 A_p^T rows x 64 K: 8 KiB
 
-__device__ __forceinline__ float nf4_weff(float level, float am) {
-  // W_eff = bf16(fl32(level) * absmax), as a float
-  uint16_t h;
-  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(level * am));
-  return __uint_as_float(static_cast<uint32_t>(h) << 16);
-}
-
 __global__ void __launch_bounds__(128) merge_nf4_kernel(const __grid_constant__ MergeNF4Maps maps,
                                                         const __grid_constant__ MergeNF4Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -331,15 +324,10 @@ __global__ void __launch_bounds__(128) merge_nf4_kernel(const __grid_constant__ 
       am = p.absmax[static_cast<long long>(row) * cb + blk];
     }
     const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    float lv[16];
 #pragma unroll
-    for (int w = 0; w < 8; ++w)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        // byte 4w + b: element 2(4w + b) in the high nibble, the next in the low nibble
-        const uint32_t byte = (cw[w] >> (8 * b)) & 0xffu;
-        u[8 * w + 2 * b] = nf4_weff(p.tab.level[byte >> 4], am);
-        u[8 * w + 2 * b + 1] = nf4_weff(p.tab.level[byte & 0xfu], am);
-      }
+    for (int k = 0; k < 16; ++k) lv[k] = p.tab.level[k];
+    nf4_dequant_regs(cw, am, lv, u);
   }
 
   // each adapter in call order: operands by TMA, the MMAs, u = fl32(fl32(s * acc) + u).  Every

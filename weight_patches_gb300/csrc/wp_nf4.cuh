@@ -79,6 +79,36 @@ __device__ __forceinline__ void nf4_dequant_row(const uint8_t* row, int unit0, i
   }
 }
 
+// All 64 elements of one block into registers as floats (the bf16 values W_eff), from its 32
+// code bytes as stored (cw[0..7], byte k: element 2k in the high nibble), its scale and the 16
+// levels: the same table and byte-permute lookups as nf4_dequant_row.
+__device__ __forceinline__ void nf4_dequant_regs(const uint32_t (&cw)[8], float am, const float (&lv)[16],
+                                                 float (&u)[64]) {
+  uint32_t e[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) e[k] = pack_bf16x2(lv[2 * k] * am, lv[2 * k + 1] * am);
+  uint32_t lo[4], hi[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    lo[j] = prmt(e[2 * j], e[2 * j + 1], 0x6420u);
+    hi[j] = prmt(e[2 * j], e[2 * j + 1], 0x7531u);
+  }
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint32_t c = cw[w];
+    const uint32_t sel = c & 0x77777777u;
+    const uint32_t pick = ((c >> 1) & 0x44444444u) | 0x32103210u;
+    uint32_t o[4];
+    lookup4(sel, pick, lo, hi, o[0], o[1]);
+    lookup4(sel >> 16, pick >> 16, lo, hi, o[2], o[3]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      u[8 * w + 2 * k] = __uint_as_float(o[k] << 16);
+      u[8 * w + 2 * k + 1] = __uint_as_float(o[k] & 0xffff0000u);
+    }
+  }
+}
+
 // The 4-bit code of x = u / absmax' (the nearest level): the number of level midpoints
 // mid[k] = fl32((level[k] + level[k+1]) / 2) below x, a value on a midpoint taking the lower
 // code; found by binary search over the increasing midpoints (four comparisons).
