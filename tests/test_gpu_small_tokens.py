@@ -6,7 +6,7 @@ hand-over to the general path.
 InvokeAI sidecar-patch article, section 五: quantised layers under few tokens go through a
 small-batch kernel; here both bf16 and 4-bit weights do, with the LoRA terms fused in.
 Covered: one token, ragged token counts, ragged weight rows, 4-bit weights with and
-without TMA-fed block scales, stacked column groups, delta-only layers, several adapters,
+without TMA-fed block scales, one to four tokens on the CUDA-core kernel (many K splits), stacked column groups, delta-only layers, several adapters,
 bias, fp32 output, zero strength, and full-size layers of the workloads (sampled output
 columns)."""
 import numpy as np
@@ -61,6 +61,25 @@ def test_nf4_weight(T, K, N):
     _check(_layer(T, K, N, [16], kind="nf4", seed=T + K))
 
 
+@pytest.mark.parametrize("T,K,N,ranks", [(1, 1024, 200, [8]), (2, 768, 264, [24, 16]), (3, 2048, 96, [16]),
+                                          (4, 512, 384, [40]), (1, 14336, 264, [16]), (4, 14336, 130, [8, 8])])
+def test_nf4_cuda_core_tokens(T, K, N, ranks):
+    """One to four tokens with a 4-bit weight and K a multiple of 256 go to the CUDA-core
+    kernel: ragged weight rows (the last 32-row group part-filled), ranks that are not
+    multiples of 16, several adapters, a bias, and long rows split into many K ranges (more
+    than eight splits for K = 14336)."""
+    _check(_layer(T, K, N, ranks, kind="nf4", bias="bf16", seed=T * 7 + K + N))
+
+
+def test_nf4_cuda_core_grouped_fp32_out():
+    """Stacked gate/up groups with their own adapters, fp32 output, a request scale, one token
+    through four."""
+    for T in (1, 4):
+        lin = _layer(T, 512, 2 * 200, [16, 8], kind="nf4", groups=2, strengths=[0.5, 1.5], seed=40 + T)
+        lin.request_scale = 0.75
+        _check(lin, out_dtype=torch.float32)
+
+
 def test_grouped_qkv():
     _check(_layer(3, 320, 3 * 320, [32, 32, 32], groups=3, seed=3))
 
@@ -87,11 +106,12 @@ def test_zero_strength_equals_base():
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
 
 
-@pytest.mark.parametrize("cfg,T", [("c1", 4), ("c3", 1), ("c3", 64)])
+@pytest.mark.parametrize("cfg,T", [("c1", 4), ("c3", 1), ("c3", 4), ("c3", 64), ("c3down", 1), ("c3down", 3)])
 def test_full_size_layers(cfg, T):
     """Full-size weights of the workloads with few tokens; the oracle checks 256 sampled
     output columns (weight rows decoded one block at a time)."""
-    lin = workloads.config1("full") if cfg == "c1" else workloads.config3("full")[0]
+    lin = {"c1": lambda: workloads.config1("full"), "c3": lambda: workloads.config3("full")[0],
+           "c3down": lambda: workloads.config3("full")[1]}[cfg]()
     X = lin.X.slice_rows(0, T)
     small = workloads.Linear(lin.name, X, lin.W, lin.bias, lin.patches, lin.request_scale, lin.groups)
     Y = gu.run_fwd(small)

@@ -84,7 +84,8 @@ int make_map_u8(CUtensorMap* m, const void* ptr, long long inner_bytes, long lon
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swizzle == 64   ? CU_TENSOR_MAP_SWIZZLE_64B
+                  swizzle == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                  : swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                   : swizzle == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
                                   : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -144,7 +145,42 @@ struct SkinnyPlan {
   int kkb = 1;                 // 64-wide K blocks per pipeline step
   long long N = 0;
   size_t part_bytes = 0;
+  // one to four tokens against a 4-bit weight: the CUDA-core kernel (wp_gemv.cu)
+  bool gemv = false;
+  int g_splits = 1, g_ks_len = 0, g_grid = 0;
+  size_t g_smem = 0;
 };
+
+// The split of K for the CUDA-core small-token kernel: each block holds the fp32 X of its
+// split, so a split is at most kGemvXBudget / T elements; among those, the split whose
+// busiest warp streams the fewest elements (32-row groups x split length), fewer splits on a
+// tie.  The grid is a multiple of the splits.
+bool plan_gemv(long long T, long long K, long long N, SkinnyPlan* sp) {
+  const int kb = static_cast<int>(K / kGemvStageK);
+  const int ngW = static_cast<int>((N + 31) / 32);
+  const int sms = device_sm_count();
+  long long best = -1;
+  for (int s_try = 1; s_try <= kGemvMaxSplits && s_try <= kb; ++s_try) {
+    const int ks_len = (kb + s_try - 1) / s_try * kGemvStageK;
+    if (T * ks_len > kGemvXBudget) continue;
+    const int splits = static_cast<int>((K + ks_len - 1) / ks_len);
+    const size_t smem = gemv_smem_bytes(static_cast<int>(T), ks_len);
+    const int per_sm = gemv_blocks_per_sm(static_cast<int>(T), smem);
+    if (per_sm < 1) continue;
+    const int nbs = sms * per_sm / splits;
+    if (nbs < 1) continue;
+    const long long rounds = (ngW + nbs * kGemvWarps - 1) / (nbs * kGemvWarps);
+    const long long cost = rounds * ks_len;
+    if (best < 0 || cost < best) {
+      best = cost;
+      sp->g_splits = splits;
+      sp->g_ks_len = ks_len;
+      sp->g_grid = nbs * splits;
+      sp->g_smem = smem;
+    }
+  }
+  return best >= 0;
+}
 
 // It serves 4-bit weights up to 64 tokens; a bf16 weight (or none) only up to 4 tokens:
 // beyond that the general path, whose tiles read a bf16 weight without dequantisation,
@@ -191,6 +227,11 @@ bool plan_skinny(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int n, 
   sp->splits = (sp->k_blocks + sp->kbps - 1) / sp->kbps;
   sp->units = rows * sp->splits;
   sp->part_bytes = round256(static_cast<size_t>(sp->splits) * T * (N + R16) * 4);
+  if (W && W->dtype == WP_NF4 && T <= kGemvMaxT && K % kGemvStageK == 0 && plan_gemv(T, K, N, sp)) {
+    sp->gemv = true;
+    sp->part_bytes =
+        std::max(sp->part_bytes, round256(static_cast<size_t>(sp->g_splits) * T * (N + R16) * 4));
+  }
   sp->use = true;
   return true;
 }
@@ -296,6 +337,38 @@ int skinny_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, boo
   }
   p.n_ad = n_adapters;
   p.a_off[n_adapters] = toff;
+
+  if (sp.gemv && aligned16(W->absmax)) {
+    GemvParams g{};
+    g.T = static_cast<int>(T); g.K = static_cast<int>(K); g.N = static_cast<int>(N);
+    g.splits = sp.g_splits; g.ks_len = sp.g_ks_len;
+    g.ngW = static_cast<int>((N + 31) / 32);
+    g.R16 = sp.R16;
+    g.n_ad = n_adapters;
+    for (int i = 0; i < n_adapters; ++i) {
+      g.a_off[i] = p.a_off[i];
+      g.rank[i] = static_cast<int>(adapters[i].A.rows);
+      g.A[i] = static_cast<const uint16_t*>(adapters[i].A.data);
+      g.lda[i] = adapters[i].A.ld;
+    }
+    g.a_off[n_adapters] = toff;
+    nf4_codebook_host(g.nf4_code);
+    g.X = static_cast<const uint16_t*>(X->data); g.ldx = X->ld;
+    g.part = part; g.ldp = q.ldp;
+    g.status = tc_status_ptr();
+    g.timeout_ns = 2000000000ull;
+    if (!g.status) return record_cuda();
+    GemvMaps gm;
+    std::memset(&gm, 0, sizeof(gm));
+    int rc = make_map_u8(&gm.wq, W->data, K / 2, N, K / 2, kGemvStageK / 2, 32, 128);
+    if (rc != WP_OK) return rc;
+    rc = make_map(&gm.am, WP_FP32, W->absmax, K / 64, N, K / 64, kGemvStageK / 64, 32, /*swizzle=*/0);
+    if (rc != WP_OK) return rc;
+    rc = launch_gemv(gm, g, sp.g_grid, sp.g_smem, stream);
+    if (rc != WP_OK) return rc;
+    q.splits = sp.g_splits;
+    return launch_skinny_reduce(q, stream);
+  }
 
   SkinnyMaps maps;
   std::memset(&maps, 0, sizeof(maps));

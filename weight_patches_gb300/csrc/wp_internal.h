@@ -201,6 +201,48 @@ int launch_skinny(const SkinnyMaps& maps, const SkinnyParams& p, size_t smem_byt
                   cudaStream_t stream);
 int launch_skinny_reduce(const SkinnyReduceParams& q, cudaStream_t stream);
 int skinny_grid_ctas(size_t smem_bytes, bool nf4);
+
+// One to four tokens against a 4-bit weight on the CUDA cores (wp_gemv.cu): each warp streams
+// 32 weight rows, one per lane, through its own ring of TMA stages (256 K elements of 32 rows:
+// 4 KiB of codes in the 128-byte swizzle and 512 B of block scales); X of the block's K range
+// waits in shared memory as bf16.  It writes the partial sums skinny_reduce_kernel reads: the
+// W rows at [split][t][n], the adapters' A rows at [split][t][N + a_off + j].
+constexpr int kGemvMaxT = 4;
+constexpr int kGemvWarps = 4;
+constexpr int kGemvStages = 3;
+constexpr int kGemvMaxSplits = 32;
+constexpr int kGemvStageK = 256;
+constexpr int kGemvCodeBytes = 32 * kGemvStageK / 2;   // 4 KiB
+constexpr int kGemvAmBytes = 32 * kGemvStageK / 64 * 4;  // 512 B
+constexpr int kGemvXBudget = 16384;                      // bf16 X elements a block holds (32 KiB)
+
+struct GemvParams {
+  int T, K, N;
+  int splits, ks_len;          // K elements per split (a multiple of 256; the last one shorter)
+  int ngW;                     // 32-row groups of W
+  int R16;                     // A rows, each adapter padded to 16 (rows past the rank write 0)
+  int n_ad;
+  int a_off[kMaxAd + 1];
+  int rank[kMaxAd];
+  const uint16_t* A[kMaxAd];
+  long long lda[kMaxAd];
+  float nf4_code[16];
+  const uint16_t* X;
+  long long ldx;
+  float* part;                 // [splits][T][ldp]
+  long long ldp;
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+struct GemvMaps {
+  CUtensorMap wq;              // codes [N, K/2] u8, boxes of 128 B x 32 rows, 128-byte swizzle
+  CUtensorMap am;              // block scales [N, K/64] fp32, boxes of 4 x 32 rows
+};
+
+size_t gemv_smem_bytes(int T, int ks_len);
+int gemv_blocks_per_sm(int T, size_t smem_bytes);
+int launch_gemv(const GemvMaps& maps, const GemvParams& p, int grid, size_t smem_bytes, cudaStream_t stream);
 int* tc_status_ptr();
 
 int tc_max_pairs(size_t smem_bytes, bool nf4);

@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
 // broadcast.  Launched as a programmatic dependent of skinny_kernel: everything before the
 // dependency wait overlaps the end of that kernel.
 constexpr int kReduceT = 16;
-constexpr int kMaxSplits = 8;                 // the host never splits K further
+constexpr int kMaxSplits = 8;                 // partial sums loaded together per round
 
 __global__ void __launch_bounds__(256) skinny_reduce_kernel(const SkinnyReduceParams q) {
   __shared__ __align__(16) uint16_t hs[kReduceT * kHCols];
@@ -432,12 +432,15 @@ __global__ void __launch_bounds__(256) skinny_reduce_kernel(const SkinnyReducePa
     const int t = idx / q.R16;
     const int j = idx - t * q.R16;
     // the splits' loads are independent: issued together, summed in order
-    float hv[kMaxSplits];
-#pragma unroll
-    for (int ks = 0; ks < kMaxSplits; ++ks) hv[ks] = ks < q.splits ? part[ks * sstride + t * q.ldp + q.N + j] : 0.f;
     float h = 0.f;
+    for (int ks0 = 0; ks0 < q.splits; ks0 += kMaxSplits) {
+      float hv[kMaxSplits];
 #pragma unroll
-    for (int ks = 0; ks < kMaxSplits; ++ks) h += hv[ks];
+      for (int ks = 0; ks < kMaxSplits; ++ks)
+        hv[ks] = ks0 + ks < q.splits ? part[(ks0 + ks) * sstride + t * q.ldp + q.N + j] : 0.f;
+#pragma unroll
+      for (int ks = 0; ks < kMaxSplits; ++ks) h += hv[ks];
+    }
     float s = 0.f;
     for (int a = 0; a < q.n_ad; ++a)
       if (j >= q.ad[a].toff && j < q.ad[a].toff + q.ad[a].rank) s = q.ad[a].s;
@@ -451,12 +454,14 @@ __global__ void __launch_bounds__(256) skinny_reduce_kernel(const SkinnyReducePa
 #pragma unroll
   for (int t = 0; t < kReduceT; ++t) acc[t] = 0.f;
   if (q.has_w) {
+    for (int ks0 = 0; ks0 < q.splits; ks0 += kMaxSplits) {
 #pragma unroll
-    for (int ks = 0; ks < kMaxSplits; ++ks) {
-      if (ks < q.splits) {
+      for (int ks = 0; ks < kMaxSplits; ++ks) {
+        if (ks0 + ks < q.splits) {
 #pragma unroll
-        for (int t = 0; t < kReduceT; ++t)
-          if (t < nt) acc[t] += part[ks * sstride + t * q.ldp + n];
+          for (int t = 0; t < kReduceT; ++t)
+            if (t < nt) acc[t] += part[(ks0 + ks) * sstride + t * q.ldp + n];
+        }
       }
     }
   }
