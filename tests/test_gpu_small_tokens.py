@@ -80,6 +80,24 @@ def test_nf4_cuda_core_grouped_fp32_out():
         _check(lin, out_dtype=torch.float32)
 
 
+@pytest.mark.parametrize("T", [1, 3])
+def test_nf4_unaligned_scales_few_tokens(T):
+    """Block scales that do not start on a 16-byte boundary cannot be copied by TMA: one to four
+    tokens then fall back to the tensor-core small-token path, which reads the scales from
+    global memory, within the same gates."""
+    lin = _layer(T, 512, 200, [16], kind="nf4", seed=70 + T)
+    W = gu.dev(lin.W)
+    buf = torch.zeros(W.absmax.numel() + 1, dtype=torch.float32, device=W.absmax.device)
+    buf[1:] = W.absmax
+    W_off = wpg.NF4Weight(W.packed, buf[1:], W.rows, W.cols)
+    assert W_off.absmax.data_ptr() % 16 != 0
+    Y = wpg.lora_linear_fwd(gu.dev(lin.X), W_off, None, gu.adapters(lin), lin.request_scale)
+    torch.cuda.synchronize()
+    assert wpg.lora_device_status() == 0
+    err, chain = gu.errors(lin, Y)
+    assert err <= BF16_TOL and err <= chain, (err, chain)
+
+
 def test_grouped_qkv():
     _check(_layer(3, 320, 3 * 320, [32, 32, 32], groups=3, seed=3))
 
