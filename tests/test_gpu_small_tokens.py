@@ -6,7 +6,8 @@ hand-over to the general path.
 InvokeAI sidecar-patch article, section 五: quantised layers under few tokens go through a
 small-batch kernel; here both bf16 and 4-bit weights do, with the LoRA terms fused in.
 Covered: one token, ragged token counts, ragged weight rows, 4-bit weights with and
-without TMA-fed block scales, one to four tokens on the CUDA-core kernel (many K splits), stacked column groups, delta-only layers, several adapters,
+without TMA-fed block scales, one to four tokens on the CUDA-core kernel (4-bit and bf16,
+many K splits), stacked column groups, delta-only layers, several adapters,
 bias, fp32 output, zero strength, and full-size layers of the workloads (sampled output
 columns)."""
 import numpy as np
@@ -51,8 +52,11 @@ def _check(lin, out_dtype=torch.bfloat16):
 
 
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 16])
-def test_bf16_weight(T):
-    _check(_layer(T, 256, 320, [16], bias="bf16", seed=T))
+@pytest.mark.parametrize("K", [256, 320])
+def test_bf16_weight(T, K):
+    """K = 256: one to four tokens on the CUDA-core kernel; K = 320 (not a multiple of 256):
+    the tensor-core small-token path; five and more tokens: the general path."""
+    _check(_layer(T, K, 320, [16], bias="bf16", seed=T + K))
 
 
 @pytest.mark.parametrize("T,K,N", [(1, 512, 384), (33, 512, 384), (20, 320, 200), (64, 256, 264)])
@@ -61,21 +65,23 @@ def test_nf4_weight(T, K, N):
     _check(_layer(T, K, N, [16], kind="nf4", seed=T + K))
 
 
+@pytest.mark.parametrize("kind", ["nf4", "bf16"])
 @pytest.mark.parametrize("T,K,N,ranks", [(1, 1024, 200, [8]), (2, 768, 264, [24, 16]), (3, 2048, 96, [16]),
                                           (4, 512, 384, [40]), (1, 14336, 264, [16]), (4, 14336, 130, [8, 8])])
-def test_nf4_cuda_core_tokens(T, K, N, ranks):
-    """One to four tokens with a 4-bit weight and K a multiple of 256 go to the CUDA-core
-    kernel: ragged weight rows (the last 32-row group part-filled), ranks that are not
+def test_cuda_core_tokens(T, K, N, ranks, kind):
+    """One to four tokens with K a multiple of 256 go to the CUDA-core kernel, 4-bit or bf16
+    weight: ragged weight rows (the last 32-row group part-filled), ranks that are not
     multiples of 16, several adapters, a bias, and long rows split into many K ranges (more
     than eight splits for K = 14336)."""
-    _check(_layer(T, K, N, ranks, kind="nf4", bias="bf16", seed=T * 7 + K + N))
+    _check(_layer(T, K, N, ranks, kind=kind, bias="bf16", seed=T * 7 + K + N))
 
 
-def test_nf4_cuda_core_grouped_fp32_out():
+@pytest.mark.parametrize("kind", ["nf4", "bf16"])
+def test_cuda_core_grouped_fp32_out(kind):
     """Stacked gate/up groups with their own adapters, fp32 output, a request scale, one token
     through four."""
     for T in (1, 4):
-        lin = _layer(T, 512, 2 * 200, [16, 8], kind="nf4", groups=2, strengths=[0.5, 1.5], seed=40 + T)
+        lin = _layer(T, 512, 2 * 200, [16, 8], kind=kind, groups=2, strengths=[0.5, 1.5], seed=40 + T)
         lin.request_scale = 0.75
         _check(lin, out_dtype=torch.float32)
 

@@ -145,7 +145,7 @@ struct SkinnyPlan {
   int kkb = 1;                 // 64-wide K blocks per pipeline step
   long long N = 0;
   size_t part_bytes = 0;
-  // one to four tokens against a 4-bit weight: the CUDA-core kernel (wp_gemv.cu)
+  // one to four tokens against a weight, K a multiple of 256: the CUDA-core kernel (wp_gemv.cu)
   bool gemv = false;
   int g_splits = 1, g_ks_len = 0, g_grid = 0;
   size_t g_smem = 0;
@@ -155,7 +155,7 @@ struct SkinnyPlan {
 // split, so a split is at most kGemvXBudget / T elements; among those, the split whose
 // busiest warp streams the fewest elements (32-row groups x split length), fewer splits on a
 // tie.  The grid is a multiple of the splits.
-bool plan_gemv(long long T, long long K, long long N, SkinnyPlan* sp) {
+bool plan_gemv(long long T, long long K, long long N, bool nf4, SkinnyPlan* sp) {
   const int kb = static_cast<int>(K / kGemvStageK);
   const int ngW = static_cast<int>((N + 31) / 32);
   const int sms = device_sm_count();
@@ -165,7 +165,7 @@ bool plan_gemv(long long T, long long K, long long N, SkinnyPlan* sp) {
     if (T * ks_len > kGemvXBudget) continue;
     const int splits = static_cast<int>((K + ks_len - 1) / ks_len);
     const size_t smem = gemv_smem_bytes(static_cast<int>(T), ks_len);
-    const int per_sm = gemv_blocks_per_sm(static_cast<int>(T), smem);
+    const int per_sm = gemv_blocks_per_sm(static_cast<int>(T), nf4, smem);
     if (per_sm < 1) continue;
     const int nbs = sms * per_sm / splits;
     if (nbs < 1) continue;
@@ -227,7 +227,7 @@ bool plan_skinny(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int n, 
   sp->splits = (sp->k_blocks + sp->kbps - 1) / sp->kbps;
   sp->units = rows * sp->splits;
   sp->part_bytes = round256(static_cast<size_t>(sp->splits) * T * (N + R16) * 4);
-  if (W && W->dtype == WP_NF4 && T <= kGemvMaxT && K % kGemvStageK == 0 && plan_gemv(T, K, N, sp)) {
+  if (W && T <= kGemvMaxT && K % kGemvStageK == 0 && plan_gemv(T, K, N, W->dtype == WP_NF4, sp)) {
     sp->gemv = true;
     sp->part_bytes =
         std::max(sp->part_bytes, round256(static_cast<size_t>(sp->g_splits) * T * (N + R16) * 4));
@@ -338,7 +338,7 @@ int skinny_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, boo
   p.n_ad = n_adapters;
   p.a_off[n_adapters] = toff;
 
-  if (sp.gemv && aligned16(W->absmax)) {
+  if (sp.gemv && (!nf4 || aligned16(W->absmax))) {
     GemvParams g{};
     g.T = static_cast<int>(T); g.K = static_cast<int>(K); g.N = static_cast<int>(N);
     g.splits = sp.g_splits; g.ks_len = sp.g_ks_len;
@@ -360,11 +360,16 @@ int skinny_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, boo
     if (!g.status) return record_cuda();
     GemvMaps gm;
     std::memset(&gm, 0, sizeof(gm));
-    int rc = make_map_u8(&gm.wq, W->data, K / 2, N, K / 2, kGemvStageK / 2, 32, 128);
+    int rc = WP_OK;
+    if (nf4) {
+      rc = make_map_u8(&gm.wq, W->data, K / 2, N, K / 2, kGemvStageK / 2, 32, 128);
+      if (rc != WP_OK) return rc;
+      rc = make_map(&gm.am, WP_FP32, W->absmax, K / 64, N, K / 64, kGemvStageK / 64, 32, /*swizzle=*/0);
+    } else {
+      rc = make_map_bf16(&gm.w, W->data, K, N, W->ld, kBK, 32);
+    }
     if (rc != WP_OK) return rc;
-    rc = make_map(&gm.am, WP_FP32, W->absmax, K / 64, N, K / 64, kGemvStageK / 64, 32, /*swizzle=*/0);
-    if (rc != WP_OK) return rc;
-    rc = launch_gemv(gm, g, sp.g_grid, sp.g_smem, stream);
+    rc = launch_gemv(gm, g, nf4, sp.g_grid, sp.g_smem, stream);
     if (rc != WP_OK) return rc;
     q.splits = sp.g_splits;
     return launch_skinny_reduce(q, stream);

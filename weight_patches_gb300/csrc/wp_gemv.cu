@@ -1,14 +1,14 @@
-// wp_gemv.cu -- the dynamic LoRA linear for one to four tokens against a 4-bit NormalFloat
-// base weight, on the CUDA cores (Unsloth fast_lora walkthrough, section 3: the 4-bit weight
-// is dequantised inside the matmul; LoRA, section 4.1: the low-rank branch X A^T is formed
-// from the same X).  With so few tokens the product is a matrix-vector one: every weight
-// element is used T times, so the work is streaming 0.5 byte per element from HBM and
-// turning it into bf16 values, not a contraction worth the tensor cores.
+// wp_gemv.cu -- the dynamic LoRA linear for one to four tokens on the CUDA cores, against a
+// 4-bit NormalFloat or a bf16 base weight (Unsloth fast_lora walkthrough, section 3: the 4-bit
+// weight is dequantised inside the matmul; LoRA, section 4.1: the low-rank branch X A^T is
+// formed from the same X).  With so few tokens the product is a matrix-vector one: every
+// weight element is used T times, so the work is streaming the weight from HBM once (and, for
+// 4 bits, turning its codes into bf16 values), not a contraction worth the tensor cores.
 //
 // Each warp owns 32 consecutive weight rows at a time, one per lane, and a ring of stages it
-// fills itself by TMA (codes: 128 B x 32 rows in the 128-byte swizzle; scales: 4 fp32 x 32
-// rows), so a lane reads its row's 16-byte units without bank conflicts and no role waits on
-// another.  A lane builds the 16 values bf16(level * absmax) of a 64-element block in two byte
+// fills itself by TMA (128 B x 32 rows in the 128-byte swizzle: 256 codes or 64 bf16 values
+// a row; for 4 bits also the rows' 4 fp32 block scales), so a lane reads its row's 16-byte
+// units without bank conflicts and no role waits on another.  A lane builds the 16 values bf16(level * absmax) of a 64-element block in two byte
 // planes and looks its codes up with byte permutes (the same W_eff the tensor-core paths put
 // in their operand tiles), then multiplies them by X read from shared memory, the same address
 // in every lane (a broadcast), with mixed-precision fmas (bf16 pairs in, fp32 sums): the
@@ -71,9 +71,11 @@ __device__ __forceinline__ void block_table(float am, const float (&lv)[16], uin
   }
 }
 
-template <int kT>
-__global__ void __launch_bounds__(kGemvWarps * 32) gemv_nf4_kernel(const __grid_constant__ GemvMaps maps,
-                                                                   const GemvParams p) {
+// kNF4: 4-bit codes and block scales, 256 K elements per stage; else bf16 rows, 64 per stage
+template <int kT, bool kNF4>
+__global__ void __launch_bounds__(kGemvWarps * 32) gemv_kernel(const __grid_constant__ GemvMaps maps,
+                                                               const GemvParams p) {
+  constexpr int kStageK = kNF4 ? kGemvStageK : 64;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* sbase = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -108,17 +110,22 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_nf4_kernel(const __grid_
   float* part = p.part + static_cast<long long>(split) * p.T * p.ldp;
 
   // ---- weight rows: flat sequence of (unit, stage) over this warp's 32-row groups
-  const int ns = klen / kGemvStageK;
+  const int ns = klen / kStageK;
   const int my_w = gw < p.ngW ? (p.ngW - gw + wstride - 1) / wstride : 0;
   const int n_it = my_w * ns;
   int issued = 0;
   auto issue = [&](int it) {
     const int g = gw + (it / ns) * wstride;
-    const int kk = k0 + (it % ns) * kGemvStageK;
+    const int kk = k0 + (it % ns) * kStageK;
     const int s = it % kGemvStages;
-    mbar_arrive_expect_tx(&bars[s], kGemvCodeBytes + kGemvAmBytes);
-    tma_load_2d(codes + s * kGemvCodeBytes, &maps.wq, kk / 2, g * 32, &bars[s]);
-    tma_load_2d(ams + s * kGemvAmBytes, &maps.am, kk / 64, g * 32, &bars[s]);
+    if (kNF4) {
+      mbar_arrive_expect_tx(&bars[s], kGemvCodeBytes + kGemvAmBytes);
+      tma_load_2d(codes + s * kGemvCodeBytes, &maps.wq, kk / 2, g * 32, &bars[s]);
+      tma_load_2d(ams + s * kGemvAmBytes, &maps.am, kk / 64, g * 32, &bars[s]);
+    } else {
+      mbar_arrive_expect_tx(&bars[s], kGemvCodeBytes);
+      tma_load_2d(codes + s * kGemvCodeBytes, &maps.w, kk, g * 32, &bars[s]);
+    }
   };
   if (lane == 0)
     for (int it = 0; it < kGemvStages - 1 && it < n_it; ++it) issue(it);
@@ -152,6 +159,23 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_nf4_kernel(const __grid_
     }
     const int st = it % ns;
     const uint8_t* crow = codes + s * kGemvCodeBytes + lane * 128;
+    if (!kNF4) {
+      // bf16 row: 64 elements in 8 units of 8
+#pragma unroll
+      for (int unit = 0; unit < 8; ++unit) {
+        const uint4 wv = *reinterpret_cast<const uint4*>(crow + ((unit ^ (lane & 7)) << 4));
+        const int e0 = st * kStageK + unit * 8;
+#pragma unroll
+        for (int t = 0; t < kT; ++t) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * p.ks_len + e0);
+          float& a = acc[t][unit & 1];
+          a = fma_bf16x2(wv.x, xv.x, a);
+          a = fma_bf16x2(wv.y, xv.y, a);
+          a = fma_bf16x2(wv.z, xv.z, a);
+          a = fma_bf16x2(wv.w, xv.w, a);
+        }
+      }
+    } else {
     const uint4 amv = *reinterpret_cast<const uint4*>(ams + s * kGemvAmBytes + lane * 16);
     const float am4[4] = {__uint_as_float(amv.x), __uint_as_float(amv.y), __uint_as_float(amv.z),
                           __uint_as_float(amv.w)};
@@ -172,7 +196,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_nf4_kernel(const __grid_
           uint32_t o[4];
           lookup4(sel, pick, lo, hi, o[0], o[1]);
           lookup4(sel >> 16, pick >> 16, lo, hi, o[2], o[3]);
-          const int e0 = st * kGemvStageK + unit * 32 + u * 8;
+          const int e0 = st * kStageK + unit * 32 + u * 8;
 #pragma unroll
           for (int t = 0; t < kT; ++t) {
             const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * p.ks_len + e0);
@@ -184,6 +208,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_nf4_kernel(const __grid_
           }
         }
       }
+    }
     }
     if (st == ns - 1) {
       const int n = (gw + (it / ns) * wstride) * 32 + lane;
@@ -232,9 +257,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_nf4_kernel(const __grid_
   }
 }
 
-template <int kT>
+template <int kT, bool kNF4>
 int launch_t(const GemvMaps& maps, const GemvParams& p, int grid, size_t smem, cudaStream_t stream) {
-  auto kern = gemv_nf4_kernel<kT>;
+  auto kern = gemv_kernel<kT, kNF4>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e == cudaSuccess) {
     kern<<<grid, kGemvWarps * 32, smem, stream>>>(maps, p);
@@ -247,13 +272,14 @@ int launch_t(const GemvMaps& maps, const GemvParams& p, int grid, size_t smem, c
   return WP_OK;
 }
 
-template <int kT>
+template <int kT, bool kNF4>
 int occupancy_t(size_t smem) {
   int n = 0;
-  if (cudaFuncSetAttribute(gemv_nf4_kernel<kT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(gemv_kernel<kT, kNF4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_nf4_kernel<kT>, kGemvWarps * 32, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_kernel<kT, kNF4>, kGemvWarps * 32, smem) !=
+      cudaSuccess)
     return 0;
   return n;
 }
@@ -265,30 +291,49 @@ size_t gemv_smem_bytes(int T, int ks_len) {
          static_cast<size_t>(T) * ks_len * 2 + kGemvWarps * kGemvStages * 8;
 }
 
-int gemv_blocks_per_sm(int T, size_t smem) {
-  // the answer depends on T and the shared memory alone; kept per (T, 1 KiB of smem)
-  static std::atomic<int> cache[kGemvMaxT + 1][kSmemLimit / 1024 + 2];
+int gemv_blocks_per_sm(int T, bool nf4, size_t smem) {
+  // the answer depends on T, the weight type and the shared memory alone; kept per 1 KiB
+  static std::atomic<int> cache[2][kGemvMaxT + 1][kSmemLimit / 1024 + 2];
   if (T < 1 || T > kGemvMaxT || smem > static_cast<size_t>(kSmemLimit)) return 0;
-  std::atomic<int>& c = cache[T][(smem + 1023) / 1024];
+  std::atomic<int>& c = cache[nf4 ? 1 : 0][T][(smem + 1023) / 1024];
   int n = c.load(std::memory_order_relaxed);
   if (n != 0) return n > 0 ? n : 0;
-  switch (T) {
-    case 1: n = occupancy_t<1>(smem); break;
-    case 2: n = occupancy_t<2>(smem); break;
-    case 3: n = occupancy_t<3>(smem); break;
-    default: n = occupancy_t<4>(smem); break;
+  if (nf4) {
+    switch (T) {
+      case 1: n = occupancy_t<1, true>(smem); break;
+      case 2: n = occupancy_t<2, true>(smem); break;
+      case 3: n = occupancy_t<3, true>(smem); break;
+      default: n = occupancy_t<4, true>(smem); break;
+    }
+  } else {
+    switch (T) {
+      case 1: n = occupancy_t<1, false>(smem); break;
+      case 2: n = occupancy_t<2, false>(smem); break;
+      case 3: n = occupancy_t<3, false>(smem); break;
+      default: n = occupancy_t<4, false>(smem); break;
+    }
   }
   c.store(n > 0 ? n : -1, std::memory_order_relaxed);
   return n;
 }
 
-int launch_gemv(const GemvMaps& maps, const GemvParams& p, int grid, size_t smem, cudaStream_t stream) {
+int launch_gemv(const GemvMaps& maps, const GemvParams& p, bool nf4, int grid, size_t smem,
+                cudaStream_t stream) {
   if (grid < 1) return WP_OK;
+  if (nf4) {
+    switch (p.T) {
+      case 1: return launch_t<1, true>(maps, p, grid, smem, stream);
+      case 2: return launch_t<2, true>(maps, p, grid, smem, stream);
+      case 3: return launch_t<3, true>(maps, p, grid, smem, stream);
+      case 4: return launch_t<4, true>(maps, p, grid, smem, stream);
+      default: return WP_ERR_UNSUPPORTED;
+    }
+  }
   switch (p.T) {
-    case 1: return launch_t<1>(maps, p, grid, smem, stream);
-    case 2: return launch_t<2>(maps, p, grid, smem, stream);
-    case 3: return launch_t<3>(maps, p, grid, smem, stream);
-    case 4: return launch_t<4>(maps, p, grid, smem, stream);
+    case 1: return launch_t<1, false>(maps, p, grid, smem, stream);
+    case 2: return launch_t<2, false>(maps, p, grid, smem, stream);
+    case 3: return launch_t<3, false>(maps, p, grid, smem, stream);
+    case 4: return launch_t<4, false>(maps, p, grid, smem, stream);
     default: return WP_ERR_UNSUPPORTED;
   }
 }

@@ -202,9 +202,10 @@ int launch_skinny(const SkinnyMaps& maps, const SkinnyParams& p, size_t smem_byt
 int launch_skinny_reduce(const SkinnyReduceParams& q, cudaStream_t stream);
 int skinny_grid_ctas(size_t smem_bytes, bool nf4);
 
-// One to four tokens against a 4-bit weight on the CUDA cores (wp_gemv.cu): each warp streams
-// 32 weight rows, one per lane, through its own ring of TMA stages (256 K elements of 32 rows:
-// 4 KiB of codes in the 128-byte swizzle and 512 B of block scales); X of the block's K range
+// One to four tokens on the CUDA cores (wp_gemv.cu): each warp streams 32 weight rows, one per
+// lane, through its own ring of TMA stages (4-bit W: 256 K elements of 32 rows, 4 KiB of codes
+// in the 128-byte swizzle and 512 B of block scales; bf16 W: 64 K elements of 32 rows, 4 KiB in
+// the same swizzle); X of the block's K range
 // waits in shared memory as bf16.  It writes the partial sums skinny_reduce_kernel reads: the
 // W rows at [split][t][n], the adapters' A rows at [split][t][N + a_off + j].
 constexpr int kGemvMaxT = 4;
@@ -236,13 +237,15 @@ struct GemvParams {
 };
 
 struct GemvMaps {
+  CUtensorMap w;               // bf16 W [N, K], boxes of 64 x 32 rows, 128-byte swizzle
   CUtensorMap wq;              // codes [N, K/2] u8, boxes of 128 B x 32 rows, 128-byte swizzle
   CUtensorMap am;              // block scales [N, K/64] fp32, boxes of 4 x 32 rows
 };
 
 size_t gemv_smem_bytes(int T, int ks_len);
-int gemv_blocks_per_sm(int T, size_t smem_bytes);
-int launch_gemv(const GemvMaps& maps, const GemvParams& p, int grid, size_t smem_bytes, cudaStream_t stream);
+int gemv_blocks_per_sm(int T, bool nf4, size_t smem_bytes);
+int launch_gemv(const GemvMaps& maps, const GemvParams& p, bool nf4, int grid, size_t smem_bytes,
+                cudaStream_t stream);
 int* tc_status_ptr();
 
 int tc_max_pairs(size_t smem_bytes, bool nf4);
