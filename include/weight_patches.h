@@ -133,6 +133,11 @@ enum { WP_OP_FWD = 0, WP_OP_FWD_GROUPED = 1, WP_OP_BWD = 2, WP_OP_FWD_HOST = 3, 
  * columns fit one 256-column accumulator: a bf16 adapter counts ceil(r / 16) * 16
  * columns, an FP32 adapter as pieces 3 * ceil(r / 16) * 16 (FP32 adapters that do not
  * fit take the CUDA-core route, at most 4 of them).
+ * Few tokens (bf16 X and adapters): one to four tokens with in % 256 == 0 stream the
+ * weight once on the CUDA cores; up to 64 tokens with a WP_NF4 weight (4 with bf16)
+ * stream it through swapped tensor-core MMAs.  Both keep the same W_eff and the single
+ * bf16 rounding of s X A^T, sum in fp32, and leave fp32 partial sums in the workspace
+ * (lora_workspace_size counts them).
  */
 int lora_linear_fwd(const wp_mat* X, const wp_mat* W, const wp_mat* bias,
                     const wp_adapter* adapters, int32_t n_adapters, double request_scale,
