@@ -58,6 +58,20 @@ def test_bwd_bf16_grouped_and_fp32_dX():
     _check_full(lin, dX, dA, dB, dx_tol=2e-3)
 
 
+@pytest.mark.parametrize("T", [1, 3])
+def test_bwd_few_tokens(T):
+    """A handful of tokens: the dX pass also returns s dY B for dA, so it must not take the
+    few-token forward routes, which do not store it."""
+    rng = np.random.default_rng(90 + T)
+    K, N, r = 256, 512, 16
+    X = workloads.draw(rng, T, K, 1.0)
+    W = workloads.draw(rng, N, K, (1.0 / K) ** 0.5)
+    p = workloads.Patch(workloads.draw(rng, r, K, (1.0 / K) ** 0.5), workloads.draw(rng, N, r, 0.02), float(r), 1.0)
+    lin = _with_dY(workloads.Linear("bwd_few_tokens", X, W, None, [p]), 91 + T)
+    dX, dA, dB = _run(lin)
+    _check_full(lin, dX, dA, dB)
+
+
 def test_bwd_without_dX():
     lin = _with_dY(workloads.config1("small"), 23)
     dX, dA, dB = _run(lin, need_dX=False)

@@ -532,9 +532,10 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   }
 
   // a few tokens: the weight-streaming small-token path, when the workspace holds its
-  // partial sums (else the general path below serves the call)
-  if (!rank_only && !swiglu && plan.skinny_bytes > 0 && workspace && ws_bytes >= plan.skinny_bytes &&
-      aligned16(workspace)) {
+  // partial sums (else the general path below serves the call); it does not store s X A^T,
+  // so calls that want it back (h_out) stay on the general path
+  if (!rank_only && !swiglu && !h_out && plan.skinny_bytes > 0 && workspace &&
+      ws_bytes >= plan.skinny_bytes && aligned16(workspace)) {
     const int rc = skinny_impl(X, W, bias, G, grouped, adapters, n_adapters, s_of, Y, workspace, stream);
     if (rc != WP_ERR_UNSUPPORTED) return rc;
   }
