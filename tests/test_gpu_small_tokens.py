@@ -7,7 +7,7 @@ InvokeAI sidecar-patch article, section 五: quantised layers under few tokens g
 small-batch kernel; here both bf16 and 4-bit weights do, with the LoRA terms fused in.
 Covered: one token, ragged token counts, ragged weight rows, 4-bit weights with and
 without TMA-fed block scales, one to four tokens on the CUDA-core kernel (4-bit and bf16,
-many K splits), stacked column groups, delta-only layers, several adapters,
+many K splits, and its fallback when the block scales are not 16-byte aligned), stacked column groups, delta-only layers, several adapters,
 bias, fp32 output, zero strength, and full-size layers of the workloads (sampled output
 columns)."""
 import numpy as np
