@@ -32,7 +32,10 @@
  *     the host before anything is launched; a rejected call launches nothing.
  *   - A kernel whose bounded wait expires records WP_ERR_TIMEOUT in a device status
  *     word instead of hanging; read it with lora_device_status() after the stream has
- *     been synchronised.
+ *     been synchronised.  The word is sticky until reset: while it reads WP_ERR_TIMEOUT,
+ *     the outputs of every call made since the last reset are undefined (a kernel that
+ *     gave up leaves its outputs partly written, and a later pass of the same call may
+ *     have combined stale scratch), even though each of those calls returned WP_OK.
  */
 #ifndef WEIGHT_PATCHES_H
 #define WEIGHT_PATCHES_H
@@ -300,9 +303,13 @@ int lora_dense_patch(void* param, int32_t param_dtype, int64_t param_numel,
  * call allocates nothing.
  *
  * Same arguments, dtypes, alignment rules and errors as lora_linear_fwd, minus the
- * workspace.  A call that would need more than 4 MiB of scratch is rejected with
+ * workspace.  A call whose general path would need more than 4 MiB of scratch (the
+ * minimum above, not counting the few-token routes' partial sums) is rejected with
  * WP_ERR_WORKSPACE before anything is launched (lora_last_cuda_error() says how much was
- * needed).  The first call on each device looks up the array's device address
+ * needed).  A call of 1 to 64 tokens takes a few-token route only when that route's fp32
+ * partial sums (splits x T x (out + sum of the ranks rounded up to 16) x 4 bytes) fit the
+ * array as well; otherwise it runs on the general path, with the same results within the
+ * tolerances of lora_linear_fwd.  The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any stream
  * capture.  Every call on a device shares the one array and leaves its contents behind
  * (the call clears the few flags it needs on its stream; every other scratch element is

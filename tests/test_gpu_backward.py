@@ -29,14 +29,20 @@ def _run(lin, need_dX=True, dX_dtype=torch.bfloat16):
 
 def _check_full(lin, dX, dA, dB, dx_tol=DX_TOL):
     X, W, _, patches = olora.decode_linear(lin)
-    g = olora.linear_bwd(X, W, to_f64(lin.dY), patches, lin.request_scale)
+    dY = to_f64(lin.dY)
+    g = olora.linear_bwd(X, W, dY, patches, lin.request_scale)
+    bX, bA, bB = gu.bwd_bounds(X, W, dY, patches, lin.request_scale, g.dX, g.dA, g.dB,
+                               dX_f32=dX is not None and dX.dtype == torch.float32)
     if dX is not None:
         err = relative_rms(gu.to_f64(dX), g.dX)
         assert err <= dx_tol, err
+        gu.assert_elementwise(gu.to_f64(dX), g.dX, bX, "dX")
     for i in range(len(patches)):
         ea = relative_rms(dA[i].double().cpu().numpy(), g.dA[i])
         eb = relative_rms(dB[i].double().cpu().numpy(), g.dB[i])
         assert ea <= DAB_TOL and eb <= DAB_TOL, (i, ea, eb)
+        gu.assert_elementwise(dA[i].double().cpu().numpy(), g.dA[i], bA[i], f"dA[{i}]")
+        gu.assert_elementwise(dB[i].double().cpu().numpy(), g.dB[i], bB[i], f"dB[{i}]")
 
 
 def _with_dY(lin, seed):
@@ -96,14 +102,35 @@ def test_bwd_nf4_full_sampled():
     dY_rows = bf16_bits_to_f64(lin.dY.data[rows])
     want_dX = olora.grad_X(X[rows], W, dY_rows, patches, lin.request_scale)
     assert relative_rms(gu.to_f64(dX)[rows], want_dX) <= DX_TOL
-    # dA, dB: sums over all tokens, accumulated over row chunks
+    zero = [np.zeros((p.rank, X.shape[1])) for p in patches]
+    zeroB = [np.zeros((p.B.shape[0], p.rank)) for p in patches]
+    bX, _, _ = gu.bwd_bounds(X[rows], W, dY_rows, patches, lin.request_scale, want_dX, zero, zeroB)
+    gu.assert_elementwise(gu.to_f64(dX)[rows], want_dX, bX, "dX (sampled rows)")
+    # dA, dB: sums over all tokens, accumulated over row chunks, with the magnitudes the
+    # element-wise bound needs (the bound's T is the whole token count)
     sumA = [0.0] * len(patches)
     sumB = [0.0] * len(patches)
+    magA = [0.0] * len(patches)
+    magB = [0.0] * len(patches)
+    G = len(patches)
+    og = W.shape[0] // G
     for r0 in range(0, lin.T, 1024):
         sl = slice(r0, min(lin.T, r0 + 1024))
-        a, b = olora.grad_AB(X[sl], bf16_bits_to_f64(lin.dY.data[sl]), patches, lin.request_scale)
+        dYs = bf16_bits_to_f64(lin.dY.data[sl])
+        a, b = olora.grad_AB(X[sl], dYs, patches, lin.request_scale)
         sumA = [x + y for x, y in zip(sumA, a)]
         sumB = [x + y for x, y in zip(sumB, b)]
+        for i, p in enumerate(patches):
+            s = abs(olora.combined_scale(p.alpha, p.rank, p.strength, lin.request_scale))
+            dyg = np.abs(dYs[:, i * og:(i + 1) * og])
+            magA[i] = magA[i] + s * ((dyg @ np.abs(p.B)).T @ np.abs(X[sl]))
+            magB[i] = magB[i] + s * (dyg.T @ (np.abs(X[sl]) @ np.abs(p.A).T))
+    T, K = X.shape
     for i in range(len(patches)):
-        assert relative_rms(dA[i].double().cpu().numpy(), sumA[i]) <= DAB_TOL
-        assert relative_rms(dB[i].double().cpu().numpy(), sumB[i]) <= DAB_TOL
+        gA, gB = dA[i].double().cpu().numpy(), dB[i].double().cpu().numpy()
+        assert relative_rms(gA, sumA[i]) <= DAB_TOL
+        assert relative_rms(gB, sumB[i]) <= DAB_TOL
+        eA = (4.0 * (og + T + 32) * 2.0 ** -24 + 2.0 ** -16) * magA[i]
+        eB = (4.0 * (K + T + 32) * 2.0 ** -24 + 2.0 ** -16) * magB[i]
+        gu.assert_elementwise(gA, sumA[i], gu.ulp_f32(np.abs(sumA[i]) + eA) + eA, f"dA[{i}]")
+        gu.assert_elementwise(gB, sumB[i], gu.ulp_f32(np.abs(sumB[i]) + eB) + eB, f"dB[{i}]")

@@ -2,7 +2,8 @@
 
 Tolerances (from the method's accuracy gate): bf16 outputs within relative RMS 4e-3 and
 no worse than the unfused bf16 chain that materialises the delta; FP32 cases within
-1e-5."""
+1e-5.  Every output element is also held to the element-wise bound of the single-rounding
+design (tests/gpu_util.py), so a single wrong element fails."""
 import numpy as np
 import pytest
 import torch
@@ -27,8 +28,10 @@ def _gate(err, chain):
 def test_c0_tiny_fp32():
     lin = workloads.config0()
     Y = gu.run_fwd(lin, out_dtype=torch.float32)
-    err = relative_rms(gu.to_f64(Y), olora.reference_output(lin))
+    want = olora.reference_output(lin)
+    err = relative_rms(gu.to_f64(Y), want)
     assert err <= FP32_TOL, err
+    gu.assert_elementwise(gu.to_f64(Y), want, gu.fwd_bound(lin, out_f32=True, y_ref=want), lin.name)
 
 
 def test_c1_grouped_small():
@@ -55,14 +58,18 @@ def test_c4_fp32_adapter_fp32_output():
     lin, _ = workloads.config4("small")
     lin.patches = lin.patches[:1]            # the fp32 adapter alone, on the bf16 layer
     Y = gu.run_fwd(lin, out_dtype=torch.float32)
-    err = relative_rms(gu.to_f64(Y), olora.reference_output(lin))
+    want = olora.reference_output(lin)
+    err = relative_rms(gu.to_f64(Y), want)
     assert err <= FP32_TOL, err
+    gu.assert_elementwise(gu.to_f64(Y), want, gu.fwd_bound(lin, out_f32=True, y_ref=want), "fp32 adapter")
     # delta only (no base weight): the fp32 adapter's contribution by itself
     Yd = gu.run_fwd(lin, out_dtype=torch.float32, with_base=False)
     X, _, _, patches = olora.decode_linear(lin)
     want = olora.linear_fwd(X, None, None, patches, lin.request_scale, out_features=lin.out_features)
     err = relative_rms(gu.to_f64(Yd), want)
     assert err <= FP32_TOL, err
+    gu.assert_elementwise(gu.to_f64(Yd), want, gu.fwd_bound(lin, out_f32=True, y_ref=want, with_base=False),
+                          "fp32 adapter, delta only")
 
 
 @pytest.mark.parametrize("T,K,N,r,xkind", [(77, 70, 40, 5, workloads.FP32), (131, 200, 96, 24, workloads.FP32),
@@ -77,8 +84,10 @@ def test_fp32_adapter_odd_shapes(T, K, N, r, xkind):
     B = workloads.draw(rng, N, r, 0.02, workloads.FP32)
     lin = workloads.Linear("odd32", X, W, None, [workloads.Patch(A, B, float(r), 0.8)], request_scale=1.3)
     Y = gu.run_fwd(lin, out_dtype=torch.float32)
-    err = relative_rms(gu.to_f64(Y), olora.reference_output(lin))
+    want = olora.reference_output(lin)
+    err = relative_rms(gu.to_f64(Y), want)
     assert err <= FP32_TOL, err
+    gu.assert_elementwise(gu.to_f64(Y), want, gu.fwd_bound(lin, out_f32=True, y_ref=want), lin.name)
 
 
 def test_fp32_output_bf16_adapters():
@@ -174,6 +183,7 @@ def test_no_worse_than_torch_unfused_chain():
     lin = workloads.config1("small")
     Y = gu.run_fwd(lin)
     want = olora.reference_output(lin)
+    gu.assert_elementwise(gu.to_f64(Y), want, gu.fwd_bound(lin, y_ref=want), lin.name)
     err = relative_rms(gu.to_f64(Y), want)
     chain = relative_rms(gu.to_f64(gu.torch_unfused_chain(lin)), want)
     assert err <= chain, (err, chain)

@@ -148,8 +148,10 @@ def test_full_size_layers(cfg, T):
     Xf = to_f64(X)
     bias = to_f64(lin.bias).reshape(-1) if lin.bias is not None else None
     want = np.empty((T, len(cols)))
+    Wc = np.empty((len(cols), Xf.shape[1]))
     for k, c in enumerate(cols):
         w = to_f64(lin.W.slice_rows(int(c), int(c) + 1))[0]
+        Wc[k] = w
         y = Xf @ w + (bias[c] if bias is not None else 0.0)
         g = c // og if lin.groups > 1 else 0
         p = olora.decode_patch(lin.patches[g])
@@ -157,3 +159,9 @@ def test_full_size_layers(cfg, T):
         y = y + s * ((Xf @ p.A.T) @ p.B[c - g * og])
         want[:, k] = y
     assert relative_rms(got[:, cols], want) <= BF16_TOL
+    # element-wise on the sampled columns: the bound's weight magnitudes from the decoded rows
+    Wfull = np.zeros((N, Xf.shape[1]))
+    Wfull[cols] = Wc
+    pats = [olora.decode_patch(p) for p in lin.patches]
+    bound = gu.linear_error_bound(Xf, Wfull, bias, pats, lin.request_scale, lin.groups, False, want, cols=cols)
+    gu.assert_elementwise(got[:, cols], want, bound, lin.name)

@@ -62,6 +62,10 @@ def test_swiglu_fwd(kind, T, d, F, r, bias):
     assert np.array_equal(_bits(h), _bits(h2))
     ref = olora.reference_output(lin)                     # exact e | g
     h_ref = osw.swiglu(ref[:, :F], ref[:, F:])
+    # element-wise: e | g within the linear's bound, h within the bound carried through silu
+    b_eg = gu.fwd_bound(lin, y_ref=ref)
+    gu.assert_elementwise(gu.to_f64(eg), ref, b_eg, "e|g")
+    gu.assert_elementwise(gu.to_f64(h), h_ref, gu.swiglu_bound(ref[:, :F], ref[:, F:], b_eg[:, :F], b_eg[:, F:]), "h")
     chain = olora.reference_chain(lin)                    # unfused bf16 chain's e | g
     h_chain = f64_to_bf16_value(osw.swiglu(chain[:, :F], chain[:, F:]))
     err, err_chain = relative_rms(gu.to_f64(h), h_ref), relative_rms(h_chain, h_ref)
@@ -161,3 +165,6 @@ def test_swiglu_c3_full_sampled_rows():
     h_ref = osw.swiglu(ref[:, :F], ref[:, F:])
     got = gu.to_f64(h[torch.as_tensor(rows, device=h.device)])
     assert relative_rms(got, h_ref) <= BF16_TOL
+    b_eg = gu.fwd_bound(gate_up, rows, y_ref=ref)
+    gu.assert_elementwise(gu.to_f64(eg[torch.as_tensor(rows, device=eg.device)]), ref, b_eg, "e|g")
+    gu.assert_elementwise(got, h_ref, gu.swiglu_bound(ref[:, :F], ref[:, F:], b_eg[:, :F], b_eg[:, F:]), "h")

@@ -212,3 +212,91 @@ def test_workload_generators_are_deterministic_and_shaped():
     lin4, payload = workloads.config4("small")
     assert [p.A.kind for p in lin4.patches] == ["fp32", "bf16", "bf16"]
     assert payload.shape == (384, 384)
+
+
+# ----------------------------------------------------------------- the unfused chain's roundings
+def _chain_examples(golden_dir):
+    with open(os.path.join(golden_dir, "unfused_chain_examples.json")) as f:
+        return json.load(f)["examples"]
+
+
+def _chain_inputs(ex):
+    X = np.array(ex["X"], float)
+    W = np.array(ex["W"], float)
+    bias = None if ex["bias"] is None else np.array(ex["bias"], float)
+    pats = []
+    for q in ex["patches"]:
+        p = _patch(q["A"], q["B"], q["alpha"], q["strength"], q["fp32"])
+        if q.get("bias_B") is not None:
+            p.bias_B = np.array(q["bias_B"], float)
+        pats.append(p)
+    return X, W, bias, pats, ex["request_scale"]
+
+
+def test_unfused_chain_hand_examples(golden_dir):
+    """Each hand-worked example pins one or two of the chain's bf16 roundings (the values
+    in the file were worked by hand, step by step)."""
+    for ex in _chain_examples(golden_dir):
+        X, W, bias, pats, rs = _chain_inputs(ex)
+        assert lora.unfused_bf16_chain(X, W, bias, pats, rs).tolist() == ex["Y_chain"], ex["name"]
+        assert lora.linear_fwd(X, W, bias, pats, rs).tolist() == ex["Y_def"], ex["name"]
+
+
+MUTATIONS = ["no_base_round", "bias_after_round", "no_t_round", "no_d_round", "bias_B_after_round",
+             "no_alpha_round", "no_strength_round", "no_scale_round", "one_round_for_scales",
+             "no_add_round", "sum_deltas_then_round", "fp32_adapter_rounded", None]
+
+
+def _mutant_chain(X, W, bias, patches, rs, mut):
+    """A test-side variant of the chain with one rounding taken out or one added; mut=None
+    is the chain as the sglang PR's Motivation describes it."""
+    rnd = f64_to_bf16_value
+    keep = lambda v, m: v if mut == m else rnd(v)
+    xw = X @ W.T
+    if mut == "bias_after_round":
+        base = rnd(rnd(xw) + (0.0 if bias is None else bias))
+    else:
+        base = keep(xw + (0.0 if bias is None else bias), "no_base_round")
+    Y = base
+    deltas = []
+    for p in patches:
+        vb = 0.0 if p.bias_B is None else p.bias_B.reshape(1, -1)
+        cs = [np.float64(np.float32(p.alpha / p.rank)), np.float64(np.float32(p.strength)),
+              np.float64(np.float32(rs))]
+        if p.fp32_adapter and mut != "fp32_adapter_rounded":
+            d = (X @ p.A.T) @ p.B.T + vb
+            for c in cs:
+                d = d * c
+        else:
+            t = keep(X @ p.A.T, "no_t_round")
+            if mut == "bias_B_after_round":
+                d = rnd(rnd(t @ p.B.T) + vb)
+            else:
+                d = keep(t @ p.B.T + vb, "no_d_round")
+            if mut == "one_round_for_scales":
+                d = rnd(d * cs[0] * cs[1] * cs[2])
+            else:
+                for c, m in zip(cs, ("no_alpha_round", "no_strength_round", "no_scale_round")):
+                    if c != 1.0:
+                        d = keep(d * c, m)
+        deltas.append(d)
+    if mut == "sum_deltas_then_round":
+        return rnd(Y + sum(deltas))
+    for d in deltas:
+        Y = keep(Y + d, "no_add_round")
+    return Y
+
+
+@pytest.mark.parametrize("mut", MUTATIONS)
+def test_chain_examples_catch_each_rounding_mutation(golden_dir, mut):
+    """A chain with one rounding dropped or one extra rounding fails at least one stored
+    example; the unmutated variant reproduces all of them (so the variant is faithful)."""
+    exs = _chain_examples(golden_dir)
+    diffs = []
+    for ex in exs:
+        X, W, bias, pats, rs = _chain_inputs(ex)
+        diffs.append(_mutant_chain(X, W, bias, pats, rs, mut).tolist() != ex["Y_chain"])
+    if mut is None:
+        assert not any(diffs)
+    else:
+        assert any(diffs), mut

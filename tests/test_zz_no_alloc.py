@@ -70,6 +70,42 @@ def test_noalloc_matches_workspace_entry_on_two_calls():
     assert wpg.lora_device_status() == 0
 
 
+def _few_token_layer(rng, T, K, N, nf4, r=16):
+    X = workloads.draw(rng, T, K, 1.0)
+    W = workloads.draw_nf4(rng, N, K) if nf4 else workloads.draw(rng, N, K, (1.0 / K) ** 0.5)
+    bias = workloads.draw(rng, 1, N, 0.01)
+    A = workloads.draw(rng, r, K, (1.0 / K) ** 0.5)
+    B = workloads.draw(rng, N, r, 0.02)
+    return workloads.Linear("few", X, W, bias, [workloads.Patch(A, B, float(r), 0.8)], request_scale=0.5)
+
+
+def test_noalloc_few_token_routes_after_a_larger_call():
+    # a larger call first, so that the shared array holds another layer's leftovers
+    lin4, _ = workloads.config4("small")
+    X, W, bias, ads = _layer(lin4)
+    _check_against_workspace_entry(X, W, bias, ads, lin4.request_scale)
+    rng = np.random.default_rng(77)
+    # 1 and 4 tokens take the CUDA-core GEMV, 32 tokens (4-bit) the tensor-core small-token
+    # kernel; both keep their fp32 partial sums in the array; each call has a bias
+    for nf4 in (False, True):
+        for T in (1, 4, 32):
+            lin = _few_token_layer(rng, T, 512, 1024, nf4)
+            _check_against_workspace_entry(*_layer(lin), lin.request_scale)
+    assert wpg.lora_device_status() == 0
+
+
+def test_noalloc_wide_layer_whose_partials_do_not_fit_runs_on_the_general_path():
+    # 4-bit 4096 -> 28672 (the stacked gate/up width) at 32 tokens: the small-token route's
+    # partial sums would take more than the array holds, so the call runs on the general
+    # path (a few KB of scratch) instead of being refused
+    rng = np.random.default_rng(78)
+    lin = _few_token_layer(rng, 32, 4096, 28672, True)
+    X, W, bias, ads = _layer(lin)
+    assert wpg.lora_workspace_size(wpg.WP_OP_FWD, X, W, ads) > SCRATCH_BYTES
+    _check_against_workspace_entry(X, W, bias, ads, lin.request_scale)
+    assert wpg.lora_device_status() == 0
+
+
 def test_noalloc_refuses_more_scratch_than_the_array_holds():
     T, K, r = 70_000, 64, 16                       # 70000 * 16 * 4 B > 4 MiB
     assert T * r * 4 > SCRATCH_BYTES

@@ -1727,7 +1727,11 @@ int lora_linear_fwd_noalloc(const wp_mat* X, const wp_mat* W, const wp_mat* bias
                             const wp_adapter* adapters, int32_t n_adapters, double request_scale,
                             const wp_out* Y, void* stream) {
   if (!X || n_adapters < 0 || (n_adapters > 0 && !adapters)) return WP_ERR_INVALID;
-  const size_t need = lora_workspace_size(WP_OP_FWD, X, W, adapters, n_adapters);
+  // The general path's own need decides; the few-token routes take the call only when their
+  // partial sums fit the array as well (fwd_impl checks that against the bytes it is given)
+  FwdPlan plan;
+  plan_fwd(X, W, adapters, n_adapters, &plan);
+  const size_t need = fwd_workspace(X, plan, /*min_only=*/true);
   if (need > kNoAllocScratchBytes) {
     char buf[160];
     snprintf(buf, sizeof(buf),
@@ -1737,12 +1741,13 @@ int lora_linear_fwd_noalloc(const wp_mat* X, const wp_mat* W, const wp_mat* bias
     return WP_ERR_WORKSPACE;
   }
   void* scratch = nullptr;
-  if (need > 0) {
+  const bool any = need > 0 || plan.skinny_bytes > 0;
+  if (any) {
     const int rc = noalloc_scratch(&scratch);
     if (rc != WP_OK) return rc;
   }
   return fwd_impl(X, W, bias, 1, false, adapters, n_adapters, request_scale, Y, scratch,
-                  need > 0 ? kNoAllocScratchBytes : 0, static_cast<cudaStream_t>(stream));
+                  any ? kNoAllocScratchBytes : 0, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"
