@@ -9,10 +9,13 @@ the same shape (cuBLAS through torch, and this library's own kernel with no adap
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fused|reference]
 
-N > 1 is launched by torchrun, one rank per GPU: every rank runs its own batch
-(token-local op, no collective on the data path; weak scaling).  Rank 0 prints one
-JSON line.  ``--impl reference`` times the CPU FP64 oracle on the host cores on a
-bounded sample of the same workload (rank 0 only).
+N > 1 runs one rank per GPU under torchrun (bench.py re-launches itself that way when it
+is started without a torchrun environment): every rank runs its own batch (token-local op,
+no collective on the data path; weak scaling).  Rank 0 prints one JSON line.  At N = 1 the
+line also carries ``per_config``: every other workload of the library timed the same way
+(forward and backward of each, the dense patch), each with its work, time, roofline
+fraction, overheads and the clocks seen while it ran.  ``--impl reference`` times the CPU
+FP64 oracle on the host cores on a bounded sample of the same workload (rank 0 only).
 """
 from __future__ import annotations
 
@@ -32,6 +35,18 @@ sys.path.insert(0, ROOT)
 WORKLOAD = ("wan2.1-1.3b stacked qkv: T=32760 (21x30x52 latent), in=1536, out=3x1536 as 3 "
             "column groups, rank=32 per group, bf16 X/W/A/B, alpha=32, strength=1, scale=1, no bias")
 METRIC = "fused LoRA linear TFLOP/s & % BF16 roofline; overhead vs bare base GEMM"
+
+
+def bench_config(ws: int) -> dict:
+    """The `config` object of the JSON line, the same for both arms."""
+    import workloads
+    f = workloads.FULL[1]
+    return {"workload": WORKLOAD, "T": f["T"], "in": f["d_in"], "out": f["groups"] * f["d_out"],
+            "groups": f["groups"], "rank_per_group": f["rank"],
+            "gflop_per_step": round(2.0 * f["T"] * (f["d_in"] * f["groups"] * f["d_out"] + f["groups"] * f["rank"] *
+                                                    (f["d_in"] + f["d_out"])) / 1e9, 2),
+            "l2": "inputs larger than L2 (X 101 MB + W 14 MB + Y 302 MB per step > 129 MB)",
+            "parallelism": f"replicas x{ws} (token-local, no collective)"}
 
 
 def flops_of(lin) -> float:
@@ -93,7 +108,7 @@ def dist_env():
 
 # ----------------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -115,6 +130,7 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
+            self.rows = []
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         try:
@@ -122,15 +138,24 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        self.rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        return self.summary()
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, max clock and the throttle reasons of the samples taken between
+        host times t0 and t1 (all samples when not given)."""
+        from datetime import datetime
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        for r in getattr(self, "rows", []):
             try:
-                sm.append(float(r[1])); smax.append(float(r[2]))
+                ts = datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                if (t0 is not None and ts < t0) or (t1 is not None and ts > t1):
+                    continue
+                sm.append(float(r[2])); smax.append(float(r[3]))
             except (ValueError, IndexError):
                 continue
-            for n, v in zip(names, r[5:9]):
+            for n, v in zip(names, r[6:10]):
                 if v.strip() == "Active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
@@ -238,10 +263,7 @@ def run_fused(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "T": T, "in": X.shape[1], "out": N, "groups": lin.groups,
-                   "rank_per_group": lin.patches[0].rank, "gflop_per_step": round(flops / 1e9, 2),
-                   "l2": "inputs larger than L2 (X 101 MB + W 14 MB + Y 302 MB per step > 129 MB)",
-                   "parallelism": f"replicas x{ws} (token-local, no collective)"},
+        "config": bench_config(ws),
         "roofline": {"bound": "tensor", "achieved": round(per_launch_tflops, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(per_launch_tflops / peak, 4), "traffic": captured_traffic(),
                      "peak_source": f"{peak_kind} bf16 burst",
@@ -257,12 +279,181 @@ def run_fused(args):
         "gpu_launches": args.steps * LAUNCHES_PER_STEP,
         "clocks": clk,
     }
+    if ws == 1 and not args.no_per_config:
+        del Xh, Yh, ws_host, Y0
+        torch.cuda.empty_cache()
+        out["per_config"] = per_config(dev, args, peak, hbm)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(lin, budget_s=args.cpu_seconds)
     if ws > 1:
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(out))
+
+
+# ----------------------------------------------------------------------- other workloads
+def per_config(dev, args, peak, hbm):
+    """Every workload of the library besides the headline one, timed like it: CUDA events on
+    the launching stream around back-to-back calls after warm-up (inputs larger than L2), and
+    for the dense patch one call at a time after an L2 flush.  Each entry: its work (GFLOP or
+    MB), ms per call, rate, fraction of the measured peak, overheads over cuBLAS's bf16 GEMM of
+    the same shape and over this library's kernel without adapters, and the clocks seen."""
+    import torch
+    import weight_patches_gb300 as wpg
+    import workloads
+
+    stream = torch.cuda.current_stream(dev)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    marks = {}
+    k, w = max(10, min(args.steps, 50)), 5
+
+    def timed(fn, kk=k, ww=w):
+        for _ in range(ww):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(kk):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / kk
+
+    def d(mat):
+        if mat.kind == "nf4":
+            return wpg.NF4Weight(torch.from_numpy(mat.data).to(dev), torch.from_numpy(mat.absmax).to(dev),
+                                 mat.rows, mat.cols)
+        return mat.torch_cpu().to(dev)
+
+    def ads_of(lin):
+        return [wpg.Adapter(d(p.A), d(p.B), p.alpha, p.strength) for p in lin.patches]
+
+    def fwd_flops(lin):
+        T, K, N, G = lin.X.rows, lin.X.cols, lin.W.rows, lin.groups
+        return 2.0 * T * (K * N + sum(p.rank * (K + N // G) for p in lin.patches))
+
+    out = {}
+
+    def fwd_entry(name, lin, note=""):
+        t0 = time.time()
+        X, W = d(lin.X), d(lin.W)
+        bias = d(lin.bias).reshape(-1) if lin.bias is not None else None
+        ads = ads_of(lin)
+        N = lin.W.rows
+        Y = torch.empty(lin.T, N, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(max(1, wpg.lora_workspace_size(wpg.WP_OP_FWD_GROUPED if lin.groups > 1 else wpg.WP_OP_FWD,
+                                                        X, W, ads)), dtype=torch.uint8, device=dev)
+        if lin.groups > 1:
+            fn = lambda: wpg.lora_linear_fwd_grouped(X, W, bias, ads, lin.request_scale, out=Y, workspace=ws)
+        else:
+            fn = lambda: wpg.lora_linear_fwd(X, W, bias, ads, lin.request_scale, out=Y, workspace=ws)
+        t_s = time.time()
+        ms = timed(fn)
+        own = timed(lambda: wpg.lora_linear_fwd(X, W, bias, [], out=Y))
+        Wb = W if not isinstance(W, wpg.NF4Weight) else torch.randn(N, lin.X.cols, device=dev).to(torch.bfloat16)
+        if bias is not None:
+            cub = timed(lambda: torch.addmm(bias, X, Wb.t(), out=Y))
+        else:
+            cub = timed(lambda: torch.matmul(X, Wb.t(), out=Y))
+        t_e = time.time()
+        assert wpg.lora_device_status() == 0
+        fl = fwd_flops(lin)
+        tf = fl / (ms * 1e-3) / 1e12
+        out[name] = {"gflop": round(fl / 1e9, 2), "ms": round(ms, 5), "tflops": round(tf, 1),
+                     "frac": round(tf / peak, 4), "own_base_ms": round(own, 5), "cublas_base_ms": round(cub, 5),
+                     "overhead_vs_cublas": round(ms / cub - 1, 4), "overhead_vs_own_base": round(ms / own - 1, 4),
+                     "clocks": None, "setup_s": round(t_s - t0, 1)}
+        if note:
+            out[name]["note"] = note
+        marks[name] = (t_s, t_e)
+
+    def bwd_entry(name, lin):
+        t0 = time.time()
+        X, W, dY = d(lin.X), d(lin.W), d(lin.dY)
+        ads = ads_of(lin)
+        ws = torch.empty(wpg.lora_workspace_size(wpg.WP_OP_BWD, X, W, ads), dtype=torch.uint8, device=dev)
+        fn = lambda: wpg.lora_linear_bwd(X, W, dY, ads, lin.request_scale, workspace=ws)
+        t_s = time.time()
+        ms = timed(fn, max(5, k // 2), 3)
+        Wb = torch.randn(lin.W.rows, lin.X.cols, device=dev).to(torch.bfloat16)
+        dX = torch.empty(lin.T, lin.X.cols, dtype=torch.bfloat16, device=dev)
+        cub = timed(lambda: torch.matmul(dY, Wb, out=dX))
+        t_e = time.time()
+        assert wpg.lora_device_status() == 0
+        T, K, N, G = lin.X.rows, lin.X.cols, lin.W.rows, lin.groups
+        fl = 2.0 * T * (K * N + sum(2 * p.rank * (N // G + K) for p in lin.patches))
+        tf = fl / (ms * 1e-3) / 1e12
+        out[name] = {"gflop": round(fl / 1e9, 2), "ms": round(ms, 5), "tflops": round(tf, 1),
+                     "frac": round(tf / peak, 4), "cublas_dX_gemm_ms": round(cub, 5),
+                     "work": "dX, dA, dB (FLOP: 2T(in out + sum_g 2 r_g (out_g + in)))",
+                     "clocks": None, "setup_s": round(t_s - t0, 1)}
+        marks[name] = (t_s, t_e)
+
+    # C0: the all-FP32 layer (CUDA-core FFMA; launch-bound at this size)
+    lin0 = workloads.config0()
+    X0, W0, b0 = d(lin0.X), d(lin0.W), d(lin0.bias).reshape(-1)
+    ads0 = ads_of(lin0)
+    Y0 = torch.empty(lin0.T, lin0.W.rows, dtype=torch.float32, device=dev)
+    t_s = time.time()
+    ms0 = timed(lambda: wpg.lora_linear_fwd(X0, W0, b0, ads0, lin0.request_scale, out=Y0), 200, 20)
+    marks["c0_tiny_fp32"] = (t_s, time.time())
+    fl0 = 2.0 * lin0.T * (128 * 256 + 8 * (128 + 256))
+    ffma_peak = device_sm_count(dev) * 128 * 2 * 2.07e9 / 1e12
+    out["c0_tiny_fp32"] = {"gflop": round(fl0 / 1e9, 5), "us": round(ms0 * 1e3, 2),
+                           "tflops": round(fl0 / (ms0 * 1e-3) / 1e12, 3), "bound": "alu (fp32 FFMA), launch-bound",
+                           "frac": round(fl0 / (ms0 * 1e-3) / 1e12 / ffma_peak, 5),
+                           "peak": f"{ffma_peak:.1f} TFLOP/s fp32 FFMA (SMs x 128 lanes x 2 x 2.07 GHz)"}
+
+    fwd_entry("wan_qkv_rank128", workloads.wan_qkv_rank128("full"),
+              "the sglang PR's own Speed Tests shape: rank 128 on each of q/k/v (two rank passes)")
+    up, down, _ = workloads.config2("full")
+    fwd_entry("c2_ffn_up", up)
+    del up
+    fwd_entry("c2_ffn_down", down)
+    del down
+    torch.cuda.empty_cache()
+    gate_up, down3 = workloads.config3("full")
+    fwd_entry("c3_nf4_gate_up_fwd", gate_up)
+    fwd_entry("c3_nf4_down_fwd", down3)
+    bwd_entry("c3_nf4_gate_up_bwd", gate_up)
+    bwd_entry("c3_nf4_down_bwd", down3)
+    del gate_up, down3
+    torch.cuda.empty_cache()
+    lin4, payload = workloads.config4("full")
+    fwd_entry("c4_sidecar", lin4, "three patches (ranks 16 fp32 / 32 / 128 bf16)")
+    # C4 .set_weight: one call at a time after an L2 flush, CUDA events around the call
+    P = d(payload)
+    param = torch.empty_like(P)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    times = []
+    t_s = time.time()
+    for i in range(k + 3):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        wpg.lora_dense_patch(param, P, wpg.WP_PATCH_SET, 1.0)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= 3:
+            times.append(e0.elapsed_time(e1))
+    marks["c4_set_weight"] = (t_s, time.time())
+    ms = statistics.median(times)
+    nbytes = 2 * P.numel() * P.element_size()
+    out["c4_set_weight"] = {"mb": round(nbytes / 1e6, 1), "ms": round(ms, 5),
+                            "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bound": "hbm",
+                            "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
+                            "timing": "one call after an L2 flush, launch included, median"}
+    clocks.stop()
+    for name, (a, b) in marks.items():
+        out[name]["clocks"] = clocks.summary(a, b)
+    return out
+
+
+def device_sm_count(dev):
+    import torch
+    return torch.cuda.get_device_properties(dev).multi_processor_count
 
 
 # ----------------------------------------------------------------------- CPU oracle
@@ -314,7 +505,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * total / len(t_steps), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "sample": f"{rows_per_step} token rows per step"},
+        "config": bench_config(ws),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
                          "kind": "oracle", "sample": f"{rows_per_step} of {T} token rows per step"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -330,9 +521,22 @@ def main():
     ap.add_argument("--impl", default="fused", choices=["fused", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-per-config", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    ws, _, _ = dist_env()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one rank per GPU: re-launch this command under torchrun
+        import socket
+        with socket.socket() as so:
+            so.bind(("127.0.0.1", 0))
+            port = so.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+        sys.exit(subprocess.call(cmd))
+    if ws != args.gpus:
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={ws}")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -132,10 +132,13 @@ enum { WP_OP_FWD = 0, WP_OP_FWD_GROUPED = 1, WP_OP_BWD = 2, WP_OP_FWD_HOST = 3, 
  *            (may be NULL when that size is 0).
  * Alignment (tensor-core path): every base pointer 16-byte aligned, every ld a
  * multiple of 8 elements (bf16) / 4 (fp32), in % 8 == 0, out % 8 == 0.
- * Limits (tensor-core path): at most 8 adapters on the tensor cores, whose rank
- * columns fit one 256-column accumulator: a bf16 adapter counts ceil(r / 16) * 16
- * columns, an FP32 adapter as pieces 3 * ceil(r / 16) * 16 (FP32 adapters that do not
- * fit take the CUDA-core route, at most 4 of them).
+ * Limits (tensor-core path): at most 8 adapters on the tensor cores, each of rank <= 256.
+ * A bf16 adapter counts ceil(r / 16) * 16 rank columns, an FP32 adapter as pieces
+ * 3 * ceil(r / 16) * 16.  When the adapters' rank columns fit one 256-column accumulator,
+ * s X A^T of all of them comes from one extra pass over X per 256 token rows; otherwise
+ * the adapters (whole) are grouped into several such rank passes of at most 256 columns
+ * each (e.g. three rank-128 q/k/v adapters: two passes), and FP32 adapters then take the
+ * CUDA-core route (at most 4 of them), as they do whenever their pieces do not fit.
  * Few tokens (bf16 X and adapters): one to four tokens with in % 256 == 0 stream the
  * weight once on the CUDA cores; up to 64 tokens with a WP_NF4 weight (4 with bf16)
  * stream it through swapped tensor-core MMAs.  Both keep the same W_eff and the single
@@ -263,8 +266,8 @@ int lora_swiglu_bwd(const wp_mat* dH, const wp_mat* EG, const wp_out* dEG, const
  *   X [T, in] WP_BF16; W [G*out_g, in] WP_BF16 or WP_NF4; dY [T, G*out_g] WP_BF16.
  *   dX: WP_BF16 or WP_FP32 output, or NULL to skip; dA[g], dB[g]: WP_FP32 outputs.
  *   dA/dB are overwritten (not accumulated).
- * Limits: bf16 adapters, r_g <= 64 each, sum over groups of ceil(r_g / 16) * 16 <= 256;
- * in % 8 == 0 and out_g % 8 == 0.
+ * Limits: bf16 adapters, r_g <= 128 each (any sum over the groups); in % 8 == 0 and
+ * out_g % 8 == 0.
  */
 int lora_linear_bwd(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int32_t n_groups,
                     const wp_adapter* adapters, double request_scale, const wp_out* dX,

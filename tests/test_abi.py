@@ -87,9 +87,11 @@ def test_fwd_rejections(lib):
     assert _fwd(lib, X, W, None, [], _o(64, 256, ld=260)) == -4
     # bf16 adapters need workspace too (their H~ rows); none given
     assert _fwd(lib, X, W, None, [_ad(8, 128, 256)], Y) == -5
-    # too many bf16 adapters' rank columns for one tensor-memory accumulator buffer
-    many = [_ad(128, 128, 256) for _ in range(3)]
-    assert _fwd(lib, X, W, None, many, Y, ws=FAKE, ws_bytes=1 << 30) == -8
+    # an adapter wider than one tensor-memory accumulator buffer, and more bf16 adapters than
+    # the kernel carries (several adapters of 384 rank columns in all are served, in passes)
+    assert _fwd(lib, X, W, None, [_ad(264, 128, 256)], Y, ws=FAKE, ws_bytes=1 << 30) == -8
+    nine = [_ad(8, 128, 256) for _ in range(9)]
+    assert _fwd(lib, X, W, None, nine, Y, ws=FAKE, ws_bytes=1 << 30) == -8
 
 
 def test_grouped_rejections(lib):

@@ -134,3 +134,31 @@ def test_bwd_nf4_full_sampled():
         eB = (4.0 * (K + T + 32) * 2.0 ** -24 + 2.0 ** -16) * magB[i]
         gu.assert_elementwise(gA, sumA[i], gu.ulp_f32(np.abs(sumA[i]) + eA) + eA, f"dA[{i}]")
         gu.assert_elementwise(gB, sumB[i], gu.ulp_f32(np.abs(sumB[i]) + eB) + eB, f"dB[{i}]")
+
+
+@pytest.mark.parametrize("ranks", [(128, 128, 128), (100,), (128, 16)])
+def test_bwd_large_ranks(ranks):
+    """Ranks up to 128 per group: the pieces of every group do not fit one 256-column
+    contraction, so dA / dB run one contraction per group; the dX pass takes several rank
+    passes."""
+    rng = np.random.default_rng(sum(ranks))
+    G = len(ranks)
+    T, K, og = 300, 192, 136
+    X = workloads.draw(rng, T, K, 1.0)
+    W = workloads.draw(rng, G * og, K, (1.0 / K) ** 0.5)
+    patches = [workloads.Patch(workloads.draw(rng, r, K, (1.0 / K) ** 0.5), workloads.draw(rng, og, r, 0.02),
+                               float(r), 0.8) for r in ranks]
+    lin = _with_dY(workloads.Linear("bwd_large_r", X, W, None, patches, request_scale=1.1, groups=G), 50 + G)
+    dX, dA, dB = _run(lin)
+    _check_full(lin, dX, dA, dB)
+
+
+def test_bwd_rank_above_limit_is_refused():
+    X = torch.zeros(64, 64, dtype=torch.bfloat16, device=gu.DEV)
+    W = torch.zeros(64, 64, dtype=torch.bfloat16, device=gu.DEV)
+    A = torch.zeros(136, 64, dtype=torch.bfloat16, device=gu.DEV)
+    B = torch.zeros(64, 136, dtype=torch.bfloat16, device=gu.DEV)
+    with pytest.raises(wpg.WeightPatchesError) as e:
+        wpg.lora_linear_bwd(X, W, torch.zeros(64, 64, dtype=torch.bfloat16, device=gu.DEV),
+                            [wpg.Adapter(A, B, 136.0)], 1.0)
+    assert e.value.status == -8

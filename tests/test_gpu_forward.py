@@ -164,6 +164,52 @@ def test_rank_mixes(ranks):
     _gate(*gu.errors(lin, Y))
 
 
+@pytest.mark.parametrize("ranks,nf4", [((200, 200, 48), False), ((256, 64), False), ((256, 256, 256, 256), False),
+                                       ((128, 128, 64), True), ((100, 30, 90, 50, 70), False)])
+def test_rank_passes(ranks, nf4):
+    """Adapters whose rank columns exceed one 256-column accumulator: s X A^T comes from
+    several rank passes per row block (adapters grouped whole, first-fit), with a 4-bit
+    weight too."""
+    rng = np.random.default_rng(sum(ranks) + nf4)
+    T, K, N = 600, 256, 384
+    X = workloads.draw(rng, T, K, 1.0)
+    W = workloads.draw_nf4(rng, N, K) if nf4 else workloads.draw(rng, N, K, (1.0 / K) ** 0.5)
+    bias = workloads.draw(rng, 1, N, 0.01)
+    patches = [workloads.Patch(workloads.draw(rng, r, K, (1.0 / K) ** 0.5), workloads.draw(rng, N, r, 0.02),
+                               float(r), 0.3 + 0.2 * i) for i, r in enumerate(ranks)]
+    lin = workloads.Linear("passes", X, W, bias, patches, request_scale=0.9)
+    Y = gu.run_fwd(lin)
+    assert wpg.lora_device_status() == 0
+    _gate(*gu.errors(lin, Y))
+
+
+def test_rank_passes_with_fp32_adapter():
+    """An FP32 adapter beside bf16 adapters of more than 256 rank columns: the bf16 ones take
+    two rank passes, the FP32 one the CUDA-core route; fp32 output to 1e-5."""
+    rng = np.random.default_rng(31)
+    T, K, N = 300, 192, 264
+    X = workloads.draw(rng, T, K, 1.0)
+    W = workloads.draw(rng, N, K, (1.0 / K) ** 0.5)
+    patches = [workloads.Patch(workloads.draw(rng, 16, K, (1.0 / K) ** 0.5, workloads.FP32),
+                               workloads.draw(rng, N, 16, 0.02, workloads.FP32), 16.0, 1.0)]
+    patches += [workloads.Patch(workloads.draw(rng, r, K, (1.0 / K) ** 0.5), workloads.draw(rng, N, r, 0.02),
+                                float(r), 0.6) for r in (160, 128)]
+    lin = workloads.Linear("passes32", X, W, None, patches, request_scale=1.0)
+    Y = gu.run_fwd(lin)
+    _gate(*gu.errors(lin, Y))
+    Y32 = gu.run_fwd(lin, out_dtype=torch.float32)
+    gu.errors(lin, Y32)                       # element-wise bound at fp32 output
+
+
+def test_wan_rank128_small():
+    """The pages' Wan2.1 adapter shape (rank 128 on each of q, k, v: 384 rank columns, two
+    rank passes) at a small size."""
+    lin = workloads.wan_qkv_rank128("small")
+    Y = gu.run_fwd(lin)
+    assert wpg.lora_device_status() == 0
+    _gate(*gu.errors(lin, Y))
+
+
 def test_rank_without_aligned_pitch_is_rejected():
     X = torch.zeros(16, 64, dtype=torch.bfloat16, device=gu.DEV)
     W = torch.zeros(64, 64, dtype=torch.bfloat16, device=gu.DEV)
@@ -209,4 +255,14 @@ def test_c4_full_sampled_rows():
     lin, _ = workloads.config4("full")
     Y = gu.run_fwd(lin)
     rows = workloads.sample_rows(lin.T, 96)
+    _gate(*gu.errors(lin, Y, rows))
+
+
+def test_wan_rank128_full_sampled_rows():
+    """The sglang PR's Wan2.1 1.3B 480p Speed Tests shape: T = 32760, 1536 -> 3 x 1536, rank
+    128 per group."""
+    lin = workloads.wan_qkv_rank128("full")
+    Y = gu.run_fwd(lin)
+    assert wpg.lora_device_status() == 0
+    rows = workloads.sample_rows(lin.T, 128)
     _gate(*gu.errors(lin, Y, rows))

@@ -259,8 +259,13 @@ int plan_fwd(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int n, FwdP
       plan->rank_cols += static_cast<int>((r + 15) / 16 * 16);
     }
   }
-  plan->pack_bytes = round256(static_cast<size_t>(std::min(plan->rank_cols, kHCols)) *
-                              static_cast<size_t>((X->cols + 7) / 8 * 8) * 2);
+  // packed A rows: one pass of rank_cols rows, or npass passes of at most kHCols rows each;
+  // the passes are filled first-fit, so at most one is half empty: npass <= 2 rank_cols /
+  // kHCols + 1 (and never more than the adapters)
+  size_t pack_rows = static_cast<size_t>(plan->rank_cols);
+  if (plan->rank_cols > kHCols)
+    pack_rows = static_cast<size_t>(kHCols) * std::min(n, 2 * plan->rank_cols / kHCols + 1);
+  plan->pack_bytes = round256(pack_rows * static_cast<size_t>((X->cols + 7) / 8 * 8) * 2);
   SkinnyPlan sp;
   if (plan_skinny(X, W, ad, n, &sp)) plan->skinny_bytes = sp.part_bytes;
   // legacy adapter bias vectors: an fp32 [out] vector ahead of everything else (out bounded
@@ -702,22 +707,43 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     if (eg) { p.eg = static_cast<uint16_t*>(eg->data); p.ld_eg = eg->ld; }
   }
   if (p.n_ad > 0) {
-    // Rank columns of the pair's MMA (N = htot = sum of pw): each CTA supplies half of
-    // every adapter's packed A rows, so both halves are equally wide
+    // Rank passes: the adapters (whole) go first-fit, widest first, into passes of at most
+    // kHCols rank columns, one accumulator buffer each; each pass is a rank item of its own
+    // per 256-row block.  Within a pass the pair's MMA has N = htot columns: each CTA
+    // supplies half of every adapter's packed A rows, so both halves are equally wide, and
+    // every pass is padded to the widest one (zero rows).
+    int order[kMaxAd], pass_w[kMaxAd] = {};
+    for (int k = 0; k < p.n_ad; ++k) order[k] = k;
+    std::stable_sort(order, order + p.n_ad, [&](int a, int b) { return p.ad[a].pw > p.ad[b].pw; });
+    int npass = 0;
+    for (int i = 0; i < p.n_ad; ++i) {
+      const int k = order[i];
+      if (p.ad[k].pw > kHCols) return WP_ERR_UNSUPPORTED;
+      int q = 0;
+      while (q < npass && pass_w[q] + p.ad[k].pw > kHCols) ++q;
+      if (q == npass) ++npass;
+      p.ad[k].pass = q;
+      pass_w[q] += p.ad[k].pw;
+    }
     int half = 0;
-    for (int k = 0; k < p.n_ad; ++k) half += p.ad[k].pw / 2;
-    if (2 * half > kHCols) return WP_ERR_UNSUPPORTED;
-    for (int k = 0, off = 0; k < p.n_ad; ++k) {
-      p.ad[k].hoff = off;
-      p.ad[k].hoff2 = half + off;
-      pk.ad[k].pw = p.ad[k].pw;
-      pk.ad[k].hoff = p.ad[k].hoff;
-      pk.ad[k].hoff2 = p.ad[k].hoff2;
-      off += p.ad[k].pw / 2;
+    for (int q = 0; q < npass; ++q) half = std::max(half, pass_w[q] / 2);
+    for (int q = 0; q < npass; ++q) {
+      for (int k = 0, off = 0; k < p.n_ad; ++k) {
+        if (p.ad[k].pass != q) continue;
+        p.ad[k].hoff = off;                     // TMEM columns within the pass
+        p.ad[k].hoff2 = half + off;
+        pk.ad[k].pw = p.ad[k].pw;
+        pk.ad[k].hoff = q * 2 * half + off;     // packed A rows
+        pk.ad[k].hoff2 = q * 2 * half + half + off;
+        off += p.ad[k].pw / 2;
+      }
     }
     p.htot = 2 * half;
+    p.npass = npass;
+    p.flag_target = 2u * static_cast<uint32_t>(npass);
     pk.n_ad = p.n_ad;
     pk.half = half;
+    pk.npass = npass;
     pk.flags = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + flags_off);
     pk.n_flags = p.r_blocks;
     p.hq = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + hq_off);
@@ -787,7 +813,8 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     if (rc != WP_OK) return rc;
   }
   if (p.n_ad > 0) {
-    rc = make_map_bf16(&maps.ap, pk.Ap, K, p.htot, pk.ldk, kBK, p.htot / 2);
+    if (static_cast<size_t>(p.npass) * p.htot * pk.ldk * 2 > plan.pack_bytes) return WP_ERR_WORKSPACE;
+    rc = make_map_bf16(&maps.ap, pk.Ap, K, static_cast<long long>(p.npass) * p.htot, pk.ldk, kBK, p.htot / 2);
     if (rc != WP_OK) return rc;
   }
   for (int k = 0; k < p.n_ad && !rank_only; ++k) {
@@ -807,7 +834,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   }
   int pairs = tc_max_pairs(smem, nf4);
   if (pairs <= 0) return WP_ERR_CUDA;
-  const int work = rank_only ? p.r_blocks : p.total_tiles;
+  const int work = rank_only ? p.r_blocks * std::max(1, p.npass) : p.total_tiles;
   if (pairs > work) pairs = work;
   // rank items two rounds of tiles ahead, or one when the X rows of two rounds would not
   // stay in L2 until their tiles come
@@ -819,15 +846,17 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
 // ------------------------------------------------------------------ backward
 // Workspace of lora_linear_bwd, in order (each region 256-byte aligned):
 //   W^T [in, Ntot] bf16 | per group: B_g^T padded to [r_g, Ntot] bf16 | per group: A_g^T
-//   [in, r8_g] bf16 | s G [T, R] fp32 | H [T, R] fp32 | reduction partials
+//   [in, r8_g] bf16 | s G [T, R] fp32 | H [T, R] fp32 | the bf16 pieces of H and of s G
+//   [T, tokN] | token-split partial sums | the forward calls' scratch
 struct BwdLayout {
-  size_t wt, bhat[kMaxGroups], at[kMaxGroups], gs, h, part, fwd, fwd_bytes, total;
+  size_t wt, bhat[kMaxGroups], at[kMaxGroups], gs, h, fwd, fwd_bytes, total;
   int r8[kMaxGroups];
   int roff[kMaxGroups];
   int R;
-  // dA / dB on the tensor cores (when the pieces fit N = 256): the bf16 pieces of H and of
-  // s G [T, tokN], and the token-split partial sums
-  bool tok;
+  // dA / dB on the tensor cores: H and s G as two bf16 pieces each (hi, lo) side by side, N
+  // = 128 or 256 columns per contraction.  All groups in one contraction when their pieces
+  // fit 256 columns; otherwise one contraction per group (each group's pieces fit: r <= 128).
+  bool per_group;
   int tokN, R16, roff16[kMaxGroups], splits_a, splits_b;
   size_t hp, gp, tpart;
 };
@@ -842,6 +871,10 @@ int tok_splits(int m_tiles, int k_blocks) {
   return s < 1 ? 1 : s;
 }
 
+// The largest rank the backward takes per group: the group's two bf16 pieces fill at most one
+// 256-column accumulator.
+constexpr int kBwdMaxRank = 128;
+
 bool bwd_layout(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int G, BwdLayout* L) {
   if (!X || !W || !ad || G < 1 || G > kMaxGroups) return false;
   const size_t T = static_cast<size_t>(X->rows), K = static_cast<size_t>(X->cols);
@@ -852,7 +885,6 @@ bool bwd_layout(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int G, B
   L->wt = off;
   off += round256(K * Ntot * 2);
   int R = 0;
-  size_t max_part = 0;
   for (int g = 0; g < G; ++g) {
     const int r = static_cast<int>(ad[g].A.rows);
     if (r <= 0) return false;
@@ -871,34 +903,28 @@ bool bwd_layout(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int G, B
   off += round256(T * R * 4);
   L->h = off;
   off += round256(T * R * 4);
-  for (int g = 0; g < G; ++g) {
-    const size_t r = static_cast<size_t>(ad[g].A.rows);
-    const int Tn = static_cast<int>(T);
-    const size_t pa = static_cast<size_t>(skinny_chunks(Tn, static_cast<int>(K))) * K * r;
-    const size_t pb = static_cast<size_t>(skinny_chunks(Tn, static_cast<int>(og))) * og * r;
-    max_part = std::max(max_part, std::max(pa, pb));
-  }
-  L->part = off;
-  off += round256(max_part * 4);
   L->R16 = 0;
+  int max16 = 0;
   for (int g = 0; g < G; ++g) {
+    const int r16 = static_cast<int>((ad[g].A.rows + 15) / 16 * 16);
     L->roff16[g] = L->R16;
-    L->R16 += static_cast<int>((ad[g].A.rows + 15) / 16 * 16);
+    L->R16 += r16;
+    max16 = std::max(max16, r16);
   }
-  L->tok = 2 * L->R16 <= 256 && K % 8 == 0 && Ntot % 8 == 0;
-  if (L->tok) {
-    L->tokN = 2 * L->R16 <= 128 ? 128 : 256;
-    const int kbt = static_cast<int>((T + 63) / 64);
-    L->splits_a = tok_splits(static_cast<int>((K + 255) / 256), kbt);
-    L->splits_b = tok_splits(static_cast<int>((Ntot + 255) / 256), kbt);
-    L->hp = off;
-    off += round256(T * L->tokN * 2);
-    L->gp = off;
-    off += round256(T * L->tokN * 2);
-    L->tpart = off;
-    off += round256(std::max(static_cast<size_t>(L->splits_a) * K, static_cast<size_t>(L->splits_b) * Ntot) *
-                    L->tokN * 4);
-  }
+  L->per_group = 2 * L->R16 > 256;
+  const int width = L->per_group ? max16 : L->R16;          // the widest contraction's ranks
+  L->tokN = 2 * width <= 128 ? 128 : 256;
+  const int kbt = static_cast<int>((T + 63) / 64);
+  const size_t Mb = L->per_group ? og : Ntot;                // dB's rows per contraction
+  L->splits_a = tok_splits(static_cast<int>((K + 255) / 256), kbt);
+  L->splits_b = tok_splits(static_cast<int>((Mb + 255) / 256), kbt);
+  L->hp = off;
+  off += round256(T * L->tokN * 2);
+  L->gp = off;
+  off += round256(T * L->tokN * 2);
+  L->tpart = off;
+  off += round256(std::max(static_cast<size_t>(L->splits_a) * K, static_cast<size_t>(L->splits_b) * Mb) *
+                  L->tokN * 4);
   // workspace of the forward call that computes dX: X := dY [T, Ntot], W := W^T, adapter g
   // A := B_g^T padded to [r_g, Ntot] (bf16), B := A_g^T [K, r_g]
   {
@@ -948,27 +974,24 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
     if (dX->rows != T || dX->cols != K) return WP_ERR_SHAPE;
   }
   float s_of[kMaxGroups];
-  int rank_cols = 0;                 // the dX forward's rank-item width
   for (int g = 0; g < G; ++g) {
     const wp_adapter& a = ad[g];
     if (!valid_input(&a.A, false) || !valid_input(&a.B, false)) return WP_ERR_INVALID;
     if (a.A.dtype != WP_BF16 || a.B.dtype != WP_BF16) return WP_ERR_DTYPE;
     const long long r = a.A.rows;
     if (r <= 0) return WP_ERR_INVALID;
-    if (r > 64) return WP_ERR_UNSUPPORTED;
+    if (r > kBwdMaxRank) return WP_ERR_UNSUPPORTED;
     if (a.A.cols != K || a.B.rows != og || a.B.cols != r) return WP_ERR_SHAPE;
     if (!std::isfinite(a.alpha) || !std::isfinite(a.strength)) return WP_ERR_INVALID;
     const double s = a.alpha / static_cast<double>(r) * a.strength * request_scale;
     if (!std::isfinite(s) || !std::isfinite(static_cast<float>(s))) return WP_ERR_INVALID;
     s_of[g] = static_cast<float>(s);
-    rank_cols += static_cast<int>((r + 15) / 16 * 16);
     const wp_out& da = dA[g];
     const wp_out& db = dB[g];
     if (!valid_output(&da) || !valid_output(&db)) return WP_ERR_INVALID;
     if (da.dtype != WP_FP32 || db.dtype != WP_FP32) return WP_ERR_DTYPE;
     if (da.rows != r || da.cols != K || db.rows != og || db.cols != r) return WP_ERR_SHAPE;
   }
-  if (rank_cols > kHCols) return WP_ERR_UNSUPPORTED;
   BwdLayout L;
   if (!bwd_layout(X, W, ad, G, &L)) return WP_ERR_INVALID;
   if (!workspace || ws_bytes < L.total) return WP_ERR_WORKSPACE;
@@ -979,7 +1002,6 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
   uint16_t* Wt = reinterpret_cast<uint16_t*>(ws + L.wt);
   float* Gs = reinterpret_cast<float*>(ws + L.gs);
   float* H = reinterpret_cast<float*>(ws + L.h);
-  float* part = reinterpret_cast<float*>(ws + L.part);
   int rc;
 
   // 1. W^T [K, Ntot] bf16: the K-major B operand of dX = dY W
@@ -1042,94 +1064,83 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
     if (rc != WP_OK) return rc;
   }
 
-  // 5. dA_g = (s_g G_g)^T X  and  dB_g = s_g dY_g^T H_g  (exact zeros when s_g == 0): on the
-  //    tensor cores as token contractions with the fp32 H and s G as two bf16 pieces each,
-  //    or, when the pieces do not fit, by the split-T FFMA reduction below
-  if (L.tok) {
+  // 5. dA_g = (s_g G_g)^T X  and  dB_g = s_g dY_g^T H_g (exact zeros when s_g == 0): token
+  //    contractions on the tensor cores with the fp32 H and s G as two bf16 pieces each; all
+  //    groups in one contraction when their pieces fit 256 columns, else one per group
+  for (int g = 0; g < G; ++g) {
+    if (s_of[g] != 0.0f) continue;
+    for (const wp_out* o : {&dA[g], &dB[g]}) {
+      cudaError_t e = cudaMemset2DAsync(o->data, o->ld * 4, 0, o->cols * 4, o->rows, stream);
+      if (e != cudaSuccess) { set_last_cuda_error(e); return WP_ERR_CUDA; }
+    }
+  }
+  uint16_t* Hp = reinterpret_cast<uint16_t*>(ws + L.hp);
+  uint16_t* Gp = reinterpret_cast<uint16_t*>(ws + L.gp);
+  float* tpart = reinterpret_cast<float*>(ws + L.tpart);
+  const int Ti = static_cast<int>(T);
+  TokGemmParams tp{};
+  tp.T = Ti; tp.k_blocks = (Ti + 63) / 64;
+  tp.part = tpart;
+  tp.status = tc_status_ptr();
+  tp.timeout_ns = 2000000000ull;
+  if (!tp.status) return record_cuda();
+  const size_t sb = 2 * 64 * 128 + static_cast<size_t>(L.tokN) / 2 * 128;
+  tp.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - 1024 - 256) / sb));
+  const size_t smem = 1024 + tp.stages * sb + 256;
+  const int max_pairs = tokgemm_max_pairs(smem);
+  if (max_pairs <= 0) return WP_ERR_CUDA;
+  // one contraction per entry of this loop: all groups at once (g0 = 0, g1 = G), or group g0
+  for (int g0 = 0; g0 < G; ) {
+    const int g1 = L.per_group ? g0 + 1 : G;
     bool any = false;
-    for (int g = 0; g < G; ++g) any = any || s_of[g] != 0.0f;
+    for (int g = g0; g < g1; ++g) any = any || s_of[g] != 0.0f;
+    if (!any) { g0 = g1; continue; }
     TokPieceMap pm{};
-    pm.G = G; pm.R16 = L.R16;
-    for (int g = 0; g < G; ++g) {
-      pm.roff16[g] = L.roff16[g]; pm.off[g] = L.roff[g]; pm.r[g] = static_cast<int>(ad[g].A.rows);
+    pm.G = g1 - g0;
+    for (int g = g0; g < g1; ++g) {
+      const int k = g - g0;
+      pm.roff16[k] = L.roff16[g] - L.roff16[g0];
+      pm.off[k] = L.roff[g];
+      pm.r[k] = static_cast<int>(ad[g].A.rows);
     }
-    uint16_t* Hp = reinterpret_cast<uint16_t*>(ws + L.hp);
-    uint16_t* Gp = reinterpret_cast<uint16_t*>(ws + L.gp);
-    float* tpart = reinterpret_cast<float*>(ws + L.tpart);
-    const int N = L.tokN;
-    const int Ti = static_cast<int>(T);
-    if (any) {
-      rc = launch_pieces(H, L.R, Ti, N, pm, Hp, stream);
-      if (rc == WP_OK) rc = launch_pieces(Gs, L.R, Ti, N, pm, Gp, stream);
-      if (rc != WP_OK) return rc;
-    }
-    TokGemmParams tp{};
-    tp.T = Ti; tp.N = N; tp.k_blocks = (Ti + 63) / 64;
-    tp.part = tpart;
-    tp.status = tc_status_ptr();
-    tp.timeout_ns = 2000000000ull;
-    if (!tp.status) return record_cuda();
-    const size_t sb = 2 * 64 * 128 + static_cast<size_t>(N) / 2 * 128;
-    tp.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - 1024 - 256) / sb));
-    const size_t smem = 1024 + tp.stages * sb + 256;
-    const int max_pairs = tokgemm_max_pairs(smem);
-    if (max_pairs <= 0) return WP_ERR_CUDA;
-    // (A, M, splits, then per group: finish into dB_g rows or dA_g transposed)
-    for (int pass = 0; pass < 2 && any; ++pass) {
+    pm.R16 = (g1 < G ? L.roff16[g1] : L.R16) - L.roff16[g0];
+    const int N = 2 * pm.R16 <= 128 ? 128 : 256;
+    tp.N = N;
+    rc = launch_pieces(H, L.R, Ti, N, pm, Hp, stream);
+    if (rc == WP_OK) rc = launch_pieces(Gs, L.R, Ti, N, pm, Gp, stream);
+    if (rc != WP_OK) return rc;
+    // dB rows: every group's columns of dY at once, or group g0's alone
+    const long long mb0 = L.per_group ? g0 * og : 0, Mb = L.per_group ? og : Ntot;
+    for (int pass = 0; pass < 2; ++pass) {
       const bool db = pass == 0;
       TokGemmMaps tm;
       std::memset(&tm, 0, sizeof(tm));
-      const long long M = db ? Ntot : K;
+      const long long M = db ? Mb : K;
       tp.M = static_cast<int>(M);
       tp.m_tiles = static_cast<int>((M + 255) / 256);
       tp.splits = db ? L.splits_b : L.splits_a;
       tp.kb_per_split = (tp.k_blocks + tp.splits - 1) / tp.splits;
       tp.splits = (tp.k_blocks + tp.kb_per_split - 1) / tp.kb_per_split;
       tp.units = tp.m_tiles * tp.splits;
-      rc = db ? make_map_bf16(&tm.a, dY->data, Ntot, T, dY->ld, 64, 64)
+      rc = db ? make_map_bf16(&tm.a, static_cast<const uint16_t*>(dY->data) + mb0, Mb, T, dY->ld, 64, 64)
               : make_map_bf16(&tm.a, X->data, K, T, X->ld, 64, 64);
       if (rc == WP_OK) rc = make_map_bf16(&tm.b, db ? Hp : Gp, N, T, N, 64, 64);
       if (rc != WP_OK) return rc;
       rc = launch_tokgemm(tm, tp, std::min(max_pairs, tp.units), smem, stream);
       if (rc != WP_OK) return rc;
-      for (int g = 0; g < G; ++g) {
+      for (int g = g0; g < g1; ++g) {
         const int r = static_cast<int>(ad[g].A.rows);
         if (s_of[g] == 0.0f) continue;
-        rc = db ? launch_tok_finish(tpart, tp.M, N, tp.splits, L.R16, L.roff16[g], r, static_cast<int>(g * og),
+        const int ro = L.roff16[g] - L.roff16[g0];
+        rc = db ? launch_tok_finish(tpart, tp.M, N, tp.splits, pm.R16, ro, r, static_cast<int>(g * og - mb0),
                                     static_cast<int>(og), s_of[g], static_cast<float*>(dB[g].data), dB[g].ld,
                                     false, stream)
-                : launch_tok_finish(tpart, tp.M, N, tp.splits, L.R16, L.roff16[g], r, 0, static_cast<int>(K), 1.0f,
+                : launch_tok_finish(tpart, tp.M, N, tp.splits, pm.R16, ro, r, 0, static_cast<int>(K), 1.0f,
                                     static_cast<float*>(dA[g].data), dA[g].ld, true, stream);
         if (rc != WP_OK) return rc;
       }
     }
-    for (int g = 0; g < G; ++g) {
-      if (s_of[g] != 0.0f) continue;
-      for (const wp_out* o : {&dA[g], &dB[g]}) {
-        cudaError_t e = cudaMemset2DAsync(o->data, o->ld * 4, 0, o->cols * 4, o->rows, stream);
-        if (e != cudaSuccess) { set_last_cuda_error(e); return WP_ERR_CUDA; }
-      }
-    }
-    return WP_OK;
-  }
-  for (int g = 0; g < G; ++g) {
-    const int r = static_cast<int>(ad[g].A.rows);
-    if (s_of[g] == 0.0f) {
-      for (const wp_out* o : {&dA[g], &dB[g]}) {
-        cudaError_t e = cudaMemset2DAsync(o->data, o->ld * 4, 0, o->cols * 4, o->rows, stream);
-        if (e != cudaSuccess) { set_last_cuda_error(e); return WP_ERR_CUDA; }
-      }
-      continue;
-    }
-    rc = launch_skinny(X->data, WP_BF16, X->ld, static_cast<int>(T), static_cast<int>(K),
-                       Gs + L.roff[g], L.R, r, 1.0f, part, static_cast<float*>(dA[g].data), dA[g].ld,
-                       /*transposed=*/true, stream);
-    if (rc != WP_OK) return rc;
-    const uint16_t* dyg = static_cast<const uint16_t*>(dY->data) + g * og;
-    rc = launch_skinny(dyg, WP_BF16, dY->ld, static_cast<int>(T), static_cast<int>(og),
-                       H + L.roff[g], L.R, r, s_of[g], part, static_cast<float*>(dB[g].data), dB[g].ld,
-                       /*transposed=*/false, stream);
-    if (rc != WP_OK) return rc;
+    g0 = g1;
   }
   return WP_OK;
 }

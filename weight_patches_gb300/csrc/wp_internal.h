@@ -51,6 +51,7 @@ struct TcAdapter {
   int toff;        // first column of this adapter's H~ (multiple of 16)
   int nchunks;     // ceil(r / 64)
   int hout_off;    // column of this adapter's s * X A^T in TcParams::h_out (if stored)
+  int pass;        // rank pass whose MMA computes this adapter's X A^T (hoff, hoff2 within it)
   float s;         // combined scale, fp32
 };
 
@@ -75,6 +76,10 @@ struct TcParams {
   int n_ad;                    // adapters on the tensor cores (bf16, or FP32 as pieces)
   int ad_begin[kMaxGroups + 1];
   int htot;                    // rank-item MMA width: twice the larger CTA half (<= 256)
+  int npass;                   // rank passes per 256-row block: the adapters' rank columns in
+                               // groups of at most 256 (htot wide each), one rank item per pass
+  uint32_t flag_target;        // a block's H~ rows are complete when its flag reaches this
+                               // (2 npass: one release per CTA per pass)
   int stages;
   int stage_bytes;             // bf16 W: 32 KiB; 4-bit W: 2 x 16 KiB X + 16 KiB dequantised W
   int code_slots;              // 4-bit W: ring of [4 KiB codes | 2 KiB block scales] slots, loaded
@@ -85,7 +90,8 @@ struct TcParams {
   TcAdapter ad[kMaxAd];
   uint16_t* hq;                // [T, hq_ld] bf16: H~ = s X A^T of every adapter (toff columns)
   int hq_ld;
-  uint32_t* flags;             // [r_blocks]: 2 once both CTAs wrote the block's H~ rows
+  uint32_t* flags;             // [r_blocks]: flag_target once both CTAs of every pass wrote the
+                               // block's H~ rows
   int n_ad32;                  // fp32 adapters (epilogue FFMA)
   TcAdapter32 ad32[kMaxAd32];
   float* h_out;                // optional [T, h_out_ld] fp32: s * X A^T of the bf16 adapters
@@ -121,7 +127,7 @@ struct TcMaps {
   CUtensorMap am;                // 4-bit W block scales: [N rows, K/64] fp32, boxes of 128 x 4
   CUtensorMap hq;                // H~ [T rows, hq_ld], boxes of 128 rows x 64 ranks
   CUtensorMap hq32;              // the same with boxes of 128 rows x 32 ranks (64-byte swizzle)
-  CUtensorMap ap;                // packed A rows [htot, K]: boxes of htot/2 rows x 64
+  CUtensorMap ap;                // packed A rows [npass htot, K]: boxes of htot/2 rows x 64
   CUtensorMap b[kMaxAd];
   CUtensorMap b32[kMaxAd];       // B with boxes of 128 rows x 32 ranks (64-byte swizzle)
 };
@@ -300,11 +306,12 @@ int launch_h32(const H32Params& p, cudaStream_t stream);
 // row j, and its B becomes Bs [out, 6 rp] = [b1 b2 b1 b3 b2 b1].
 struct PackAdapter {
   const void* A; long long lda; int dtype;
-  int r, pw, rp, hoff, hoff2, split3;
+  int r, pw, rp, hoff, hoff2, split3;   // hoff, hoff2: packed rows (pass q's rows start at q htot)
   const float* B; long long ldb; int out; uint16_t* Bs;   // FP32 adapters only
 };
 struct PackParams {
-  int n_ad, K, ldk, half;
+  int n_ad, K, ldk, half;        // half = htot / 2: the packed A rows are npass blocks of htot rows
+  int npass;
   int rows_total;                // set by launch_rank_pack
   uint16_t* Ap;
   uint32_t* flags;               // row-block flags of the forward kernel, cleared here
@@ -416,12 +423,6 @@ int launch_transpose_bf16(const void* src, long long ld_s, int R, int C, void* d
                           cudaStream_t stream);
 int launch_nf4_dequant_t(const void* codes, const float* absmax, int N, int K, const NF4Table& tab,
                          void* dst, long long ld_d, cudaStream_t stream);
-int skinny_chunks(int T, int M);
-// out = scale * P^T Q (M x R), or its transpose; P [T, M] bf16/fp32, Q [T, R] fp32, R <= 64;
-// `part` holds skinny_chunks(T, M) * M * R floats.
-int launch_skinny(const void* P, int p_dtype, long long ldp, int T, int M, const float* Q,
-                  long long ldq, int R, float scale, float* part, float* out, long long ldo,
-                  bool transposed, cudaStream_t stream);
 
 // ------------------------------------------------------------------ dense patch
 int launch_dense_patch(void* param, int param_dtype, const void* payload, int payload_dtype,

@@ -361,18 +361,21 @@ __global__ void __launch_bounds__(256) rank_pack_kernel(const PackParams p) {
   // finish before it touches the packed rows, the B pieces or the flags
   grid_launch_dependents();
   const int htot = 2 * p.half;
+  const int arows = htot * p.npass;
   if (blockIdx.x == 0 && blockIdx.y == 0)
     for (int i = threadIdx.x; i < p.n_flags; i += blockDim.x) p.flags[i] = 0u;
   for (int vr = blockIdx.y; vr < p.rows_total; vr += gridDim.y) {
-    if (vr < htot) {
-      // packed A row pr: find the adapter and rank column it holds
+    if (vr < arows) {
+      // packed A row pr of pass pr / htot: find the adapter and rank column it holds (rows
+      // past the pass's adapters are zero)
       const int pr = vr;
+      const bool first_half = pr % htot < p.half;
       int da = -1, u = 0;
       for (int a = 0; a < p.n_ad; ++a) {
-        const int base = pr < p.half ? p.ad[a].hoff : p.ad[a].hoff2;
+        const int base = first_half ? p.ad[a].hoff : p.ad[a].hoff2;
         if (pr >= base && pr < base + p.ad[a].pw / 2) {
           da = a;
-          u = pr - base + (pr < p.half ? 0 : p.ad[a].pw / 2);
+          u = pr - base + (first_half ? 0 : p.ad[a].pw / 2);
         }
       }
       const bool split3 = da >= 0 && p.ad[da].split3;
@@ -407,7 +410,7 @@ __global__ void __launch_bounds__(256) rank_pack_kernel(const PackParams p) {
       }
     } else {
       // B-piece row: (adapter, output row o) in order
-      int f = vr - htot;
+      int f = vr - arows;
       for (int a = 0; a < p.n_ad; ++a) {
         const PackAdapter& d = p.ad[a];
         if (!d.split3) continue;
@@ -428,7 +431,7 @@ __global__ void __launch_bounds__(256) rank_pack_kernel(const PackParams p) {
 
 int launch_rank_pack(const PackParams& p0, cudaStream_t stream) {
   PackParams p = p0;
-  p.rows_total = 2 * p.half;
+  p.rows_total = 2 * p.half * p.npass;
   for (int a = 0; a < p.n_ad; ++a)
     if (p.ad[a].split3) p.rows_total += p.ad[a].out;
   if (p.rows_total == 0 && p.n_flags == 0) return WP_OK;

@@ -75,14 +75,17 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, int L) {
 // A tile of round k waits only for rank items of rounds < k, and every pair walks its
 // items in order, so the schedule cannot deadlock while all pairs are resident.
 struct Item {
-  bool rank;   // rank item (X_m A^T of every adapter) rather than an output tile
+  bool rank;   // rank item (X_m A^T of the adapters of one rank pass) rather than an output tile
   int m;       // row block
+  int q;       // rank pass (rank items)
   Tile t;      // the tile (output items)
 };
 
+// Rank items are numbered i = m * npass + q (row block m, pass q); item i belongs to pair
+// (i + total_tiles) mod npairs.
 struct ItemIter {
   int k;        // next tile round of this pair
-  int m_next;   // next row block whose rank item this pair owns
+  int m_next;   // next rank item this pair owns
 };
 
 __device__ __forceinline__ ItemIter item_iter_begin(const TcParams& p, int pair, int npairs) {
@@ -93,12 +96,13 @@ __device__ __forceinline__ ItemIter item_iter_begin(const TcParams& p, int pair,
 __device__ __forceinline__ bool next_item(ItemIter& s, const TcParams& p, int pair, int npairs,
                                           Item& it) {
   const int tile_pos = pair + s.k * npairs;
-  if (p.n_ad > 0 && s.m_next < p.r_blocks) {
-    const int due =
-        static_cast<int>((static_cast<long long>(s.m_next >> p.m_shift) * p.G * p.nt_g) / npairs) - p.rlead;
+  if (p.n_ad > 0 && s.m_next < p.r_blocks * p.npass) {
+    const int m = s.m_next / p.npass;
+    const int due = static_cast<int>((static_cast<long long>(m >> p.m_shift) * p.G * p.nt_g) / npairs) - p.rlead;
     if (due <= s.k || tile_pos >= p.total_tiles) {
       it.rank = true;
-      it.m = s.m_next;
+      it.m = m;
+      it.q = s.m_next - m * p.npass;
       it.t = Tile{0, 0, 0};
       s.m_next += npairs;
       return true;
@@ -106,6 +110,7 @@ __device__ __forceinline__ bool next_item(ItemIter& s, const TcParams& p, int pa
   }
   if (tile_pos >= p.total_tiles) return false;
   it.rank = false;
+  it.q = 0;
   it.t = decode_tile(p, tile_pos);
   it.m = it.t.m;
   ++s.k;
@@ -282,13 +287,14 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       while (ok && next_item(iter, p, pair, npairs, it)) {
         if (it.rank) {
           const int x_row = it.m * kPairM + static_cast<int>(cta) * kBM;
-          // X rows of the block and this CTA's half of the packed A rows (one box each)
+          const int a_row = it.q * p.htot + static_cast<int>(cta) * half;   // the pass's packed rows
+          // X rows of the block and this CTA's half of the pass's packed A rows (one box each)
           for (int kb = 0; kb < p.k_blocks; ++kb) {
             uint8_t* st;
             uint32_t fb;
             if (!(ok = claim(2u * kATileBytes + rank_tx, st, fb))) break;
             tma_load_2d_pair(st, &maps.x, kb * kBK, x_row, fb);
-            tma_load_2d_pair_hint(st + kATileBytes, &maps.ap, kb * kBK, static_cast<int>(cta) * half, fb, keep);
+            tma_load_2d_pair_hint(st + kATileBytes, &maps.ap, kb * kBK, a_row, fb, keep);
             advance();
           }
           continue;
@@ -301,7 +307,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         const int nblk = min(kMH, p.r_blocks - blk0);
         // the blocks' flags, read (acquire) before the base K loop: the read's latency is
         // covered by the stages already queued for the MMA, and the flags are usually set
-        uint32_t peek = 2u;
+        uint32_t peek = p.flag_target;
         if (a1 > a0)
           for (int h = 0; h < nblk; ++h) peek = min(peek, ld_acquire_gpu(p.flags + blk0 + h));
         if (p.has_base) {
@@ -329,8 +335,8 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         if (a1 > a0) {
           // second contraction: H~ of the tile's rows (written by the rank items of its
           // blocks) and B
-          for (int h = 0; h < nblk && ok && peek < 2u; ++h)
-            ok = flag_wait(p.flags + blk0 + h, 2u, abort_flag, tmo, status);
+          for (int h = 0; h < nblk && ok && peek < p.flag_target; ++h)
+            ok = flag_wait(p.flags + blk0 + h, p.flag_target, abort_flag, tmo, status);
           if (!ok) break;
           fence_proxy_async_global();
           for (int a = a0; a < a1 && ok; ++a) {
@@ -534,6 +540,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         const bool row_ok = row < p.T;
         uint16_t* hrow = p.hq + static_cast<long long>(row_ok ? row : 0) * p.hq_ld;
         for (int a = 0; a < p.n_ad; ++a) {
+          if (p.ad[a].pass != it.q) continue;          // another pass's adapter
           const float s = p.ad[a].s;
           const int units = p.ad[a].pw >> 3;           // 8 rank columns per unit
           // TMEM column of unit u: the two halves of an adapter's columns may lie apart

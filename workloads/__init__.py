@@ -274,6 +274,24 @@ def config4(scale: str = "full") -> tuple:
     return lin, payload
 
 
+def wan_qkv_rank128(scale: str = "full") -> Linear:
+    """The sglang PR's own Speed Tests shape for Wan2.1 1.3B 480p: stacked q/k/v of the
+    1536-wide attention (T = 32760 = 21 x 30 x 52 latent tokens) with a rank-128 adapter
+    per group (alpha = 128, strength 1, scale 1), bf16, no bias.  "small" keeps the three
+    rank-128 groups at T = 600, in = 256, out = 3 x 320."""
+    T, di, do = (32760, 1536, 1536) if scale == "full" else (600, 256, 320)
+    G, r = 3, 128
+    rng = np.random.default_rng(11)
+    X = draw(rng, T, di, 1.0)
+    W = draw(rng, G * do, di, (1.0 / di) ** 0.5)
+    patches = []
+    for _ in range(G):
+        A = draw(rng, r, di, (1.0 / di) ** 0.5)
+        B = draw(rng, do, r, 0.02)
+        patches.append(Patch(A, B, float(r), 1.0))
+    return Linear("wan_qkv_rank128", X, W, None, patches, request_scale=1.0, groups=G)
+
+
 def combined_scale_inputs(lin: Linear):
     """(alpha, rank, strength, request_scale) per patch, as stored (no arithmetic)."""
     return [(p.alpha, p.rank, p.strength, lin.request_scale) for p in lin.patches]
