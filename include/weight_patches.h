@@ -107,7 +107,8 @@ typedef struct wp_adapter {
 } wp_adapter;
 
 /* Operation ids for lora_workspace_size(). */
-enum { WP_OP_FWD = 0, WP_OP_FWD_GROUPED = 1, WP_OP_BWD = 2, WP_OP_FWD_HOST = 3, WP_OP_SWIGLU_FWD = 4, WP_OP_MERGE = 5 };
+enum { WP_OP_FWD = 0, WP_OP_FWD_GROUPED = 1, WP_OP_BWD = 2, WP_OP_FWD_HOST = 3, WP_OP_SWIGLU_FWD = 4, WP_OP_MERGE = 5,
+       WP_OP_FWD_EXACT = 6 };
 
 /*
  * lora_linear_fwd -- Y = X W^T + bias + sum_p s_p (X A_p^T) B_p^T.
@@ -292,6 +293,35 @@ int lora_dense_patch(void* param, int32_t param_dtype, int64_t param_numel,
                      int32_t kind, double strength, void* stream);
 
 /*
+ * lora_linear_fwd_exact -- the unfused dynamic-LoRA chain, the "exact" tier.
+ * (sglang PR "[diffusion] Add the dynamic LoRA delta inside the second GEMM", Motivation:
+ *  the chain every dynamic layer ran before the fused design; Modifications: the exact
+ *  tier keeps that chain and skips multiplications by a unit scale, which leaves every bit
+ *  of the output as it was.)
+ *     Y = bf16(X W^T + bias)
+ *     for each adapter p, in order (its column group when n_groups > 0):
+ *       t = bf16(X A_p^T);  d = bf16(t B_p^T [+ bias_B,p])
+ *       d = bf16(d * c) for c = fl32(alpha_p / r_p), fl32(strength_p), fl32(request_scale)
+ *       Y = bf16(Y + d)
+ *   An FP32 adapter keeps its two GEMMs and its scaling in FP32 (s = alpha/r * strength *
+ *   request_scale formed in double) and is added once: Y = bf16(Y + fl32 delta).
+ *   skip_unit_scales != 0 skips each scale multiplication whose c is exactly 1.0 (the PR's
+ *   exact tier); 0 runs every one (the chain before the PR).  The two give bit-identical Y.
+ *   Every elementwise step is the correctly rounded bf16 of its exact result; the GEMMs sum
+ *   in fp32 on the tensor cores.  This path materialises t and d (it is the reference the
+ *   fused lora_linear_fwd improves on), so it is slower by design.
+ *   X [T, in] WP_BF16; W [n_groups * out_g, in] (or [out, in]) WP_BF16 or WP_NF4; bias as
+ *   lora_linear_fwd; adapters: n_adapters (== n_groups when n_groups > 0); Y [T, out] WP_BF16.
+ *   workspace: lora_workspace_size(WP_OP_FWD_EXACT, X, W, adapters, n_adapters) bytes.
+ * Limits: bf16 adapters of rank r % 8 == 0 (t is a GEMM output); out_g % 8 == 0; the
+ * alignment rules of lora_linear_fwd.  Errors as lora_linear_fwd.
+ */
+int lora_linear_fwd_exact(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int32_t n_groups,
+                          const wp_adapter* adapters, int32_t n_adapters, double request_scale,
+                          int32_t skip_unit_scales, const wp_out* Y, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/*
  * lora_linear_fwd_noalloc -- lora_linear_fwd for callers that cannot provide or allocate
  * device scratch memory.  The pages have no counterpart: this is a deployment variant.
  *
@@ -334,6 +364,21 @@ const char* lora_status_string(int status);
 /* Reads (and, if `reset` != 0, clears) the device status word of the current device:
  * WP_OK or WP_ERR_TIMEOUT.  Synchronous: call after the stream has finished. */
 int lora_device_status(int32_t reset);
+
+/* How long every bounded device wait of the library's kernels spins (mbarriers, the fused
+ * forward's row-block flags) before the kernel records WP_ERR_TIMEOUT in the device status
+ * word, drains its own copies in flight, frees its tensor memory and returns.  Applies to
+ * calls made after it, process-wide.  Default 2 s; accepted range 1 ms .. 60 s, otherwise
+ * WP_ERR_INVALID and the setting is unchanged.  Not in the pages: a safety bound of this
+ * library's persistent kernels. */
+int lora_set_wait_limit(uint64_t timeout_ns);
+
+/* Test hook for the timeout path (not in the pages): while `on` is non-zero, the tiles of
+ * every fused forward launched afterwards wait for one more release of their row-block flag
+ * than any rank item gives, so that bounded wait runs out (after lora_set_wait_limit's
+ * limit) and the call's outputs are left undefined; lora_device_status() then reads
+ * WP_ERR_TIMEOUT.  Process-wide; 0 restores normal operation.  Always returns WP_OK. */
+int lora_debug_hold_flags(int32_t on);
 
 /* The library's 16 NormalFloat levels in ascending order (host memory, fp32). */
 void lora_nf4_codebook(float out[16]);

@@ -170,3 +170,15 @@ def test_workspace_reserves_the_folded_bias(lib):
     a = lib.lora_workspace_size(wpg.WP_OP_FWD, ctypes.byref(X), ctypes.byref(W), plain, 1)
     b = lib.lora_workspace_size(wpg.WP_OP_FWD, ctypes.byref(X), ctypes.byref(W), vec, 1)
     assert b - a == 256 * 4 + (-(256 * 4) % 256)                          # fp32 [out], 256-byte rounded
+
+
+def test_exact_tier_rejections(lib):
+    X, W, Y = _m(64, 128), _m(256, 128), _o(64, 256)
+    call = lambda ads, y=Y, groups=0: lib.lora_linear_fwd_exact(
+        ctypes.byref(X), ctypes.byref(W), None, groups, (wpg.WpAdapter * max(1, len(ads)))(*ads), len(ads), 1.0, 1,
+        ctypes.byref(y), ctypes.c_void_p(FAKE), 1 << 30, None)
+    assert call([_ad(12, 128, 256)]) == -4                     # t = X A^T needs r % 8 == 0
+    assert call([_ad(8, 128, 256)], y=_o(64, 256, dtype=wpg.WP_FP32)) == -3   # the chain's Y is bf16
+    assert call([_ad(8, 128, 256)], groups=2) == -1            # one adapter per group
+    assert lib.lora_workspace_size(wpg.WP_OP_FWD_EXACT, ctypes.byref(X), ctypes.byref(W),
+                                   (wpg.WpAdapter * 1)(_ad(8, 128, 256)), 1) >= 64 * 256 * 4

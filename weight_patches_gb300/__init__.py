@@ -10,6 +10,7 @@ Entry points (same names as the C ABI):
     lora_linear_fwd          Y = X W^T + bias + sum_p s_p (X A_p^T) B_p^T
     lora_linear_fwd_grouped  stacked column groups, one adapter per group
     lora_linear_bwd          closed-form dX, dA, dB
+    lora_linear_fwd_exact    the unfused bf16 chain (the "exact" tier), unit scales skipped or not
     lora_dense_patch         .diff / .diff_b (add) and .set_weight (replace), in place
 """
 from __future__ import annotations
@@ -26,7 +27,7 @@ LIB_PATH = os.path.join(_HERE, "libweight_patches_gb300.so")
 
 WP_BF16, WP_FP32, WP_NF4 = 0, 1, 2
 WP_PATCH_ADD, WP_PATCH_SET = 0, 1
-WP_OP_FWD, WP_OP_FWD_GROUPED, WP_OP_BWD, WP_OP_FWD_HOST, WP_OP_SWIGLU_FWD, WP_OP_MERGE = 0, 1, 2, 3, 4, 5
+WP_OP_FWD, WP_OP_FWD_GROUPED, WP_OP_BWD, WP_OP_FWD_HOST, WP_OP_SWIGLU_FWD, WP_OP_MERGE, WP_OP_FWD_EXACT = range(7)
 STATUS = {0: "WP_OK", -1: "WP_ERR_INVALID", -2: "WP_ERR_SHAPE", -3: "WP_ERR_DTYPE",
           -4: "WP_ERR_ALIGN", -5: "WP_ERR_WORKSPACE", -6: "WP_ERR_CUDA", -7: "WP_ERR_TIMEOUT",
           -8: "WP_ERR_UNSUPPORTED"}
@@ -74,6 +75,7 @@ def _load():
     lib.lora_linear_fwd_grouped.argtypes = [pm, pm, pm, I32, pa, D, po, P, SZ, P]
     lib.lora_linear_fwd_noalloc.argtypes = [pm, pm, pm, pa, I32, D, po, P]
     lib.lora_linear_fwd_host.argtypes = [pm, pm, pm, I32, pa, I32, D, po, P, SZ, P]
+    lib.lora_linear_fwd_exact.argtypes = [pm, pm, pm, I32, pa, I32, D, I32, po, P, SZ, P]
     lib.lora_linear_bwd.argtypes = [pm, pm, pm, I32, pa, D, po, po, po, P, SZ, P]
     lib.lora_swiglu_fwd.argtypes = [pm, pm, pm, pa, D, po, po, P, SZ, P]
     lib.lora_merge.argtypes = [pm, po, pa, I32, D, P, SZ, P]
@@ -84,11 +86,14 @@ def _load():
     lib.lora_status_string.argtypes = [ctypes.c_int]
     lib.lora_status_string.restype = ctypes.c_char_p
     lib.lora_device_status.argtypes = [I32]
+    lib.lora_set_wait_limit.argtypes = [ctypes.c_uint64]
+    lib.lora_debug_hold_flags.argtypes = [I32]
     lib.lora_nf4_codebook.argtypes = [ctypes.POINTER(ctypes.c_float)]
     lib.lora_nf4_codebook.restype = None
     lib.lora_last_cuda_error.restype = ctypes.c_char_p
     for name in ("lora_linear_fwd", "lora_linear_fwd_grouped", "lora_linear_bwd", "lora_dense_patch",
-                 "lora_device_status", "lora_linear_fwd_noalloc", "lora_linear_fwd_host"):
+                 "lora_device_status", "lora_linear_fwd_noalloc", "lora_linear_fwd_host",
+                 "lora_linear_fwd_exact", "lora_set_wait_limit", "lora_debug_hold_flags"):
         getattr(lib, name).restype = ctypes.c_int
     _LIB = lib
     return lib
@@ -313,6 +318,24 @@ def lora_linear_fwd_host(X_host: torch.Tensor, W, bias: Optional[torch.Tensor], 
     return out
 
 
+def lora_linear_fwd_exact(X: torch.Tensor, W, bias: Optional[torch.Tensor], adapters: Sequence[Adapter],
+                          request_scale: float = 1.0, skip_unit_scales: bool = True, grouped: bool = False,
+                          out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The unfused bf16 chain (base, X A^T, then B^T, one rounded multiplication per scale, the
+    add), the exact tier when ``skip_unit_scales``; ``grouped``: one adapter per column group."""
+    n = W.rows if isinstance(W, NF4Weight) else W.shape[0]
+    if out is None:
+        out = torch.empty(X.shape[0], n, dtype=torch.bfloat16, device=X.device)
+    xm, wm, bm, arr, ym = _mat(X), _mat(W), _mat(bias), _adapters(adapters), _out(out)
+    ws, nbytes = _workspace(WP_OP_FWD_EXACT, xm, wm, arr, len(adapters), X.device, workspace)
+    st = _load().lora_linear_fwd_exact(ctypes.byref(xm), ctypes.byref(wm), _ref(bm), len(adapters) if grouped else 0,
+                                       arr, len(adapters), float(request_scale), 1 if skip_unit_scales else 0,
+                                       ctypes.byref(ym), ws.data_ptr() if ws is not None else None, nbytes,
+                                       _stream(X.device))
+    _check(st, "lora_linear_fwd_exact")
+    return out
+
+
 def lora_linear_bwd(X: torch.Tensor, W, dY: torch.Tensor, adapters: Sequence[Adapter],
                     request_scale: float = 1.0, need_dX: bool = True,
                     dX_dtype: torch.dtype = torch.bfloat16, workspace: Optional[torch.Tensor] = None):
@@ -349,6 +372,11 @@ def lora_device_status(reset: bool = True) -> int:
     """The device status word (0, or -7 after a bounded wait expired).  Synchronises."""
     torch.cuda.synchronize()
     return _load().lora_device_status(1 if reset else 0)
+
+
+def lora_set_wait_limit(timeout_ns: int) -> None:
+    """How long a bounded device wait spins before its kernel gives up (default 2 s)."""
+    _check(_load().lora_set_wait_limit(int(timeout_ns)), "lora_set_wait_limit")
 
 
 def lora_nf4_codebook() -> list:

@@ -4,6 +4,7 @@
 // call.  The library never allocates device memory and never synchronises; all work
 // is enqueued on the caller's stream.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -20,6 +21,13 @@ namespace wp {
 
 namespace {
 thread_local std::string g_last_error;
+
+// How long a bounded device wait spins before its kernel gives up (lora_set_wait_limit), and
+// the test hook that holds the fused forward's row-block flags one release short
+// (lora_debug_hold_flags).
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_hold_flags{0};
+unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -361,7 +369,7 @@ int skinny_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, boo
     g.X = static_cast<const uint16_t*>(X->data); g.ldx = X->ld;
     g.part = part; g.ldp = q.ldp;
     g.status = tc_status_ptr();
-    g.timeout_ns = 2000000000ull;
+    g.timeout_ns = wait_limit_ns();
     if (!g.status) return record_cuda();
     GemvMaps gm;
     std::memset(&gm, 0, sizeof(gm));
@@ -388,7 +396,7 @@ int skinny_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, boo
   p.splits = sp.splits; p.kb_per_split = sp.kbps; p.units = sp.units; p.kkb = sp.kkb;
   p.part = part; p.ldp = q.ldp;
   p.status = tc_status_ptr();
-  p.timeout_ns = 2000000000ull;
+  p.timeout_ns = wait_limit_ns();
   if (!p.status) return record_cuda();
   // barriers (3 per stage, 1 per code slot, 5 more), the TMEM address, the abort flag and
   // the per-slot copy counts
@@ -605,7 +613,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   p.bias = bias ? bias->data : nullptr; p.bias_f32 = bias && bias->dtype == WP_FP32;
   p.bias_vec = bias && aligned16(bias->data) ? 1 : 0;
   if (!rank_only) { p.Y = Y->data; p.ldy = Y->ld; p.y_f32 = Y->dtype == WP_FP32; }
-  p.timeout_ns = 2000000000ull;
+  p.timeout_ns = wait_limit_ns();
 
   // Plan the adapters (host only; every rejection happens before any CUDA call).
   H32Params hp{};
@@ -740,7 +748,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
     }
     p.htot = 2 * half;
     p.npass = npass;
-    p.flag_target = 2u * static_cast<uint32_t>(npass);
+    p.flag_target = 2u * static_cast<uint32_t>(npass) + (g_hold_flags.load() ? 1u : 0u);
     pk.n_ad = p.n_ad;
     pk.half = half;
     pk.npass = npass;
@@ -1082,7 +1090,7 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
   tp.T = Ti; tp.k_blocks = (Ti + 63) / 64;
   tp.part = tpart;
   tp.status = tc_status_ptr();
-  tp.timeout_ns = 2000000000ull;
+  tp.timeout_ns = wait_limit_ns();
   if (!tp.status) return record_cuda();
   const size_t sb = 2 * 64 * 128 + static_cast<size_t>(L.tokN) / 2 * 128;
   tp.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemLimit - 1024 - 256) / sb));
@@ -1141,6 +1149,126 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
       }
     }
     g0 = g1;
+  }
+  return WP_OK;
+}
+
+// ------------------------------------------------------------------ the unfused chain (exact tier)
+// sglang PR "[diffusion] Add the dynamic LoRA delta inside the second GEMM", Motivation and
+// Modifications (exact tier): base = bf16(X W^T + bias); per adapter t = bf16(X A^T),
+// d = bf16(t B^T) (+ its legacy vector inside that GEMM), d = bf16(d c) for each scale c of
+// (alpha/r, strength, request scale) -- a c of exactly 1.0 skipped when asked, which changes
+// no bit -- and Y = bf16(Y + d), adapter after adapter; an FP32 adapter keeps its GEMMs and
+// scaling in FP32 and is added once.  The GEMMs run on the fused kernel without adapters.
+// Workspace, in order (each region 256-byte aligned): t [T, r_max] bf16 | d [T, N] fp32-sized
+// | the scratch of the FP32 adapters' delta-only forwards.
+struct ExactLayout {
+  size_t t, d, fwd, fwd_bytes, total;
+};
+
+bool exact_layout(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int n, ExactLayout* L) {
+  *L = ExactLayout{};
+  if (!X || !W || n < 0 || (n > 0 && !ad) || X->rows < 0 || W->rows < 0) return false;
+  const size_t T = static_cast<size_t>(X->rows), N = static_cast<size_t>(W->rows);
+  size_t rmax = 0, fwd = 0;
+  for (int i = 0; i < n; ++i) {
+    rmax = std::max(rmax, static_cast<size_t>(std::max<int64_t>(ad[i].A.rows, 0)));
+    if (ad[i].A.dtype == WP_FP32) {
+      FwdPlan plan;
+      plan_fwd(X, nullptr, &ad[i], 1, &plan);
+      fwd = std::max(fwd, fwd_workspace(X, plan));
+    }
+  }
+  size_t off = 0;
+  L->t = off;
+  off += round256(T * rmax * 2);
+  L->d = off;
+  off += n > 0 ? round256(T * N * 4) : 0;
+  L->fwd = off;
+  L->fwd_bytes = fwd;
+  off += fwd;
+  L->total = off;
+  return true;
+}
+
+int exact_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int n_groups, const wp_adapter* ad, int n,
+               double request_scale, bool skip_unit, const wp_out* Y, void* workspace, size_t ws_bytes,
+               cudaStream_t stream) {
+  if (!valid_input(X, false) || !W || !valid_input(W, true) || !valid_output(Y)) return WP_ERR_INVALID;
+  if (X->dtype != WP_BF16 || Y->dtype != WP_BF16) return WP_ERR_DTYPE;   // the chain's tensors are bf16
+  if (W->dtype != WP_BF16 && W->dtype != WP_NF4) return WP_ERR_DTYPE;
+  if (n_groups < 0 || n < 0 || n > kMaxAd + kMaxAd32 || (n > 0 && !ad)) return WP_ERR_INVALID;
+  if (n_groups > 0 && n != n_groups) return WP_ERR_INVALID;
+  if (!std::isfinite(request_scale)) return WP_ERR_INVALID;
+  const long long T = X->rows, K = X->cols, N = W->rows;
+  const int G = n_groups > 0 ? n_groups : 1;
+  if (W->cols != K || Y->rows != T || Y->cols != N || N % G) return WP_ERR_SHAPE;
+  const long long cols = N / G;
+  if (cols % 8 || Y->ld % 8 || !aligned16(Y->data)) return WP_ERR_ALIGN;
+  for (int i = 0; i < n; ++i) {
+    const wp_adapter& a = ad[i];
+    if (!valid_input(&a.A, false) || !valid_input(&a.B, false)) return WP_ERR_INVALID;
+    if (a.A.dtype != a.B.dtype) return WP_ERR_DTYPE;
+    const long long r = a.A.rows;
+    if (r <= 0) return WP_ERR_INVALID;
+    if (a.A.cols != K || a.B.cols != r || a.B.rows != cols) return WP_ERR_SHAPE;
+    if (!std::isfinite(a.alpha) || !std::isfinite(a.strength)) return WP_ERR_INVALID;
+    const double sc = a.alpha / static_cast<double>(r) * a.strength * request_scale;
+    if (!std::isfinite(sc) || !std::isfinite(static_cast<float>(sc))) return WP_ERR_INVALID;
+    if (a.A.dtype == WP_BF16 && r % 8) return WP_ERR_ALIGN;    // t [T, r] is a GEMM output
+    if (a.bias_B && a.bias_B_dtype != WP_BF16 && a.bias_B_dtype != WP_FP32) return WP_ERR_DTYPE;
+  }
+  ExactLayout L;
+  if (!exact_layout(X, W, ad, n, &L)) return WP_ERR_INVALID;
+  if (L.total > 0 && (!workspace || ws_bytes < L.total)) return WP_ERR_WORKSPACE;
+  if (L.total > 0 && !aligned16(workspace)) return WP_ERR_ALIGN;
+  if (T == 0) return WP_OK;
+  char* ws = static_cast<char*>(workspace);
+  // base = bf16(X W^T + bias), straight into Y
+  int rc = fwd_impl(X, W, bias, 1, false, nullptr, 0, 1.0, Y, nullptr, 0, stream);
+  if (rc != WP_OK) return rc;
+  void* t = ws + L.t;
+  void* d = ws + L.d;
+  for (int i = 0; i < n; ++i) {
+    const wp_adapter& a = ad[i];
+    const int r = static_cast<int>(a.A.rows);
+    const int g = n_groups > 0 ? i : 0;
+    ChainParams add{};
+    add.mode = kChainAdd;
+    add.T = T; add.N = cols;
+    add.Y = static_cast<uint16_t*>(Y->data) + g * cols; add.ldy = Y->ld;
+    add.d = d; add.ldd = cols;
+    if (a.A.dtype == WP_FP32) {
+      // FP32 GEMMs and scaling, added once
+      const wp_out dout{d, WP_FP32, T, cols, cols};
+      rc = fwd_impl(X, nullptr, nullptr, 1, false, &a, 1, request_scale, &dout, ws + L.fwd, L.fwd_bytes, stream);
+      if (rc != WP_OK) return rc;
+      add.d_f32 = 1;
+    } else {
+      const wp_out tout{t, WP_BF16, T, r, r};
+      rc = fwd_impl(X, &a.A, nullptr, 1, false, nullptr, 0, 1.0, &tout, nullptr, 0, stream);
+      if (rc != WP_OK) return rc;
+      const wp_mat tin{t, WP_BF16, T, r, r, nullptr};
+      const wp_mat vb{a.bias_B, a.bias_B_dtype, 1, cols, cols, nullptr};
+      const wp_out dout{d, WP_BF16, T, cols, cols};
+      rc = fwd_impl(&tin, &a.B, a.bias_B ? &vb : nullptr, 1, false, nullptr, 0, 1.0, &dout, nullptr, 0, stream);
+      if (rc != WP_OK) return rc;
+      const float scales[3] = {static_cast<float>(a.alpha / r), static_cast<float>(a.strength),
+                               static_cast<float>(request_scale)};
+      for (float c : scales) {
+        if (skip_unit && c == 1.0f) continue;
+        ChainParams sc{};
+        sc.mode = kChainScale;
+        sc.T = T; sc.N = cols;
+        sc.Y = static_cast<uint16_t*>(d); sc.ldy = cols;
+        sc.c = c;
+        rc = launch_chain(sc, stream);
+        if (rc != WP_OK) return rc;
+      }
+      add.d_f32 = 0;
+    }
+    rc = launch_chain(add, stream);
+    if (rc != WP_OK) return rc;
   }
   return WP_OK;
 }
@@ -1375,7 +1503,7 @@ int merge_pass(const void* P, long long ldp, const void* Q, long long ldq, long 
     mp.R = R; mp.ldr = ldr; mp.r_f32 = r_f32 ? 1 : 0;
     mp.Y = Y; mp.ldy = ldy; mp.y_f32 = y_f32 ? 1 : 0;
     mp.status = tc_status_ptr();
-    mp.timeout_ns = 2000000000ull;
+    mp.timeout_ns = wait_limit_ns();
     if (!mp.status) return record_cuda();
     return launch_merge_tile(mm, mp, stream);
   }
@@ -1393,7 +1521,7 @@ int merge_pass(const void* P, long long ldp, const void* Q, long long ldq, long 
   p.has_base = 1;
   p.Y = Y; p.ldy = ldy; p.y_f32 = y_f32 ? 1 : 0;
   p.acc_scale = s; p.resid = R; p.ld_resid = ldr; p.resid_f32 = r_f32 ? 1 : 0;
-  p.timeout_ns = 2000000000ull;
+  p.timeout_ns = wait_limit_ns();
   p.stage_bytes = kATileBytes + kBHalfBytes;
   const size_t fixed = 1024 + 2 * kStgBytes + 512;
   p.stages = std::min<int>(kMaxStages, static_cast<int>((kSmemLimit - fixed) / p.stage_bytes));
@@ -1527,7 +1655,7 @@ int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n,
     fp.absmax = const_cast<float*>(W->absmax);
     fp.tab = tab;
     fp.status = tc_status_ptr();
-    fp.timeout_ns = 2000000000ull;
+    fp.timeout_ns = wait_limit_ns();
     if (!fp.status) return record_cuda();
     rc = launch_merge_nf4(fm, fp, stream);
   } else if (nf4) {
@@ -1642,11 +1770,23 @@ size_t lora_workspace_size(int32_t op, const wp_mat* X, const wp_mat* W,
     BwdLayout L;
     return bwd_layout(X, W, adapters, n_adapters, &L) ? L.total : 0;
   }
+  if (op == WP_OP_FWD_EXACT) {
+    ExactLayout L;
+    return exact_layout(X, W, adapters, n_adapters, &L) ? L.total : 0;
+  }
   if (op == WP_OP_FWD_HOST) {
     HostLayout L;
     return host_layout(X, W, adapters, n_adapters, &L) ? L.total : 0;
   }
   return 0;
+}
+
+int lora_linear_fwd_exact(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int32_t n_groups,
+                          const wp_adapter* adapters, int32_t n_adapters, double request_scale,
+                          int32_t skip_unit_scales, const wp_out* Y, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  return exact_impl(X, W, bias, n_groups, adapters, n_adapters, request_scale, skip_unit_scales != 0, Y, workspace,
+                    workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 int lora_linear_fwd_host(const wp_mat* X_host, const wp_mat* W, const wp_mat* bias,
@@ -1678,6 +1818,17 @@ int lora_device_status(int32_t reset) {
 }
 
 void lora_nf4_codebook(float out[16]) { nf4_codebook_host(out); }
+
+int lora_set_wait_limit(uint64_t timeout_ns) {
+  if (timeout_ns < 1000000ull || timeout_ns > 60000000000ull) return WP_ERR_INVALID;
+  g_wait_limit_ns.store(timeout_ns);
+  return WP_OK;
+}
+
+int lora_debug_hold_flags(int32_t on) {
+  g_hold_flags.store(on ? 1 : 0);
+  return WP_OK;
+}
 
 const char* lora_last_cuda_error(void) { return g_last_error.c_str(); }
 

@@ -424,6 +424,20 @@ int launch_transpose_bf16(const void* src, long long ld_s, int R, int C, void* d
 int launch_nf4_dequant_t(const void* codes, const float* absmax, int N, int K, const NF4Table& tab,
                          void* dst, long long ld_d, cudaStream_t stream);
 
+// ------------------------------------------------------------------ unfused chain (exact tier)
+// One elementwise step of the chain on a [T, N] bf16 matrix Y (N % 8 == 0, 16-byte aligned
+// rows): kChainScale: Y = bf16(Y * c); kChainAdd: Y = bf16(Y + d), d [T, N] bf16 or fp32.
+// Each result is the correctly rounded value of the exact product or sum (wp_chain.cu).
+enum { kChainScale = 0, kChainAdd = 1 };
+struct ChainParams {
+  int mode;
+  long long T, N;
+  uint16_t* Y; long long ldy;
+  const void* d; long long ldd; int d_f32;
+  float c;
+};
+int launch_chain(const ChainParams& q, cudaStream_t stream);
+
 // ------------------------------------------------------------------ dense patch
 int launch_dense_patch(void* param, int param_dtype, const void* payload, int payload_dtype,
                        long long n, int kind, float k, cudaStream_t stream);
