@@ -292,7 +292,11 @@ def run_fused(args):
 
 
 # ----------------------------------------------------------------------- other workloads
-def per_config(dev, args, peak, hbm):
+CASES = ("c0_tiny_fp32", "f32_layer", "wan_qkv_rank128", "c2_ffn_up", "c2_ffn_down", "c3_nf4_gate_up_fwd",
+         "c3_nf4_down_fwd", "c3_nf4_gate_up_bwd", "c3_nf4_down_bwd", "c3_swiglu_bwd", "c4_sidecar", "c4_set_weight")
+
+
+def per_config(dev, args, peak, hbm, only=None):
     """Every workload of the library besides the headline one, timed like it: CUDA events on
     the launching stream around back-to-back calls after warm-up (inputs larger than L2), and
     for the dense patch one call at a time after an L2 flush.  Each entry: its work (GFLOP or
@@ -303,6 +307,7 @@ def per_config(dev, args, peak, hbm):
     import workloads
 
     stream = torch.cuda.current_stream(dev)
+    want = lambda name: only is None or name in only
     clocks = ClockSampler(0)
     clocks.start()
     time.sleep(0.3)
@@ -391,64 +396,115 @@ def per_config(dev, args, peak, hbm):
                      "clocks": None, "setup_s": round(t_s - t0, 1)}
         marks[name] = (t_s, t_e)
 
-    # C0: the all-FP32 layer (CUDA-core FFMA; launch-bound at this size)
-    lin0 = workloads.config0()
-    X0, W0, b0 = d(lin0.X), d(lin0.W), d(lin0.bias).reshape(-1)
-    ads0 = ads_of(lin0)
-    Y0 = torch.empty(lin0.T, lin0.W.rows, dtype=torch.float32, device=dev)
-    t_s = time.time()
-    ms0 = timed(lambda: wpg.lora_linear_fwd(X0, W0, b0, ads0, lin0.request_scale, out=Y0), 200, 20)
-    marks["c0_tiny_fp32"] = (t_s, time.time())
-    fl0 = 2.0 * lin0.T * (128 * 256 + 8 * (128 + 256))
     ffma_peak = device_sm_count(dev) * 128 * 2 * 2.07e9 / 1e12
-    out["c0_tiny_fp32"] = {"gflop": round(fl0 / 1e9, 5), "us": round(ms0 * 1e3, 2),
-                           "tflops": round(fl0 / (ms0 * 1e-3) / 1e12, 3), "bound": "alu (fp32 FFMA), launch-bound",
-                           "frac": round(fl0 / (ms0 * 1e-3) / 1e12 / ffma_peak, 5),
-                           "peak": f"{ffma_peak:.1f} TFLOP/s fp32 FFMA (SMs x 128 lanes x 2 x 2.07 GHz)"}
 
-    fwd_entry("wan_qkv_rank128", workloads.wan_qkv_rank128("full"),
-              "the sglang PR's own Speed Tests shape: rank 128 on each of q/k/v (two rank passes)")
-    up, down, _ = workloads.config2("full")
-    fwd_entry("c2_ffn_up", up)
-    del up
-    fwd_entry("c2_ffn_down", down)
-    del down
-    torch.cuda.empty_cache()
-    gate_up, down3 = workloads.config3("full")
-    fwd_entry("c3_nf4_gate_up_fwd", gate_up)
-    fwd_entry("c3_nf4_down_fwd", down3)
-    bwd_entry("c3_nf4_gate_up_bwd", gate_up)
-    bwd_entry("c3_nf4_down_bwd", down3)
-    del gate_up, down3
-    torch.cuda.empty_cache()
-    lin4, payload = workloads.config4("full")
-    fwd_entry("c4_sidecar", lin4, "three patches (ranks 16 fp32 / 32 / 128 bf16)")
-    # C4 .set_weight: one call at a time after an L2 flush, CUDA events around the call
-    P = d(payload)
-    param = torch.empty_like(P)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    times = []
-    t_s = time.time()
-    for i in range(k + 3):
-        flush.fill_(i & 0xFF)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        wpg.lora_dense_patch(param, P, wpg.WP_PATCH_SET, 1.0)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        if i >= 3:
-            times.append(e0.elapsed_time(e1))
-    marks["c4_set_weight"] = (t_s, time.time())
-    ms = statistics.median(times)
-    nbytes = 2 * P.numel() * P.element_size()
-    out["c4_set_weight"] = {"mb": round(nbytes / 1e6, 1), "ms": round(ms, 5),
-                            "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bound": "hbm",
-                            "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
-                            "timing": "one call after an L2 flush, launch included, median"}
+    def f32_entry(name, lin, note):
+        X0, W0, b0 = d(lin.X), d(lin.W), d(lin.bias).reshape(-1)
+        ads0 = ads_of(lin)
+        Y0 = torch.empty(lin.T, lin.W.rows, dtype=torch.float32, device=dev)
+        ws0 = torch.empty(max(1, wpg.lora_workspace_size(wpg.WP_OP_FWD, X0, W0, ads0)), dtype=torch.uint8,
+                          device=dev)
+        t_s = time.time()
+        ms0 = timed(lambda: wpg.lora_linear_fwd(X0, W0, b0, ads0, lin.request_scale, out=Y0, workspace=ws0),
+                    max(k, 20), 10)
+        marks[name] = (t_s, time.time())
+        fl0 = fwd_flops(lin)
+        tf = fl0 / (ms0 * 1e-3) / 1e12
+        out[name] = {"gflop": round(fl0 / 1e9, 5), "us": round(ms0 * 1e3, 2), "tflops": round(tf, 3),
+                     "bound": "alu (fp32 FFMA)", "frac": round(tf / ffma_peak, 4), "note": note,
+                     "peak": f"{ffma_peak:.1f} TFLOP/s fp32 FFMA (SMs x 128 lanes x 2 x 2.07 GHz)"}
+
+    if want("c0_tiny_fp32"):
+        f32_entry("c0_tiny_fp32", workloads.config0(), "the all-FP32 layer of the tiny workload: launch-bound")
+    if want("f32_layer"):
+        rng = np.random.default_rng(21)
+        T, K, N, r = 4096, 1024, 1024, 16
+        lf = workloads.Linear("f32_layer", workloads.draw(rng, T, K, 1.0, workloads.FP32),
+                              workloads.draw(rng, N, K, (1.0 / K) ** 0.5, workloads.FP32),
+                              workloads.draw(rng, 1, N, 0.01, workloads.FP32),
+                              [workloads.Patch(workloads.draw(rng, r, K, (1.0 / K) ** 0.5, workloads.FP32),
+                                               workloads.draw(rng, N, r, 0.02, workloads.FP32), float(r), 0.8)])
+        f32_entry("f32_layer", lf, "an all-FP32 layer large enough to fill the GPU: T=4096, 1024 -> 1024, rank 16 "
+                                   "(rank_proj_kernel + f32_linear_kernel)")
+    if want("wan_qkv_rank128"):
+        fwd_entry("wan_qkv_rank128", workloads.wan_qkv_rank128("full"),
+                  "the sglang PR's own Speed Tests shape: rank 128 on each of q/k/v (two rank passes)")
+    if want("c2_ffn_up") or want("c2_ffn_down"):
+        up, down, _ = workloads.config2("full")
+        if want("c2_ffn_up"):
+            fwd_entry("c2_ffn_up", up)
+        del up
+        if want("c2_ffn_down"):
+            fwd_entry("c2_ffn_down", down)
+        del down
+        torch.cuda.empty_cache()
+    c3 = ("c3_nf4_gate_up_fwd", "c3_nf4_down_fwd", "c3_nf4_gate_up_bwd", "c3_nf4_down_bwd")
+    if any(want(n) for n in c3):
+        gate_up, down3 = workloads.config3("full")
+        for n, lin, fn in zip(c3, (gate_up, down3, gate_up, down3), (fwd_entry, fwd_entry, bwd_entry, bwd_entry)):
+            if want(n):
+                fn(n, lin)
+        del gate_up, down3
+        torch.cuda.empty_cache()
+    if want("c3_swiglu_bwd"):
+        # the SwiGLU backward step on the C3 shape: dH [T, F], e | g [T, 2F] -> de | dg and h
+        rng = np.random.default_rng(22)
+        T, F = workloads.FULL[3]["T"], workloads.FULL[3]["d_ff"]
+        dH = workloads.draw(rng, T, F, 1.0).torch_cpu().to(dev)
+        EG = workloads.draw(rng, T, 2 * F, 1.0).torch_cpu().to(dev)
+        dEG = torch.empty_like(EG)
+        Hh = torch.empty_like(dH)
+        t_s = time.time()
+        ms = timed(lambda: wpg.lora_swiglu_bwd(dH, EG, deg=dEG, h=Hh, want_h=True))
+        marks["c3_swiglu_bwd"] = (t_s, time.time())
+        nbytes = T * F * (2 + 4 + 4 + 2)
+        out["c3_swiglu_bwd"] = {"mb": round(nbytes / 1e6, 1), "ms": round(ms, 5),
+                                "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bound": "hbm",
+                                "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
+                                "work": "read dH, e, g; write de, dg, h (12 B per element of F)"}
+    if want("c4_sidecar") or want("c4_set_weight"):
+        lin4, payload = workloads.config4("full")
+        if want("c4_sidecar"):
+            fwd_entry("c4_sidecar", lin4, "three patches (ranks 16 fp32 / 32 / 128 bf16)")
+        if want("c4_set_weight"):
+            # one call at a time after an L2 flush, CUDA events around the call
+            P = d(payload)
+            param = torch.empty_like(P)
+            flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+            times = []
+            t_s = time.time()
+            for i in range(k + 3):
+                flush.fill_(i & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                wpg.lora_dense_patch(param, P, wpg.WP_PATCH_SET, 1.0)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                if i >= 3:
+                    times.append(e0.elapsed_time(e1))
+            marks["c4_set_weight"] = (t_s, time.time())
+            ms = statistics.median(times)
+            nbytes = 2 * P.numel() * P.element_size()
+            out["c4_set_weight"] = {"mb": round(nbytes / 1e6, 1), "ms": round(ms, 5),
+                                    "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bound": "hbm",
+                                    "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
+                                    "timing": "one call after an L2 flush, launch included, median"}
     clocks.stop()
     for name, (a, b) in marks.items():
         out[name]["clocks"] = clocks.summary(a, b)
     return out
+
+
+def run_case(args):
+    """One workload of per_config on its own (for profiling a single kernel's launches)."""
+    import torch
+    if args.case not in CASES:
+        sys.exit(f"bench.py: unknown case {args.case!r}; cases: {', '.join(CASES)}")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, hbm, _ = measured_peaks()
+    res = per_config(dev, args, peak, hbm, only={args.case})
+    print(json.dumps({"case": args.case, **res[args.case]}))
 
 
 def device_sm_count(dev):
@@ -522,6 +578,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--case", default=None, help="time one workload of per_config alone: " + ", ".join(CASES))
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -539,6 +596,8 @@ def main():
         sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={ws}")
     if args.impl == "reference":
         run_reference(args)
+    elif args.case:
+        run_case(args)
     else:
         run_fused(args)
 
