@@ -92,9 +92,12 @@ def test_bwd_nf4_small():
         _check_full(lin, dX, dA, dB)
 
 
-def test_bwd_nf4_full_sampled():
-    gate_up, _ = workloads.config3("full")
-    lin = gate_up
+@pytest.mark.parametrize("which", ["gate_up", "down"])
+def test_bwd_nf4_full_sampled(which):
+    """The 4-bit C3 layers at full size: the dX pass dequantises the stored weight straight into
+    MN-major tiles (no transposed copy); dX on sampled rows, dA and dB everywhere."""
+    gate_up, down = workloads.config3("full")
+    lin = gate_up if which == "gate_up" else down
     dX, dA, dB = _run(lin)
     X, W, _, patches = olora.decode_linear(lin)
     rows = workloads.sample_rows(lin.T, 48)
@@ -162,3 +165,21 @@ def test_bwd_rank_above_limit_is_refused():
         wpg.lora_linear_bwd(X, W, torch.zeros(64, 64, dtype=torch.bfloat16, device=gu.DEV),
                             [wpg.Adapter(A, B, 136.0)], 1.0)
     assert e.value.status == -8
+
+
+@pytest.mark.parametrize("kind,T,K,N,G", [("bf16", 300, 200, 264, 1), ("bf16", 260, 520, 3 * 136, 3),
+                                          ("nf4", 300, 320, 384, 1), ("nf4", 520, 512, 2 * 192, 2),
+                                          ("nf4", 129, 192, 128, 1)])
+def test_bwd_weight_read_as_stored(kind, T, K, N, G):
+    """dX = dY W with W [out, in] read as stored (MN-major tiles): ragged in (the dX columns)
+    and out (the reduction), bf16 and 4-bit W, block scales by TMA (in % 256 == 0) and from
+    global memory."""
+    rng = np.random.default_rng(T + K + N)
+    X = workloads.draw(rng, T, K, 1.0)
+    W = workloads.draw_nf4(rng, N, K) if kind == "nf4" else workloads.draw(rng, N, K, (1.0 / K) ** 0.5)
+    og = N // G
+    patches = [workloads.Patch(workloads.draw(rng, 16, K, (1.0 / K) ** 0.5), workloads.draw(rng, og, 16, 0.02),
+                               16.0, 0.9) for _ in range(G)]
+    lin = _with_dY(workloads.Linear("bwd_stored_w", X, W, None, patches, request_scale=1.2, groups=G), T + 1)
+    dX, dA, dB = _run(lin)
+    _check_full(lin, dX, dA, dB)

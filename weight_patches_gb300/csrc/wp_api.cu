@@ -460,7 +460,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
              const wp_adapter* adapters, int n_adapters, double request_scale, const wp_out* Y,
              void* workspace, size_t ws_bytes, cudaStream_t stream, float* h_out = nullptr,
              int h_out_ld = 0, bool rank_only = false, bool swiglu = false,
-             const wp_out* eg = nullptr) {
+             const wp_out* eg = nullptr, bool w_mn = false) {
   if (!valid_input(X, false)) return WP_ERR_INVALID;
   if (W && !valid_input(W, true)) return WP_ERR_INVALID;
   if (rank_only ? (W || bias || !h_out || n_adapters < 1 || X->dtype != WP_BF16) : !valid_output(Y))
@@ -474,14 +474,17 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   if (swiglu && (!W || !grouped || G != 2 || rank_only || Y->dtype != WP_BF16)) return WP_ERR_INVALID;
   if (eg && (!swiglu || !valid_output(eg) || eg->dtype != WP_BF16)) return WP_ERR_INVALID;
 
+  // w_mn (the backward's dX pass): W is stored [in, out], i.e. the forward's W as it is
+  if (w_mn && (!W || swiglu || rank_only || G != 1)) return WP_ERR_INVALID;
   const long long T = X->rows, K = X->cols;
-  const long long N = W ? W->rows : rank_only ? G * adapters[0].B.rows : Y->cols;
-  if (W && W->cols != K) return WP_ERR_SHAPE;
+  const long long N = W ? (w_mn ? W->cols : W->rows) : rank_only ? G * adapters[0].B.rows : Y->cols;
+  if (W && (w_mn ? W->rows : W->cols) != K) return WP_ERR_SHAPE;
   if (!rank_only && (Y->rows != T || Y->cols != (swiglu ? N / 2 : N))) return WP_ERR_SHAPE;
   if (eg && (eg->rows != T || eg->cols != N)) return WP_ERR_SHAPE;
   if (N % G) return WP_ERR_SHAPE;
   const long long out_g = N / G;
-  if (W && W->dtype == WP_NF4 && (K % 64 != 0 || W->ld != K)) return WP_ERR_SHAPE;
+  if (W && W->dtype == WP_NF4 && !w_mn && (K % 64 != 0 || W->ld != K)) return WP_ERR_SHAPE;
+  if (W && W->dtype == WP_NF4 && w_mn && (N % 64 != 0 || W->ld != N)) return WP_ERR_SHAPE;
   if (bias) {
     if (!bias->data || (bias->dtype != WP_BF16 && bias->dtype != WP_FP32)) return WP_ERR_INVALID;
     if (bias->rows * bias->cols != N) return WP_ERR_SHAPE;
@@ -547,7 +550,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   // a few tokens: the weight-streaming small-token path, when the workspace holds its
   // partial sums (else the general path below serves the call); it does not store s X A^T,
   // so calls that want it back (h_out) stay on the general path
-  if (!rank_only && !swiglu && !h_out && plan.skinny_bytes > 0 && workspace &&
+  if (!rank_only && !swiglu && !h_out && !w_mn && plan.skinny_bytes > 0 && workspace &&
       ws_bytes >= plan.skinny_bytes && aligned16(workspace)) {
     const int rc = skinny_impl(X, W, bias, G, grouped, adapters, n_adapters, s_of, Y, workspace, stream);
     if (rc != WP_ERR_UNSUPPORTED) return rc;
@@ -610,6 +613,7 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   p.total_tiles = rank_only ? 0 : static_cast<int>(total);
   p.k_blocks = static_cast<int>((K + kBK - 1) / kBK);
   p.has_base = W ? 1 : 0;
+  p.w_mn = w_mn ? 1 : 0;
   p.bias = bias ? bias->data : nullptr; p.bias_f32 = bias && bias->dtype == WP_FP32;
   p.bias_vec = bias && aligned16(bias->data) ? 1 : 0;
   if (!rank_only) { p.Y = Y->data; p.ldy = Y->ld; p.y_f32 = Y->dtype == WP_FP32; }
@@ -792,7 +796,20 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   // adapters' A rows, 128 rows of H~ and 128 rows of a B tile.
   int rc = make_map_bf16(&maps.x, X->data, K, T, X->ld, kBK, kBM);
   if (rc != WP_OK) return rc;
-  if (nf4) {
+  if (nf4 && w_mn) {
+    // codes stored [K rows, N/2 bytes]; each CTA loads 64 K rows x 64 bytes (its 128 output
+    // columns) per K step, in the 64-byte swizzle; block scales [K, N/64] in boxes of 64 rows
+    // x 4 blocks when a row of them is a multiple of 16 bytes
+    rc = make_map_u8(&maps.wq, W->data, N / 2, K, N / 2, 64, kBK, 64);
+    if (rc != WP_OK) return rc;
+    p.absmax = W->absmax;
+    p.am_tma = (N % 256 == 0 && aligned16(W->absmax)) ? 1 : 0;
+    if (p.am_tma) {
+      rc = make_map(&maps.am, WP_FP32, W->absmax, N / 64, K, N / 64, 4, kBK, /*swizzle=*/0);
+      if (rc != WP_OK) return rc;
+    }
+    nf4_codebook_host(p.nf4_code);
+  } else if (nf4) {
     // codes: [N rows, K/2 bytes]; each CTA loads 128 rows x 32 bytes (64 elements) per K step
     rc = make_map_u8(&maps.wq, W->data, K / 2, N, K / 2, kBK / 2, 128, 32);
     if (rc != WP_OK) return rc;
@@ -804,6 +821,10 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
       if (rc != WP_OK) return rc;
     }
     nf4_codebook_host(p.nf4_code);
+  } else if (W && w_mn) {
+    // W stored [K rows, N columns]: boxes of 64 output columns x 64 K rows (MN-major tiles)
+    rc = make_map_bf16(&maps.w, W->data, N, K, W->ld, 64, kBK);
+    if (rc != WP_OK) return rc;
   } else if (W) {
     rc = make_map_bf16(&maps.w, W->data, K, N, W->ld, kBK, 128);
     if (rc != WP_OK) return rc;
@@ -853,11 +874,11 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
 
 // ------------------------------------------------------------------ backward
 // Workspace of lora_linear_bwd, in order (each region 256-byte aligned):
-//   W^T [in, Ntot] bf16 | per group: B_g^T padded to [r_g, Ntot] bf16 | per group: A_g^T
+//   per group: B_g^T padded to [r_g, Ntot] bf16 | per group: A_g^T
 //   [in, r8_g] bf16 | s G [T, R] fp32 | H [T, R] fp32 | the bf16 pieces of H and of s G
 //   [T, tokN] | token-split partial sums | the forward calls' scratch
 struct BwdLayout {
-  size_t wt, bhat[kMaxGroups], at[kMaxGroups], gs, h, fwd, fwd_bytes, total;
+  size_t bhat[kMaxGroups], at[kMaxGroups], gs, h, fwd, fwd_bytes, total;
   int r8[kMaxGroups];
   int roff[kMaxGroups];
   int R;
@@ -890,8 +911,6 @@ bool bwd_layout(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int G, B
   if (Ntot % G) return false;
   const size_t og = Ntot / G;
   size_t off = 0;
-  L->wt = off;
-  off += round256(K * Ntot * 2);
   int R = 0;
   for (int g = 0; g < G; ++g) {
     const int r = static_cast<int>(ad[g].A.rows);
@@ -933,13 +952,14 @@ bool bwd_layout(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int G, B
   L->tpart = off;
   off += round256(std::max(static_cast<size_t>(L->splits_a) * K, static_cast<size_t>(L->splits_b) * Mb) *
                   L->tokN * 4);
-  // workspace of the forward call that computes dX: X := dY [T, Ntot], W := W^T, adapter g
-  // A := B_g^T padded to [r_g, Ntot] (bf16), B := A_g^T [K, r_g]
+  // workspace of the forward call that computes dX: X := dY [T, Ntot], the weight W [Ntot, K]
+  // as stored (read MN-major: in = Ntot, out = K), adapter g A := B_g^T padded to [r_g, Ntot]
+  // (bf16), B := A_g^T [K, r_g]
   {
     const wp_mat dy{nullptr, WP_BF16, static_cast<int64_t>(T), static_cast<int64_t>(Ntot),
                     static_cast<int64_t>(Ntot), nullptr};
     const wp_mat wt{nullptr, WP_BF16, static_cast<int64_t>(K), static_cast<int64_t>(Ntot),
-                    static_cast<int64_t>(Ntot), nullptr};
+                    static_cast<int64_t>(Ntot), nullptr};   // the sizes the plan reads: out = K
     wp_adapter fa[kMaxGroups] = {};
     for (int g = 0; g < G; ++g) {
       const int64_t r = ad[g].A.rows;
@@ -1007,24 +1027,11 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
   if (T == 0) return WP_OK;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  uint16_t* Wt = reinterpret_cast<uint16_t*>(ws + L.wt);
   float* Gs = reinterpret_cast<float*>(ws + L.gs);
   float* H = reinterpret_cast<float*>(ws + L.h);
   int rc;
 
-  // 1. W^T [K, Ntot] bf16: the K-major B operand of dX = dY W
-  if (W->dtype == WP_NF4) {
-    NF4Table tab;
-    nf4_codebook_host(tab.level);
-    rc = launch_nf4_dequant_t(W->data, W->absmax, static_cast<int>(Ntot), static_cast<int>(K), tab,
-                              Wt, Ntot, stream);
-  } else {
-    rc = launch_transpose_bf16(W->data, W->ld, static_cast<int>(Ntot), static_cast<int>(K), Wt, Ntot,
-                               stream);
-  }
-  if (rc != WP_OK) return rc;
-
-  // 2. per group: B_g^T placed at the group's columns of a zero [r_g, Ntot] matrix (so
+  // 1. per group: B_g^T placed at the group's columns of a zero [r_g, Ntot] matrix (so
   //    dY B_hat_g^T = dY_g B_g), and A_g^T [K, r8_g]
   wp_adapter fwd_ad[kMaxGroups] = {};             // (no legacy bias vectors: dX does not have them)
   for (int g = 0; g < G; ++g) {
@@ -1044,7 +1051,7 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
     fwd_ad[g].strength = a.strength;
   }
 
-  // 3. H = X A_g^T (fp32, for dB): rank items only, on the tensor cores (s = 1)
+  // 2. H = X A_g^T (fp32, for dB): rank items only, on the tensor cores (s = 1)
   {
     wp_adapter h_ad[kMaxGroups];
     for (int g = 0; g < G; ++g) {
@@ -1058,12 +1065,12 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
     if (rc != WP_OK) return rc;
   }
 
-  // 4. dX = dY W + sum_g s_g (dY B_g) A_g on the fused tensor-core kernel, which also
-  //    leaves s_g dY B_g (fp32) in Gs; without dX, a rank-items-only call computes Gs
-  const wp_mat Wt_m{Wt, WP_BF16, K, Ntot, Ntot, nullptr};
+  // 3. dX = dY W + sum_g s_g (dY B_g) A_g on the fused tensor-core kernel, the weight read as
+  //    stored ([Ntot, K]: MN-major tiles, a 4-bit W dequantised straight into them), which
+  //    also leaves s_g dY B_g (fp32) in Gs; without dX, a rank-items-only call computes Gs
   if (dX) {
-    rc = fwd_impl(dY, &Wt_m, nullptr, 1, false, fwd_ad, G, request_scale, dX, ws + L.fwd,
-                  L.fwd_bytes, stream, Gs, L.R);
+    rc = fwd_impl(dY, W, nullptr, 1, false, fwd_ad, G, request_scale, dX, ws + L.fwd, L.fwd_bytes, stream, Gs,
+                  L.R, /*rank_only=*/false, /*swiglu=*/false, /*eg=*/nullptr, /*w_mn=*/true);
     if (rc != WP_OK) return rc;
   } else {
     // s_g dY B_g alone: rank items only
@@ -1072,7 +1079,7 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
     if (rc != WP_OK) return rc;
   }
 
-  // 5. dA_g = (s_g G_g)^T X  and  dB_g = s_g dY_g^T H_g (exact zeros when s_g == 0): token
+  // 4. dA_g = (s_g G_g)^T X  and  dB_g = s_g dY_g^T H_g (exact zeros when s_g == 0): token
   //    contractions on the tensor cores with the fp32 H and s G as two bf16 pieces each; all
   //    groups in one contraction when their pieces fit 256 columns, else one per group
   for (int g = 0; g < G; ++g) {

@@ -34,6 +34,7 @@ constexpr int kTcThreadsNF4 = 768;
 constexpr int kMHalvesNF4 = 2;
 constexpr int kRawBytes = 128 * 32;             // 4-bit codes of 128 rows x 64 K per stage
 constexpr int kAmBytes = 128 * 4 * 4;           // block scales of 128 rows x 4 K steps
+constexpr int kAmBytesMN = 64 * 4 * 4;         // W stored [in, out]: 64 K rows x a 4-block box
 constexpr int kCodeSlotBytes = kRawBytes + kAmBytes;
 constexpr int kMaxCodeSlots = 8;
 constexpr int kMaxStages = 8;
@@ -71,6 +72,9 @@ struct TcParams {
   int r_blocks;                // 256-row blocks: one rank item and one flag each
   int m_shift;                 // 4-bit W: 1 (a tile is two 256-row halves that share the
                                // dequantised weight tile), else 0
+  int w_mn;                    // W stored [in, out] (the backward's dX pass reads the forward's
+                               // W as it is): weight tiles are MN-major MMA operands; a 4-bit
+                               // W's codes are [in rows, out / 2 bytes], blocks of 64 along out
   int rlead;                   // rank items run this many rounds of tiles ahead of their tiles
   int has_base;
   int n_ad;                    // adapters on the tensor cores (bf16, or FP32 as pieces)
@@ -124,7 +128,9 @@ struct TcMaps {
   CUtensorMap w;
   CUtensorMap y;                 // output, 128-byte swizzled boxes of 128 rows
   CUtensorMap wq;                // 4-bit W codes: [N rows, K/2 bytes], boxes of 128 x 32 bytes
+                                 // (w_mn: [K rows, N/2 bytes], boxes of 64 x 64 bytes)
   CUtensorMap am;                // 4-bit W block scales: [N rows, K/64] fp32, boxes of 128 x 4
+                                 // (w_mn: [K rows, N/64], boxes of 64 x 4)
   CUtensorMap hq;                // H~ [T rows, hq_ld], boxes of 128 rows x 64 ranks
   CUtensorMap hq32;              // the same with boxes of 128 rows x 32 ranks (64-byte swizzle)
   CUtensorMap ap;                // packed A rows [npass htot, K]: boxes of htot/2 rows x 64
@@ -421,8 +427,6 @@ int launch_nf4_requant(const float* U, long long numel, const NF4Table& tab, voi
                        cudaStream_t stream);
 int launch_transpose_bf16(const void* src, long long ld_s, int R, int C, void* dst, long long ld_d,
                           cudaStream_t stream);
-int launch_nf4_dequant_t(const void* codes, const float* absmax, int N, int K, const NF4Table& tab,
-                         void* dst, long long ld_d, cudaStream_t stream);
 
 // ------------------------------------------------------------------ unfused chain (exact tier)
 // One elementwise step of the chain on a [T, N] bf16 matrix Y (N % 8 == 0, 16-byte aligned

@@ -535,6 +535,26 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
          | ((M >> 4) << 24);    // M / 16
 }
 
+// MN-major operand in the 128-byte swizzle: 64-element chunks along M/N 8192 bytes apart
+// (boxes of 64 K rows x 64 elements), 8-row groups along K 1024 bytes apart; K advances
+// 2048 bytes per 16-deep MMA.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);          // start address
+  d |= static_cast<uint64_t>(8192 >> 4) << 16;                      // LBO: next 64-element chunk
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                      // SBO: next 8-row group along K
+  d |= static_cast<uint64_t>(1) << 46;                              // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                              // 128-byte swizzle
+  return d;
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(uint32_t M, uint32_t N) {
+  return idesc_bf16_f32(M, N) | (1u << 15) | (1u << 16);            // A and B MN-major
+}
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(uint32_t M, uint32_t N) {
+  return idesc_bf16_f32(M, N) | (1u << 16);                         // B MN-major
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

@@ -269,10 +269,19 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         // free once the group that dequantised the slot's previous step is done with it
         if (!mbar_wait(&code_empty[slot], ((c_issued / R) & 1u) ^ 1u, abort_flag, tmo, status)) return false;
         uint8_t* cs = codes + slot * kCodeSlotBytes;
-        mbar_arrive_expect_tx(&code_full[slot], kRawBytes + (p.am_tma ? kAmBytes : 0));
-        tma_load_2d_hint(cs, &maps.wq, c_kb * (kBK / 2), c_wrow, &code_full[slot], keep);
-        // the block scales of this K step and the next three (16-byte boxes)
-        if (p.am_tma) tma_load_2d_hint(cs + kRawBytes, &maps.am, c_kb & ~3, c_wrow, &code_full[slot], keep);
+        if (p.w_mn) {
+          // W stored [in, out]: 64 rows of the step's K range x this CTA's 128 output columns
+          // (64 bytes), and their block scales (a 16-byte box of four blocks holding both)
+          mbar_arrive_expect_tx(&code_full[slot], kRawBytes + (p.am_tma ? kAmBytesMN : 0));
+          tma_load_2d_hint(cs, &maps.wq, c_wrow / 2, c_kb * kBK, &code_full[slot], keep);
+          if (p.am_tma)
+            tma_load_2d_hint(cs + kRawBytes, &maps.am, (c_wrow / 64) & ~3, c_kb * kBK, &code_full[slot], keep);
+        } else {
+          mbar_arrive_expect_tx(&code_full[slot], kRawBytes + (p.am_tma ? kAmBytes : 0));
+          tma_load_2d_hint(cs, &maps.wq, c_kb * (kBK / 2), c_wrow, &code_full[slot], keep);
+          // the block scales of this K step and the next three (16-byte boxes)
+          if (p.am_tma) tma_load_2d_hint(cs + kRawBytes, &maps.am, c_kb & ~3, c_wrow, &code_full[slot], keep);
+        }
         ++c_kb;
         ++c_issued;
         return true;
@@ -326,7 +335,14 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               continue;
             } else {
               tma_load_2d_pair(st, &maps.x, kb * kBK, x_row, fb);
-              tma_load_2d_pair_hint(st + kATileBytes, &maps.w, kb * kBK, w_row, fb, keep);
+              if (p.w_mn) {
+                // W stored [in, out]: the step's 64 K rows x this CTA's 128 output columns, as
+                // two 64-column boxes (an MN-major operand)
+                tma_load_2d_pair_hint(st + kATileBytes, &maps.w, w_row, kb * kBK, fb, keep);
+                tma_load_2d_pair_hint(st + kATileBytes + kATileBytes / 2, &maps.w, w_row + 64, kb * kBK, fb, keep);
+              } else {
+                tma_load_2d_pair_hint(st + kATileBytes, &maps.w, kb * kBK, w_row, fb, keep);
+              }
             }
             advance();
           }
@@ -389,6 +405,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       uint32_t nuse[2] = {0, 0};
       int count = 0;
       const uint32_t idesc_acc = idesc_bf16_f32(kPairM, kBN);
+      const uint32_t idesc_acc_mn = idesc_bf16_f32_bmn(kPairM, kBN);
       const uint32_t idesc_h = idesc_bf16_f32(kPairM, p.htot > 0 ? p.htot : 16);
       const uint32_t stage_base = smem_u32(sbase);
       bool ok = true;
@@ -435,13 +452,16 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
             for (int kb = 0; kb < p.k_blocks; ++kb) {
               uint32_t st;
               if (!(ok = take(st))) break;
+              // the weight slot: K-major, or MN-major when W is stored [in, out]
               const uint64_t bd = sw128_kmajor_desc(st + kXBytes);
+              const uint32_t bmn = st + kXBytes;
 #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk)
 #pragma unroll
                 for (int h = 0; h < kMH; ++h)
-                  mma_bf16_pair(acc_t + h * kBN, sw128_kmajor_desc(st + h * kATileBytes) + 2 * kk, bd + 2 * kk,
-                                idesc_acc, (kb | kk) != 0 ? 1u : 0u);
+                  mma_bf16_pair(acc_t + h * kBN, sw128_kmajor_desc(st + h * kATileBytes) + 2 * kk,
+                                p.w_mn ? sw128_mnmajor_desc(bmn + kk * 2048) : bd + 2 * kk,
+                                p.w_mn ? idesc_acc_mn : idesc_acc, (kb | kk) != 0 ? 1u : 0u);
               give_back();
             }
           }
@@ -1002,9 +1022,15 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       }
       const Tile& t = it.t;
       const int a0 = p.ad_begin[t.g], a1 = p.ad_begin[t.g + 1];
+      // K-major: thread r dequantises weight row (output column) wrow, 64 K values per step.
+      // W stored [in, out] (w_mn): thread r takes K row kb * 64 + (r & 63) of the step and the
+      // 64 output columns mcol.. of half r >> 6 of this CTA's 128, written as row r of the
+      // MN-major tile (the two 64-column halves 8 KiB apart)
       const int wrow = weight_row(p, t, cta) + r;
       const bool wrow_ok = wrow < p.N;
       const float* am_row = p.absmax + static_cast<long long>(wrow_ok ? wrow : 0) * kb64;
+      const int mcol = weight_row(p, t, cta) + 64 * (r >> 6);
+      const int mrow = r & 63;
       for (int kb = 0; kb < p.k_blocks && ok; ++kb, ++kc) {
         if (static_cast<int>(kc % 3u) != group) {       // another group's K step
           pass();
@@ -1015,10 +1041,21 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         const uint8_t* raw = codes + slot * kCodeSlotBytes;                // codes | block scales
         // block scale: from the stage (TMA, no global load left in flight when this warp
-        // releases the tile to the peer CTA) or, for K % 256 != 0, straight from memory
-        const float am = p.am_tma ? reinterpret_cast<const float*>(raw + kRawBytes)[r * 4 + (kb & 3)]
-                                  : (wrow_ok ? __ldg(am_row + kb) : 0.f);
-        nf4_dequant_row(raw + r * 32, 0, (r >> 2) & 1, am, lv, smem_u32(sbase + stage * SB + kXBytes), r);
+        // releases the tile to the peer CTA) or, when the scales' rows are not 16-byte
+        // multiples, straight from memory
+        if (p.w_mn) {
+          const int krow = kb * kBK + mrow;
+          const float am = p.am_tma ? reinterpret_cast<const float*>(raw + kRawBytes)[mrow * 4 + ((mcol >> 6) & 3)]
+                                    : ((krow < p.K && mcol < p.N)
+                                           ? __ldg(p.absmax + static_cast<long long>(krow) * (p.N / 64) + mcol / 64)
+                                           : 0.f);
+          nf4_dequant_row(raw + mrow * 64, 2 * (r >> 6), (mrow >> 1) & 3, am, lv,
+                          smem_u32(sbase + stage * SB + kXBytes), r);
+        } else {
+          const float am = p.am_tma ? reinterpret_cast<const float*>(raw + kRawBytes)[r * 4 + (kb & 3)]
+                                    : (wrow_ok ? __ldg(am_row + kb) : 0.f);
+          nf4_dequant_row(raw + r * 32, 0, (r >> 2) & 1, am, lv, smem_u32(sbase + stage * SB + kXBytes), r);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {

@@ -23,19 +23,6 @@ namespace {
 
 constexpr int kTgABytes = 2 * 64 * 128;          // this CTA's 128 rows of D: two 64-column boxes
 
-__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);          // start address
-  d |= static_cast<uint64_t>(8192 >> 4) << 16;                      // LBO: next 64-column chunk
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;                      // SBO: next 8-token group
-  d |= static_cast<uint64_t>(1) << 46;                              // descriptor version
-  d |= static_cast<uint64_t>(2) << 61;                              // 128-byte swizzle
-  return d;
-}
-
-__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(uint32_t M, uint32_t N) {
-  return idesc_bf16_f32(M, N) | (1u << 15) | (1u << 16);            // A and B MN-major
-}
 
 __global__ void __launch_bounds__(192, 1) tokgemm_kernel(const __grid_constant__ TokGemmMaps maps,
                                                          const __grid_constant__ TokGemmParams p) {
