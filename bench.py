@@ -293,7 +293,8 @@ def run_fused(args):
 
 # ----------------------------------------------------------------------- other workloads
 CASES = ("c0_tiny_fp32", "f32_layer", "wan_qkv_rank128", "c2_ffn_up", "c2_ffn_down", "c3_nf4_gate_up_fwd",
-         "c3_nf4_down_fwd", "c3_nf4_gate_up_bwd", "c3_nf4_down_bwd", "c3_swiglu_bwd", "c4_sidecar", "c4_set_weight")
+         "c3_nf4_down_fwd", "c3_nf4_gate_up_bwd", "c3_nf4_down_bwd", "c3_swiglu_bwd", "c3_nf4_merge", "c4_sidecar",
+         "c4_set_weight")
 
 
 def per_config(dev, args, peak, hbm, only=None):
@@ -462,28 +463,50 @@ def per_config(dev, args, peak, hbm, only=None):
                                 "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bound": "hbm",
                                 "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
                                 "work": "read dH, e, g; write de, dg, h (12 B per element of F)"}
+    def flushed(fn):
+        # one call at a time after an L2 flush, CUDA events around the call; the median
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        times = []
+        for i in range(k + 3):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 3:
+                times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
+
+    if want("c3_nf4_merge"):
+        # the rank-16 patch baked into the 4-bit C3 down weight in place (dequantise, add,
+        # requantise); a small request scale keeps the repeated merges near the seeded weight
+        down3 = workloads.config3("full")[1]
+        W3, ads3 = d(down3.W), ads_of(down3)
+        ws3 = torch.empty(max(1, wpg.lora_workspace_size(wpg.WP_OP_MERGE, None, W3, ads3)), dtype=torch.uint8,
+                          device=dev)
+        t_s = time.time()
+        ms = flushed(lambda: wpg.lora_merge(W3, ads3, 1e-4, workspace=ws3))
+        marks["c3_nf4_merge"] = (t_s, time.time())
+        assert wpg.lora_device_status() == 0
+        nbytes = 2 * (W3.packed.numel() + W3.absmax.numel() * 4)
+        out["c3_nf4_merge"] = {"mb": round(nbytes / 1e6, 1), "ms": round(ms, 5),
+                               "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bound": "hbm",
+                               "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
+                               "work": "codes and scales read and written once (the adapter's 0.3 MB aside)",
+                               "timing": "one call after an L2 flush, launch included, median"}
+        del W3, ads3, ws3
+        torch.cuda.empty_cache()
     if want("c4_sidecar") or want("c4_set_weight"):
         lin4, payload = workloads.config4("full")
         if want("c4_sidecar"):
             fwd_entry("c4_sidecar", lin4, "three patches (ranks 16 fp32 / 32 / 128 bf16)")
         if want("c4_set_weight"):
-            # one call at a time after an L2 flush, CUDA events around the call
             P = d(payload)
             param = torch.empty_like(P)
-            flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-            times = []
             t_s = time.time()
-            for i in range(k + 3):
-                flush.fill_(i & 0xFF)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                wpg.lora_dense_patch(param, P, wpg.WP_PATCH_SET, 1.0)
-                e1.record(stream)
-                torch.cuda.synchronize(dev)
-                if i >= 3:
-                    times.append(e0.elapsed_time(e1))
+            ms = flushed(lambda: wpg.lora_dense_patch(param, P, wpg.WP_PATCH_SET, 1.0))
             marks["c4_set_weight"] = (t_s, time.time())
-            ms = statistics.median(times)
             nbytes = 2 * P.numel() * P.element_size()
             out["c4_set_weight"] = {"mb": round(nbytes / 1e6, 1), "ms": round(ms, 5),
                                     "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bound": "hbm",

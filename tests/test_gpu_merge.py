@@ -88,11 +88,18 @@ def test_merge_zero_strength_and_unmerge():
     assert not np.array_equal(merged, W0.data)
 
 
-@pytest.mark.parametrize("rows,cols,scale", [(256, 512, 1.0), (200, 320, 40.0)])
-def test_merge_nf4(rows, cols, scale):
+@pytest.mark.parametrize("rows,cols,scale,ranks", [
+    (256, 512, 1.0, [16]),
+    (200, 320, 40.0, [16]),                 # columns not a multiple of 256: 64-column tiles
+    (200, 768, 30.0, [16]),                 # ragged row tile, three 256-column tiles a row
+    (384, 1024, 20.0, [16, 100, 8]),        # three adapters, two K blocks: one operand stage
+    (128, 256, 20.0, [256]),                # four K blocks: the 64-column form again
+    (2560, 4096, 10.0, [32]),               # more tiles than SMs: each CTA takes two or three
+])
+def test_merge_nf4(rows, cols, scale, ranks):
     rng = np.random.default_rng(rows + cols)
     W0 = workloads.draw_nf4(rng, rows, cols)
-    ps = _patches(rng, [16], rows, cols)
+    ps = _patches(rng, ranks, rows, cols)
     W = gu.dev(W0)
     ads = [wpg.Adapter(gu.dev(p.A), gu.dev(p.B), p.alpha, p.strength) for p in ps]
     wpg.lora_merge(W, ads, scale)

@@ -1607,6 +1607,13 @@ int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n,
     if (s_of[i] != 0.0f && (ad[i].A.rows + kBK - 1) / kBK > kMergeTileMaxK) fused = false;
   MergeNF4Maps fm;
   MergeNF4Params fp{};
+  if (fused) {
+    // the 256-column form when the shape, the alignment and shared memory allow it
+    int nk_pre = 0;
+    for (int i = 0; i < n; ++i)
+      if (s_of[i] != 0.0f) nk_pre = std::max(nk_pre, static_cast<int>((ad[i].A.rows + kBK - 1) / kBK));
+    fp.wide = aligned16(W->data) && aligned16(W->absmax) && merge_nf4_wide_plan(nk_pre, in, &fp.s_op, &fp.s_c);
+  }
   if (nf4) nf4_codebook_host(tab.level);
   if (nf4 && !fused) {
     rc = launch_nf4_to_f32(W->data, W->absmax, out * in, tab, U, stream);
@@ -1636,7 +1643,7 @@ int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n,
       const int k = fp.n++;
       rc = make_map_bf16(&fm.p[k], bp, r, out, ldb, kBK, 128);
       if (rc != WP_OK) return rc;
-      rc = make_map_bf16(&fm.q[k], at, r, in, r8, kBK, 64);
+      rc = make_map_bf16(&fm.q[k], at, r, in, r8, kBK, fp.wide ? 256 : 64);
       if (rc != WP_OK) return rc;
       fp.nk[k] = (r + kBK - 1) / kBK;
       fp.nk_max = std::max(fp.nk_max, fp.nk[k]);
@@ -1661,6 +1668,12 @@ int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n,
     fp.codes = static_cast<uint8_t*>(wdata);
     fp.absmax = const_cast<float*>(W->absmax);
     fp.tab = tab;
+    if (!nf4_code_cells(tab, &fp.cells)) return WP_ERR_UNSUPPORTED;
+    if (fp.wide) {
+      rc = make_map_u8(&fm.codes, W->data, in / 2, out, in / 2, 128, 128, 128);
+      if (rc == WP_OK) rc = make_map(&fm.am, WP_FP32, W->absmax, in / 64, out, in / 64, 4, 128, /*swizzle=*/0);
+      if (rc != WP_OK) return rc;
+    }
     fp.status = tc_status_ptr();
     fp.timeout_ns = wait_limit_ns();
     if (!fp.status) return record_cuda();

@@ -376,7 +376,7 @@ struct BiasFoldParams {
 };
 int launch_bias_fold(const BiasFoldParams& p, cudaStream_t stream);
 
-// One merge pass on 128 x 128 output tiles, a CTA each: Y = fl32(fl32(s * acc) + R) with
+// One merge pass on 128 x 128 output tiles, a CTA each: Y = fl32(s * acc + R) with
 // acc = P Q^T, P [rows, r] and Q [cols, r] bf16 K-major (r <= kMergeTileMaxK * 64), R and Y
 // [rows, cols] bf16 or fp32 (R may be Y), cols % 8 == 0, 16-byte aligned rows.
 constexpr int kMergeTileMaxK = 4;
@@ -400,16 +400,32 @@ struct MergeTileMaps {
 };
 int launch_merge_tile(const MergeTileMaps& maps, const MergeTileParams& p, cudaStream_t stream);
 
-// A whole 4-bit merge in one pass (ranks up to kMergeTileMaxK * 64): a CTA per 128 rows x 64
-// columns, a thread per 64-element block: W_eff = bf16(fl32(level[q]) * absmax) in registers,
-// u = fl32(fl32(s_p * acc_p) + u) for each adapter in call order (acc_p = B_p A_p on the tensor
-// cores), then the block requantised as nf4_requant_kernel does and written in place.
+// A whole 4-bit merge in one pass (ranks up to kMergeTileMaxK * 64), a thread per 64-element
+// block: W_eff = bf16(fl32(level[q]) * absmax) in registers, u = fl32(s_p * acc_p + u) for
+// each adapter in call order (acc_p = B_p A_p on the tensor cores), then the block
+// requantised as nf4_requant_kernel does and written in place.  Two forms: one CTA per SM on
+// 128 x 256 tiles whose codes and scales move by TMA (merge_nf4_wide_plan), else persistent
+// CTAs on 128 x 64 tiles with plain loads and stores.
+// The 4-bit code of x in [-1, 1] by cells of width 1/16: cell c = floor(16 x) + 16 holds at
+// most one level midpoint (they are at least 0.08 apart), so the code is base[c] (the
+// midpoints below the cell) plus one when x exceeds the cell's next midpoint next_mid[c] (the
+// smallest midpoint at or above the cell's start; 2 when none).
+constexpr int kCodeCells = 33;            // 32 cells of width 1/16 over [-1, 1), and x = 1
+struct NF4Cells {
+  float next_mid[kCodeCells];
+  int base[kCodeCells];
+};
+bool nf4_code_cells(const NF4Table& tab, NF4Cells* cells);
+
 struct MergeNF4Params {
   int rows, cols;              // W [rows, cols], cols % 64 == 0
   uint8_t* codes;              // [rows, cols / 2], rewritten
   float* absmax;               // [rows * cols / 64], rewritten
   NF4Table tab;
+  NF4Cells cells;              // the code search by cells (nf4_code_cells)
   int n, nk_max;               // adapters (non-zero s), the most K blocks of any of them
+  int wide;                    // the 256-column form (merge_nf4_wide_plan), with its stage counts
+  int s_op, s_c;
   int nk[kMaxAd];
   float s[kMaxAd];
   int* status;
@@ -417,8 +433,13 @@ struct MergeNF4Params {
 };
 struct MergeNF4Maps {
   CUtensorMap p[kMaxAd];       // B_p [rows, r_p]: boxes of 64 K x 128 rows
-  CUtensorMap q[kMaxAd];       // A_p^T [cols, r_p]: boxes of 64 K x 64 rows
+  CUtensorMap q[kMaxAd];       // A_p^T [cols, r_p]: boxes of 64 K x 64 rows (wide: x 256 rows)
+  CUtensorMap codes;           // wide: codes [rows, cols / 2] bytes, boxes of 128 B x 128 rows, 128-byte swizzle
+  CUtensorMap am;              // wide: absmax [rows, cols / 64] fp32, boxes of 4 x 128 rows
 };
+// The wide form applies (columns a multiple of 256, shared memory for at least two code
+// stages): its operand and code stage counts.
+bool merge_nf4_wide_plan(int nk_max, long long cols, int* s_op, int* s_c);
 int launch_merge_nf4(const MergeNF4Maps& maps, const MergeNF4Params& p, cudaStream_t stream);
 
 int launch_nf4_to_f32(const void* codes, const float* absmax, long long numel, const NF4Table& tab, float* U,

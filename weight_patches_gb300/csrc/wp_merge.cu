@@ -125,4 +125,25 @@ int launch_nf4_requant(const float* U, long long numel, const NF4Table& tab, voi
   return WP_OK;
 }
 
+// The code search by cells: cell c holds [-1 + c/16, -1 + (c+1)/16), 32 cells over [-1, 1)
+// and a 33rd from 1.  The midpoints (fp32, as the kernels form them) below a
+// cell's lower end count into its base code; the first midpoint at or above it is the one a
+// value in the cell is compared against.  False if a cell holds two midpoints (one compare
+// cannot resolve it); the NF4 midpoints are at least 0.08 apart, so no cell holds two.
+bool nf4_code_cells(const NF4Table& tab, NF4Cells* cells) {
+  float mid[15];
+  for (int k = 0; k < 15; ++k) mid[k] = (tab.level[k] + tab.level[k + 1]) * 0.5f;
+  for (int k = 0; k + 1 < 15; ++k)
+    if (!(mid[k] < mid[k + 1])) return false;
+  for (int c = 0; c < kCodeCells; ++c) {
+    const float lo = -1.0f + static_cast<float>(c) / 16.0f, hi = lo + 1.0f / 16.0f;
+    int base = 0;
+    while (base < 15 && mid[base] < lo) ++base;
+    if (base + 1 < 15 && mid[base + 1] < hi) return false;
+    cells->base[c] = base;
+    cells->next_mid[c] = base < 15 ? mid[base] : 2.0f;
+  }
+  return true;
+}
+
 }  // namespace wp

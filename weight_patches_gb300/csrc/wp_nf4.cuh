@@ -13,6 +13,8 @@
 
 #include <cstdint>
 
+#include "wp_internal.h"
+
 #include "wp_ptx.cuh"
 
 namespace wp {
@@ -107,6 +109,105 @@ __device__ __forceinline__ void nf4_dequant_regs(const uint32_t (&cw)[8], float 
       u[8 * w + 2 * k + 1] = __uint_as_float(o[k] & 0xffff0000u);
     }
   }
+}
+
+// x = fl32(u / a) for a > 0 by Markstein's division (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with
+// y = RN(1/a), q = RN(u y) is within an ulp of u / a, the residual e = u - a q is exact as one
+// fused multiply-add, and RN(q + e y) is the correctly rounded quotient as long as nothing
+// underflows.  For a in [2^-90, 2^90] and a quotient of magnitude 2^-5 or more (every level
+// midpoint is further than that from zero) the residual is a multiple of 2^-141, so it is
+// exact; a smaller quotient may come out an ulp off, which moves it across no midpoint.
+// Outside that range scale_reciprocal gives 0 and the caller divides plainly instead.
+__device__ __forceinline__ float div_by_scale(float u, float a, float y) {
+  const float q = __fmul_rn(u, y);
+  const float e = __fmaf_rn(-q, a, u);
+  return __fmaf_rn(e, y, q);
+}
+
+// y for div_by_scale: RN(1/a) for a in [2^-90, 2^90], else 0 (the plain division).
+__device__ __forceinline__ float scale_reciprocal(float a) {
+  return a >= 0x1p-90f && a <= 0x1p90f ? __frcp_rn(a) : 0.f;
+}
+
+// max(a, b) with a NaN operand giving NaN (fmaxf drops it)
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// The 4-bit code of x in [-1, 1] (the number of level midpoints below it) by the cells of
+// nf4_code_cells, held in shared memory at cells_addr as two word arrays of kCodeCells: the
+// cells' next midpoints, then their base codes, for cell c = floor(16 x) + 16.  Two 4-byte
+// tables rather than one of pairs: a warp's 32 lookups then fall in 32 different banks
+// unless two lanes read cells 0 and 32.  The index comes from one fused multiply-add rounded
+// down, RD(16 x + 2^23 + 16): the sum lies in [2^23, 2^24), where the float spacing is 1, so
+// its bits are those of 2^23 plus c exactly.  kClamp: x may be a NaN, which lands outside the
+// 33 cells and takes cell 0, whose compare fails (code 0, as nf4_code_of gives).
+template <bool kClamp>
+__device__ __forceinline__ uint32_t nf4_code_by_cells(float x, uint32_t cells_addr) {
+  const uint32_t bits = __float_as_uint(__fmaf_rd(x, 16.0f, 8388624.0f));
+  uint32_t addr;
+  if (kClamp) {
+    uint32_t c = bits - 0x4B000000u;
+    c = c < static_cast<uint32_t>(kCodeCells) ? c : 0u;
+    addr = cells_addr + 4u * c;
+  } else {
+    addr = 4u * bits + (cells_addr - 4u * 0x4B000000u);   // the same address, modulo 2^32
+  }
+  float next_mid;
+  uint32_t base, gt;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(next_mid) : "r"(addr));
+  asm volatile("ld.shared.u32 %0, [%1+%2];" : "=r"(base) : "r"(addr), "n"(4 * kCodeCells));
+  asm("set.gt.u32.f32 %0, %1, %2;" : "=r"(gt) : "f"(x), "f"(next_mid));   // all ones when above
+  return base - gt;
+}
+
+// Requantise one block held in registers: absmax' = m = max |u| (m > 0), the codes of
+// x = fl32(u / m) packed as stored (byte k: element 2k in the high nibble).  kFast: the
+// quotient by div_by_scale with y = scale_reciprocal(m) != 0 and no NaN in the block; else the
+// plain division and the NaN-safe cell index.
+template <bool kFast>
+__device__ __forceinline__ void nf4_requant_regs(const float (&u)[64], float m, float y, uint32_t cells_addr,
+                                                 uint32_t (&cw)[8]) {
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    uint32_t c4 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float x = kFast ? div_by_scale(u[8 * w + i], m, y) : __fdiv_rn(u[8 * w + i], m);
+      c4 += nf4_code_by_cells<!kFast>(x, cells_addr) << (8 * (i >> 1) + ((i & 1) ? 0 : 4));
+    }
+    cw[w] = c4;
+  }
+}
+
+// The whole requantisation of a block: returns absmax' = max |u| (the largest of the other
+// elements when some are NaN) and the codes, x = fl32(u / absmax') rounded to the nearest
+// level (a value on a midpoint takes the lower code); an all-zero block keeps scale 0 and
+// level 0's code.  One pass finds the maximum with a NaN kept, which sends such a block the
+// plain way; the usual block takes the fast quotient once for all its elements.
+__device__ __forceinline__ float nf4_requant_block(const float (&u)[64], uint32_t cells_addr, uint32_t (&cw)[8]) {
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) m = fmax_nan(m, fabsf(u[i]));
+  const bool nan_in = m != m;
+  if (nan_in) {
+    m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(u[i]));
+  }
+  const float y = nan_in ? 0.f : scale_reciprocal(m);
+  if (y != 0.f) {
+    nf4_requant_regs<true>(u, m, y, cells_addr, cw);
+  } else if (m > 0.f) {
+    nf4_requant_regs<false>(u, m, y, cells_addr, cw);
+  } else {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) cw[w] = 0x77777777u;
+  }
+  return m;
 }
 
 // The 4-bit code of x = u / absmax' (the nearest level): the number of level midpoints
