@@ -1608,11 +1608,16 @@ int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n,
   MergeNF4Maps fm;
   MergeNF4Params fp{};
   if (fused) {
-    // the 256-column form when the shape, the alignment and shared memory allow it
-    int nk_pre = 0;
+    // the 256-column form when the shape, the alignment and shared memory allow it; it reads
+    // each A_p where it lies
+    int ranks[kMaxAd], nr = 0;
+    bool ok = aligned16(W->data) && aligned16(W->absmax);
     for (int i = 0; i < n; ++i)
-      if (s_of[i] != 0.0f) nk_pre = std::max(nk_pre, static_cast<int>((ad[i].A.rows + kBK - 1) / kBK));
-    fp.wide = aligned16(W->data) && aligned16(W->absmax) && merge_nf4_wide_plan(nk_pre, in, &fp.s_op, &fp.s_c);
+      if (s_of[i] != 0.0f) {
+        ranks[nr++] = static_cast<int>(ad[i].A.rows);
+        ok = ok && aligned16(ad[i].A.data) && ad[i].A.ld % 8 == 0;
+      }
+    fp.wide = ok && merge_nf4_wide_plan(ranks, nr, in, &fp);
   }
   if (nf4) nf4_codebook_host(tab.level);
   if (nf4 && !fused) {
@@ -1626,8 +1631,10 @@ int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n,
     const int r = static_cast<int>(a.A.rows);
     const long long r8 = (r + 7) / 8 * 8;
     uint16_t* at = reinterpret_cast<uint16_t*>(ws + L.at[i]);
-    rc = launch_transpose_bf16(a.A.data, a.A.ld, r, static_cast<int>(in), at, r8, stream);
-    if (rc != WP_OK) return rc;
+    if (!fp.wide) {
+      rc = launch_transpose_bf16(a.A.data, a.A.ld, r, static_cast<int>(in), at, r8, stream);
+      if (rc != WP_OK) return rc;
+    }
     const void* bp = a.B.data;
     long long ldb = a.B.ld;
     if (L.copy_b[i]) {
@@ -1643,7 +1650,8 @@ int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n,
       const int k = fp.n++;
       rc = make_map_bf16(&fm.p[k], bp, r, out, ldb, kBK, 128);
       if (rc != WP_OK) return rc;
-      rc = make_map_bf16(&fm.q[k], at, r, in, r8, kBK, fp.wide ? 256 : 64);
+      rc = fp.wide ? make_map_bf16(&fm.q[k], a.A.data, in, r, a.A.ld, 64, fp.kbox[k])
+                   : make_map_bf16(&fm.q[k], at, r, in, r8, kBK, 64);
       if (rc != WP_OK) return rc;
       fp.nk[k] = (r + kBK - 1) / kBK;
       fp.nk_max = std::max(fp.nk_max, fp.nk[k]);
@@ -1671,7 +1679,7 @@ int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n,
     if (!nf4_code_cells(tab, &fp.cells)) return WP_ERR_UNSUPPORTED;
     if (fp.wide) {
       rc = make_map_u8(&fm.codes, W->data, in / 2, out, in / 2, 128, 128, 128);
-      if (rc == WP_OK) rc = make_map(&fm.am, WP_FP32, W->absmax, in / 64, out, in / 64, 4, 128, /*swizzle=*/0);
+      if (rc == WP_OK) rc = make_map(&fm.am, WP_FP32, W->absmax, in / 64, out, in / 64, 16, 128, /*swizzle=*/0);
       if (rc != WP_OK) return rc;
     }
     fp.status = tc_status_ptr();

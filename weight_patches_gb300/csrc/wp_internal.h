@@ -424,8 +424,11 @@ struct MergeNF4Params {
   NF4Table tab;
   NF4Cells cells;              // the code search by cells (nf4_code_cells)
   int n, nk_max;               // adapters (non-zero s), the most K blocks of any of them
-  int wide;                    // the 256-column form (merge_nf4_wide_plan), with its stage counts
-  int s_op, s_c;
+  int wide;                    // the 256-column form (merge_nf4_wide_plan), with its plan:
+  int s_a, s_c;                //   A_p stages and code stages,
+  int kbox[kMaxAd];            //   each adapter's K rows per A_p box (r rounded up to 16, at most 64),
+  int boff[kMaxAd];            //   its first B_p box in a group buffer,
+  int a_bytes, b_bytes;        //   one A_p stage, one group's B_p boxes
   int nk[kMaxAd];
   float s[kMaxAd];
   int* status;
@@ -433,13 +436,14 @@ struct MergeNF4Params {
 };
 struct MergeNF4Maps {
   CUtensorMap p[kMaxAd];       // B_p [rows, r_p]: boxes of 64 K x 128 rows
-  CUtensorMap q[kMaxAd];       // A_p^T [cols, r_p]: boxes of 64 K x 64 rows (wide: x 256 rows)
+  CUtensorMap q[kMaxAd];       // A_p^T [cols, r_p]: boxes of 64 K x 64 rows; wide: A_p [r_p, cols] itself,
+                               // boxes of 64 columns x kbox rows
   CUtensorMap codes;           // wide: codes [rows, cols / 2] bytes, boxes of 128 B x 128 rows, 128-byte swizzle
   CUtensorMap am;              // wide: absmax [rows, cols / 64] fp32, boxes of 4 x 128 rows
 };
-// The wide form applies (columns a multiple of 256, shared memory for at least two code
-// stages): its operand and code stage counts.
-bool merge_nf4_wide_plan(int nk_max, long long cols, int* s_op, int* s_c);
+// The wide form applies (columns a multiple of 256, shared memory for its stages) to adapters
+// of these ranks: fills p's plan (kbox, nk, boff, a_bytes, b_bytes, s_a, s_c).
+bool merge_nf4_wide_plan(const int* ranks, int n, long long cols, MergeNF4Params* p);
 int launch_merge_nf4(const MergeNF4Maps& maps, const MergeNF4Params& p, cudaStream_t stream);
 
 int launch_nf4_to_f32(const void* codes, const float* absmax, long long numel, const NF4Table& tab, float* U,

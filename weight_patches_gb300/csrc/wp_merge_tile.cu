@@ -474,23 +474,31 @@ __global__ void __launch_bounds__(128, 4) merge_nf4_kernel(const __grid_constant
 }
 
 // The wide form, for weights whose columns are a multiple of 256: one CTA per SM, sixteen
-// warps, tiles of 128 rows x 256 columns.  Warp w reads tensor-memory lanes 32 (w % 4) on and
-// owns column block w / 4 of the tile, a thread per row and block as above; one job per tile
-// and adapter is a single 128 x 256 MMA.  The codes and scales move by TMA: the tile's 16 KiB
-// of codes (128 B a row, 128-byte swizzle, so that the rows a warp reads fall in different
-// banks) and its 2 KiB of scales (4 a row) land in one of s_c (3 or 4) shared-memory stages
-// s_c - 2 tiles ahead, are requantised in place and leave by TMA stores, so that every global
-// access is a whole-line transfer that no thread waits for.  Thread 0 issues the copies, the
-// MMAs and the stores between its share of the arithmetic: at the top of job j the operands
-// of job j + s_op and the MMAs of job j + 1, at a tile's first job the store of the tile before
-// and the codes of a later tile into the stage stored a tile ago.  Operand stages s_op (1 or 2)
-// and two 256-column accumulator buffers as above.
+// compute warps and a producer warp, tiles of 128 rows x 256 columns.  Compute warp w reads
+// tensor-memory lanes 32 (w % 4) on and owns column block w / 4 of the tile, a thread per row
+// and block as above; one job per tile and adapter is a single 128 x 256 MMA.
+//
+// A CTA takes a contiguous run of groups, a group being 4 tiles side by side (128 x 1024;
+// fewer at a row's end), in row-major order.  Everything moves by TMA, in as few box rows as
+// the layouts allow (the copy engine's time goes by rows):
+//   codes   one 128 x 128-byte box per tile (128-byte swizzle, so that the rows a warp reads
+//           fall in different banks), in and out through a ring of s_c stages, loaded s_c - 3
+//           tiles ahead;
+//   scales  one 128 x 16-float box per group, in and out (a ring of three group buffers);
+//   B_p     the 128 rows x r of every adapter once per group (K-major, 64-wide K boxes, two
+//           group buffers);
+//   A_p     per job, read where it lies ([r, in] row-major: the MMA's B operand MN-major), four
+//           boxes of 64 columns x kbox rows (kbox = r rounded up to 16, at most 64), a ring of
+//           s_a stages.
+// The producer's lane 0 issues all copies and MMAs and the stores, waiting only on barriers;
+// the compute warps wait for their tile's codes and scales and for each job's accumulator,
+// release the accumulator buffer per warp (empty) and report the tile written (cwritten).
 constexpr int kWCols = 256;                       // tile columns
 constexpr int kWCodeBox = 128 * 128;              // 128 rows x 128 code bytes: 16 KiB
-constexpr int kWAmBox = 128 * 16;                 // 128 rows x 4 scales: 2 KiB
-constexpr int kWCodeStage = kWCodeBox + kWAmBox;  // 18 KiB (a multiple of 1 KiB)
-constexpr int kWQBox = kWCols * kBK * 2;          // 256 A_p^T rows x 64 K: 32 KiB
-constexpr int kWOpK = kMNBoxP + kWQBox;           // one K block of both operands: 48 KiB
+constexpr int kWAmBox = 128 * 64;                 // a group's scales: 128 rows x 16 floats, 8 KiB
+constexpr int kWAmRing = 3;
+constexpr int kWMaxSA = 4, kWMaxSC = 8;
+constexpr int kWThreads = 17 * 32;
 
 __device__ __forceinline__ void lds128w(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr));
@@ -499,42 +507,53 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-__global__ void __launch_bounds__(512, 1) merge_nf4_wide_kernel(const __grid_constant__ MergeNF4Maps maps,
-                                                                const __grid_constant__ MergeNF4Params p) {
+__global__ void __launch_bounds__(kWThreads, 1) merge_nf4_wide_kernel(const __grid_constant__ MergeNF4Maps maps,
+                                                                      const __grid_constant__ MergeNF4Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* sbase = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  const int op_bytes = p.nk_max * kWOpK;          // [nk_max] B_p boxes, then [nk_max] A_p^T boxes
-  const int S_op = p.s_op, S_c = p.s_c;
-  uint8_t* sC = sbase + S_op * op_bytes;          // [S_c] code stages: codes box, then scales box
-  uint64_t* full = reinterpret_cast<uint64_t*>(sC + S_c * kWCodeStage);   // [2] operand stage landed
-  uint64_t* done = full + 2;                      // [2] accumulator buffer's MMAs finished
-  uint64_t* empty = full + 4;                     // [2] every warp has read an accumulator buffer
-  uint64_t* cfull = full + 6;                     // [4] code stage landed
-  uint64_t* cwritten = full + 10;                 // [4] every warp has written its requantised codes
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 14);
+  const int S_a = p.s_a, S_c = p.s_c;
+  uint8_t* sB = sbase;                            // [2] groups' B_p boxes, [adapter][K block] of 16 KiB
+  uint8_t* sA = sB + 2 * p.b_bytes;               // [S_a] jobs' A_p boxes, [K block][column group]
+  uint8_t* sC = sA + S_a * p.a_bytes;             // [S_c] tiles' codes
+  uint8_t* sM = sC + S_c * kWCodeBox;             // [3] groups' scales
+  uint64_t* fullA = reinterpret_cast<uint64_t*>(sM + kWAmRing * kWAmBox);   // [4] A_p stage landed
+  uint64_t* done = fullA + kWMaxSA;               // [2] accumulator buffer's MMAs finished
+  uint64_t* empty = done + 2;                     // [2] every compute warp has read a buffer
+  uint64_t* cfull = empty + 2;                    // [8] code stage landed
+  uint64_t* cwritten = cfull + kWMaxSC;           // [8] every compute warp has written its codes
+  uint64_t* bfull = cwritten + kWMaxSC;           // [2] a group's B_p landed
+  uint64_t* mfull = bfull + 2;                    // [3] a group's scales landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mfull + kWAmRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   __shared__ uint32_t s_cells[2 * kCodeCells];    // the code search by cells: next midpoints, base codes
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = 32 * (warp & 3) + lane;           // row within the tile
-  const int b = warp >> 2;                        // 64-column block within the tile
-  const int nbw = p.cols / kWCols;
-  const int tiles = nbw * ((p.rows + 127) / 128);
-  const int ntile = blockIdx.x < tiles ? (tiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
-  const int J = ntile * p.n;
+  const int nbw = p.cols / kWCols, ngc = (nbw + 3) / 4, nrt = (p.rows + 127) / 128;
+  const long long G = static_cast<long long>(ngc) * nrt;
+  const int g0 = static_cast<int>(G * blockIdx.x / gridDim.x), g1 = static_cast<int>(G * (blockIdx.x + 1) / gridDim.x);
+  auto tiles_before = [&](int g) { return (g / ngc) * nbw + min((g % ngc) * 4, nbw); };
+  const int T0 = tiles_before(g0), ntile = tiles_before(g1) - T0, J = ntile * p.n;
+  // tile k of this CTA: global tile T0 + k, row-major; its group (counted from this CTA's
+  // first) and its place in the group
+  auto group_of = [&](int k) { const int t = T0 + k; return (t / nbw) * ngc + (t % nbw) / 4 - g0; };
+  auto pos_of = [&](int k) { return ((T0 + k) % nbw) & 3; };
+  auto last_in_group = [&](int k) { const int tc = (T0 + k) % nbw; return (tc & 3) == 3 || tc == nbw - 1; };
+
   for (int c = threadIdx.x; c < kCodeCells; c += blockDim.x)
     s_cells[c] = __float_as_uint(p.cells.next_mid[c]), s_cells[kCodeCells + c] = static_cast<uint32_t>(p.cells.base[c]);
   if (threadIdx.x == 0) {
+    for (int i = 0; i < kWMaxSA; ++i) mbar_init(fullA + i, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(full + i, 1);
       mbar_init(done + i, 1);
       mbar_init(empty + i, 16);
+      mbar_init(bfull + i, 1);
     }
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kWMaxSC; ++i) {
       mbar_init(cfull + i, 1);
       mbar_init(cwritten + i, 16);
     }
+    for (int i = 0; i < kWAmRing; ++i) mbar_init(mfull + i, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -546,172 +565,207 @@ __global__ void __launch_bounds__(512, 1) merge_nf4_wide_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  const uint32_t cells_addr = smem_u32(s_cells);
 
-  auto tile_at = [&](int k, int& row0, int& tc) {
-    const int t = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
-    row0 = (t / nbw) * 128;
-    tc = t % nbw;
-  };
-  auto op_par = [&](int j) { return static_cast<uint32_t>(S_op == 2 ? (j >> 1) : j) & 1u; };
-  // thread 0's issue state: how many jobs' operands, MMAs and tiles' codes it has started
-  int op_issued = 0, mma_issued = 0, codes_issued = 0;
-  auto issue_op = [&](int j) {
-    const int k = j / p.n, a = j - k * p.n, os = S_op == 2 ? (j & 1) : 0;
-    int row0, tc;
-    tile_at(k, row0, tc);
-    uint8_t* sP = sbase + os * op_bytes;
-    uint8_t* sQ = sP + p.nk_max * kMNBoxP;
-    const uint64_t keep = l2_evict_last();
-    mbar_arrive_expect_tx(full + os, static_cast<uint32_t>(p.nk[a]) * kWOpK);
-    for (int kb = 0; kb < p.nk[a]; ++kb) {
-      tma_load_2d_hint(sP + kb * kMNBoxP, &maps.p[a], kb * kBK, row0, full + os, keep);
-      tma_load_2d_hint(sQ + kb * kWQBox, &maps.q[a], kb * kBK, tc * kWCols, full + os, keep);
-    }
-    op_issued = j + 1;
-  };
-  auto issue_mma = [&](int j) {
-    const int a = j % p.n, os = S_op == 2 ? (j & 1) : 0, tb = j & 1;
-    if (!mbar_wait(full + os, op_par(j), abort_flag, p.timeout_ns, p.status)) return;
-    tc_fence_after();
-    const uint8_t* sP = sbase + os * op_bytes;
-    const uint8_t* sQ = sP + p.nk_max * kMNBoxP;
-    const uint32_t idesc = idesc_bf16_f32(128, kWCols);
-    for (int kb = 0; kb < p.nk[a]; ++kb) {
-      const uint64_t ad = sw128_kmajor_desc(smem_u32(sP + kb * kMNBoxP));
-      const uint64_t bd = sw128_kmajor_desc(smem_u32(sQ + kb * kWQBox));
-#pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk)
-        mma_bf16(tmem + static_cast<uint32_t>(kWCols * tb), ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
-    }
-    mma_commit(done + tb);
-    mma_issued = j + 1;
-  };
-  const uint64_t stream_out = l2_evict_first();
-  auto issue_codes = [&](int k) {
-    const int cs = k % S_c;
-    int row0, tc;
-    tile_at(k, row0, tc);
-    uint8_t* st = sC + cs * kWCodeStage;
-    mbar_arrive_expect_tx(cfull + cs, kWCodeStage);
-    tma_load_2d_hint(st, &maps.codes, tc * 128, row0, cfull + cs, stream_out);
-    tma_load_2d_hint(st + kWCodeBox, &maps.am, tc * 4, row0, cfull + cs, stream_out);
-    codes_issued = k + 1;
-  };
-  // the requantised tile k goes out once every warp has written it
-  auto store_tile = [&](int k) {
-    const int cs = k % S_c;
-    if (!mbar_wait(cwritten + cs, static_cast<uint32_t>(k / S_c) & 1u, abort_flag, p.timeout_ns, p.status)) return;
-    int row0, tc;
-    tile_at(k, row0, tc);
-    const uint8_t* st = sC + cs * kWCodeStage;
-    tma_store_2d_hint(&maps.codes, tc * 128, row0, st, stream_out);
-    tma_store_2d_hint(&maps.am, tc * 4, row0, st + kWCodeBox, stream_out);
-    bulk_commit();
-  };
-  if (threadIdx.x == 0) {
-    for (int k = 0; k < S_c && k < ntile; ++k) issue_codes(k);
-    for (int j = 0; j < S_op && j < J; ++j) issue_op(j);
-    if (J > 0) issue_mma(0);
-  }
-
-  bool bad = false;                               // warp-uniform
-  for (int k = 0; k < ntile && !bad; ++k) {
-    const int cs = k % S_c;
-    const uint32_t st = smem_u32(sC + cs * kWCodeStage);
-    const uint32_t sw = static_cast<uint32_t>(r & 7);
-    const uint32_t a0 = st + r * 128 + (((2u * b) ^ sw) << 4), a1 = st + r * 128 + (((2u * b + 1u) ^ sw) << 4);
-    const uint32_t aam = st + kWCodeBox + r * 16 + 4 * b;
-    if (!__all_sync(0xffffffffu, mbar_wait(cfull + cs, static_cast<uint32_t>(k / S_c) & 1u, abort_flag,
-                                           p.timeout_ns, p.status))) {
-      bad = true;
-      break;
-    }
-    float u[64];
-    {
-      uint32_t cw[8];
-      lds128w(a0, cw[0], cw[1], cw[2], cw[3]);
-      lds128w(a1, cw[4], cw[5], cw[6], cw[7]);
-      float am;
-      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(am) : "r"(aam));
-      float lv[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) lv[i] = p.tab.level[i];
-      nf4_dequant_regs(cw, am, lv, u);
-    }
-    for (int a = 0; a < p.n; ++a) {
-      const int j = k * p.n + a, tb = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(done + tb, static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
-                                             p.timeout_ns, p.status))) {
-        bad = true;
-        break;
-      }
-      tc_fence_after();
-      if (threadIdx.x == 0) {
-        // operand stage of job j: MMA j (waited above) was its last reader; accumulator
-        // buffer tb ^ 1: free once every warp has read job j - 1.  A failed wait raises the
-        // abort flag, which every later wait sees.
-        if (j + S_op < J) issue_op(j + S_op);
-        if (j + 1 < J && (j == 0 || mbar_wait(empty + (tb ^ 1), static_cast<uint32_t>((j - 1) >> 1) & 1u,
-                                              abort_flag, p.timeout_ns, p.status)))
-          issue_mma(j + 1);
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + static_cast<uint32_t>(kWCols * tb + 64 * b + 32 * h), v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          u[32 * h + i] = __fmaf_rn(__uint_as_float(v[i]), p.s[a], u[32 * h + i]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty + tb);
-      if (threadIdx.x == 0 && a == 0 && !*abort_flag) {
-        // the stage of tile k - 2 (stored a tile ago) takes the codes of tile k - 2 + S_c;
-        // the requantised tile k - 1 goes out
-        if (k >= 2 && k - 2 + S_c < ntile) {
-          bulk_wait_read_0();
-          issue_codes(k - 2 + S_c);
+  if (warp == 16) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t keep = l2_evict_last(), stream_out = l2_evict_first();
+      int a_last = -1, mma_last = -1, codes_last = -1, b_last = -1, m_last = -1;   // for the drain
+      auto tile_at = [&](int k, int& row0, int& tc) {
+        row0 = ((T0 + k) / nbw) * 128;
+        tc = (T0 + k) % nbw;
+      };
+      auto load_codes = [&](int k) {
+        int row0, tc;
+        tile_at(k, row0, tc);
+        const int cs = k % S_c;
+        mbar_arrive_expect_tx(cfull + cs, kWCodeBox);
+        tma_load_2d_hint(sC + cs * kWCodeBox, &maps.codes, tc * 128, row0, cfull + cs, stream_out);
+        codes_last = k;
+      };
+      auto load_scales = [&](int k) {             // the group starting at tile k
+        int row0, tc;
+        tile_at(k, row0, tc);
+        const int gl = group_of(k), ms = gl % kWAmRing;
+        mbar_arrive_expect_tx(mfull + ms, kWAmBox);
+        tma_load_2d_hint(sM + ms * kWAmBox, &maps.am, (tc / 4) * 16, row0, mfull + ms, stream_out);
+        m_last = gl;
+      };
+      auto load_b = [&](int k) {                  // every adapter's B_p rows of the group at tile k
+        int row0, tc;
+        tile_at(k, row0, tc);
+        const int gl = group_of(k), bs = gl & 1;
+        mbar_arrive_expect_tx(bfull + bs, static_cast<uint32_t>(p.b_bytes));
+        for (int a = 0; a < p.n; ++a)
+          for (int kb = 0; kb < p.nk[a]; ++kb)
+            tma_load_2d_hint(sB + bs * p.b_bytes + (p.boff[a] + kb) * kMNBoxP, &maps.p[a], kb * kBK, row0, bfull + bs,
+                             keep);
+        b_last = gl;
+      };
+      auto load_a = [&](int j) {
+        const int k = j / p.n, a = j - k * p.n, st = j % S_a, kbox = p.kbox[a];
+        int row0, tc;
+        tile_at(k, row0, tc);
+        uint8_t* dst = sA + st * p.a_bytes;
+        mbar_arrive_expect_tx(fullA + st, static_cast<uint32_t>(p.nk[a] * 4 * kbox * 128));
+        for (int kb = 0; kb < p.nk[a]; ++kb)
+          for (int g = 0; g < 4; ++g)
+            tma_load_2d_hint(dst + (kb * 4 + g) * kbox * 128, &maps.q[a], tc * kWCols + 64 * g, kb * kbox, fullA + st,
+                             keep);
+        a_last = j;
+      };
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return mbar_wait(bar, parity, abort_flag, p.timeout_ns, p.status);
+      };
+      auto issue_mma = [&](int j) {
+        const int k = j / p.n, a = j - k * p.n, st = j % S_a, tb = j & 1, gl = group_of(k);
+        const uint8_t* bb = sB + (gl & 1) * p.b_bytes + p.boff[a] * kMNBoxP;
+        const uint8_t* ab = sA + st * p.a_bytes;
+        const int kbox = p.kbox[a];
+        const uint32_t idesc = idesc_bf16_f32_bmn(128, kWCols);
+        for (int kb = 0; kb < p.nk[a]; ++kb) {
+          const uint64_t ad = sw128_kmajor_desc(smem_u32(bb + kb * kMNBoxP));
+          for (int kk = 0; kk < kbox / 16; ++kk) {
+            const uint64_t bd = sw128_mnmajor_desc_lbo(smem_u32(ab + kb * 4 * kbox * 128 + kk * 2048), kbox * 128);
+            mma_bf16(tmem + static_cast<uint32_t>(kWCols * tb), ad + 2 * kk, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
         }
-        if (k >= 1) store_tile(k - 1);
-      }
-    }
-    if (bad) break;
-    // requantise (see merge_nf4_kernel) into the stage, in place
-    uint32_t cw[8];
-    const float m = nf4_requant_block(u, cells_addr, cw);
-    sts128(a0, cw[0], cw[1], cw[2], cw[3]);
-    sts128(a1, cw[4], cw[5], cw[6], cw[7]);
-    asm volatile("st.shared.f32 [%0], %1;" ::"r"(aam), "f"(m) : "memory");
-    fence_proxy_async_smem();                     // the TMA store reads what this thread wrote
-    __syncwarp();
-    if (lane == 0) mbar_arrive(cwritten + cs);
-  }
+        mma_commit(done + tb);
+        mma_last = j;
+      };
+      // the requantised tile k goes out once every compute warp has written it, with its
+      // group's scales after the group's last tile
+      auto store_tile = [&](int k) {
+        const int cs = k % S_c;
+        if (!wait(cwritten + cs, static_cast<uint32_t>(k / S_c) & 1u)) return;
+        int row0, tc;
+        tile_at(k, row0, tc);
+        tma_store_2d_hint(&maps.codes, tc * 128, row0, sC + cs * kWCodeBox, stream_out);
+        if (last_in_group(k))
+          tma_store_2d_hint(&maps.am, (tc / 4) * 16, row0, sM + (group_of(k) % kWAmRing) * kWAmBox, stream_out);
+        bulk_commit();
+      };
 
-  if (threadIdx.x == 0) {
-    if (!bad && !*abort_flag && ntile > 0) store_tile(ntile - 1);
-    if (*abort_flag) {
-      // after a timed-out wait: the copies and MMAs started finish before the exit
-      const uint64_t t0 = globaltimer_ns();
-      for (int k = codes_issued - S_c; k < codes_issued; ++k)
-        if (k >= 0)
-          while (!mbar_try_wait(smem_u32(cfull + k % S_c), static_cast<uint32_t>(k / S_c) & 1u) &&
-                 globaltimer_ns() - t0 < 100000000ull) {
+      if (ntile > 0) {
+        for (int k = 0; k < S_c - 3 && k < ntile; ++k) load_codes(k);
+        load_scales(0);
+        load_b(0);
+        for (int j = 0; j < S_a - 1 && j < J; ++j) load_a(j);
+      }
+      for (int k = 0; k < ntile && !*abort_flag; ++k) {
+        if (k >= 2) store_tile(k - 2);
+        const int kc = k + S_c - 3;               // the codes of tile kc into the stage of tile kc - S_c
+        if (kc < ntile) {
+          if (kc >= S_c) bulk_wait_read_le1();
+          load_codes(kc);
+        }
+        if (k + 1 < ntile && pos_of(k + 1) == 0) {
+          // the next group: its B_p buffer's last readers are the MMAs up to job k n - 1, its
+          // scale buffer's last store has been issued (three groups back)
+          if (k > 0 && !wait(done + ((k * p.n - 1) & 1), static_cast<uint32_t>((k * p.n - 1) >> 1) & 1u)) break;
+          load_b(k + 1);
+          bulk_wait_read_0();
+          load_scales(k + 1);
+        }
+        for (int a = 0; a < p.n && !*abort_flag; ++a) {
+          const int j = k * p.n + a;
+          if (j >= 2 && !wait(empty + (j & 1), static_cast<uint32_t>((j - 2) >> 1) & 1u)) break;
+          if (!wait(fullA + j % S_a, static_cast<uint32_t>(j / S_a) & 1u)) break;
+          if (a == 0 && (k == 0 || pos_of(k) == 0) &&
+              !wait(bfull + (group_of(k) & 1), static_cast<uint32_t>(group_of(k) >> 1) & 1u))
+            break;
+          tc_fence_after();
+          issue_mma(j);
+          // the A_p stage of job j - 1 takes job j + S_a - 1 once MMA j - 1 has finished
+          const int ja = j + S_a - 1;
+          if (ja < J) {
+            if (j >= 1 && !wait(done + ((j - 1) & 1), static_cast<uint32_t>((j - 1) >> 1) & 1u)) break;
+            load_a(ja);
           }
-      for (int j = op_issued - S_op; j < op_issued; ++j)
-        if (j >= 0)
-          while (!mbar_try_wait(smem_u32(full + (S_op == 2 ? (j & 1) : 0)), op_par(j)) &&
-                 globaltimer_ns() - t0 < 150000000ull) {
+        }
+      }
+      if (!*abort_flag) {
+        if (ntile >= 2) store_tile(ntile - 2);
+        if (ntile >= 1) store_tile(ntile - 1);
+      }
+      if (*abort_flag) {
+        // after a timed-out wait: the copies and MMAs started finish before the exit
+        const uint64_t t0 = globaltimer_ns();
+        auto drain = [&](uint64_t* bar, uint32_t parity) {
+          while (!mbar_try_wait(smem_u32(bar), parity) && globaltimer_ns() - t0 < 200000000ull) {
           }
-      for (int j = mma_issued - 2; j < mma_issued; ++j)
-        if (j >= 0)
-          while (!mbar_try_wait(smem_u32(done + (j & 1)), static_cast<uint32_t>(j >> 1) & 1u) &&
-                 globaltimer_ns() - t0 < 200000000ull) {
-          }
+        };
+        for (int k = max(0, codes_last - S_c + 1); k <= codes_last; ++k)
+          drain(cfull + k % S_c, static_cast<uint32_t>(k / S_c) & 1u);
+        for (int j = max(0, a_last - S_a + 1); j <= a_last; ++j) drain(fullA + j % S_a, static_cast<uint32_t>(j / S_a) & 1u);
+        for (int g = max(0, b_last - 1); g <= b_last; ++g) drain(bfull + (g & 1), static_cast<uint32_t>(g >> 1) & 1u);
+        for (int g = max(0, m_last - kWAmRing + 1); g <= m_last; ++g)
+          drain(mfull + g % kWAmRing, static_cast<uint32_t>(g / kWAmRing) & 1u);
+        for (int j = max(0, mma_last - 1); j <= mma_last; ++j) drain(done + (j & 1), static_cast<uint32_t>(j >> 1) & 1u);
+      }
+      bulk_wait_all();                            // the stores have read shared memory and landed
     }
-    bulk_wait_all();                              // the stores have read shared memory and landed
+  } else {
+    // ------------------------------------------------------------------ compute warps
+    const int r = 32 * (warp & 3) + lane;         // row within the tile
+    const int b = warp >> 2;                      // 64-column block within the tile
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t cells_addr = smem_u32(s_cells);
+    for (int k = 0; k < ntile; ++k) {
+      const int cs = k % S_c, gl = group_of(k);
+      const uint32_t st = smem_u32(sC + cs * kWCodeBox);
+      const uint32_t sw = static_cast<uint32_t>(r & 7);
+      const uint32_t a0 = st + r * 128 + (((2u * b) ^ sw) << 4), a1 = st + r * 128 + (((2u * b + 1u) ^ sw) << 4);
+      const uint32_t aam = smem_u32(sM + (gl % kWAmRing) * kWAmBox) + r * 64 + (4 * pos_of(k) + b) * 4;
+      bool ok = true;
+      if (k == 0 || pos_of(k) == 0)
+        ok = mbar_wait(mfull + gl % kWAmRing, static_cast<uint32_t>(gl / kWAmRing) & 1u, abort_flag, p.timeout_ns,
+                       p.status);
+      ok = ok && mbar_wait(cfull + cs, static_cast<uint32_t>(k / S_c) & 1u, abort_flag, p.timeout_ns, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      float u[64];
+      {
+        uint32_t cw[8];
+        lds128w(a0, cw[0], cw[1], cw[2], cw[3]);
+        lds128w(a1, cw[4], cw[5], cw[6], cw[7]);
+        float am;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(am) : "r"(aam));
+        float lv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) lv[i] = p.tab.level[i];
+        nf4_dequant_regs(cw, am, lv, u);
+      }
+      bool bad = false;
+      for (int a = 0; a < p.n; ++a) {
+        const int j = k * p.n + a, tb = j & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(done + tb, static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
+                                               p.timeout_ns, p.status))) {
+          bad = true;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + static_cast<uint32_t>(kWCols * tb + 64 * b + 32 * h), v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[32 * h + i] = __fmaf_rn(__uint_as_float(v[i]), p.s[a], u[32 * h + i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + tb);
+      }
+      if (bad) break;
+      // requantise (see merge_nf4_kernel) into the stage and the group's scales, in place
+      uint32_t cw[8];
+      const float m = nf4_requant_block(u, cells_addr, cw);
+      sts128(a0, cw[0], cw[1], cw[2], cw[3]);
+      sts128(a1, cw[4], cw[5], cw[6], cw[7]);
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(aam), "f"(m) : "memory");
+      fence_proxy_async_smem();                   // the TMA stores read what this thread wrote
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cwritten + cs);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -723,31 +777,46 @@ __global__ void __launch_bounds__(512, 1) merge_nf4_wide_kernel(const __grid_con
 
 }  // namespace
 
-bool merge_nf4_wide_plan(int nk_max, long long cols, int* s_op, int* s_c) {
-  if (cols % kWCols != 0 || nk_max < 1 || nk_max > kMergeTileMaxK) return false;
-  const long long budget = 227 * 1024 - 1024 - 128 - static_cast<long long>(kCodeCells) * 2 * sizeof(uint32_t);
-  const long long op = static_cast<long long>(nk_max) * kWOpK;
-  const int so = 2 * op + 2 * kWCodeStage <= budget ? 2 : 1;
-  const long long sc = std::min<long long>(4, (budget - so * op) / kWCodeStage);
-  if (sc < 3) return false;                      // the codes of tile k + s_c - 2 leave at tile k
-  *s_op = so;
-  *s_c = static_cast<int>(sc);
-  return true;
+bool merge_nf4_wide_plan(const int* ranks, int n, long long cols, MergeNF4Params* p) {
+  if (cols % kWCols != 0 || n < 1 || n > kMaxAd) return false;
+  int boff = 0, a_bytes = 0;
+  for (int a = 0; a < n; ++a) {
+    const int r = ranks[a];
+    if (r < 1 || r > kMergeTileMaxK * kBK) return false;
+    p->kbox[a] = std::min(kBK, (r + 15) / 16 * 16);
+    p->nk[a] = (r + p->kbox[a] - 1) / p->kbox[a];
+    p->boff[a] = boff;
+    boff += p->nk[a];
+    a_bytes = std::max(a_bytes, p->nk[a] * 4 * p->kbox[a] * 128);
+  }
+  p->b_bytes = boff * kMNBoxP;
+  p->a_bytes = a_bytes;
+  const long long budget = 227 * 1024 - 1024 - 256 - static_cast<long long>(kCodeCells) * 2 * sizeof(uint32_t);
+  const long long fixed = 2LL * p->b_bytes + static_cast<long long>(kWAmRing) * kWAmBox;
+  for (int sa = 3; sa >= 2; --sa) {
+    const long long sc = std::min<long long>(kWMaxSC, (budget - fixed - sa * static_cast<long long>(a_bytes)) / kWCodeBox);
+    if (sc >= 4) {                                 // the codes of tile k + s_c - 3 go in at tile k
+      p->s_a = sa;
+      p->s_c = static_cast<int>(sc);
+      return true;
+    }
+  }
+  return false;
 }
 
 int launch_merge_nf4(const MergeNF4Maps& maps, const MergeNF4Params& p, cudaStream_t stream) {
   if (p.rows <= 0 || p.cols <= 0 || p.n <= 0) return WP_OK;
   if (p.n > kMaxAd || p.nk_max < 1 || p.nk_max > kMergeTileMaxK || p.cols % 64 != 0) return WP_ERR_UNSUPPORTED;
   if (p.wide) {
-    if (p.cols % kWCols != 0 || p.s_op < 1 || p.s_op > 2 || p.s_c < 3 || p.s_c > 4) return WP_ERR_UNSUPPORTED;
-    const size_t smem = 1024 + static_cast<size_t>(p.s_op) * p.nk_max * kWOpK +
-                        static_cast<size_t>(p.s_c) * kWCodeStage + 128;
+    if (p.cols % kWCols != 0 || p.s_a < 2 || p.s_a > kWMaxSA || p.s_c < 4 || p.s_c > kWMaxSC) return WP_ERR_UNSUPPORTED;
+    const size_t smem = 1024 + 2 * static_cast<size_t>(p.b_bytes) + static_cast<size_t>(p.s_a) * p.a_bytes +
+                        static_cast<size_t>(p.s_c) * kWCodeBox + static_cast<size_t>(kWAmRing) * kWAmBox + 256;
     cudaError_t e = cudaFuncSetAttribute(merge_nf4_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e == cudaSuccess) {
-      const long long tiles = static_cast<long long>(p.cols / kWCols) * ((p.rows + 127) / 128);
-      const unsigned grid = static_cast<unsigned>(std::min<long long>(tiles, device_sm_count()));
-      merge_nf4_wide_kernel<<<grid, 512, smem, stream>>>(maps, p);
+      const long long groups = static_cast<long long>((p.cols / kWCols + 3) / 4) * ((p.rows + 127) / 128);
+      const unsigned grid = static_cast<unsigned>(std::min<long long>(groups, device_sm_count()));
+      merge_nf4_wide_kernel<<<grid, kWThreads, smem, stream>>>(maps, p);
       e = cudaGetLastError();
     }
     if (e != cudaSuccess) {

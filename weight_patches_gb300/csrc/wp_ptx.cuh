@@ -548,6 +548,17 @@ __device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
+// The same with the distance between 64-element chunks given (a box of fewer than 64 K rows).
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc_lbo(uint32_t smem_addr, uint32_t lbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);          // start address
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;     // LBO: next 64-element chunk
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                      // SBO: next 8-row group along K
+  d |= static_cast<uint64_t>(1) << 46;                              // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                              // 128-byte swizzle
+  return d;
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(uint32_t M, uint32_t N) {
   return idesc_bf16_f32(M, N) | (1u << 15) | (1u << 16);            // A and B MN-major
 }
