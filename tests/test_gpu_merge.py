@@ -1,14 +1,15 @@
 """LoRA merge on the GPU against the FP64 oracle (piper-offload docs, "LoRA merge" and
 "Quantized weight support").
 
-bf16 weight: the kernel rounds fl32(W) + fl32(s * acc) (fp32 accumulation of B A) to bf16,
-the oracle rounds the exact W + s B A: the two agree except where the exact value lies
-within float32 noise of a bf16 rounding boundary, so nearly every element is bit-equal and
-none is further apart than one bf16 ulp plus that float32 noise -- r accumulation roundings
-of at most 2^-24 of sum |s B_oj A_ji|, and the roundings of the product and of the sum with W
-(it matters only where W and the update cancel and the result's own ulp is tiny).  4-bit weight: the new block scales agree to float32
-accuracy, and the codes agree except where the oracle's normalised value lies within
-float32 noise of a decision midpoint (there either neighbour is valid)."""
+bf16 weight: the kernel rounds fl32(s * acc + W) (fp32 accumulation of B A, one fused
+multiply-add) to bf16, the oracle rounds the exact W + s B A: the two agree except where the
+exact value lies within float32 noise of a bf16 rounding boundary, so nearly every element is
+bit-equal and none is further apart than one bf16 ulp plus that float32 noise -- r
+accumulation roundings of at most 2^-24 of sum |s B_oj A_ji|, and the rounding of the fused
+sum with W (it matters only where W and the update cancel and the result's own ulp is tiny).
+4-bit weight: the new block scales agree to float32 accuracy, and the codes agree except where
+the oracle's normalised value lies within float32 noise of a decision midpoint (there either
+neighbour is valid)."""
 import numpy as np
 import pytest
 import torch
