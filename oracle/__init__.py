@@ -18,11 +18,13 @@ Modules
                unfused bf16 reference chain used by the accuracy gate
   swiglu       the SwiGLU activation around the LoRA MLP and its backward, and the
                whole MLP's forward and closed-form gradients
-  merge        baking adapters into a bf16 or 4-bit weight (rounded / re-encoded once)
+  merge        baking adapters into a bf16 or 4-bit weight (rounded / re-encoded once,
+               deterministically or stochastically)
+  rng          Philox4x32-10, the counter-based generator of the stochastic re-encoding
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test against
 something other than itself (brute force, closed forms, invariants, library
 special cases); none is "parity unpinned" except the claim that the NF4 codebook is
 bit-identical to the one bitsandbytes ships (see ``nf4``).
 """
-from . import numerics, nf4, dense_patch, lora, swiglu, merge  # noqa: F401
+from . import numerics, nf4, dense_patch, lora, swiglu, merge, rng  # noqa: F401
