@@ -487,13 +487,18 @@ def per_config(dev, args, peak, hbm, only=None):
                           device=dev)
         t_s = time.time()
         ms = flushed(lambda: wpg.lora_merge(W3, ads3, 1e-4, workspace=ws3))
+        seeds = iter(range(1, 1 << 20))
+        ms_st = flushed(lambda: wpg.lora_merge(W3, ads3, 1e-4, workspace=ws3, rounding_seed=next(seeds)))
         marks["c3_nf4_merge"] = (t_s, time.time())
         assert wpg.lora_device_status() == 0
         nbytes = 2 * (W3.packed.numel() + W3.absmax.numel() * 4)
         out["c3_nf4_merge"] = {"mb": round(nbytes / 1e6, 1), "ms": round(ms, 5),
                                "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bound": "hbm",
                                "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
-                               "work": "codes and scales read and written once (the adapter's 0.3 MB aside)",
+                               "stochastic": {"ms": round(ms_st, 5),
+                                              "frac": round(nbytes / (ms_st * 1e-3) / 1e9 / hbm, 4)},
+                               "work": "codes and scales read and written once (the adapter's 0.3 MB aside); "
+                                       "stochastic: the same with the Philox-sampled codes",
                                "timing": "one call after an L2 flush, launch included, median"}
         del W3, ads3, ws3
         torch.cuda.empty_cache()

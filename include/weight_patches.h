@@ -218,6 +218,23 @@ int lora_merge(const wp_mat* W, const wp_out* bias, const wp_adapter* adapters, 
                double scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * lora_merge_seeded -- lora_merge with the stochastic re-encoding of a 4-bit weight
+ * (piper-offload docs, "LoRA merge": the default for quantised merges, so that updates smaller
+ * than one quantisation step are not rounded away systematically).  The block scales are the
+ * deterministic ones (absmax' = max |u|); only each code is sampled, between the two levels
+ * around x = fl32(u / absmax'): x on a level keeps that level's code, otherwise the upper
+ * level lo < x < hi is taken when U * w < d * 2^23 (d = fl32(x - lo), w = fl32(hi - lo)), U
+ * being the element's 23-bit draw: word e % 4 of Philox4x32-10 (Salmon et al., SC 2011) of
+ * counter (e / 4 as two 32-bit words, 0, 0) under key (the seed's low and high 32 bits), shifted
+ * right by 9, e = row * in + column the element's logical index -- so the codes depend on the
+ * seed and the data only, not on the launch.  The same seed gives the same codes.  A bf16 W has
+ * no code to sample: the call is lora_merge.  Arguments, workspace and errors as lora_merge.
+ */
+int lora_merge_seeded(const wp_mat* W, const wp_out* bias, const wp_adapter* adapters, int32_t n_adapters,
+                      double scale, uint64_t rounding_seed, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/*
  * lora_swiglu_fwd -- the front half of a SwiGLU LoRA MLP in one pass: the gate and up
  * LoRA linears and the activation,
  *     e = X W_gate^T + bias_gate + s_g (X A_g^T) B_g^T,

@@ -120,6 +120,44 @@ def test_merge_nf4(rows, cols, scale, ranks):
         assert np.mean(got_codes != orig) > 0.01                # the update moved codes
 
 
+@pytest.mark.parametrize("rows,cols,scale,ranks", [
+    (256, 512, 1.0, [16]),                  # 256-column tiles
+    (200, 320, 40.0, [16]),                 # 64-column tiles
+    (384, 1024, 20.0, [16, 100, 8]),        # several adapters
+    (128, 256, 20.0, [300]),                # a rank above 256: the three-kernel route
+    (2560, 4096, 10.0, [32]),               # more tiles than SMs
+])
+def test_merge_nf4_stochastic(rows, cols, scale, ranks):
+    """The stochastic re-encoding against the oracle's, element by element: equal codes
+    wherever the oracle's decision is further than float32 noise from flipping (its slack),
+    equal scales; the same seed gives the same codes, another seed others."""
+    rng = np.random.default_rng(rows + cols + 1)
+    W0 = workloads.draw_nf4(rng, rows, cols)
+    ps = _patches(rng, ranks, rows, cols)
+    ads = [wpg.Adapter(gu.dev(p.A), gu.dev(p.B), p.alpha, p.strength) for p in ps]
+    seed = 0x9E3779B97F4A7C15 + rows
+    got = []
+    for sd in (seed, seed, seed + 1):
+        W = gu.dev(W0)
+        wpg.lora_merge(W, ads, scale, rounding_seed=sd)
+        torch.cuda.synchronize()
+        assert wpg.lora_device_status() == 0
+        got.append((onf4.unpack_codes(W.packed.cpu().numpy(), rows, cols), W.absmax.cpu().numpy()))
+    want_codes, want_am, x, slack = om.merge_nf4(W0.data, W0.absmax, rows, cols, [decode_patch(p) for p in ps],
+                                                 scale, rounding_seed=seed)
+    codes, am = got[0]
+    np.testing.assert_allclose(am, want_am, rtol=1e-5, atol=0)
+    sure = slack > 1e-5
+    assert sure.mean() > 0.99
+    assert np.array_equal(codes[sure], want_codes[sure])
+    assert np.all(np.abs(codes.astype(int) - want_codes.astype(int)) <= 1)
+    assert np.array_equal(codes, got[1][0])                    # the same seed, the same codes
+    other = om.merge_nf4(W0.data, W0.absmax, rows, cols, [decode_patch(p) for p in ps], scale,
+                         rounding_seed=seed + 1)[0]
+    moved = np.mean(want_codes != other)                       # another seed samples anew
+    assert moved > 0 and np.mean(codes != got[2][0]) > 0.5 * moved
+
+
 def test_merge_full_size_sidecar():
     """The 5120 x 5120 sidecar weight with its rank-128 patch (bf16), every element checked."""
     lin, _ = workloads.config4("full")

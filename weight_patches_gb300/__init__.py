@@ -79,6 +79,7 @@ def _load():
     lib.lora_linear_bwd.argtypes = [pm, pm, pm, I32, pa, D, po, po, po, P, SZ, P]
     lib.lora_swiglu_fwd.argtypes = [pm, pm, pm, pa, D, po, po, P, SZ, P]
     lib.lora_merge.argtypes = [pm, po, pa, I32, D, P, SZ, P]
+    lib.lora_merge_seeded.argtypes = [pm, po, pa, I32, D, ctypes.c_uint64, P, SZ, P]
     lib.lora_swiglu_bwd.argtypes = [pm, pm, po, po, P]
     lib.lora_dense_patch.argtypes = [P, I32, I64, P, I32, I64, I32, D, P]
     lib.lora_workspace_size.argtypes = [I32, pm, pm, pa, I32]
@@ -233,10 +234,11 @@ def lora_linear_fwd_grouped(X: torch.Tensor, W_stacked, bias: Optional[torch.Ten
 
 
 def lora_merge(W, adapters: Sequence[Adapter], scale: float = 1.0, workspace: Optional[torch.Tensor] = None,
-               bias: Optional[torch.Tensor] = None):
+               bias: Optional[torch.Tensor] = None, rounding_seed: Optional[int] = None):
     """Bake the adapters into W in place: W <- W + sum_p s_p B_p A_p (s_p = alpha/r * strength
-    * scale), accumulated in fp32 and rounded once; a 4-bit ``NF4Weight`` is requantised
-    (round to nearest).  Adapters with a legacy ``bias_B`` also update ``bias`` in place
+    * scale), accumulated in fp32 and rounded once; a 4-bit ``NF4Weight`` is requantised,
+    round to nearest, or with ``rounding_seed`` (an unsigned 64-bit integer) stochastically
+    (``lora_merge_seeded``).  Adapters with a legacy ``bias_B`` also update ``bias`` in place
     (bias <- bias + sum_p s_p bias_B_p, one rounding); the call fails before writing anything
     when such an adapter meets ``bias=None``.  Returns W."""
     wm, arr = _mat(W), _adapters(adapters)
@@ -250,9 +252,18 @@ def lora_merge(W, adapters: Sequence[Adapter], scale: float = 1.0, workspace: Op
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=device)
     nbytes = workspace.numel() if workspace is not None else 0
-    st = _load().lora_merge(ctypes.byref(wm), _ref(bo), arr, len(adapters), float(scale),
-                            workspace.data_ptr() if workspace is not None else None, nbytes, _stream(device))
-    _check(st, "lora_merge")
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    if rounding_seed is None:
+        st = _load().lora_merge(ctypes.byref(wm), _ref(bo), arr, len(adapters), float(scale), ws_ptr, nbytes,
+                                _stream(device))
+        _check(st, "lora_merge")
+    else:
+        seed = int(rounding_seed)
+        if not 0 <= seed < 1 << 64:
+            raise ValueError("rounding_seed must be an unsigned 64-bit integer")
+        st = _load().lora_merge_seeded(ctypes.byref(wm), _ref(bo), arr, len(adapters), float(scale), seed, ws_ptr,
+                                       nbytes, _stream(device))
+        _check(st, "lora_merge_seeded")
     return W
 
 

@@ -1547,7 +1547,7 @@ int merge_pass(const void* P, long long ldp, const void* Q, long long ldq, long 
 }
 
 int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n, double scale, void* workspace,
-               size_t ws_bytes, cudaStream_t stream) {
+               size_t ws_bytes, cudaStream_t stream, bool stochastic = false, uint64_t seed = 0) {
   if (!W || !W->data || W->rows <= 0 || W->cols <= 0) return WP_ERR_INVALID;
   if (W->dtype != WP_BF16 && W->dtype != WP_NF4) return WP_ERR_DTYPE;
   if (!std::isfinite(scale)) return WP_ERR_INVALID;
@@ -1676,7 +1676,10 @@ int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n,
     fp.codes = static_cast<uint8_t*>(wdata);
     fp.absmax = const_cast<float*>(W->absmax);
     fp.tab = tab;
-    if (!nf4_code_cells(tab, &fp.cells)) return WP_ERR_UNSUPPORTED;
+    if (!nf4_code_cells(tab, &fp.cells) || !nf4_level_cells(tab, &fp.lcells)) return WP_ERR_UNSUPPORTED;
+    fp.stochastic = stochastic ? 1 : 0;
+    fp.seed_lo = static_cast<uint32_t>(seed);
+    fp.seed_hi = static_cast<uint32_t>(seed >> 32);
     if (fp.wide) {
       rc = make_map_u8(&fm.codes, W->data, in / 2, out, in / 2, 128, 128, 128);
       if (rc == WP_OK) rc = make_map(&fm.am, WP_FP32, W->absmax, in / 64, out, in / 64, 16, 128, /*swizzle=*/0);
@@ -1687,7 +1690,8 @@ int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n,
     if (!fp.status) return record_cuda();
     rc = launch_merge_nf4(fm, fp, stream);
   } else if (nf4) {
-    rc = launch_nf4_requant(U, out * in, tab, wdata, const_cast<float*>(W->absmax), stream);
+    rc = stochastic ? launch_nf4_requant_stochastic(U, out * in, tab, wdata, const_cast<float*>(W->absmax), seed, stream)
+                    : launch_nf4_requant(U, out * in, tab, wdata, const_cast<float*>(W->absmax), stream);
   }
   if (rc == WP_OK && fold.n > 0) {
     // bias <- bias + sum_p s_p bias_B_p, rounded once to the bias's dtype
@@ -1725,6 +1729,12 @@ int lora_merge(const wp_mat* W, const wp_out* bias, const wp_adapter* adapters, 
                void* workspace, size_t workspace_bytes, void* stream) {
   return merge_impl(W, bias, adapters, n_adapters, scale, workspace, workspace_bytes,
                     static_cast<cudaStream_t>(stream));
+}
+
+int lora_merge_seeded(const wp_mat* W, const wp_out* bias, const wp_adapter* adapters, int32_t n_adapters,
+                      double scale, uint64_t rounding_seed, void* workspace, size_t workspace_bytes, void* stream) {
+  return merge_impl(W, bias, adapters, n_adapters, scale, workspace, workspace_bytes,
+                    static_cast<cudaStream_t>(stream), true, rounding_seed);
 }
 
 int lora_swiglu_fwd(const wp_mat* X, const wp_mat* W_gate_up, const wp_mat* bias,

@@ -416,6 +416,16 @@ struct NF4Cells {
   int base[kCodeCells];
 };
 bool nf4_code_cells(const NF4Table& tab, NF4Cells* cells);
+// The stochastic re-encoding's cells (same width): per cell the first level at or above its
+// start (2 when none), that level's index, the level before it (-2 when none) and the one after
+// it (2 when none).  False if a cell holds two levels (the NF4 levels are at least 0.079 apart).
+struct NF4LevelCells {
+  float next_l[kCodeCells];
+  int base[kCodeCells];
+  float prev_l[kCodeCells];
+  float after_l[kCodeCells];
+};
+bool nf4_level_cells(const NF4Table& tab, NF4LevelCells* cells);
 
 struct MergeNF4Params {
   int rows, cols;              // W [rows, cols], cols % 64 == 0
@@ -423,6 +433,9 @@ struct MergeNF4Params {
   float* absmax;               // [rows * cols / 64], rewritten
   NF4Table tab;
   NF4Cells cells;              // the code search by cells (nf4_code_cells)
+  int stochastic;              // the stochastic re-encoding, keyed by seed_lo, seed_hi
+  uint32_t seed_lo, seed_hi;
+  NF4LevelCells lcells;        // its cells (nf4_level_cells)
   int n, nk_max;               // adapters (non-zero s), the most K blocks of any of them
   int wide;                    // the 256-column form (merge_nf4_wide_plan), with its plan:
   int s_a, s_c;                //   A_p stages and code stages,
@@ -450,6 +463,9 @@ int launch_nf4_to_f32(const void* codes, const float* absmax, long long numel, c
                       cudaStream_t stream);
 int launch_nf4_requant(const float* U, long long numel, const NF4Table& tab, void* codes, float* absmax,
                        cudaStream_t stream);
+// The same with the stochastic re-encoding (U's linear index is the element's logical index).
+int launch_nf4_requant_stochastic(const float* U, long long numel, const NF4Table& tab, void* codes,
+                                  float* absmax, uint64_t seed, cudaStream_t stream);
 int launch_transpose_bf16(const void* src, long long ld_s, int R, int C, void* dst, long long ld_d,
                           cudaStream_t stream);
 

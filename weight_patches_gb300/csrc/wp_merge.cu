@@ -108,6 +108,61 @@ int launch_nf4_to_f32(const void* codes, const float* absmax, long long numel, c
   return WP_OK;
 }
 
+// The stochastic form: a thread per 64-element block (rows of U are whole blocks), the block's
+// level cells in shared memory.
+__global__ void __launch_bounds__(128) nf4_requant_stochastic_kernel(const float* U, long long nblk,
+                                                                     const __grid_constant__ NF4LevelCells lc,
+                                                                     uint8_t* codes, float* absmax, uint32_t k0,
+                                                                     uint32_t k1) {
+  __shared__ uint32_t s_l[4 * kCodeCells];
+  for (int c = threadIdx.x; c < kCodeCells; c += blockDim.x) {
+    s_l[c] = __float_as_uint(lc.next_l[c]);
+    s_l[kCodeCells + c] = static_cast<uint32_t>(lc.base[c]);
+    s_l[2 * kCodeCells + c] = __float_as_uint(lc.prev_l[c]);
+    s_l[3 * kCodeCells + c] = __float_as_uint(lc.after_l[c]);
+  }
+  __syncthreads();
+  const uint32_t cells = smem_u32(s_l);
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long bk = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; bk < nblk; bk += stride) {
+    float u[64];
+    const float4* src = reinterpret_cast<const float4*>(U + bk * 64);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float4 v = src[i];
+      u[4 * i] = v.x;
+      u[4 * i + 1] = v.y;
+      u[4 * i + 2] = v.z;
+      u[4 * i + 3] = v.w;
+    }
+    uint32_t cw[8];
+    const float m = nf4_requant_block_stochastic(u, cells, static_cast<unsigned long long>(bk) * 64, k0, k1, cw);
+    uint4* dst = reinterpret_cast<uint4*>(codes + bk * 32);
+    dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    absmax[bk] = m;
+  }
+}
+
+int launch_nf4_requant_stochastic(const float* U, long long numel, const NF4Table& tab, void* codes,
+                                  float* absmax, uint64_t seed, cudaStream_t stream) {
+  const long long nblk = numel / 64;
+  if (nblk <= 0) return WP_OK;
+  NF4LevelCells lc;
+  if (!nf4_level_cells(tab, &lc)) return WP_ERR_UNSUPPORTED;
+  long long blocks = (nblk + 127) / 128;
+  const long long cap = static_cast<long long>(device_sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  nf4_requant_stochastic_kernel<<<static_cast<unsigned>(blocks), 128, 0, stream>>>(
+      U, nblk, lc, static_cast<uint8_t*>(codes), absmax, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    return WP_ERR_CUDA;
+  }
+  return WP_OK;
+}
+
 int launch_nf4_requant(const float* U, long long numel, const NF4Table& tab, void* codes, float* absmax,
                        cudaStream_t stream) {
   const long long n8 = numel / 8;
@@ -142,6 +197,25 @@ bool nf4_code_cells(const NF4Table& tab, NF4Cells* cells) {
     if (base + 1 < 15 && mid[base + 1] < hi) return false;
     cells->base[c] = base;
     cells->next_mid[c] = base < 15 ? mid[base] : 2.0f;
+  }
+  return true;
+}
+
+// The stochastic re-encoding's cells (the same 33 cells): the first level at or above a cell's
+// start, its index, the level before it and the level after it.  False if a cell holds two
+// levels.
+bool nf4_level_cells(const NF4Table& tab, NF4LevelCells* cells) {
+  for (int k = 0; k + 1 < 16; ++k)
+    if (!(tab.level[k] < tab.level[k + 1])) return false;
+  for (int c = 0; c < kCodeCells; ++c) {
+    const float lo = -1.0f + static_cast<float>(c) / 16.0f, hi = lo + 1.0f / 16.0f;
+    int base = 0;
+    while (base < 16 && tab.level[base] < lo) ++base;
+    if (base + 1 < 16 && tab.level[base + 1] < hi) return false;
+    cells->base[c] = base;
+    cells->next_l[c] = base < 16 ? tab.level[base] : 2.0f;
+    cells->prev_l[c] = base > 0 ? tab.level[base - 1] : -2.0f;
+    cells->after_l[c] = base + 1 < 16 ? tab.level[base + 1] : 2.0f;
   }
   return true;
 }

@@ -280,6 +280,20 @@ namespace {
 constexpr int kMNBoxP = 128 * kBK * 2;            // 128 B_p rows x 64 K: 16 KiB
 constexpr int kMNBoxQ = 64 * kBK * 2;             // 64 A_p^T rows x 64 K: 8 KiB
 
+// The cell tables in shared memory: the code search (next midpoints, base codes), then the
+// stochastic re-encoding's level cells (next level, its index, the level before, the level
+// after), kCodeCells words each.
+constexpr int kCellWords = 6 * kCodeCells;
+constexpr size_t kCellBytes = kCellWords * sizeof(uint32_t);
+__device__ __forceinline__ void fill_cells(uint32_t* t, int c, const MergeNF4Params& p) {
+  t[c] = __float_as_uint(p.cells.next_mid[c]);
+  t[kCodeCells + c] = static_cast<uint32_t>(p.cells.base[c]);
+  t[2 * kCodeCells + c] = __float_as_uint(p.lcells.next_l[c]);
+  t[3 * kCodeCells + c] = static_cast<uint32_t>(p.lcells.base[c]);
+  t[4 * kCodeCells + c] = __float_as_uint(p.lcells.prev_l[c]);
+  t[5 * kCodeCells + c] = __float_as_uint(p.lcells.after_l[c]);
+}
+
 // Persistent: a CTA takes the 128-row x 64-column tiles blockIdx.x, + gridDim.x, ... (row tile
 // major, so the CTAs resident at one time share B_p's rows and sweep A_p^T's), and within a
 // tile the adapters in call order.  Each (tile, adapter) job has an operand stage and a
@@ -289,6 +303,7 @@ constexpr int kMNBoxQ = 64 * kBK * 2;             // 64 A_p^T rows x 64 K: 8 KiB
 // between its share of the arithmetic.  The warps never wait for one another: a warp that has
 // read its lanes of a buffer arrives on the buffer's "empty" barrier, and thread 0 waits there
 // before the MMAs that overwrite it.
+template <bool kStoch>
 __global__ void __launch_bounds__(128, 4) merge_nf4_kernel(const __grid_constant__ MergeNF4Maps maps,
                                                            const __grid_constant__ MergeNF4Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -300,7 +315,7 @@ __global__ void __launch_bounds__(128, 4) merge_nf4_kernel(const __grid_constant
   uint64_t* empty = full + 4;                     // [2] every warp has read a buffer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 6);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  __shared__ uint32_t s_cells[2 * kCodeCells];    // the code search by cells: next midpoints, base codes
+  __shared__ uint32_t s_cells[kCellWords];        // the code search by cells, then the level cells
 
   const int warp = threadIdx.x >> 5;
   const int nb = p.cols / 64;                     // column blocks
@@ -309,7 +324,7 @@ __global__ void __launch_bounds__(128, 4) merge_nf4_kernel(const __grid_constant
   const int J = ntile * p.n;                      // this CTA's jobs
   const long long cb = static_cast<long long>(p.cols) / 64;     // blocks per row
   for (int c = threadIdx.x; c < kCodeCells; c += blockDim.x)
-    s_cells[c] = __float_as_uint(p.cells.next_mid[c]), s_cells[kCodeCells + c] = static_cast<uint32_t>(p.cells.base[c]);
+    fill_cells(s_cells, c, p);
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(full + i, 1);
@@ -441,8 +456,10 @@ __global__ void __launch_bounds__(128, 4) merge_nf4_kernel(const __grid_constant
       // requantise: absmax' = max |u|, x = fl32(u / absmax'), code = the number of level
       // midpoints x exceeds; an all-zero block keeps scale 0 and level 0's code
       uint32_t cw[8];
-      const float m = nf4_requant_block(u, cells_addr, cw);
-      uint4* dst = reinterpret_cast<uint4*>(p.codes + (static_cast<long long>(row) * p.cols + blk * 64) / 2);
+      const long long e0 = static_cast<long long>(row) * p.cols + blk * 64;
+      const float m = kStoch ? nf4_requant_block_stochastic(u, cells_addr + 8 * kCodeCells, e0, p.seed_lo, p.seed_hi, cw)
+                             : nf4_requant_block(u, cells_addr, cw);
+      uint4* dst = reinterpret_cast<uint4*>(p.codes + e0 / 2);
       dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
       dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
       p.absmax[static_cast<long long>(row) * cb + blk] = m;
@@ -507,6 +524,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+template <bool kStoch>
 __global__ void __launch_bounds__(kWThreads, 1) merge_nf4_wide_kernel(const __grid_constant__ MergeNF4Maps maps,
                                                                       const __grid_constant__ MergeNF4Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -526,7 +544,7 @@ __global__ void __launch_bounds__(kWThreads, 1) merge_nf4_wide_kernel(const __gr
   uint64_t* mfull = bfull + 2;                    // [3] a group's scales landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mfull + kWAmRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  __shared__ uint32_t s_cells[2 * kCodeCells];    // the code search by cells: next midpoints, base codes
+  __shared__ uint32_t s_cells[kCellWords];        // the code search by cells, then the level cells
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nbw = p.cols / kWCols, ngc = (nbw + 3) / 4, nrt = (p.rows + 127) / 128;
@@ -541,7 +559,7 @@ __global__ void __launch_bounds__(kWThreads, 1) merge_nf4_wide_kernel(const __gr
   auto last_in_group = [&](int k) { const int tc = (T0 + k) % nbw; return (tc & 3) == 3 || tc == nbw - 1; };
 
   for (int c = threadIdx.x; c < kCodeCells; c += blockDim.x)
-    s_cells[c] = __float_as_uint(p.cells.next_mid[c]), s_cells[kCodeCells + c] = static_cast<uint32_t>(p.cells.base[c]);
+    fill_cells(s_cells, c, p);
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWMaxSA; ++i) mbar_init(fullA + i, 1);
     for (int i = 0; i < 2; ++i) {
@@ -758,7 +776,14 @@ __global__ void __launch_bounds__(kWThreads, 1) merge_nf4_wide_kernel(const __gr
       if (bad) break;
       // requantise (see merge_nf4_kernel) into the stage and the group's scales, in place
       uint32_t cw[8];
-      const float m = nf4_requant_block(u, cells_addr, cw);
+      float m;
+      if (kStoch) {
+        const int t = T0 + k;
+        const long long e0 = static_cast<long long>((t / nbw) * 128 + r) * p.cols + (t % nbw) * kWCols + 64 * b;
+        m = nf4_requant_block_stochastic(u, cells_addr + 8 * kCodeCells, e0, p.seed_lo, p.seed_hi, cw);
+      } else {
+        m = nf4_requant_block(u, cells_addr, cw);
+      }
       sts128(a0, cw[0], cw[1], cw[2], cw[3]);
       sts128(a1, cw[4], cw[5], cw[6], cw[7]);
       asm volatile("st.shared.f32 [%0], %1;" ::"r"(aam), "f"(m) : "memory");
@@ -791,7 +816,7 @@ bool merge_nf4_wide_plan(const int* ranks, int n, long long cols, MergeNF4Params
   }
   p->b_bytes = boff * kMNBoxP;
   p->a_bytes = a_bytes;
-  const long long budget = 227 * 1024 - 1024 - 256 - static_cast<long long>(kCodeCells) * 2 * sizeof(uint32_t);
+  const long long budget = 227 * 1024 - 1024 - 256 - static_cast<long long>(kCellBytes);
   const long long fixed = 2LL * p->b_bytes + static_cast<long long>(kWAmRing) * kWAmBox;
   for (int sa = 3; sa >= 2; --sa) {
     const long long sc = std::min<long long>(kWMaxSC, (budget - fixed - sa * static_cast<long long>(a_bytes)) / kWCodeBox);
@@ -811,12 +836,12 @@ int launch_merge_nf4(const MergeNF4Maps& maps, const MergeNF4Params& p, cudaStre
     if (p.cols % kWCols != 0 || p.s_a < 2 || p.s_a > kWMaxSA || p.s_c < 4 || p.s_c > kWMaxSC) return WP_ERR_UNSUPPORTED;
     const size_t smem = 1024 + 2 * static_cast<size_t>(p.b_bytes) + static_cast<size_t>(p.s_a) * p.a_bytes +
                         static_cast<size_t>(p.s_c) * kWCodeBox + static_cast<size_t>(kWAmRing) * kWAmBox + 256;
-    cudaError_t e = cudaFuncSetAttribute(merge_nf4_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    auto kernel = p.stochastic ? merge_nf4_wide_kernel<true> : merge_nf4_wide_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e == cudaSuccess) {
       const long long groups = static_cast<long long>((p.cols / kWCols + 3) / 4) * ((p.rows + 127) / 128);
       const unsigned grid = static_cast<unsigned>(std::min<long long>(groups, device_sm_count()));
-      merge_nf4_wide_kernel<<<grid, kWThreads, smem, stream>>>(maps, p);
+      kernel<<<grid, kWThreads, smem, stream>>>(maps, p);
       e = cudaGetLastError();
     }
     if (e != cudaSuccess) {
@@ -828,23 +853,22 @@ int launch_merge_nf4(const MergeNF4Maps& maps, const MergeNF4Params& p, cudaStre
   size_t smem = 1024 + 2 * static_cast<size_t>(p.nk_max) * (kMNBoxP + kMNBoxQ) + 64;
   // at most 4 CTAs per SM: their 4 x 128 tensor-memory columns fill the SM's 512, and a fifth
   // CTA's allocation would wait for a persistent CTA to leave
-  const size_t floor = 228 * 1024 / 4 - 1024 - kCodeCells * 2 * sizeof(uint32_t) - 16;
+  const size_t floor = 228 * 1024 / 4 - 1024 - kCellBytes - 16;
   if (smem < floor) smem = floor;
-  cudaError_t e = cudaFuncSetAttribute(merge_nf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  auto kernel = p.stochastic ? merge_nf4_kernel<true> : merge_nf4_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   // the whole shared-memory carveout, so that the CTAs the padding allows do fit
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(merge_nf4_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess) {
     // CTAs per SM: the shared memory's count (each CTA also holds the static cell table and
     // the 1 KiB the driver reserves), at most 4; 128 threads x 128 registers allow 4 as well
-    const size_t per_cta = smem + kCodeCells * 2 * sizeof(uint32_t) + 16 + 1024;
+    const size_t per_cta = smem + kCellBytes + 16 + 1024;
     const int per_sm = static_cast<int>(std::min<size_t>(4, 228 * 1024 / per_cta));
     const long long tiles = static_cast<long long>(p.cols / 64) * ((p.rows + 127) / 128);
     const long long cap = static_cast<long long>(device_sm_count()) * std::max(1, per_sm);
     const unsigned grid = static_cast<unsigned>(std::min(tiles, cap));
-    merge_nf4_kernel<<<grid, 128, smem, stream>>>(maps, p);
+    kernel<<<grid, 128, smem, stream>>>(maps, p);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) {

@@ -210,6 +210,101 @@ __device__ __forceinline__ float nf4_requant_block(const float (&u)[64], uint32_
   return m;
 }
 
+// ---------------------------------------------------------------- stochastic re-encoding
+// Philox4x32-10 (J. K. Salmon, M. A. Moraes, R. O. Dror, D. E. Shaw, "Parallel random numbers:
+// as easy as 1, 2, 3", SC 2011): ten rounds of (c0, c1, c2, c3) <- (hi(M1 c2) ^ c1 ^ k0,
+// lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)) with the key advanced by the two Weyl
+// constants between rounds.
+__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    if (i > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c[0]), lo0 = 0xD2511F53u * c[0];
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c[2]), lo1 = 0xCD9E8D57u * c[2];
+    const uint32_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+  }
+}
+
+// The stochastic code of x in [-1, 1] with the element's draw U (23 bits), by the level cells
+// of nf4_level_cells at cells_addr: four word arrays of kCodeCells (the first level at or
+// above the cell's start, its index, the level before it and the level after it).  x equal
+// to a level keeps that level's code; otherwise, between its neighbours lo < x < hi, the
+// upper code when U w < d 2^23 (d = fl32(x - lo), w = fl32(hi - lo)); the fused multiply-add
+// below has the sign of U w - d 2^23 exactly, both products being exact.  A NaN x takes code 0.
+template <bool kClamp>
+__device__ __forceinline__ uint32_t nf4_code_stochastic(float x, uint32_t U, uint32_t cells_addr) {
+  const uint32_t bits = __float_as_uint(__fmaf_rd(x, 16.0f, 8388624.0f));
+  uint32_t c = bits - 0x4B000000u;
+  if (kClamp) c = c < static_cast<uint32_t>(kCodeCells) ? c : 0u;
+  const uint32_t addr = cells_addr + 4u * c;
+  float next_l, prev_l, after_l;
+  uint32_t base;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(next_l) : "r"(addr));
+  asm volatile("ld.shared.u32 %0, [%1+%2];" : "=r"(base) : "r"(addr), "n"(4 * kCodeCells));
+  asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(prev_l) : "r"(addr), "n"(8 * kCodeCells));
+  asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(after_l) : "r"(addr), "n"(12 * kCodeCells));
+  const bool gt = x > next_l;
+  const float lo = gt ? next_l : prev_l, hi = gt ? after_l : next_l;
+  const float d = __fsub_rn(x, lo), w = __fsub_rn(hi, lo);
+  const float uf = __fsub_rn(__uint_as_float(0x4B000000u | U), 8388608.0f);      // U exactly
+  const bool up = __fmaf_rn(uf, w, -__fmul_rn(d, 8388608.0f)) < 0.f;
+  uint32_t code = x == next_l ? base : base + (gt ? 1u : 0u) + (up ? 1u : 0u) - 1u;
+  if (kClamp && x != x) code = 0u;
+  return code;
+}
+
+// The stochastic requantisation of a block whose first element has logical index e0 (a
+// multiple of 4): absmax' and x exactly as nf4_requant_block, then each code sampled with
+// the element's Philox draw (counter = e / 4, word e % 4, key = the seed's two words).
+__device__ __forceinline__ float nf4_requant_block_stochastic(const float (&u)[64], uint32_t cells_addr,
+                                                              unsigned long long e0, uint32_t k0, uint32_t k1,
+                                                              uint32_t (&cw)[8]) {
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) m = fmax_nan(m, fabsf(u[i]));
+  const bool nan_in = m != m;
+  if (nan_in) {
+    m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(u[i]));
+  }
+  if (!(m > 0.f)) {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) cw[w] = 0x77777777u;
+    return m;
+  }
+  const float y = nan_in ? 0.f : scale_reciprocal(m);
+  const unsigned long long q0 = e0 >> 2;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    uint32_t c4 = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {                 // four elements per Philox call
+      const unsigned long long q = q0 + 2 * w + h;
+      uint32_t r[4] = {static_cast<uint32_t>(q), static_cast<uint32_t>(q >> 32), 0u, 0u};
+      philox4x32_10(r, k0, k1);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = 4 * h + j;                  // element 8 w + i
+        const float v = u[8 * w + i];
+        const float x = y != 0.f ? div_by_scale(v, m, y) : __fdiv_rn(v, m);
+        const uint32_t code = y != 0.f ? nf4_code_stochastic<false>(x, r[j] >> 9, cells_addr)
+                                       : nf4_code_stochastic<true>(x, r[j] >> 9, cells_addr);
+        c4 += code << (8 * (i >> 1) + ((i & 1) ? 0 : 4));
+      }
+    }
+    cw[w] = c4;
+  }
+  return m;
+}
+
 // The 4-bit code of x = u / absmax' (the nearest level): the number of level midpoints
 // mid[k] = fl32((level[k] + level[k+1]) / 2) below x, a value on a midpoint taking the lower
 // code; found by binary search over the increasing midpoints (four comparisons).
