@@ -30,6 +30,9 @@
  *     the legacy default stream).  Inputs are never written.
  *   - Return value: WP_OK (0) or a negative WP_ERR_* code.  Argument checks run on
  *     the host before anything is launched; a rejected call launches nothing.
+ *   - An empty batch (a matrix of zero rows: T = 0 tokens) is legal and its pointers may
+ *     be null; such a call writes nothing, except lora_linear_bwd, whose dA and dB are
+ *     then sums over no tokens and are set to zero.
  *   - A kernel whose bounded wait expires records WP_ERR_TIMEOUT in a device status
  *     word instead of hanging; read it with lora_device_status() after the stream has
  *     been synchronised.  The word is sticky until reset: while it reads WP_ERR_TIMEOUT,

@@ -113,11 +113,13 @@ int make_map_bf16(CUtensorMap* m, const void* ptr, long long inner, long long ou
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A matrix of no rows needs no memory: its pointers may be null (an empty batch).
 bool valid_input(const wp_mat* m, bool allow_nf4) {
-  if (!m || !m->data) return false;
+  if (!m) return false;
   if (m->rows < 0 || m->cols <= 0) return false;
+  if (!m->data && m->rows != 0) return false;
   if (m->dtype == WP_NF4) {
-    if (!allow_nf4 || !m->absmax) return false;
+    if (!allow_nf4 || (!m->absmax && m->rows != 0)) return false;
     return true;
   }
   if (m->dtype != WP_BF16 && m->dtype != WP_FP32) return false;
@@ -125,7 +127,7 @@ bool valid_input(const wp_mat* m, bool allow_nf4) {
 }
 
 bool valid_output(const wp_out* y) {
-  if (!y || !y->data) return false;
+  if (!y || (!y->data && y->rows != 0)) return false;
   if (y->dtype != WP_BF16 && y->dtype != WP_FP32) return false;
   return y->rows >= 0 && y->cols > 0 && y->ld >= y->cols;
 }
@@ -1024,7 +1026,17 @@ int bwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int G, const wp
   if (!bwd_layout(X, W, ad, G, &L)) return WP_ERR_INVALID;
   if (!workspace || ws_bytes < L.total) return WP_ERR_WORKSPACE;
   if (!aligned16(workspace)) return WP_ERR_ALIGN;
-  if (T == 0) return WP_OK;
+  if (T == 0) {
+    // no tokens: dA and dB are sums over nothing
+    for (int g = 0; g < G; ++g) {
+      for (const wp_out* o : {&dA[g], &dB[g]}) {
+        const cudaError_t e = cudaMemset2DAsync(o->data, static_cast<size_t>(o->ld) * 4, 0,
+                                                static_cast<size_t>(o->cols) * 4, o->rows, stream);
+        if (e != cudaSuccess) return record_cuda();
+      }
+    }
+    return WP_OK;
+  }
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* Gs = reinterpret_cast<float*>(ws + L.gs);
@@ -1748,7 +1760,8 @@ int lora_swiglu_fwd(const wp_mat* X, const wp_mat* W_gate_up, const wp_mat* bias
 int lora_swiglu_bwd(const wp_mat* dH, const wp_mat* EG, const wp_out* dEG, const wp_out* H,
                     void* stream) {
   if (!dH || !EG || !dEG) return WP_ERR_INVALID;
-  if (!dH->data || !EG->data || !dEG->data || (H && !H->data)) return WP_ERR_INVALID;
+  const bool none = dH->rows == 0;                 // an empty batch needs no memory
+  if (!none && (!dH->data || !EG->data || !dEG->data || (H && !H->data))) return WP_ERR_INVALID;
   if (dH->dtype != WP_BF16 || EG->dtype != WP_BF16 || dEG->dtype != WP_BF16 ||
       (H && H->dtype != WP_BF16))
     return WP_ERR_DTYPE;
@@ -1781,7 +1794,7 @@ int lora_linear_bwd(const wp_mat* X, const wp_mat* W, const wp_mat* dY, int32_t 
 int lora_dense_patch(void* param, int32_t param_dtype, int64_t param_numel, const void* payload,
                      int32_t payload_dtype, int64_t payload_numel, int32_t kind, double strength,
                      void* stream) {
-  if (!param || !payload) return WP_ERR_INVALID;
+  if ((!param || !payload) && param_numel != 0) return WP_ERR_INVALID;
   if (kind != WP_PATCH_ADD && kind != WP_PATCH_SET) return WP_ERR_INVALID;
   if (!std::isfinite(strength)) return WP_ERR_INVALID;
   if ((param_dtype != WP_BF16 && param_dtype != WP_FP32) ||
