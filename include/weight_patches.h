@@ -395,9 +395,11 @@ int lora_set_wait_limit(uint64_t timeout_ns);
 
 /* Test hook for the timeout path (not in the pages): while `on` is non-zero, the tiles of
  * every fused forward launched afterwards wait for one more release of their row-block flag
- * than any rank item gives, so that bounded wait runs out (after lora_set_wait_limit's
- * limit) and the call's outputs are left undefined; lora_device_status() then reads
- * WP_ERR_TIMEOUT.  Process-wide; 0 restores normal operation.  Always returns WP_OK. */
+ * than any rank item gives, and every one-pass 4-bit merge (ranks up to 256) leaves the MMAs
+ * of its CTAs' last jobs unissued, so those bounded waits run out (after
+ * lora_set_wait_limit's limit) and the call's outputs are left undefined;
+ * lora_device_status() then reads WP_ERR_TIMEOUT.  Process-wide; 0 restores normal
+ * operation.  Always returns WP_OK. */
 int lora_debug_hold_flags(int32_t on);
 
 /* The library's 16 NormalFloat levels in ascending order (host memory, fp32). */

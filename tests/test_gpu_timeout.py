@@ -43,6 +43,47 @@ def test_flag_wait_runs_out_and_the_device_stays_usable():
     assert wpg.lora_device_status() == 0
 
 
+@pytest.mark.parametrize("cols", [512, 320])      # the 256-column and the 64-column one-pass merge
+def test_merge_wait_runs_out_and_the_device_stays_usable(cols):
+    """The one-pass 4-bit merge under the same hook: its CTAs' last MMAs are never issued, so
+    the compute warps' bounded waits for them expire; every warp (and the producer) leaves,
+    the copies and MMAs in flight are waited for, tensor memory is freed.  Then a normal merge
+    on the same device matches the oracle."""
+    import numpy as np
+    from oracle import merge as om
+    from oracle import nf4 as onf4
+    from oracle.lora import decode_patch
+    rng = np.random.default_rng(cols)
+    rows = 256
+    W0 = workloads.draw_nf4(rng, rows, cols)
+    p = workloads.Patch(workloads.draw(rng, 16, cols, 0.05), workloads.draw(rng, rows, 16, 0.05), 16.0, 1.0)
+    ads = [wpg.Adapter(gu.dev(p.A), gu.dev(p.B), p.alpha, p.strength)]
+    lib = wpg.lib()
+    assert wpg.lora_device_status(reset=True) in (0, -7)
+    wpg.lora_set_wait_limit(50_000_000)
+    lib.lora_debug_hold_flags(1)
+    try:
+        t0 = time.time()
+        wpg.lora_merge(gu.dev(W0), ads, 1.0)
+        torch.cuda.synchronize()
+        elapsed = time.time() - t0
+        assert wpg.lora_device_status(reset=True) == -7
+    finally:
+        lib.lora_debug_hold_flags(0)
+        wpg.lora_set_wait_limit(2_000_000_000)
+    assert elapsed < 30.0, elapsed
+    W = gu.dev(W0)
+    wpg.lora_merge(W, ads, 1.0)
+    torch.cuda.synchronize()
+    assert wpg.lora_device_status() == 0
+    want_codes, want_am, x = om.merge_nf4(W0.data, W0.absmax, rows, cols, [decode_patch(p)], 1.0)
+    got = onf4.unpack_codes(W.packed.cpu().numpy(), rows, cols)
+    np.testing.assert_allclose(W.absmax.cpu().numpy(), want_am, rtol=1e-5, atol=0)
+    lv = onf4.codebook_f64()
+    near = np.min(np.abs(x[..., None].astype(np.float64) - (lv[:-1] + lv[1:]) / 2), axis=-1) <= 1e-5
+    assert np.array_equal(got[~near], want_codes[~near])
+
+
 def test_wait_limit_range_is_checked():
     with pytest.raises(wpg.WeightPatchesError):
         wpg.lora_set_wait_limit(10)                              # below 1 ms

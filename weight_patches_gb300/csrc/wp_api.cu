@@ -23,8 +23,8 @@ namespace {
 thread_local std::string g_last_error;
 
 // How long a bounded device wait spins before its kernel gives up (lora_set_wait_limit), and
-// the test hook that holds the fused forward's row-block flags one release short
-// (lora_debug_hold_flags).
+// the test hook that holds the fused forward's row-block flags one release short and keeps
+// the one-pass 4-bit merge's last MMAs back (lora_debug_hold_flags).
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_hold_flags{0};
 unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
@@ -1690,6 +1690,7 @@ int merge_impl(const wp_mat* W, const wp_out* bias, const wp_adapter* ad, int n,
     fp.tab = tab;
     if (!nf4_code_cells(tab, &fp.cells) || !nf4_level_cells(tab, &fp.lcells)) return WP_ERR_UNSUPPORTED;
     fp.stochastic = stochastic ? 1 : 0;
+    fp.hold = g_hold_flags.load() ? 1 : 0;
     fp.seed_lo = static_cast<uint32_t>(seed);
     fp.seed_hi = static_cast<uint32_t>(seed >> 32);
     if (fp.wide) {

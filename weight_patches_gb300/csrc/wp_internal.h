@@ -433,6 +433,7 @@ struct MergeNF4Params {
   float* absmax;               // [rows * cols / 64], rewritten
   NF4Table tab;
   NF4Cells cells;              // the code search by cells (nf4_code_cells)
+  int hold;                    // test hook (lora_debug_hold_flags): the last job's MMAs are not issued
   int stochastic;              // the stochastic re-encoding, keyed by seed_lo, seed_hi
   uint32_t seed_lo, seed_hi;
   NF4LevelCells lcells;        // its cells (nf4_level_cells)

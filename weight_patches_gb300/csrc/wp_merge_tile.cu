@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(128, 4) merge_nf4_kernel(const __grid_constant
   if (threadIdx.x == 0) {
     if (J > 0) issue_tma(0);
     if (J > 1) issue_tma(1);
-    if (J > 0) issue_mma(0);
+    if (J > 0 && !(p.hold && J == 1)) issue_mma(0);   // hold: the last job's MMAs never come
   }
 
   // this thread's row of a tile: its 64-element block, 32 code bytes and a scale
@@ -446,8 +446,10 @@ __global__ void __launch_bounds__(128, 4) merge_nf4_kernel(const __grid_constant
         // job j - 1 once its empty phase completes.  A failed wait raises the abort flag, which
         // every later wait sees.
         if (j + 2 < J) issue_tma(j + 2);
-        if (j + 1 < J && (j == 0 || mbar_wait(empty + (st ^ 1), static_cast<uint32_t>((j - 1) >> 1) & 1u,
-                                              abort_flag, p.timeout_ns, p.status)))
+        // (hold: the last job's MMAs never come)
+        if (j + 1 < J && !(p.hold && j + 1 == J - 1) &&
+            (j == 0 ||
+             mbar_wait(empty + (st ^ 1), static_cast<uint32_t>((j - 1) >> 1) & 1u, abort_flag, p.timeout_ns, p.status)))
           issue_mma(j + 1);
       }
     }
@@ -693,7 +695,7 @@ __global__ void __launch_bounds__(kWThreads, 1) merge_nf4_wide_kernel(const __gr
               !wait(bfull + (group_of(k) & 1), static_cast<uint32_t>(group_of(k) >> 1) & 1u))
             break;
           tc_fence_after();
-          issue_mma(j);
+          if (!(p.hold && j == J - 1)) issue_mma(j);   // hold: the last job's MMAs never come
           // the A_p stage of job j - 1 takes job j + S_a - 1 once MMA j - 1 has finished
           const int ja = j + S_a - 1;
           if (ja < J) {
