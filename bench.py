@@ -293,8 +293,8 @@ def run_fused(args):
 
 # ----------------------------------------------------------------------- other workloads
 CASES = ("c0_tiny_fp32", "f32_layer", "wan_qkv_rank128", "c2_ffn_up", "c2_ffn_down", "c3_nf4_gate_up_fwd",
-         "c3_nf4_down_fwd", "c3_nf4_gate_up_bwd", "c3_nf4_down_bwd", "c3_swiglu_bwd", "c3_nf4_merge", "c4_sidecar",
-         "c4_set_weight")
+         "c3_nf4_down_fwd", "c3_nf4_gate_up_bwd", "c3_nf4_down_bwd", "c3_swiglu_bwd", "c3_nf4_merge",
+         "c3_nf4_gate_up_t1", "c3_nf4_gate_up_t16", "c4_sidecar", "c4_set_weight")
 
 
 def per_config(dev, args, peak, hbm, only=None):
@@ -501,6 +501,31 @@ def per_config(dev, args, peak, hbm, only=None):
                                        "stochastic: the same with the Philox-sampled codes",
                                "timing": "one call after an L2 flush, launch included, median"}
         del W3, ads3, ws3
+        torch.cuda.empty_cache()
+    for name, T_few in (("c3_nf4_gate_up_t1", 1), ("c3_nf4_gate_up_t16", 16)):
+        if not want(name):
+            continue
+        # a few tokens through the 4-bit gate/up layer: the weight-streaming paths (the CUDA-core
+        # GEMV up to 4 tokens, the tensor-core small-token kernel above); bound by reading the
+        # 4-bit weight once
+        g3 = workloads.config3("full")[0]
+        lf = workloads.Linear(g3.name, g3.X.slice_rows(0, T_few), g3.W, g3.bias, g3.patches, g3.request_scale,
+                              g3.groups)
+        Xf, Wf, adsf = d(lf.X), d(lf.W), ads_of(lf)
+        Yf = torch.empty(T_few, lf.W.rows, dtype=torch.bfloat16, device=dev)
+        wsf = torch.empty(max(1, wpg.lora_workspace_size(wpg.WP_OP_FWD_GROUPED, Xf, Wf, adsf)), dtype=torch.uint8,
+                          device=dev)
+        t_s = time.time()
+        ms = flushed(lambda: wpg.lora_linear_fwd_grouped(Xf, Wf, None, adsf, lf.request_scale, out=Yf, workspace=wsf))
+        marks[name] = (t_s, time.time())
+        assert wpg.lora_device_status() == 0
+        nbytes = Wf.packed.numel() + Wf.absmax.numel() * 4
+        out[name] = {"tokens": T_few, "mb": round(nbytes / 1e6, 1), "ms": round(ms, 5),
+                     "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bound": "hbm",
+                     "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
+                     "work": "the 4-bit weight (codes and scales) read once; the call's kernels and launches",
+                     "timing": "one call after an L2 flush, launch included, median"}
+        del Xf, Wf, adsf, Yf, wsf
         torch.cuda.empty_cache()
     if want("c4_sidecar") or want("c4_set_weight"):
         lin4, payload = workloads.config4("full")
