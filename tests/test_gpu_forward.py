@@ -258,6 +258,28 @@ def test_c4_full_sampled_rows():
     _gate(*gu.errors(lin, Y, rows))
 
 
+def test_c4_fp32_adapter_full_sampled_rows():
+    """The FP32 adapter of C4 at full size (T = 8192, 5120 -> 5120, rank 16, fp32 A and B on
+    bf16 activations; three bf16 pieces on the tensor cores): fp32 output, with and without the
+    base weight, on sampled rows against the FP64 definition -- the same 1e-5 gate as the small
+    case, and every element within its bound."""
+    lin, _ = workloads.config4("full")
+    lin.patches = lin.patches[:1]
+    rows = workloads.sample_rows(lin.T, 64)
+    Y = gu.run_fwd(lin, out_dtype=torch.float32)
+    want = olora.reference_output(lin, rows)
+    got = gu.to_f64(Y)[rows]
+    assert relative_rms(got, want) <= FP32_TOL
+    gu.assert_elementwise(got, want, gu.fwd_bound(lin, rows, out_f32=True, y_ref=want), "fp32 adapter, full size")
+    Yd = gu.run_fwd(lin, out_dtype=torch.float32, with_base=False)
+    X, _, _, patches = olora.decode_linear(lin, rows)
+    want = olora.linear_fwd(X, None, None, patches, lin.request_scale, out_features=lin.out_features)
+    got = gu.to_f64(Yd)[rows]
+    assert relative_rms(got, want) <= FP32_TOL
+    gu.assert_elementwise(got, want, gu.fwd_bound(lin, rows, out_f32=True, y_ref=want, with_base=False),
+                          "fp32 adapter, full size, delta only")
+
+
 def test_wan_rank128_full_sampled_rows():
     """The sglang PR's Wan2.1 1.3B 480p Speed Tests shape: T = 32760, 1536 -> 3 x 1536, rank
     128 per group."""
