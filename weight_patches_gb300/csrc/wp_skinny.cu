@@ -415,10 +415,49 @@ __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
 constexpr int kReduceT = 16;
 constexpr int kMaxSplits = 8;                 // partial sums loaded together per round
 
+// sum_k p[k * stride] for k = 0 .. n - 1, added in k order from 0.  The loads go out
+// kMaxSplits at a time with no condition between them (an index past the end reads the last
+// split again and is not added), so they overlap instead of waiting for one another.
+__device__ __forceinline__ float sum_splits(const float* p, long long stride, int n) {
+  float sum = 0.f;
+  for (int k0 = 0; k0 < n; k0 += kMaxSplits) {
+    float v[kMaxSplits];
+#pragma unroll
+    for (int k = 0; k < kMaxSplits; ++k) v[k] = p[min(k0 + k, n - 1) * stride];
+#pragma unroll
+    for (int k = 0; k < kMaxSplits; ++k)
+      if (k0 + k < n) sum += v[k];
+  }
+  return sum;
+}
+
+// The splits' partial sums of kNT tokens' columns, all loads of a group of splits issued
+// before any is added (an index past the last token or split reads an existing entry, which
+// is not added); each token's sum in split order from 0.
+template <int kNT>
+__device__ __forceinline__ void sum_splits_t(const float* p, long long stride, long long ldp, int n, int nt,
+                                             float (&acc)[kNT]) {
+  constexpr int kG = kNT >= 16 ? 4 : kMaxSplits;
+  for (int k0 = 0; k0 < n; k0 += kG) {
+    float v[kG][kNT];
+#pragma unroll
+    for (int k = 0; k < kG; ++k)
+#pragma unroll
+      for (int t = 0; t < kNT; ++t) v[k][t] = p[min(k0 + k, n - 1) * stride + min(t, nt - 1) * ldp];
+#pragma unroll
+    for (int k = 0; k < kG; ++k)
+      if (k0 + k < n)
+#pragma unroll
+        for (int t = 0; t < kNT; ++t) acc[t] += v[k][t];
+  }
+}
+
+// kNT: the tokens a block carries (the call's T when it is at most 4, else 16 per block row)
+template <int kNT>
 __global__ void __launch_bounds__(256) skinny_reduce_kernel(const SkinnyReduceParams q) {
-  __shared__ __align__(16) uint16_t hs[kReduceT * kHCols];
-  const int t0 = blockIdx.y * kReduceT;
-  const int nt = min(kReduceT, q.T - t0);
+  __shared__ __align__(16) uint16_t hs[kNT * kHCols];
+  const int t0 = blockIdx.y * kNT;
+  const int nt = min(kNT, q.T - t0);
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   const long long sstride = static_cast<long long>(q.T) * q.ldp;
   const float* part = q.part + static_cast<long long>(t0) * q.ldp;
@@ -431,16 +470,7 @@ __global__ void __launch_bounds__(256) skinny_reduce_kernel(const SkinnyReducePa
   for (int idx = threadIdx.x; idx < nt * q.R16; idx += blockDim.x) {
     const int t = idx / q.R16;
     const int j = idx - t * q.R16;
-    // the splits' loads are independent: issued together, summed in order
-    float h = 0.f;
-    for (int ks0 = 0; ks0 < q.splits; ks0 += kMaxSplits) {
-      float hv[kMaxSplits];
-#pragma unroll
-      for (int ks = 0; ks < kMaxSplits; ++ks)
-        hv[ks] = ks0 + ks < q.splits ? part[(ks0 + ks) * sstride + t * q.ldp + q.N + j] : 0.f;
-#pragma unroll
-      for (int ks = 0; ks < kMaxSplits; ++ks) h += hv[ks];
-    }
+    const float h = sum_splits(part + t * q.ldp + q.N + j, sstride, q.splits);
     float s = 0.f;
     for (int a = 0; a < q.n_ad; ++a)
       if (j >= q.ad[a].toff && j < q.ad[a].toff + q.ad[a].rank) s = q.ad[a].s;
@@ -450,23 +480,12 @@ __global__ void __launch_bounds__(256) skinny_reduce_kernel(const SkinnyReducePa
   }
   __syncthreads();
   if (n >= q.N) return;
-  float acc[kReduceT];
+  float acc[kNT];
 #pragma unroll
-  for (int t = 0; t < kReduceT; ++t) acc[t] = 0.f;
-  if (q.has_w) {
-    for (int ks0 = 0; ks0 < q.splits; ks0 += kMaxSplits) {
+  for (int t = 0; t < kNT; ++t) acc[t] = 0.f;
+  if (q.has_w) sum_splits_t<kNT>(part + n, sstride, q.ldp, q.splits, nt, acc);
 #pragma unroll
-      for (int ks = 0; ks < kMaxSplits; ++ks) {
-        if (ks0 + ks < q.splits) {
-#pragma unroll
-          for (int t = 0; t < kReduceT; ++t)
-            if (t < nt) acc[t] += part[(ks0 + ks) * sstride + t * q.ldp + n];
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < kReduceT; ++t) acc[t] += bias;
+  for (int t = 0; t < kNT; ++t) acc[t] += bias;
   const int g = n / q.out_g;
   const int col = n - g * q.out_g;
   for (int a = 0; a < q.n_ad; ++a) {
@@ -490,7 +509,7 @@ __global__ void __launch_bounds__(256) skinny_reduce_kernel(const SkinnyReducePa
       }
       // H~ columns past the rank are zero (s = 0 there), so whole groups of 8 are safe
 #pragma unroll
-      for (int t = 0; t < kReduceT; ++t) {
+      for (int t = 0; t < kNT; ++t) {
         if (t < nt) {
           const uint4 hv = *reinterpret_cast<const uint4*>(hs + t * q.R16 + q.ad[a].toff + j0);
           const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
@@ -504,7 +523,7 @@ __global__ void __launch_bounds__(256) skinny_reduce_kernel(const SkinnyReducePa
     }
   }
 #pragma unroll
-  for (int t = 0; t < kReduceT; ++t) {
+  for (int t = 0; t < kNT; ++t) {
     if (t >= nt) break;
     const long long o = static_cast<long long>(t0 + t) * q.ldy + n;
     if (q.y_f32) {
@@ -553,8 +572,10 @@ int launch_skinny(const SkinnyMaps& maps, const SkinnyParams& p, size_t smem_byt
 }
 
 int launch_skinny_reduce(const SkinnyReduceParams& q, cudaStream_t stream) {
+  if (q.T <= 0 || q.N <= 0) return WP_OK;
+  const int nt = q.T <= 4 ? q.T : kReduceT;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((q.N + 255) / 256, (q.T + kReduceT - 1) / kReduceT);
+  cfg.gridDim = dim3((q.N + 255) / 256, (q.T + nt - 1) / nt);
   cfg.blockDim = dim3(256);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -562,7 +583,14 @@ int launch_skinny_reduce(const SkinnyReduceParams& q, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_reduce_kernel, q);
+  cudaError_t e;
+  switch (nt) {
+    case 1: e = cudaLaunchKernelEx(&cfg, skinny_reduce_kernel<1>, q); break;
+    case 2: e = cudaLaunchKernelEx(&cfg, skinny_reduce_kernel<2>, q); break;
+    case 3: e = cudaLaunchKernelEx(&cfg, skinny_reduce_kernel<3>, q); break;
+    case 4: e = cudaLaunchKernelEx(&cfg, skinny_reduce_kernel<4>, q); break;
+    default: e = cudaLaunchKernelEx(&cfg, skinny_reduce_kernel<kReduceT>, q); break;
+  }
   if (e != cudaSuccess) {
     set_last_cuda_error(e);
     return WP_ERR_CUDA;
