@@ -452,7 +452,8 @@ __device__ __forceinline__ void sum_splits_t(const float* p, long long stride, l
   }
 }
 
-// kNT: the tokens a block carries (the call's T when it is at most 4, else 16 per block row)
+// kNT: the tokens a block carries (the call's T when it is at most 4, 8 up to 8, else 16 per
+// block row)
 template <int kNT>
 __global__ void __launch_bounds__(256) skinny_reduce_kernel(const SkinnyReduceParams q) {
   __shared__ __align__(16) uint16_t hs[kNT * kHCols];
@@ -573,7 +574,7 @@ int launch_skinny(const SkinnyMaps& maps, const SkinnyParams& p, size_t smem_byt
 
 int launch_skinny_reduce(const SkinnyReduceParams& q, cudaStream_t stream) {
   if (q.T <= 0 || q.N <= 0) return WP_OK;
-  const int nt = q.T <= 4 ? q.T : kReduceT;
+  const int nt = q.T <= 4 ? q.T : (q.T <= 8 ? 8 : kReduceT);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((q.N + 255) / 256, (q.T + nt - 1) / nt);
   cfg.blockDim = dim3(256);
@@ -589,6 +590,7 @@ int launch_skinny_reduce(const SkinnyReduceParams& q, cudaStream_t stream) {
     case 2: e = cudaLaunchKernelEx(&cfg, skinny_reduce_kernel<2>, q); break;
     case 3: e = cudaLaunchKernelEx(&cfg, skinny_reduce_kernel<3>, q); break;
     case 4: e = cudaLaunchKernelEx(&cfg, skinny_reduce_kernel<4>, q); break;
+    case 8: e = cudaLaunchKernelEx(&cfg, skinny_reduce_kernel<8>, q); break;
     default: e = cudaLaunchKernelEx(&cfg, skinny_reduce_kernel<kReduceT>, q); break;
   }
   if (e != cudaSuccess) {
