@@ -38,9 +38,6 @@ __device__ __forceinline__ void store_from_f32(void* p, int dtype, long long i, 
   }
 }
 
-constexpr int kTile = 64;
-constexpr int kKc = 32;
-
 }  // namespace
 
 // s * X A^T for skinny A (a few to a few hundred rank columns).  One block: 32 token
@@ -242,68 +239,153 @@ __global__ void __launch_bounds__(128) rank_proj_kernel(const H32Params p) {
   }
 }
 
-// One block: 64 x 64 outputs, 256 threads, 4 x 4 per thread.
-__global__ void __launch_bounds__(256) f32_linear_kernel(const F32Params p, const float* H,
-                                                          int h_cols) {
-  __shared__ float xs[kTile][kKc + 1];
-  __shared__ float ws[kTile][kKc + 1];
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  const int row0 = blockIdx.y * kTile, col0 = blockIdx.x * kTile;
-  float acc[4][4];
+// One block: 128 x 128 outputs, 256 threads, 8 x 8 per thread (rows ty*4 + {0..3} and
+// 64 + ty*4 + {0..3}, columns tx*4 + {0..3} and 64 + tx*4 + {0..3}).  K goes 8 at a time
+// through two shared-memory buffers holding the X and W tiles K-major ([k][row]), so a thread
+// reads its 8 X and 8 W values of one k with four 16-byte loads (the X ones a broadcast
+// across the warp) and issues 64 fmas for them; the next K slice's global loads are in flight
+// in registers meanwhile (4 consecutive k of one row per thread, one vector load when the rows
+// allow it).  Each output's sum over k runs in k order from 0 in fp32 fmas; then the bias and
+// the adapters' H B^T terms, rank by rank in adapter order, as fmas onto it.
+constexpr int kSM = 128, kSN = 128, kSK = 8;
+
+// 4 consecutive elements of a row as fp32 (vec: one 8- or 16-byte load; else one by one,
+// zero past k_end)
+template <bool kF32>
+__device__ __forceinline__ void load4(const void* base, long long off, int k, int k_end, bool vec, float (&v)[4]) {
+  if (kF32) {
+    const float* q = static_cast<const float*>(base) + off;
+    if (vec) {
+      const float4 f = *reinterpret_cast<const float4*>(q);
+      v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    } else {
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 4; ++i) v[i] = k + i < k_end ? q[i] : 0.f;
+    }
+  } else {
+    const uint16_t* q = static_cast<const uint16_t*>(base) + off;
+    if (vec) {
+      const uint2 h = *reinterpret_cast<const uint2*>(q);
+      v[0] = __uint_as_float(h.x << 16); v[1] = __uint_as_float(h.x & 0xffff0000u);
+      v[2] = __uint_as_float(h.y << 16); v[3] = __uint_as_float(h.y & 0xffff0000u);
+    } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+      for (int i = 0; i < 4; ++i) v[i] = k + i < k_end ? __uint_as_float(static_cast<uint32_t>(q[i]) << 16) : 0.f;
+    }
+  }
+}
+
+template <bool kXF32, bool kWF32>
+__global__ void __launch_bounds__(256, 2) f32_linear_kernel(const F32Params p, const float* H, int h_cols,
+                                                             int vec) {
+  __shared__ __align__(16) float xs[2][kSK][kSM];
+  __shared__ __align__(16) float ws[2][kSK][kSN];
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int row0 = blockIdx.y * kSM, col0 = blockIdx.x * kSN;
+  const int lr = tid >> 1, lk = (tid & 1) * 4;    // the slice loads: row lr, k offsets lk .. lk + 3
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
   if (p.W) {
-    for (int k0 = 0; k0 < p.K; k0 += kKc) {
-      for (int idx = threadIdx.x; idx < kTile * kKc; idx += 256) {
-        const int r = idx / kKc, k = idx % kKc;
-        const int kk = k0 + k;
-        const int t = row0 + r, o = col0 + r;
-        xs[r][k] = (t < p.T && kk < p.K) ? load_as_f32(p.X, p.x_dtype, (long long)t * p.ldx + kk) : 0.f;
-        ws[r][k] = (o < p.N && kk < p.K) ? load_as_f32(p.W, p.w_dtype, (long long)o * p.ldw + kk) : 0.f;
+    float xr[4], wr[4];
+    const int t = row0 + lr, o = col0 + lr;
+    auto gload = [&](int k0) {
+      const int k = k0 + lk;
+      if (t < p.T && k < p.K) {
+        load4<kXF32>(p.X, static_cast<long long>(t) * p.ldx + k, k, p.K, vec != 0, xr);
+      } else {
+        xr[0] = xr[1] = xr[2] = xr[3] = 0.f;
       }
-      __syncthreads();
-#pragma unroll 8
-      for (int k = 0; k < kKc; ++k) {
-        float a[4], b[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) a[i] = xs[ty * 4 + i][k];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) b[j] = ws[tx * 4 + j][k];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      if (o < p.N && k < p.K) {
+        load4<kWF32>(p.W, static_cast<long long>(o) * p.ldw + k, k, p.K, vec != 0, wr);
+      } else {
+        wr[0] = wr[1] = wr[2] = wr[3] = 0.f;
       }
+    };
+    auto sstore = [&](int buf) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        xs[buf][lk + q][lr] = xr[q];
+        ws[buf][lk + q][lr] = wr[q];
+      }
+    };
+    gload(0);
+    sstore(0);
+    __syncthreads();
+    int buf = 0;
+    for (int k0 = 0; k0 < p.K; k0 += kSK) {
+      const bool more = k0 + kSK < p.K;
+      if (more) gload(k0 + kSK);
+#pragma unroll
+      for (int k = 0; k < kSK; ++k) {
+        const float4 a0 = *reinterpret_cast<const float4*>(&xs[buf][k][ty * 4]);
+        const float4 a1 = *reinterpret_cast<const float4*>(&xs[buf][k][64 + ty * 4]);
+        const float4 b0 = *reinterpret_cast<const float4*>(&ws[buf][k][tx * 4]);
+        const float4 b1 = *reinterpret_cast<const float4*>(&ws[buf][k][64 + tx * 4]);
+        const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      }
+      if (more) sstore(buf ^ 1);
       __syncthreads();
+      buf ^= 1;
     }
   }
 
+  // epilogue: bias, then each adapter's rank terms in order, for all 64 outputs at once
+  int trow[8], ocol[8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = row0 + ty * 4 + i;
-    if (t >= p.T) continue;
+  for (int i = 0; i < 8; ++i) trow[i] = row0 + (i < 4 ? ty * 4 + i : 60 + ty * 4 + i);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int o = col0 + tx * 4 + j;
-      if (o >= p.N) continue;
-      float v = acc[i][j];
-      if (p.bias) v += load_as_f32(p.bias, p.bias_dtype, o);
-      int off = 0;
-      for (int a = 0; a < p.n_ad; ++a) {
-        const F32Adapter& ad = p.ad[a];
-        if (o >= p.col_begin[a] && o < p.col_end[a]) {
-          const long long brow = (long long)(o - p.col_begin[a]) * ad.ldb;
-          const float* hrow = H + (long long)t * h_cols + off;
-          for (int jj = 0; jj < ad.rank; ++jj)
-            v = fmaf(hrow[jj], load_as_f32(ad.B, ad.b_dtype, brow + jj), v);
-        }
-        off += ad.rank;
-      }
-      store_from_f32(p.Y, p.y_dtype, (long long)t * p.ldy + o, v);
+  for (int j = 0; j < 8; ++j) ocol[j] = col0 + (j < 4 ? tx * 4 + j : 60 + tx * 4 + j);
+  if (p.bias) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float bj = ocol[j] < p.N ? load_as_f32(p.bias, p.bias_dtype, ocol[j]) : 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i][j] += bj;
     }
+  }
+  int off = 0;
+  for (int a = 0; a < p.n_ad; ++a) {
+    const F32Adapter& ad = p.ad[a];
+    bool in[8], any = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      in[j] = ocol[j] < p.N && ocol[j] >= p.col_begin[a] && ocol[j] < p.col_end[a];
+      any = any || in[j];
+    }
+    if (any) {
+      for (int jj = 0; jj < ad.rank; ++jj) {
+        float h[8], bb[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = trow[i] < p.T ? H[static_cast<long long>(trow[i]) * h_cols + off + jj] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          bb[j] = in[j] ? load_as_f32(ad.B, ad.b_dtype, static_cast<long long>(ocol[j] - p.col_begin[a]) * ad.ldb + jj)
+                        : 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (in[j]) acc[i][j] = fmaf(h[i], bb[j], acc[i][j]);
+      }
+    }
+    off += ad.rank;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (trow[i] >= p.T) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (ocol[j] < p.N) store_from_f32(p.Y, p.y_dtype, static_cast<long long>(trow[i]) * p.ldy + ocol[j], acc[i][j]);
   }
 }
 
@@ -447,8 +529,18 @@ int launch_rank_pack(const PackParams& p0, cudaStream_t stream) {
 
 int launch_f32_linear(const F32Params& p, const float* H, int h_cols, cudaStream_t stream) {
   if (p.T <= 0 || p.N <= 0) return WP_OK;
-  dim3 grid((p.N + kTile - 1) / kTile, (p.T + kTile - 1) / kTile);
-  f32_linear_kernel<<<grid, 256, 0, stream>>>(p, H, h_cols);
+  dim3 grid((p.N + kSN - 1) / kSN, std::min((p.T + kSM - 1) / kSM, 65535));
+  // vector loads of 4 consecutive K elements: every row start and K itself 4-element aligned
+  const auto aligned = [](const void* ptr, long long ld, int bytes) {
+    return reinterpret_cast<uintptr_t>(ptr) % (4 * bytes) == 0 && ld % 4 == 0;
+  };
+  const int xb = p.x_dtype == WP_FP32 ? 4 : 2, wb = p.w_dtype == WP_FP32 ? 4 : 2;
+  const int vec = p.K % 4 == 0 && aligned(p.X, p.ldx, xb) && (!p.W || aligned(p.W, p.ldw, wb)) ? 1 : 0;
+  const bool xf = p.x_dtype == WP_FP32, wf = !p.W || p.w_dtype == WP_FP32;
+  if (xf && wf) f32_linear_kernel<true, true><<<grid, 256, 0, stream>>>(p, H, h_cols, vec);
+  else if (xf) f32_linear_kernel<true, false><<<grid, 256, 0, stream>>>(p, H, h_cols, vec);
+  else if (wf) f32_linear_kernel<false, true><<<grid, 256, 0, stream>>>(p, H, h_cols, vec);
+  else f32_linear_kernel<false, false><<<grid, 256, 0, stream>>>(p, H, h_cols, vec);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_last_cuda_error(e);
