@@ -173,7 +173,7 @@ int lora_linear_fwd_grouped(const wp_mat* X, const wp_mat* W_stacked, const wp_m
  * (n_groups >= 1) with X and Y in host memory, for callers whose activations live on the
  * host.  A deployment variant with no counterpart in the pages.
  *
- * The rows are processed in chunks of 4096: the host-to-device copy of chunk i + 1, the
+ * The rows are processed in chunks of 2048: the host-to-device copy of chunk i + 1, the
  * forward of chunk i and the device-to-host copy of chunk i - 1 run at the same time on
  * three streams owned by the library (created on the first call per device); the call
  * returns at once and `stream` waits for the whole operation.  X and Y should be pinned

@@ -1296,7 +1296,7 @@ int exact_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int n_group
 // Workspace of lora_linear_fwd_host, in order (each region 256-byte aligned): X chunks
 // [2][chunk, in] | Y chunks [2][chunk, out] (fp32-sized, whatever Y's type) | the
 // forward's scratch for one chunk.
-constexpr long long kHostChunkRows = 4096;
+constexpr long long kHostChunkRows = 2048;
 
 struct HostLayout {
   size_t x[2], y[2], fwd, fwd_bytes, total;
