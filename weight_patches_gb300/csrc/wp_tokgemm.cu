@@ -202,58 +202,82 @@ __global__ void __launch_bounds__(192, 1) tokgemm_kernel(const __grid_constant__
 // fp32 [T, R] (row pitch ld) -> bf16 pieces [T, N]: column off[g] + j of group g (j < r[g])
 // gets hi = bf16(v) in column roff16[g] + j and lo = bf16(v - hi) in column R16 + roff16[g] + j;
 // every other column is zero.
+// A block takes kPieceRows token rows; thread c owns output column c of every one of them (its
+// group, rank column and piece worked out once), so loads and stores are contiguous along c.
+constexpr int kPieceRows = 8;
+
 __global__ void __launch_bounds__(256) pieces_kernel(const float* src, long long ld, int T, int N,
                                                      TokPieceMap pm, uint16_t* dst) {
-  const long long n = static_cast<long long>(T) * N;
-  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n;
-       e += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int t = static_cast<int>(e / N);
-    const int c = static_cast<int>(e - static_cast<long long>(t) * N);
-    const int piece = c >= pm.R16 ? 1 : 0;
-    const int cc = c - piece * pm.R16;
+  const int c = threadIdx.x;
+  const int piece = c >= pm.R16 ? 1 : 0;
+  const int cc = c - piece * pm.R16;
+  int col = -1;                                   // the source column, or -1 for a zero
+  if (c < N && cc < pm.R16)
+    for (int g = 0; g < pm.G; ++g) {
+      const int j = cc - pm.roff16[g];
+      if (j >= 0 && j < pm.r[g]) col = pm.off[g] + j;
+    }
+  for (int i = 0; i < kPieceRows; ++i) {
+    const long long t = static_cast<long long>(blockIdx.x) * kPieceRows + i;
+    if (t >= T || c >= N) break;
     uint16_t out = 0;
-    if (cc < pm.R16) {
-      for (int g = 0; g < pm.G; ++g) {
-        const int j = cc - pm.roff16[g];
-        if (j >= 0 && j < pm.r[g]) {
-          const float v = src[static_cast<long long>(t) * ld + pm.off[g] + j];
-          uint16_t hi;
-          asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(hi) : "f"(v));
-          if (piece == 0) {
-            out = hi;
-          } else {
-            const float rest = __fsub_rn(v, __uint_as_float(static_cast<uint32_t>(hi) << 16));
-            asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(out) : "f"(rest));
-          }
-        }
+    if (col >= 0) {
+      const float v = src[t * ld + col];
+      uint16_t hi;
+      asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(hi) : "f"(v));
+      if (piece == 0) {
+        out = hi;
+      } else {
+        const float rest = __fsub_rn(v, __uint_as_float(static_cast<uint32_t>(hi) << 16));
+        asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(out) : "f"(rest));
       }
     }
-    dst[e] = out;
+    dst[t * N + c] = out;
   }
 }
 
 // out_g[j, i] (transposed) or out_g[m, j]: scale * sum over splits of (hi + lo columns), rows
-// [row0, row0 + rows) of D for group g, in a fixed order.
+// [row0, row0 + rows) of D for group g, in a fixed order.  A block takes kFinRows rows and all r
+// columns: loads along j (contiguous in the partial sums), every split's loads issued before
+// any is added (in split order); the transposed form goes through shared memory so that its
+// stores run along m.
+constexpr int kFinRows = 16;
+constexpr int kFinMaxR = 128;
+
 __global__ void __launch_bounds__(256) tok_finish_kernel(const float* part, int M, int N, int splits, int R16,
                                                          int roff16, int r, int row0, int rows, float scale,
                                                          float* out, long long ldo, int transposed) {
-  const long long n = static_cast<long long>(rows) * r;
-  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n;
-       e += static_cast<long long>(gridDim.x) * blockDim.x) {
-    // consecutive threads take consecutive rows m: coalesced transposed stores
-    const int j = static_cast<int>(e / rows);
-    const int mm = static_cast<int>(e - static_cast<long long>(j) * rows);
-    const long long m = row0 + mm;
+  __shared__ float tile[kFinRows][kFinMaxR + 1];
+  const int m0 = blockIdx.x * kFinRows;
+  const int nm = min(kFinRows, rows - m0);
+  for (int idx = threadIdx.x; idx < nm * r; idx += blockDim.x) {
+    const int mm = idx / r, j = idx - mm * r;
+    const long long m = row0 + m0 + mm;
     float acc = 0.f;
-    for (int ks = 0; ks < splits; ++ks) {
-      const float* pr = part + (static_cast<long long>(ks) * M + m) * N;
-      acc += __fadd_rn(pr[roff16 + j], pr[R16 + roff16 + j]);
+    for (int k0 = 0; k0 < splits; k0 += 4) {
+      float hi[4], lo[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float* pr = part + (static_cast<long long>(min(k0 + q, splits - 1)) * M + m) * N;
+        hi[q] = pr[roff16 + j];
+        lo[q] = pr[R16 + roff16 + j];
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (k0 + q < splits) acc += __fadd_rn(hi[q], lo[q]);
     }
     const float v = __fmul_rn(acc, scale);
     if (transposed)
-      out[static_cast<long long>(j) * ldo + mm] = v;
+      tile[mm][j] = v;
     else
-      out[static_cast<long long>(mm) * ldo + j] = v;
+      out[static_cast<long long>(m0 + mm) * ldo + j] = v;
+  }
+  if (transposed) {
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < nm * r; idx += blockDim.x) {
+      const int j = idx / nm, mm = idx - j * nm;
+      out[static_cast<long long>(j) * ldo + m0 + mm] = tile[mm][j];
+    }
   }
 }
 
@@ -307,12 +331,11 @@ int launch_tokgemm(const TokGemmMaps& maps, const TokGemmParams& p, int pairs, s
 
 int launch_pieces(const float* src, long long ld, int T, int N, const TokPieceMap& pm, uint16_t* dst,
                   cudaStream_t stream) {
-  const long long n = static_cast<long long>(T) * N;
-  long long blocks = (n + 255) / 256;
-  const long long cap = static_cast<long long>(device_sm_count()) * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) return WP_OK;
-  pieces_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, ld, T, N, pm, dst);
+  if (T <= 0 || N <= 0) return WP_OK;
+  if (N > 256) return WP_ERR_UNSUPPORTED;
+  const long long blocks = (static_cast<long long>(T) + kPieceRows - 1) / kPieceRows;
+  if (blocks > 0x7FFFFFFFLL) return WP_ERR_UNSUPPORTED;
+  pieces_kernel<<<static_cast<unsigned>(blocks), N, 0, stream>>>(src, ld, T, N, pm, dst);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_last_cuda_error(e);
@@ -323,13 +346,11 @@ int launch_pieces(const float* src, long long ld, int T, int N, const TokPieceMa
 
 int launch_tok_finish(const float* part, int M, int N, int splits, int R16, int roff16, int r, int row0, int rows,
                       float scale, float* out, long long ldo, bool transposed, cudaStream_t stream) {
-  const long long n = static_cast<long long>(rows) * r;
-  long long blocks = (n + 255) / 256;
-  const long long cap = static_cast<long long>(device_sm_count()) * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) return WP_OK;
-  tok_finish_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(part, M, N, splits, R16, roff16, r, row0,
-                                                                      rows, scale, out, ldo, transposed ? 1 : 0);
+  if (rows <= 0 || r <= 0 || splits <= 0) return WP_OK;
+  if (r > kFinMaxR) return WP_ERR_UNSUPPORTED;
+  const int blocks = (rows + kFinRows - 1) / kFinRows;
+  tok_finish_kernel<<<blocks, 256, 0, stream>>>(part, M, N, splits, R16, roff16, r, row0, rows, scale, out, ldo,
+                                                transposed ? 1 : 0);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_last_cuda_error(e);
