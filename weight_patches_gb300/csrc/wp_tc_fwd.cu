@@ -409,18 +409,31 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       const uint32_t idesc_h = idesc_bf16_f32(kPairM, p.htot > 0 ? p.htot : 16);
       const uint32_t stage_base = smem_u32(sbase);
       bool ok = true;
+      // This thread issues every MMA of the pair, so its instructions between two MMAs are
+      // on the tensor core's critical path: the shared-memory descriptors of stage 0's
+      // slots are formed once, and a step only adds its stage's offset (the start-address
+      // field counts 16-byte units and stays below 2^14 for any shared-memory address).
+      const uint64_t d_x = sw128_kmajor_desc(stage_base);                 // X / H~ rows
+      const uint64_t d_w = sw128_kmajor_desc(stage_base + kXBytes);       // W, packed A or B rows
+      const uint64_t d_w_mn = sw128_mnmajor_desc(stage_base + kXBytes);   // W stored [in, out]
+      const uint64_t d_x64 = sw64_kmajor_desc(stage_base);                // 32-rank boxes
+      const uint64_t d_w64 = sw64_kmajor_desc(stage_base + kXBytes);
+      constexpr uint64_t kHalfStep = kATileBytes >> 4;                    // next M half's X rows
+      const uint32_t stage_units = static_cast<uint32_t>(SB) >> 4;
       // Operands of a step: A (X or H~ rows of each half) first, then B.  Every step
       // waits for the TMA bytes of both CTAs (full) and, with a 4-bit W, for the
       // dequantisation warps (wfull: the weight tile of a base step is written; on the
       // other steps it keeps every dequantisation warp in step).
       int s0 = 0;
-      auto take = [&](uint32_t& st) -> bool {
+      uint32_t off_next = 0;                  // descriptor offset of `stage`
+      auto take = [&](uint64_t& off) -> bool {
         if (!mbar_wait(&full[stage], phase, abort_flag, tmo, status)) return false;
         if (kNF4 && !mbar_wait_cluster(&wfull[stage], phase, abort_flag, tmo, status)) return false;
         s0 = stage;
-        if (++stage == S) { stage = 0; phase ^= 1; }
+        off = off_next;
+        off_next += stage_units;
+        if (++stage == S) { stage = 0; phase ^= 1; off_next = 0; }
         tc_fence_after();
-        st = stage_base + s0 * SB;
         return true;
       };
       auto give_back = [&]() { mma_commit_pair_mc(&empty[s0], kBothCtas); };
@@ -436,48 +449,58 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         tc_fence_after();
         const uint32_t acc_t = tmem + b * kBN;
         if (it.rank) {
-          // one MMA per K step covers every adapter: N = htot rank columns
+          // one MMA per K step covers every adapter: N = htot rank columns (the packed A
+          // rows sit one X box further)
           for (int kb = 0; kb < p.k_blocks; ++kb) {
-            uint32_t st;
-            if (!(ok = take(st))) break;
-            const uint64_t ad = sw128_kmajor_desc(st);
-            const uint64_t rd = sw128_kmajor_desc(st + kATileBytes);
+            uint64_t off;
+            if (!(ok = take(off))) break;
+            const uint64_t ad = d_x + off, rd = ad + kHalfStep;
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
               mma_bf16_pair(acc_t, ad + 2 * kk, rd + 2 * kk, idesc_h, (kb | kk) != 0 ? 1u : 0u);
             give_back();
           }
         } else {
-          if (p.has_base) {
+          if (p.has_base && !p.w_mn) {
             for (int kb = 0; kb < p.k_blocks; ++kb) {
-              uint32_t st;
-              if (!(ok = take(st))) break;
-              // the weight slot: K-major, or MN-major when W is stored [in, out]
-              const uint64_t bd = sw128_kmajor_desc(st + kXBytes);
-              const uint32_t bmn = st + kXBytes;
+              uint64_t off;
+              if (!(ok = take(off))) break;
+              const uint64_t ad = d_x + off, bd = d_w + off;
 #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk)
 #pragma unroll
                 for (int h = 0; h < kMH; ++h)
-                  mma_bf16_pair(acc_t + h * kBN, sw128_kmajor_desc(st + h * kATileBytes) + 2 * kk,
-                                p.w_mn ? sw128_mnmajor_desc(bmn + kk * 2048) : bd + 2 * kk,
-                                p.w_mn ? idesc_acc_mn : idesc_acc, (kb | kk) != 0 ? 1u : 0u);
+                  mma_bf16_pair(acc_t + h * kBN, ad + h * kHalfStep + 2 * kk, bd + 2 * kk, idesc_acc,
+                                (kb | kk) != 0 ? 1u : 0u);
+              give_back();
+            }
+          } else if (p.has_base) {
+            // W stored [in, out]: an MN-major weight slot, 2048 bytes per 16 K rows
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+              uint64_t off;
+              if (!(ok = take(off))) break;
+              const uint64_t ad = d_x + off, bd = d_w_mn + off;
+#pragma unroll
+              for (int kk = 0; kk < kBK / 16; ++kk)
+#pragma unroll
+                for (int h = 0; h < kMH; ++h)
+                  mma_bf16_pair(acc_t + h * kBN, ad + h * kHalfStep + 2 * kk, bd + kk * (2048 >> 4), idesc_acc_mn,
+                                (kb | kk) != 0 ? 1u : 0u);
               give_back();
             }
           }
           bool accum = p.has_base != 0;
           for (int a = a0; a < a1 && ok; ++a) {
             for (int c = 0; c < p.ad[a].nchunks; ++c) {
-              uint32_t st;
-              if (!(ok = take(st))) break;
+              uint64_t off;
+              if (!(ok = take(off))) break;
               const int kext = min(64, p.ad[a].rpad16 - 64 * c);
               const bool narrow = kext <= 32;              // 32-rank boxes, 64-byte swizzle
-              auto desc = [&](uint32_t addr) { return narrow ? sw64_kmajor_desc(addr) : sw128_kmajor_desc(addr); };
-              const uint64_t bd = desc(st + kXBytes);
+              const uint64_t ad = (narrow ? d_x64 : d_x) + off, bd = (narrow ? d_w64 : d_w) + off;
               for (int kk = 0; kk < kext / 16; ++kk)
 #pragma unroll
                 for (int h = 0; h < kMH; ++h)
-                  mma_bf16_pair(acc_t + h * kBN, desc(st + h * kATileBytes) + 2 * kk, bd + 2 * kk, idesc_acc,
+                  mma_bf16_pair(acc_t + h * kBN, ad + h * kHalfStep + 2 * kk, bd + 2 * kk, idesc_acc,
                                 (accum || kk > 0) ? 1u : 0u);
               accum = true;
               give_back();
