@@ -76,6 +76,8 @@ struct TcParams {
                                // W as it is): weight tiles are MN-major MMA operands; a 4-bit
                                // W's codes are [in rows, out / 2 bytes], blocks of 64 along out
   int rlead;                   // rank items run this many rounds of tiles ahead of their tiles
+  int step_j, step_g, step_m;  // the number of pairs in (row block, group, column tile) digits
+                               // (set by the launcher)
   int has_base;
   int n_ad;                    // adapters on the tensor cores (bf16, or FP32 as pieces)
   int ad_begin[kMaxGroups + 1];

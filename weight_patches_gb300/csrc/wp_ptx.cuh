@@ -503,27 +503,24 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
 // Shared-memory matrix descriptor for a K-major operand in the 128-byte swizzle
 // layout: rows of 128 bytes (64 bf16 along K), 8-row groups 1024 bytes apart.  The
 // tile base must be 1024-byte aligned; advancing K by 16 elements inside the atom
-// adds 32 bytes to the start address.
+// adds 32 bytes to the start address.  The fields other than the start address (bits
+// 0..13, in 16-byte units) are constants:
+constexpr uint64_t kDescSw128K = (uint64_t{1} << 16)               // LBO (unused here)
+                                 | (uint64_t{1024 >> 4} << 32)     // SBO: 8-row group stride
+                                 | (uint64_t{1} << 46)             // descriptor version
+                                 | (uint64_t{2} << 61);            // 128-byte swizzle
 __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);          // start address
-  d |= static_cast<uint64_t>(1) << 16;                              // LBO (unused here)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;                      // SBO: 8-row group stride
-  d |= static_cast<uint64_t>(1) << 46;                              // descriptor version
-  d |= static_cast<uint64_t>(2) << 61;                              // 128-byte swizzle
-  return d;
+  return kDescSw128K | static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
 }
 
 // The same for rows of 64 bytes (32 bf16 along K) in the 64-byte swizzle layout: 8-row
 // groups of 512 bytes.
+constexpr uint64_t kDescSw64K = (uint64_t{1} << 16)                // LBO (unused here)
+                                | (uint64_t{512 >> 4} << 32)       // SBO: 8-row group stride
+                                | (uint64_t{1} << 46)              // descriptor version
+                                | (uint64_t{4} << 61);             // 64-byte swizzle
 __device__ __forceinline__ uint64_t sw64_kmajor_desc(uint32_t smem_addr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);          // start address
-  d |= static_cast<uint64_t>(1) << 16;                              // LBO (unused here)
-  d |= static_cast<uint64_t>(512 >> 4) << 32;                       // SBO: 8-row group stride
-  d |= static_cast<uint64_t>(1) << 46;                              // descriptor version
-  d |= static_cast<uint64_t>(4) << 61;                              // 64-byte swizzle
-  return d;
+  return kDescSw64K | static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
 }
 
 // Instruction descriptor: kind::f16, bf16 A and B, fp32 D, both operands K-major.
@@ -538,14 +535,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
 // MN-major operand in the 128-byte swizzle: 64-element chunks along M/N 8192 bytes apart
 // (boxes of 64 K rows x 64 elements), 8-row groups along K 1024 bytes apart; K advances
 // 2048 bytes per 16-deep MMA.
+constexpr uint64_t kDescSw128MN = (uint64_t{8192 >> 4} << 16)      // LBO: next 64-element chunk
+                                  | (uint64_t{1024 >> 4} << 32)    // SBO: next 8-row group along K
+                                  | (uint64_t{1} << 46)            // descriptor version
+                                  | (uint64_t{2} << 61);           // 128-byte swizzle
 __device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);          // start address
-  d |= static_cast<uint64_t>(8192 >> 4) << 16;                      // LBO: next 64-element chunk
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;                      // SBO: next 8-row group along K
-  d |= static_cast<uint64_t>(1) << 46;                              // descriptor version
-  d |= static_cast<uint64_t>(2) << 61;                              // 128-byte swizzle
-  return d;
+  return kDescSw128MN | static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
 }
 
 // The same with the distance between 64-element chunks given (a box of fewer than 64 K rows).

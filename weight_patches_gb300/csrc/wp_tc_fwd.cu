@@ -82,38 +82,63 @@ struct Item {
 };
 
 // Rank items are numbered i = m * npass + q (row block m, pass q); item i belongs to pair
-// (i + total_tiles) mod npairs.
+// (i + total_tiles) mod npairs.  The walk is incremental: the next tile is the current one
+// stepped by npairs in (row block, group, column tile) digits, and the round at which the
+// next rank item is due is formed once per rank item, so that the threads on the tensor
+// core's critical path divide nothing per item.
 struct ItemIter {
-  int k;        // next tile round of this pair
+  int k;        // tile rounds handed out so far
+  int pos;      // position of the next tile: pair + k * npairs
+  Tile t;       // the tile at pos (while pos < total_tiles)
   int m_next;   // next rank item this pair owns
+  int due;      // the round at whose start item m_next runs
 };
 
+__device__ __forceinline__ int rank_item_due(const TcParams& p, int i, int npairs) {
+  const int m = p.npass == 1 ? i : i / p.npass;
+  // (m >> m_shift) * tpb <= total_tiles < 2^31
+  const uint32_t first = static_cast<uint32_t>((m >> p.m_shift) * p.G * p.nt_g) / static_cast<uint32_t>(npairs);
+  return static_cast<int>(first) - p.rlead;
+}
+
 __device__ __forceinline__ ItemIter item_iter_begin(const TcParams& p, int pair, int npairs) {
-  const int first = ((pair - p.total_tiles) % npairs + npairs) % npairs;
-  return ItemIter{0, first};
+  ItemIter s;
+  s.k = 0;
+  s.pos = pair;
+  s.t = pair < p.total_tiles ? decode_tile(p, pair) : Tile{0, 0, 0};
+  s.m_next = ((pair - p.total_tiles) % npairs + npairs) % npairs;
+  s.due = p.n_ad > 0 ? rank_item_due(p, s.m_next, npairs) : 0;
+  return s;
 }
 
 __device__ __forceinline__ bool next_item(ItemIter& s, const TcParams& p, int pair, int npairs,
                                           Item& it) {
-  const int tile_pos = pair + s.k * npairs;
-  if (p.n_ad > 0 && s.m_next < p.r_blocks * p.npass) {
-    const int m = s.m_next / p.npass;
-    const int due = static_cast<int>((static_cast<long long>(m >> p.m_shift) * p.G * p.nt_g) / npairs) - p.rlead;
-    if (due <= s.k || tile_pos >= p.total_tiles) {
-      it.rank = true;
-      it.m = m;
-      it.q = s.m_next - m * p.npass;
-      it.t = Tile{0, 0, 0};
-      s.m_next += npairs;
-      return true;
-    }
+  (void)pair;
+  const int n_rank = p.r_blocks * p.npass;
+  if (p.n_ad > 0 && s.m_next < n_rank && (s.due <= s.k || s.pos >= p.total_tiles)) {
+    it.rank = true;
+    it.m = p.npass == 1 ? s.m_next : s.m_next / p.npass;
+    it.q = s.m_next - it.m * p.npass;
+    it.t = Tile{0, 0, 0};
+    s.m_next += npairs;
+    if (s.m_next < n_rank) s.due = rank_item_due(p, s.m_next, npairs);
+    return true;
   }
-  if (tile_pos >= p.total_tiles) return false;
+  if (s.pos >= p.total_tiles) return false;
   it.rank = false;
   it.q = 0;
-  it.t = decode_tile(p, tile_pos);
-  it.m = it.t.m;
+  it.t = s.t;
+  it.m = s.t.m;
   ++s.k;
+  s.pos += npairs;
+  // npairs = (step_m * G + step_g) * nt_g + step_j, with step_j < nt_g and step_g < G
+  s.t.j += p.step_j;
+  const int cj = s.t.j >= p.nt_g ? 1 : 0;
+  s.t.j -= cj * p.nt_g;
+  s.t.g += p.step_g + cj;
+  const int cg = s.t.g >= p.G ? 1 : 0;
+  s.t.g -= cg * p.G;
+  s.t.m += p.step_m + cg;
   return true;
 }
 
@@ -232,20 +257,21 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       const uint64_t keep = l2_evict_last();   // W, A, B and H~ are re-read by many tiles
       int stage = 0;
       uint32_t phase = 0;
-      int issued[kMaxStages];
-      for (int s = 0; s < kMaxStages; ++s) issued[s] = 0;
+      uint32_t n_issued = 0;                  // stages claimed and filled so far
       bool ok = true;
       // Claim the next stage once the MMAs have released it; the leader's full barrier
-      // expects `tx` bytes from both CTAs.
+      // expects `tx` bytes from both CTAs.  (The leader's barrier address as both CTAs see
+      // it is formed once: the claim sits between an MMA's release and the next loads.)
+      const uint32_t full_l0 = mapa_shared(smem_u32(&full[0]), 0);
       auto claim = [&](uint32_t tx, uint8_t*& st, uint32_t& fb) -> bool {
         if (!mbar_wait_cluster(&empty[stage], phase ^ 1, abort_flag, tmo, status)) return false;
         st = sbase + stage * SB;
-        fb = mapa_shared(smem_u32(&full[stage]), 0);
+        fb = full_l0 + static_cast<uint32_t>(stage) * 8u;
         if (leader) mbar_arrive_expect_tx(&full[stage], tx);
         return true;
       };
       auto advance = [&]() {
-        ++issued[stage];
+        ++n_issued;
         if (++stage == S) { stage = 0; phase ^= 1; }
       };
       const uint32_t rank_tx = static_cast<uint32_t>(p.htot) * 128;   // packed A rows, both CTAs
@@ -380,8 +406,9 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         // Wait (bounded) for the copies put in flight before the CTA exits: the pair's
         // copies complete on the leader's barriers, a 4-bit W's codes on code_full.
         for (int s = 0; s < S; ++s) {
-          if (issued[s] == 0 || !leader) continue;
-          const uint32_t par = static_cast<uint32_t>((issued[s] - 1) & 1);
+          const uint32_t n = n_issued / S + (static_cast<uint32_t>(s) < n_issued % S ? 1u : 0u);
+          if (n == 0 || !leader) continue;
+          const uint32_t par = (n - 1) & 1u;
           const uint64_t t0 = globaltimer_ns();
           const uint32_t a = smem_u32(&full[s]);
           while (!mbar_try_wait_cluster(a, par) && globaltimer_ns() - t0 < 100000000ull) {
@@ -410,15 +437,12 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       const uint32_t stage_base = smem_u32(sbase);
       bool ok = true;
       // This thread issues every MMA of the pair, so its instructions between two MMAs are
-      // on the tensor core's critical path: the shared-memory descriptors of stage 0's
-      // slots are formed once, and a step only adds its stage's offset (the start-address
-      // field counts 16-byte units and stays below 2^14 for any shared-memory address).
-      const uint64_t d_x = sw128_kmajor_desc(stage_base);                 // X / H~ rows
-      const uint64_t d_w = sw128_kmajor_desc(stage_base + kXBytes);       // W, packed A or B rows
-      const uint64_t d_w_mn = sw128_mnmajor_desc(stage_base + kXBytes);   // W stored [in, out]
-      const uint64_t d_x64 = sw64_kmajor_desc(stage_base);                // 32-rank boxes
-      const uint64_t d_w64 = sw64_kmajor_desc(stage_base + kXBytes);
-      constexpr uint64_t kHalfStep = kATileBytes >> 4;                    // next M half's X rows
+      // on the tensor core's critical path: a step's descriptors are the constant fields
+      // and the start address (16-byte units, below 2^14 for any shared-memory address) of
+      // its slot, stage 0's plus the stage's offset.
+      const uint32_t u_x = stage_base >> 4;                     // X / H~ rows
+      const uint32_t u_w = (stage_base + kXBytes) >> 4;         // W, packed A or B rows
+      constexpr uint32_t kHalfStep = kATileBytes >> 4;          // next M half's X rows
       const uint32_t stage_units = static_cast<uint32_t>(SB) >> 4;
       // Operands of a step: A (X or H~ rows of each half) first, then B.  Every step
       // waits for the TMA bytes of both CTAs (full) and, with a 4-bit W, for the
@@ -426,7 +450,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       // other steps it keeps every dequantisation warp in step).
       int s0 = 0;
       uint32_t off_next = 0;                  // descriptor offset of `stage`
-      auto take = [&](uint64_t& off) -> bool {
+      auto take = [&](uint32_t& off) -> bool {
         if (!mbar_wait(&full[stage], phase, abort_flag, tmo, status)) return false;
         if (kNF4 && !mbar_wait_cluster(&wfull[stage], phase, abort_flag, tmo, status)) return false;
         s0 = stage;
@@ -452,9 +476,9 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
           // one MMA per K step covers every adapter: N = htot rank columns (the packed A
           // rows sit one X box further)
           for (int kb = 0; kb < p.k_blocks; ++kb) {
-            uint64_t off;
+            uint32_t off;
             if (!(ok = take(off))) break;
-            const uint64_t ad = d_x + off, rd = ad + kHalfStep;
+            const uint64_t ad = kDescSw128K | (u_x + off), rd = kDescSw128K | (u_x + off + kHalfStep);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
               mma_bf16_pair(acc_t, ad + 2 * kk, rd + 2 * kk, idesc_h, (kb | kk) != 0 ? 1u : 0u);
@@ -463,9 +487,9 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         } else {
           if (p.has_base && !p.w_mn) {
             for (int kb = 0; kb < p.k_blocks; ++kb) {
-              uint64_t off;
+              uint32_t off;
               if (!(ok = take(off))) break;
-              const uint64_t ad = d_x + off, bd = d_w + off;
+              const uint64_t ad = kDescSw128K | (u_x + off), bd = kDescSw128K | (u_w + off);
 #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk)
 #pragma unroll
@@ -477,9 +501,9 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
           } else if (p.has_base) {
             // W stored [in, out]: an MN-major weight slot, 2048 bytes per 16 K rows
             for (int kb = 0; kb < p.k_blocks; ++kb) {
-              uint64_t off;
+              uint32_t off;
               if (!(ok = take(off))) break;
-              const uint64_t ad = d_x + off, bd = d_w_mn + off;
+              const uint64_t ad = kDescSw128K | (u_x + off), bd = kDescSw128MN | (u_w + off);
 #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk)
 #pragma unroll
@@ -492,11 +516,12 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
           bool accum = p.has_base != 0;
           for (int a = a0; a < a1 && ok; ++a) {
             for (int c = 0; c < p.ad[a].nchunks; ++c) {
-              uint64_t off;
+              uint32_t off;
               if (!(ok = take(off))) break;
               const int kext = min(64, p.ad[a].rpad16 - 64 * c);
               const bool narrow = kext <= 32;              // 32-rank boxes, 64-byte swizzle
-              const uint64_t ad = (narrow ? d_x64 : d_x) + off, bd = (narrow ? d_w64 : d_w) + off;
+              const uint64_t bits = narrow ? kDescSw64K : kDescSw128K;
+              const uint64_t ad = bits | (u_x + off), bd = bits | (u_w + off);
               for (int kk = 0; kk < kext / 16; ++kk)
 #pragma unroll
                 for (int h = 0; h < kMH; ++h)
@@ -1184,8 +1209,17 @@ int tc_max_pairs(size_t smem_bytes, bool nf4) {
   return n;
 }
 
-int launch_tc_fwd(const TcMaps& maps, const TcParams& p, int grid, size_t smem_bytes,
+int launch_tc_fwd(const TcMaps& maps, const TcParams& params, int grid, size_t smem_bytes,
                   cudaStream_t stream, bool nf4) {
+  // the pairs' stride through the tiles, in (row block, group, column tile) digits
+  TcParams p = params;
+  const int npairs = grid / 2;
+  p.step_j = p.step_g = p.step_m = 0;
+  if (p.nt_g > 0 && p.G > 0 && npairs > 0) {
+    p.step_j = npairs % p.nt_g;
+    p.step_g = (npairs / p.nt_g) % p.G;
+    p.step_m = npairs / p.nt_g / p.G;
+  }
   const bool f32 = p.n_ad32 > 0;
   if (nf4)
     return f32 ? launch_impl<true, true>(maps, p, grid, smem_bytes, stream)
