@@ -340,11 +340,12 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         const int x_row = t.m * (kPairM * kMH) + static_cast<int>(cta) * kBM;
         const int blk0 = t.m * kMH;                           // the tile's 256-row blocks
         const int nblk = min(kMH, p.r_blocks - blk0);
-        // the blocks' flags, read (acquire) before the base K loop: the read's latency is
-        // covered by the stages already queued for the MMA, and the flags are usually set
+        // the blocks' flags, read (relaxed) before the base K loop and used at its end, so
+        // that the read's latency overlaps the base steps' loads (an acquire here would hold
+        // back every later load until the flag's line came back); usually they are set
         uint32_t peek = p.flag_target;
         if (a1 > a0)
-          for (int h = 0; h < nblk; ++h) peek = min(peek, ld_acquire_gpu(p.flags + blk0 + h));
+          for (int h = 0; h < nblk; ++h) peek = min(peek, ld_relaxed_gpu(p.flags + blk0 + h));
         if (p.has_base) {
           const int w_row = weight_row(p, t, cta);
           for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -377,8 +378,12 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         if (a1 > a0) {
           // second contraction: H~ of the tile's rows (written by the rank items of its
           // blocks) and B
-          for (int h = 0; h < nblk && ok && peek < p.flag_target; ++h)
-            ok = flag_wait(p.flags + blk0 + h, p.flag_target, abort_flag, tmo, status);
+          if (peek >= p.flag_target) {
+            fence_acq_rel_gpu();                 // the relaxed reads saw every release: acquire
+          } else {
+            for (int h = 0; h < nblk && ok; ++h)
+              ok = flag_wait(p.flags + blk0 + h, p.flag_target, abort_flag, tmo, status);
+          }
           if (!ok) break;
           fence_proxy_async_global();
           for (int a = a0; a < a1 && ok; ++a) {
