@@ -434,8 +434,10 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
     if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t nuse[2] = {0, 0};
       int count = 0;
+      // item `count` uses accumulator buffer count & 1 (a 4-bit W's tile: buffer 0 always);
+      // the parity of that buffer's earlier uses
+      auto use_parity = [&]() -> uint32_t { return static_cast<uint32_t>(kNF4 ? count : (count >> 1)) & 1u; };
       const uint32_t idesc_acc = idesc_bf16_f32(kPairM, kBN);
       const uint32_t idesc_acc_mn = idesc_bf16_f32_bmn(kPairM, kBN);
       const uint32_t idesc_h = idesc_bf16_f32(kPairM, p.htot > 0 ? p.htot : 16);
@@ -473,7 +475,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         const int a1 = it.rank ? 0 : p.ad_begin[it.t.g + 1];
         if (!it.rank && !(p.has_base || a1 > a0)) continue;   // bias-only tile: no MMA
         const int b = kNF4 ? 0 : (count & 1);   // a 4-bit W's tile fills all 512 columns
-        if (!(ok = mbar_wait_cluster(&acc_empty[b], (nuse[b] & 1) ^ 1, abort_flag, tmo, status)))
+        if (!(ok = mbar_wait_cluster(&acc_empty[b], use_parity() ^ 1u, abort_flag, tmo, status)))
           break;
         tc_fence_after();
         const uint32_t acc_t = tmem + b * kBN;
@@ -539,7 +541,6 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         }
         if (!ok) break;
         mma_commit_pair_mc(&acc_full[b], kBothCtas);
-        ++nuse[b];
         ++count;
       }
       // Every MMA this thread issued must finish before tensor memory is freed.
@@ -578,12 +579,11 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         bulk_wait_read_le1();
       }
     };
-    const uint32_t acc_empty_l[2] = {mapa_shared(smem_u32(&acc_empty[0]), 0),
-                                     mapa_shared(smem_u32(&acc_empty[1]), 0)};
+    const uint32_t acc_empty_l0 = mapa_shared(smem_u32(&acc_empty[0]), 0);   // buffer b: + 8 b
     const uint64_t stream_out = l2_evict_first();   // Y is written once: keep X and W in L2
     const int cw = p.y_f32 ? 32 : 64;               // columns per 128-byte row chunk
-    uint32_t nuse[2] = {0, 0};
     int count = 0;
+    auto use_parity = [&]() -> uint32_t { return static_cast<uint32_t>(kNF4 ? count : (count >> 1)) & 1u; };
     uint32_t sidx = 0;                              // staging chunks issued so far
     if (p.n_ad > 0) grid_dependency_wait();          // rank items release flags cleared by it
     ItemIter iter = item_iter_begin(p, pair, npairs);
@@ -593,19 +593,18 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       if (it.rank && eg == 1) {
         // 4-bit W: warpgroup 1 has no rows of the rank item to read; it only counts the
         // item off the accumulator buffer, after the MMAs filled it
-        const bool okw = mbar_wait_cluster(&acc_full[b], nuse[b] & 1, abort_flag, tmo, status);
+        const bool okw = mbar_wait_cluster(&acc_full[b], use_parity(), abort_flag, tmo, status);
         if (named_bar_any(!okw, bar_any, 128)) break;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(acc_empty_l[b]);
-        ++nuse[b];
+        if (lane == 0) mbar_arrive_cluster(acc_empty_l0 + 8u * static_cast<uint32_t>(b));
         ++count;
         continue;
       }
       if (it.rank) {
         // s X A^T of every adapter -> bf16 H~ rows of this block in global memory (and
         // the fp32 values in h_out when asked), then the block's flag
-        const bool okw = mbar_wait_cluster(&acc_full[b], nuse[b] & 1, abort_flag, tmo, status);
+        const bool okw = mbar_wait_cluster(&acc_full[b], use_parity(), abort_flag, tmo, status);
         if (named_bar_any(!okw, bar_any, 128)) break;
         tc_fence_after();
         const uint32_t h_t = tmem + b * kBN;
@@ -625,15 +624,16 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
             // [b1 b2 b1 b3 b2 b1] of B: every product above 2^-24 of the leading one is kept
             const int pu = units / 3;                  // units per piece
             for (int u = 0; u < pu; ++u) {
-              uint32_t q0[8], q1[8], q2[8];
-              tmem_ld8(h_t + lane_base + col(u), q0);
-              tmem_ld8(h_t + lane_base + col(u + pu), q1);
-              tmem_ld8(h_t + lane_base + col(u + 2 * pu), q2);
+              // the unit's three pieces under one TMEM wait (the fourth address repeats one)
+              uint32_t q[32];
+              const uint32_t ta[4] = {h_t + lane_base + col(u), h_t + lane_base + col(u + pu),
+                                      h_t + lane_base + col(u + 2 * pu), h_t + lane_base + col(u)};
+              tmem_ld8x4(ta, q);
               uint32_t w1[4], w2[4], w3[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                const float x0 = s * ((u2f(q0[2 * i]) + u2f(q1[2 * i])) + u2f(q2[2 * i]));
-                const float x1 = s * ((u2f(q0[2 * i + 1]) + u2f(q1[2 * i + 1])) + u2f(q2[2 * i + 1]));
+                const float x0 = s * ((u2f(q[2 * i]) + u2f(q[8 + 2 * i])) + u2f(q[16 + 2 * i]));
+                const float x1 = s * ((u2f(q[2 * i + 1]) + u2f(q[8 + 2 * i + 1])) + u2f(q[16 + 2 * i + 1]));
                 w1[i] = pack_bf16x2(x0, x1);
                 const float y0 = x0 - __uint_as_float(w1[i] << 16);
                 const float y1 = x1 - __uint_as_float(w1[i] & 0xffff0000u);
@@ -650,18 +650,18 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
             continue;
           }
           for (int u0 = 0; u0 < units; u0 += 4) {
-            // 32 ranks per TMEM load where the columns allow it, 8 otherwise
+            // 32 ranks per TMEM load where the columns allow it, else four 8-column loads
+            // under one wait (a unit past the adapter's last repeats the first); registers
+            // are indexed by constants only, so that r stays out of local memory
             uint32_t r[32];
             const int n = min(4, units - u0);
             if (n == 4 && col(u0 + 3) == col(u0) + 24) {
               tmem_ld32(h_t + lane_base + col(u0), r);
             } else {
-              for (int k = 0; k < n; ++k) {
-                uint32_t r8[8];
-                tmem_ld8(h_t + lane_base + col(u0 + k), r8);
+              uint32_t ta[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) r[k * 8 + i] = r8[i];
-              }
+              for (int k = 0; k < 4; ++k) ta[k] = h_t + lane_base + col(k < n ? u0 + k : u0);
+              tmem_ld8x4(ta, r);
             }
             if (!row_ok) continue;
             if (p.h_out) {
@@ -671,7 +671,9 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               for (int i = 0; i < 32; ++i)
                 if (i < n * 8 && u0 * 8 + i < p.ad[a].rank) ho[u0 * 8 + i] = u2f(r[i]) * s;
             }
-            for (int k = 0; k < n; ++k) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              if (k >= n) break;
               const uint32_t* q8 = r + k * 8;
               st_global_v4(hrow + p.ad[a].toff + (u0 + k) * 8, pack_bf16x2(u2f(q8[0]) * s, u2f(q8[1]) * s),
                            pack_bf16x2(u2f(q8[2]) * s, u2f(q8[3]) * s), pack_bf16x2(u2f(q8[4]) * s, u2f(q8[5]) * s),
@@ -682,13 +684,12 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         // the accumulator is fully in registers: hand it back to the MMA
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(acc_empty_l[b]);
+        if (lane == 0) mbar_arrive_cluster(acc_empty_l0 + 8u * static_cast<uint32_t>(b));
         // H~ rows visible to the TMA loads of other pairs: every thread orders its stores
         // for the async proxy, the barrier gathers them, and one release counts this CTA in
         fence_proxy_async_global();
         named_bar_sync(bar_main, 128);
         if (elected) red_release_gpu_add(p.flags + it.m, 1u);
-        ++nuse[b];
         ++count;
         continue;
       }
@@ -716,7 +717,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
         if (next_item(peek, p, pair, npairs, nx) && !nx.rank) prefetch_tile(nx.t);
       }
       if (any_mma) {
-        const bool ok = mbar_wait_cluster(&acc_full[b], nuse[b] & 1, abort_flag, tmo, status);
+        const bool ok = mbar_wait_cluster(&acc_full[b], use_parity(), abort_flag, tmo, status);
         if (named_bar_any(!ok, bar_any, 128)) break;
         tc_fence_after();
       }
@@ -752,7 +753,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               if (h == h_end - 1 && c == nch - 1 && sub == 3) {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(acc_empty_l[b]);
+                if (lane == 0) mbar_arrive_cluster(acc_empty_l0 + 8u * static_cast<uint32_t>(b));
               }
               const int nc = min(16, ncols - sub * 16);
               const int col = cig + sub * 16;              // first column of the sub-chunk
@@ -805,7 +806,6 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
             }
           }
         }
-        ++nuse[b];
         ++count;
         continue;
       }
@@ -861,7 +861,7 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
               // the accumulator is fully in registers: hand it back to the MMA
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive_cluster(acc_empty_l[b]);
+              if (lane == 0) mbar_arrive_cluster(acc_empty_l0 + 8u * static_cast<uint32_t>(b));
             }
           } else {
 #pragma unroll
@@ -1028,7 +1028,6 @@ __global__ void __launch_bounds__(kNF4 ? kTcThreadsNF4 : kTcThreads, 1)
       }
       }
       if (any_mma) {
-        ++nuse[b];
         ++count;
       }
     }
