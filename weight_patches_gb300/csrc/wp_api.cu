@@ -871,6 +871,15 @@ int fwd_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, bool g
   // stay in L2 until their tiles come
   const double x_two_rounds = 2.0 * pairs / (G * p.nt_g) * (kPairM << p.m_shift) * static_cast<double>(K) * 2;
   p.rlead = x_two_rounds <= 48.0 * (1 << 20) ? 2 : 1;
+  // every pair opens with its first rank item unless the X rows those items read are far
+  // more than L2 holds (they would then be read from HBM a second time when their tiles come):
+  // measured, 30-168 MB of them (rank-128 q/k/v, the three-patch sidecar) gained 1.5-1.8 %,
+  // 350 MB (the 8960-deep down projection) lost 2.6 %; the bound is 1.5 L2 capacities
+  if (p.n_ad > 0) {
+    const int first_items = std::min(pairs, p.r_blocks * std::max(1, p.npass));
+    const double first_x = static_cast<double>(first_items) / std::max(1, p.npass) * kPairM * static_cast<double>(K) * 2;
+    p.rank_first = first_x <= 192.0 * (1 << 20) ? 1 : 0;
+  }
   return launch_tc_fwd(maps, p, 2 * pairs, smem, stream, nf4);
 }
 

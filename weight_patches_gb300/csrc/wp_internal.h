@@ -76,6 +76,7 @@ struct TcParams {
                                // W as it is): weight tiles are MN-major MMA operands; a 4-bit
                                // W's codes are [in rows, out / 2 bytes], blocks of 64 along out
   int rlead;                   // rank items run this many rounds of tiles ahead of their tiles
+  int rank_first;              // every pair opens with its first rank item
   int step_j, step_g, step_m;  // the number of pairs in (row block, group, column tile) digits
                                // (set by the launcher)
   int has_base;

@@ -71,8 +71,8 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, int L) {
 // q + k * npairs.  The rank item of row block m belongs to pair (m + total_tiles) mod npairs
 // (so the pairs with one tile fewer take rank items first) and runs at the start of that
 // pair's round r(m) - rlead, where r(m) = floor(m * tpb / npairs) is the first round that
-// can hold a tile of m (or as soon as the pair has no tiles left); a pair's first rank item
-// runs before its first tile.
+// can hold a tile of m (or as soon as the pair has no tiles left); with rank_first a pair's
+// first rank item runs before its first tile.
 // A tile of round k waits only for rank items of rounds < k, and every pair walks its
 // items in order, so the schedule cannot deadlock while all pairs are resident.
 struct Item {
@@ -96,10 +96,11 @@ struct ItemIter {
 };
 
 __device__ __forceinline__ int rank_item_due(const TcParams& p, int i, int npairs) {
-  // every pair opens with its first rank item: the first round's tiles need the H~ of the
-  // first row blocks by the end of their K loops, and a handful of pairs computing those
-  // alone (from cold memory, like everyone else) finish well after that
-  if (i < npairs) return 0;
+  // rank_first: every pair opens with its first rank item.  The first round's tiles need
+  // the H~ of the first row blocks by the end of their K loops, and a handful of pairs
+  // computing those alone (from cold memory, like everyone else) finish well after that;
+  // the host asks for it where those items' X rows stay in L2 until their tiles come.
+  if (p.rank_first && i < npairs) return 0;
   const int m = p.npass == 1 ? i : i / p.npass;
   // (m >> m_shift) * tpb <= total_tiles < 2^31
   const uint32_t first = static_cast<uint32_t>((m >> p.m_shift) * p.G * p.nt_g) / static_cast<uint32_t>(npairs);
