@@ -325,6 +325,9 @@ def per_config(dev, args, peak, hbm, only=None):
     k, w = max(10, min(args.steps, 50)), 5
 
     def timed(fn, kk=k, ww=w):
+        # every measurement starts after the same short idle pause, so that none of them runs
+        # in a hotter, power-capped stretch than the fused call it is compared with
+        time.sleep(0.3)
         for _ in range(ww):
             fn()
         torch.cuda.synchronize(dev)
