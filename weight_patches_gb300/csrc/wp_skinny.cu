@@ -207,8 +207,7 @@ __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
       }
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued[kMaxStages];
-      for (int s = 0; s < kMaxStages; ++s) issued[s] = 0;
+      uint32_t n_issued = 0;                  // stages filled so far (no per-stage array: local memory)
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
         const Unit t = unit_of(p, u);
         for (int kb = t.kb0; kb < t.kb1; kb += kkb) {
@@ -225,12 +224,13 @@ __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
             if (t.a_blk) load_a_block(st + h * kWTileBytes, a0, kb + h, &full[stage], keep);
             else if (!kNF4) tma_load_2d_hint(st + h * kWTileBytes, &maps.w, (kb + h) * kBK, t.rb * 128, &full[stage], once);
           }
-          ++issued[stage];
+          ++n_issued;
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
       if (!ok)
-        for (int s = 0; s < S; ++s) settle(&full[s], issued[s]);
+        for (int s = 0; s < S; ++s)
+          settle(&full[s], n_issued / S + (static_cast<uint32_t>(s) < n_issued % S ? 1u : 0u));
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -238,34 +238,41 @@ __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t nuse[2] = {0, 0};
       int count = 0;
       bool ok = true;
       const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(p.Tp));
       const uint32_t stage_base = smem_u32(sbase);
+      // This thread's instructions between two MMAs are on the tensor core's critical path
+      // (a 128 x Tp x 16 MMA is short): descriptors are the constant fields and the start
+      // address (16-byte units) of stage 0's slots plus the stage's offset.
+      const uint32_t u_w = stage_base >> 4, u_x = (stage_base + static_cast<uint32_t>(x_off)) >> 4;
+      const uint32_t w_step = kWTileBytes >> 4, x_step = static_cast<uint32_t>(XB) >> 4;
+      const uint32_t stage_units = static_cast<uint32_t>(SB) >> 4;
+      uint32_t off = 0;
       for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
         const Unit t = unit_of(p, u);
         const int b = count & 1;
-        if (!(ok = mbar_wait(&acc_empty[b], (nuse[b] & 1) ^ 1, abort_flag, tmo, status))) break;
+        // unit `count` uses buffer count & 1, whose earlier uses number count >> 1
+        if (!(ok = mbar_wait(&acc_empty[b], ((static_cast<uint32_t>(count) >> 1) & 1u) ^ 1u, abort_flag, tmo, status)))
+          break;
         tc_fence_after();
         for (int kb = t.kb0; kb < t.kb1; kb += kkb) {
           if (kNF4 && !(ok = mbar_wait(&wfull[stage], phase, abort_flag, tmo, status))) break;
           if (!(ok = mbar_wait(&full[stage], phase, abort_flag, tmo, status))) break;
           tc_fence_after();
-          const uint32_t st = stage_base + stage * SB;
           for (int h = 0; h < kkb; ++h) {
-            const uint64_t ad = sw128_kmajor_desc(st + h * kWTileBytes);
-            const uint64_t bd = sw128_kmajor_desc(st + x_off + h * XB);
+            const uint64_t ad = kDescSw128K | (u_w + off + h * w_step);
+            const uint64_t bd = kDescSw128K | (u_x + off + h * x_step);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
               mma_bf16(tmem + b * 64, ad + 2 * kk, bd + 2 * kk, idesc, (kb > t.kb0 || h > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&empty[stage]);
-          if (++stage == S) { stage = 0; phase ^= 1; }
+          off += stage_units;
+          if (++stage == S) { stage = 0; phase ^= 1; off = 0; }
         }
         if (!ok) break;
         mma_commit(&acc_full[b]);
-        ++nuse[b];
         ++count;
       }
       // every MMA issued must finish before tensor memory is freed
@@ -280,12 +287,11 @@ __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
     // thread = one row of the block (its TMEM lane), Tp token columns
     const int q = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    uint32_t nuse[2] = {0, 0};
     int count = 0;
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
       const Unit t = unit_of(p, u);
       const int b = count & 1;
-      const bool ok = mbar_wait(&acc_full[b], nuse[b] & 1, abort_flag, tmo, status);
+      const bool ok = mbar_wait(&acc_full[b], (static_cast<uint32_t>(count) >> 1) & 1u, abort_flag, tmo, status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const int lrow = q * 32 + lane;
@@ -315,7 +321,6 @@ __global__ void __launch_bounds__(kNF4 ? kSkinnyThreadsNF4 : kSkinnyThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[b]);
-      ++nuse[b];
       ++count;
     }
   } else if (kNF4) {
