@@ -159,6 +159,8 @@ struct SkinnyPlan {
   bool gemv = false;
   int g_splits = 1, g_ks_len = 0, g_grid = 0;
   size_t g_smem = 0;
+  // one token against a 4-bit weight, K a multiple of 2048: the plain-load kernel instead
+  bool g_ld = false;
 };
 
 // The split of K for the CUDA-core small-token kernel: each block holds the fp32 X of its
@@ -239,6 +241,14 @@ bool plan_skinny(const wp_mat* X, const wp_mat* W, const wp_adapter* ad, int n, 
   sp->part_bytes = round256(static_cast<size_t>(sp->splits) * T * (N + R16) * 4);
   if (W && T <= kGemvMaxT && K % kGemvStageK == 0 && plan_gemv(T, K, N, W->dtype == WP_NF4, sp)) {
     sp->gemv = true;
+    if (W->dtype == WP_NF4 && T == 1 && K % kGemvLdSlice == 0 && K / kGemvLdSlice <= kGemvMaxSplits) {
+      // one split per 2048-element slice; two 8-warp blocks per SM over the slices
+      sp->g_ld = true;
+      sp->g_splits = static_cast<int>(K / kGemvLdSlice);
+      sp->g_ks_len = kGemvLdSlice;
+      sp->g_grid = std::max(1, 2 * grid / sp->g_splits) * sp->g_splits;
+      sp->g_smem = 0;
+    }
     sp->part_bytes =
         std::max(sp->part_bytes, round256(static_cast<size_t>(sp->g_splits) * T * (N + R16) * 4));
   }
@@ -373,9 +383,15 @@ int skinny_impl(const wp_mat* X, const wp_mat* W, const wp_mat* bias, int G, boo
     g.status = tc_status_ptr();
     g.timeout_ns = wait_limit_ns();
     if (!g.status) return record_cuda();
+    int rc = WP_OK;
+    if (sp.g_ld) {
+      rc = launch_gemv_ld(g, W->data, W->absmax, sp.g_grid, stream);
+      if (rc != WP_OK) return rc;
+      q.splits = sp.g_splits;
+      return launch_skinny_reduce(q, stream);
+    }
     GemvMaps gm;
     std::memset(&gm, 0, sizeof(gm));
-    int rc = WP_OK;
     if (nf4) {
       rc = make_map_u8(&gm.wq, W->data, K / 2, N, K / 2, kGemvStageK / 2, 32, 128);
       if (rc != WP_OK) return rc;

@@ -257,6 +257,160 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_kernel(const __grid_cons
   }
 }
 
+// A 16-byte load of weight bytes read once: not kept in L1.
+__device__ __forceinline__ uint4 ld_once_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_once_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
+// The 4-bit weight against one token by plain loads.  The TMA ring above pays the
+// copy engine per row of every box (32 rows of 128 code bytes and 32 rows of 16 scale
+// bytes a stage), which held the weight stream to about half the HBM rate.  Here a warp
+// takes whole 2048-element slices of a row: lane l loads the 32 code bytes of elements
+// [64 l, 64 l + 64) of the slice (one 64-element block, so one scale and one 16-entry table
+// per lane and row) with two 16-byte loads, the warp's loads covering 1 KiB of the row, and
+// keeps its 64 X values in registers for every row it takes (two tokens' would not fit
+// beside the ring without spilling, so two to four tokens stay on the kernel above).  A split is one slice (K must
+// be a multiple of 2048); the row's slice sum is a shuffle reduction, written where the
+// small-token reduce reads the K splits.  Rows go two at a time through a three-deep ring of
+// registers, so four rows' loads are in flight while two are computed.
+template <int kT>
+__global__ void __launch_bounds__(kGemvLdWarps * 32, 2) gemv_nf4_ld_kernel(const GemvParams p,
+                                                                             const uint8_t* __restrict__ codes,
+                                                                             const float* __restrict__ absmax) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x % p.splits;
+  const int jb = blockIdx.x / p.splits;
+  const int nbs = gridDim.x / p.splits;           // the host launches a multiple of the splits
+  const int kl = split * kGemvLdSlice + lane * 64;    // this lane's 64 elements
+  uint32_t xw[kT][32];                            // X pairs (elements 2i, 2i + 1) of them
+#pragma unroll
+  for (int t = 0; t < kT; ++t)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.X + t * p.ldx + kl + 8 * i));
+      xw[t][4 * i] = v.x; xw[t][4 * i + 1] = v.y; xw[t][4 * i + 2] = v.z; xw[t][4 * i + 3] = v.w;
+    }
+  float lv[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) lv[i] = p.nf4_code[i];
+  const int gw = jb * kGemvLdWarps + warp;
+  const int wstride = nbs * kGemvLdWarps;
+  float* part = p.part + static_cast<long long>(split) * p.T * p.ldp;
+  const long long row_bytes = p.K / 2, row_blocks = p.K / 64;
+
+  struct Rows {
+    uint4 c[2][2];    // [row][16-byte half]
+    float am[2];
+  };
+  // rows gw + (2 j + i) wstride, i = 0, 1 (past the last row: zeros, nothing read)
+  auto load = [&](Rows& b, int j) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = gw + (2 * j + i) * wstride;
+      if (r < p.N) {
+        const uint8_t* src = codes + static_cast<long long>(r) * row_bytes + kl / 2;
+        b.c[i][0] = ld_once_v4(src);
+        b.c[i][1] = ld_once_v4(src + 16);
+        b.am[i] = ld_once_f32(absmax + static_cast<long long>(r) * row_blocks + kl / 64);
+      } else {
+        b.c[i][0] = b.c[i][1] = make_uint4(0u, 0u, 0u, 0u);
+        b.am[i] = 0.f;
+      }
+    }
+  };
+  auto compute = [&](const Rows& b, int j) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = gw + (2 * j + i) * wstride;
+      uint32_t lo[4], hi[4];
+      block_table(b.am[i], lv, lo, hi);
+      const uint32_t cw[8] = {b.c[i][0].x, b.c[i][0].y, b.c[i][0].z, b.c[i][0].w,
+                              b.c[i][1].x, b.c[i][1].y, b.c[i][1].z, b.c[i][1].w};
+      float acc[kT][2];
+#pragma unroll
+      for (int t = 0; t < kT; ++t) acc[t][0] = acc[t][1] = 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t c = cw[u];
+        const uint32_t sel = c & 0x77777777u;
+        const uint32_t pick = ((c >> 1) & 0x44444444u) | 0x32103210u;
+        uint32_t o[4];
+        lookup4(sel, pick, lo, hi, o[0], o[1]);
+        lookup4(sel >> 16, pick >> 16, lo, hi, o[2], o[3]);
+#pragma unroll
+        for (int t = 0; t < kT; ++t) {
+          float& a = acc[t][u & 1];
+          a = fma_bf16x2(o[0], xw[t][4 * u], a);
+          a = fma_bf16x2(o[1], xw[t][4 * u + 1], a);
+          a = fma_bf16x2(o[2], xw[t][4 * u + 2], a);
+          a = fma_bf16x2(o[3], xw[t][4 * u + 3], a);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kT; ++t) {
+        float sum = acc[t][0] + acc[t][1];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (lane == 0 && r < p.N) part[static_cast<long long>(t) * p.ldp + r] = sum;
+      }
+    }
+  };
+  const int nrows = gw < p.N ? (p.N - gw + wstride - 1) / wstride : 0;
+  const int npr = (nrows + 1) / 2;                // row pairs of this warp
+  Rows b0, b1, b2;
+  load(b0, 0);
+  load(b1, 1);
+  for (int j = 0; j < npr; j += 3) {
+    load(b2, j + 2);
+    compute(b0, j);
+    if (j + 1 >= npr) break;
+    load(b0, j + 3);
+    compute(b1, j + 1);
+    if (j + 2 >= npr) break;
+    load(b1, j + 4);
+    compute(b2, j + 2);
+  }
+
+  // adapter A rows (bf16): the same lane slices, one row per warp
+  for (int ar = gw; ar < p.R16; ar += wstride) {
+    int a = 0;
+    while (a + 1 < p.n_ad && ar >= p.a_off[a + 1]) ++a;
+    const int j = ar - p.a_off[a];
+    float sum[kT];
+#pragma unroll
+    for (int t = 0; t < kT; ++t) sum[t] = 0.f;
+    if (j < p.rank[a]) {
+      const uint16_t* row = p.A[a] + j * p.lda[a] + kl;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + 8 * i));
+#pragma unroll
+        for (int t = 0; t < kT; ++t) {
+          sum[t] = fma_bf16x2(v.x, xw[t][4 * i], sum[t]);
+          sum[t] = fma_bf16x2(v.y, xw[t][4 * i + 1], sum[t]);
+          sum[t] = fma_bf16x2(v.z, xw[t][4 * i + 2], sum[t]);
+          sum[t] = fma_bf16x2(v.w, xw[t][4 * i + 3], sum[t]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kT; ++t) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum[t] += __shfl_xor_sync(0xffffffffu, sum[t], o);
+      if (lane == 0) part[static_cast<long long>(t) * p.ldp + p.N + ar] = sum[t];
+    }
+  }
+}
+
 template <int kT, bool kNF4>
 int launch_t(const GemvMaps& maps, const GemvParams& p, int grid, size_t smem, cudaStream_t stream) {
   auto kern = gemv_kernel<kT, kNF4>;
@@ -315,6 +469,19 @@ int gemv_blocks_per_sm(int T, bool nf4, size_t smem) {
   }
   c.store(n > 0 ? n : -1, std::memory_order_relaxed);
   return n;
+}
+
+int launch_gemv_ld(const GemvParams& p, const void* codes, const float* absmax, int grid, cudaStream_t stream) {
+  if (grid < 1) return WP_OK;
+  const uint8_t* c = static_cast<const uint8_t*>(codes);
+  if (p.T != 1) return WP_ERR_UNSUPPORTED;
+  gemv_nf4_ld_kernel<1><<<grid, kGemvLdWarps * 32, 0, stream>>>(p, c, absmax);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    return WP_ERR_CUDA;
+  }
+  return WP_OK;
 }
 
 int launch_gemv(const GemvMaps& maps, const GemvParams& p, bool nf4, int grid, size_t smem,

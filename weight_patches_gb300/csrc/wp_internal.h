@@ -231,6 +231,9 @@ constexpr int kGemvStageK = 256;
 constexpr int kGemvCodeBytes = 32 * kGemvStageK / 2;   // 4 KiB
 constexpr int kGemvAmBytes = 32 * kGemvStageK / 64 * 4;  // 512 B
 constexpr int kGemvXBudget = 16384;                      // bf16 X elements a block holds (32 KiB)
+// the plain-load 4-bit kernel for one token: 2048-element K splits, 8 warps a block
+constexpr int kGemvLdSlice = 2048;
+constexpr int kGemvLdWarps = 8;
 
 struct GemvParams {
   int T, K, N;
@@ -261,6 +264,7 @@ size_t gemv_smem_bytes(int T, int ks_len);
 int gemv_blocks_per_sm(int T, bool nf4, size_t smem_bytes);
 int launch_gemv(const GemvMaps& maps, const GemvParams& p, bool nf4, int grid, size_t smem_bytes,
                 cudaStream_t stream);
+int launch_gemv_ld(const GemvParams& p, const void* codes, const float* absmax, int grid, cudaStream_t stream);
 int* tc_status_ptr();
 
 int tc_max_pairs(size_t smem_bytes, bool nf4);
