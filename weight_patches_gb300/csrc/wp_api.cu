@@ -917,14 +917,24 @@ struct BwdLayout {
   size_t hp, gp, tpart;
 };
 
-// Token splits of a contraction with m_tiles 256-row blocks over k_blocks 64-token steps: about
-// one unit per SM, at least 8 steps per unit.
+// Token splits of a contraction with m_tiles 256-row blocks over k_blocks 64-token steps, its
+// units (row block, token range) dealt to the CTA pairs: the count whose busiest pair streams
+// the fewest steps (units per pair rounded up x steps per unit; the fewest splits on a tie), at
+// least 8 steps per unit.  (About one unit per SM, the earlier rule, left 2.1 units per pair on
+// average where the busiest had 3.)
 int tok_splits(int m_tiles, int k_blocks) {
-  const int sms = device_sm_count();
-  int s = (sms + m_tiles - 1) / m_tiles;
+  const int pairs = std::max(1, device_sm_count() / 2);
   const int cap = std::max(1, k_blocks / 8);
-  if (s > cap) s = cap;
-  return s < 1 ? 1 : s;
+  int best_s = 1;
+  long long best = -1;
+  for (int s = 1; s <= cap; ++s) {
+    const int per = (k_blocks + s - 1) / s;              // steps per unit
+    const int used = (k_blocks + per - 1) / per;         // splits that hold steps
+    const long long rounds = (static_cast<long long>(m_tiles) * used + pairs - 1) / pairs;
+    const long long cost = rounds * per;
+    if (best < 0 || cost < best) { best = cost; best_s = used; }
+  }
+  return best_s;
 }
 
 // The largest rank the backward takes per group: the group's two bf16 pieces fill at most one
