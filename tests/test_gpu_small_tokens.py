@@ -76,6 +76,19 @@ def test_cuda_core_tokens(T, K, N, ranks, kind):
     _check(_layer(T, K, N, ranks, kind=kind, bias="bf16", seed=T * 7 + K + N))
 
 
+@pytest.mark.parametrize("K,N,ranks,groups", [(2048, 130, [8, 8], 1), (6144, 1000, [16], 1), (4096, 2 * 200, [16, 8], 2)])
+def test_plain_load_kernel_one_token(K, N, ranks, groups):
+    """One token against a 4-bit weight whose K is a multiple of 2048 takes the plain-load
+    kernel (a 2048-element split per slice, a row's slice per warp, X in registers): one, three
+    and two splits, ragged rows (130, 1000), several adapters, a bias, stacked groups with fp32
+    output and a request scale."""
+    lin = _layer(1, K, N, ranks, kind="nf4", bias="bf16" if groups == 1 else None, groups=groups,
+                 strengths=[0.5, 1.5][:len(ranks)], seed=K + N)
+    if groups > 1:
+        lin.request_scale = 0.75
+    _check(lin, out_dtype=torch.float32 if groups > 1 else torch.bfloat16)
+
+
 @pytest.mark.parametrize("kind", ["nf4", "bf16"])
 def test_cuda_core_grouped_fp32_out(kind):
     """Stacked gate/up groups with their own adapters, fp32 output, a request scale, one token
